@@ -1,0 +1,62 @@
+"""Test-side helpers: build host pools from seeded workloads with the oracle's
+encoder, poison unused slots, and small utilities shared by the tests.
+
+Pool arrays per layer (the library's documented layout): data
+[num_pages][n_kv][16][D] (uint16 f16 bits or int8 q8_0 codes), q8_0 scales
+[num_pages][n_kv][16][D/32] (uint16 f16 bits)."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle as O
+from paged_kv_decode_09_gb300 import workloads as W
+
+F16_NAN = np.uint16(0x7E00)
+
+
+def encode_pool(wl: W.Workload, layer: int = 0, include_appended: bool = True,
+                poison: bool = True):
+    """(k_data, v_data, k_scales, v_scales) host arrays of one layer's pool.
+
+    Context values come from the seeded generator and are stored by the
+    oracle's encoder.  Slots that hold no token (and, with
+    include_appended=False, the slot the step will append into) are poisoned
+    with f16 NaN (f16 data, or the q8_0 block scales), so that a kernel reading
+    one produces NaN."""
+    cfg = wl.cfg
+    k, v = W.context_values(wl, layer)
+    kd, ks = O.encode_pool(cfg.dtype, k)
+    vd, vs = O.encode_pool(cfg.dtype, v)
+    if poison:
+        unused = ~W.used_slots(wl, include_appended=include_appended)  # [pages][16]
+        sel = np.broadcast_to(unused[:, None, :], (wl.num_pages, cfg.n_kv_heads, W.PAGE))
+        if cfg.dtype == W.F16:
+            kd[sel] = F16_NAN
+            vd[sel] = F16_NAN
+        else:
+            ks[sel] = F16_NAN
+            vs[sel] = F16_NAN
+            kd[sel] = 127
+            vd[sel] = 127
+    return kd, vd, ks, vs
+
+
+def oracle_decode(wl: W.Workload, pool, seq_lens=None, q=None, scale=None):
+    kd, vd, ks, vs = pool
+    return O.decode_attention(wl.cfg.dtype, wl.q if q is None else q, kd, vd, ks, vs,
+                              wl.block_table, wl.seq_lens if seq_lens is None else seq_lens,
+                              wl.num_pages, wl.cfg.n_kv_heads,
+                              wl.scale if scale is None else scale)
+
+
+def stored_values_dense(dtype, data, scales):
+    """float64 values of pool elements [..., D] using numpy's own float16
+    widening (a route independent of the oracle's)."""
+    if dtype == W.F16:
+        return data.view(np.float16).astype(np.float64)
+    sc = scales.view(np.float16).astype(np.float64)
+    return np.repeat(sc, 32, axis=-1) * data.astype(np.float64)
+
+
+def max_abs_err(a, b):
+    return float(np.max(np.abs(np.asarray(a, np.float64) - np.asarray(b, np.float64))))

@@ -1,0 +1,59 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a copy of the oracle's C source (a dropped
+term, a wrong sign, a wrong or transposed index, a wrong rounding rule),
+builds it on the CPU, and runs the oracle pin tests against that copy: at least
+one pin must fail.  Nothing here touches a GPU."""
+import os
+import subprocess
+import sys
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "pkv_oracle.c")
+PINS = ["tests/test_oracle_f16.py", "tests/test_oracle_q8_0.py",
+        "tests/test_oracle_attention.py", "tests/test_oracle_plan_append.py"]
+
+MUTANTS = {
+    "no_normalisation": ("for (int d = 0; d < D; ++d) o[d] /= l;", ""),
+    "interleaved_gqa": ("h = g / group;", "h = g % n_kv;"),
+    "slot_as_page": ("block_table[(int64_t)i * bt_stride + t / ORACLE_PAGE]",
+                     "block_table[(int64_t)i * bt_stride + t % ORACLE_PAGE]"),
+    "transposed_page_head": ("int64_t row = (page * n_kv + kvh) * ORACLE_PAGE + slot;",
+                             "int64_t row = (kvh * n_kv + page) * ORACLE_PAGE + slot;"),
+    "dropped_scale": ("s[t - t0] = scale * dot;", "s[t - t0] = dot;"),
+    "dropped_q8_scale": ("return sc * (double)((const int8_t *)data)[row * D + d];",
+                         "return (double)((const int8_t *)data)[row * D + d];"),
+    "wrong_q8_block_index": ("scales[row * (D / ORACLE_QBLOCK) + d / ORACLE_QBLOCK]",
+                             "scales[row * (D / ORACLE_QBLOCK) + d % (D / ORACLE_QBLOCK)]"),
+    "softmax_sign": ("double p = exp(s[t] - m);", "double p = exp(m - s[t]);"),
+    "ties_to_odd": ("(rem == 0.5 && fmod(whole, 2.0) != 0.0)", "(rem == 0.5 && fmod(whole, 2.0) == 0.0)"),
+    "ties_toward_plus_inf": ("return y < 0.0 ? -floor(-y + 0.5) : floor(y + 0.5);",
+                             "return floor(y + 0.5);"),
+    "q8_scale_126": ("float d = fdiv32(amax, 127.0f);", "float d = fdiv32(amax, 126.0f);"),
+    "merge_sign": ("double w = exp2((double)m2[s] - M);", "double w = exp2(M - (double)m2[s]);"),
+    "segment_start": ("int64_t a = (int64_t)n_kv * row_page_start[i] + h * npg, b = a + npg;",
+                      "int64_t a = (int64_t)n_kv * row_page_start[i] + h, b = a + npg;"),
+    "append_slot": ("int slot = pos % ORACLE_PAGE;", "int slot = L % ORACLE_PAGE;"),
+    "partial_base_e": ("double p = exp2(s[t - t0] - m);", "double p = exp(s[t - t0] - m);"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site not unique or missing: {old!r}"
+    with tempfile.TemporaryDirectory() as tmp:
+        c = os.path.join(tmp, "mut.c")
+        so = os.path.join(tmp, "libmut.so")
+        with open(c, "w") as f:
+            f.write(src.replace(old, new))
+        subprocess.run(["gcc", "-O2", "-std=gnu11", "-shared", "-fPIC", "-ffp-contract=off",
+                        c, "-o", so, "-lm"], check=True)
+        env = dict(os.environ, PKV_ORACLE_LIB=so)
+        r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                            *PINS], cwd=ROOT, env=env, capture_output=True, text=True)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"

@@ -1,0 +1,122 @@
+"""Pins for the oracle's work split (plan) and its kv_append.
+
+Plan: units are (row, KV head, page) tiles in that order; C chunks cover
+[floor(k T / C), floor((k + 1) T / C)); a segment (row, head) is split into
+pieces by the chunks it meets.  Pinned to hand-derived fixtures and to a
+brute-force enumeration of every unit.
+
+Append (tinyllm, "The repository currently provides": block table per active
+sequence; "Known limitations": 16-token pages): row i's new token goes to page
+block_table[i][(L_i - 1) // 16], slot (L_i - 1) % 16, stored with the f16 or
+q8_0 encoder; nothing else in the pool changes."""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+from conftest import GOLDEN
+from paged_kv_decode_09_gb300 import workloads as W
+
+
+def _golden():
+    with open(os.path.join(GOLDEN, "plan_tiny.json")) as f:
+        return json.load(f)["cases"]
+
+
+@pytest.mark.parametrize("case", _golden(), ids=lambda c: f"C{c['chunks']}_{len(c['seq_lens'])}rows")
+def test_plan_golden(case):
+    rps, first, last, T = O.plan(np.array(case["seq_lens"], np.int32), case["n_kv"], case["chunks"])
+    assert T == case["total"]
+    np.testing.assert_array_equal(rps, case["row_page_start"])
+    np.testing.assert_array_equal(first, case["seg_first_chunk"])
+    np.testing.assert_array_equal(last, case["seg_last_chunk"])
+
+
+def _enumerate(seq_lens, n_kv, C):
+    """Brute force: list every unit with its (segment, chunk) and derive the
+    chunks each segment meets."""
+    units = []  # (segment, chunk) per unit, in unit order
+    for i, L in enumerate(seq_lens):
+        npg = (max(L, 0) + 15) // 16
+        for h in range(n_kv):
+            for p in range(npg):
+                units.append(i * n_kv + h)
+    T = len(units)
+    chunk_of = []
+    for k in range(C):
+        chunk_of += [k] * ((k + 1) * T // C - k * T // C)
+    J = len(seq_lens) * n_kv
+    first, last = [-1] * J, [-1] * J
+    for x, j in enumerate(units):
+        if first[j] < 0:
+            first[j] = chunk_of[x]
+        last[j] = chunk_of[x]
+    return T, first, last
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_plan_matches_unit_enumeration(seed):
+    rng = np.random.default_rng(seed)
+    rows = int(rng.integers(1, 12))
+    lens = rng.integers(0, 200, rows).astype(np.int32)
+    lens[rng.integers(0, rows)] = 0
+    n_kv = int(rng.choice([1, 2, 8]))
+    for C in (1, 3, 7, 152, 1000):
+        rps, first, last, T = O.plan(lens, n_kv, C)
+        T2, f2, l2 = _enumerate(lens.tolist(), n_kv, C)
+        assert T == T2
+        np.testing.assert_array_equal(first, f2)
+        np.testing.assert_array_equal(last, l2)
+        np.testing.assert_array_equal(np.diff(rps), (np.maximum(lens, 0) + 15) // 16)
+
+
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0])
+def test_append_writes_one_slot_with_encoder_bytes(dtype):
+    rng = np.random.default_rng(21)
+    rows, n_kv, D, num_pages = 4, 2, 128, 12
+    lens = np.array([1, 17, 32, 5], np.int32)   # slot 0 of page 0, slot 0 of page 1, slot 15, slot 4
+    bt = np.full((rows, 3), -1, np.int32)
+    bt[:, :2] = rng.permutation(num_pages)[:8].reshape(rows, 2)
+    q8 = dtype == W.Q8_0
+    kd = rng.integers(0, 2**15, (num_pages, n_kv, 16, D)).astype(np.uint16)
+    if q8:
+        kd = rng.integers(-127, 128, (num_pages, n_kv, 16, D)).astype(np.int8)
+    vd = kd.copy()
+    ks = rng.integers(0, 2**14, (num_pages, n_kv, 16, D // 32)).astype(np.uint16) if q8 else None
+    vs = ks.copy() if q8 else None
+    before = [a.copy() for a in (kd, vd) + ((ks, vs) if q8 else ())]
+    k_new = rng.standard_normal((rows, n_kv, D)).astype(np.float32)
+    v_new = rng.standard_normal((rows, n_kv, D)).astype(np.float32)
+    O.kv_append(dtype, k_new, v_new, bt, lens, num_pages, kd, vd, ks, vs)
+    touched = np.zeros((num_pages, 16), bool)
+    for i, L in enumerate(lens):
+        page, slot = bt[i, (L - 1) // 16], (L - 1) % 16
+        touched[page, slot] = True
+        for h in range(n_kv):
+            if q8:
+                ck, sk = O.q8_0_encode(k_new[i, h])
+                cv, sv = O.q8_0_encode(v_new[i, h])
+                np.testing.assert_array_equal(kd[page, h, slot], ck)
+                np.testing.assert_array_equal(ks[page, h, slot], sk)
+                np.testing.assert_array_equal(vd[page, h, slot], cv)
+                np.testing.assert_array_equal(vs[page, h, slot], sv)
+            else:
+                np.testing.assert_array_equal(kd[page, h, slot], O.f16_encode(k_new[i, h]))
+                np.testing.assert_array_equal(vd[page, h, slot], O.f16_encode(v_new[i, h]))
+    # explicit page/slot addressing of the worked rows
+    assert touched[bt[0, 0], 0] and touched[bt[1, 1], 0] and touched[bt[2, 1], 15]
+    assert touched[bt[3, 0], 4]
+    for arr, old in zip((kd, vd) + ((ks, vs) if q8 else ()), before):
+        keep = ~touched
+        np.testing.assert_array_equal(arr[keep[:, None, :].repeat(n_kv, 1)],
+                                      old[keep[:, None, :].repeat(n_kv, 1)])
+
+
+def test_append_rejects_page_outside_pool():
+    bt = np.array([[7]], np.int32)
+    kd = np.zeros((4, 1, 16, 32), np.uint16)
+    with pytest.raises(ValueError):
+        O.kv_append(W.F16, np.zeros((1, 1, 32), np.float32), np.zeros((1, 1, 32), np.float32),
+                    bt, np.array([3], np.int32), 4, kd, kd.copy())
