@@ -1,0 +1,215 @@
+/*
+ * pkv.h — C ABI of libpkv.so: one decode step of paged-KV attention on a
+ * GB300 GPU (sm_103a).
+ *
+ * What it computes.  Rows (active sequences) are decoded together in one batch
+ * (Leone, "What ships": continuous decode batching across active requests;
+ * tinyllm, "The repository currently provides": variable-length batched decode
+ * for several active sequences).  Each row's K/V live in a shared pool of
+ * fixed 16-token physical pages, reached through that row's block table
+ * (tinyllm, "The repository currently provides": a runner-owned physical KV
+ * page pool and a logical block table per active sequence; "Known
+ * limitations": 16-token pages).  Attention is GQA (tinyllm, "The repository
+ * currently provides": GQA attention), and K/V are stored as f16 or q8_0
+ * (Leone, "What ships": f16 and q8 KV storage; LeatEngine, "Run": the q8_0
+ * KV cache, as llama.cpp keeps it, in about half the memory of f16).  For
+ * row i and query head g, with G = n_q_heads / n_kv_heads and h = g / G:
+ *
+ *     out[i][g] = sum_{t < L_i} softmax_t(scale * <q[i][g], K[i][h][t]>) V[i][h][t]
+ *
+ * where K and V are the stored values and L_i = seq_lens[i].  tinyllm's own
+ * paged path gathers a row's pages and right-pads them before dense attention
+ * ("Known limitations"); this library reads the pages in place instead.
+ *
+ * Conventions (readings where the pages are silent):
+ *   - seq_lens[i] counts the tokens row i attends to, INCLUDING the token
+ *     appended this step; kv_append writes position seq_lens[i] - 1.
+ *   - Block table: int32 [num_rows][bt_stride]; entry p of row i is the
+ *     physical page of tokens 16p .. 16p + 15.  Only the first
+ *     ceil(seq_lens[i] / 16) entries are read.
+ *   - Pool, per layer, per K and per V (layer l starts at l times the
+ *     per-layer size):
+ *       f16 : data   [num_pages][n_kv_heads][16][head_dim]  binary16
+ *       q8_0: data   [num_pages][n_kv_heads][16][head_dim]  int8 codes
+ *             scales [num_pages][n_kv_heads][16][head_dim/32] binary16
+ *     q8_0 value = scale of the element's 32-wide block (along head_dim)
+ *     times its code.  Encoding: d = amax / 127 (fp32, IEEE division), stored
+ *     scale = binary16(d) rounded to nearest even, code = round(x / d) with
+ *     ties away from zero (using the fp32 d); amax = 0 gives d = 0, codes 0.
+ *   - q, out: fp32 [num_rows][n_q_heads][head_dim].  k_new, v_new: fp32
+ *     [num_rows][n_kv_heads][head_dim].
+ *   - head_dim must be 128; n_q_heads / n_kv_heads must be 1, 2 or 4.
+ *
+ * Ownership and threading.  Every data pointer is a DEVICE pointer that the
+ * caller allocates and frees; the library allocates no device memory, frees
+ * nothing and never synchronises a stream on the decode path.  `stream` is a
+ * cudaStream_t (NULL: the legacy default stream); all work is queued on it and
+ * the calls return before it runs.  The opaque pkv_pool is a small host-side
+ * descriptor; it holds the caller's pointers, not copies.
+ *
+ * Errors.  Every call checks its arguments on the host and returns a status
+ * before queueing anything; a failed launch returns PKV_ERR_CUDA.  Problems
+ * only the device can see (a block-table entry outside the pool, a length
+ * beyond the block table, a bounded wait that gave up) do not fault: the
+ * kernels clamp or skip the access and record a PKV_DEV_* bit in the pool's
+ * optional device status word, which kv_pool_read_status returns.
+ * pkv_last_error_message gives a one-line reason for the calling thread's
+ * last failed call.
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_PAGE_TOKENS 16
+#define PKV_HEAD_DIM 128
+#define PKV_Q8_BLOCK 32
+#define PKV_MAX_ROWS 2048 /* rows per call (per-CTA row tables live in shared memory) */
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer, bad layer */
+    PKV_ERR_UNSUPPORTED = 2,  /* head_dim != 128, GQA group not in {1,2,4}, too many rows */
+    PKV_ERR_CAPACITY = 3,     /* more pages than the pool holds */
+    PKV_ERR_WORKSPACE = 4,    /* workspace missing or smaller than required */
+    PKV_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
+} pkv_status;
+
+/* Bits the kernels OR into the pool's device status word. */
+#define PKV_DEV_BAD_PAGE 1u   /* block-table entry outside [0, num_pages): page 0 read instead, or write skipped */
+#define PKV_DEV_BAD_LENGTH 2u /* seq_lens[i] < 0 or > 16 * bt_stride: clamped */
+#define PKV_DEV_TIMEOUT 4u    /* a bounded wait on a shared-memory barrier gave up */
+
+typedef enum pkv_kv_dtype {
+    PKV_KV_F16 = 0,
+    PKV_KV_Q8_0 = 1,
+} pkv_kv_dtype;
+
+typedef struct pkv_pool pkv_pool;
+
+/* Bytes of one pool array for all layers: which = 0 the data array (K or V),
+ * which = 1 the q8_0 scale array (0 for f16).  Returns 0 for invalid sizes. */
+size_t kv_pool_bytes(int num_layers, int num_pages, int n_kv_heads, int head_dim,
+                     pkv_kv_dtype dtype, int which);
+
+/* Describe a caller-owned KV page pool (tinyllm, "The repository currently
+ * provides": one runner-owned physical KV page pool).
+ *   k_data, v_data     device arrays of kv_pool_bytes(..., 0) bytes, 16-byte aligned
+ *   k_scales, v_scales q8_0: device arrays of kv_pool_bytes(..., 1) bytes,
+ *                      16-byte aligned; f16: must be NULL
+ *   device_status      optional device int32 (NULL: none), zero before first
+ *                      use; kernels OR PKV_DEV_* bits into it.
+ * On success *out receives a descriptor to free with kv_pool_destroy. */
+pkv_status kv_pool_create(pkv_pool **out, int num_layers, int num_pages, int n_kv_heads,
+                          int head_dim, pkv_kv_dtype dtype, void *k_data, void *v_data,
+                          void *k_scales, void *v_scales, int32_t *device_status);
+
+/* Free a descriptor (not the caller's arrays).  NULL is allowed. */
+void kv_pool_destroy(pkv_pool *pool);
+
+/* Wait for `stream`, copy the pool's device status word into *status and
+ * reset it to 0.  This call synchronises; it is not part of the decode path.
+ * Without a status word, *status = 0. */
+pkv_status kv_pool_read_status(const pkv_pool *pool, void *stream, int32_t *status);
+
+/* kv_append — store one new K and V token per row into its page slot
+ * (tinyllm, "The repository currently provides": an incremental decoder per
+ * active sequence writing through its block table; Leone, "What ships" and
+ * LeatEngine, "Run": f16 and q8_0 KV storage).
+ * For each row i with L = seq_lens[i] >= 1 and each KV head h, encodes
+ * k_new[i][h][:] and v_new[i][h][:] (fp32, 16-byte aligned) into page
+ * block_table[i][(L - 1) / 16], slot (L - 1) % 16 of `layer`.  Rows with
+ * L == 0 write nothing.  One launch; asynchronous on `stream`. */
+pkv_status kv_append(const pkv_pool *pool, int layer, const float *k_new, const float *v_new,
+                     const int32_t *block_table, int bt_stride, const int32_t *seq_lens,
+                     int num_rows, void *stream);
+
+/* Number of work chunks (one per resident CTA of the attention kernel) that
+ * fills this GPU, for calls of up to max_rows rows with this pool and
+ * n_q_heads.  Queries the current device. */
+pkv_status paged_decode_default_chunks(const pkv_pool *pool, int n_q_heads, int max_rows,
+                                       int *chunks);
+
+/* Workspace bytes paged_decode_attention needs for up to max_rows rows with
+ * num_chunks chunks.  Layout (256-byte aligned parts), with
+ * S = num_chunks + num_rows * n_kv_heads partial slots and G = n_q/n_kv:
+ *     part_ml  float [S][G][2]  (m2, l) per slot and query head of the group
+ *     part_acc float [S][G][head_dim]
+ * part_acc starts at the first multiple of 256 bytes after part_ml.
+ * Returns 0 for invalid sizes. */
+size_t paged_decode_workspace_bytes(int max_rows, int n_q_heads, int n_kv_heads, int head_dim,
+                                    int num_chunks);
+
+/* paged_decode_attention — decode attention for a batch of variable-length
+ * rows straight from the paged pool (the operation tinyllm's paged-reference
+ * path computes by gathering and right-padding, "Known limitations").
+ *   q            fp32 [num_rows][n_q_heads][128], 16-byte aligned
+ *   block_table  int32 [num_rows][bt_stride]; seq_lens int32 [num_rows]
+ *   scale        softmax scale (1/sqrt(head_dim) for the usual attention)
+ *   out          fp32 [num_rows][n_q_heads][128], 16-byte aligned
+ *   workspace    device scratch of paged_decode_workspace_bytes(num_rows ...)
+ *                bytes, 256-byte aligned; its contents need no initialisation
+ *   num_chunks   work chunks (0: paged_decode_default_chunks for num_rows)
+ * The (row, KV head, page) tiles of the batch are split into num_chunks
+ * equal contiguous chunks, one per CTA; a CTA streams its tiles through
+ * shared memory, keeps a base-2 online softmax in fp32 for the G query heads
+ * of the tile's KV head, and writes either the final output (when it holds a
+ * whole (row, KV head)) or a partial state (m2, l, acc) to slot
+ * chunk + row * n_kv_heads + head of the workspace; a second launch merges
+ * the partials (paged_decode_combine).  Rows with seq_lens[i] == 0 get zeros.
+ * Two launches, no host synchronisation. */
+pkv_status paged_decode_attention(const pkv_pool *pool, int layer, const float *q,
+                                  const int32_t *block_table, int bt_stride,
+                                  const int32_t *seq_lens, int num_rows, int n_q_heads,
+                                  float scale, float *out, void *workspace,
+                                  size_t workspace_bytes, int num_chunks, void *stream);
+
+/* paged_decode_plan — the work split paged_decode_attention uses, written out
+ * for inspection.  Units are (row, KV head, page) tiles in that order; row i
+ * has ceil(seq_lens[i] / 16) pages; T = n_kv_heads * total pages; chunk k
+ * covers units [floor(k T / C), floor((k + 1) T / C)) with C = num_chunks.
+ *   row_page_start  int32 [num_rows + 1]: exclusive prefix sum of pages
+ *   seg_first_chunk, seg_last_chunk  int32 [num_rows * n_kv_heads]: first and
+ *                   last chunk meeting segment (row, head) (-1 if empty)
+ * One single-CTA launch. */
+pkv_status paged_decode_plan(const int32_t *seq_lens, int num_rows, int n_kv_heads,
+                             int bt_stride, int num_chunks, int32_t *row_page_start,
+                             int32_t *seg_first_chunk, int32_t *seg_last_chunk, void *stream);
+
+/* paged_decode_combine — merge the base-2 partial states of every
+ * (row, query head) split over several chunks:
+ *     M = max_s m2_s,  out = sum_s 2^(m2_s - M) acc_s / sum_s 2^(m2_s - M) l_s
+ * over the slots chunk + row * n_kv_heads + head of the chunks the plan
+ * assigns to the segment.  Segments held whole by one chunk are left as they
+ * are; rows with seq_lens[i] == 0 get zeros.  The workspace layout is the one
+ * paged_decode_workspace_bytes describes.  One launch. */
+pkv_status paged_decode_combine(const int32_t *seq_lens, int num_rows, int n_q_heads,
+                                int n_kv_heads, int head_dim, int bt_stride, int num_chunks,
+                                const void *workspace, size_t workspace_bytes, float *out,
+                                void *stream);
+
+/* pkv_decode_step — one decode step of one layer: kv_append of the new token
+ * of every row, then paged_decode_attention over the lengths that include it.
+ * Same arguments as the two calls; three launches in stream order. */
+pkv_status pkv_decode_step(const pkv_pool *pool, int layer, const float *q, const float *k_new,
+                           const float *v_new, const int32_t *block_table, int bt_stride,
+                           const int32_t *seq_lens, int num_rows, int n_q_heads, float scale,
+                           float *out, void *workspace, size_t workspace_bytes, int num_chunks,
+                           void *stream);
+
+/* Name of a status code ("PKV_OK", ...). */
+const char *pkv_status_string(pkv_status status);
+
+/* One-line reason for the calling thread's last failed call ("" if none). */
+const char *pkv_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

@@ -1,0 +1,165 @@
+// pkv_device.cuh — device helpers shared by the kernels of libpkv.so:
+// inline-PTX wrappers for mbarriers and 1-D bulk async copies (global ->
+// shared), a bounded barrier wait, and the per-CTA plan (row page offsets and
+// the chunk a unit belongs to).
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+constexpr int kPage = PKV_PAGE_TOKENS;  // tokens per page
+constexpr int kD = PKV_HEAD_DIM;        // head_dim handled by the kernels
+constexpr int kQBlock = PKV_Q8_BLOCK;   // q8_0 block along head_dim
+constexpr unsigned kFull = 0xffffffffu;
+
+// A wait on a shared-memory barrier gives up after this long (the whole
+// decode of a batch takes well under a millisecond).
+constexpr unsigned long long kWaitLimitNs = 1ull << 30;  // ~1.07 s
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async (bulk copy) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of `bar` with the given parity to complete.  Returns
+// false, without waiting further, once *abort is set or after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// 1-D bulk async copy global -> shared, completing `bytes` of transaction on
+// `bar`, with an L2 eviction-priority hint.  Both addresses 16-byte aligned,
+// bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
+      "%2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// The KV stream is read once per call: mark it first to leave L2.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// Named barrier over `count` threads (id 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void record_status(int32_t* status, uint32_t bits) {
+  if (status) atomicOr(reinterpret_cast<unsigned int*>(status), bits);
+}
+
+// ---------------------------------------------------------------- plan ----
+// The per-CTA plan: validated lengths and the exclusive prefix sum of pages
+// per row, in shared memory.  lens[i] is seq_lens[i] clamped to
+// [0, 16 * bt_stride] (a clamp records PKV_DEV_BAD_LENGTH); row_start has
+// num_rows + 1 entries.  Warp 0 scans; every thread of the CTA must call it.
+__device__ __forceinline__ void plan_rows(const int32_t* __restrict__ seq_lens, int num_rows,
+                                          int bt_stride, int32_t* status, int* lens,
+                                          int* row_start) {
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    if (lane == 0) row_start[0] = 0;
+    for (int base = 0; base < num_rows; base += 32) {
+      const int r = base + lane;
+      int L = 0;
+      if (r < num_rows) {
+        L = seq_lens[r];
+        const int cap = bt_stride * kPage;
+        if (L < 0 || L > cap) {
+          record_status(status, PKV_DEV_BAD_LENGTH);
+          L = L < 0 ? 0 : cap;
+        }
+        lens[r] = L;
+      }
+      int v = (L + kPage - 1) / kPage;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += u;
+      }
+      if (r < num_rows) row_start[r + 1] = carry + v;
+      carry += __shfl_sync(kFull, v, 31);
+    }
+  }
+  __syncthreads();
+}
+
+// Chunk holding unit x (0 <= x < T) when T units are split into C chunks
+// [floor(kT/C), floor((k+1)T/C)): the largest k with floor(kT/C) <= x, which
+// is ceil((x + 1) C / T) - 1.
+__device__ __forceinline__ int chunk_of(long long x, long long T, int C) {
+  return static_cast<int>(((x + 1) * C + T - 1) / T - 1);
+}
+
+// Row holding unit x: the largest i with n_kv * row_start[i] <= x (rows with
+// no pages are skipped automatically).  Requires x < n_kv * row_start[rows].
+__device__ __forceinline__ int row_of(const int* row_start, int num_rows, int n_kv,
+                                      long long x) {
+  int lo = 0, hi = num_rows;  // n_kv*row_start[lo] <= x < n_kv*row_start[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (static_cast<long long>(n_kv) * row_start[mid] <= x)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  return lo;
+}
+
+}  // namespace pkv

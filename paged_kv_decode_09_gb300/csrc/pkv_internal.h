@@ -1,0 +1,90 @@
+// pkv_internal.h — argument blocks and launchers shared between the C-ABI
+// layer (api.cu) and the kernel files (append.cu, decode.cu).  Not installed.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Arguments of the split-KV decode kernel.  Pool pointers already point at
+// the layer's arrays.
+struct DecodeArgs {
+  const uint8_t* k_data;
+  const uint8_t* v_data;
+  const uint8_t* k_scales;  // q8_0 only
+  const uint8_t* v_scales;  // q8_0 only
+  int num_pages;
+  int n_kv;
+  const float* q;
+  const int32_t* block_table;
+  int bt_stride;
+  const int32_t* seq_lens;
+  int num_rows;
+  int n_q;
+  float qscale;  // softmax scale * log2(e): scores are kept in base 2
+  float* out;
+  float* part_ml;   // [slots][G][2]
+  float* part_acc;  // [slots][G][128]
+  int32_t* status;  // optional device status word
+};
+
+struct CombineArgs {
+  const int32_t* seq_lens;
+  int num_rows;
+  int n_q;
+  int n_kv;
+  int bt_stride;
+  int num_chunks;
+  const float* part_ml;
+  const float* part_acc;
+  float* out;
+};
+
+struct PlanArgs {
+  const int32_t* seq_lens;
+  int num_rows;
+  int n_kv;
+  int bt_stride;
+  int num_chunks;
+  int32_t* row_page_start;
+  int32_t* seg_first_chunk;
+  int32_t* seg_last_chunk;
+};
+
+struct AppendArgs {
+  uint8_t* k_data;
+  uint8_t* v_data;
+  uint8_t* k_scales;
+  uint8_t* v_scales;
+  int num_pages;
+  int n_kv;
+  const float* k_new;
+  const float* v_new;
+  const int32_t* block_table;
+  int bt_stride;
+  const int32_t* seq_lens;
+  int num_rows;
+  int32_t* status;
+};
+
+// Workspace layout of the partial states (see paged_decode_workspace_bytes).
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+inline size_t part_ml_bytes(long long slots, int group) {
+  return align256(static_cast<size_t>(slots) * group * 2 * sizeof(float));
+}
+inline size_t part_acc_bytes(long long slots, int group) {
+  return align256(static_cast<size_t>(slots) * group * PKV_HEAD_DIM * sizeof(float));
+}
+
+cudaError_t launch_paged_decode(int dtype, int group, const DecodeArgs& a, int chunks,
+                                cudaStream_t stream);
+cudaError_t paged_decode_blocks_per_sm(int dtype, int group, int rows, int* blocks);
+cudaError_t launch_combine(int group, const CombineArgs& a, cudaStream_t stream);
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
+cudaError_t launch_append(int dtype, const AppendArgs& a, cudaStream_t stream);
+
+}  // namespace pkv
