@@ -1,0 +1,656 @@
+// decode.cu — split-KV paged decode attention, the merge of its partial
+// states, and the plan kernel.
+//
+// The operation (tinyllm, "The repository currently provides": GQA attention,
+// per-sequence block tables into a physical KV page pool; "Known limitations":
+// 16-token pages, and a paged-reference decode that gathers pages before a
+// dense attention): for each row i and query head g of KV head h = g / G,
+//     out[i][g] = softmax_t(scale <q[i][g], K[i][h][t]>) V[i][h][t],  t < L_i.
+// Here the pages are read in place.
+//
+// Work split.  The batch is a list of T = n_kv * sum_i ceil(L_i/16) units,
+// one per (row, KV head, page) in that order.  CTA k of C takes units
+// [floor(kT/C), floor((k+1)T/C)), so every CTA streams the same number of
+// 4 KiB (f16) or 2176-byte (q8_0) tiles whatever the length mix: one 40k-token
+// row and many 16-token rows keep all SMs equally busy.  The units of one
+// (row, head) that fall in one CTA form a "piece"; a piece that is the whole
+// segment writes the output, otherwise it writes a partial state to slot
+// k + (i * n_kv + h) (pieces in unit order increase k, j or both, so the slot
+// is unique), and the combine kernel merges them.
+//
+// Inside a CTA: warp 4 is the producer; its lane 0 streams the chunk's K and V
+// tiles into a ring of shared-memory stages with 1-D bulk async copies
+// tracked by mbarriers (full: bytes landed; empty: the consumer is done).
+// Warps 0-3 are consumers; warp w takes the stages of units w, w+4, ... of the
+// chunk.  Each consumer keeps a base-2 online softmax in fp32 for the G query
+// heads of the unit's KV head, sharing every K and V element it converts
+// across the group.  At the end of a piece the four warps merge through
+// shared memory.
+//
+// Lane layout of a consumer warp on one 16-token page (lane = 8 tg + dj):
+//   scores: lane handles tokens 4tg..4tg+3 and 16 of the 128 dims (f16: two
+//     8-dim chunks dj and dj+8; q8_0: the 16 dims 16dj..16dj+15, inside one
+//     32-wide q8_0 block), for all G heads; the 8 lanes of a token group then
+//     reduce-scatter their 4G partial dot products (3 shuffle steps), leaving
+//     each lane max(G/2, 1) complete scores of one head.
+//   values: lane owns dims 4 lane .. 4 lane + 3 of the accumulator for all G
+//     heads and walks all 16 tokens, reading the probabilities from shared
+//     memory.
+#include <cmath>
+#include <cstdint>
+
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+
+// Shared-memory stage of one unit: the K tile then the V tile of one
+// (page, KV head); q8_0 tiles are codes followed by their block scales.
+template <int DT>
+struct Tiles;
+template <>
+struct Tiles<PKV_KV_F16> {
+  static constexpr uint32_t kData = kPage * kD * 2;  // 4096
+  static constexpr uint32_t kScale = 0;
+  static constexpr uint32_t kTile = kData;
+  static constexpr uint32_t kStage = 2 * kTile;
+  static constexpr int kStages = 8;
+};
+template <>
+struct Tiles<PKV_KV_Q8_0> {
+  static constexpr uint32_t kData = kPage * kD;                   // 2048 codes
+  static constexpr uint32_t kScale = kPage * (kD / kQBlock) * 2;  // 128 bytes of f16 scales
+  static constexpr uint32_t kTile = kData + kScale;
+  static constexpr uint32_t kStage = 2 * kTile;
+  static constexpr int kStages = 12;
+};
+
+// Lane bookkeeping of the score phase for a GQA group of G query heads.
+template <int G>
+struct Group {
+  static_assert(G == 1 || G == 2 || G == 4, "group of 1, 2 or 4 query heads");
+  static constexpr int kLog2 = G == 1 ? 0 : (G == 2 ? 1 : 2);
+  static constexpr int kVals = 4 * G;              // partial dot products per lane
+  static constexpr int kSpl = G >= 2 ? G / 2 : 1;  // complete scores per lane afterwards
+  static constexpr int kTokLanes = 4 / kSpl;       // lanes (low dj bits) splitting a head's 4 tokens
+};
+
+template <int DT, int G>
+struct Smem {
+  static constexpr int kStages = Tiles<DT>::kStages;
+  static constexpr uint32_t kBar = kStages * Tiles<DT>::kStage;       // full[], empty[]
+  static constexpr uint32_t kMrgAcc = kBar + 2 * kStages * 8;          // f32 [warps][G][D]
+  static constexpr uint32_t kMrgMl = kMrgAcc + kConsumerWarps * G * kD * 4;  // f32 [warps][G][2]
+  static constexpr uint32_t kProb = kMrgMl + kConsumerWarps * G * 2 * 4;     // f32 [warps][G][16]
+  static constexpr uint32_t kAlpha = kProb + kConsumerWarps * G * kPage * 4;  // f32 [warps][4]
+  static constexpr uint32_t kFlags = kAlpha + kConsumerWarps * 4 * 4;        // abort, issued
+  static constexpr uint32_t kRows = kFlags + 16;  // int row_start[rows + 1], lens[rows]
+  static size_t bytes(int rows) { return kRows + (2 * static_cast<size_t>(rows) + 1) * 4; }
+  static_assert(kMrgAcc % 16 == 0 && kMrgMl % 16 == 0 && kProb % 16 == 0 && kAlpha % 16 == 0,
+                "vector accesses need 16-byte aligned regions");
+};
+
+// ---------------------------------------------------------- conversions ----
+__device__ __forceinline__ void f16x8_to_f32(const uint4& u, float* f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+    f[2 * i] = v.x;
+    f[2 * i + 1] = v.y;
+  }
+}
+
+__device__ __forceinline__ void f16x4_to_f32(const uint2& u, float* f) {
+  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+  f[0] = a.x;
+  f[1] = a.y;
+  f[2] = b.x;
+  f[3] = b.y;
+}
+
+__device__ __forceinline__ void i8x4_to_f32(uint32_t w, float* f) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) f[i] = static_cast<float>(static_cast<int8_t>((w >> (8 * i)) & 0xffu));
+}
+
+// ------------------------------------------------------- warp reductions ----
+// One reduce-scatter step over lane bit `mask`: N values in, N/2 out.  Lanes
+// with the bit set keep the upper half, the others the lower half, each
+// adding its partner's copy.
+template <int N>
+__device__ __forceinline__ void rs_step(float* v, int mask, int lane) {
+  const bool up = (lane & mask) != 0;
+#pragma unroll
+  for (int k = 0; k < N / 2; ++k) {
+    const float send = up ? v[k] : v[k + N / 2];
+    const float keep = up ? v[k + N / 2] : v[k];
+    v[k] = keep + __shfl_xor_sync(kFull, send, mask);
+  }
+}
+
+// Full dot products of the 8 lanes of a token group: v[g*4 + j] (token
+// 4tg + j, head g) in, Group<G>::kSpl complete scores out in v[0..kSpl): head
+// dj >> (3 - log2 G), tokens 4tg + (dj & (kTokLanes-1)) * kSpl + s.
+template <int G>
+__device__ __forceinline__ void reduce_scores(float* v, int lane) {
+  if constexpr (G == 1) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] += __shfl_xor_sync(kFull, v[k], 4);
+    rs_step<4>(v, 2, lane);
+    rs_step<2>(v, 1, lane);
+  } else {
+    rs_step<4 * G>(v, 4, lane);
+    rs_step<2 * G>(v, 2, lane);
+    rs_step<G>(v, 1, lane);
+  }
+}
+
+// Sum (or max) over the lanes holding distinct tokens of the lane's head.
+template <int G>
+__device__ __forceinline__ float head_sum(float x) {
+#pragma unroll
+  for (int m = 1; m < Group<G>::kTokLanes; m <<= 1) x += __shfl_xor_sync(kFull, x, m);
+  x += __shfl_xor_sync(kFull, x, 8);
+  x += __shfl_xor_sync(kFull, x, 16);
+  return x;
+}
+template <int G>
+__device__ __forceinline__ float head_max(float x) {
+#pragma unroll
+  for (int m = 1; m < Group<G>::kTokLanes; m <<= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, m));
+  x = fmaxf(x, __shfl_xor_sync(kFull, x, 8));
+  x = fmaxf(x, __shfl_xor_sync(kFull, x, 16));
+  return x;
+}
+
+// Per-consumer-warp online softmax state for one piece.
+template <int G>
+struct WarpState {
+  float q[G][16];    // this lane's 16 dims of each query head, times scale*log2(e)
+  float m;           // running max (base 2) of the lane's head
+  float l;           // running sum of the lane's own tokens (reduced at the end)
+  float acc[G][4];   // dims 4 lane .. 4 lane + 3 of each head
+};
+
+// The dims of q a lane's 16 score-phase registers hold.
+template <int DT>
+__device__ __forceinline__ int q_dim(int dj, int e) {
+  if constexpr (DT == PKV_KV_F16)
+    return (e < 8) ? dj * 8 + e : 64 + dj * 8 + (e - 8);
+  else
+    return dj * 16 + e;
+}
+
+// Process one staged (page, KV head) unit of nvalid tokens (1..16).
+template <int DT, int G>
+__device__ __forceinline__ void process_unit(const uint8_t* st, int nvalid, int lane,
+                                             WarpState<G>& S, float* prob, float* alpha) {
+  using GR = Group<G>;
+  using TL = Tiles<DT>;
+  const int tg = lane >> 3, dj = lane & 7;
+
+  // ---- scores: 4 tokens x 16 dims x G heads per lane
+  float v[GR::kVals];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int t = tg * 4 + j;
+    float kf[16];
+    float ksc = 1.0f;
+    if constexpr (DT == PKV_KV_F16) {
+      const uint4 a = *reinterpret_cast<const uint4*>(st + t * 256 + dj * 16);
+      const uint4 b = *reinterpret_cast<const uint4*>(st + t * 256 + 128 + dj * 16);
+      f16x8_to_f32(a, kf);
+      f16x8_to_f32(b, kf + 8);
+    } else {
+      const uint4 c = *reinterpret_cast<const uint4*>(st + t * kD + dj * 16);
+      i8x4_to_f32(c.x, kf);
+      i8x4_to_f32(c.y, kf + 4);
+      i8x4_to_f32(c.z, kf + 8);
+      i8x4_to_f32(c.w, kf + 12);
+      const __half* sc = reinterpret_cast<const __half*>(st + TL::kData);
+      ksc = __half2float(sc[t * (kD / kQBlock) + (dj >> 1)]);
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        s0 = fmaf(S.q[g][e], kf[e], s0);
+        s1 = fmaf(S.q[g][8 + e], kf[8 + e], s1);
+      }
+      v[g * 4 + j] = (s0 + s1) * ksc;
+    }
+  }
+  reduce_scores<G>(v, lane);
+
+  // ---- online softmax of the lane's head over this page
+  const int g_lane = dj >> (3 - GR::kLog2);
+  const int t0 = tg * 4 + (dj & (GR::kTokLanes - 1)) * GR::kSpl;
+  float mx = -INFINITY;
+#pragma unroll
+  for (int s = 0; s < GR::kSpl; ++s) {
+    if (t0 + s >= nvalid) v[s] = -INFINITY;
+    mx = fmaxf(mx, v[s]);
+  }
+  mx = head_max<G>(mx);
+  const float m_new = fmaxf(S.m, mx);
+  const float al = exp2f(S.m - m_new);
+  float psum = 0.f;
+#pragma unroll
+  for (int s = 0; s < GR::kSpl; ++s) {
+    const float p = exp2f(v[s] - m_new);
+    psum += p;
+    prob[g_lane * kPage + t0 + s] = p;
+  }
+  S.l = S.l * al + psum;
+  S.m = m_new;
+  if (tg == 0 && (dj & (GR::kTokLanes - 1)) == 0) alpha[g_lane] = al;
+  __syncwarp();
+
+  // ---- values: acc[g][dims of lane] = acc * alpha + sum_t p[g][t] V[t]
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float a = alpha[g];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) S.acc[g][e] *= a;
+  }
+  const uint8_t* vt = st + TL::kTile;
+  if (nvalid == kPage) {
+#pragma unroll
+    for (int t4 = 0; t4 < kPage; t4 += 4) {
+      float4 p4[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) p4[g] = *reinterpret_cast<const float4*>(prob + g * kPage + t4);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int t = t4 + u;
+        float vf[4];
+        float vsc = 1.0f;
+        if constexpr (DT == PKV_KV_F16) {
+          f16x4_to_f32(*reinterpret_cast<const uint2*>(vt + t * 256 + lane * 8), vf);
+        } else {
+          i8x4_to_f32(*reinterpret_cast<const uint32_t*>(vt + t * kD + lane * 4), vf);
+          vsc = __half2float(
+              reinterpret_cast<const __half*>(vt + TL::kData)[t * (kD / kQBlock) + (lane >> 3)]);
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float p = (&p4[g].x)[u] * vsc;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) S.acc[g][e] = fmaf(p, vf[e], S.acc[g][e]);
+        }
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int t = 0; t < nvalid; ++t) {
+      float vf[4];
+      float vsc = 1.0f;
+      if constexpr (DT == PKV_KV_F16) {
+        f16x4_to_f32(*reinterpret_cast<const uint2*>(vt + t * 256 + lane * 8), vf);
+      } else {
+        i8x4_to_f32(*reinterpret_cast<const uint32_t*>(vt + t * kD + lane * 4), vf);
+        vsc = __half2float(
+            reinterpret_cast<const __half*>(vt + TL::kData)[t * (kD / kQBlock) + (lane >> 3)]);
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float p = prob[g * kPage + t] * vsc;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) S.acc[g][e] = fmaf(p, vf[e], S.acc[g][e]);
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// --------------------------------------------------------------- kernel ----
+template <int DT, int G>
+__global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs a) {
+  using TL = Tiles<DT>;
+  using SM = Smem<DT, G>;
+  using GR = Group<G>;
+  constexpr int NST = TL::kStages;
+  static_assert(NST % kConsumerWarps == 0, "stages are handed to consumer warps round-robin");
+  extern __shared__ __align__(128) uint8_t smem[];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + SM::kFlags);  // [0] abort [1] issued
+  int* row_start = reinterpret_cast<int*>(smem + SM::kRows);
+  int* lens = row_start + a.num_rows + 1;
+  const uint32_t full0 = smem_addr(smem + SM::kBar);
+  const uint32_t empty0 = full0 + NST * 8;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    flags[0] = 0;
+    flags[1] = 0;
+    fence_mbar_init();
+  }
+  plan_rows(a.seq_lens, a.num_rows, a.bt_stride, blockIdx.x == 0 ? a.status : nullptr, lens,
+            row_start);
+
+  const long long T = static_cast<long long>(a.n_kv) * row_start[a.num_rows];
+  const int C = gridDim.x, k = blockIdx.x;
+  const long long c_begin = static_cast<long long>(k) * T / C;
+  const long long c_end = static_cast<long long>(k + 1) * T / C;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------- producer ----
+    const uint32_t stage0 = smem_addr(smem);
+    const uint64_t policy = policy_evict_first();
+    // (page, head) of unit base + lane, read through the block table.
+    auto fetch = [&](long long base, int& page, int& head) {
+      const long long x = base + lane;
+      page = 0;
+      head = 0;
+      if (x < c_end) {
+        const int i = row_of(row_start, a.num_rows, a.n_kv, x);
+        const int npg = row_start[i + 1] - row_start[i];
+        const int off = static_cast<int>(x - static_cast<long long>(a.n_kv) * row_start[i]);
+        head = off / npg;
+        const int p = off - head * npg;
+        int pg = __ldg(a.block_table + static_cast<long long>(i) * a.bt_stride + p);
+        if (pg < 0 || pg >= a.num_pages) {
+          record_status(a.status, PKV_DEV_BAD_PAGE);
+          pg = 0;
+        }
+        page = pg;
+      }
+    };
+    int pg_cur, h_cur;
+    fetch(c_begin, pg_cur, h_cur);
+    uint32_t it = 0;
+    bool stop = false;
+    for (long long base = c_begin; base < c_end && !stop; base += 32) {
+      int pg_nxt = 0, h_nxt = 0;
+      if (base + 32 < c_end) fetch(base + 32, pg_nxt, h_nxt);  // one batch ahead
+      const int n = static_cast<int>(min(32LL, c_end - base));
+      for (int kk = 0; kk < n; ++kk) {
+        const int pg = __shfl_sync(kFull, pg_cur, kk);
+        const int hh = __shfl_sync(kFull, h_cur, kk);
+        int ok = 1;
+        if (lane == 0) {
+          const int s = it % NST;
+          if (it >= NST) ok = mbar_wait_bounded(empty0 + 8 * s, ((it / NST) - 1) & 1, flags);
+          if (ok && flags[0]) ok = 0;
+          if (ok) {
+            const uint32_t bar = full0 + 8 * s;
+            const uint32_t dst = stage0 + s * TL::kStage;
+            const size_t unit = static_cast<size_t>(pg) * a.n_kv + hh;
+            mbar_arrive_expect_tx(bar, TL::kStage);
+            bulk_g2s(dst, a.k_data + unit * TL::kData, TL::kData, bar, policy);
+            if constexpr (DT == PKV_KV_Q8_0)
+              bulk_g2s(dst + TL::kData, a.k_scales + unit * TL::kScale, TL::kScale, bar, policy);
+            bulk_g2s(dst + TL::kTile, a.v_data + unit * TL::kData, TL::kData, bar, policy);
+            if constexpr (DT == PKV_KV_Q8_0)
+              bulk_g2s(dst + TL::kTile + TL::kData, a.v_scales + unit * TL::kScale, TL::kScale,
+                       bar, policy);
+            ++it;
+            flags[1] = static_cast<int>(it);
+          } else if (!flags[0]) {
+            flags[0] = 1;
+            record_status(a.status, PKV_DEV_TIMEOUT);
+          }
+        }
+        if (!__shfl_sync(kFull, ok, 0)) {
+          stop = true;
+          break;
+        }
+      }
+      pg_cur = pg_nxt;
+      h_cur = h_nxt;
+    }
+  } else {
+    // ------------------------------------------------------- consumers ----
+    const int tg = lane >> 3, dj = lane & 7;
+    float* mrg_acc = reinterpret_cast<float*>(smem + SM::kMrgAcc);
+    float* mrg_ml = reinterpret_cast<float*>(smem + SM::kMrgMl);
+    float* prob = reinterpret_cast<float*>(smem + SM::kProb) + warp * G * kPage;
+    float* alpha = reinterpret_cast<float*>(smem + SM::kAlpha) + warp * 4;
+    const int g_lane = dj >> (3 - GR::kLog2);
+    const bool head_writer =
+        tg == 0 && (dj & (GR::kTokLanes - 1)) == 0 && (G > 1 || dj < 4);
+    bool aborted = false;
+    WarpState<G> S;
+
+    for (long long x = c_begin; x < c_end;) {
+      const int i = row_of(row_start, a.num_rows, a.n_kv, x);
+      const int npg = row_start[i + 1] - row_start[i];
+      const long long row_base = static_cast<long long>(a.n_kv) * row_start[i];
+      const int h = static_cast<int>((x - row_base) / npg);
+      const long long seg_start = row_base + static_cast<long long>(h) * npg;
+      const long long seg_end = seg_start + npg;
+      const long long b = min(seg_end, c_end);
+      const int L = lens[i];
+      const bool whole = (x == seg_start) && (b == seg_end);
+
+      const float* qrow = a.q + (static_cast<long long>(i) * a.n_q + h * G) * kD;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+#pragma unroll
+        for (int e = 0; e < 16; e += 4) {
+          const float4 f = __ldg(reinterpret_cast<const float4*>(qrow + g * kD + q_dim<DT>(dj, e)));
+          S.q[g][e] = f.x * a.qscale;
+          S.q[g][e + 1] = f.y * a.qscale;
+          S.q[g][e + 2] = f.z * a.qscale;
+          S.q[g][e + 3] = f.w * a.qscale;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) S.acc[g][e] = 0.f;
+      }
+      S.m = -INFINITY;
+      S.l = 0.f;
+
+      const int r = static_cast<int>((x - c_begin) % kConsumerWarps);
+      for (long long pos = x + ((warp - r + kConsumerWarps) % kConsumerWarps); pos < b;
+           pos += kConsumerWarps) {
+        const uint32_t it = static_cast<uint32_t>(pos - c_begin);
+        const int s = it % NST;
+        bool ok = !aborted && mbar_wait_bounded(full0 + 8 * s, (it / NST) & 1, flags);
+        ok = __all_sync(kFull, ok);
+        if (!ok) {
+          if (!aborted && lane == 0 && !flags[0]) {
+            flags[0] = 1;
+            record_status(a.status, PKV_DEV_TIMEOUT);
+          }
+          aborted = true;
+          continue;
+        }
+        const int nvalid = min(kPage, L - static_cast<int>(pos - seg_start) * kPage);
+        process_unit<DT, G>(smem + s * TL::kStage, nvalid, lane, S, prob, alpha);
+        if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      }
+
+      // ---- merge the four warps' states of this piece
+      const float l_tot = head_sum<G>(S.l);
+      if (head_writer) {
+        mrg_ml[(warp * G + g_lane) * 2] = S.m;
+        mrg_ml[(warp * G + g_lane) * 2 + 1] = l_tot;
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+        *reinterpret_cast<float4*>(mrg_acc + (warp * G + g) * kD + lane * 4) =
+            make_float4(S.acc[g][0], S.acc[g][1], S.acc[g][2], S.acc[g][3]);
+      named_barrier(1, kConsumerThreads);
+      if (!aborted) {
+        const int d = threadIdx.x;  // 0..127
+        const long long slot = k + static_cast<long long>(i) * a.n_kv + h;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float M = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mrg_ml[(w * G + g) * 2]);
+          float Ls = 0.f, A = 0.f;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float f = exp2f(mrg_ml[(w * G + g) * 2] - M);
+            Ls = fmaf(f, mrg_ml[(w * G + g) * 2 + 1], Ls);
+            A = fmaf(f, mrg_acc[(w * G + g) * kD + d], A);
+          }
+          if (whole) {
+            a.out[(static_cast<long long>(i) * a.n_q + h * G + g) * kD + d] = A / Ls;
+          } else {
+            a.part_acc[(slot * G + g) * kD + d] = A;
+            if (d == 0) {
+              a.part_ml[(slot * G + g) * 2] = M;
+              a.part_ml[(slot * G + g) * 2 + 1] = Ls;
+            }
+          }
+        }
+      }
+      named_barrier(1, kConsumerThreads);
+      x = b;
+    }
+  }
+
+  // After a timeout no bulk copy may still be landing in this CTA's shared
+  // memory when it exits: wait (bounded) for the last NST issued copies.
+  __syncthreads();
+  if (threadIdx.x == 0 && flags[0]) {
+    const int issued = flags[1];
+    const int zero = 0;
+    for (int it = issued > NST ? issued - NST : 0; it < issued; ++it)
+      mbar_wait_bounded(full0 + 8 * (it % NST), (it / NST) & 1, &zero);
+  }
+}
+
+// ---------------------------------------------------------------- merge ----
+// One CTA per (row, KV head) segment, one thread per dim.  Merges the
+// partial states of the pieces the plan gives the segment.
+template <int G>
+__global__ void __launch_bounds__(kD) combine_kernel(const CombineArgs a) {
+  extern __shared__ int csm[];
+  int* row_start = csm;
+  int* lens = csm + a.num_rows + 1;
+  plan_rows(a.seq_lens, a.num_rows, a.bt_stride, nullptr, lens, row_start);
+  const int j = blockIdx.x, i = j / a.n_kv, h = j % a.n_kv, d = threadIdx.x;
+  const int npg = row_start[i + 1] - row_start[i];
+  float* o = a.out + (static_cast<long long>(i) * a.n_q + h * G) * kD;
+  if (npg == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) o[g * kD + d] = 0.f;
+    return;
+  }
+  const long long T = static_cast<long long>(a.n_kv) * row_start[a.num_rows];
+  const long long s0 = static_cast<long long>(a.n_kv) * row_start[i] + static_cast<long long>(h) * npg;
+  const int k0 = chunk_of(s0, T, a.num_chunks), k1 = chunk_of(s0 + npg - 1, T, a.num_chunks);
+  if (k0 == k1) return;  // one piece: the attention kernel wrote the output
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float M = -INFINITY;
+    for (int kk = k0; kk <= k1; ++kk) M = fmaxf(M, a.part_ml[((kk + static_cast<long long>(j)) * G + g) * 2]);
+    float Ls = 0.f, A = 0.f;
+    for (int kk = k0; kk <= k1; ++kk) {
+      const long long slot = kk + static_cast<long long>(j);
+      const float f = exp2f(a.part_ml[(slot * G + g) * 2] - M);
+      Ls = fmaf(f, a.part_ml[(slot * G + g) * 2 + 1], Ls);
+      A = fmaf(f, a.part_acc[(slot * G + g) * kD + d], A);
+    }
+    o[g * kD + d] = A / Ls;
+  }
+}
+
+// ----------------------------------------------------------------- plan ----
+__global__ void __launch_bounds__(256) plan_kernel(const PlanArgs a) {
+  extern __shared__ int psm[];
+  int* row_start = psm;
+  int* lens = psm + a.num_rows + 1;
+  plan_rows(a.seq_lens, a.num_rows, a.bt_stride, nullptr, lens, row_start);
+  for (int r = threadIdx.x; r <= a.num_rows; r += blockDim.x) a.row_page_start[r] = row_start[r];
+  const long long T = static_cast<long long>(a.n_kv) * row_start[a.num_rows];
+  for (int j = threadIdx.x; j < a.num_rows * a.n_kv; j += blockDim.x) {
+    const int i = j / a.n_kv, h = j % a.n_kv;
+    const int npg = row_start[i + 1] - row_start[i];
+    int f = -1, l = -1;
+    if (npg > 0) {
+      const long long s0 = static_cast<long long>(a.n_kv) * row_start[i] + static_cast<long long>(h) * npg;
+      f = chunk_of(s0, T, a.num_chunks);
+      l = chunk_of(s0 + npg - 1, T, a.num_chunks);
+    }
+    a.seg_first_chunk[j] = f;
+    a.seg_last_chunk[j] = l;
+  }
+}
+
+// ------------------------------------------------------------ launchers ----
+template <int DT, int G>
+static cudaError_t launch_decode_t(const DecodeArgs& a, int chunks, cudaStream_t st) {
+  const size_t smem = Smem<DT, G>::bytes(a.num_rows);
+  cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<DT, G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  paged_decode_kernel<DT, G><<<chunks, kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int DT, int G>
+static cudaError_t occupancy_t(int rows, int* blocks) {
+  const size_t smem = Smem<DT, G>::bytes(rows);
+  cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<DT, G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, paged_decode_kernel<DT, G>,
+                                                       kThreads, smem);
+}
+
+#define PKV_DISPATCH(DT_, G_, CALL)          \
+  do {                                       \
+    if ((DT_) == PKV_KV_F16) {               \
+      if ((G_) == 1) return CALL(0, 1);      \
+      if ((G_) == 2) return CALL(0, 2);      \
+      if ((G_) == 4) return CALL(0, 4);      \
+    } else {                                 \
+      if ((G_) == 1) return CALL(1, 1);      \
+      if ((G_) == 2) return CALL(1, 2);      \
+      if ((G_) == 4) return CALL(1, 4);      \
+    }                                        \
+    return cudaErrorInvalidValue;            \
+  } while (0)
+
+cudaError_t launch_paged_decode(int dtype, int group, const DecodeArgs& a, int chunks,
+                                cudaStream_t st) {
+#define PKV_CALL(D, G) launch_decode_t<D, G>(a, chunks, st)
+  PKV_DISPATCH(dtype, group, PKV_CALL);
+#undef PKV_CALL
+}
+
+cudaError_t paged_decode_blocks_per_sm(int dtype, int group, int rows, int* blocks) {
+#define PKV_CALL(D, G) occupancy_t<D, G>(rows, blocks)
+  PKV_DISPATCH(dtype, group, PKV_CALL);
+#undef PKV_CALL
+}
+
+cudaError_t launch_combine(int group, const CombineArgs& a, cudaStream_t st) {
+  const int segs = a.num_rows * a.n_kv;
+  if (segs == 0) return cudaSuccess;
+  const size_t smem = (2 * static_cast<size_t>(a.num_rows) + 1) * sizeof(int);
+  if (group == 1)
+    combine_kernel<1><<<segs, kD, smem, st>>>(a);
+  else if (group == 2)
+    combine_kernel<2><<<segs, kD, smem, st>>>(a);
+  else if (group == 4)
+    combine_kernel<4><<<segs, kD, smem, st>>>(a);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t st) {
+  const size_t smem = (2 * static_cast<size_t>(a.num_rows) + 1) * sizeof(int);
+  plan_kernel<<<1, 256, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv
