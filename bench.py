@@ -1,0 +1,464 @@
+#!/usr/bin/env python3
+"""Benchmark one decode step of paged-KV attention on GB300.
+
+A step is one pass of the whole hot path over one batch: kv_append of each
+row's new token, then paged decode attention (split-KV kernel + merge) over
+lengths that include it, for one layer's pool.  Default workload: the 8B layer
+shape with f16 KV (8 rows, L ~ U[1024, 8192], 32 q / 8 KV heads, head_dim 128).
+Steps rotate over several layer pools whose total size is more than 4x the
+L2 cache, so every step reads KV from HBM.
+
+Metric (bytes counted per step: K and V of every attended token, q, out):
+  value      KV GB/s, device-resident inputs, CUDA events on the stream
+  roofline   the split-KV kernel's algorithmic GB/s over its own mean event time,
+             against the measured HBM copy bandwidth
+  e2e        the same metric through the C ABI with the step's inputs copied
+             from pinned host memory and the output copied back, every step
+  cpu_baseline  the FP64 CPU oracle on a bounded sample of the same batch
+
+`--impl reference` times the oracle alone on the host cores (the same metric).
+Under torchrun each rank runs its own replica of the batch (no collective on
+the data path); times are the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_BYTES = 126 * 2**20
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--workload", default="llama8b_f16")
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--layers", type=int, default=0, help="layer pools to rotate (0: auto)")
+    p.add_argument("--chunks", type=int, default=0, help="work chunks (0: one per resident CTA)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU baseline budget")
+    return p.parse_args()
+
+
+# ------------------------------------------------------------ distributed ----
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x across ranks (x itself at world size 1)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- clocks ----
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.06)
+        self.proc.terminate()
+        self.proc.wait(timeout=5)
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ sizes ----
+def read_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def step_bytes(wl) -> int:
+    """Algorithmic bytes of one decode call: K and V of every attended token
+    (f16: 2 bytes per element; q8_0: 34 bytes per 32 elements), q and out."""
+    cfg = wl.cfg
+    per_elem = 2.0 if cfg.dtype == 0 else 34.0 / 32.0
+    kv = int(sum(int(L) for L in wl.seq_lens)) * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem
+    qo = 2 * wl.rows * cfg.n_q_heads * cfg.head_dim * 4
+    return int(kv + qo)
+
+
+def profile_traffic(workload: str):
+    """DRAM bytes per split-KV launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    src = os.path.join(ROOT, "paged_kv_decode_09_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in ("decode.cu", "pkv_device.cuh"):
+        with open(os.path.join(src, name), "rb") as f:
+            h.update(f.read())
+    digest = h.hexdigest()[:16]
+    path = os.path.join(ROOT, "profiles", f"paged_decode_split_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_sha256_16:\s*([0-9a-f]{16})", text)
+    if not m or m.group(2) != digest:
+        return None
+    return int(m.group(1))
+
+
+# ------------------------------------------------------------- our kernels ----
+def fill_pool(api, pool, layers, seed):
+    """Fill every slot of every layer with N(0,1) values stored by the
+    library's own kv_append (one pseudo-row per slot)."""
+    import torch
+    g = torch.Generator(device=pool.device).manual_seed(seed)
+    per = 2048
+    for layer in range(layers):
+        for p0 in range(0, pool.num_pages, per):
+            p1 = min(p0 + per, pool.num_pages)
+            rows = (p1 - p0) * 16
+            r = torch.arange(rows, device=pool.device, dtype=torch.int32)
+            bt = (p0 + r // 16).to(torch.int32).reshape(rows, 1).contiguous()
+            sl = (r % 16 + 1).to(torch.int32).contiguous()
+            k = torch.randn(rows, pool.n_kv, 128, device=pool.device, generator=g)
+            v = torch.randn(rows, pool.n_kv, 128, device=pool.device, generator=g)
+            api.kv_append(pool, layer, k, v, bt, sl)
+    torch.cuda.synchronize()
+
+
+def run_ours(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    from paged_kv_decode_09_gb300 import api
+    from paged_kv_decode_09_gb300 import workloads as W
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = W.draw(args.workload)
+    cfg = wl.cfg
+    layer_bytes = 2 * api.KVPool.bytes(1, wl.num_pages, cfg.n_kv_heads, cfg.dtype, 0) + \
+        2 * api.KVPool.bytes(1, wl.num_pages, cfg.n_kv_heads, cfg.dtype, 1)
+    layers = args.layers or max(2, min(cfg.model_layers, -(-4 * L2_BYTES // layer_bytes)))
+    pool = api.KVPool(layers, wl.num_pages, cfg.n_kv_heads, cfg.dtype, device=dev)
+    fill_pool(api, pool, layers, seed=1234 + rank)
+
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    q, k_new, v_new = t(wl.q), t(wl.k_new), t(wl.v_new)
+    bt, sl = t(wl.block_table), t(wl.seq_lens)
+    out = torch.empty_like(q)
+    ws = api.Workspace(pool, cfg.n_q_heads, wl.rows, args.chunks)
+    L = api.lib()
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    P = lambda x: ctypes.c_void_p(x.data_ptr())  # noqa: E731
+    a_q, a_k, a_v, a_bt, a_sl, a_out, a_ws = map(P, (q, k_new, v_new, bt, sl, out, ws.tensor))
+    H, R, NQ, S, CH = pool.handle, wl.rows, cfg.n_q_heads, wl.bt_stride, ws.num_chunks
+    scale = ctypes.c_float(wl.scale)
+
+    def chk(st, what):
+        if st:
+            raise api.PkvError(st, what, L.pkv_last_error_message().decode())
+
+    def step(layer, ev=None):
+        chk(L.kv_append(H, layer, a_k, a_v, a_bt, S, a_sl, R, sp), "kv_append")
+        if ev is not None:
+            ev[0].record(stream)
+        chk(L.paged_decode_split(H, layer, a_q, a_bt, S, a_sl, R, NQ, scale, a_out, a_ws,
+                                 ws.nbytes, CH, sp), "paged_decode_split")
+        if ev is not None:
+            ev[1].record(stream)
+        chk(L.paged_decode_combine(a_sl, R, NQ, cfg.n_kv_heads, 128, S, CH, a_ws, ws.nbytes,
+                                   a_out, sp), "paged_decode_combine")
+
+    for w in range(args.warmup):
+        step(w % layers)
+    torch.cuda.synchronize()
+    assert pool.read_status() == 0, "device status word set during warm-up"
+
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.1)
+    e0.record(stream)
+    for s in range(K):
+        step(s % layers, evs[s])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    barrier(world)
+    total_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    split_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    assert pool.read_status() == 0, "device status word set during the timed steps"
+
+    # ---- end to end through the C ABI: pinned host inputs in, output out
+    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k_new, v_new))
+    hbt, hsl = bt.cpu().pin_memory(), sl.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hbt, hsl))
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step(layer):
+        for d_, h_ in ((q, hq), (k_new, hk), (v_new, hv), (bt, hbt), (sl, hsl)):
+            d_.copy_(h_, non_blocking=True)
+        chk(L.pkv_decode_step(H, layer, a_q, a_k, a_v, a_bt, S, a_sl, R, NQ, scale, a_out, a_ws,
+                              ws.nbytes, CH, sp), "pkv_decode_step")
+        hout.copy_(out, non_blocking=True)
+
+    Ke = min(K, 2000)
+    for w in range(args.warmup):
+        e2e_step(w % layers)
+    torch.cuda.synchronize()
+    barrier(world)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for s in range(Ke):
+        e2e_step(s % layers)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), world)
+
+    nbytes = step_bytes(wl)
+    peak, peak_src = read_peak()
+    step_s = total_ms / 1e3 / K
+    value = world * nbytes / step_s / 1e9
+    achieved = nbytes / (split_ms / 1e3) / 1e9
+    tokens = int(sum(int(x) for x in wl.seq_lens))
+    result = {
+        "metric": "paged decode-attn KV GB/s & % of GB300 HBM peak; rows*tokens/s at 1 GPU",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / K, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": W.DTYPE_NAMES[cfg.dtype] + " KV, f32 compute",
+        "data": "synthetic: seeded lengths/block tables/q; KV N(0,1) stored by kv_append",
+        "config": {
+            "workload": cfg.name, "description": cfg.description, "rows": wl.rows,
+            "n_q_heads": cfg.n_q_heads, "n_kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim,
+            "kv_dtype": W.DTYPE_NAMES[cfg.dtype], "tokens_attended": tokens,
+            "pages_per_layer": wl.num_pages, "layers_rotated": layers,
+            "l2": f"inputs larger than L2: {layers} layer pools of "
+                  f"{layer_bytes / 2**20:.0f} MiB rotated (> 4x the 126 MiB L2)",
+            "chunks": CH, "bytes_per_step": nbytes, "parallelism": f"replicas x{world}",
+        },
+        "frac_of_hbm_peak": round(value / world / peak, 4),
+        "rows_tokens_per_s": round(world * tokens / step_s, 1),
+        "rows_per_s": round(world * wl.rows / step_s, 1),
+        "roofline": {
+            "bound": "hbm", "kernel": f"paged_decode_kernel<{W.DTYPE_NAMES[cfg.dtype]}, G="
+                                      f"{cfg.group}>",
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (copy bandwidth)",
+            "traffic": profile_traffic(cfg.name), "mean_launch_us": round(split_ms * 1e3, 3),
+        },
+        "e2e": {"value": round(world * nbytes / (e2e_ms / 1e3 / Ke) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
+                "ms_per_step": round(e2e_ms / Ke, 6)},
+        "gpu_launches": 3 * K,
+        "clocks": clock_info,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl, pool, args.cpu_seconds)
+    return result
+
+
+def cpu_baseline(wl, pool, budget_s):
+    """The FP64 oracle, as it stands, on a bounded sample of rows of layer 0."""
+    import numpy as np
+    import torch
+
+    import oracle as O
+    cfg = wl.cfg
+    if cfg.dtype == 0:
+        kd = pool.k_data[0].cpu().view(torch.int16).numpy().view(np.uint16)
+        vd = pool.v_data[0].cpu().view(torch.int16).numpy().view(np.uint16)
+        ks = vs = None
+    else:
+        kd, vd = pool.k_data[0].cpu().numpy(), pool.v_data[0].cpu().numpy()
+        ks = pool.k_scales[0].cpu().view(torch.int16).numpy().view(np.uint16)
+        vs = pool.v_scales[0].cpu().view(torch.int16).numpy().view(np.uint16)
+    order = np.argsort(wl.seq_lens)  # shortest rows first, to bound the sample
+    done, secs, rows = 0, 0.0, []
+    for i in order:
+        t0 = time.perf_counter()
+        O.decode_attention(cfg.dtype, wl.q[i:i + 1], kd, vd, ks, vs, wl.block_table[i:i + 1],
+                           wl.seq_lens[i:i + 1], wl.num_pages, cfg.n_kv_heads, wl.scale)
+        secs += time.perf_counter() - t0
+        rows.append(int(i))
+        done += int(wl.seq_lens[i])
+        if secs > budget_s:
+            break
+    per_elem = 2.0 if cfg.dtype == 0 else 34.0 / 32.0
+    nbytes = done * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem + 2 * len(rows) * cfg.n_q_heads * 128 * 4
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": O.num_threads(),
+            "kind": "oracle",
+            "sample": f"{len(rows)} of {wl.rows} rows ({done} attended tokens) of one layer, "
+                      f"attention only, {secs:.1f} s",
+            "rows_tokens_per_s": round(done / secs, 1)}
+
+
+# ------------------------------------------------------------- reference ----
+def run_reference(args):
+    """The FP64 oracle on the host cores, each step one row of the batch."""
+    import numpy as np
+
+    import oracle as O
+    from paged_kv_decode_09_gb300 import workloads as W
+    wl = W.draw(args.workload)
+    cfg = wl.cfg
+    k, v = W.context_values(wl)
+    kd, ks = O.encode_pool(cfg.dtype, k)
+    vd, vs = O.encode_pool(cfg.dtype, v)
+    del k, v
+    order = np.argsort(wl.seq_lens)
+    G = cfg.group
+    # A step is one row, or (when K rows would overrun the time budget) every
+    # G-th query head of one row, i.e. one query head per KV head: 1/G of the
+    # row's work, with the same per-head computation.
+    heads = slice(None)
+
+    def one(i):
+        q = wl.q[i:i + 1, heads]
+        O.decode_attention(cfg.dtype, q, kd, vd, ks, vs, wl.block_table[i:i + 1],
+                           wl.seq_lens[i:i + 1], wl.num_pages, cfg.n_kv_heads, wl.scale)
+
+    per_elem = 2.0 if cfg.dtype == 0 else 34.0 / 32.0
+
+    def row_bytes(i, frac):
+        return frac * (int(wl.seq_lens[i]) * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem
+                       + 2 * cfg.n_q_heads * 128 * 4)
+
+    mid = order[len(order) // 2]
+    t0 = time.perf_counter()
+    one(mid)
+    t_row = time.perf_counter() - t0
+    frac, sample = 1.0, "one row of the batch per step, cycling shortest first"
+    if (args.steps + args.warmup) * t_row > 150.0 and G > 1:
+        heads, frac = slice(None, None, G), 1.0 / G
+        sample = (f"every {G}th query head (one per KV head) of one row per step, cycling "
+                  f"shortest first: 1/{G} of a row's work")
+    for w in range(args.warmup):
+        one(order[w % wl.rows])
+    nbytes, tokens, secs = 0.0, 0, 0.0
+    for s in range(args.steps):
+        i = order[s % wl.rows]
+        t0 = time.perf_counter()
+        one(i)
+        secs += time.perf_counter() - t0
+        nbytes += row_bytes(i, frac)
+        tokens += frac * int(wl.seq_lens[i])
+    value = nbytes / secs / 1e9
+    return {
+        "impl": "reference",
+        "metric": "paged decode-attn KV GB/s & % of GB300 HBM peak; rows*tokens/s at 1 GPU",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(secs * 1e3 / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic: same seeded workload, pool encoded by the oracle",
+        "config": {"workload": cfg.name, "description": cfg.description, "sample": sample},
+        "rows_tokens_per_s": round(tokens / secs, 1),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": O.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        # host-only: rank 0 alone times the oracle, the other ranks exit at once
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    rank, world, local = dist_init(args)
+    result = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -124,7 +124,8 @@ pkv_status kv_pool_read_status(const pkv_pool *pool, void *stream, int32_t *stat
  * For each row i with L = seq_lens[i] >= 1 and each KV head h, encodes
  * k_new[i][h][:] and v_new[i][h][:] (fp32, 16-byte aligned) into page
  * block_table[i][(L - 1) / 16], slot (L - 1) % 16 of `layer`.  Rows with
- * L == 0 write nothing.  One launch; asynchronous on `stream`. */
+ * L == 0 write nothing.  num_rows is not limited by PKV_MAX_ROWS (up to 2^24).
+ * One launch; asynchronous on `stream`. */
 pkv_status kv_append(const pkv_pool *pool, int layer, const float *k_new, const float *v_new,
                      const int32_t *block_table, int bt_stride, const int32_t *seq_lens,
                      int num_rows, void *stream);
@@ -168,6 +169,18 @@ pkv_status paged_decode_attention(const pkv_pool *pool, int layer, const float *
                                   const int32_t *seq_lens, int num_rows, int n_q_heads,
                                   float scale, float *out, void *workspace,
                                   size_t workspace_bytes, int num_chunks, void *stream);
+
+/* paged_decode_split — the first of the two launches of
+ * paged_decode_attention alone (same arguments): every piece that holds a
+ * whole (row, KV head) writes `out`, the others write their partial states to
+ * the workspace.  paged_decode_combine with the same seq_lens, num_chunks and
+ * workspace completes the call.  Exposed so that callers can time or
+ * schedule the two launches separately.  One launch. */
+pkv_status paged_decode_split(const pkv_pool *pool, int layer, const float *q,
+                              const int32_t *block_table, int bt_stride, const int32_t *seq_lens,
+                              int num_rows, int n_q_heads, float scale, float *out,
+                              void *workspace, size_t workspace_bytes, int num_chunks,
+                              void *stream);
 
 /* paged_decode_plan — the work split paged_decode_attention uses, written out
  * for inspection.  Units are (row, KV head, page) tiles in that order; row i

@@ -1,0 +1,280 @@
+"""ctypes binding of libpkv.so (C ABI in include/pkv.h).
+
+Argument marshalling only: every function checks tensor dtypes, shapes and
+devices, passes raw device pointers and the current torch CUDA stream to the
+C entry point of the same name, and raises PkvError on a non-zero status.  All
+compute runs in the library's CUDA kernels; there is no CPU fallback, and a
+missing library raises on first use.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+F16, Q8_0 = 0, 1
+PAGE = 16
+HEAD_DIM = 128
+Q8_BLOCK = 32
+MAX_ROWS = 2048
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libpkv.so")
+_lock = threading.Lock()
+_lib = None
+
+STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARG", 2: "PKV_ERR_UNSUPPORTED",
+                3: "PKV_ERR_CAPACITY", 4: "PKV_ERR_WORKSPACE", 5: "PKV_ERR_CUDA"}
+DEV_BAD_PAGE, DEV_BAD_LENGTH, DEV_TIMEOUT = 1, 2, 4
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, where: str, message: str):
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+_vp, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+_SIGS = {
+    "kv_pool_bytes": ([_i, _i, _i, _i, _i, _i], _sz),
+    "kv_pool_create": ([ctypes.POINTER(_vp), _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp], _i),
+    "kv_pool_destroy": ([_vp], None),
+    "kv_pool_read_status": ([_vp, _vp, ctypes.POINTER(ctypes.c_int32)], _i),
+    "kv_append": ([_vp, _i, _vp, _vp, _vp, _i, _vp, _i, _vp], _i),
+    "paged_decode_default_chunks": ([_vp, _i, _i, ctypes.POINTER(_i)], _i),
+    "paged_decode_workspace_bytes": ([_i, _i, _i, _i, _i], _sz),
+    "paged_decode_attention": ([_vp, _i, _vp, _vp, _i, _vp, _i, _i, ctypes.c_float, _vp, _vp,
+                                _sz, _i, _vp], _i),
+    "paged_decode_split": ([_vp, _i, _vp, _vp, _i, _vp, _i, _i, ctypes.c_float, _vp, _vp,
+                            _sz, _i, _vp], _i),
+    "paged_decode_plan": ([_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp], _i),
+    "paged_decode_combine": ([_vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp], _i),
+    "pkv_decode_step": ([_vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, ctypes.c_float, _vp, _vp,
+                         _sz, _i, _vp], _i),
+    "pkv_status_string": ([_i], ctypes.c_char_p),
+    "pkv_last_error_message": ([], ctypes.c_char_p),
+}
+
+
+def lib():
+    """The loaded libpkv.so.  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise PkvError(-1, "libpkv", f"{_LIB_PATH} is missing: run "
+                               "paged_kv_decode_09_gb300.build.build() (nvcc, sm_103a) first")
+            L = ctypes.CDLL(_LIB_PATH)
+            for name, (args, res) in _SIGS.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().pkv_status_string(status).decode()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise PkvError(status, where, lib().pkv_last_error_message().decode())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, dtype, name, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+class KVPool:
+    """A caller-owned paged KV pool (torch tensors) and its library descriptor.
+
+    k_data / v_data: [layers][pages][n_kv][16][128] float16 (f16) or int8 (q8_0);
+    k_scales / v_scales (q8_0): [layers][pages][n_kv][16][4] float16;
+    status: int32 [1] device status word."""
+
+    def __init__(self, num_layers, num_pages, n_kv_heads, dtype=F16, head_dim=HEAD_DIM,
+                 device="cuda", tensors=None):
+        self.num_layers, self.num_pages, self.n_kv = num_layers, num_pages, n_kv_heads
+        self.dtype, self.head_dim = dtype, head_dim
+        self.device = torch.device(device)
+        shape = (num_layers, num_pages, n_kv_heads, PAGE, head_dim)
+        sshape = (num_layers, num_pages, n_kv_heads, PAGE, head_dim // Q8_BLOCK)
+        if tensors is None:
+            tdt = torch.float16 if dtype == F16 else torch.int8
+            tensors = [torch.empty(shape, dtype=tdt, device=self.device),
+                       torch.empty(shape, dtype=tdt, device=self.device)]
+            if dtype == Q8_0:
+                tensors += [torch.empty(sshape, dtype=torch.float16, device=self.device),
+                            torch.empty(sshape, dtype=torch.float16, device=self.device)]
+        self.k_data, self.v_data = tensors[0], tensors[1]
+        self.k_scales = tensors[2] if dtype == Q8_0 else None
+        self.v_scales = tensors[3] if dtype == Q8_0 else None
+        tdt = torch.float16 if dtype == F16 else torch.int8
+        for name in ("k_data", "v_data"):
+            _need(getattr(self, name), tdt, name, shape, self.device)
+        if dtype == Q8_0:
+            for name in ("k_scales", "v_scales"):
+                _need(getattr(self, name), torch.float16, name, sshape, self.device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        h = ctypes.c_void_p()
+        _check(lib().kv_pool_create(ctypes.byref(h), num_layers, num_pages, n_kv_heads, head_dim,
+                                    dtype, _ptr(self.k_data), _ptr(self.v_data),
+                                    _ptr(self.k_scales), _ptr(self.v_scales), _ptr(self.status)),
+               "kv_pool_create")
+        self.handle = h
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h and _lib is not None:
+            _lib.kv_pool_destroy(h)
+            self.handle = None
+
+    def read_status(self, stream=None) -> int:
+        """Synchronise and return (and clear) the device status word."""
+        out = ctypes.c_int32(0)
+        _check(lib().kv_pool_read_status(self.handle, _stream(stream), ctypes.byref(out)),
+               "kv_pool_read_status")
+        return out.value
+
+    @staticmethod
+    def bytes(num_layers, num_pages, n_kv_heads, dtype, which=0, head_dim=HEAD_DIM) -> int:
+        return lib().kv_pool_bytes(num_layers, num_pages, n_kv_heads, head_dim, dtype, which)
+
+
+def default_chunks(pool: KVPool, n_q_heads: int, max_rows: int) -> int:
+    c = ctypes.c_int(0)
+    _check(lib().paged_decode_default_chunks(pool.handle, n_q_heads, max_rows, ctypes.byref(c)),
+           "paged_decode_default_chunks")
+    return c.value
+
+
+def workspace_bytes(max_rows: int, n_q_heads: int, n_kv_heads: int, num_chunks: int,
+                    head_dim: int = HEAD_DIM) -> int:
+    n = lib().paged_decode_workspace_bytes(max_rows, n_q_heads, n_kv_heads, head_dim, num_chunks)
+    if n == 0 and max_rows > 0:
+        raise PkvError(1, "paged_decode_workspace_bytes", "invalid sizes")
+    return n
+
+
+class Workspace:
+    """Device scratch for paged_decode_attention (partial states)."""
+
+    def __init__(self, pool: KVPool, n_q_heads: int, max_rows: int, num_chunks: int = 0):
+        self.num_chunks = num_chunks or default_chunks(pool, n_q_heads, max_rows)
+        self.nbytes = workspace_bytes(max_rows, n_q_heads, pool.n_kv, self.num_chunks)
+        self.tensor = torch.empty(max(self.nbytes, 256), dtype=torch.uint8, device=pool.device)
+
+
+def _rows(block_table, seq_lens, device):
+    _need(block_table, torch.int32, "block_table", device=device)
+    _need(seq_lens, torch.int32, "seq_lens", device=device)
+    if block_table.dim() != 2 or seq_lens.dim() != 1 or block_table.shape[0] != seq_lens.shape[0]:
+        raise ValueError("block_table must be [rows][stride] and seq_lens [rows]")
+    return seq_lens.shape[0], block_table.shape[1]
+
+
+def kv_append(pool: KVPool, layer: int, k_new, v_new, block_table, seq_lens, stream=None):
+    rows, stride = _rows(block_table, seq_lens, pool.device)
+    shape = (rows, pool.n_kv, pool.head_dim)
+    _need(k_new, torch.float32, "k_new", shape, pool.device)
+    _need(v_new, torch.float32, "v_new", shape, pool.device)
+    _check(lib().kv_append(pool.handle, layer, _ptr(k_new), _ptr(v_new), _ptr(block_table),
+                           stride, _ptr(seq_lens), rows, _stream(stream)), "kv_append")
+
+
+def paged_decode_attention(pool: KVPool, layer: int, q, block_table, seq_lens, scale: float,
+                           out=None, workspace: Workspace | None = None, num_chunks: int = 0,
+                           stream=None):
+    rows, stride = _rows(block_table, seq_lens, pool.device)
+    _need(q, torch.float32, "q", device=pool.device)
+    if q.dim() != 3 or q.shape[0] != rows or q.shape[2] != pool.head_dim:
+        raise ValueError("q must be [rows][n_q_heads][128]")
+    n_q = q.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.float32, "out", q.shape, pool.device)
+    if workspace is None:
+        workspace = Workspace(pool, n_q, max(rows, 1), num_chunks)
+    chunks = num_chunks or workspace.num_chunks
+    _check(lib().paged_decode_attention(pool.handle, layer, _ptr(q), _ptr(block_table), stride,
+                                        _ptr(seq_lens), rows, n_q, float(scale), _ptr(out),
+                                        _ptr(workspace.tensor), workspace.nbytes, chunks,
+                                        _stream(stream)), "paged_decode_attention")
+    return out
+
+
+def decode_step(pool: KVPool, layer: int, q, k_new, v_new, block_table, seq_lens, scale: float,
+                out=None, workspace: Workspace | None = None, num_chunks: int = 0, stream=None):
+    """kv_append then paged_decode_attention (pkv_decode_step)."""
+    rows, stride = _rows(block_table, seq_lens, pool.device)
+    _need(q, torch.float32, "q", device=pool.device)
+    shape = (rows, pool.n_kv, pool.head_dim)
+    _need(k_new, torch.float32, "k_new", shape, pool.device)
+    _need(v_new, torch.float32, "v_new", shape, pool.device)
+    n_q = q.shape[1]
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.float32, "out", q.shape, pool.device)
+    if workspace is None:
+        workspace = Workspace(pool, n_q, max(rows, 1), num_chunks)
+    chunks = num_chunks or workspace.num_chunks
+    _check(lib().pkv_decode_step(pool.handle, layer, _ptr(q), _ptr(k_new), _ptr(v_new),
+                                 _ptr(block_table), stride, _ptr(seq_lens), rows, n_q,
+                                 float(scale), _ptr(out), _ptr(workspace.tensor),
+                                 workspace.nbytes, chunks, _stream(stream)), "pkv_decode_step")
+    return out
+
+
+def paged_decode_plan(seq_lens, n_kv_heads: int, bt_stride: int, num_chunks: int, stream=None):
+    """(row_page_start [rows+1], seg_first_chunk, seg_last_chunk [rows*n_kv]) int32 tensors."""
+    _need(seq_lens, torch.int32, "seq_lens")
+    rows = seq_lens.shape[0]
+    dev = seq_lens.device
+    rps = torch.empty(rows + 1, dtype=torch.int32, device=dev)
+    first = torch.empty(max(rows * n_kv_heads, 1), dtype=torch.int32, device=dev)
+    last = torch.empty_like(first)
+    _check(lib().paged_decode_plan(_ptr(seq_lens), rows, n_kv_heads, bt_stride, num_chunks,
+                                   _ptr(rps), _ptr(first), _ptr(last), _stream(stream)),
+           "paged_decode_plan")
+    return rps, first[:rows * n_kv_heads], last[:rows * n_kv_heads]
+
+
+def paged_decode_combine(seq_lens, n_q_heads: int, n_kv_heads: int, bt_stride: int,
+                         num_chunks: int, workspace: torch.Tensor, out, stream=None):
+    """Merge partial states held in `workspace` (layout of paged_decode_workspace_bytes)."""
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(workspace, torch.uint8, "workspace")
+    _need(out, torch.float32, "out")
+    rows = seq_lens.shape[0]
+    _check(lib().paged_decode_combine(_ptr(seq_lens), rows, n_q_heads, n_kv_heads, HEAD_DIM,
+                                      bt_stride, num_chunks, _ptr(workspace), workspace.numel(),
+                                      _ptr(out), _stream(stream)), "paged_decode_combine")
+    return out

@@ -66,10 +66,11 @@ pkv_status check_geometry(int n_q, int n_kv, int head_dim) {
   return PKV_OK;
 }
 
-pkv_status check_rows(int num_rows, int bt_stride, const int32_t* bt, const int32_t* sl) {
+pkv_status check_rows(int num_rows, int bt_stride, const int32_t* bt, const int32_t* sl,
+                      int max_rows = PKV_MAX_ROWS) {
   if (num_rows < 0) return fail(PKV_ERR_INVALID_ARG, "num_rows < 0");
-  if (num_rows > PKV_MAX_ROWS)
-    return fail(PKV_ERR_UNSUPPORTED, "num_rows %d > %d", num_rows, PKV_MAX_ROWS);
+  if (num_rows > max_rows)
+    return fail(PKV_ERR_UNSUPPORTED, "num_rows %d > %d", num_rows, max_rows);
   if (num_rows > 0 && (!bt || !sl)) return fail(PKV_ERR_INVALID_ARG, "null block table or seq_lens");
   if (bt_stride < 1) return fail(PKV_ERR_INVALID_ARG, "bt_stride < 1");
   if (!aligned(bt, 4) || !aligned(sl, 4))
@@ -110,7 +111,8 @@ pkv_status default_chunks(const pkv_pool* p, int n_q, int rows, int* chunks) {
 pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q,
                           const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
                           int num_rows, int n_q, float scale, float* out, void* workspace,
-                          size_t workspace_bytes, int num_chunks, void* stream) {
+                          size_t workspace_bytes, int num_chunks, void* stream,
+                          bool run_combine) {
   pkv_status s = check_pool_layer(pool, layer);
   if (s) return s;
   if ((s = check_geometry(n_q, pool->n_kv, pool->head_dim))) return s;
@@ -151,6 +153,7 @@ pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q,
   a.status = pool->status;
   cudaError_t e = pkv::launch_paged_decode(pool->dtype, g, a, num_chunks, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged decode launch");
+  if (!run_combine) return PKV_OK;
 
   pkv::CombineArgs c;
   c.seq_lens = seq_lens;
@@ -241,11 +244,10 @@ pkv_status kv_append(const pkv_pool* pool, int layer, const float* k_new, const 
                      int num_rows, void* stream) {
   pkv_status s = check_pool_layer(pool, layer);
   if (s) return s;
-  if ((s = check_rows(num_rows, bt_stride, block_table, seq_lens))) return s;
+  if ((s = check_rows(num_rows, bt_stride, block_table, seq_lens, 1 << 24))) return s;
   if (num_rows > 0 && (!k_new || !v_new)) return fail(PKV_ERR_INVALID_ARG, "null k_new or v_new");
   if (!aligned(k_new, 16) || !aligned(v_new, 16))
     return fail(PKV_ERR_INVALID_ARG, "k_new / v_new not 16-byte aligned");
-  if (num_rows > 65535) return fail(PKV_ERR_UNSUPPORTED, "more than 65535 rows");
   if (num_rows == 0) return PKV_OK;
   pkv::AppendArgs a;
   a.k_data = pool->k_data + layer * pool->layer_data_bytes;
@@ -290,7 +292,16 @@ pkv_status paged_decode_attention(const pkv_pool* pool, int layer, const float* 
                                   float scale, float* out, void* workspace,
                                   size_t workspace_bytes, int num_chunks, void* stream) {
   return attention_impl(pool, layer, q, block_table, bt_stride, seq_lens, num_rows, n_q_heads,
-                        scale, out, workspace, workspace_bytes, num_chunks, stream);
+                        scale, out, workspace, workspace_bytes, num_chunks, stream, true);
+}
+
+pkv_status paged_decode_split(const pkv_pool* pool, int layer, const float* q,
+                              const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                              int num_rows, int n_q_heads, float scale, float* out,
+                              void* workspace, size_t workspace_bytes, int num_chunks,
+                              void* stream) {
+  return attention_impl(pool, layer, q, block_table, bt_stride, seq_lens, num_rows, n_q_heads,
+                        scale, out, workspace, workspace_bytes, num_chunks, stream, false);
 }
 
 pkv_status paged_decode_plan(const int32_t* seq_lens, int num_rows, int n_kv_heads,
@@ -362,7 +373,7 @@ pkv_status pkv_decode_step(const pkv_pool* pool, int layer, const float* q, cons
                      stream)))
     return s;
   return attention_impl(pool, layer, q, block_table, bt_stride, seq_lens, num_rows, n_q_heads,
-                        scale, out, workspace, workspace_bytes, num_chunks, stream);
+                        scale, out, workspace, workspace_bytes, num_chunks, stream, true);
 }
 
 const char* pkv_status_string(pkv_status s) {

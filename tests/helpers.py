@@ -60,3 +60,57 @@ def stored_values_dense(dtype, data, scales):
 
 def max_abs_err(a, b):
     return float(np.max(np.abs(np.asarray(a, np.float64) - np.asarray(b, np.float64))))
+
+
+# ------------------------------------------------------------- device side ----
+def device_pool(wl: W.Workload, host_pool, num_layers: int = 1, layer: int = 0):
+    """A library KVPool on cuda:0 holding the host pool arrays in `layer`
+    (other layers are filled with f16 NaN / NaN scales)."""
+    import torch
+    from paged_kv_decode_09_gb300 import api
+    cfg = wl.cfg
+    pool = api.KVPool(num_layers, wl.num_pages, cfg.n_kv_heads, cfg.dtype, device="cuda")
+    kd, vd, ks, vs = host_pool
+    if cfg.dtype == W.F16:
+        for t in (pool.k_data, pool.v_data):
+            t.view(torch.int16).fill_(0x7E00)
+        pool.k_data[layer].copy_(torch.from_numpy(kd.view(np.float16)))
+        pool.v_data[layer].copy_(torch.from_numpy(vd.view(np.float16)))
+    else:
+        for t in (pool.k_scales, pool.v_scales):
+            t.view(torch.int16).fill_(0x7E00)
+        pool.k_data.fill_(127)
+        pool.v_data.fill_(127)
+        pool.k_data[layer].copy_(torch.from_numpy(kd))
+        pool.v_data[layer].copy_(torch.from_numpy(vd))
+        pool.k_scales[layer].copy_(torch.from_numpy(ks.view(np.float16)))
+        pool.v_scales[layer].copy_(torch.from_numpy(vs.view(np.float16)))
+    return pool
+
+
+def host_arrays(pool, layer: int = 0):
+    """(k_data, v_data, k_scales, v_scales) numpy copies of one layer of a device pool."""
+    import torch
+    if pool.dtype == W.F16:
+        return (pool.k_data[layer].cpu().view(torch.int16).numpy().view(np.uint16),
+                pool.v_data[layer].cpu().view(torch.int16).numpy().view(np.uint16), None, None)
+    return (pool.k_data[layer].cpu().numpy(), pool.v_data[layer].cpu().numpy(),
+            pool.k_scales[layer].cpu().view(torch.int16).numpy().view(np.uint16),
+            pool.v_scales[layer].cpu().view(torch.int16).numpy().view(np.uint16))
+
+
+def to_dev(a, dtype=None):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    return t if dtype is None else t.to(dtype)
+
+
+# Tolerances of the attention parity tests: the stated bound (2e-3 max abs
+# against the FP64 oracle) and a tighter internal one.  fp32 accumulation over
+# a few thousand tokens with O(1) logits errs by ~1e-6; 1e-4 leaves margin
+# while still failing on a single dropped or misplaced token of a short row.
+ATOL_STATED = 2e-3
+
+
+def tight_tol(ref):
+    return 1e-4 * max(1.0, float(np.max(np.abs(ref))))

@@ -1,0 +1,84 @@
+"""The C ABI without a GPU: libpkv.so builds and loads, exports every function
+include/pkv.h declares, and rejects bad arguments on the host before any CUDA
+call (so these calls are safe on a machine without a device)."""
+import ctypes
+import os
+import re
+import shutil
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_decode_09_gb300 import api, build
+    if not os.path.exists(build.LIB):
+        if not (shutil.which("nvcc") or os.path.exists("/usr/local/cuda/bin/nvcc")):
+            pytest.skip("no nvcc to build libpkv.so")
+        build.build()
+    else:
+        build.build()  # rebuilds only if a source is newer
+    return api.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)) -
+                  {"if", "sizeof", "defined"})
+
+
+def test_every_declared_function_is_exported(lib):
+    names = _declared()
+    assert {"kv_pool_create", "kv_append", "paged_decode_attention"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in pkv.h but not exported"
+
+
+def test_pool_bytes(lib):
+    # f16: 2 bytes per element; q8_0: 1 byte per element + 2 bytes per 32-element block
+    assert lib.kv_pool_bytes(2, 10, 8, 128, 0, 0) == 2 * 10 * 8 * 16 * 128 * 2
+    assert lib.kv_pool_bytes(2, 10, 8, 128, 0, 1) == 0
+    assert lib.kv_pool_bytes(2, 10, 8, 128, 1, 0) == 2 * 10 * 8 * 16 * 128
+    assert lib.kv_pool_bytes(2, 10, 8, 128, 1, 1) == 2 * 10 * 8 * 16 * 4 * 2
+    assert lib.kv_pool_bytes(0, 10, 8, 128, 0, 0) == 0
+
+
+def test_workspace_bytes(lib):
+    chunks, rows, n_q, n_kv = 456, 8, 32, 8
+    slots, G = chunks + rows * n_kv, n_q // n_kv
+    ml = (slots * G * 2 * 4 + 255) // 256 * 256
+    acc = (slots * G * 128 * 4 + 255) // 256 * 256
+    assert lib.paged_decode_workspace_bytes(rows, n_q, n_kv, 128, chunks) == ml + acc
+    assert lib.paged_decode_workspace_bytes(rows, 30, 8, 128, chunks) == 0   # 30 % 8 != 0
+    assert lib.paged_decode_workspace_bytes(rows, 32, 8, 64, chunks) == 0    # head_dim 64
+
+
+def test_host_validation_without_device(lib):
+    from paged_kv_decode_09_gb300 import api
+    h = ctypes.c_void_p()
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: validation fails first
+    st = lib.kv_pool_create(ctypes.byref(h), 1, 4, 8, 128, 0, None, fake, None, None, None)
+    assert st == 1 and b"null" in lib.pkv_last_error_message()
+    st = lib.kv_pool_create(ctypes.byref(h), 1, 4, 8, 64, 0, fake, fake, None, None, None)
+    assert st == 2
+    st = lib.kv_pool_create(ctypes.byref(h), 1, 4, 8, 128, 1, fake, fake, None, None, None)
+    assert st == 1  # q8_0 needs scales
+    st = lib.kv_pool_create(ctypes.byref(h), 1, 4, 8, 128, 0, ctypes.c_void_p(3), fake, None,
+                            None, None)
+    assert st == 1  # misaligned
+    # a descriptor over fake pointers: creating it touches no device memory
+    assert lib.kv_pool_create(ctypes.byref(h), 2, 4, 8, 128, 0, fake, fake, None, None, None) == 0
+    bt = ctypes.c_void_p(1 << 21)
+    assert lib.kv_append(h, 2, fake, fake, bt, 1, bt, 1, None) == 1          # layer out of range
+    assert lib.kv_append(h, 0, ctypes.c_void_p(4), fake, bt, 1, bt, 1, None) == 1  # misaligned
+    assert lib.paged_decode_attention(h, 0, fake, bt, 1, bt, 1, 24, 0.1, fake, fake, 1 << 20,
+                                      4, None) == 2                          # group 3
+    assert lib.paged_decode_attention(h, 0, fake, bt, 1, bt, 4, 16, 0.1, fake, fake, 256,
+                                      4, None) == 4                          # workspace too small
+    assert lib.paged_decode_attention(h, 0, fake, bt, 1, bt, 5000, 16, 0.1, fake, fake, 256,
+                                      4, None) == 2                          # too many rows
+    lib.kv_pool_destroy(h)
+    assert api.status_string(4) == "PKV_ERR_WORKSPACE"

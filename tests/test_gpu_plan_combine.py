@@ -1,0 +1,82 @@
+"""The plan and combine steps on the GPU against the oracle.
+
+Plan: bit-exact row page offsets and per-segment chunk ranges.
+Combine: the GPU merge of partial states that the ORACLE computed (base 2:
+m2 = max log2(e) scale <q, K_t>, l = sum 2^(s2_t - m2), acc = sum 2^(..) V_t)
+against the oracle's merge of the same fp32 partials."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from helpers import encode_pool, to_dev
+from paged_kv_decode_09_gb300 import api
+from paged_kv_decode_09_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_plan_bit_exact(seed):
+    rng = np.random.default_rng(seed)
+    rows = int(rng.integers(1, 300))
+    lens = rng.integers(0, 5000, rows).astype(np.int32)
+    lens[rng.integers(0, rows, 3)] = 0
+    n_kv = int(rng.choice([1, 2, 8]))
+    stride = int((lens.max() + 15) // 16) + 1
+    for chunks in (1, 5, 152, 456, 100000):
+        rps, first, last = api.paged_decode_plan(to_dev(lens), n_kv, stride, chunks)
+        o_rps, o_first, o_last, _ = O.plan(lens, n_kv, chunks)
+        np.testing.assert_array_equal(rps.cpu().numpy(), o_rps)
+        np.testing.assert_array_equal(first.cpu().numpy(), o_first)
+        np.testing.assert_array_equal(last.cpu().numpy(), o_last)
+
+
+def test_combine_of_oracle_partials():
+    wl = W.draw("tiny", lengths=[100, 37, 1, 64])
+    cfg = wl.cfg
+    G = cfg.group
+    host = encode_pool(wl)
+    chunks = 9
+    rps, first, last, T = O.plan(wl.seq_lens, cfg.n_kv_heads, chunks)
+    slots = chunks + wl.rows * cfg.n_kv_heads
+    part_ml = np.zeros((slots, G, 2), np.float32)
+    part_acc = np.zeros((slots, G, 128), np.float32)
+    want = np.zeros((wl.rows, cfg.n_q_heads, 128))
+    merged = np.zeros(wl.rows * cfg.n_kv_heads, bool)
+    for i in range(wl.rows):
+        npg = rps[i + 1] - rps[i]
+        for h in range(cfg.n_kv_heads):
+            j = i * cfg.n_kv_heads + h
+            if first[j] == last[j]:
+                continue  # one piece: not the combine's business
+            merged[j] = True
+            seg0 = cfg.n_kv_heads * rps[i] + h * npg
+            for k in range(first[j], last[j] + 1):
+                a = max(k * T // chunks, seg0) - seg0
+                b = min((k + 1) * T // chunks, seg0 + npg) - seg0
+                t0, t1 = a * 16, min(b * 16, int(wl.seq_lens[i]))
+                for g in range(G):
+                    m2, l, acc = O.attention_partial(cfg.dtype, wl.q[i], *host, wl.block_table,
+                                                     wl.num_pages, cfg.n_kv_heads, i, h * G + g,
+                                                     wl.scale, t0, t1)
+                    part_ml[k + j, g] = (m2, l)
+                    part_acc[k + j, g] = acc
+            for g in range(G):
+                s = [k + j for k in range(first[j], last[j] + 1)]
+                want[i, h * G + g] = O.combine(part_ml[s, g, 0], part_ml[s, g, 1], part_acc[s, g])
+    assert merged.sum() >= 8
+    nbytes = api.workspace_bytes(wl.rows, cfg.n_q_heads, cfg.n_kv_heads, chunks)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    ml_bytes = (slots * G * 2 * 4 + 255) // 256 * 256
+    ws[:part_ml.nbytes] = torch.from_numpy(part_ml.view(np.uint8).reshape(-1)).cuda()
+    ws[ml_bytes:ml_bytes + part_acc.nbytes] = torch.from_numpy(
+        part_acc.view(np.uint8).reshape(-1)).cuda()
+    out = torch.full((wl.rows, cfg.n_q_heads, 128), 7.0, device="cuda")
+    api.paged_decode_combine(to_dev(wl.seq_lens), cfg.n_q_heads, cfg.n_kv_heads, wl.bt_stride,
+                             chunks, ws, out)
+    got = out.cpu().numpy().reshape(wl.rows, cfg.n_kv_heads, G, 128)
+    w = want.reshape(wl.rows, cfg.n_kv_heads, G, 128)
+    m = merged.reshape(wl.rows, cfg.n_kv_heads)
+    np.testing.assert_allclose(got[m], w[m], rtol=0, atol=1e-6)
+    assert np.all(got[~m] == 7.0)  # untouched where one piece holds the segment
