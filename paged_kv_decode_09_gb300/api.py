@@ -125,6 +125,8 @@ class KVPool:
         self.num_layers, self.num_pages, self.n_kv = num_layers, num_pages, n_kv_heads
         self.dtype, self.head_dim = dtype, head_dim
         self.device = torch.device(device)
+        if self.device.index is None:
+            self.device = torch.device(self.device.type, torch.cuda.current_device())
         shape = (num_layers, num_pages, n_kv_heads, PAGE, head_dim)
         sshape = (num_layers, num_pages, n_kv_heads, PAGE, head_dim // Q8_BLOCK)
         if tensors is None:
