@@ -545,12 +545,20 @@ __global__ void __launch_bounds__(kD) combine_kernel(const CombineArgs a) {
   const long long s0 = static_cast<long long>(a.n_kv) * row_start[i] + static_cast<long long>(h) * npg;
   const int k0 = chunk_of(s0, T, a.num_chunks), k1 = chunk_of(s0 + npg - 1, T, a.num_chunks);
   if (k0 == k1) return;  // one piece: the attention kernel wrote the output
+  // Chunks between k0 and k1 may be empty (more chunks than units): they hold
+  // no piece, and their slots were never written.
+  auto empty = [&](int kk) {
+    return static_cast<long long>(kk) * T / a.num_chunks ==
+           static_cast<long long>(kk + 1) * T / a.num_chunks;
+  };
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     float M = -INFINITY;
-    for (int kk = k0; kk <= k1; ++kk) M = fmaxf(M, a.part_ml[((kk + static_cast<long long>(j)) * G + g) * 2]);
+    for (int kk = k0; kk <= k1; ++kk)
+      if (!empty(kk)) M = fmaxf(M, a.part_ml[((kk + static_cast<long long>(j)) * G + g) * 2]);
     float Ls = 0.f, A = 0.f;
     for (int kk = k0; kk <= k1; ++kk) {
+      if (empty(kk)) continue;
       const long long slot = kk + static_cast<long long>(j);
       const float f = exp2f(a.part_ml[(slot * G + g) * 2] - M);
       Ls = fmaf(f, a.part_ml[(slot * G + g) * 2 + 1], Ls);

@@ -32,16 +32,18 @@ def test_plan_bit_exact(seed):
         np.testing.assert_array_equal(last.cpu().numpy(), o_last)
 
 
-def test_combine_of_oracle_partials():
+@pytest.mark.parametrize("chunks", [9, 200])
+def test_combine_of_oracle_partials(chunks):
+    """chunks = 200 > 88 units: most chunks are empty, and the slots they
+    would own hold garbage that the merge must not read."""
     wl = W.draw("tiny", lengths=[100, 37, 1, 64])
     cfg = wl.cfg
     G = cfg.group
     host = encode_pool(wl)
-    chunks = 9
     rps, first, last, T = O.plan(wl.seq_lens, cfg.n_kv_heads, chunks)
     slots = chunks + wl.rows * cfg.n_kv_heads
-    part_ml = np.zeros((slots, G, 2), np.float32)
-    part_acc = np.zeros((slots, G, 128), np.float32)
+    part_ml = np.full((slots, G, 2), 1e30, np.float32)    # garbage in unwritten slots
+    part_acc = np.full((slots, G, 128), np.nan, np.float32)
     want = np.zeros((wl.rows, cfg.n_q_heads, 128))
     merged = np.zeros(wl.rows * cfg.n_kv_heads, bool)
     for i in range(wl.rows):
@@ -52,9 +54,13 @@ def test_combine_of_oracle_partials():
                 continue  # one piece: not the combine's business
             merged[j] = True
             seg0 = cfg.n_kv_heads * rps[i] + h * npg
+            pieces = []
             for k in range(first[j], last[j] + 1):
                 a = max(k * T // chunks, seg0) - seg0
                 b = min((k + 1) * T // chunks, seg0 + npg) - seg0
+                if a >= b:
+                    continue  # an empty chunk: no piece
+                pieces.append(k + j)
                 t0, t1 = a * 16, min(b * 16, int(wl.seq_lens[i]))
                 for g in range(G):
                     m2, l, acc = O.attention_partial(cfg.dtype, wl.q[i], *host, wl.block_table,
@@ -63,7 +69,7 @@ def test_combine_of_oracle_partials():
                     part_ml[k + j, g] = (m2, l)
                     part_acc[k + j, g] = acc
             for g in range(G):
-                s = [k + j for k in range(first[j], last[j] + 1)]
+                s = pieces
                 want[i, h * G + g] = O.combine(part_ml[s, g, 0], part_ml[s, g, 1], part_acc[s, g])
     assert merged.sum() >= 8
     nbytes = api.workspace_bytes(wl.rows, cfg.n_q_heads, cfg.n_kv_heads, chunks)
