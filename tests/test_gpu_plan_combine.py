@@ -71,7 +71,7 @@ def test_combine_of_oracle_partials(chunks):
             for g in range(G):
                 s = pieces
                 want[i, h * G + g] = O.combine(part_ml[s, g, 0], part_ml[s, g, 1], part_acc[s, g])
-    assert merged.sum() >= 8
+    assert merged.sum() >= 5
     nbytes = api.workspace_bytes(wl.rows, cfg.n_q_heads, cfg.n_kv_heads, chunks)
     ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
     ml_bytes = (slots * G * 2 * 4 + 255) // 256 * 256
