@@ -348,8 +348,9 @@ void oracle_combine(int n, const float *m2, const float *l, const float *acc, in
  * ceil(L_i / 16) pages (L_i <= 0 gives 0).  Units are numbered in the order
  * (row, KV head, page): segment j = i * n_kv + h holds the npg_i units of
  * (row i, head h) starting at seg_start(j) = n_kv * sum_{r<i} npg_r + h * npg_i.
- * With T = n_kv * sum_i npg_i units and C chunks, chunk k covers units
- * [floor(k T / C), floor((k + 1) T / C)).  A segment's pieces are its
+ * With T = n_kv * sum_i npg_i units and C chunks requested, Ce = min(C, T)
+ * chunks are used (so none is empty) and chunk k < Ce covers units
+ * [floor(k T / Ce), floor((k + 1) T / Ce)).  A segment's pieces are its
  * intersections with the chunks; first/last chunk record which chunks they
  * are (-1, -1 for an empty segment).
  *
@@ -372,8 +373,9 @@ int oracle_plan(int num_rows, const int32_t *seq_lens, int n_kv, int num_chunks,
             int64_t j = (int64_t)i * n_kv + h;
             int64_t a = (int64_t)n_kv * row_page_start[i] + h * npg, b = a + npg;
             int32_t first = -1, last = -1;
-            for (int64_t k = 0; k < num_chunks; ++k) {
-                int64_t c0 = k * T / num_chunks, c1 = (k + 1) * T / num_chunks;
+            const int64_t Ce = T < num_chunks ? T : num_chunks;
+            for (int64_t k = 0; k < Ce; ++k) {
+                int64_t c0 = k * T / Ce, c1 = (k + 1) * T / Ce;
                 if (a < b && c0 < c1 && c0 < b && a < c1) { /* non-empty overlap */
                     if (first < 0) first = (int32_t)k;
                     last = (int32_t)k;

@@ -1,7 +1,8 @@
 """Pins for the oracle's work split (plan) and its kv_append.
 
-Plan: units are (row, KV head, page) tiles in that order; C chunks cover
-[floor(k T / C), floor((k + 1) T / C)); a segment (row, head) is split into
+Plan: units are (row, KV head, page) tiles in that order; of C chunks asked
+for, Ce = min(C, T) are used, chunk k covering [floor(k T / Ce),
+floor((k + 1) T / Ce)), so none is empty; a segment (row, head) is split into
 pieces by the chunks it meets.  Pinned to hand-derived fixtures and to a
 brute-force enumeration of every unit.
 
@@ -44,9 +45,12 @@ def _enumerate(seq_lens, n_kv, C):
             for p in range(npg):
                 units.append(i * n_kv + h)
     T = len(units)
+    Ce = min(C, T)
     chunk_of = []
-    for k in range(C):
-        chunk_of += [k] * ((k + 1) * T // C - k * T // C)
+    for k in range(Ce):
+        n = (k + 1) * T // Ce - k * T // Ce
+        assert n >= 1  # no empty chunk
+        chunk_of += [k] * n
     J = len(seq_lens) * n_kv
     first, last = [-1] * J, [-1] * J
     for x, j in enumerate(units):
