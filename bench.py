@@ -1,17 +1,18 @@
 #!/usr/bin/env python3
 """Benchmark one decode step of paged-KV attention on GB300.
 
-A step is one pass of the whole hot path over one batch: kv_append of each
-row's new token, then paged decode attention (split-KV kernel + merge) over
-lengths that include it, for one layer's pool.  Default workload: the 8B layer
+A step is one pass of the whole hot path over one batch for one layer's pool:
+pkv_decode_step, which stores each row's new token (kv_append's encoding) and
+runs split-KV paged decode attention with its in-kernel merge over lengths
+that include the token -- one kernel launch.  Default workload: the 8B layer
 shape with f16 KV (8 rows, L ~ U[1024, 8192], 32 q / 8 KV heads, head_dim 128).
 Steps rotate over several layer pools whose total size is more than 4x the
 L2 cache, so every step reads KV from HBM.
 
 Metric (bytes counted per step: K and V of every attended token, q, out):
   value      KV GB/s, device-resident inputs, CUDA events on the stream
-  roofline   the split-KV kernel's algorithmic GB/s over its own mean event time,
-             against the measured HBM copy bandwidth
+  roofline   the decode kernel's algorithmic GB/s over the mean of its per-launch
+             event times, against the measured HBM copy bandwidth
   e2e        the same metric through the C ABI with the step's inputs copied
              from pinned host memory and the output copied back, every step
   cpu_baseline  the FP64 CPU oracle on a bounded sample of the same batch
@@ -233,15 +234,12 @@ def run_ours(args, rank, world, local):
             raise api.PkvError(st, what, L.pkv_last_error_message().decode())
 
     def step(layer, ev=None):
-        chk(L.kv_append(H, layer, a_k, a_v, a_bt, S, a_sl, R, sp), "kv_append")
         if ev is not None:
             ev[0].record(stream)
-        chk(L.paged_decode_split(H, layer, a_q, a_bt, S, a_sl, R, NQ, scale, a_out, a_ws,
-                                 ws.nbytes, CH, sp), "paged_decode_split")
+        chk(L.pkv_decode_step(H, layer, a_q, a_k, a_v, a_bt, S, a_sl, R, NQ, scale, a_out, a_ws,
+                              ws.nbytes, CH, sp), "pkv_decode_step")
         if ev is not None:
             ev[1].record(stream)
-        chk(L.paged_decode_combine(a_sl, R, NQ, cfg.n_kv_heads, 128, S, CH, a_ws, ws.nbytes,
-                                   a_out, sp), "paged_decode_combine")
 
     for w in range(args.warmup):
         step(w % layers)
@@ -337,7 +335,7 @@ def run_ours(args, rank, world, local):
         "e2e": {"value": round(world * nbytes / (e2e_ms / 1e3 / Ke) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
                 "ms_per_step": round(e2e_ms / Ke, 6)},
-        "gpu_launches": 3 * K,
+        "gpu_launches": K,
         "clocks": clock_info,
     }
     if rank == 0 and not args.no_cpu_baseline:

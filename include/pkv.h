@@ -137,12 +137,16 @@ pkv_status paged_decode_default_chunks(const pkv_pool *pool, int n_q_heads, int 
                                        int *chunks);
 
 /* Workspace bytes paged_decode_attention needs for up to max_rows rows with
- * num_chunks chunks.  Layout (256-byte aligned parts), with
- * S = num_chunks + num_rows * n_kv_heads partial slots and G = n_q/n_kv:
+ * num_chunks chunks.  Layout for a call of num_rows rows, in parts that each
+ * start on a 256-byte boundary, with S = num_chunks + num_rows * n_kv_heads
+ * partial slots and G = n_q / n_kv:
+ *     counters int32 [num_rows * n_kv_heads]  arrival count per (row, KV head)
  *     part_ml  float [S][G][2]  (m2, l) per slot and query head of the group
  *     part_acc float [S][G][head_dim]
- * part_acc starts at the first multiple of 256 bytes after part_ml.
- * Returns 0 for invalid sizes. */
+ * The workspace must be zero-filled once before its first use (the counters
+ * must start at 0); every call that completes leaves the counters at 0 again.
+ * After a call that reported PKV_DEV_TIMEOUT, zero it again.  Calls that
+ * share a workspace must not run concurrently.  Returns 0 for invalid sizes. */
 size_t paged_decode_workspace_bytes(int max_rows, int n_q_heads, int n_kv_heads, int head_dim,
                                     int num_chunks);
 
@@ -154,28 +158,28 @@ size_t paged_decode_workspace_bytes(int max_rows, int n_q_heads, int n_kv_heads,
  *   scale        softmax scale (1/sqrt(head_dim) for the usual attention)
  *   out          fp32 [num_rows][n_q_heads][128], 16-byte aligned
  *   workspace    device scratch of paged_decode_workspace_bytes(num_rows ...)
- *                bytes, 256-byte aligned; its contents need no initialisation
+ *                bytes, 256-byte aligned, zero-filled before its first use
  *   num_chunks   work chunks (0: paged_decode_default_chunks for num_rows)
- * The (row, KV head, page) tiles of the batch are split into num_chunks
- * equal contiguous chunks, one per CTA; a CTA streams its tiles through
- * shared memory, keeps a base-2 online softmax in fp32 for the G query heads
- * of the tile's KV head, and writes either the final output (when it holds a
- * whole (row, KV head)) or a partial state (m2, l, acc) to slot
- * chunk + row * n_kv_heads + head of the workspace; a second launch merges
- * the partials (paged_decode_combine).  Rows with seq_lens[i] == 0 get zeros.
- * Two launches, no host synchronisation. */
+ * The T (row, KV head, page) tiles of the batch are split into
+ * min(num_chunks, T) equal contiguous chunks, one per CTA; a CTA streams its
+ * tiles through shared memory, keeps a base-2 online softmax in fp32 for the
+ * G query heads of the tile's KV head, and writes either the final output
+ * (when it holds a whole (row, KV head)) or a partial state (m2, l, acc) to
+ * slot chunk + row * n_kv_heads + head of the workspace.  The last CTA to
+ * finish a piece of a split (row, KV head) merges all its pieces into the
+ * output.  Rows with seq_lens[i] == 0 get zeros.  One launch, no host
+ * synchronisation. */
 pkv_status paged_decode_attention(const pkv_pool *pool, int layer, const float *q,
                                   const int32_t *block_table, int bt_stride,
                                   const int32_t *seq_lens, int num_rows, int n_q_heads,
                                   float scale, float *out, void *workspace,
                                   size_t workspace_bytes, int num_chunks, void *stream);
 
-/* paged_decode_split — the first of the two launches of
- * paged_decode_attention alone (same arguments): every piece that holds a
- * whole (row, KV head) writes `out`, the others write their partial states to
- * the workspace.  paged_decode_combine with the same seq_lens, num_chunks and
- * workspace completes the call.  Exposed so that callers can time or
- * schedule the two launches separately.  One launch. */
+/* paged_decode_split — paged_decode_attention without the in-kernel merge
+ * (same arguments): every piece that holds a whole (row, KV head) writes
+ * `out`, the others leave their partial states in the workspace, and
+ * paged_decode_combine with the same seq_lens, num_chunks and workspace
+ * completes the call.  The counters are not used.  One launch. */
 pkv_status paged_decode_split(const pkv_pool *pool, int layer, const float *q,
                               const int32_t *block_table, int bt_stride, const int32_t *seq_lens,
                               int num_rows, int n_q_heads, float scale, float *out,
@@ -206,9 +210,12 @@ pkv_status paged_decode_combine(const int32_t *seq_lens, int num_rows, int n_q_h
                                 const void *workspace, size_t workspace_bytes, float *out,
                                 void *stream);
 
-/* pkv_decode_step — one decode step of one layer: kv_append of the new token
- * of every row, then paged_decode_attention over the lengths that include it.
- * Same arguments as the two calls; three launches in stream order. */
+/* pkv_decode_step — one decode step of one layer: the new K/V token of every
+ * row is stored as kv_append would store it, and attention runs over the
+ * lengths that include it (paged_decode_attention).  One launch: the CTA
+ * that reads a row's last page stores the new token there just before
+ * reading it.  A row's last page must not be shared with another row (full
+ * pages may be).  Same arguments as the two calls. */
 pkv_status pkv_decode_step(const pkv_pool *pool, int layer, const float *q, const float *k_new,
                            const float *v_new, const int32_t *block_table, int bt_stride,
                            const int32_t *seq_lens, int num_rows, int n_q_heads, float scale,

@@ -13,7 +13,7 @@ the library is missing, every call raises: there is no CPU fallback.
 """
 _API_NAMES = {
     "F16", "Q8_0", "PAGE", "PkvError", "KVPool", "kv_append", "paged_decode_attention",
-    "paged_decode_plan", "paged_decode_combine", "decode_step", "workspace_bytes",
+    "paged_decode_plan", "paged_decode_combine", "paged_decode_split", "decode_step", "workspace_bytes",
     "default_chunks", "status_string", "library_path", "Workspace",
 }
 

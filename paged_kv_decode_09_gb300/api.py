@@ -187,12 +187,13 @@ def workspace_bytes(max_rows: int, n_q_heads: int, n_kv_heads: int, num_chunks: 
 
 
 class Workspace:
-    """Device scratch for paged_decode_attention (partial states)."""
+    """Device scratch for paged_decode_attention: arrival counters and partial
+    states.  Zero-filled here, as the library requires before first use."""
 
     def __init__(self, pool: KVPool, n_q_heads: int, max_rows: int, num_chunks: int = 0):
         self.num_chunks = num_chunks or default_chunks(pool, n_q_heads, max_rows)
         self.nbytes = workspace_bytes(max_rows, n_q_heads, pool.n_kv, self.num_chunks)
-        self.tensor = torch.empty(max(self.nbytes, 256), dtype=torch.uint8, device=pool.device)
+        self.tensor = torch.zeros(max(self.nbytes, 256), dtype=torch.uint8, device=pool.device)
 
 
 def _rows(block_table, seq_lens, device):
@@ -235,7 +236,7 @@ def paged_decode_attention(pool: KVPool, layer: int, q, block_table, seq_lens, s
 
 def decode_step(pool: KVPool, layer: int, q, k_new, v_new, block_table, seq_lens, scale: float,
                 out=None, workspace: Workspace | None = None, num_chunks: int = 0, stream=None):
-    """kv_append then paged_decode_attention (pkv_decode_step)."""
+    """Append each row's new token, then attend (pkv_decode_step, one launch)."""
     rows, stride = _rows(block_table, seq_lens, pool.device)
     _need(q, torch.float32, "q", device=pool.device)
     shape = (rows, pool.n_kv, pool.head_dim)
@@ -252,6 +253,20 @@ def decode_step(pool: KVPool, layer: int, q, k_new, v_new, block_table, seq_lens
                                  _ptr(block_table), stride, _ptr(seq_lens), rows, n_q,
                                  float(scale), _ptr(out), _ptr(workspace.tensor),
                                  workspace.nbytes, chunks, _stream(stream)), "pkv_decode_step")
+    return out
+
+
+def paged_decode_split(pool: KVPool, layer: int, q, block_table, seq_lens, scale: float, out,
+                       workspace: Workspace, stream=None):
+    """The decode kernel without the in-kernel merge; partial states stay in
+    the workspace for paged_decode_combine."""
+    rows, stride = _rows(block_table, seq_lens, pool.device)
+    _need(q, torch.float32, "q", device=pool.device)
+    _need(out, torch.float32, "out", q.shape, pool.device)
+    _check(lib().paged_decode_split(pool.handle, layer, _ptr(q), _ptr(block_table), stride,
+                                    _ptr(seq_lens), rows, q.shape[1], float(scale), _ptr(out),
+                                    _ptr(workspace.tensor), workspace.nbytes,
+                                    workspace.num_chunks, _stream(stream)), "paged_decode_split")
     return out
 
 

@@ -92,7 +92,26 @@ long long partial_slots(int num_chunks, int num_rows, int n_kv) {
 size_t workspace_needed(int num_rows, int n_q, int n_kv, int num_chunks) {
   const long long slots = partial_slots(num_chunks, num_rows, n_kv);
   const int g = n_q / n_kv;
-  return pkv::part_ml_bytes(slots, g) + pkv::part_acc_bytes(slots, g);
+  return pkv::counter_bytes(static_cast<long long>(num_rows) * n_kv) +
+         pkv::part_ml_bytes(slots, g) + pkv::part_acc_bytes(slots, g);
+}
+
+// Workspace parts for a call: counters, part_ml, part_acc.
+struct WsParts {
+  int32_t* counters;
+  float* part_ml;
+  float* part_acc;
+};
+WsParts workspace_parts(void* ws, int num_rows, int n_q, int n_kv, int num_chunks) {
+  const long long slots = partial_slots(num_chunks, num_rows, n_kv);
+  uint8_t* p = static_cast<uint8_t*>(ws);
+  WsParts w;
+  w.counters = reinterpret_cast<int32_t*>(p);
+  p += pkv::counter_bytes(static_cast<long long>(num_rows) * n_kv);
+  w.part_ml = reinterpret_cast<float*>(p);
+  p += pkv::part_ml_bytes(slots, n_q / n_kv);
+  w.part_acc = reinterpret_cast<float*>(p);
+  return w;
 }
 
 pkv_status default_chunks(const pkv_pool* p, int n_q, int rows, int* chunks) {
@@ -108,11 +127,16 @@ pkv_status default_chunks(const pkv_pool* p, int n_q, int rows, int* chunks) {
   return PKV_OK;
 }
 
-pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q,
-                          const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
-                          int num_rows, int n_q, float scale, float* out, void* workspace,
-                          size_t workspace_bytes, int num_chunks, void* stream,
-                          bool run_combine) {
+enum class Mode { kMerged, kSplitOnly };
+
+// One launch of the decode kernel: kMerged merges split segments in-kernel
+// (arrival counters) and, given k_new/v_new, appends the new tokens first;
+// kSplitOnly leaves the partial states for paged_decode_combine.
+pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q, const float* k_new,
+                          const float* v_new, const int32_t* block_table, int bt_stride,
+                          const int32_t* seq_lens, int num_rows, int n_q, float scale, float* out,
+                          void* workspace, size_t workspace_bytes, int num_chunks, void* stream,
+                          Mode mode) {
   pkv_status s = check_pool_layer(pool, layer);
   if (s) return s;
   if ((s = check_geometry(n_q, pool->n_kv, pool->head_dim))) return s;
@@ -129,15 +153,14 @@ pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q,
   if (!aligned(workspace, 256)) return fail(PKV_ERR_INVALID_ARG, "workspace not 256-byte aligned");
 
   const int g = n_q / pool->n_kv;
-  const long long slots = partial_slots(num_chunks, num_rows, pool->n_kv);
-  float* part_ml = static_cast<float*>(workspace);
-  float* part_acc = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                             pkv::part_ml_bytes(slots, g));
+  const WsParts w = workspace_parts(workspace, num_rows, n_q, pool->n_kv, num_chunks);
   pkv::DecodeArgs a;
   a.k_data = pool->k_data + layer * pool->layer_data_bytes;
   a.v_data = pool->v_data + layer * pool->layer_data_bytes;
   a.k_scales = pool->k_scales ? pool->k_scales + layer * pool->layer_scale_bytes : nullptr;
   a.v_scales = pool->v_scales ? pool->v_scales + layer * pool->layer_scale_bytes : nullptr;
+  a.k_new = mode == Mode::kMerged ? k_new : nullptr;
+  a.v_new = mode == Mode::kMerged ? v_new : nullptr;
   a.num_pages = pool->num_pages;
   a.n_kv = pool->n_kv;
   a.q = q;
@@ -148,25 +171,12 @@ pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q,
   a.n_q = n_q;
   a.qscale = scale * 1.4426950408889634f;  // log2(e): base-2 softmax
   a.out = out;
-  a.part_ml = part_ml;
-  a.part_acc = part_acc;
+  a.part_ml = w.part_ml;
+  a.part_acc = w.part_acc;
+  a.counters = mode == Mode::kMerged ? w.counters : nullptr;
   a.status = pool->status;
   cudaError_t e = pkv::launch_paged_decode(pool->dtype, g, a, num_chunks, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged decode launch");
-  if (!run_combine) return PKV_OK;
-
-  pkv::CombineArgs c;
-  c.seq_lens = seq_lens;
-  c.num_rows = num_rows;
-  c.n_q = n_q;
-  c.n_kv = pool->n_kv;
-  c.bt_stride = bt_stride;
-  c.num_chunks = num_chunks;
-  c.part_ml = part_ml;
-  c.part_acc = part_acc;
-  c.out = out;
-  e = pkv::launch_combine(g, c, as_stream(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   return PKV_OK;
 }
 
@@ -291,8 +301,9 @@ pkv_status paged_decode_attention(const pkv_pool* pool, int layer, const float* 
                                   const int32_t* seq_lens, int num_rows, int n_q_heads,
                                   float scale, float* out, void* workspace,
                                   size_t workspace_bytes, int num_chunks, void* stream) {
-  return attention_impl(pool, layer, q, block_table, bt_stride, seq_lens, num_rows, n_q_heads,
-                        scale, out, workspace, workspace_bytes, num_chunks, stream, true);
+  return attention_impl(pool, layer, q, nullptr, nullptr, block_table, bt_stride, seq_lens,
+                        num_rows, n_q_heads, scale, out, workspace, workspace_bytes, num_chunks,
+                        stream, Mode::kMerged);
 }
 
 pkv_status paged_decode_split(const pkv_pool* pool, int layer, const float* q,
@@ -300,8 +311,9 @@ pkv_status paged_decode_split(const pkv_pool* pool, int layer, const float* q,
                               int num_rows, int n_q_heads, float scale, float* out,
                               void* workspace, size_t workspace_bytes, int num_chunks,
                               void* stream) {
-  return attention_impl(pool, layer, q, block_table, bt_stride, seq_lens, num_rows, n_q_heads,
-                        scale, out, workspace, workspace_bytes, num_chunks, stream, false);
+  return attention_impl(pool, layer, q, nullptr, nullptr, block_table, bt_stride, seq_lens,
+                        num_rows, n_q_heads, scale, out, workspace, workspace_bytes, num_chunks,
+                        stream, Mode::kSplitOnly);
 }
 
 pkv_status paged_decode_plan(const int32_t* seq_lens, int num_rows, int n_kv_heads,
@@ -335,7 +347,8 @@ pkv_status paged_decode_combine(const int32_t* seq_lens, int num_rows, int n_q_h
   if (!aligned(workspace, 256)) return fail(PKV_ERR_INVALID_ARG, "workspace not 256-byte aligned");
   if (num_rows == 0) return PKV_OK;
   const int g = n_q_heads / n_kv_heads;
-  const long long slots = partial_slots(num_chunks, num_rows, n_kv_heads);
+  const WsParts w =
+      workspace_parts(const_cast<void*>(workspace), num_rows, n_q_heads, n_kv_heads, num_chunks);
   pkv::CombineArgs c;
   c.seq_lens = seq_lens;
   c.num_rows = num_rows;
@@ -343,9 +356,8 @@ pkv_status paged_decode_combine(const int32_t* seq_lens, int num_rows, int n_q_h
   c.n_kv = n_kv_heads;
   c.bt_stride = bt_stride;
   c.num_chunks = num_chunks;
-  c.part_ml = static_cast<const float*>(workspace);
-  c.part_acc = reinterpret_cast<const float*>(static_cast<const uint8_t*>(workspace) +
-                                              pkv::part_ml_bytes(slots, g));
+  c.part_ml = w.part_ml;
+  c.part_acc = w.part_acc;
   c.out = out;
   cudaError_t e = pkv::launch_combine(g, c, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "combine launch");
@@ -357,23 +369,14 @@ pkv_status pkv_decode_step(const pkv_pool* pool, int layer, const float* q, cons
                            const int32_t* seq_lens, int num_rows, int n_q_heads, float scale,
                            float* out, void* workspace, size_t workspace_bytes, int num_chunks,
                            void* stream) {
-  // Validate the attention arguments before queueing the append, so that a
-  // failed call leaves the pool untouched.
-  pkv_status s = check_pool_layer(pool, layer);
-  if (s) return s;
-  if ((s = check_geometry(n_q_heads, pool->n_kv, pool->head_dim))) return s;
-  if (num_chunks == 0 && num_rows > 0 && num_rows <= PKV_MAX_ROWS &&
-      (s = default_chunks(pool, n_q_heads, num_rows, &num_chunks)))
-    return s;
-  if (num_rows > 0 && num_chunks > 0 &&
-      (!workspace || workspace_bytes < workspace_needed(num_rows, n_q_heads, pool->n_kv, num_chunks)))
-    return fail(PKV_ERR_WORKSPACE, "workspace too small");
-  if (num_rows > 0 && (!q || !out)) return fail(PKV_ERR_INVALID_ARG, "null q or out");
-  if ((s = kv_append(pool, layer, k_new, v_new, block_table, bt_stride, seq_lens, num_rows,
-                     stream)))
-    return s;
-  return attention_impl(pool, layer, q, block_table, bt_stride, seq_lens, num_rows, n_q_heads,
-                        scale, out, workspace, workspace_bytes, num_chunks, stream, true);
+  // One launch: the kernel stores each row's new token into its last page
+  // just before reading that page, then attends and merges.
+  if (num_rows > 0 && (!k_new || !v_new)) return fail(PKV_ERR_INVALID_ARG, "null k_new or v_new");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16))
+    return fail(PKV_ERR_INVALID_ARG, "k_new / v_new not 16-byte aligned");
+  return attention_impl(pool, layer, q, k_new, v_new, block_table, bt_stride, seq_lens, num_rows,
+                        n_q_heads, scale, out, workspace, workspace_bytes, num_chunks, stream,
+                        Mode::kMerged);
 }
 
 const char* pkv_status_string(pkv_status s) {

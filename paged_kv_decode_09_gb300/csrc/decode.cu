@@ -9,14 +9,22 @@
 // Here the pages are read in place.
 //
 // Work split.  The batch is a list of T = n_kv * sum_i ceil(L_i/16) units,
-// one per (row, KV head, page) in that order.  CTA k of C takes units
-// [floor(kT/C), floor((k+1)T/C)), so every CTA streams the same number of
+// one per (row, KV head, page) in that order.  With C = min(grid, T) chunks,
+// CTA k < C takes units [floor(kT/C), floor((k+1)T/C)) (never empty; CTAs
+// k >= C idle), so every CTA streams the same number of
 // 4 KiB (f16) or 2176-byte (q8_0) tiles whatever the length mix: one 40k-token
 // row and many 16-token rows keep all SMs equally busy.  The units of one
 // (row, head) that fall in one CTA form a "piece"; a piece that is the whole
 // segment writes the output, otherwise it writes a partial state to slot
 // k + (i * n_kv + h) (pieces in unit order increase k, j or both, so the slot
-// is unique), and the combine kernel merges them.
+// is unique).  A segment spanning chunks k0..k1 has k1 - k0 + 1 pieces.  In
+// the merging mode each piece then bumps the segment's arrival counter, and
+// the last to arrive merges all pieces into the output and resets the
+// counter; otherwise the combine kernel merges them in a second launch.
+//
+// Fused append: when new K/V are given, the producer stores each row's new
+// token into its last page (the same encoding as kv_append) just before it
+// bulk-copies that page, so attention sees it without a separate launch.
 //
 // Inside a CTA: warp 4 is the producer; its lane 0 streams the chunk's K and V
 // tiles into a ring of shared-memory stages with 1-D bulk async copies
@@ -310,6 +318,101 @@ __device__ __forceinline__ void process_unit(const uint8_t* st, int nvalid, int 
   __syncwarp();
 }
 
+// ---------------------------------------------------------------- merge ----
+// Merge the base-2 partial states of segment j held in slots k + j for the
+// chunks k0..k1 that meet it; one thread per dim d, all G heads:
+//   M = max_k m2_k,  out = sum_k 2^(m2_k - M) acc_k / sum_k 2^(m2_k - M) l_k.
+// Loads go through L2 (other CTAs wrote the slots in this launch) and are
+// issued in batches so the merge is not a chain of dependent misses.
+template <int G>
+__device__ __forceinline__ void merge_segment(const float* part_ml, const float* part_acc,
+                                              long long j, int k0, int k1, float* o, int d) {
+  constexpr int kBatch = 8;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float M = -INFINITY;
+    for (int kk = k0; kk <= k1; kk += kBatch) {
+      float m[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        m[u] = (kk + u <= k1) ? __ldcg(part_ml + ((kk + u + j) * G + g) * 2) : -INFINITY;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) M = fmaxf(M, m[u]);
+    }
+    float Ls = 0.f, A = 0.f;
+    for (int kk = k0; kk <= k1; kk += kBatch) {
+      float m[kBatch], l[kBatch], x[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const bool in = kk + u <= k1;
+        const long long slot = kk + u + j;
+        m[u] = in ? __ldcg(part_ml + (slot * G + g) * 2) : -INFINITY;
+        l[u] = in ? __ldcg(part_ml + (slot * G + g) * 2 + 1) : 0.f;
+        x[u] = in ? __ldcg(part_acc + (slot * G + g) * kD + d) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const float w = exp2f(m[u] - M);
+        Ls = fmaf(w, l[u], Ls);
+        A = fmaf(w, x[u], A);
+      }
+    }
+    o[g * kD + d] = A / Ls;
+  }
+}
+
+// Chunks actually used for T units when C are launched: min(C, T), so that
+// no chunk is empty.
+__device__ __forceinline__ int used_chunks(long long T, int C) {
+  return static_cast<int>(T < C ? T : C);
+}
+
+// ------------------------------------------------------------- append ----
+// The producer warp stores row i's new K and V token of KV head h into slot
+// (L - 1) % 16 of tile (page, h) before it bulk-copies that tile: 4 dims per
+// lane; q8_0 blocks of 32 dims span 8 lanes.  Same encoding as kv_append.
+template <int DT>
+__device__ __forceinline__ void append_in_producer(const DecodeArgs& a, int i, int h, int page,
+                                                   int slot, int lane) {
+  using TL = Tiles<DT>;
+  const size_t tile = static_cast<size_t>(page) * a.n_kv + h;
+  const long long src = (static_cast<long long>(i) * a.n_kv + h) * kD + lane * 4;
+#pragma unroll
+  for (int which = 0; which < 2; ++which) {
+    const float4 x = __ldg(reinterpret_cast<const float4*>((which ? a.v_new : a.k_new) + src));
+    uint8_t* data = which ? a.v_data : a.k_data;
+    if constexpr (DT == PKV_KV_F16) {
+      const __half2 lo = __floats2half2_rn(x.x, x.y), hi = __floats2half2_rn(x.z, x.w);
+      uint2 w;
+      w.x = *reinterpret_cast<const uint32_t*>(&lo);
+      w.y = *reinterpret_cast<const uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(data + tile * TL::kData + slot * (kD * 2) + lane * 8) = w;
+    } else {
+      float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+      const float dq = amax / 127.0f;
+      const float v[4] = {x.x, x.y, x.z, x.w};
+      uint32_t packed = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float c = dq != 0.0f ? fminf(fmaxf(roundf(v[e] / dq), -127.0f), 127.0f) : 0.0f;
+        packed |= (static_cast<uint32_t>(static_cast<int>(c)) & 0xffu) << (8 * e);
+      }
+      *reinterpret_cast<uint32_t*>(data + tile * TL::kData + slot * kD + lane * 4) = packed;
+      if ((lane & 7) == 0) {
+        uint8_t* sc = which ? a.v_scales : a.k_scales;
+        reinterpret_cast<__half*>(sc + tile * TL::kScale)[slot * (kD / kQBlock) + (lane >> 3)] =
+            __float2half_rn(dq);
+      }
+    }
+  }
+  // The tile is read next by the async proxy (bulk copy): order these generic
+  // writes before it.
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  __syncwarp();
+}
+
 // --------------------------------------------------------------- kernel ----
 template <int DT, int G>
 __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs a) {
@@ -317,11 +420,11 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs
   using SM = Smem<DT, G>;
   using GR = Group<G>;
   constexpr int NST = TL::kStages;
-  static_assert(NST % kConsumerWarps == 0, "stages are handed to consumer warps round-robin");
   extern __shared__ __align__(128) uint8_t smem[];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  volatile int* flags = reinterpret_cast<volatile int*>(smem + SM::kFlags);  // [0] abort [1] issued
+  // [0] abort, [1] copies issued, [2] this CTA merges the current segment
+  volatile int* flags = reinterpret_cast<volatile int*>(smem + SM::kFlags);
   int* row_start = reinterpret_cast<int*>(smem + SM::kRows);
   int* lens = row_start + a.num_rows + 1;
   const uint32_t full0 = smem_addr(smem + SM::kBar);
@@ -334,25 +437,30 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs
     }
     flags[0] = 0;
     flags[1] = 0;
+    flags[2] = 0;
     fence_mbar_init();
   }
   plan_rows(a.seq_lens, a.num_rows, a.bt_stride, blockIdx.x == 0 ? a.status : nullptr, lens,
             row_start);
 
   const long long T = static_cast<long long>(a.n_kv) * row_start[a.num_rows];
-  const int C = gridDim.x, k = blockIdx.x;
-  const long long c_begin = static_cast<long long>(k) * T / C;
-  const long long c_end = static_cast<long long>(k + 1) * T / C;
+  const int C = used_chunks(T, gridDim.x), k = blockIdx.x;
+  const long long c_begin = k < C ? static_cast<long long>(k) * T / C : T;
+  const long long c_end = k < C ? static_cast<long long>(k + 1) * T / C : T;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------- producer ----
     const uint32_t stage0 = smem_addr(smem);
     const uint64_t policy = policy_evict_first();
-    // (page, head) of unit base + lane, read through the block table.
-    auto fetch = [&](long long base, int& page, int& head) {
+    // Unit base + lane: its page, KV head and row, and whether it is the
+    // row's last page (where the new token goes); bad pages read page 0 and
+    // take no append.
+    auto fetch = [&](long long base, int& page, int& head, int& row, int& last) {
       const long long x = base + lane;
       page = 0;
       head = 0;
+      row = 0;
+      last = 0;
       if (x < c_end) {
         const int i = row_of(row_start, a.num_rows, a.n_kv, x);
         const int npg = row_start[i + 1] - row_start[i];
@@ -360,24 +468,31 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs
         head = off / npg;
         const int p = off - head * npg;
         int pg = __ldg(a.block_table + static_cast<long long>(i) * a.bt_stride + p);
+        last = (p == npg - 1) ? 1 : 0;
         if (pg < 0 || pg >= a.num_pages) {
           record_status(a.status, PKV_DEV_BAD_PAGE);
           pg = 0;
+          last = 0;
         }
         page = pg;
+        row = i;
       }
     };
-    int pg_cur, h_cur;
-    fetch(c_begin, pg_cur, h_cur);
+    int pg_cur, h_cur, r_cur, l_cur;
+    fetch(c_begin, pg_cur, h_cur, r_cur, l_cur);
     uint32_t it = 0;
     bool stop = false;
     for (long long base = c_begin; base < c_end && !stop; base += 32) {
-      int pg_nxt = 0, h_nxt = 0;
-      if (base + 32 < c_end) fetch(base + 32, pg_nxt, h_nxt);  // one batch ahead
+      int pg_nxt = 0, h_nxt = 0, r_nxt = 0, l_nxt = 0;
+      if (base + 32 < c_end) fetch(base + 32, pg_nxt, h_nxt, r_nxt, l_nxt);  // one batch ahead
       const int n = static_cast<int>(min(32LL, c_end - base));
       for (int kk = 0; kk < n; ++kk) {
         const int pg = __shfl_sync(kFull, pg_cur, kk);
         const int hh = __shfl_sync(kFull, h_cur, kk);
+        if (a.k_new != nullptr && __shfl_sync(kFull, l_cur, kk)) {
+          const int row = __shfl_sync(kFull, r_cur, kk);
+          append_in_producer<DT>(a, row, hh, pg, (lens[row] - 1) % kPage, lane);
+        }
         int ok = 1;
         if (lane == 0) {
           const int s = it % NST;
@@ -409,6 +524,8 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs
       }
       pg_cur = pg_nxt;
       h_cur = h_nxt;
+      r_cur = r_nxt;
+      l_cur = l_nxt;
     }
   } else {
     // ------------------------------------------------------- consumers ----
@@ -423,6 +540,14 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs
     bool aborted = false;
     WarpState<G> S;
 
+    // Rows without tokens attend to nothing: their output is zero.
+    if (k == 0) {
+      for (int i = 0; i < a.num_rows; ++i)
+        if (row_start[i + 1] == row_start[i])
+          for (int e = threadIdx.x; e < a.n_q * kD; e += kConsumerThreads)
+            a.out[static_cast<long long>(i) * a.n_q * kD + e] = 0.f;
+    }
+
     for (long long x = c_begin; x < c_end;) {
       const int i = row_of(row_start, a.num_rows, a.n_kv, x);
       const int npg = row_start[i + 1] - row_start[i];
@@ -432,7 +557,8 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs
       const long long seg_end = seg_start + npg;
       const long long b = min(seg_end, c_end);
       const int L = lens[i];
-      const bool whole = (x == seg_start) && (b == seg_end);
+      const long long j = static_cast<long long>(i) * a.n_kv + h;
+      const int k0 = chunk_of(seg_start, T, C), k1 = chunk_of(seg_end - 1, T, C);
 
       const float* qrow = a.q + (static_cast<long long>(i) * a.n_q + h * G) * kD;
 #pragma unroll
@@ -471,7 +597,9 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs
         if (lane == 0) mbar_arrive(empty0 + 8 * s);
       }
 
-      // ---- merge the four warps' states of this piece
+      // ---- merge the four warps' states of this piece.  Every consumer
+      // thread passes the same four barriers whatever happened, so that an
+      // abort can never leave a barrier short of threads.
       const float l_tot = head_sum<G>(S.l);
       if (head_writer) {
         mrg_ml[(warp * G + g_lane) * 2] = S.m;
@@ -482,9 +610,10 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs
         *reinterpret_cast<float4*>(mrg_acc + (warp * G + g) * kD + lane * 4) =
             make_float4(S.acc[g][0], S.acc[g][1], S.acc[g][2], S.acc[g][3]);
       named_barrier(1, kConsumerThreads);
+      const bool whole = (k0 == k1);
+      const int d = threadIdx.x;  // 0..127
       if (!aborted) {
-        const int d = threadIdx.x;  // 0..127
-        const long long slot = k + static_cast<long long>(i) * a.n_kv + h;
+        const long long slot = k + j;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           float M = -INFINITY;
@@ -508,6 +637,22 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs
           }
         }
       }
+      // Last piece of a split segment to finish merges it (counters mode).
+      __threadfence();
+      named_barrier(1, kConsumerThreads);
+      if (d == 0) {
+        int last = 0;
+        if (!whole && a.counters != nullptr && !aborted && !flags[0])
+          last = atomicAdd(a.counters + j, 1) == k1 - k0;
+        flags[2] = last;
+      }
+      named_barrier(1, kConsumerThreads);
+      if (flags[2]) {
+        __threadfence();
+        merge_segment<G>(a.part_ml, a.part_acc, j, k0, k1,
+                         a.out + (static_cast<long long>(i) * a.n_q + h * G) * kD, d);
+        if (d == 0) a.counters[j] = 0;  // ready for the next call
+      }
       named_barrier(1, kConsumerThreads);
       x = b;
     }
@@ -524,9 +669,9 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs
   }
 }
 
-// ---------------------------------------------------------------- merge ----
-// One CTA per (row, KV head) segment, one thread per dim.  Merges the
-// partial states of the pieces the plan gives the segment.
+// ------------------------------------------------------------ combine ----
+// One CTA per (row, KV head) segment, one thread per dim: merges the pieces
+// of segments split over several chunks; zeros for rows without tokens.
 template <int G>
 __global__ void __launch_bounds__(kD) combine_kernel(const CombineArgs a) {
   extern __shared__ int csm[];
@@ -542,30 +687,11 @@ __global__ void __launch_bounds__(kD) combine_kernel(const CombineArgs a) {
     return;
   }
   const long long T = static_cast<long long>(a.n_kv) * row_start[a.num_rows];
+  const int C = used_chunks(T, a.num_chunks);
   const long long s0 = static_cast<long long>(a.n_kv) * row_start[i] + static_cast<long long>(h) * npg;
-  const int k0 = chunk_of(s0, T, a.num_chunks), k1 = chunk_of(s0 + npg - 1, T, a.num_chunks);
+  const int k0 = chunk_of(s0, T, C), k1 = chunk_of(s0 + npg - 1, T, C);
   if (k0 == k1) return;  // one piece: the attention kernel wrote the output
-  // Chunks between k0 and k1 may be empty (more chunks than units): they hold
-  // no piece, and their slots were never written.
-  auto empty = [&](int kk) {
-    return static_cast<long long>(kk) * T / a.num_chunks ==
-           static_cast<long long>(kk + 1) * T / a.num_chunks;
-  };
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float M = -INFINITY;
-    for (int kk = k0; kk <= k1; ++kk)
-      if (!empty(kk)) M = fmaxf(M, a.part_ml[((kk + static_cast<long long>(j)) * G + g) * 2]);
-    float Ls = 0.f, A = 0.f;
-    for (int kk = k0; kk <= k1; ++kk) {
-      if (empty(kk)) continue;
-      const long long slot = kk + static_cast<long long>(j);
-      const float f = exp2f(a.part_ml[(slot * G + g) * 2] - M);
-      Ls = fmaf(f, a.part_ml[(slot * G + g) * 2 + 1], Ls);
-      A = fmaf(f, a.part_acc[(slot * G + g) * kD + d], A);
-    }
-    o[g * kD + d] = A / Ls;
-  }
+  merge_segment<G>(a.part_ml, a.part_acc, j, k0, k1, o, d);
 }
 
 // ----------------------------------------------------------------- plan ----
@@ -576,14 +702,15 @@ __global__ void __launch_bounds__(256) plan_kernel(const PlanArgs a) {
   plan_rows(a.seq_lens, a.num_rows, a.bt_stride, nullptr, lens, row_start);
   for (int r = threadIdx.x; r <= a.num_rows; r += blockDim.x) a.row_page_start[r] = row_start[r];
   const long long T = static_cast<long long>(a.n_kv) * row_start[a.num_rows];
+  const int C = used_chunks(T, a.num_chunks);
   for (int j = threadIdx.x; j < a.num_rows * a.n_kv; j += blockDim.x) {
     const int i = j / a.n_kv, h = j % a.n_kv;
     const int npg = row_start[i + 1] - row_start[i];
     int f = -1, l = -1;
     if (npg > 0) {
       const long long s0 = static_cast<long long>(a.n_kv) * row_start[i] + static_cast<long long>(h) * npg;
-      f = chunk_of(s0, T, a.num_chunks);
-      l = chunk_of(s0 + npg - 1, T, a.num_chunks);
+      f = chunk_of(s0, T, C);
+      l = chunk_of(s0 + npg - 1, T, C);
     }
     a.seg_first_chunk[j] = f;
     a.seg_last_chunk[j] = l;

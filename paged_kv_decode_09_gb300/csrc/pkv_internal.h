@@ -13,10 +13,12 @@ namespace pkv {
 // Arguments of the split-KV decode kernel.  Pool pointers already point at
 // the layer's arrays.
 struct DecodeArgs {
-  const uint8_t* k_data;
-  const uint8_t* v_data;
-  const uint8_t* k_scales;  // q8_0 only
-  const uint8_t* v_scales;  // q8_0 only
+  uint8_t* k_data;
+  uint8_t* v_data;
+  uint8_t* k_scales;  // q8_0 only
+  uint8_t* v_scales;  // q8_0 only
+  const float* k_new;  // non-null: append each row's new token first (fused step)
+  const float* v_new;
   int num_pages;
   int n_kv;
   const float* q;
@@ -29,6 +31,7 @@ struct DecodeArgs {
   float* out;
   float* part_ml;   // [slots][G][2]
   float* part_acc;  // [slots][G][128]
+  int32_t* counters;  // non-null: [rows * n_kv] arrival counters, merge in-kernel
   int32_t* status;  // optional device status word
 };
 
@@ -71,8 +74,12 @@ struct AppendArgs {
   int32_t* status;
 };
 
-// Workspace layout of the partial states (see paged_decode_workspace_bytes).
+// Workspace layout (see paged_decode_workspace_bytes): arrival counters,
+// then the partial states.
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+inline size_t counter_bytes(long long segments) {
+  return align256(static_cast<size_t>(segments) * sizeof(int32_t));
+}
 inline size_t part_ml_bytes(long long slots, int group) {
   return align256(static_cast<size_t>(slots) * group * 2 * sizeof(float));
 }

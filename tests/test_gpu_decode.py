@@ -151,3 +151,63 @@ def test_host_validation_errors():
     assert e.value.status == 4
     out = api.paged_decode_attention(pool, 0, q, bt, sl, 0.1, workspace=ws)
     assert out.shape == q.shape
+
+
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0])
+def test_fused_step_append_is_bit_exact(dtype):
+    """pkv_decode_step stores each row's token inside the attention kernel:
+    the pool afterwards must equal the oracle's append byte for byte."""
+    from helpers import host_arrays
+    wl = W.draw("skewed")
+    wl.cfg = W.Config(**{**wl.cfg.__dict__, "dtype": dtype})
+    host = encode_pool(wl, include_appended=False)
+    pool = device_pool(wl, host, num_layers=2, layer=1)
+    out = api.decode_step(pool, 1, to_dev(wl.q), to_dev(wl.k_new), to_dev(wl.v_new),
+                          to_dev(wl.block_table), to_dev(wl.seq_lens), wl.scale, num_chunks=333)
+    torch.cuda.synchronize()
+    assert pool.read_status() == 0
+    want = [None if a is None else a.copy() for a in host]
+    O.kv_append(dtype, wl.k_new, wl.v_new, wl.block_table, wl.seq_lens, wl.num_pages, *want)
+    for g, w in zip(host_arrays(pool, 1), want):
+        if w is not None:
+            np.testing.assert_array_equal(g, w)
+    rows = np.arange(0, wl.rows, 7)
+    ref = O.decode_attention(dtype, wl.q[rows], *want, wl.block_table[rows], wl.seq_lens[rows],
+                             wl.num_pages, wl.cfg.n_kv_heads, wl.scale)
+    _check(out.cpu().numpy()[rows], ref)
+
+
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0])
+def test_split_then_combine_equals_merged(dtype):
+    wl = W.draw("llama8b_f16")
+    wl.cfg = W.Config(**{**wl.cfg.__dict__, "dtype": dtype})
+    host = encode_pool(wl)
+    pool = device_pool(wl, host)
+    q, bt, sl = to_dev(wl.q), to_dev(wl.block_table), to_dev(wl.seq_lens)
+    merged = api.paged_decode_attention(pool, 0, q, bt, sl, wl.scale).cpu().numpy()
+    ws = api.Workspace(pool, wl.cfg.n_q_heads, wl.rows)
+    out = torch.full_like(q, float("nan"))
+    api.paged_decode_split(pool, 0, q, bt, sl, wl.scale, out, ws)
+    api.paged_decode_combine(sl, wl.cfg.n_q_heads, wl.cfg.n_kv_heads, wl.bt_stride,
+                             ws.num_chunks, ws.tensor, out)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(out.cpu().numpy(), merged)
+    _check(merged, oracle_decode(wl, host))
+
+
+def test_workspace_reuse_across_calls_and_shapes():
+    """The arrival counters return to zero after every call: one workspace
+    serves many calls, with different batches and chunk splits."""
+    wl = W.draw("qwen3_0p6b_layer")
+    host = encode_pool(wl)
+    pool = device_pool(wl, host)
+    ws = api.Workspace(pool, wl.cfg.n_q_heads, wl.rows, 97)
+    ref = oracle_decode(wl, host)
+    q, bt, sl = to_dev(wl.q), to_dev(wl.block_table), to_dev(wl.seq_lens)
+    for rep in range(3):
+        out = api.paged_decode_attention(pool, 0, q, bt, sl, wl.scale, workspace=ws)
+        _check(out.cpu().numpy(), ref)
+        sub = api.paged_decode_attention(pool, 0, q[:3].contiguous(), bt[:3].contiguous(),
+                                         sl[:3].contiguous(), wl.scale, workspace=ws)
+        _check(sub.cpu().numpy(), ref[:3])
+    assert int(ws.tensor[:wl.rows * wl.cfg.n_kv_heads * 4].view(torch.int32).abs().sum()) == 0

@@ -74,9 +74,13 @@ def test_combine_of_oracle_partials(chunks):
     assert merged.sum() >= 5
     nbytes = api.workspace_bytes(wl.rows, cfg.n_q_heads, cfg.n_kv_heads, chunks)
     ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
-    ml_bytes = (slots * G * 2 * 4 + 255) // 256 * 256
-    ws[:part_ml.nbytes] = torch.from_numpy(part_ml.view(np.uint8).reshape(-1)).cuda()
-    ws[ml_bytes:ml_bytes + part_acc.nbytes] = torch.from_numpy(
+    # layout: counters [rows * n_kv] int32, part_ml, part_acc; each part 256-byte aligned
+    up = lambda n: (n + 255) // 256 * 256  # noqa: E731
+    ml_at = up(wl.rows * cfg.n_kv_heads * 4)
+    acc_at = ml_at + up(slots * G * 2 * 4)
+    assert acc_at + up(part_acc.nbytes) == nbytes
+    ws[ml_at:ml_at + part_ml.nbytes] = torch.from_numpy(part_ml.view(np.uint8).reshape(-1)).cuda()
+    ws[acc_at:acc_at + part_acc.nbytes] = torch.from_numpy(
         part_acc.view(np.uint8).reshape(-1)).cuda()
     out = torch.full((wl.rows, cfg.n_q_heads, 128), 7.0, device="cuda")
     api.paged_decode_combine(to_dev(wl.seq_lens), cfg.n_q_heads, cfg.n_kv_heads, wl.bt_stride,
