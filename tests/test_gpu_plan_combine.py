@@ -34,8 +34,8 @@ def test_plan_bit_exact(seed):
 
 @pytest.mark.parametrize("chunks", [9, 200])
 def test_combine_of_oracle_partials(chunks):
-    """chunks = 200 > 88 units: most chunks are empty, and the slots they
-    would own hold garbage that the merge must not read."""
+    """chunks = 200 > 120 units: only 120 chunks are used, one unit each;
+    slots no piece owns hold garbage that the merge must not read."""
     wl = W.draw("tiny", lengths=[100, 37, 1, 64])
     cfg = wl.cfg
     G = cfg.group
@@ -54,12 +54,12 @@ def test_combine_of_oracle_partials(chunks):
                 continue  # one piece: not the combine's business
             merged[j] = True
             seg0 = cfg.n_kv_heads * rps[i] + h * npg
+            Ce = min(chunks, T)  # chunks actually used: none is empty
             pieces = []
             for k in range(first[j], last[j] + 1):
-                a = max(k * T // chunks, seg0) - seg0
-                b = min((k + 1) * T // chunks, seg0 + npg) - seg0
-                if a >= b:
-                    continue  # an empty chunk: no piece
+                a = max(k * T // Ce, seg0) - seg0
+                b = min((k + 1) * T // Ce, seg0 + npg) - seg0
+                assert a < b
                 pieces.append(k + j)
                 t0, t1 = a * 16, min(b * 16, int(wl.seq_lens[i]))
                 for g in range(G):
