@@ -222,6 +222,34 @@ pkv_status pkv_decode_step(const pkv_pool *pool, int layer, const float *q, cons
                            float *out, void *workspace, size_t workspace_bytes, int num_chunks,
                            void *stream);
 
+/* Bytes of scratch held by paged_decode_attention_static (per GPU that
+ * loads the library, for the life of the process). */
+#define PKV_STATIC_SCRATCH_BYTES (8u << 20)
+
+/* paged_decode_attention_static — paged_decode_attention for callers that
+ * cannot allocate device memory when they decode: a serving process whose
+ * device memory is all reserved up front by its KV pool and caching
+ * allocator, or code where a cudaMalloc is not allowed or would stall the
+ * device.  The pages describe no such entry point; it has no counterpart
+ * there.  Same arguments as paged_decode_attention without the workspace:
+ * the scratch is a PKV_STATIC_SCRATCH_BYTES array inside the library, and
+ * the call allocates and frees nothing.
+ *   - Calls whose paged_decode_workspace_bytes(num_rows, n_q_heads, n_kv,
+ *     128, num_chunks) exceed PKV_STATIC_SCRATCH_BYTES return
+ *     PKV_ERR_WORKSPACE (for example, with G = 4 and the default chunks of
+ *     a GB300, a few hundred rows of 8 KV heads fit).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last
+ *     call's partial states; each call clears the arrival counters first
+ *     (one cudaMemsetAsync on `stream`).  Calls that overlap on the GPU
+ *     (other streams, other host threads) race on it: serialise them. */
+pkv_status paged_decode_attention_static(const pkv_pool *pool, int layer, const float *q,
+                                         const int32_t *block_table, int bt_stride,
+                                         const int32_t *seq_lens, int num_rows, int n_q_heads,
+                                         float scale, float *out, int num_chunks, void *stream);
+
 /* Name of a status code ("PKV_OK", ...). */
 const char *pkv_status_string(pkv_status status);
 

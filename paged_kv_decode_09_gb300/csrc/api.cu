@@ -182,6 +182,11 @@ pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q, const
 
 }  // namespace
 
+namespace pkv {
+int pool_kv_heads(const pkv_pool* pool) { return pool ? pool->n_kv : 0; }
+pkv_status record_error(pkv_status s, const char* msg) { return fail(s, "%s", msg); }
+}  // namespace pkv
+
 extern "C" {
 
 size_t kv_pool_bytes(int num_layers, int num_pages, int n_kv_heads, int head_dim,

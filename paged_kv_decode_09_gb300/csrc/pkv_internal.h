@@ -87,6 +87,10 @@ inline size_t part_acc_bytes(long long slots, int group) {
   return align256(static_cast<size_t>(slots) * group * PKV_HEAD_DIM * sizeof(float));
 }
 
+// Helpers the C-ABI layer exports to the other translation units.
+int pool_kv_heads(const pkv_pool* pool);                 // n_kv_heads of a pool descriptor
+pkv_status record_error(pkv_status s, const char* msg);  // sets pkv_last_error_message
+
 cudaError_t launch_paged_decode(int dtype, int group, const DecodeArgs& a, int chunks,
                                 cudaStream_t stream);
 cudaError_t paged_decode_blocks_per_sm(int dtype, int group, int rows, int* blocks);
