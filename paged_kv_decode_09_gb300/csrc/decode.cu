@@ -52,9 +52,29 @@
 
 namespace pkv {
 
-constexpr int kConsumerWarps = 4;
+// Build-time knobs (defaults are the tuned values): consumer warps per CTA,
+// shared-memory stages per dtype, and the minimum CTAs per SM the register
+// allocation must allow.
+#ifndef PKV_CONSUMER_WARPS
+#define PKV_CONSUMER_WARPS 4
+#endif
+#ifndef PKV_F16_STAGES
+#define PKV_F16_STAGES 8
+#endif
+#ifndef PKV_Q8_STAGES
+#define PKV_Q8_STAGES 12
+#endif
+#ifndef PKV_MIN_CTAS_PER_SM
+#define PKV_MIN_CTAS_PER_SM 3
+#endif
+#ifndef PKV_MERGE_BATCH
+#define PKV_MERGE_BATCH 4
+#endif
+
+constexpr int kConsumerWarps = PKV_CONSUMER_WARPS;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
+static_assert(kConsumerWarps >= 4, "the piece merge maps one consumer thread per dim");
 
 // Shared-memory stage of one unit: the K tile then the V tile of one
 // (page, KV head); q8_0 tiles are codes followed by their block scales.
@@ -66,7 +86,7 @@ struct Tiles<PKV_KV_F16> {
   static constexpr uint32_t kScale = 0;
   static constexpr uint32_t kTile = kData;
   static constexpr uint32_t kStage = 2 * kTile;
-  static constexpr int kStages = 8;
+  static constexpr int kStages = PKV_F16_STAGES;
 };
 template <>
 struct Tiles<PKV_KV_Q8_0> {
@@ -74,7 +94,7 @@ struct Tiles<PKV_KV_Q8_0> {
   static constexpr uint32_t kScale = kPage * (kD / kQBlock) * 2;  // 128 bytes of f16 scales
   static constexpr uint32_t kTile = kData + kScale;
   static constexpr uint32_t kStage = 2 * kTile;
-  static constexpr int kStages = 12;
+  static constexpr int kStages = PKV_Q8_STAGES;
 };
 
 // Lane bookkeeping of the score phase for a GQA group of G query heads.
@@ -180,10 +200,10 @@ __device__ __forceinline__ float head_max(float x) {
 // Per-consumer-warp online softmax state for one piece.
 template <int G>
 struct WarpState {
-  float q[G][16];    // this lane's 16 dims of each query head, times scale*log2(e)
+  float2 q[G][8];    // this lane's 16 dims of each query head (pairs), times scale*log2(e)
   float m;           // running max (base 2) of the lane's head
   float l;           // running sum of the lane's own tokens (reduced at the end)
-  float acc[G][4];   // dims 4 lane .. 4 lane + 3 of each head
+  float2 acc[G][2];  // dims 4 lane .. 4 lane + 3 of each head (pairs)
 };
 
 // The dims of q a lane's 16 score-phase registers hold.
@@ -226,13 +246,14 @@ __device__ __forceinline__ void process_unit(const uint8_t* st, int nvalid, int 
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      float s0 = 0.f, s1 = 0.f;
+      // packed fp32 FMA on dim pairs: two partial sums per lane, added at the end
+      float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        s0 = fmaf(S.q[g][e], kf[e], s0);
-        s1 = fmaf(S.q[g][8 + e], kf[8 + e], s1);
+      for (int e = 0; e < 4; ++e) {
+        s0 = __ffma2_rn(S.q[g][e], make_float2(kf[2 * e], kf[2 * e + 1]), s0);
+        s1 = __ffma2_rn(S.q[g][4 + e], make_float2(kf[8 + 2 * e], kf[8 + 2 * e + 1]), s1);
       }
-      v[g * 4 + j] = (s0 + s1) * ksc;
+      v[g * 4 + j] = ((s0.x + s0.y) + (s1.x + s1.y)) * ksc;
     }
   }
   reduce_scores<G>(v, lane);
@@ -264,9 +285,9 @@ __device__ __forceinline__ void process_unit(const uint8_t* st, int nvalid, int 
   // ---- values: acc[g][dims of lane] = acc * alpha + sum_t p[g][t] V[t]
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    const float a = alpha[g];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) S.acc[g][e] *= a;
+    const float2 a2 = make_float2(alpha[g], alpha[g]);
+    S.acc[g][0] = __fmul2_rn(S.acc[g][0], a2);
+    S.acc[g][1] = __fmul2_rn(S.acc[g][1], a2);
   }
   const uint8_t* vt = st + TL::kTile;
   if (nvalid == kPage) {
@@ -290,8 +311,9 @@ __device__ __forceinline__ void process_unit(const uint8_t* st, int nvalid, int 
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const float p = (&p4[g].x)[u] * vsc;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) S.acc[g][e] = fmaf(p, vf[e], S.acc[g][e]);
+          const float2 p2 = make_float2(p, p);
+          S.acc[g][0] = __ffma2_rn(p2, make_float2(vf[0], vf[1]), S.acc[g][0]);
+          S.acc[g][1] = __ffma2_rn(p2, make_float2(vf[2], vf[3]), S.acc[g][1]);
         }
       }
     }
@@ -310,8 +332,9 @@ __device__ __forceinline__ void process_unit(const uint8_t* st, int nvalid, int 
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const float p = prob[g * kPage + t] * vsc;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) S.acc[g][e] = fmaf(p, vf[e], S.acc[g][e]);
+        const float2 p2 = make_float2(p, p);
+        S.acc[g][0] = __ffma2_rn(p2, make_float2(vf[0], vf[1]), S.acc[g][0]);
+        S.acc[g][1] = __ffma2_rn(p2, make_float2(vf[2], vf[3]), S.acc[g][1]);
       }
     }
   }
@@ -321,44 +344,53 @@ __device__ __forceinline__ void process_unit(const uint8_t* st, int nvalid, int 
 // ---------------------------------------------------------------- merge ----
 // Merge the base-2 partial states of segment j held in slots k + j for the
 // chunks k0..k1 that meet it; one thread per dim d, all G heads:
-//   M = max_k m2_k,  out = sum_k 2^(m2_k - M) acc_k / sum_k 2^(m2_k - M) l_k.
-// Loads go through L2 (other CTAs wrote the slots in this launch) and are
-// issued in batches so the merge is not a chain of dependent misses.
+//   M = max_k m2_k,  out = sum_k 2^(m2_k - M) acc_k / sum_k 2^(m2_k - M) l_k,
+// evaluated batch by batch with a running maximum (the sums are rescaled when
+// it grows).  Loads go through L2 (other CTAs wrote the slots in this
+// launch); a batch of pieces costs one round trip.
 template <int G>
 __device__ __forceinline__ void merge_segment(const float* part_ml, const float* part_acc,
                                               long long j, int k0, int k1, float* o, int d) {
-  constexpr int kBatch = 8;
+  constexpr int kBatch = PKV_MERGE_BATCH;  // pieces loaded per round trip, all G heads at once
+  float M[G], Ls[G], A[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    float M = -INFINITY;
-    for (int kk = k0; kk <= k1; kk += kBatch) {
-      float m[kBatch];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u)
-        m[u] = (kk + u <= k1) ? __ldcg(part_ml + ((kk + u + j) * G + g) * 2) : -INFINITY;
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) M = fmaxf(M, m[u]);
-    }
-    float Ls = 0.f, A = 0.f;
-    for (int kk = k0; kk <= k1; kk += kBatch) {
-      float m[kBatch], l[kBatch], x[kBatch];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const bool in = kk + u <= k1;
-        const long long slot = kk + u + j;
-        m[u] = in ? __ldcg(part_ml + (slot * G + g) * 2) : -INFINITY;
-        l[u] = in ? __ldcg(part_ml + (slot * G + g) * 2 + 1) : 0.f;
-        x[u] = in ? __ldcg(part_acc + (slot * G + g) * kD + d) : 0.f;
-      }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const float w = exp2f(m[u] - M);
-        Ls = fmaf(w, l[u], Ls);
-        A = fmaf(w, x[u], A);
-      }
-    }
-    o[g * kD + d] = A / Ls;
+    M[g] = -INFINITY;
+    Ls[g] = 0.f;
+    A[g] = 0.f;
   }
+  for (int kk = k0; kk <= k1; kk += kBatch) {
+    float m[kBatch][G], l[kBatch][G], x[kBatch][G];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const bool in = kk + u <= k1;
+      const long long slot = kk + u + j;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        m[u][g] = in ? __ldcg(part_ml + (slot * G + g) * 2) : -INFINITY;
+        l[u][g] = in ? __ldcg(part_ml + (slot * G + g) * 2 + 1) : 0.f;
+        x[u][g] = in ? __ldcg(part_acc + (slot * G + g) * kD + d) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float bm = M[g];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) bm = fmaxf(bm, m[u][g]);
+      const float sc = exp2f(M[g] - bm);  // 0 on the first batch (M = -inf)
+      Ls[g] *= sc;
+      A[g] *= sc;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const float w = exp2f(m[u][g] - bm);
+        Ls[g] = fmaf(w, l[u][g], Ls[g]);
+        A[g] = fmaf(w, x[u][g], A[g]);
+      }
+      M[g] = bm;
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) o[g * kD + d] = A[g] / Ls[g];
 }
 
 // Chunks actually used for T units when C are launched: min(C, T), so that
@@ -415,11 +447,18 @@ __device__ __forceinline__ void append_in_producer(const DecodeArgs& a, int i, i
 
 // --------------------------------------------------------------- kernel ----
 template <int DT, int G>
-__global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs a) {
+__global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
+    paged_decode_kernel(const DecodeArgs a) {
   using TL = Tiles<DT>;
   using SM = Smem<DT, G>;
   using GR = Group<G>;
   constexpr int NST = TL::kStages;
+  // A consumer waits on full[s] with the parity of its round r, which is only
+  // meaningful once round r - 1 of that stage has completed (a wait two
+  // phases ahead would pass at once and read stale data).  With NST a
+  // multiple of the consumer warps, round r - 1 of the stage belongs to the
+  // same warp, which consumed it before.
+  static_assert(NST % kConsumerWarps == 0, "stages must be a multiple of the consumer warps");
   extern __shared__ __align__(128) uint8_t smem[];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -566,13 +605,11 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs
 #pragma unroll
         for (int e = 0; e < 16; e += 4) {
           const float4 f = __ldg(reinterpret_cast<const float4*>(qrow + g * kD + q_dim<DT>(dj, e)));
-          S.q[g][e] = f.x * a.qscale;
-          S.q[g][e + 1] = f.y * a.qscale;
-          S.q[g][e + 2] = f.z * a.qscale;
-          S.q[g][e + 3] = f.w * a.qscale;
+          S.q[g][e / 2] = make_float2(f.x * a.qscale, f.y * a.qscale);
+          S.q[g][e / 2 + 1] = make_float2(f.z * a.qscale, f.w * a.qscale);
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) S.acc[g][e] = 0.f;
+        S.acc[g][0] = make_float2(0.f, 0.f);
+        S.acc[g][1] = make_float2(0.f, 0.f);
       }
       S.m = -INFINITY;
       S.l = 0.f;
@@ -608,11 +645,11 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs
 #pragma unroll
       for (int g = 0; g < G; ++g)
         *reinterpret_cast<float4*>(mrg_acc + (warp * G + g) * kD + lane * 4) =
-            make_float4(S.acc[g][0], S.acc[g][1], S.acc[g][2], S.acc[g][3]);
+            make_float4(S.acc[g][0].x, S.acc[g][0].y, S.acc[g][1].x, S.acc[g][1].y);
       named_barrier(1, kConsumerThreads);
       const bool whole = (k0 == k1);
-      const int d = threadIdx.x;  // 0..127
-      if (!aborted) {
+      const int d = threadIdx.x;  // dims: consumer threads 0..127
+      if (!aborted && d < kD) {
         const long long slot = k + j;
 #pragma unroll
         for (int g = 0; g < G; ++g) {
@@ -638,19 +675,21 @@ __global__ void __launch_bounds__(kThreads) paged_decode_kernel(const DecodeArgs
         }
       }
       // Last piece of a split segment to finish merges it (counters mode).
-      __threadfence();
+      const bool counted = !whole && a.counters != nullptr;
+      if (counted) __threadfence();  // partial visible before the arrival below
       named_barrier(1, kConsumerThreads);
       if (d == 0) {
         int last = 0;
-        if (!whole && a.counters != nullptr && !aborted && !flags[0])
+        if (counted && !aborted && !flags[0])
           last = atomicAdd(a.counters + j, 1) == k1 - k0;
         flags[2] = last;
       }
       named_barrier(1, kConsumerThreads);
       if (flags[2]) {
         __threadfence();
-        merge_segment<G>(a.part_ml, a.part_acc, j, k0, k1,
-                         a.out + (static_cast<long long>(i) * a.n_q + h * G) * kD, d);
+        if (d < kD)
+          merge_segment<G>(a.part_ml, a.part_acc, j, k0, k1,
+                           a.out + (static_cast<long long>(i) * a.n_q + h * G) * kD, d);
         if (d == 0) a.counters[j] = 0;  // ready for the next call
       }
       named_barrier(1, kConsumerThreads);
