@@ -22,20 +22,23 @@
 // the last to arrive merges all pieces into the output and resets the
 // counter; otherwise the combine kernel merges them in a second launch.
 //
-// Fused append: when new K/V are given, the producer stores each row's new
-// token into its last page (the same encoding as kv_append) just before it
-// bulk-copies that page, so attention sees it without a separate launch.
+// Fused append: when new K/V are given, the warp that reads a row's last page
+// first stores the row's new token into it (the same encoding as kv_append),
+// so attention sees it without a separate launch.
 //
-// Inside a CTA: warp 4 is the producer; its lane 0 streams the chunk's K and V
-// tiles into a ring of shared-memory stages with 1-D bulk async copies
-// tracked by mbarriers (full: bytes landed; empty: the consumer is done).
-// Warps 0-3 are consumers; warp w takes the stages of units w, w+4, ... of the
-// chunk.  Each consumer keeps a base-2 online softmax in fp32 for the G query
-// heads of the unit's KV head, sharing every K and V element it converts
-// across the group.  At the end of a piece the four warps merge through
-// shared memory.
+// Inside a CTA: four warps, each feeding itself.  Warp w takes units w, w+4,
+// ... of the chunk and keeps its own ring of shared-memory stages: it issues
+// the 1-D bulk async copies of its next units (K tile, then V tile, of one
+// (page, KV head)), waits on the stage's mbarrier, computes, and re-issues
+// into the stage it just read.  Each stage has one owner, so no empty
+// barriers are needed and four threads per CTA keep copies in flight.  Each
+// warp keeps a base-2 online softmax in fp32 for the G query heads of the
+// unit's KV head, sharing every K and V element it converts across the group.
+// At the end of a piece the warps leave their states in a shared merge
+// buffer; the last to arrive combines them and does the global writes,
+// while the others carry on streaming.
 //
-// Lane layout of a consumer warp on one 16-token page (lane = 8 tg + dj):
+// Lane layout of a warp on one 16-token page (lane = 8 tg + dj):
 //   scores: lane handles tokens 4tg..4tg+3 and 16 of the 128 dims (f16: two
 //     8-dim chunks dj and dj+8; q8_0: the 16 dims 16dj..16dj+15, inside one
 //     32-wide q8_0 block), for all G heads; the 8 lanes of a token group then
@@ -55,14 +58,11 @@ namespace pkv {
 // Build-time knobs (defaults are the tuned values): consumer warps per CTA,
 // shared-memory stages per dtype, and the minimum CTAs per SM the register
 // allocation must allow.
-#ifndef PKV_CONSUMER_WARPS
-#define PKV_CONSUMER_WARPS 4
+#ifndef PKV_F16_RING
+#define PKV_F16_RING 2
 #endif
-#ifndef PKV_F16_STAGES
-#define PKV_F16_STAGES 8
-#endif
-#ifndef PKV_Q8_STAGES
-#define PKV_Q8_STAGES 12
+#ifndef PKV_Q8_RING
+#define PKV_Q8_RING 3
 #endif
 #ifndef PKV_MIN_CTAS_PER_SM
 #define PKV_MIN_CTAS_PER_SM 3
@@ -71,10 +71,8 @@ namespace pkv {
 #define PKV_MERGE_BATCH 4
 #endif
 
-constexpr int kConsumerWarps = PKV_CONSUMER_WARPS;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
-static_assert(kConsumerWarps >= 4, "the piece merge maps one consumer thread per dim");
+constexpr int kWarps = 4;  // warps per CTA; the piece merge gives each lane 4 of the 128 dims
+constexpr int kThreads = kWarps * 32;
 
 // Shared-memory stage of one unit: the K tile then the V tile of one
 // (page, KV head); q8_0 tiles are codes followed by their block scales.
@@ -86,7 +84,7 @@ struct Tiles<PKV_KV_F16> {
   static constexpr uint32_t kScale = 0;
   static constexpr uint32_t kTile = kData;
   static constexpr uint32_t kStage = 2 * kTile;
-  static constexpr int kStages = PKV_F16_STAGES;
+  static constexpr int kRing = PKV_F16_RING;  // stages per warp
 };
 template <>
 struct Tiles<PKV_KV_Q8_0> {
@@ -94,7 +92,7 @@ struct Tiles<PKV_KV_Q8_0> {
   static constexpr uint32_t kScale = kPage * (kD / kQBlock) * 2;  // 128 bytes of f16 scales
   static constexpr uint32_t kTile = kData + kScale;
   static constexpr uint32_t kStage = 2 * kTile;
-  static constexpr int kStages = PKV_Q8_STAGES;
+  static constexpr int kRing = PKV_Q8_RING;  // stages per warp
 };
 
 // Lane bookkeeping of the score phase for a GQA group of G query heads.
@@ -109,14 +107,14 @@ struct Group {
 
 template <int DT, int G>
 struct Smem {
-  static constexpr int kStages = Tiles<DT>::kStages;
-  static constexpr uint32_t kBar = kStages * Tiles<DT>::kStage;       // full[], empty[]
-  static constexpr uint32_t kMrgAcc = kBar + 2 * kStages * 8;          // f32 [warps][G][D]
-  static constexpr uint32_t kMrgMl = kMrgAcc + kConsumerWarps * G * kD * 4;  // f32 [warps][G][2]
-  static constexpr uint32_t kProb = kMrgMl + kConsumerWarps * G * 2 * 4;     // f32 [warps][G][16]
-  static constexpr uint32_t kAlpha = kProb + kConsumerWarps * G * kPage * 4;  // f32 [warps][4]
-  static constexpr uint32_t kFlags = kAlpha + kConsumerWarps * 4 * 4;        // abort, issued
-  static constexpr uint32_t kRows = kFlags + 16;  // int row_start[rows + 1], lens[rows]
+  static constexpr int kStages = kWarps * Tiles<DT>::kRing;
+  static constexpr uint32_t kBar = kStages * Tiles<DT>::kStage;           // full[warp][ring]
+  static constexpr uint32_t kMrgAcc = kBar + ((kStages * 8 + 15) / 16) * 16;  // f32 [warps][G][D]
+  static constexpr uint32_t kMrgMl = kMrgAcc + kWarps * G * kD * 4;        // f32 [warps][G][2]
+  static constexpr uint32_t kProb = kMrgMl + kWarps * G * 2 * 4;           // f32 [warps][G][16]
+  static constexpr uint32_t kAlpha = kProb + kWarps * G * kPage * 4;       // f32 [warps][4]
+  static constexpr uint32_t kCtl = kAlpha + kWarps * 4 * 4;                // int [4]
+  static constexpr uint32_t kRows = kCtl + 16;  // int row_start[rows + 1], lens[rows]
   static size_t bytes(int rows) { return kRows + (2 * static_cast<size_t>(rows) + 1) * 4; }
   static_assert(kMrgAcc % 16 == 0 && kMrgMl % 16 == 0 && kProb % 16 == 0 && kAlpha % 16 == 0,
                 "vector accesses need 16-byte aligned regions");
@@ -400,11 +398,11 @@ __device__ __forceinline__ int used_chunks(long long T, int C) {
 }
 
 // ------------------------------------------------------------- append ----
-// The producer warp stores row i's new K and V token of KV head h into slot
-// (L - 1) % 16 of tile (page, h) before it bulk-copies that tile: 4 dims per
-// lane; q8_0 blocks of 32 dims span 8 lanes.  Same encoding as kv_append.
+// A warp stores row i's new K and V token of KV head h into slot (L - 1) % 16
+// of tile (page, h) just before it bulk-copies that tile: 4 dims per lane;
+// q8_0 blocks of 32 dims span 8 lanes.  Same encoding as kv_append.
 template <int DT>
-__device__ __forceinline__ void append_in_producer(const DecodeArgs& a, int i, int h, int page,
+__device__ __forceinline__ void append_token(const DecodeArgs& a, int i, int h, int page,
                                                    int slot, int lane) {
   using TL = Tiles<DT>;
   const size_t tile = static_cast<size_t>(page) * a.n_kv + h;
@@ -445,6 +443,115 @@ __device__ __forceinline__ void append_in_producer(const DecodeArgs& a, int i, i
   __syncwarp();
 }
 
+// ------------------------------------------------------------ piece merge ----
+// The warp that arrives last at the end of a piece combines the four warps'
+// states from shared memory: lane l owns dims 4l..4l+3 of every head.  A
+// whole segment is written to the output; otherwise the piece's partial
+// state goes to its workspace slot.
+template <int G>
+__device__ __forceinline__ void piece_merge(const float* mrg_acc, const float* mrg_ml, bool whole,
+                                            float* out_seg, float* part_ml, float* part_acc,
+                                            long long slot, int lane) {
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mrg_ml[(w * G + g) * 2]);
+    float Ls = 0.f;
+    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = exp2f(mrg_ml[(w * G + g) * 2] - M);
+      Ls = fmaf(f, mrg_ml[(w * G + g) * 2 + 1], Ls);
+      const float4 x = *reinterpret_cast<const float4*>(mrg_acc + (w * G + g) * kD + lane * 4);
+      A.x = fmaf(f, x.x, A.x);
+      A.y = fmaf(f, x.y, A.y);
+      A.z = fmaf(f, x.z, A.z);
+      A.w = fmaf(f, x.w, A.w);
+    }
+    if (whole) {
+      *reinterpret_cast<float4*>(out_seg + g * kD + lane * 4) =
+          make_float4(A.x / Ls, A.y / Ls, A.z / Ls, A.w / Ls);
+    } else {
+      *reinterpret_cast<float4*>(part_acc + (slot * G + g) * kD + lane * 4) = A;
+      if (lane == 0) {
+        part_ml[(slot * G + g) * 2] = M;
+        part_ml[(slot * G + g) * 2 + 1] = Ls;
+      }
+    }
+  }
+}
+
+// The same merge as merge_segment, done by one warp (lane l: dims 4l..4l+3).
+template <int G>
+__device__ __forceinline__ void merge_segment_warp(const float* part_ml, const float* part_acc,
+                                                   long long j, int k0, int k1, float* o, int lane) {
+  constexpr int kBatch = 2;
+  float M[G], Ls[G];
+  float4 A[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    M[g] = -INFINITY;
+    Ls[g] = 0.f;
+    A[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int kk = k0; kk <= k1; kk += kBatch) {
+    float m[kBatch][G], l[kBatch][G];
+    float4 x[kBatch][G];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const bool in = kk + u <= k1;
+      const long long slot = kk + u + j;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        m[u][g] = in ? __ldcg(part_ml + (slot * G + g) * 2) : -INFINITY;
+        l[u][g] = in ? __ldcg(part_ml + (slot * G + g) * 2 + 1) : 0.f;
+        x[u][g] = in ? __ldcg(reinterpret_cast<const float4*>(part_acc + (slot * G + g) * kD) + lane)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float bm = M[g];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) bm = fmaxf(bm, m[u][g]);
+      const float sc = exp2f(M[g] - bm);
+      Ls[g] *= sc;
+      A[g].x *= sc;
+      A[g].y *= sc;
+      A[g].z *= sc;
+      A[g].w *= sc;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const float w = exp2f(m[u][g] - bm);
+        Ls[g] = fmaf(w, l[u][g], Ls[g]);
+        A[g].x = fmaf(w, x[u][g].x, A[g].x);
+        A[g].y = fmaf(w, x[u][g].y, A[g].y);
+        A[g].z = fmaf(w, x[u][g].z, A[g].z);
+        A[g].w = fmaf(w, x[u][g].w, A[g].w);
+      }
+      M[g] = bm;
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+    *reinterpret_cast<float4*>(o + g * kD + lane * 4) =
+        make_float4(A[g].x / Ls[g], A[g].y / Ls[g], A[g].z / Ls[g], A[g].w / Ls[g]);
+}
+
+// Spin (bounded) until the shared merge buffer has been released for piece
+// `piece`; false on timeout or abort.
+__device__ __forceinline__ bool wait_merge_buffer(volatile int* ctl, int piece) {
+  if (ctl[2] >= piece) return true;
+  const unsigned long long t0 = global_ns();
+  while (ctl[2] < piece) {
+    if (ctl[0]) return false;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+    __nanosleep(32);
+  }
+  return true;
+}
+
 // --------------------------------------------------------------- kernel ----
 template <int DT, int G>
 __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
@@ -452,31 +559,24 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
   using TL = Tiles<DT>;
   using SM = Smem<DT, G>;
   using GR = Group<G>;
-  constexpr int NST = TL::kStages;
-  // A consumer waits on full[s] with the parity of its round r, which is only
-  // meaningful once round r - 1 of that stage has completed (a wait two
-  // phases ahead would pass at once and read stale data).  With NST a
-  // multiple of the consumer warps, round r - 1 of the stage belongs to the
-  // same warp, which consumed it before.
-  static_assert(NST % kConsumerWarps == 0, "stages must be a multiple of the consumer warps");
+  constexpr int R = TL::kRing;
   extern __shared__ __align__(128) uint8_t smem[];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // [0] abort, [1] copies issued, [2] this CTA merges the current segment
-  volatile int* flags = reinterpret_cast<volatile int*>(smem + SM::kFlags);
+  // [0] abort  [1] warps arrived at the current piece end  [2] merge-buffer generation
+  volatile int* ctl = reinterpret_cast<volatile int*>(smem + SM::kCtl);
   int* row_start = reinterpret_cast<int*>(smem + SM::kRows);
   int* lens = row_start + a.num_rows + 1;
-  const uint32_t full0 = smem_addr(smem + SM::kBar);
-  const uint32_t empty0 = full0 + NST * 8;
+  const uint32_t bar0 = smem_addr(smem + SM::kBar) + warp * R * 8;  // this warp's barriers
+  uint8_t* ring = smem + static_cast<size_t>(warp) * R * TL::kStage;  // this warp's stages
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NST; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
-    }
-    flags[0] = 0;
-    flags[1] = 0;
-    flags[2] = 0;
+    ctl[0] = 0;
+    ctl[1] = 0;
+    ctl[2] = 0;
+  }
+  if (lane == 0) {
+    for (int s = 0; s < R; ++s) mbar_init(bar0 + 8 * s, 1);
     fence_mbar_init();
   }
   plan_rows(a.seq_lens, a.num_rows, a.bt_stride, blockIdx.x == 0 ? a.status : nullptr, lens,
@@ -487,224 +587,212 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
   const long long c_begin = k < C ? static_cast<long long>(k) * T / C : T;
   const long long c_end = k < C ? static_cast<long long>(k + 1) * T / C : T;
 
-  if (warp == kConsumerWarps) {
-    // ------------------------------------------------------- producer ----
-    const uint32_t stage0 = smem_addr(smem);
-    const uint64_t policy = policy_evict_first();
-    // Unit base + lane: its page, KV head and row, and whether it is the
-    // row's last page (where the new token goes); bad pages read page 0 and
-    // take no append.
-    auto fetch = [&](long long base, int& page, int& head, int& row, int& last) {
-      const long long x = base + lane;
-      page = 0;
-      head = 0;
-      row = 0;
-      last = 0;
-      if (x < c_end) {
-        const int i = row_of(row_start, a.num_rows, a.n_kv, x);
-        const int npg = row_start[i + 1] - row_start[i];
-        const int off = static_cast<int>(x - static_cast<long long>(a.n_kv) * row_start[i]);
-        head = off / npg;
-        const int p = off - head * npg;
-        int pg = __ldg(a.block_table + static_cast<long long>(i) * a.bt_stride + p);
-        last = (p == npg - 1) ? 1 : 0;
-        if (pg < 0 || pg >= a.num_pages) {
-          record_status(a.status, PKV_DEV_BAD_PAGE);
-          pg = 0;
-          last = 0;
-        }
-        page = pg;
-        row = i;
-      }
-    };
-    int pg_cur, h_cur, r_cur, l_cur;
-    fetch(c_begin, pg_cur, h_cur, r_cur, l_cur);
-    uint32_t it = 0;
-    bool stop = false;
-    for (long long base = c_begin; base < c_end && !stop; base += 32) {
-      int pg_nxt = 0, h_nxt = 0, r_nxt = 0, l_nxt = 0;
-      if (base + 32 < c_end) fetch(base + 32, pg_nxt, h_nxt, r_nxt, l_nxt);  // one batch ahead
-      const int n = static_cast<int>(min(32LL, c_end - base));
-      for (int kk = 0; kk < n; ++kk) {
-        const int pg = __shfl_sync(kFull, pg_cur, kk);
-        const int hh = __shfl_sync(kFull, h_cur, kk);
-        if (a.k_new != nullptr && __shfl_sync(kFull, l_cur, kk)) {
-          const int row = __shfl_sync(kFull, r_cur, kk);
-          append_in_producer<DT>(a, row, hh, pg, (lens[row] - 1) % kPage, lane);
-        }
-        int ok = 1;
-        if (lane == 0) {
-          const int s = it % NST;
-          if (it >= NST) ok = mbar_wait_bounded(empty0 + 8 * s, ((it / NST) - 1) & 1, flags);
-          if (ok && flags[0]) ok = 0;
-          if (ok) {
-            const uint32_t bar = full0 + 8 * s;
-            const uint32_t dst = stage0 + s * TL::kStage;
-            const size_t unit = static_cast<size_t>(pg) * a.n_kv + hh;
-            mbar_arrive_expect_tx(bar, TL::kStage);
-            bulk_g2s(dst, a.k_data + unit * TL::kData, TL::kData, bar, policy);
-            if constexpr (DT == PKV_KV_Q8_0)
-              bulk_g2s(dst + TL::kData, a.k_scales + unit * TL::kScale, TL::kScale, bar, policy);
-            bulk_g2s(dst + TL::kTile, a.v_data + unit * TL::kData, TL::kData, bar, policy);
-            if constexpr (DT == PKV_KV_Q8_0)
-              bulk_g2s(dst + TL::kTile + TL::kData, a.v_scales + unit * TL::kScale, TL::kScale,
-                       bar, policy);
-            ++it;
-            flags[1] = static_cast<int>(it);
-          } else if (!flags[0]) {
-            flags[0] = 1;
-            record_status(a.status, PKV_DEV_TIMEOUT);
-          }
-        }
-        if (!__shfl_sync(kFull, ok, 0)) {
-          stop = true;
-          break;
-        }
-      }
-      pg_cur = pg_nxt;
-      h_cur = h_nxt;
-      r_cur = r_nxt;
-      l_cur = l_nxt;
-    }
-  } else {
-    // ------------------------------------------------------- consumers ----
-    const int tg = lane >> 3, dj = lane & 7;
-    float* mrg_acc = reinterpret_cast<float*>(smem + SM::kMrgAcc);
-    float* mrg_ml = reinterpret_cast<float*>(smem + SM::kMrgMl);
-    float* prob = reinterpret_cast<float*>(smem + SM::kProb) + warp * G * kPage;
-    float* alpha = reinterpret_cast<float*>(smem + SM::kAlpha) + warp * 4;
-    const int g_lane = dj >> (3 - GR::kLog2);
-    const bool head_writer =
-        tg == 0 && (dj & (GR::kTokLanes - 1)) == 0 && (G > 1 || dj < 4);
-    bool aborted = false;
-    WarpState<G> S;
-
-    // Rows without tokens attend to nothing: their output is zero.
-    if (k == 0) {
-      for (int i = 0; i < a.num_rows; ++i)
-        if (row_start[i + 1] == row_start[i])
-          for (int e = threadIdx.x; e < a.n_q * kD; e += kConsumerThreads)
-            a.out[static_cast<long long>(i) * a.n_q * kD + e] = 0.f;
-    }
-
-    for (long long x = c_begin; x < c_end;) {
-      const int i = row_of(row_start, a.num_rows, a.n_kv, x);
-      const int npg = row_start[i + 1] - row_start[i];
-      const long long row_base = static_cast<long long>(a.n_kv) * row_start[i];
-      const int h = static_cast<int>((x - row_base) / npg);
-      const long long seg_start = row_base + static_cast<long long>(h) * npg;
-      const long long seg_end = seg_start + npg;
-      const long long b = min(seg_end, c_end);
-      const int L = lens[i];
-      const long long j = static_cast<long long>(i) * a.n_kv + h;
-      const int k0 = chunk_of(seg_start, T, C), k1 = chunk_of(seg_end - 1, T, C);
-
-      const float* qrow = a.q + (static_cast<long long>(i) * a.n_q + h * G) * kD;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-#pragma unroll
-        for (int e = 0; e < 16; e += 4) {
-          const float4 f = __ldg(reinterpret_cast<const float4*>(qrow + g * kD + q_dim<DT>(dj, e)));
-          S.q[g][e / 2] = make_float2(f.x * a.qscale, f.y * a.qscale);
-          S.q[g][e / 2 + 1] = make_float2(f.z * a.qscale, f.w * a.qscale);
-        }
-        S.acc[g][0] = make_float2(0.f, 0.f);
-        S.acc[g][1] = make_float2(0.f, 0.f);
-      }
-      S.m = -INFINITY;
-      S.l = 0.f;
-
-      const int r = static_cast<int>((x - c_begin) % kConsumerWarps);
-      for (long long pos = x + ((warp - r + kConsumerWarps) % kConsumerWarps); pos < b;
-           pos += kConsumerWarps) {
-        const uint32_t it = static_cast<uint32_t>(pos - c_begin);
-        const int s = it % NST;
-        bool ok = !aborted && mbar_wait_bounded(full0 + 8 * s, (it / NST) & 1, flags);
-        ok = __all_sync(kFull, ok);
-        if (!ok) {
-          if (!aborted && lane == 0 && !flags[0]) {
-            flags[0] = 1;
-            record_status(a.status, PKV_DEV_TIMEOUT);
-          }
-          aborted = true;
-          continue;
-        }
-        const int nvalid = min(kPage, L - static_cast<int>(pos - seg_start) * kPage);
-        process_unit<DT, G>(smem + s * TL::kStage, nvalid, lane, S, prob, alpha);
-        if (lane == 0) mbar_arrive(empty0 + 8 * s);
-      }
-
-      // ---- merge the four warps' states of this piece.  Every consumer
-      // thread passes the same four barriers whatever happened, so that an
-      // abort can never leave a barrier short of threads.
-      const float l_tot = head_sum<G>(S.l);
-      if (head_writer) {
-        mrg_ml[(warp * G + g_lane) * 2] = S.m;
-        mrg_ml[(warp * G + g_lane) * 2 + 1] = l_tot;
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-        *reinterpret_cast<float4*>(mrg_acc + (warp * G + g) * kD + lane * 4) =
-            make_float4(S.acc[g][0].x, S.acc[g][0].y, S.acc[g][1].x, S.acc[g][1].y);
-      named_barrier(1, kConsumerThreads);
-      const bool whole = (k0 == k1);
-      const int d = threadIdx.x;  // dims: consumer threads 0..127
-      if (!aborted && d < kD) {
-        const long long slot = k + j;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float M = -INFINITY;
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mrg_ml[(w * G + g) * 2]);
-          float Ls = 0.f, A = 0.f;
-#pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
-            const float f = exp2f(mrg_ml[(w * G + g) * 2] - M);
-            Ls = fmaf(f, mrg_ml[(w * G + g) * 2 + 1], Ls);
-            A = fmaf(f, mrg_acc[(w * G + g) * kD + d], A);
-          }
-          if (whole) {
-            a.out[(static_cast<long long>(i) * a.n_q + h * G + g) * kD + d] = A / Ls;
-          } else {
-            a.part_acc[(slot * G + g) * kD + d] = A;
-            if (d == 0) {
-              a.part_ml[(slot * G + g) * 2] = M;
-              a.part_ml[(slot * G + g) * 2 + 1] = Ls;
-            }
-          }
-        }
-      }
-      // Last piece of a split segment to finish merges it (counters mode).
-      const bool counted = !whole && a.counters != nullptr;
-      if (counted) __threadfence();  // partial visible before the arrival below
-      named_barrier(1, kConsumerThreads);
-      if (d == 0) {
-        int last = 0;
-        if (counted && !aborted && !flags[0])
-          last = atomicAdd(a.counters + j, 1) == k1 - k0;
-        flags[2] = last;
-      }
-      named_barrier(1, kConsumerThreads);
-      if (flags[2]) {
-        __threadfence();
-        if (d < kD)
-          merge_segment<G>(a.part_ml, a.part_acc, j, k0, k1,
-                           a.out + (static_cast<long long>(i) * a.n_q + h * G) * kD, d);
-        if (d == 0) a.counters[j] = 0;  // ready for the next call
-      }
-      named_barrier(1, kConsumerThreads);
-      x = b;
-    }
+  // Rows without tokens attend to nothing: their output is zero.
+  if (k == 0) {
+    for (int i = 0; i < a.num_rows; ++i)
+      if (row_start[i + 1] == row_start[i])
+        for (int e = threadIdx.x; e < a.n_q * kD; e += kThreads)
+          a.out[static_cast<long long>(i) * a.n_q * kD + e] = 0.f;
   }
 
-  // After a timeout no bulk copy may still be landing in this CTA's shared
-  // memory when it exits: wait (bounded) for the last NST issued copies.
-  __syncthreads();
-  if (threadIdx.x == 0 && flags[0]) {
-    const int issued = flags[1];
+  // This warp's units: chunk positions first + 4u, u < n_units.
+  const long long first = c_begin + warp;
+  const int n_units = first < c_end ? static_cast<int>((c_end - first + kWarps - 1) / kWarps) : 0;
+
+  // Unit descriptors, 32 at a time (lane j: unit base + j): page, KV head,
+  // row, and whether it is the row's last page (bad pages read page 0 and
+  // take no append).  Two batches are kept: the current one and the next.
+  auto fetch = [&](int base, int& pg, int& hh, int& row, int& last) {
+    const int u = base + lane;
+    pg = 0;
+    hh = 0;
+    row = 0;
+    last = 0;
+    if (u < n_units) {
+      const long long x = first + static_cast<long long>(u) * kWarps;
+      const int i = row_of(row_start, a.num_rows, a.n_kv, x);
+      const int npg = row_start[i + 1] - row_start[i];
+      const int off = static_cast<int>(x - static_cast<long long>(a.n_kv) * row_start[i]);
+      hh = off / npg;
+      const int p = off - hh * npg;
+      int page = __ldg(a.block_table + static_cast<long long>(i) * a.bt_stride + p);
+      last = (p == npg - 1) ? 1 : 0;
+      if (page < 0 || page >= a.num_pages) {
+        record_status(a.status, PKV_DEV_BAD_PAGE);
+        page = 0;
+        last = 0;
+      }
+      pg = page;
+      row = i;
+    }
+  };
+  int c_pg, c_h, c_row, c_last, n_pg, n_h, n_row, n_last;
+  int batch = 0;
+  fetch(0, c_pg, c_h, c_row, c_last);
+  fetch(32, n_pg, n_h, n_row, n_last);
+  int issued = 0;
+  const uint64_t policy = policy_evict_first();
+
+  // Issue unit `issued` into its stage (warp-uniform).
+  auto issue = [&]() {
+    const int u = issued;
+    if (u >= batch + 32) {
+      c_pg = n_pg;
+      c_h = n_h;
+      c_row = n_row;
+      c_last = n_last;
+      batch += 32;
+      fetch(batch + 32, n_pg, n_h, n_row, n_last);
+    }
+    const int jj = u - batch;
+    const int pg = __shfl_sync(kFull, c_pg, jj);
+    const int hh = __shfl_sync(kFull, c_h, jj);
+    if (a.k_new != nullptr && __shfl_sync(kFull, c_last, jj)) {
+      const int row = __shfl_sync(kFull, c_row, jj);
+      append_token<DT>(a, row, hh, pg, (lens[row] - 1) % kPage, lane);
+    }
+    // The warp's earlier reads of this stage come before the copy rewrites it.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+      const int s = u % R;
+      const uint32_t bar = bar0 + 8 * s;
+      const uint32_t dst = smem_addr(ring + s * TL::kStage);
+      const size_t unit = static_cast<size_t>(pg) * a.n_kv + hh;
+      mbar_arrive_expect_tx(bar, TL::kStage);
+      bulk_g2s(dst, a.k_data + unit * TL::kData, TL::kData, bar, policy);
+      if constexpr (DT == PKV_KV_Q8_0)
+        bulk_g2s(dst + TL::kData, a.k_scales + unit * TL::kScale, TL::kScale, bar, policy);
+      bulk_g2s(dst + TL::kTile, a.v_data + unit * TL::kData, TL::kData, bar, policy);
+      if constexpr (DT == PKV_KV_Q8_0)
+        bulk_g2s(dst + TL::kTile + TL::kData, a.v_scales + unit * TL::kScale, TL::kScale, bar,
+                 policy);
+    }
+    ++issued;
+  };
+  while (issued < n_units && issued < R) issue();
+
+  const int tg = lane >> 3, dj = lane & 7;
+  float* mrg_acc = reinterpret_cast<float*>(smem + SM::kMrgAcc);
+  float* mrg_ml = reinterpret_cast<float*>(smem + SM::kMrgMl);
+  float* prob = reinterpret_cast<float*>(smem + SM::kProb) + warp * G * kPage;
+  float* alpha = reinterpret_cast<float*>(smem + SM::kAlpha) + warp * 4;
+  const int g_lane = dj >> (3 - GR::kLog2);
+  const bool head_writer = tg == 0 && (dj & (GR::kTokLanes - 1)) == 0 && (G > 1 || dj < 4);
+  bool aborted = false;
+  int consumed = 0;
+  WarpState<G> S;
+
+  int piece = 0;
+  for (long long x = c_begin; x < c_end; ++piece) {
+    const int i = row_of(row_start, a.num_rows, a.n_kv, x);
+    const int npg = row_start[i + 1] - row_start[i];
+    const long long row_base = static_cast<long long>(a.n_kv) * row_start[i];
+    const int h = static_cast<int>((x - row_base) / npg);
+    const long long seg_start = row_base + static_cast<long long>(h) * npg;
+    const long long seg_end = seg_start + npg;
+    const long long b = min(seg_end, c_end);
+    const int L = lens[i];
+    const long long j = static_cast<long long>(i) * a.n_kv + h;
+    const int k0 = chunk_of(seg_start, T, C), k1 = chunk_of(seg_end - 1, T, C);
+
+    const float* qrow = a.q + (static_cast<long long>(i) * a.n_q + h * G) * kD;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+#pragma unroll
+      for (int e = 0; e < 16; e += 4) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(qrow + g * kD + q_dim<DT>(dj, e)));
+        S.q[g][e / 2] = make_float2(f.x * a.qscale, f.y * a.qscale);
+        S.q[g][e / 2 + 1] = make_float2(f.z * a.qscale, f.w * a.qscale);
+      }
+      S.acc[g][0] = make_float2(0.f, 0.f);
+      S.acc[g][1] = make_float2(0.f, 0.f);
+    }
+    S.m = -INFINITY;
+    S.l = 0.f;
+
+    const int r = static_cast<int>((x - c_begin) % kWarps);
+    for (long long pos = x + ((warp - r + kWarps) % kWarps); pos < b; pos += kWarps) {
+      const int u = static_cast<int>((pos - first) / kWarps);
+      const int s = u % R;
+      bool ok = !aborted && mbar_wait_bounded(bar0 + 8 * s, (u / R) & 1, ctl);
+      ok = __all_sync(kFull, ok);
+      if (!ok) {
+        if (!aborted && lane == 0 && !ctl[0]) {
+          ctl[0] = 1;
+          record_status(a.status, PKV_DEV_TIMEOUT);
+        }
+        aborted = true;
+        continue;
+      }
+      consumed = u + 1;
+      const int nvalid = min(kPage, L - static_cast<int>(pos - seg_start) * kPage);
+      process_unit<DT, G>(ring + s * TL::kStage, nvalid, lane, S, prob, alpha);
+      if (issued < n_units) issue();
+    }
+
+    // ---- piece end: leave this warp's state in the shared merge buffer;
+    // the last warp to arrive merges (the others go on streaming).
+    const float l_tot = head_sum<G>(S.l);
+    int ok = 1;
+    if (lane == 0) ok = wait_merge_buffer(ctl, piece);
+    ok = __shfl_sync(kFull, ok, 0);
+    if (!ok && !aborted) {
+      if (lane == 0 && !ctl[0]) {
+        ctl[0] = 1;
+        record_status(a.status, PKV_DEV_TIMEOUT);
+      }
+      aborted = true;
+    }
+    if (head_writer) {
+      mrg_ml[(warp * G + g_lane) * 2] = aborted ? -INFINITY : S.m;
+      mrg_ml[(warp * G + g_lane) * 2 + 1] = l_tot;
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      *reinterpret_cast<float4*>(mrg_acc + (warp * G + g) * kD + lane * 4) =
+          make_float4(S.acc[g][0].x, S.acc[g][0].y, S.acc[g][1].x, S.acc[g][1].y);
+    __syncwarp();
+    int lastw = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      lastw = atomicAdd(const_cast<int*>(&ctl[1]), 1) == kWarps - 1;
+    }
+    lastw = __shfl_sync(kFull, lastw, 0);
+    if (lastw) {
+      __threadfence_block();
+      const bool whole = (k0 == k1);
+      const bool live = !ctl[0];
+      float* out_seg = a.out + (static_cast<long long>(i) * a.n_q + h * G) * kD;
+      if (live)
+        piece_merge<G>(mrg_acc, mrg_ml, whole, out_seg, a.part_ml, a.part_acc, k + j, lane);
+      __syncwarp();
+      if (lane == 0) {  // release the merge buffer for the next piece
+        ctl[1] = 0;
+        __threadfence_block();
+        ctl[2] = piece + 1;
+      }
+      if (live && !whole && a.counters != nullptr) {
+        __threadfence();  // this piece's partial is visible before its arrival
+        __syncwarp();
+        int seg_last = 0;
+        if (lane == 0) seg_last = atomicAdd(a.counters + j, 1) == k1 - k0;
+        seg_last = __shfl_sync(kFull, seg_last, 0);
+        if (seg_last) {
+          __threadfence();
+          merge_segment_warp<G>(a.part_ml, a.part_acc, j, k0, k1, out_seg, lane);
+          if (lane == 0) a.counters[j] = 0;  // ready for the next call
+        }
+      }
+    }
+    x = b;
+  }
+
+  // Copies still in flight after an abort must land before the CTA exits.
+  if (aborted || ctl[0]) {
     const int zero = 0;
-    for (int it = issued > NST ? issued - NST : 0; it < issued; ++it)
-      mbar_wait_bounded(full0 + 8 * (it % NST), (it / NST) & 1, &zero);
+    for (int u = consumed > issued - R ? consumed : issued - R; u < issued; ++u)
+      if (u >= 0) mbar_wait_bounded(bar0 + 8 * (u % R), (u / R) & 1, &zero);
   }
 }
 

@@ -191,7 +191,8 @@ def test_split_then_combine_equals_merged(dtype):
     api.paged_decode_combine(sl, wl.cfg.n_q_heads, wl.cfg.n_kv_heads, wl.bt_stride,
                              ws.num_chunks, ws.tensor, out)
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(out.cpu().numpy(), merged)
+    # the two merges batch the pieces differently: same sums, other rounding order
+    np.testing.assert_allclose(out.cpu().numpy(), merged, rtol=0, atol=1e-6)
     _check(merged, oracle_decode(wl, host))
 
 
