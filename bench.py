@@ -168,7 +168,7 @@ def profile_traffic(workload: str):
         with open(os.path.join(src, name), "rb") as f:
             h.update(f.read())
     digest = h.hexdigest()[:16]
-    path = os.path.join(ROOT, "profiles", f"paged_decode_split_{workload}.md")
+    path = os.path.join(ROOT, "profiles", f"paged_decode_kernel_{workload}.md")
     try:
         text = open(path).read()
     except OSError:

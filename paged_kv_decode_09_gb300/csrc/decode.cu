@@ -68,7 +68,7 @@ namespace pkv {
 #define PKV_MIN_CTAS_PER_SM 3
 #endif
 #ifndef PKV_MERGE_BATCH
-#define PKV_MERGE_BATCH 4
+#define PKV_MERGE_BATCH 8
 #endif
 
 constexpr int kWarps = 4;  // warps per CTA; the piece merge gives each lane 4 of the 128 dims
@@ -140,9 +140,23 @@ __device__ __forceinline__ void f16x4_to_f32(const uint2& u, float* f) {
   f[3] = b.y;
 }
 
+// Four signed bytes to floats, exactly: bias each byte to b + 128 (xor 0x80),
+// place it in the low mantissa byte of 2^23 (the float 2^23 + b + 128), and
+// subtract 2^23 + 128 -- one byte permute per value and one packed subtract
+// per pair instead of integer-to-float conversions.
 __device__ __forceinline__ void i8x4_to_f32(uint32_t w, float* f) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) f[i] = static_cast<float>(static_cast<int8_t>((w >> (8 * i)) & 0xffu));
+  const uint32_t u = w ^ 0x80808080u;
+  const float2 bias = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+  const float2 lo = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
+                                           __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441))),
+                               bias);
+  const float2 hi = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
+                                           __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443))),
+                               bias);
+  f[0] = lo.x;
+  f[1] = lo.y;
+  f[2] = hi.x;
+  f[3] = hi.y;
 }
 
 // ------------------------------------------------------- warp reductions ----
@@ -731,9 +745,12 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
       if (issued < n_units) issue();
     }
 
-    // ---- piece end: leave this warp's state in the shared merge buffer;
-    // the last warp to arrive merges (the others go on streaming).
+    // ---- piece end: leave this warp's state in the shared merge buffer.
+    // For every piece but the chunk's last, the last warp to arrive merges
+    // while the others go on streaming; the chunk's last piece is merged by
+    // the whole CTA, since all its warps are done by then.
     const float l_tot = head_sum<G>(S.l);
+    const bool final_piece = (b == c_end);
     int ok = 1;
     if (lane == 0) ok = wait_merge_buffer(ctl, piece);
     ok = __shfl_sync(kFull, ok, 0);
@@ -752,36 +769,84 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
     for (int g = 0; g < G; ++g)
       *reinterpret_cast<float4*>(mrg_acc + (warp * G + g) * kD + lane * 4) =
           make_float4(S.acc[g][0].x, S.acc[g][0].y, S.acc[g][1].x, S.acc[g][1].y);
-    __syncwarp();
-    int lastw = 0;
-    if (lane == 0) {
-      __threadfence_block();
-      lastw = atomicAdd(const_cast<int*>(&ctl[1]), 1) == kWarps - 1;
-    }
-    lastw = __shfl_sync(kFull, lastw, 0);
-    if (lastw) {
-      __threadfence_block();
-      const bool whole = (k0 == k1);
+    const bool whole = (k0 == k1);
+    float* out_seg = a.out + (static_cast<long long>(i) * a.n_q + h * G) * kD;
+    if (final_piece) {
+      named_barrier(1, kThreads);
       const bool live = !ctl[0];
-      float* out_seg = a.out + (static_cast<long long>(i) * a.n_q + h * G) * kD;
-      if (live)
-        piece_merge<G>(mrg_acc, mrg_ml, whole, out_seg, a.part_ml, a.part_acc, k + j, lane);
-      __syncwarp();
-      if (lane == 0) {  // release the merge buffer for the next piece
-        ctl[1] = 0;
-        __threadfence_block();
-        ctl[2] = piece + 1;
+      const int d = threadIdx.x;  // one dim per thread, all heads
+      if (live) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float M = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mrg_ml[(w * G + g) * 2]);
+          float Ls = 0.f, A = 0.f;
+#pragma unroll
+          for (int w = 0; w < kWarps; ++w) {
+            const float f = exp2f(mrg_ml[(w * G + g) * 2] - M);
+            Ls = fmaf(f, mrg_ml[(w * G + g) * 2 + 1], Ls);
+            A = fmaf(f, mrg_acc[(w * G + g) * kD + d], A);
+          }
+          if (whole) {
+            out_seg[g * kD + d] = A / Ls;
+          } else {
+            a.part_acc[((k + j) * G + g) * kD + d] = A;
+            if (d == 0) {
+              a.part_ml[((k + j) * G + g) * 2] = M;
+              a.part_ml[((k + j) * G + g) * 2 + 1] = Ls;
+            }
+          }
+        }
       }
-      if (live && !whole && a.counters != nullptr) {
-        __threadfence();  // this piece's partial is visible before its arrival
-        __syncwarp();
+      const bool counted = live && !whole && a.counters != nullptr;
+      named_barrier(1, kThreads);
+      if (threadIdx.x == 0) {
         int seg_last = 0;
-        if (lane == 0) seg_last = atomicAdd(a.counters + j, 1) == k1 - k0;
-        seg_last = __shfl_sync(kFull, seg_last, 0);
-        if (seg_last) {
-          __threadfence();
-          merge_segment_warp<G>(a.part_ml, a.part_acc, j, k0, k1, out_seg, lane);
-          if (lane == 0) a.counters[j] = 0;  // ready for the next call
+        if (counted) {
+          __threadfence();  // the CTA's partial (ordered by the barrier) before the arrival
+          seg_last = atomicAdd(a.counters + j, 1) == k1 - k0;
+        }
+        ctl[1] = seg_last;
+      }
+      named_barrier(1, kThreads);
+      if (ctl[1]) {
+        __threadfence();
+        merge_segment<G>(a.part_ml, a.part_acc, j, k0, k1, out_seg, d);
+        if (d == 0) a.counters[j] = 0;  // ready for the next call
+      }
+    } else {
+      __syncwarp();
+      int lastw = 0;
+      if (lane == 0) {
+        __threadfence_block();
+        lastw = atomicAdd(const_cast<int*>(&ctl[1]), 1) == kWarps - 1;
+      }
+      lastw = __shfl_sync(kFull, lastw, 0);
+      if (lastw) {
+        __threadfence_block();
+        const bool live = !ctl[0];
+        if (live)
+          piece_merge<G>(mrg_acc, mrg_ml, whole, out_seg, a.part_ml, a.part_acc, k + j, lane);
+        __syncwarp();
+        if (lane == 0) {  // release the merge buffer for the next piece
+          ctl[1] = 0;
+          __threadfence_block();
+          ctl[2] = piece + 1;
+        }
+        if (live && !whole && a.counters != nullptr) {
+          __syncwarp();
+          int seg_last = 0;
+          if (lane == 0) {
+            __threadfence();  // the warp's partial (ordered by __syncwarp) before the arrival
+            seg_last = atomicAdd(a.counters + j, 1) == k1 - k0;
+          }
+          seg_last = __shfl_sync(kFull, seg_last, 0);
+          if (seg_last) {
+            __threadfence();
+            merge_segment_warp<G>(a.part_ml, a.part_acc, j, k0, k1, out_seg, lane);
+            if (lane == 0) a.counters[j] = 0;  // ready for the next call
+          }
         }
       }
     }
