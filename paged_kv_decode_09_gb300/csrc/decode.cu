@@ -111,8 +111,10 @@ struct Smem {
   static constexpr uint32_t kBar = kStages * Tiles<DT>::kStage;           // full[warp][ring]
   static constexpr uint32_t kMrgAcc = kBar + ((kStages * 8 + 15) / 16) * 16;  // f32 [warps][G][D]
   static constexpr uint32_t kMrgMl = kMrgAcc + kWarps * G * kD * 4;        // f32 [warps][G][2]
-  static constexpr uint32_t kProb = kMrgMl + kWarps * G * 2 * 4;           // f32 [warps][G][16]
-  static constexpr uint32_t kAlpha = kProb + kWarps * G * kPage * 4;       // f32 [warps][4]
+  // probabilities per warp: f16 [G][16]; q8_0 [4 blocks][G][16] (pre-scaled by V block scales)
+  static constexpr int kProbPerWarp = (DT == PKV_KV_F16 ? 1 : kD / kQBlock) * G * kPage;
+  static constexpr uint32_t kProb = kMrgMl + kWarps * G * 2 * 4;           // f32 [warps][kProbPerWarp]
+  static constexpr uint32_t kAlpha = kProb + kWarps * kProbPerWarp * 4;    // f32 [warps][4]
   static constexpr uint32_t kCtl = kAlpha + kWarps * 4 * 4;                // int [4]
   static constexpr uint32_t kRows = kCtl + 16;  // int row_start[rows + 1], lens[rows]
   static size_t bytes(int rows) { return kRows + (2 * static_cast<size_t>(rows) + 1) * 4; }
@@ -258,14 +260,12 @@ __device__ __forceinline__ void process_unit(const uint8_t* st, int nvalid, int 
     }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      // packed fp32 FMA on dim pairs: two partial sums per lane, added at the end
-      float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+      // packed fp32 FMA on dim pairs: one pair accumulator per (head, token)
+      float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        s0 = __ffma2_rn(S.q[g][e], make_float2(kf[2 * e], kf[2 * e + 1]), s0);
-        s1 = __ffma2_rn(S.q[g][4 + e], make_float2(kf[8 + 2 * e], kf[8 + 2 * e + 1]), s1);
-      }
-      v[g * 4 + j] = ((s0.x + s0.y) + (s1.x + s1.y)) * ksc;
+      for (int e = 0; e < 8; ++e)
+        s2 = __ffma2_rn(S.q[g][e], make_float2(kf[2 * e], kf[2 * e + 1]), s2);
+      v[g * 4 + j] = (s2.x + s2.y) * ksc;
     }
   }
   reduce_scores<G>(v, lane);
@@ -287,7 +287,21 @@ __device__ __forceinline__ void process_unit(const uint8_t* st, int nvalid, int 
   for (int s = 0; s < GR::kSpl; ++s) {
     const float p = exp2f(v[s] - m_new);
     psum += p;
-    prob[g_lane * kPage + t0 + s] = p;
+    if constexpr (DT == PKV_KV_F16) {
+      prob[g_lane * kPage + t0 + s] = p;
+    } else {
+      // q8_0: fold the V block scales of token t0+s into its probability:
+      // prob[block][head][token] = p * scale(V, token, block).
+      const int t = t0 + s;
+      const uint2 sc4 = *reinterpret_cast<const uint2*>(st + TL::kTile + TL::kData +
+                                                        t * (kD / kQBlock) * 2);
+      const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sc4.x));
+      const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&sc4.y));
+      prob[(0 * G + g_lane) * kPage + t] = p * s01.x;
+      prob[(1 * G + g_lane) * kPage + t] = p * s01.y;
+      prob[(2 * G + g_lane) * kPage + t] = p * s23.x;
+      prob[(3 * G + g_lane) * kPage + t] = p * s23.y;
+    }
   }
   S.l = S.l * al + psum;
   S.m = m_new;
@@ -302,27 +316,25 @@ __device__ __forceinline__ void process_unit(const uint8_t* st, int nvalid, int 
     S.acc[g][1] = __fmul2_rn(S.acc[g][1], a2);
   }
   const uint8_t* vt = st + TL::kTile;
+  // f16: prob[head][token]; q8_0: prob[block][head][token], block of this lane's dims
+  const float* pl = (DT == PKV_KV_F16) ? prob : prob + (lane >> 3) * G * kPage;
   if (nvalid == kPage) {
 #pragma unroll
     for (int t4 = 0; t4 < kPage; t4 += 4) {
       float4 p4[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) p4[g] = *reinterpret_cast<const float4*>(prob + g * kPage + t4);
+      for (int g = 0; g < G; ++g) p4[g] = *reinterpret_cast<const float4*>(pl + g * kPage + t4);
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int t = t4 + u;
         float vf[4];
-        float vsc = 1.0f;
-        if constexpr (DT == PKV_KV_F16) {
+        if constexpr (DT == PKV_KV_F16)
           f16x4_to_f32(*reinterpret_cast<const uint2*>(vt + t * 256 + lane * 8), vf);
-        } else {
+        else
           i8x4_to_f32(*reinterpret_cast<const uint32_t*>(vt + t * kD + lane * 4), vf);
-          vsc = __half2float(
-              reinterpret_cast<const __half*>(vt + TL::kData)[t * (kD / kQBlock) + (lane >> 3)]);
-        }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float p = (&p4[g].x)[u] * vsc;
+          const float p = (&p4[g].x)[u];
           const float2 p2 = make_float2(p, p);
           S.acc[g][0] = __ffma2_rn(p2, make_float2(vf[0], vf[1]), S.acc[g][0]);
           S.acc[g][1] = __ffma2_rn(p2, make_float2(vf[2], vf[3]), S.acc[g][1]);
@@ -333,17 +345,13 @@ __device__ __forceinline__ void process_unit(const uint8_t* st, int nvalid, int 
 #pragma unroll 1
     for (int t = 0; t < nvalid; ++t) {
       float vf[4];
-      float vsc = 1.0f;
-      if constexpr (DT == PKV_KV_F16) {
+      if constexpr (DT == PKV_KV_F16)
         f16x4_to_f32(*reinterpret_cast<const uint2*>(vt + t * 256 + lane * 8), vf);
-      } else {
+      else
         i8x4_to_f32(*reinterpret_cast<const uint32_t*>(vt + t * kD + lane * 4), vf);
-        vsc = __half2float(
-            reinterpret_cast<const __half*>(vt + TL::kData)[t * (kD / kQBlock) + (lane >> 3)]);
-      }
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        const float p = prob[g * kPage + t] * vsc;
+        const float p = pl[g * kPage + t];
         const float2 p2 = make_float2(p, p);
         S.acc[g][0] = __ffma2_rn(p2, make_float2(vf[0], vf[1]), S.acc[g][0]);
         S.acc[g][1] = __ffma2_rn(p2, make_float2(vf[2], vf[3]), S.acc[g][1]);
@@ -689,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
   const int tg = lane >> 3, dj = lane & 7;
   float* mrg_acc = reinterpret_cast<float*>(smem + SM::kMrgAcc);
   float* mrg_ml = reinterpret_cast<float*>(smem + SM::kMrgMl);
-  float* prob = reinterpret_cast<float*>(smem + SM::kProb) + warp * G * kPage;
+  float* prob = reinterpret_cast<float*>(smem + SM::kProb) + warp * SM::kProbPerWarp;
   float* alpha = reinterpret_cast<float*>(smem + SM::kAlpha) + warp * 4;
   const int g_lane = dj >> (3 - GR::kLog2);
   const bool head_writer = tg == 0 && (dj & (GR::kTokLanes - 1)) == 0 && (G > 1 || dj < 4);
