@@ -349,15 +349,10 @@ void oracle_combine(int n, const float *m2, const float *l, const float *acc, in
  * (row, KV head, page): segment j = i * n_kv + h holds the npg_i units of
  * (row i, head h) starting at seg_start(j) = n_kv * sum_{r<i} npg_r + h * npg_i.
  * With T = n_kv * sum_i npg_i units and C chunks requested, Ce = min(C, T)
- * base chunks are used, base chunk k covering [floor(k T / Ce),
- * floor((k + 1) T / Ce)).  When T >= 3 Ce every base chunk of n units is
- * split further into a head of n - floor(n / 3) units and a tail of
- * floor(n / 3) units (the tails are the part any CTA may take over), giving
- * 2 Ce chunks numbered head k = 2k, tail k = 2k + 1; otherwise the base
- * chunks are the chunks.  Either way the chunks tile [0, T) in order and none
- * is empty.  A segment's pieces are its intersections with the chunks;
- * first/last chunk record which chunks they are (-1, -1 for an empty
- * segment).
+ * chunks are used (so none is empty) and chunk k < Ce covers units
+ * [floor(k T / Ce), floor((k + 1) T / Ce)).  A segment's pieces are its
+ * intersections with the chunks; first/last chunk record which chunks they
+ * are (-1, -1 for an empty segment).
  *
  * Outputs: row_page_start[rows + 1] (exclusive prefix sum of npg),
  * seg_first_chunk[rows * n_kv], seg_last_chunk[rows * n_kv], *total = T. */
@@ -372,30 +367,15 @@ int oracle_plan(int num_rows, const int32_t *seq_lens, int n_kv, int num_chunks,
     }
     int64_t T = (int64_t)n_kv * row_page_start[num_rows];
     *total = T;
-    const int64_t Ce = T < num_chunks ? T : num_chunks;
-    const int split = Ce > 0 && T >= 3 * Ce;
-    /* chunk list: begin of every chunk, in order, plus T at the end */
-    int64_t nchunks = split ? 2 * Ce : Ce;
-    int64_t *begin = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nchunks + 1));
-    if (!begin) return ORACLE_BAD_ARG;
-    for (int64_t k = 0; k < Ce; ++k) {
-        int64_t b0 = k * T / Ce, b1 = (k + 1) * T / Ce;
-        if (split) {
-            begin[2 * k] = b0;
-            begin[2 * k + 1] = b1 - (b1 - b0) / 3;
-        } else {
-            begin[k] = b0;
-        }
-    }
-    begin[nchunks] = T;
     for (int i = 0; i < num_rows; ++i) {
         int64_t npg = row_page_start[i + 1] - row_page_start[i];
         for (int h = 0; h < n_kv; ++h) {
             int64_t j = (int64_t)i * n_kv + h;
             int64_t a = (int64_t)n_kv * row_page_start[i] + h * npg, b = a + npg;
             int32_t first = -1, last = -1;
-            for (int64_t k = 0; k < nchunks; ++k) {
-                int64_t c0 = begin[k], c1 = begin[k + 1];
+            const int64_t Ce = T < num_chunks ? T : num_chunks;
+            for (int64_t k = 0; k < Ce; ++k) {
+                int64_t c0 = k * T / Ce, c1 = (k + 1) * T / Ce;
                 if (a < b && c0 < c1 && c0 < b && a < c1) { /* non-empty overlap */
                     if (first < 0) first = (int32_t)k;
                     last = (int32_t)k;
@@ -405,6 +385,5 @@ int oracle_plan(int num_rows, const int32_t *seq_lens, int n_kv, int num_chunks,
             seg_last_chunk[j] = last;
         }
     }
-    free(begin);
     return ORACLE_OK;
 }

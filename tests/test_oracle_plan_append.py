@@ -1,10 +1,9 @@
 """Pins for the oracle's work split (plan) and its kv_append.
 
 Plan: units are (row, KV head, page) tiles in that order; of C chunks asked
-for, Ce = min(C, T) base chunks are used, base chunk k covering
-[floor(k T / Ce), floor((k + 1) T / Ce)); when T >= 3 Ce each splits into a
-head (n - n // 3 units) and a tail (n // 3 units); no chunk is empty; a
-segment (row, head) is split into pieces by the chunks it meets.  Pinned to hand-derived fixtures and to a
+for, Ce = min(C, T) are used, chunk k covering [floor(k T / Ce),
+floor((k + 1) T / Ce)), so none is empty; a segment (row, head) is split into
+pieces by the chunks it meets.  Pinned to hand-derived fixtures and to a
 brute-force enumeration of every unit.
 
 Append (tinyllm, "The repository currently provides": block table per active
@@ -47,17 +46,11 @@ def _enumerate(seq_lens, n_kv, C):
                 units.append(i * n_kv + h)
     T = len(units)
     Ce = min(C, T)
-    split = Ce > 0 and T >= 3 * Ce
     chunk_of = []
     for k in range(Ce):
         n = (k + 1) * T // Ce - k * T // Ce
-        assert n >= 1  # no empty base chunk
-        if split:
-            tail = n // 3
-            assert tail >= 1 and n - tail >= 1  # no empty head or tail
-            chunk_of += [2 * k] * (n - tail) + [2 * k + 1] * tail
-        else:
-            chunk_of += [k] * n
+        assert n >= 1  # no empty chunk
+        chunk_of += [k] * n
     J = len(seq_lens) * n_kv
     first, last = [-1] * J, [-1] * J
     for x, j in enumerate(units):
