@@ -11,8 +11,9 @@ L2 cache, so every step reads KV from HBM.
 
 Metric (bytes counted per step: K and V of every attended token, q, out):
   value      KV GB/s, device-resident inputs, CUDA events on the stream
-  roofline   the decode kernel's algorithmic GB/s over the mean of its per-launch
-             event times, against the measured HBM copy bandwidth
+  roofline   the decode kernel's algorithmic GB/s over its mean launch-to-launch
+             time in the timed region (the only kernel there), against the
+             measured HBM copy bandwidth
   e2e        the same metric through the C ABI with the step's inputs copied
              from pinned host memory and the output copied back, every step
   cpu_baseline  the FP64 CPU oracle on a bounded sample of the same batch
@@ -53,6 +54,10 @@ def parse_args():
     p.add_argument("--chunks", type=int, default=0, help="work chunks (0: one per resident CTA)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU baseline budget")
+    p.add_argument("--kernel", choices=["step", "append", "split_combine", "plan"], default="step",
+                   help="step: the decode step (the benchmark); the others run --steps calls of\n"
+                        "one other entry point on the workload and print its mean call time\n"
+                        "(for profiling those kernels alone; not the benchmark metric)")
     return p.parse_args()
 
 
@@ -233,22 +238,19 @@ def run_ours(args, rank, world, local):
         if st:
             raise api.PkvError(st, what, L.pkv_last_error_message().decode())
 
-    def step(layer, ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+    def step(layer):
         chk(L.pkv_decode_step(H, layer, a_q, a_k, a_v, a_bt, S, a_sl, R, NQ, scale, a_out, a_ws,
                               ws.nbytes, CH, sp), "pkv_decode_step")
-        if ev is not None:
-            ev[1].record(stream)
 
     for w in range(args.warmup):
         step(w % layers)
     torch.cuda.synchronize()
     assert pool.read_status() == 0, "device status word set during warm-up"
 
+    # The timed steps are back-to-back launches of the decode kernel on one
+    # stream, bracketed by one pair of events (an event between launches would
+    # add its own gap and break the programmatic dependent launch).
     K = args.steps
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(K)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     barrier(world)
@@ -257,13 +259,13 @@ def run_ours(args, rank, world, local):
     time.sleep(0.1)
     e0.record(stream)
     for s in range(K):
-        step(s % layers, evs[s])
+        step(s % layers)
     e1.record(stream)
     torch.cuda.synchronize()
     clock_info = clocks.stop()
     barrier(world)
     total_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    split_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    launch_ms = total_ms / K  # the only kernel in the timed region: its mean launch-to-launch time
     assert pool.read_status() == 0, "device status word set during the timed steps"
 
     # ---- end to end through the C ABI: pinned host inputs in, output out
@@ -298,7 +300,7 @@ def run_ours(args, rank, world, local):
     peak, peak_src = read_peak()
     step_s = total_ms / 1e3 / K
     value = world * nbytes / step_s / 1e9
-    achieved = nbytes / (split_ms / 1e3) / 1e9
+    achieved = nbytes / (launch_ms / 1e3) / 1e9
     tokens = int(sum(int(x) for x in wl.seq_lens))
     result = {
         "metric": "paged decode-attn KV GB/s & % of GB300 HBM peak; rows*tokens/s at 1 GPU",
@@ -330,7 +332,8 @@ def run_ours(args, rank, world, local):
                                       f"{cfg.group}>",
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (copy bandwidth)",
-            "traffic": profile_traffic(cfg.name), "mean_launch_us": round(split_ms * 1e3, 3),
+            "traffic": profile_traffic(cfg.name), "mean_launch_us": round(launch_ms * 1e3, 3),
+            "timing": "events around the K back-to-back launches of the timed region",
         },
         "e2e": {"value": round(world * nbytes / (e2e_ms / 1e3 / Ke) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
@@ -341,6 +344,55 @@ def run_ours(args, rank, world, local):
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, pool, args.cpu_seconds)
     return result
+
+
+def run_kernel(args, local):
+    """--steps calls of one entry point other than the decode step, timed with
+    events on the stream: kv_append (new K/V of every row), paged_decode_split
+    followed by paged_decode_combine, or paged_decode_plan."""
+    import numpy as np
+    import torch
+
+    from paged_kv_decode_09_gb300 import api
+    from paged_kv_decode_09_gb300 import workloads as W
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = W.draw(args.workload)
+    cfg = wl.cfg
+    layers = 2
+    pool = api.KVPool(layers, wl.num_pages, cfg.n_kv_heads, cfg.dtype, device=dev)
+    if args.kernel == "split_combine":
+        fill_pool(api, pool, layers, seed=1234)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    q, k_new, v_new = t(wl.q), t(wl.k_new), t(wl.v_new)
+    bt, sl = t(wl.block_table), t(wl.seq_lens)
+    out = torch.empty_like(q)
+    ws = api.Workspace(pool, cfg.n_q_heads, wl.rows, args.chunks)
+
+    def call(i):
+        if args.kernel == "append":
+            api.kv_append(pool, i % layers, k_new, v_new, bt, sl)
+        elif args.kernel == "split_combine":
+            api.paged_decode_split(pool, i % layers, q, bt, sl, wl.scale, out, ws)
+            api.paged_decode_combine(sl, cfg.n_q_heads, cfg.n_kv_heads, wl.bt_stride,
+                                     ws.num_chunks, ws.tensor, out)
+        else:
+            api.paged_decode_plan(sl, cfg.n_kv_heads, wl.bt_stride, ws.num_chunks)
+
+    for i in range(args.warmup):
+        call(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        call(i)
+    e1.record()
+    torch.cuda.synchronize()
+    assert pool.read_status() == 0
+    return {"kernel": args.kernel, "workload": cfg.name, "calls": args.steps,
+            "mean_call_us": round(e0.elapsed_time(e1) * 1e3 / max(1, args.steps), 3),
+            "note": "per-entry-point timing for profiling; not the benchmark metric"}
 
 
 def cpu_baseline(wl, pool, budget_s):
@@ -451,6 +503,9 @@ def main():
         # host-only: rank 0 alone times the oracle, the other ranks exit at once
         if int(os.environ.get("RANK", "0")) == 0:
             print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.kernel != "step":
+        print(json.dumps(run_kernel(args, int(os.environ.get("LOCAL_RANK", "0")))), flush=True)
         return
     rank, world, local = dist_init(args)
     result = run_ours(args, rank, world, local)

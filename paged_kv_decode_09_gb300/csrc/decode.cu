@@ -28,36 +28,49 @@
 //
 // Inside a CTA: four warps, each feeding itself.  Warp w takes units w, w+4,
 // ... of the chunk and keeps its own ring of shared-memory stages: it issues
-// the 1-D bulk async copies of its next units (K tile, then V tile, of one
-// (page, KV head)), waits on the stage's mbarrier, computes, and re-issues
-// into the stage it just read.  Each stage has one owner, so no empty
-// barriers are needed and four threads per CTA keep copies in flight.  Each
-// warp keeps a base-2 online softmax in fp32 for the G query heads of the
-// unit's KV head, sharing every K and V element it converts across the group.
-// At the end of a piece the warps leave their states in a shared merge
-// buffer; the last to arrive combines them and does the global writes,
-// while the others carry on streaming.
+// the tensor copies of its next units (K tile, then V tile, of one (page, KV
+// head), through tensor maps that apply the 128-byte swizzle, so that the
+// matrix loads below are free of bank conflicts), waits on the stage's
+// mbarrier, computes, and re-issues into the stage it just read.  Each stage
+// has one owner, so no empty barriers are needed and four threads per CTA
+// keep copies in flight.  At the end of a piece the warps leave their states
+// in a shared merge buffer; the last to arrive combines them and does the
+// global writes, while the others carry on streaming.
 //
-// Lane layout of a warp on one 16-token page (lane = 8 tg + dj):
-//   scores: lane handles tokens 4tg..4tg+3 and 16 of the 128 dims (f16: two
-//     8-dim chunks dj and dj+8; q8_0: the 16 dims 16dj..16dj+15, inside one
-//     32-wide q8_0 block), for all G heads; the 8 lanes of a token group then
-//     reduce-scatter their 4G partial dot products (3 shuffle steps), leaving
-//     each lane max(G/2, 1) complete scores of one head.
-//   values: lane owns dims 4 lane .. 4 lane + 3 of the accumulator for all G
-//     heads and walks all 16 tokens, reading the probabilities from shared
-//     memory.
+// One page on the tensor cores (warp-wide mma.sync, fp32 accumulation).  The
+// stored K and V values are exact in f16 (f16 KV, and the q8_0 codes, which
+// are integers of at most 8 bits); the fp32 operands, q (times scale*log2 e,
+// normalised per head by a power of two) and the probabilities, are each
+// split into an f16 high part and the f16 rounding of the remainder, the two
+// parts sitting in adjacent MMA columns, so a product keeps about 22
+// significant bits.  Columns n = 2g + part, g < G (up to 8 for G = 4).
+//   scores:  S[16 tokens][8 cols] = K[16 tokens][128 dims] Q^T, 8 k-steps of
+//     16 dims (q8_0: one 32-dim block = 2 k-steps into a fresh accumulator,
+//     then times the token's block scale).  Lane 4 gid + tig ends with head
+//     tig's scores of tokens gid and gid + 8 (hi + lo columns).
+//   softmax: base 2 over the page, shared by the 8 lanes of a head; the
+//     running maximum is raised (and the state rescaled) only when a page
+//     exceeds it by more than 8, so probabilities stay below 2^8.
+//   values:  O^T[128 dims][8 cols] += V^T[128 dims][16 tokens] P^T, P^T
+//     built by 4 shuffles (q8_0: times the V block scales, one B operand per
+//     block).  Lane 4 gid + tig accumulates head tig's output at 16 of the
+//     dims, hi and lo columns, summed at the end of the piece.
 #include <cmath>
 #include <cstdint>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
 
-// Build-time knobs (defaults are the tuned values): consumer warps per CTA,
-// shared-memory stages per dtype, and the minimum CTAs per SM the register
-// allocation must allow.
+// Build-time knobs (defaults are the tuned values): shared-memory stages per
+// warp for each dtype, the minimum CTAs per SM the register allocation must
+// allow, programmatic dependent launch of the decode kernel (1 on), and the
+// partial states a merge loads per round trip.
 #ifndef PKV_F16_RING
 #define PKV_F16_RING 2
 #endif
@@ -67,295 +80,362 @@ namespace pkv {
 #ifndef PKV_MIN_CTAS_PER_SM
 #define PKV_MIN_CTAS_PER_SM 3
 #endif
+#ifndef PKV_PDL
+#define PKV_PDL 1
+#endif
 #ifndef PKV_MERGE_BATCH
 #define PKV_MERGE_BATCH 8
 #endif
 
-constexpr int kWarps = 4;  // warps per CTA; the piece merge gives each lane 4 of the 128 dims
+constexpr int kWarps = 4;  // warps per CTA; the final piece merge gives each thread one dim
 constexpr int kThreads = kWarps * 32;
+static_assert(kThreads == kD, "the final piece merge maps one thread to one dim");
+
+// Tensor maps of the layer's K and V tiles (kernel parameters).
+struct TileMaps {
+  CUtensorMap k;
+  CUtensorMap v;
+};
 
 // Shared-memory stage of one unit: the K tile then the V tile of one
-// (page, KV head); q8_0 tiles are codes followed by their block scales.
+// (page, KV head), each [16 tokens][128 dims] under the 128-byte swizzle
+// (f16: two 2 KiB halves of 64 dims); q8_0 block scales in a separate area.
 template <int DT>
 struct Tiles;
 template <>
 struct Tiles<PKV_KV_F16> {
-  static constexpr uint32_t kData = kPage * kD * 2;  // 4096
+  static constexpr uint32_t kData = kPage * kD * 2;  // 4096 bytes of one K or V tile
   static constexpr uint32_t kScale = 0;
-  static constexpr uint32_t kTile = kData;
-  static constexpr uint32_t kStage = 2 * kTile;
+  static constexpr uint32_t kCodes = 2 * kData;  // K and V tiles of a stage
+  static constexpr uint32_t kScales = 0;
+  static constexpr uint32_t kTx = kCodes;  // bytes a stage's barrier waits for
   static constexpr int kRing = PKV_F16_RING;  // stages per warp
 };
 template <>
 struct Tiles<PKV_KV_Q8_0> {
   static constexpr uint32_t kData = kPage * kD;                   // 2048 codes
   static constexpr uint32_t kScale = kPage * (kD / kQBlock) * 2;  // 128 bytes of f16 scales
-  static constexpr uint32_t kTile = kData + kScale;
-  static constexpr uint32_t kStage = 2 * kTile;
+  static constexpr uint32_t kCodes = 2 * kData;
+  static constexpr uint32_t kScales = 2 * kScale;  // K scales then V scales
+  static constexpr uint32_t kTx = kCodes + kScales;
   static constexpr int kRing = PKV_Q8_RING;  // stages per warp
 };
 
-// Lane bookkeeping of the score phase for a GQA group of G query heads.
-template <int G>
-struct Group {
-  static_assert(G == 1 || G == 2 || G == 4, "group of 1, 2 or 4 query heads");
-  static constexpr int kLog2 = G == 1 ? 0 : (G == 2 ? 1 : 2);
-  static constexpr int kVals = 4 * G;              // partial dot products per lane
-  static constexpr int kSpl = G >= 2 ? G / 2 : 1;  // complete scores per lane afterwards
-  static constexpr int kTokLanes = 4 / kSpl;       // lanes (low dj bits) splitting a head's 4 tokens
-};
-
+// Offsets from a 1024-byte aligned base.  The tiles come first (the swizzle
+// atom is 1024 bytes), then scales, barriers, the merge buffer, control
+// words and the plan.
 template <int DT, int G>
 struct Smem {
   static constexpr int kStages = kWarps * Tiles<DT>::kRing;
-  static constexpr uint32_t kBar = kStages * Tiles<DT>::kStage;           // full[warp][ring]
+  static constexpr uint32_t kAlign = 1024;
+  static constexpr uint32_t kScl = kStages * Tiles<DT>::kCodes;           // [warp][ring][K, V]
+  static constexpr uint32_t kBar = kScl + kStages * Tiles<DT>::kScales;   // full[warp][ring]
   static constexpr uint32_t kMrgAcc = kBar + ((kStages * 8 + 15) / 16) * 16;  // f32 [warps][G][D]
   static constexpr uint32_t kMrgMl = kMrgAcc + kWarps * G * kD * 4;        // f32 [warps][G][2]
-  // probabilities per warp: f16 [G][16]; q8_0 [4 blocks][G][16] (pre-scaled by V block scales)
-  static constexpr int kProbPerWarp = (DT == PKV_KV_F16 ? 1 : kD / kQBlock) * G * kPage;
-  static constexpr uint32_t kProb = kMrgMl + kWarps * G * 2 * 4;           // f32 [warps][kProbPerWarp]
-  static constexpr uint32_t kAlpha = kProb + kWarps * kProbPerWarp * 4;    // f32 [warps][4]
-  static constexpr uint32_t kCtl = kAlpha + kWarps * 4 * 4;                // int [4]
+  static constexpr uint32_t kCtl = kMrgMl + kWarps * G * 2 * 4;            // int [4]
   static constexpr uint32_t kRows = kCtl + 16;  // int row_start[rows + 1], lens[rows]
-  static size_t bytes(int rows) { return kRows + (2 * static_cast<size_t>(rows) + 1) * 4; }
-  static_assert(kMrgAcc % 16 == 0 && kMrgMl % 16 == 0 && kProb % 16 == 0 && kAlpha % 16 == 0,
+  static size_t bytes(int rows) {
+    return kAlign + kRows + (2 * static_cast<size_t>(rows) + 1) * 4;  // kAlign: base alignment slack
+  }
+  static_assert(Tiles<DT>::kCodes % 1024 == 0, "tile stages keep the swizzle atom alignment");
+  static_assert(kMrgAcc % 16 == 0 && kMrgMl % 16 == 0 && kCtl % 16 == 0,
                 "vector accesses need 16-byte aligned regions");
 };
 
-// ---------------------------------------------------------- conversions ----
-__device__ __forceinline__ void f16x8_to_f32(const uint4& u, float* f) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 v = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-    f[2 * i] = v.x;
-    f[2 * i + 1] = v.y;
+// ------------------------------------------------------------ operands ----
+// Byte offset of the 16-byte chunk c (8 f16 or 16 int8 values) of token row t
+// in a swizzled tile: 128-byte rows, chunk index xor (row mod 8); f16 tiles
+// keep dims 64..127 in a second 2 KiB half.
+template <int DT>
+__device__ __forceinline__ uint32_t tile_offset(int t, int c) {
+  if constexpr (DT == PKV_KV_F16)
+    return (c >> 3) * 2048 + t * 128 + (((c & 7) ^ (t & 7)) << 4);
+  else
+    return t * 128 + ((c ^ (t & 7)) << 4);
+}
+
+// Two signed 8-bit codes of `u` (the word xor 0x80808080, i.e. code + 128 in
+// each byte) as an exact f16 pair: the bytes chosen by `sel` go into the low
+// mantissa byte of 1024 (0x64xx = 1024 + code + 128), then 1152 is
+// subtracted in f16.
+template <uint32_t kSel>
+__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t u) {
+  const uint32_t biased = __byte_perm(u, 0x64646464u, kSel);
+  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&biased),
+                            __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+constexpr uint32_t kSelB01 = 0x4140, kSelB23 = 0x4342, kSelB02 = 0x4240, kSelB13 = 0x4341;
+
+// The f16 part (`lo` false: the rounding of x; true: the rounding of the
+// remainder) of a pair, low half x0.
+__device__ __forceinline__ uint32_t split_f16x2(float x0, float x1, bool lo) {
+  __half2 h = __floats2half2_rn(x0, x1);
+  if (lo) {
+    const float2 f = __half22float2(h);
+    h = __floats2half2_rn(x0 - f.x, x1 - f.y);
   }
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-__device__ __forceinline__ void f16x4_to_f32(const uint2& u, float* f) {
-  const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
-  const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
-  f[0] = a.x;
-  f[1] = a.y;
-  f[2] = b.x;
-  f[3] = b.y;
-}
-
-// Four signed bytes to floats, exactly: bias each byte to b + 128 (xor 0x80),
-// place it in the low mantissa byte of 2^23 (the float 2^23 + b + 128), and
-// subtract 2^23 + 128 -- one byte permute per value and one packed subtract
-// per pair instead of integer-to-float conversions.
-__device__ __forceinline__ void i8x4_to_f32(uint32_t w, float* f) {
-  const uint32_t u = w ^ 0x80808080u;
-  const float2 bias = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
-  const float2 lo = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
-                                           __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441))),
-                               bias);
-  const float2 hi = __fadd2_rn(make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
-                                           __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443))),
-                               bias);
-  f[0] = lo.x;
-  f[1] = lo.y;
-  f[2] = hi.x;
-  f[3] = hi.y;
-}
-
-// ------------------------------------------------------- warp reductions ----
-// One reduce-scatter step over lane bit `mask`: N values in, N/2 out.  Lanes
-// with the bit set keep the upper half, the others the lower half, each
-// adding its partner's copy.
-template <int N>
-__device__ __forceinline__ void rs_step(float* v, int mask, int lane) {
-  const bool up = (lane & mask) != 0;
-#pragma unroll
-  for (int k = 0; k < N / 2; ++k) {
-    const float send = up ? v[k] : v[k + N / 2];
-    const float keep = up ? v[k + N / 2] : v[k];
-    v[k] = keep + __shfl_xor_sync(kFull, send, mask);
-  }
-}
-
-// Full dot products of the 8 lanes of a token group: v[g*4 + j] (token
-// 4tg + j, head g) in, Group<G>::kSpl complete scores out in v[0..kSpl): head
-// dj >> (3 - log2 G), tokens 4tg + (dj & (kTokLanes-1)) * kSpl + s.
-template <int G>
-__device__ __forceinline__ void reduce_scores(float* v, int lane) {
-  if constexpr (G == 1) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) v[k] += __shfl_xor_sync(kFull, v[k], 4);
-    rs_step<4>(v, 2, lane);
-    rs_step<2>(v, 1, lane);
-  } else {
-    rs_step<4 * G>(v, 4, lane);
-    rs_step<2 * G>(v, 2, lane);
-    rs_step<G>(v, 1, lane);
-  }
-}
-
-// Sum (or max) over the lanes holding distinct tokens of the lane's head.
-template <int G>
-__device__ __forceinline__ float head_sum(float x) {
-#pragma unroll
-  for (int m = 1; m < Group<G>::kTokLanes; m <<= 1) x += __shfl_xor_sync(kFull, x, m);
-  x += __shfl_xor_sync(kFull, x, 8);
-  x += __shfl_xor_sync(kFull, x, 16);
-  return x;
-}
-template <int G>
-__device__ __forceinline__ float head_max(float x) {
-#pragma unroll
-  for (int m = 1; m < Group<G>::kTokLanes; m <<= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, m));
-  x = fmaxf(x, __shfl_xor_sync(kFull, x, 8));
-  x = fmaxf(x, __shfl_xor_sync(kFull, x, 16));
-  return x;
-}
-
-// Per-consumer-warp online softmax state for one piece.
-template <int G>
+// Per-warp online softmax state for one piece.
 struct WarpState {
-  float2 q[G][8];    // this lane's 16 dims of each query head (pairs), times scale*log2(e)
-  float m;           // running max (base 2) of the lane's head
-  float l;           // running sum of the lane's own tokens (reduced at the end)
-  float2 acc[G][2];  // dims 4 lane .. 4 lane + 3 of each head (pairs)
+  uint32_t qb[8][2];  // B operand of the scores per k-step: column gid (head gid/2, part gid%2)
+  float qexp;         // 2^e of head tig: undoes its power-of-two normalisation
+  float m;            // running max (base 2) of head tig, equal on its 8 lanes
+  float l;            // this lane's share of head tig's sum of probabilities
+  float o[8][4];      // O^T accumulators: dims (see dim_of) x columns (tig, hi), (tig, lo)
+  int ve;             // q8_0: biased f32 exponent bound of the piece's V block scales so far
 };
 
-// The dims of q a lane's 16 score-phase registers hold.
+// The P operand is scaled by a power of two so that its f16 parts stay
+// normal: f16 KV by 2^7 (p <= 2^8, so P <= 2^15); q8_0, where P carries the V
+// block scale, by 2^(7 - x) with 2^x > every V scale of the piece so far
+// (raised, with the accumulators rescaled, when a page exceeds it).  O holds
+// the scaled sums; o_scale() undoes it.
+constexpr int kPShift = 7;
 template <int DT>
-__device__ __forceinline__ int q_dim(int dj, int e) {
+__device__ __forceinline__ float o_scale(const WarpState& S) {
   if constexpr (DT == PKV_KV_F16)
-    return (e < 8) ? dj * 8 + e : 64 + dj * 8 + (e - 8);
+    return 1.0f / (1 << kPShift);
   else
-    return dj * 16 + e;
+    return exp2f(static_cast<float>(S.ve - 126 - kPShift));  // 2^(x - 7), x = ve - 126
 }
 
-// Process one staged (page, KV head) unit of nvalid tokens (1..16).
+// The dim of accumulator o[r][e] (e = 0, 2; e + 1 is its lo column) in lane
+// 4 gid + tig.
+template <int DT>
+__device__ __forceinline__ int dim_of(int r, int e, int gid) {
+  if constexpr (DT == PKV_KV_F16)
+    return 16 * r + gid + (e ? 8 : 0);
+  else
+    return 16 * r + 2 * gid + (e ? 1 : 0);
+}
+
+// Load head (gid/2)'s query for a piece into the lane's B fragments: the
+// dims of k-step ks are 16ks + 2tig + {0,1} and 16ks + 2tig + 8 + {0,1}
+// (f16) or 16ks + 4tig + {0,1} and {2,3} (q8_0, matching how the codes are
+// placed in the A fragments).  Each head is scaled by 2^-e so that its
+// largest |q| lies in [2^13, 2^14) and both f16 parts stay normal.
 template <int DT, int G>
-__device__ __forceinline__ void process_unit(const uint8_t* st, int nvalid, int lane,
-                                             WarpState<G>& S, float* prob, float* alpha) {
-  using GR = Group<G>;
-  using TL = Tiles<DT>;
-  const int tg = lane >> 3, dj = lane & 7;
-
-  // ---- scores: 4 tokens x 16 dims x G heads per lane
-  float v[GR::kVals];
+__device__ __forceinline__ void load_query(const float* qrow, float qscale, int lane,
+                                           WarpState& S) {
+  const int gid = lane >> 2, tig = lane & 3, g2 = gid >> 1;
+  const bool lo = (gid & 1) != 0;
+  float v[32];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int t = tg * 4 + j;
-    float kf[16];
-    float ksc = 1.0f;
-    if constexpr (DT == PKV_KV_F16) {
-      const uint4 a = *reinterpret_cast<const uint4*>(st + t * 256 + dj * 16);
-      const uint4 b = *reinterpret_cast<const uint4*>(st + t * 256 + 128 + dj * 16);
-      f16x8_to_f32(a, kf);
-      f16x8_to_f32(b, kf + 8);
-    } else {
-      const uint4 c = *reinterpret_cast<const uint4*>(st + t * kD + dj * 16);
-      i8x4_to_f32(c.x, kf);
-      i8x4_to_f32(c.y, kf + 4);
-      i8x4_to_f32(c.z, kf + 8);
-      i8x4_to_f32(c.w, kf + 12);
-      const __half* sc = reinterpret_cast<const __half*>(st + TL::kData);
-      ksc = __half2float(sc[t * (kD / kQBlock) + (dj >> 1)]);
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      // packed fp32 FMA on dim pairs: one pair accumulator per (head, token)
-      float2 s2 = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        s2 = __ffma2_rn(S.q[g][e], make_float2(kf[2 * e], kf[2 * e + 1]), s2);
-      v[g * 4 + j] = (s2.x + s2.y) * ksc;
-    }
-  }
-  reduce_scores<G>(v, lane);
-
-  // ---- online softmax of the lane's head over this page
-  const int g_lane = dj >> (3 - GR::kLog2);
-  const int t0 = tg * 4 + (dj & (GR::kTokLanes - 1)) * GR::kSpl;
-  float mx = -INFINITY;
-#pragma unroll
-  for (int s = 0; s < GR::kSpl; ++s) {
-    if (t0 + s >= nvalid) v[s] = -INFINITY;
-    mx = fmaxf(mx, v[s]);
-  }
-  mx = head_max<G>(mx);
-  const float m_new = fmaxf(S.m, mx);
-  const float al = exp2f(S.m - m_new);
-  float psum = 0.f;
-#pragma unroll
-  for (int s = 0; s < GR::kSpl; ++s) {
-    const float p = exp2f(v[s] - m_new);
-    psum += p;
-    if constexpr (DT == PKV_KV_F16) {
-      prob[g_lane * kPage + t0 + s] = p;
-    } else {
-      // q8_0: fold the V block scales of token t0+s into its probability:
-      // prob[block][head][token] = p * scale(V, token, block).
-      const int t = t0 + s;
-      const uint2 sc4 = *reinterpret_cast<const uint2*>(st + TL::kTile + TL::kData +
-                                                        t * (kD / kQBlock) * 2);
-      const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(&sc4.x));
-      const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(&sc4.y));
-      prob[(0 * G + g_lane) * kPage + t] = p * s01.x;
-      prob[(1 * G + g_lane) * kPage + t] = p * s01.y;
-      prob[(2 * G + g_lane) * kPage + t] = p * s23.x;
-      prob[(3 * G + g_lane) * kPage + t] = p * s23.y;
-    }
-  }
-  S.l = S.l * al + psum;
-  S.m = m_new;
-  if (tg == 0 && (dj & (GR::kTokLanes - 1)) == 0) alpha[g_lane] = al;
-  __syncwarp();
-
-  // ---- values: acc[g][dims of lane] = acc * alpha + sum_t p[g][t] V[t]
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const float2 a2 = make_float2(alpha[g], alpha[g]);
-    S.acc[g][0] = __fmul2_rn(S.acc[g][0], a2);
-    S.acc[g][1] = __fmul2_rn(S.acc[g][1], a2);
-  }
-  const uint8_t* vt = st + TL::kTile;
-  // f16: prob[head][token]; q8_0: prob[block][head][token], block of this lane's dims
-  const float* pl = (DT == PKV_KV_F16) ? prob : prob + (lane >> 3) * G * kPage;
-  if (nvalid == kPage) {
-#pragma unroll
-    for (int t4 = 0; t4 < kPage; t4 += 4) {
-      float4 p4[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) p4[g] = *reinterpret_cast<const float4*>(pl + g * kPage + t4);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int t = t4 + u;
-        float vf[4];
-        if constexpr (DT == PKV_KV_F16)
-          f16x4_to_f32(*reinterpret_cast<const uint2*>(vt + t * 256 + lane * 8), vf);
-        else
-          i8x4_to_f32(*reinterpret_cast<const uint32_t*>(vt + t * kD + lane * 4), vf);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float p = (&p4[g].x)[u];
-          const float2 p2 = make_float2(p, p);
-          S.acc[g][0] = __ffma2_rn(p2, make_float2(vf[0], vf[1]), S.acc[g][0]);
-          S.acc[g][1] = __ffma2_rn(p2, make_float2(vf[2], vf[3]), S.acc[g][1]);
-        }
+  for (int ks = 0; ks < 8; ++ks) {
+    if (g2 < G) {
+      const float* qh = qrow + g2 * kD;
+      if constexpr (DT == PKV_KV_F16) {
+        const float2 x = __ldg(reinterpret_cast<const float2*>(qh + 16 * ks + 2 * tig));
+        const float2 y = __ldg(reinterpret_cast<const float2*>(qh + 16 * ks + 8 + 2 * tig));
+        v[4 * ks] = x.x;
+        v[4 * ks + 1] = x.y;
+        v[4 * ks + 2] = y.x;
+        v[4 * ks + 3] = y.y;
+      } else {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(qh + 16 * ks + 4 * tig));
+        v[4 * ks] = x.x;
+        v[4 * ks + 1] = x.y;
+        v[4 * ks + 2] = x.z;
+        v[4 * ks + 3] = x.w;
       }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[4 * ks + e] = 0.f;
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    v[e] *= qscale;
+    amax = fmaxf(amax, fabsf(v[e]));
+  }
+  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+  int e2 = 0;
+  if (amax > 0.f && amax <= 3.0e38f) {
+    int ex;
+    frexpf(amax, &ex);  // amax in [2^(ex-1), 2^ex)
+    e2 = ex - 14;
+  }
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    S.qb[ks][0] = split_f16x2(ldexpf(v[4 * ks], -e2), ldexpf(v[4 * ks + 1], -e2), lo);
+    S.qb[ks][1] = split_f16x2(ldexpf(v[4 * ks + 2], -e2), ldexpf(v[4 * ks + 3], -e2), lo);
+  }
+  // lane 8 tig holds head tig (gid = 2 tig)
+  S.qexp = ldexpf(1.0f, __shfl_sync(kFull, e2, 8 * tig));
+}
+
+// Process one staged (page, KV head) unit of nvalid tokens (1..16): tiles at
+// shared address `st` (K, then V at + kData), q8_0 scales at `sc` (K, then V
+// at + kScale).  Rows nvalid..15 of the tiles hold whatever the pool holds
+// there (possibly NaN): they are masked out of the scores, and f16 V rows are
+// zeroed before the values MMA.
+template <int DT, int G>
+__device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int nvalid, int lane,
+                                             WarpState& S) {
+  using TL = Tiles<DT>;
+  const int gid = lane >> 2, tig = lane & 3;
+  // ldmatrix row addresses: lane 8j + r gives row r of matrix j = token
+  // r + 8 (j & 1), chunk 2c + (j >> 1) at k-step (or dim block) c.
+  const int ld_tok = (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int ld_chunk = lane >> 4;
+  const uint32_t kt = smem_addr(st), vt = kt + TL::kData;
+
+  // ---- scores
+  float s0, s1;
+  if constexpr (DT == PKV_KV_F16) {
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(kt + tile_offset<DT>(ld_tok, 2 * ks + ld_chunk), a0, a1, a2, a3);
+      mma_16816(c, a0, a1, a2, a3, S.qb[ks][0], S.qb[ks][1]);
+    }
+    s0 = c[0] + c[1];
+    s1 = c[2] + c[3];
+  } else {
+    // K block scales of tokens gid and gid + 8
+    const uint2 k0 = *reinterpret_cast<const uint2*>(sc + gid * 8);
+    const uint2 k1 = *reinterpret_cast<const uint2*>(sc + (gid + 8) * 8);
+    const float2 k0a = __half22float2(*reinterpret_cast<const __half2*>(&k0.x));
+    const float2 k0b = __half22float2(*reinterpret_cast<const __half2*>(&k0.y));
+    const float2 k1a = __half22float2(*reinterpret_cast<const __half2*>(&k1.x));
+    const float2 k1b = __half22float2(*reinterpret_cast<const __half2*>(&k1.y));
+    const float ks0[4] = {k0a.x, k0a.y, k0b.x, k0b.y}, ks1[4] = {k1a.x, k1a.y, k1b.x, k1b.y};
+    s0 = 0.f;
+    s1 = 0.f;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      uint32_t w0, w1, w2, w3;  // tokens gid, gid+8 of chunk 2b; the same of chunk 2b+1
+      ldsm_x4(kt + tile_offset<DT>(ld_tok, 2 * b + ld_chunk), w0, w1, w2, w3);
+      w0 ^= 0x80808080u;
+      w1 ^= 0x80808080u;
+      w2 ^= 0x80808080u;
+      w3 ^= 0x80808080u;
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_16816(c, codes_to_f16x2<kSelB01>(w0), codes_to_f16x2<kSelB01>(w1),
+                codes_to_f16x2<kSelB23>(w0), codes_to_f16x2<kSelB23>(w1), S.qb[2 * b][0],
+                S.qb[2 * b][1]);
+      mma_16816(c, codes_to_f16x2<kSelB01>(w2), codes_to_f16x2<kSelB01>(w3),
+                codes_to_f16x2<kSelB23>(w2), codes_to_f16x2<kSelB23>(w3), S.qb[2 * b + 1][0],
+                S.qb[2 * b + 1][1]);
+      s0 = fmaf(ks0[b], c[0] + c[1], s0);
+      s1 = fmaf(ks1[b], c[2] + c[3], s1);
+    }
+  }
+  s0 = gid < nvalid ? s0 * S.qexp : -INFINITY;
+  s1 = gid + 8 < nvalid ? s1 * S.qexp : -INFINITY;
+
+  // ---- online softmax of head tig over the page (its 8 lanes: xor 4, 8, 16)
+  float mx = fmaxf(s0, s1);
+  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 4));
+  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
+  mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
+  const bool grow = mx > S.m + 8.0f;  // true on the first page (m = -inf)
+  if (__any_sync(kFull, grow)) {
+    const float m_new = grow ? mx : S.m;
+    const float al = exp2f(S.m - m_new);  // 1 if unchanged, 0 from -inf
+    S.l *= al;
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) S.o[r][e] *= al;
+    S.m = m_new;
+  }
+  const float p0 = exp2f(s0 - S.m), p1 = exp2f(s1 - S.m);
+  S.l += p0 + p1;
+
+  // ---- P^T operand: column gid (head gid/2, part gid%2) at tokens 2tig,
+  // 2tig+1 (b0) and 2tig+8, 2tig+9 (b1); lane 8 tig + g holds head g's
+  // tokens 2tig and 2tig + 8, lane 8 tig + 4 + g tokens 2tig+1 and 2tig+9.
+  const int g2 = gid >> 1;
+  const bool lo = (gid & 1) != 0;
+  const int src = 8 * tig + (g2 & 3);
+  float pa = __shfl_sync(kFull, p0, src), pb = __shfl_sync(kFull, p0, src + 4);
+  float pc = __shfl_sync(kFull, p1, src), pd = __shfl_sync(kFull, p1, src + 4);
+  if (g2 >= G) pa = pb = pc = pd = 0.f;
+  const int t0 = 2 * tig;
+
+  // ---- values
+  if constexpr (DT == PKV_KV_F16) {
+    if (nvalid < kPage) {  // zero the V rows past the valid tokens (NaN * 0 is NaN)
+      for (int x = lane; x < (kPage - nvalid) * 16; x += 32) {
+        const int t = nvalid + (x >> 4), c = x & 15;
+        *reinterpret_cast<uint4*>(st + TL::kData + (c >> 3) * 2048 + t * 128 + (c & 7) * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+      __syncwarp();
+    }
+    constexpr float kUp = static_cast<float>(1 << kPShift);
+    const uint32_t b0 = split_f16x2(pa * kUp, pb * kUp, lo), b1 = split_f16x2(pc * kUp, pd * kUp, lo);
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      uint32_t w0, w1, w2, w3;  // (tokens 0-7 | 8-15) x (chunk 2mt | 2mt+1), transposed
+      ldsm_x4_trans(vt + tile_offset<DT>(ld_tok, 2 * mt + ld_chunk), w0, w1, w2, w3);
+      mma_16816(S.o[mt], w0, w2, w1, w3, b0, b1);
     }
   } else {
-#pragma unroll 1
-    for (int t = 0; t < nvalid; ++t) {
-      float vf[4];
-      if constexpr (DT == PKV_KV_F16)
-        f16x4_to_f32(*reinterpret_cast<const uint2*>(vt + t * 256 + lane * 8), vf);
-      else
-        i8x4_to_f32(*reinterpret_cast<const uint32_t*>(vt + t * kD + lane * 4), vf);
+    // V block scales of tokens 2tig, 2tig+1 and 2tig+8, 2tig+9 (4 per token)
+    const uint4 va = *reinterpret_cast<const uint4*>(sc + TL::kScale + t0 * 8);
+    const uint4 vb = *reinterpret_cast<const uint4*>(sc + TL::kScale + (t0 + 8) * 8);
+    const __half* ha = reinterpret_cast<const __half*>(&va);
+    const __half* hb = reinterpret_cast<const __half*>(&vb);
+    // masked tokens have p = 0, but their scales may be NaN: they are left
+    // out of the scale bound (fmaxf drops NaN) and their P is set to 0
+    const bool ok0 = t0 < nvalid, ok1 = t0 + 1 < nvalid, ok2 = t0 + 8 < nvalid,
+               ok3 = t0 + 9 < nvalid;
+    float vs[16];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float p = pl[g * kPage + t];
-        const float2 p2 = make_float2(p, p);
-        S.acc[g][0] = __ffma2_rn(p2, make_float2(vf[0], vf[1]), S.acc[g][0]);
-        S.acc[g][1] = __ffma2_rn(p2, make_float2(vf[2], vf[3]), S.acc[g][1]);
-      }
+    for (int b = 0; b < 4; ++b) {
+      vs[b] = ok0 ? __half2float(ha[b]) : 0.f;
+      vs[4 + b] = ok1 ? __half2float(ha[4 + b]) : 0.f;
+      vs[8 + b] = ok2 ? __half2float(hb[b]) : 0.f;
+      vs[12 + b] = ok3 ? __half2float(hb[4 + b]) : 0.f;
+    }
+    float vmax = 0.f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e) vmax = fmaxf(vmax, fabsf(vs[e]));
+    vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, 1));  // the page's 16 tokens: over tig
+    vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, 2));
+    // biased exponent of vmax: vmax < 2^(ve - 126); raise the piece's bound
+    const int ve = static_cast<int>((__float_as_uint(vmax) >> 23) & 0xff);
+    if (ve > S.ve) {  // warp-uniform
+      const float r = exp2f(static_cast<float>(S.ve - ve));  // 0 on the first page
+#pragma unroll
+      for (int rr = 0; rr < 8; ++rr)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) S.o[rr][e] *= r;
+      S.ve = ve;
+    }
+    // 2^(7 - x); every scale so far is 0 while ve is 0 (f16 scales as f32
+    // have biased exponents of at least 103, so the power stays finite)
+    const float up = S.ve ? exp2f(static_cast<float>(kPShift + 126 - S.ve)) : 0.f;
+    pa *= up;
+    pb *= up;
+    pc *= up;
+    pd *= up;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const float x0 = pa * vs[b];
+      const float x1 = pb * vs[4 + b];
+      const float x2 = pc * vs[8 + b];
+      const float x3 = pd * vs[12 + b];
+      const uint32_t b0 = split_f16x2(x0, x1, lo), b1 = split_f16x2(x2, x3, lo);
+      uint32_t w0, w1, w2, w3;  // (tokens 0-7 | 8-15) x (chunk 2b | 2b+1), 16-bit transposed
+      ldsm_x4_trans(vt + tile_offset<DT>(ld_tok, 2 * b + ld_chunk), w0, w1, w2, w3);
+      w0 ^= 0x80808080u;
+      w1 ^= 0x80808080u;
+      w2 ^= 0x80808080u;
+      w3 ^= 0x80808080u;
+      // row gid <- dim 2gid of the chunk (bytes 0, 2), row gid + 8 <- dim 2gid+1 (bytes 1, 3)
+      mma_16816(S.o[2 * b], codes_to_f16x2<kSelB02>(w0), codes_to_f16x2<kSelB13>(w0),
+                codes_to_f16x2<kSelB02>(w1), codes_to_f16x2<kSelB13>(w1), b0, b1);
+      mma_16816(S.o[2 * b + 1], codes_to_f16x2<kSelB02>(w2), codes_to_f16x2<kSelB13>(w2),
+                codes_to_f16x2<kSelB02>(w3), codes_to_f16x2<kSelB13>(w3), b0, b1);
     }
   }
   __syncwarp();
@@ -577,12 +657,15 @@ __device__ __forceinline__ bool wait_merge_buffer(volatile int* ctl, int piece) 
 // --------------------------------------------------------------- kernel ----
 template <int DT, int G>
 __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
-    paged_decode_kernel(const DecodeArgs a) {
+    paged_decode_kernel(const __grid_constant__ DecodeArgs a,
+                        const __grid_constant__ TileMaps maps) {
   using TL = Tiles<DT>;
   using SM = Smem<DT, G>;
-  using GR = Group<G>;
   constexpr int R = TL::kRing;
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  // the swizzled tiles need a 1024-byte aligned base (the launch adds the slack)
+  uint8_t* smem = smem_raw + ((SM::kAlign - (smem_addr(smem_raw) & (SM::kAlign - 1))) &
+                              (SM::kAlign - 1));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // [0] abort  [1] warps arrived at the current piece end  [2] merge-buffer generation
@@ -590,7 +673,8 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
   int* row_start = reinterpret_cast<int*>(smem + SM::kRows);
   int* lens = row_start + a.num_rows + 1;
   const uint32_t bar0 = smem_addr(smem + SM::kBar) + warp * R * 8;  // this warp's barriers
-  uint8_t* ring = smem + static_cast<size_t>(warp) * R * TL::kStage;  // this warp's stages
+  uint8_t* ring = smem + static_cast<size_t>(warp) * R * TL::kCodes;  // this warp's tiles
+  uint8_t* ring_sc = smem + SM::kScl + static_cast<size_t>(warp) * R * TL::kScales;  // q8_0 scales
 
   if (threadIdx.x == 0) {
     ctl[0] = 0;
@@ -601,6 +685,13 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
     for (int s = 0; s < R; ++s) mbar_init(bar0 + 8 * s, 1);
     fence_mbar_init();
   }
+  // Under programmatic dependent launch this grid may start while the
+  // previous kernel of the stream still runs: nothing in global memory is
+  // touched before that kernel has completed and its writes are visible.
+  // The next kernel of the stream may then be scheduled at once (its blocks
+  // find room as ours exit).
+  grid_dependency_wait();
+  grid_launch_dependents();
   plan_rows(a.seq_lens, a.num_rows, a.bt_stride, blockIdx.x == 0 ? a.status : nullptr, lens,
             row_start);
 
@@ -679,31 +770,33 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
     if (lane == 0) {
       const int s = u % R;
       const uint32_t bar = bar0 + 8 * s;
-      const uint32_t dst = smem_addr(ring + s * TL::kStage);
-      const size_t unit = static_cast<size_t>(pg) * a.n_kv + hh;
-      mbar_arrive_expect_tx(bar, TL::kStage);
-      bulk_g2s(dst, a.k_data + unit * TL::kData, TL::kData, bar, policy);
-      if constexpr (DT == PKV_KV_Q8_0)
-        bulk_g2s(dst + TL::kData, a.k_scales + unit * TL::kScale, TL::kScale, bar, policy);
-      bulk_g2s(dst + TL::kTile, a.v_data + unit * TL::kData, TL::kData, bar, policy);
-      if constexpr (DT == PKV_KV_Q8_0)
-        bulk_g2s(dst + TL::kTile + TL::kData, a.v_scales + unit * TL::kScale, TL::kScale, bar,
-                 policy);
+      const uint32_t dst = smem_addr(ring + s * TL::kCodes);
+      const int z = pg * a.n_kv + hh;  // tile index (the host checks num_pages * n_kv < 2^31)
+      mbar_arrive_expect_tx(bar, TL::kTx);
+      if constexpr (DT == PKV_KV_F16) {
+        tma_load_3d(dst, &maps.k, 0, 0, z, bar, policy);
+        tma_load_3d(dst + 2048, &maps.k, 64, 0, z, bar, policy);
+        tma_load_3d(dst + TL::kData, &maps.v, 0, 0, z, bar, policy);
+        tma_load_3d(dst + TL::kData + 2048, &maps.v, 64, 0, z, bar, policy);
+      } else {
+        const uint32_t sdst = smem_addr(ring_sc + s * TL::kScales);
+        const size_t unit = static_cast<size_t>(z);
+        tma_load_3d(dst, &maps.k, 0, 0, z, bar, policy);
+        bulk_g2s(sdst, a.k_scales + unit * TL::kScale, TL::kScale, bar, policy);
+        tma_load_3d(dst + TL::kData, &maps.v, 0, 0, z, bar, policy);
+        bulk_g2s(sdst + TL::kScale, a.v_scales + unit * TL::kScale, TL::kScale, bar, policy);
+      }
     }
     ++issued;
   };
   while (issued < n_units && issued < R) issue();
 
-  const int tg = lane >> 3, dj = lane & 7;
+  const int gid = lane >> 2, tig = lane & 3;
   float* mrg_acc = reinterpret_cast<float*>(smem + SM::kMrgAcc);
   float* mrg_ml = reinterpret_cast<float*>(smem + SM::kMrgMl);
-  float* prob = reinterpret_cast<float*>(smem + SM::kProb) + warp * SM::kProbPerWarp;
-  float* alpha = reinterpret_cast<float*>(smem + SM::kAlpha) + warp * 4;
-  const int g_lane = dj >> (3 - GR::kLog2);
-  const bool head_writer = tg == 0 && (dj & (GR::kTokLanes - 1)) == 0 && (G > 1 || dj < 4);
   bool aborted = false;
   int consumed = 0;
-  WarpState<G> S;
+  WarpState S;
 
   int piece = 0;
   for (long long x = c_begin; x < c_end; ++piece) {
@@ -718,20 +811,14 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
     const long long j = static_cast<long long>(i) * a.n_kv + h;
     const int k0 = chunk_of(seg_start, T, C), k1 = chunk_of(seg_end - 1, T, C);
 
-    const float* qrow = a.q + (static_cast<long long>(i) * a.n_q + h * G) * kD;
+    load_query<DT, G>(a.q + (static_cast<long long>(i) * a.n_q + h * G) * kD, a.qscale, lane, S);
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
+    for (int r = 0; r < 8; ++r)
 #pragma unroll
-      for (int e = 0; e < 16; e += 4) {
-        const float4 f = __ldg(reinterpret_cast<const float4*>(qrow + g * kD + q_dim<DT>(dj, e)));
-        S.q[g][e / 2] = make_float2(f.x * a.qscale, f.y * a.qscale);
-        S.q[g][e / 2 + 1] = make_float2(f.z * a.qscale, f.w * a.qscale);
-      }
-      S.acc[g][0] = make_float2(0.f, 0.f);
-      S.acc[g][1] = make_float2(0.f, 0.f);
-    }
+      for (int e = 0; e < 4; ++e) S.o[r][e] = 0.f;
     S.m = -INFINITY;
     S.l = 0.f;
+    S.ve = 0;
 
     const int r = static_cast<int>((x - c_begin) % kWarps);
     for (long long pos = x + ((warp - r + kWarps) % kWarps); pos < b; pos += kWarps) {
@@ -749,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
       }
       consumed = u + 1;
       const int nvalid = min(kPage, L - static_cast<int>(pos - seg_start) * kPage);
-      process_unit<DT, G>(ring + s * TL::kStage, nvalid, lane, S, prob, alpha);
+      process_unit<DT, G>(ring + s * TL::kCodes, ring_sc + s * TL::kScales, nvalid, lane, S);
       if (issued < n_units) issue();
     }
 
@@ -757,7 +844,10 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
     // For every piece but the chunk's last, the last warp to arrive merges
     // while the others go on streaming; the chunk's last piece is merged by
     // the whole CTA, since all its warps are done by then.
-    const float l_tot = head_sum<G>(S.l);
+    float l_tot = S.l;  // head tig's sum over its 8 lanes
+    l_tot += __shfl_xor_sync(kFull, l_tot, 4);
+    l_tot += __shfl_xor_sync(kFull, l_tot, 8);
+    l_tot += __shfl_xor_sync(kFull, l_tot, 16);
     const bool final_piece = (b == c_end);
     int ok = 1;
     if (lane == 0) ok = wait_merge_buffer(ctl, piece);
@@ -769,14 +859,19 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
       }
       aborted = true;
     }
-    if (head_writer) {
-      mrg_ml[(warp * G + g_lane) * 2] = aborted ? -INFINITY : S.m;
-      mrg_ml[(warp * G + g_lane) * 2 + 1] = l_tot;
-    }
+    if (tig < G) {
+      if (gid == 0) {
+        mrg_ml[(warp * G + tig) * 2] = aborted ? -INFINITY : S.m;
+        mrg_ml[(warp * G + tig) * 2 + 1] = l_tot;
+      }
+      float* acc_h = mrg_acc + (warp * G + tig) * kD;
+      const float osc = o_scale<DT>(S);
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-      *reinterpret_cast<float4*>(mrg_acc + (warp * G + g) * kD + lane * 4) =
-          make_float4(S.acc[g][0].x, S.acc[g][0].y, S.acc[g][1].x, S.acc[g][1].y);
+      for (int r = 0; r < 8; ++r) {  // hi + lo columns
+        acc_h[dim_of<DT>(r, 0, gid)] = (S.o[r][0] + S.o[r][1]) * osc;
+        acc_h[dim_of<DT>(r, 2, gid)] = (S.o[r][2] + S.o[r][3]) * osc;
+      }
+    }
     const bool whole = (k0 == k1);
     float* out_seg = a.out + (static_cast<long long>(i) * a.n_q + h * G) * kD;
     if (final_piece) {
@@ -918,14 +1013,69 @@ __global__ void __launch_bounds__(256) plan_kernel(const PlanArgs a) {
 }
 
 // ------------------------------------------------------------ launchers ----
+// cuTensorMapEncodeTiled, from the driver through the runtime (no link
+// against the driver library).
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// A layer's K or V data as a 3-D tensor [tiles][16 tokens][128 dims] read in
+// [16][64] (f16) or [16][128] (q8_0 codes) boxes of 128-byte rows under the
+// 128-byte swizzle.
+static cudaError_t encode_tile_map(CUtensorMap* m, int dtype, void* base, long long tiles) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const bool f16 = dtype == PKV_KV_F16;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(kPage),
+                              static_cast<cuuint64_t>(tiles)};
+  const cuuint64_t strides[2] = {f16 ? 256u : 128u, f16 ? 4096u : 2048u};  // bytes
+  const cuuint32_t box[3] = {f16 ? 64u : 128u, static_cast<cuuint32_t>(kPage), 1u};
+  const cuuint32_t estride[3] = {1u, 1u, 1u};
+  const CUresult r =
+      fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims,
+         strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int DT, int G>
 static cudaError_t launch_decode_t(const DecodeArgs& a, int chunks, cudaStream_t st) {
+  const long long tiles = static_cast<long long>(a.num_pages) * a.n_kv;
+  if (tiles >= (1ll << 31)) return cudaErrorInvalidValue;
+  TileMaps maps;
+  cudaError_t em = encode_tile_map(&maps.k, DT, a.k_data, tiles);
+  if (em == cudaSuccess) em = encode_tile_map(&maps.v, DT, a.v_data, tiles);
+  if (em != cudaSuccess) return em;
   const size_t smem = Smem<DT, G>::bytes(a.num_rows);
   cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<DT, G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  paged_decode_kernel<DT, G><<<chunks, kThreads, smem, st>>>(a);
+  // Programmatic dependent launch: the grid may be scheduled while the
+  // previous kernel of the stream finishes; the kernel itself waits for that
+  // kernel's completion before its first global access.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(chunks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = PKV_PDL;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, paged_decode_kernel<DT, G>, a, maps);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -87,11 +87,68 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// 3-D tiled bulk tensor copy global -> shared through a tensor map (the
+// map's swizzle applies), completing its bytes on `bar`, with an L2 hint.
+// `tmap` is the generic address of a CUtensorMap kernel parameter; x must be
+// a multiple of 16 bytes' worth of elements and dst aligned to the swizzle
+// atom (1024 bytes for the 128-byte swizzle).
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int x, int y, int z,
+                                            uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// Four 8x8 16-bit matrices from shared memory; lanes 8j..8j+7 give the row
+// addresses of matrix j, and lane t receives row t/4, elements 2(t%4) and
+// 2(t%4)+1 of each (the transposed matrix with .trans).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+// D = A B + D on the tensor cores for one warp: A 16x16 f16 (row), B 16x8
+// f16 (column), D 16x8 f32.  Lane t = 4 gid + tig holds A rows gid and
+// gid + 8 at columns 2tig, 2tig+1 (a0, a1) and 2tig+8, 2tig+9 (a2, a3), B
+// rows 2tig, 2tig+1 (b0) and 2tig+8, 2tig+9 (b1) of column gid, and D rows
+// gid (d[0], d[1]) and gid + 8 (d[2], d[3]) at columns 2tig, 2tig+1.
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // The KV stream is read once per call: mark it first to leave L2.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// Programmatic dependent launch: wait until the grids this one depends on
+// have completed and their memory operations are visible (returns at once
+// when the grid was launched without the attribute), and allow the next
+// dependent grid of the stream to be scheduled.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Named barrier over `count` threads (id 0 is __syncthreads).
