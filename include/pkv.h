@@ -104,6 +104,10 @@ size_t kv_pool_bytes(int num_layers, int num_pages, int n_kv_heads, int head_dim
  *                      16-byte aligned; f16: must be NULL
  *   device_status      optional device int32 (NULL: none), zero before first
  *                      use; kernels OR PKV_DEV_* bits into it.
+ * num_pages * n_kv_heads must be below 2^31 (PKV_ERR_UNSUPPORTED).  Creating
+ * a descriptor touches no device memory and needs no driver; the first
+ * attention call on a layer encodes that layer's tensor maps (host only)
+ * into the descriptor and reports PKV_ERR_CUDA if the driver cannot.
  * On success *out receives a descriptor to free with kv_pool_destroy. */
 pkv_status kv_pool_create(pkv_pool **out, int num_layers, int num_pages, int n_kv_heads,
                           int head_dim, pkv_kv_dtype dtype, void *k_data, void *v_data,

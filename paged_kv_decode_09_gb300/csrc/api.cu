@@ -5,7 +5,9 @@
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <atomic>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "pkv.h"
@@ -24,6 +26,16 @@ struct pkv_pool {
   int32_t* status;
   size_t layer_data_bytes;
   size_t layer_scale_bytes;
+  // Per layer, the tensor maps through which the attention kernel reads the
+  // K and V tiles: encoded on the layer's first attention call (host only),
+  // so that creating a descriptor needs no driver.
+  pkv::TileMaps* maps;       // [num_layers]
+  std::atomic<int>* ready;   // [num_layers]: 1 once maps[layer] is valid
+  std::mutex maps_mutex;
+  ~pkv_pool() {
+    delete[] maps;
+    delete[] ready;
+  }
 };
 
 namespace {
@@ -127,6 +139,23 @@ pkv_status default_chunks(const pkv_pool* p, int n_q, int rows, int* chunks) {
   return PKV_OK;
 }
 
+// The layer's tensor maps, encoded on first use.
+pkv_status layer_maps(const pkv_pool* pool, int layer, const pkv::TileMaps** maps) {
+  pkv_pool* p = const_cast<pkv_pool*>(pool);
+  if (!p->ready[layer].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(p->maps_mutex);
+    if (!p->ready[layer].load(std::memory_order_relaxed)) {
+      const cudaError_t e = pkv::encode_tile_maps(
+          p->dtype, p->k_data + layer * p->layer_data_bytes, p->v_data + layer * p->layer_data_bytes,
+          static_cast<long long>(p->num_pages) * p->n_kv, &p->maps[layer]);
+      if (e != cudaSuccess) return cuda_fail(e, "tensor maps of the pool layer");
+      p->ready[layer].store(1, std::memory_order_release);
+    }
+  }
+  *maps = &p->maps[layer];
+  return PKV_OK;
+}
+
 enum class Mode { kMerged, kSplitOnly };
 
 // One launch of the decode kernel: kMerged merges split segments in-kernel
@@ -175,7 +204,10 @@ pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q, const
   a.part_acc = w.part_acc;
   a.counters = mode == Mode::kMerged ? w.counters : nullptr;
   a.status = pool->status;
-  cudaError_t e = pkv::launch_paged_decode(pool->dtype, g, a, num_chunks, as_stream(stream));
+  const pkv::TileMaps* maps = nullptr;
+  if ((s = layer_maps(pool, layer, &maps))) return s;
+  cudaError_t e = pkv::launch_paged_decode(pool->dtype, g, a, *maps, num_chunks,
+                                           as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged decode launch");
   return PKV_OK;
 }
@@ -221,7 +253,7 @@ pkv_status kv_pool_create(pkv_pool** out, int num_layers, int num_pages, int n_k
   }
   if (device_status && !aligned(device_status, 4))
     return fail(PKV_ERR_INVALID_ARG, "status word not 4-byte aligned");
-  pkv_pool* p = new (std::nothrow) pkv_pool;
+  pkv_pool* p = new (std::nothrow) pkv_pool();
   if (!p) return fail(PKV_ERR_INVALID_ARG, "out of host memory");
   p->num_layers = num_layers;
   p->num_pages = num_pages;
@@ -235,6 +267,19 @@ pkv_status kv_pool_create(pkv_pool** out, int num_layers, int num_pages, int n_k
   p->status = device_status;
   p->layer_data_bytes = data_bytes_per_layer(num_pages, n_kv_heads, head_dim, dtype);
   p->layer_scale_bytes = scale_bytes_per_layer(num_pages, n_kv_heads, head_dim, dtype);
+  p->maps = nullptr;
+  p->ready = nullptr;
+  if (static_cast<long long>(num_pages) * n_kv_heads >= (1ll << 31)) {
+    delete p;
+    return fail(PKV_ERR_UNSUPPORTED, "num_pages * n_kv_heads must be below 2^31");
+  }
+  p->maps = new (std::nothrow) pkv::TileMaps[num_layers];
+  p->ready = new (std::nothrow) std::atomic<int>[num_layers];
+  if (!p->maps || !p->ready) {
+    delete p;
+    return fail(PKV_ERR_INVALID_ARG, "out of host memory");
+  }
+  for (int l = 0; l < num_layers; ++l) p->ready[l].store(0);
   *out = p;
   return PKV_OK;
 }

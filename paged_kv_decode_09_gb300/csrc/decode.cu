@@ -55,11 +55,11 @@
 //     built by 4 shuffles (q8_0: times the V block scales, one B operand per
 //     block).  Lane 4 gid + tig accumulates head tig's output at 16 of the
 //     dims, hi and lo columns, summed at the end of the piece.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
 
-#include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include "pkv_device.cuh"
@@ -90,12 +90,6 @@ namespace pkv {
 constexpr int kWarps = 4;  // warps per CTA; the final piece merge gives each thread one dim
 constexpr int kThreads = kWarps * 32;
 static_assert(kThreads == kD, "the final piece merge maps one thread to one dim");
-
-// Tensor maps of the layer's K and V tiles (kernel parameters).
-struct TileMaps {
-  CUtensorMap k;
-  CUtensorMap v;
-};
 
 // Shared-memory stage of one unit: the K tile then the V tile of one
 // (page, KV head), each [16 tokens][128 dims] under the 128-byte swizzle
@@ -1048,18 +1042,39 @@ static cudaError_t encode_tile_map(CUtensorMap* m, int dtype, void* base, long l
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t encode_tile_maps(int dtype, void* k_data, void* v_data, long long tiles,
+                             TileMaps* maps) {
+  if (tiles <= 0 || tiles >= (1ll << 31)) return cudaErrorInvalidValue;  // int tile index
+  cudaError_t e = encode_tile_map(&maps->k, dtype, k_data, tiles);
+  if (e == cudaSuccess) e = encode_tile_map(&maps->v, dtype, v_data, tiles);
+  return e;
+}
+
+// The kernel's dynamic shared-memory limit, raised only when a call needs
+// more than any earlier call (per device).
 template <int DT, int G>
-static cudaError_t launch_decode_t(const DecodeArgs& a, int chunks, cudaStream_t st) {
-  const long long tiles = static_cast<long long>(a.num_pages) * a.n_kv;
-  if (tiles >= (1ll << 31)) return cudaErrorInvalidValue;
-  TileMaps maps;
-  cudaError_t em = encode_tile_map(&maps.k, DT, a.k_data, tiles);
-  if (em == cudaSuccess) em = encode_tile_map(&maps.v, DT, a.v_data, tiles);
-  if (em != cudaSuccess) return em;
+static cudaError_t ensure_smem(size_t smem) {
+  static std::atomic<size_t> granted[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && granted[dev].load(std::memory_order_relaxed) >= smem)
+    return cudaSuccess;
+  e = cudaFuncSetAttribute(paged_decode_kernel<DT, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
+  if (e == cudaSuccess && dev >= 0 && dev < 64) {
+    size_t cur = granted[dev].load();
+    while (cur < smem && !granted[dev].compare_exchange_weak(cur, smem)) {
+    }
+  }
+  return e;
+}
+
+template <int DT, int G>
+static cudaError_t launch_decode_t(const DecodeArgs& a, const TileMaps& maps, int chunks,
+                                   cudaStream_t st) {
   const size_t smem = Smem<DT, G>::bytes(a.num_rows);
-  cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<DT, G>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = ensure_smem<DT, G>(smem);
   if (e != cudaSuccess) return e;
   // Programmatic dependent launch: the grid may be scheduled while the
   // previous kernel of the stream finishes; the kernel itself waits for that
@@ -1082,9 +1097,7 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, int chunks, cudaStream_t
 template <int DT, int G>
 static cudaError_t occupancy_t(int rows, int* blocks) {
   const size_t smem = Smem<DT, G>::bytes(rows);
-  cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<DT, G>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
+  cudaError_t e = ensure_smem<DT, G>(smem);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, paged_decode_kernel<DT, G>,
                                                        kThreads, smem);
@@ -1104,9 +1117,9 @@ static cudaError_t occupancy_t(int rows, int* blocks) {
     return cudaErrorInvalidValue;            \
   } while (0)
 
-cudaError_t launch_paged_decode(int dtype, int group, const DecodeArgs& a, int chunks,
-                                cudaStream_t st) {
-#define PKV_CALL(D, G) launch_decode_t<D, G>(a, chunks, st)
+cudaError_t launch_paged_decode(int dtype, int group, const DecodeArgs& a, const TileMaps& maps,
+                                int chunks, cudaStream_t st) {
+#define PKV_CALL(D, G) launch_decode_t<D, G>(a, maps, chunks, st)
   PKV_DISPATCH(dtype, group, PKV_CALL);
 #undef PKV_CALL
 }

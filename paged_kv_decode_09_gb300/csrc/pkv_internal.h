@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "pkv.h"
@@ -91,8 +92,17 @@ inline size_t part_acc_bytes(long long slots, int group) {
 int pool_kv_heads(const pkv_pool* pool);                 // n_kv_heads of a pool descriptor
 pkv_status record_error(pkv_status s, const char* msg);  // sets pkv_last_error_message
 
-cudaError_t launch_paged_decode(int dtype, int group, const DecodeArgs& a, int chunks,
-                                cudaStream_t stream);
+// Tensor maps of one layer's K and V data, [tiles][16 tokens][128 dims]
+// under the 128-byte swizzle (encoded once per layer when a pool is created).
+struct TileMaps {
+  CUtensorMap k;
+  CUtensorMap v;
+};
+cudaError_t encode_tile_maps(int dtype, void* k_data, void* v_data, long long tiles,
+                             TileMaps* maps);
+
+cudaError_t launch_paged_decode(int dtype, int group, const DecodeArgs& a, const TileMaps& maps,
+                                int chunks, cudaStream_t stream);
 cudaError_t paged_decode_blocks_per_sm(int dtype, int group, int rows, int* blocks);
 cudaError_t launch_combine(int group, const CombineArgs& a, cudaStream_t stream);
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
