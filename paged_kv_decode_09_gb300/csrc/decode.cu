@@ -68,23 +68,27 @@
 namespace pkv {
 
 // Build-time knobs (defaults are the tuned values): shared-memory stages per
-// warp for each dtype, the minimum CTAs per SM the register allocation must
-// allow, programmatic dependent launch of the decode kernel (1 on), and the
-// partial states a merge loads per round trip.
+// warp and the CTAs per SM the register allocation must allow, for each
+// dtype (q8_0 is bound by instruction issue: more warps hide more latency),
+// programmatic dependent launch of the decode kernel (1 on), and the partial
+// states a merge loads per round trip.
 #ifndef PKV_F16_RING
 #define PKV_F16_RING 2
 #endif
 #ifndef PKV_Q8_RING
-#define PKV_Q8_RING 3
+#define PKV_Q8_RING 2
 #endif
-#ifndef PKV_MIN_CTAS_PER_SM
-#define PKV_MIN_CTAS_PER_SM 3
+#ifndef PKV_F16_CTAS_PER_SM
+#define PKV_F16_CTAS_PER_SM 3
+#endif
+#ifndef PKV_Q8_CTAS_PER_SM
+#define PKV_Q8_CTAS_PER_SM 4
 #endif
 #ifndef PKV_PDL
 #define PKV_PDL 1
 #endif
 #ifndef PKV_MERGE_BATCH
-#define PKV_MERGE_BATCH 8
+#define PKV_MERGE_BATCH 8  // 4 for q8_0, whose 4 CTAs per SM leave 128 registers a thread
 #endif
 
 constexpr int kWarps = 4;  // warps per CTA; the final piece merge gives each thread one dim
@@ -179,21 +183,25 @@ struct WarpState {
   float m;            // running max (base 2) of head tig, equal on its 8 lanes
   float l;            // this lane's share of head tig's sum of probabilities
   float o[8][4];      // O^T accumulators: dims (see dim_of) x columns (tig, hi), (tig, lo)
-  int ve;             // q8_0: biased f32 exponent bound of the piece's V block scales so far
+  int vx;             // q8_0: every V block scale of the piece so far is below 2^vx
 };
 
 // The P operand is scaled by a power of two so that its f16 parts stay
 // normal: f16 KV by 2^7 (p <= 2^8, so P <= 2^15); q8_0, where P carries the V
-// block scale, by 2^(7 - x) with 2^x > every V scale of the piece so far
-// (raised, with the accumulators rescaled, when a page exceeds it).  O holds
-// the scaled sums; o_scale() undoes it.
+// block scale, by 2^(7 - vx) with 2^vx above every V scale of the piece so
+// far (raised, with the accumulators rescaled, when a page exceeds it).  O
+// holds the scaled sums; o_scale() undoes it.
 constexpr int kPShift = 7;
+constexpr int kNoScale = -64;  // vx before the piece's first page
+__device__ __forceinline__ float pow2i(int e) {  // 2^e for -126 <= e <= 127
+  return __int_as_float((127 + e) << 23);
+}
 template <int DT>
 __device__ __forceinline__ float o_scale(const WarpState& S) {
   if constexpr (DT == PKV_KV_F16)
     return 1.0f / (1 << kPShift);
   else
-    return exp2f(static_cast<float>(S.ve - 126 - kPShift));  // 2^(x - 7), x = ve - 126
+    return pow2i(S.vx - kPShift);
 }
 
 // The dim of accumulator o[r][e] (e = 0, 2; e + 1 is its lo column) in lane
@@ -292,14 +300,9 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
     s0 = c[0] + c[1];
     s1 = c[2] + c[3];
   } else {
-    // K block scales of tokens gid and gid + 8
+    // K block scales of tokens gid and gid + 8 (four f16 each)
     const uint2 k0 = *reinterpret_cast<const uint2*>(sc + gid * 8);
     const uint2 k1 = *reinterpret_cast<const uint2*>(sc + (gid + 8) * 8);
-    const float2 k0a = __half22float2(*reinterpret_cast<const __half2*>(&k0.x));
-    const float2 k0b = __half22float2(*reinterpret_cast<const __half2*>(&k0.y));
-    const float2 k1a = __half22float2(*reinterpret_cast<const __half2*>(&k1.x));
-    const float2 k1b = __half22float2(*reinterpret_cast<const __half2*>(&k1.y));
-    const float ks0[4] = {k0a.x, k0a.y, k0b.x, k0b.y}, ks1[4] = {k1a.x, k1a.y, k1b.x, k1b.y};
     s0 = 0.f;
     s1 = 0.f;
 #pragma unroll
@@ -317,8 +320,12 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
       mma_16816(c, codes_to_f16x2<kSelB01>(w2), codes_to_f16x2<kSelB01>(w3),
                 codes_to_f16x2<kSelB23>(w2), codes_to_f16x2<kSelB23>(w3), S.qb[2 * b + 1][0],
                 S.qb[2 * b + 1][1]);
-      s0 = fmaf(ks0[b], c[0] + c[1], s0);
-      s1 = fmaf(ks1[b], c[2] + c[3], s1);
+      // (token gid, token gid + 8) scales of block b, as a pair
+      const uint32_t kp = __byte_perm(b < 2 ? k0.x : k0.y, b < 2 ? k1.x : k1.y,
+                                      (b & 1) ? 0x7632 : 0x5410);
+      const float2 ksc = __half22float2(*reinterpret_cast<const __half2*>(&kp));
+      s0 = fmaf(ksc.x, c[0] + c[1], s0);
+      s1 = fmaf(ksc.y, c[2] + c[3], s1);
     }
   }
   s0 = gid < nvalid ? s0 * S.qexp : -INFINITY;
@@ -373,51 +380,45 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
       mma_16816(S.o[mt], w0, w2, w1, w3, b0, b1);
     }
   } else {
-    // V block scales of tokens 2tig, 2tig+1 and 2tig+8, 2tig+9 (4 per token)
-    const uint4 va = *reinterpret_cast<const uint4*>(sc + TL::kScale + t0 * 8);
-    const uint4 vb = *reinterpret_cast<const uint4*>(sc + TL::kScale + (t0 + 8) * 8);
-    const __half* ha = reinterpret_cast<const __half*>(&va);
-    const __half* hb = reinterpret_cast<const __half*>(&vb);
-    // masked tokens have p = 0, but their scales may be NaN: they are left
-    // out of the scale bound (fmaxf drops NaN) and their P is set to 0
-    const bool ok0 = t0 < nvalid, ok1 = t0 + 1 < nvalid, ok2 = t0 + 8 < nvalid,
-               ok3 = t0 + 9 < nvalid;
-    float vs[16];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      vs[b] = ok0 ? __half2float(ha[b]) : 0.f;
-      vs[4 + b] = ok1 ? __half2float(ha[4 + b]) : 0.f;
-      vs[8 + b] = ok2 ? __half2float(hb[b]) : 0.f;
-      vs[12 + b] = ok3 ? __half2float(hb[4 + b]) : 0.f;
+    // V block scales of tokens 2tig, 2tig+1 (va) and 2tig+8, 2tig+9 (vb): the
+    // four f16 block scales of a token are 8 contiguous bytes
+    uint4 va = *reinterpret_cast<const uint4*>(sc + TL::kScale + t0 * 8);
+    uint4 vb = *reinterpret_cast<const uint4*>(sc + TL::kScale + (t0 + 8) * 8);
+    if (nvalid < kPage) {  // masked tokens have p = 0 but their scales may be NaN
+      if (t0 >= nvalid) va.x = va.y = 0u;
+      if (t0 + 1 >= nvalid) va.z = va.w = 0u;
+      if (t0 + 8 >= nvalid) vb.x = vb.y = 0u;
+      if (t0 + 9 >= nvalid) vb.z = vb.w = 0u;
     }
-    float vmax = 0.f;
-#pragma unroll
-    for (int e = 0; e < 16; ++e) vmax = fmaxf(vmax, fabsf(vs[e]));
-    vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, 1));  // the page's 16 tokens: over tig
-    vmax = fmaxf(vmax, __shfl_xor_sync(kFull, vmax, 2));
-    // biased exponent of vmax: vmax < 2^(ve - 126); raise the piece's bound
-    const int ve = static_cast<int>((__float_as_uint(vmax) >> 23) & 0xff);
-    if (ve > S.ve) {  // warp-uniform
-      const float r = exp2f(static_cast<float>(S.ve - ve));  // 0 on the first page
+    // the page's largest |scale|: non-negative f16 bit patterns order as integers
+    uint32_t mb = __vmaxu2(__vmaxu2(va.x & 0x7fff7fffu, va.y & 0x7fff7fffu),
+                           __vmaxu2(va.z & 0x7fff7fffu, va.w & 0x7fff7fffu));
+    mb = __vmaxu2(mb, __vmaxu2(__vmaxu2(vb.x & 0x7fff7fffu, vb.y & 0x7fff7fffu),
+                               __vmaxu2(vb.z & 0x7fff7fffu, vb.w & 0x7fff7fffu)));
+    uint32_t m16 = max(mb & 0xffffu, mb >> 16);
+    m16 = max(m16, __shfl_xor_sync(kFull, m16, 1));  // the page's 16 tokens: over tig
+    m16 = max(m16, __shfl_xor_sync(kFull, m16, 2));
+    // an f16 with biased exponent e is below 2^(e - 14) (subnormals: 2^-14)
+    const int vx = static_cast<int>(m16 >> 10) - 14;
+    if (vx > S.vx) {  // warp-uniform: raise the bound, rescale the accumulators
+      const float r = pow2i(max(S.vx - vx, -126));
 #pragma unroll
       for (int rr = 0; rr < 8; ++rr)
 #pragma unroll
         for (int e = 0; e < 4; ++e) S.o[rr][e] *= r;
-      S.ve = ve;
+      S.vx = vx;
     }
-    // 2^(7 - x); every scale so far is 0 while ve is 0 (f16 scales as f32
-    // have biased exponents of at least 103, so the power stays finite)
-    const float up = S.ve ? exp2f(static_cast<float>(kPShift + 126 - S.ve)) : 0.f;
-    pa *= up;
-    pb *= up;
-    pc *= up;
-    pd *= up;
+    const float up = pow2i(kPShift - S.vx);  // 2^(7 - vx)
+    const float2 pab = make_float2(pa * up, pb * up), pcd = make_float2(pc * up, pd * up);
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const float x0 = pa * vs[b];
-      const float x1 = pb * vs[4 + b];
-      const float x2 = pc * vs[8 + b];
-      const float x3 = pd * vs[12 + b];
+      // (token t0, t0 + 1) and (t0 + 8, t0 + 9) scale pairs of block b
+      const uint32_t sel = (b & 1) ? 0x7632 : 0x5410;
+      const uint32_t sa = __byte_perm(b < 2 ? va.x : va.y, b < 2 ? va.z : va.w, sel);
+      const uint32_t sb = __byte_perm(b < 2 ? vb.x : vb.y, b < 2 ? vb.z : vb.w, sel);
+      const float2 x01 = __fmul2_rn(pab, __half22float2(*reinterpret_cast<const __half2*>(&sa)));
+      const float2 x23 = __fmul2_rn(pcd, __half22float2(*reinterpret_cast<const __half2*>(&sb)));
+      const float x0 = x01.x, x1 = x01.y, x2 = x23.x, x3 = x23.y;
       const uint32_t b0 = split_f16x2(x0, x1, lo), b1 = split_f16x2(x2, x3, lo);
       uint32_t w0, w1, w2, w3;  // (tokens 0-7 | 8-15) x (chunk 2b | 2b+1), 16-bit transposed
       ldsm_x4_trans(vt + tile_offset<DT>(ld_tok, 2 * b + ld_chunk), w0, w1, w2, w3);
@@ -442,10 +443,9 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
 // evaluated batch by batch with a running maximum (the sums are rescaled when
 // it grows).  Loads go through L2 (other CTAs wrote the slots in this
 // launch); a batch of pieces costs one round trip.
-template <int G>
+template <int G, int kBatch = PKV_MERGE_BATCH>  // kBatch: pieces loaded per round trip
 __device__ __forceinline__ void merge_segment(const float* part_ml, const float* part_acc,
                                               long long j, int k0, int k1, float* o, int d) {
-  constexpr int kBatch = PKV_MERGE_BATCH;  // pieces loaded per round trip, all G heads at once
   float M[G], Ls[G], A[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -650,7 +650,8 @@ __device__ __forceinline__ bool wait_merge_buffer(volatile int* ctl, int piece) 
 
 // --------------------------------------------------------------- kernel ----
 template <int DT, int G>
-__global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
+__global__ void __launch_bounds__(kThreads, DT == PKV_KV_F16 ? PKV_F16_CTAS_PER_SM
+                                                              : PKV_Q8_CTAS_PER_SM)
     paged_decode_kernel(const __grid_constant__ DecodeArgs a,
                         const __grid_constant__ TileMaps maps) {
   using TL = Tiles<DT>;
@@ -812,7 +813,7 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
       for (int e = 0; e < 4; ++e) S.o[r][e] = 0.f;
     S.m = -INFINITY;
     S.l = 0.f;
-    S.ve = 0;
+    S.vx = kNoScale;
 
     const int r = static_cast<int>((x - c_begin) % kWarps);
     for (long long pos = x + ((warp - r + kWarps) % kWarps); pos < b; pos += kWarps) {
@@ -909,7 +910,8 @@ __global__ void __launch_bounds__(kThreads, PKV_MIN_CTAS_PER_SM)
       named_barrier(1, kThreads);
       if (ctl[1]) {
         __threadfence();
-        merge_segment<G>(a.part_ml, a.part_acc, j, k0, k1, out_seg, d);
+        merge_segment<G, DT == PKV_KV_F16 ? PKV_MERGE_BATCH : PKV_MERGE_BATCH / 2>(
+            a.part_ml, a.part_acc, j, k0, k1, out_seg, d);
         if (d == 0) a.counters[j] = 0;  // ready for the next call
       }
     } else {
