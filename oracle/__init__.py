@@ -65,7 +65,8 @@ def lib():
                                            _vp, _vp, _vp, _vp]
             L.oracle_kv_append.restype = _i
             L.oracle_decode_attention.argtypes = [_i, _i, _i, _i, _i, _f32p, _vp, _vp, _vp, _vp,
-                                                  _i32p, _i, _i32p, _i, ctypes.c_double, _f64p]
+                                                  _i32p, _i, _i32p, _i, ctypes.c_double, _i,
+                                                  _f64p]
             L.oracle_decode_attention.restype = _i
             L.oracle_attention_partial.argtypes = [
                 _i, _i, _i, _i, _f32p, _vp, _vp, _vp, _vp, _i32p, _i, _i, _i, _i,
@@ -74,7 +75,7 @@ def lib():
             L.oracle_attention_partial.restype = _i
             L.oracle_combine.argtypes = [_i, _f32p, _f32p, _f32p, _i, _f64p]
             L.oracle_combine.restype = None
-            L.oracle_plan.argtypes = [_i, _i32p, _i, _i, _i32p, _i32p, _i32p, _i64p]
+            L.oracle_plan.argtypes = [_i, _i32p, _i, _i, _i, _i32p, _i32p, _i32p, _i64p]
             L.oracle_plan.restype = _i
             _lib = L
     return _lib
@@ -166,8 +167,9 @@ def kv_append(dtype, k_new, v_new, block_table, seq_lens, num_pages, k_data, v_d
 
 
 def decode_attention(dtype, q, k_data, v_data, k_scales, v_scales, block_table, seq_lens,
-                     num_pages, n_kv, scale):
-    """out[i][g] = softmax_t(scale <q[i][g], K[i][g//G][t]>) V, t < seq_lens[i],
+                     num_pages, n_kv, scale, window=0):
+    """out[i][g] = softmax_t(scale <q[i][g], K[i][g//G][t]>) V over the row's
+    tokens max(0, L - window) <= t < L (all L for window 0), L = seq_lens[i],
     in float64 [rows][n_q][D]; zeros for rows with seq_lens[i] <= 0."""
     q = np.ascontiguousarray(q, np.float32)
     bt = np.ascontiguousarray(block_table, np.int32)
@@ -179,7 +181,7 @@ def decode_attention(dtype, q, k_data, v_data, k_scales, v_scales, block_table, 
     st = lib().oracle_decode_attention(dtype, rows, n_q, n_kv, D, q.reshape(-1), _ptr(k_data),
                                        _ptr(v_data), _ptr(k_scales), _ptr(v_scales),
                                        bt.reshape(-1), bt.shape[1], sl, num_pages,
-                                       float(scale), out.reshape(-1))
+                                       float(scale), int(window), out.reshape(-1))
     if st:
         raise ValueError(f"oracle_decode_attention: status {st}")
     return out
@@ -217,7 +219,7 @@ def combine(m2, l, acc):
     return out
 
 
-def plan(seq_lens, n_kv, num_chunks):
+def plan(seq_lens, n_kv, num_chunks, window=0):
     """Work split of one decode call (see oracle_plan in the C source):
     (row_page_start[rows+1], seg_first_chunk[rows*n_kv], seg_last_chunk[...], T)."""
     sl = np.ascontiguousarray(seq_lens, np.int32)
@@ -226,7 +228,7 @@ def plan(seq_lens, n_kv, num_chunks):
     first = np.zeros(max(rows * n_kv, 1), np.int32)
     last = np.zeros(max(rows * n_kv, 1), np.int32)
     total = np.zeros(1, np.int64)
-    st = lib().oracle_plan(rows, sl, n_kv, num_chunks, rps, first, last, total)
+    st = lib().oracle_plan(rows, sl, n_kv, num_chunks, int(window), rps, first, last, total)
     if st:
         raise ValueError(f"oracle_plan: status {st}")
     return rps, first[:rows * n_kv], last[:rows * n_kv], int(total[0])

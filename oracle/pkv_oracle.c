@@ -27,6 +27,9 @@
  *   - Variable-length batched decode: tinyllm, "The repository currently
  *     provides" (variable-length batched decode for several active
  *     sequences); Leone, "What ships" (continuous decode batching).
+ *   - Sliding-window KV caches: Leone, "Capabilities".  Reading: with a
+ *     window W > 0 a row of L tokens attends to its last W tokens,
+ *     [max(0, L - W), L), the new token included; W = 0 means all L.
  *
  * Readings where the pages are silent (each is restated where it is used):
  *   - GQA head map: query head g reads KV head g / (n_q_heads / n_kv_heads).
@@ -238,17 +241,21 @@ static int scores(int dtype, const void *k_data, const uint16_t *k_scales, int n
     return ORACLE_OK;
 }
 
+/* First attended token of a row of L tokens under a window W (0: none). */
+static int window_start(int L, int window) { return window > 0 && L > window ? L - window : 0; }
+
 /* Decode attention for every row and query head:
- *   out[i][g] = sum_{t < L_i} softmax_t(scale * <q[i][g], K[i][h][t]>) V[i][h][t]
- * with h = g / (n_q / n_kv), K and V the stored values gathered through the
- * block table, evaluated in double with the maximum subtracted before exp.
- * Rows with L_i <= 0 produce zeros.  out is double [rows][n_q][D]. */
+ *   out[i][g] = sum_{a_i <= t < L_i} softmax_t(scale * <q[i][g], K[i][h][t]>) V[i][h][t]
+ * with h = g / (n_q / n_kv), a_i = max(0, L_i - window) (a_i = 0 for window
+ * 0), K and V the stored values gathered through the block table, evaluated
+ * in double with the maximum subtracted before exp.  Rows with L_i <= 0
+ * produce zeros.  out is double [rows][n_q][D]. */
 int oracle_decode_attention(int dtype, int num_rows, int n_q, int n_kv, int D, const float *q,
                             const void *k_data, const void *v_data, const uint16_t *k_scales,
                             const uint16_t *v_scales, const int32_t *block_table,
                             int bt_stride, const int32_t *seq_lens, int num_pages,
-                            double scale, double *out) {
-    if (n_kv <= 0 || n_q % n_kv || D % ORACLE_QBLOCK) return ORACLE_BAD_ARG;
+                            double scale, int window, double *out) {
+    if (n_kv <= 0 || n_q % n_kv || D % ORACLE_QBLOCK || window < 0) return ORACLE_BAD_ARG;
     for (int i = 0; i < num_rows; ++i)
         if (seq_lens[i] > (int64_t)bt_stride * ORACLE_PAGE) return ORACLE_BAD_ARG;
     const int group = n_q / n_kv;
@@ -260,19 +267,20 @@ int oracle_decode_attention(int dtype, int num_rows, int n_q, int n_kv, int D, c
         double *o = out + ig * D;
         for (int d = 0; d < D; ++d) o[d] = 0.0;
         if (L <= 0) continue;
-        double *s = (double *)malloc(sizeof(double) * (size_t)L);
+        const int a = window_start(L, window), n = L - a;
+        double *s = (double *)malloc(sizeof(double) * (size_t)n);
         if (!s || scores(dtype, k_data, k_scales, n_kv, D, block_table, bt_stride, num_pages,
-                         i, h, q + ig * D, scale, 0, L, s) != ORACLE_OK) {
+                         i, h, q + ig * D, scale, a, L, s) != ORACLE_OK) {
 #pragma omp atomic write
             status = ORACLE_BAD_PAGE;
             free(s);
             continue;
         }
         double m = -INFINITY;
-        for (int t = 0; t < L; ++t) m = s[t] > m ? s[t] : m;
+        for (int t = 0; t < n; ++t) m = s[t] > m ? s[t] : m;
         double l = 0.0;
-        for (int t = 0; t < L; ++t) {
-            double p = exp(s[t] - m);
+        for (int t = a; t < L; ++t) {
+            double p = exp(s[t - a] - m);
             l += p;
             int64_t page = page_of(block_table, bt_stride, i, t, num_pages);
             for (int d = 0; d < D; ++d)
@@ -344,8 +352,10 @@ void oracle_combine(int n, const float *m2, const float *l, const float *acc, in
 
 /* The work split of one decode call, written out by brute force.
  *
- * Work unit: one (page, KV head) tile of a row.  Rows i have npg_i =
- * ceil(L_i / 16) pages (L_i <= 0 gives 0).  Units are numbered in the order
+ * Work unit: one (page, KV head) tile of a row.  Row i reads npg_i pages:
+ * those that hold a token of [a_i, L_i), a_i = max(0, L_i - window) (a_i = 0
+ * for window 0), so npg_i = ceil(L_i / 16) - floor(a_i / 16), 0 for L_i <= 0;
+ * its page p < npg_i is block-table entry floor(a_i / 16) + p.  Units are numbered in the order
  * (row, KV head, page): segment j = i * n_kv + h holds the npg_i units of
  * (row i, head h) starting at seg_start(j) = n_kv * sum_{r<i} npg_r + h * npg_i.
  * With T = n_kv * sum_i npg_i units and C chunks requested, Ce = min(C, T)
@@ -356,14 +366,16 @@ void oracle_combine(int n, const float *m2, const float *l, const float *acc, in
  *
  * Outputs: row_page_start[rows + 1] (exclusive prefix sum of npg),
  * seg_first_chunk[rows * n_kv], seg_last_chunk[rows * n_kv], *total = T. */
-int oracle_plan(int num_rows, const int32_t *seq_lens, int n_kv, int num_chunks,
+int oracle_plan(int num_rows, const int32_t *seq_lens, int n_kv, int num_chunks, int window,
                 int32_t *row_page_start, int32_t *seg_first_chunk, int32_t *seg_last_chunk,
                 int64_t *total) {
-    if (num_rows < 0 || n_kv <= 0 || num_chunks <= 0) return ORACLE_BAD_ARG;
+    if (num_rows < 0 || n_kv <= 0 || num_chunks <= 0 || window < 0) return ORACLE_BAD_ARG;
     row_page_start[0] = 0;
     for (int i = 0; i < num_rows; ++i) {
         int L = seq_lens[i] > 0 ? seq_lens[i] : 0;
-        row_page_start[i + 1] = row_page_start[i] + (L + ORACLE_PAGE - 1) / ORACLE_PAGE;
+        int npg = L > 0 ? (L + ORACLE_PAGE - 1) / ORACLE_PAGE - window_start(L, window) / ORACLE_PAGE
+                        : 0;
+        row_page_start[i + 1] = row_page_start[i] + npg;
     }
     int64_t T = (int64_t)n_kv * row_page_start[num_rows];
     *total = T;

@@ -251,3 +251,81 @@ def test_merge_is_invariant_to_rescaled_partials():
     # one partial: out = acc / l
     np.testing.assert_allclose(O.combine(m2[:1], l[:1], acc[:1]),
                                acc[0].astype(np.float64) / np.float64(l[0]), rtol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# Sliding window (Leone, "Capabilities": sliding-window KV caches).  Reading:
+# with W > 0 a row of L tokens attends to [max(0, L - W), L).
+
+def _brute_window(dtype, q, dk, dv, lens, n_q, n_kv, scale, window):
+    """Dense brute force over each row's last `window` tokens."""
+    G = n_q // n_kv
+    rows, _, D = q.shape
+    out = np.zeros((rows, n_q, D))
+    for i, L in enumerate(lens):
+        a = max(0, L - window)
+        K = stored_values_dense(dtype, dk[i][0], dk[i][1])
+        V = stored_values_dense(dtype, dv[i][0], dv[i][1])
+        for g in range(n_q):
+            h = g // G
+            w = [math.exp(scale * math.fsum(float(x) * float(y) for x, y in zip(q[i, g], K[h, t])))
+                 for t in range(a, L)]
+            den = math.fsum(w)
+            for d in range(D):
+                out[i, g, d] = math.fsum(w[t - a] * V[h, t, d] for t in range(a, L)) / den
+    return out
+
+
+@pytest.mark.parametrize("dtype", [O.F16, O.Q8_0])
+@pytest.mark.parametrize("window", [1, 5, 16, 17, 39])
+def test_window_against_dense_brute_force(dtype, window):
+    lens, n_q, n_kv, D = [1, 16, 17, 40], 4, 2, 32
+    q, dk, dv, pool, bt, num_pages = _case(31 + window, dtype, lens, n_q, n_kv, D)
+    got = O.decode_attention(dtype, q, *pool, bt, np.array(lens, np.int32), num_pages, n_kv, 0.2,
+                             window=window)
+    ref = _brute_window(dtype, q, dk, dv, lens, n_q, n_kv, 0.2, window)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("dtype", [O.F16, O.Q8_0])
+def test_window_at_least_the_length_is_full_attention(dtype):
+    lens, n_q, n_kv, D = [3, 33, 64], 4, 2, 64
+    q, dk, dv, pool, bt, num_pages = _case(41, dtype, lens, n_q, n_kv, D)
+    sl = np.array(lens, np.int32)
+    full = O.decode_attention(dtype, q, *pool, bt, sl, num_pages, n_kv, 0.1)
+    for window in (64, 65, 10**6):
+        np.testing.assert_array_equal(
+            O.decode_attention(dtype, q, *pool, bt, sl, num_pages, n_kv, 0.1, window=window), full)
+
+
+@pytest.mark.parametrize("dtype", [O.F16, O.Q8_0])
+def test_window_one_returns_the_newest_v(dtype):
+    lens, n_q, n_kv, D = [1, 20, 48], 4, 2, 64
+    q, dk, dv, pool, bt, num_pages = _case(43, dtype, lens, n_q, n_kv, D)
+    out = O.decode_attention(dtype, q, *pool, bt, np.array(lens, np.int32), num_pages, n_kv, 0.5,
+                             window=1)
+    for i, L in enumerate(lens):
+        V = stored_values_dense(dtype, dv[i][0], dv[i][1])
+        for g in range(n_q):
+            np.testing.assert_array_equal(out[i, g], V[g // 2, L - 1])
+
+
+@pytest.mark.parametrize("dtype", [O.F16, O.Q8_0])
+def test_window_equals_full_attention_of_the_truncated_rows(dtype):
+    """The last W tokens re-paged from slot 0 as rows of their own give the
+    same result, bit for bit (same values, same order of summation)."""
+    lens, n_q, n_kv, D, window = [9, 30, 70, 100], 4, 2, 64, 37
+    q, dk, dv, pool, bt, num_pages = _case(47, dtype, lens, n_q, n_kv, D)
+    got = O.decode_attention(dtype, q, *pool, bt, np.array(lens, np.int32), num_pages, n_kv, 0.15,
+                             window=window)
+    cut = [min(L, window) for L in lens]
+
+    def tail(parts, L):
+        data, sc = parts
+        return (data[:, L - min(L, window):], None if sc is None else sc[:, L - min(L, window):])
+
+    dk2 = [tail(dk[i], L) for i, L in enumerate(lens)]
+    dv2 = [tail(dv[i], L) for i, L in enumerate(lens)]
+    pool2, bt2, np2 = _scatter_rows(np.random.default_rng(48), dtype, dk2, dv2, cut, n_kv, D)
+    want = O.decode_attention(dtype, q, *pool2, bt2, np.array(cut, np.int32), np2, n_kv, 0.15)
+    np.testing.assert_array_equal(got, want)

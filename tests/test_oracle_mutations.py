@@ -38,6 +38,11 @@ MUTANTS = {
                       "int64_t a = (int64_t)n_kv * row_page_start[i] + h, b = a + npg;"),
     "append_slot": ("int slot = pos % ORACLE_PAGE;", "int slot = L % ORACLE_PAGE;"),
     "partial_base_e": ("double p = exp2(s[t - t0] - m);", "double p = exp(s[t - t0] - m);"),
+    "window_one_too_short": ("return window > 0 && L > window ? L - window : 0;",
+                             "return window > 0 && L > window ? L - window + 1 : 0;"),
+    "window_first_page_rounded_up": (
+        "- window_start(L, window) / ORACLE_PAGE",
+        "- (window_start(L, window) + ORACLE_PAGE - 1) / ORACLE_PAGE"),
 }
 
 

@@ -35,12 +35,19 @@ def test_plan_golden(case):
     np.testing.assert_array_equal(last, case["seg_last_chunk"])
 
 
-def _enumerate(seq_lens, n_kv, C):
+def _pages_read(L, window):
+    """Pages of a row holding an attended token: tokens max(0, L - window)..L-1
+    (all L for window 0), by brute force over the tokens."""
+    first = max(0, L - window) if window > 0 else 0
+    return sorted({t // 16 for t in range(first, max(L, 0))})
+
+
+def _enumerate(seq_lens, n_kv, C, window=0):
     """Brute force: list every unit with its (segment, chunk) and derive the
     chunks each segment meets."""
     units = []  # (segment, chunk) per unit, in unit order
     for i, L in enumerate(seq_lens):
-        npg = (max(L, 0) + 15) // 16
+        npg = len(_pages_read(L, window))
         for h in range(n_kv):
             for p in range(npg):
                 units.append(i * n_kv + h)
@@ -74,6 +81,28 @@ def test_plan_matches_unit_enumeration(seed):
         np.testing.assert_array_equal(first, f2)
         np.testing.assert_array_equal(last, l2)
         np.testing.assert_array_equal(np.diff(rps), (np.maximum(lens, 0) + 15) // 16)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_windowed_plan_matches_unit_enumeration(seed):
+    """With a sliding window a row's units are the pages holding its last W
+    tokens; page p of the row's units is block-table entry floor(a / 16) + p."""
+    rng = np.random.default_rng(100 + seed)
+    rows = int(rng.integers(1, 10))
+    lens = rng.integers(0, 300, rows).astype(np.int32)
+    n_kv = int(rng.choice([1, 2, 8]))
+    for window in (1, 15, 16, 17, 64, 100, 299, 1000):
+        for C in (1, 5, 152):
+            rps, first, last, T = O.plan(lens, n_kv, C, window=window)
+            T2, f2, l2 = _enumerate(lens.tolist(), n_kv, C, window)
+            assert T == T2
+            np.testing.assert_array_equal(first, f2)
+            np.testing.assert_array_equal(last, l2)
+            pages = [_pages_read(int(L), window) for L in lens]
+            np.testing.assert_array_equal(np.diff(rps), [len(p) for p in pages])
+            for L, p in zip(lens, pages):  # contiguous run starting at floor(a / 16)
+                if p:
+                    assert p == list(range(max(0, int(L) - window) // 16, p[-1] + 1))
 
 
 @pytest.mark.parametrize("dtype", [W.F16, W.Q8_0])
