@@ -54,6 +54,8 @@ def parse_args():
     p.add_argument("--chunks", type=int, default=0, help="work chunks (0: one per resident CTA)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU baseline budget")
+    p.add_argument("--window", type=int, default=0,
+                   help="sliding window of every layer (0: none); bytes count attended tokens")
     p.add_argument("--kernel", choices=["step", "append", "split_combine", "plan"], default="step",
                    help="step: the decode step (the benchmark); the others run --steps calls of\n"
                         "one other entry point on the workload and print its mean call time\n"
@@ -154,12 +156,17 @@ def read_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def step_bytes(wl) -> int:
+def attended_tokens(wl, window=0) -> int:
+    """Tokens attended by one decode call: L per row, min(L, window) with a window."""
+    return int(sum(min(int(L), window) if window > 0 else int(L) for L in wl.seq_lens))
+
+
+def step_bytes(wl, window=0) -> int:
     """Algorithmic bytes of one decode call: K and V of every attended token
     (f16: 2 bytes per element; q8_0: 34 bytes per 32 elements), q and out."""
     cfg = wl.cfg
     per_elem = 2.0 if cfg.dtype == 0 else 34.0 / 32.0
-    kv = int(sum(int(L) for L in wl.seq_lens)) * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem
+    kv = attended_tokens(wl, window) * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem
     qo = 2 * wl.rows * cfg.n_q_heads * cfg.head_dim * 4
     return int(kv + qo)
 
@@ -220,6 +227,8 @@ def run_ours(args, rank, world, local):
     layers = args.layers or max(2, min(cfg.model_layers, -(-4 * L2_BYTES // layer_bytes)))
     pool = api.KVPool(layers, wl.num_pages, cfg.n_kv_heads, cfg.dtype, device=dev)
     fill_pool(api, pool, layers, seed=1234 + rank)
+    for layer in range(layers):
+        pool.set_window(layer, args.window)
 
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
     q, k_new, v_new = t(wl.q), t(wl.k_new), t(wl.v_new)
@@ -296,12 +305,12 @@ def run_ours(args, rank, world, local):
     barrier(world)
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world)
 
-    nbytes = step_bytes(wl)
+    nbytes = step_bytes(wl, args.window)
     peak, peak_src = read_peak()
     step_s = total_ms / 1e3 / K
     value = world * nbytes / step_s / 1e9
     achieved = nbytes / (launch_ms / 1e3) / 1e9
-    tokens = int(sum(int(x) for x in wl.seq_lens))
+    tokens = attended_tokens(wl, args.window)
     result = {
         "metric": "paged decode-attn KV GB/s & % of GB300 HBM peak; rows*tokens/s at 1 GPU",
         "value": round(value, 2),
@@ -323,6 +332,7 @@ def run_ours(args, rank, world, local):
             "l2": f"inputs larger than L2: {layers} layer pools of "
                   f"{layer_bytes / 2**20:.0f} MiB rotated (> 4x the 126 MiB L2)",
             "chunks": CH, "bytes_per_step": nbytes, "parallelism": f"replicas x{world}",
+            **({"window": args.window} if args.window else {}),
         },
         "frac_of_hbm_peak": round(value / world / peak, 4),
         "rows_tokens_per_s": round(world * tokens / step_s, 1),
@@ -332,7 +342,8 @@ def run_ours(args, rank, world, local):
                                       f"{cfg.group}>",
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (copy bandwidth)",
-            "traffic": profile_traffic(cfg.name), "mean_launch_us": round(launch_ms * 1e3, 3),
+            "traffic": None if args.window else profile_traffic(cfg.name),
+            "mean_launch_us": round(launch_ms * 1e3, 3),
             "timing": "events around the K back-to-back launches of the timed region",
         },
         "e2e": {"value": round(world * nbytes / (e2e_ms / 1e3 / Ke) / 1e9, 2), "unit": "GB/s",
@@ -342,7 +353,7 @@ def run_ours(args, rank, world, local):
         "clocks": clock_info,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(wl, pool, args.cpu_seconds)
+        result["cpu_baseline"] = cpu_baseline(wl, pool, args.cpu_seconds, args.window)
     return result
 
 
@@ -395,7 +406,7 @@ def run_kernel(args, local):
             "note": "per-entry-point timing for profiling; not the benchmark metric"}
 
 
-def cpu_baseline(wl, pool, budget_s):
+def cpu_baseline(wl, pool, budget_s, window=0):
     """The FP64 oracle, as it stands, on a bounded sample of rows of layer 0."""
     import numpy as np
     import torch
@@ -415,10 +426,11 @@ def cpu_baseline(wl, pool, budget_s):
     for i in order:
         t0 = time.perf_counter()
         O.decode_attention(cfg.dtype, wl.q[i:i + 1], kd, vd, ks, vs, wl.block_table[i:i + 1],
-                           wl.seq_lens[i:i + 1], wl.num_pages, cfg.n_kv_heads, wl.scale)
+                           wl.seq_lens[i:i + 1], wl.num_pages, cfg.n_kv_heads, wl.scale,
+                           window=window)
         secs += time.perf_counter() - t0
         rows.append(int(i))
-        done += int(wl.seq_lens[i])
+        done += min(int(wl.seq_lens[i]), window) if window > 0 else int(wl.seq_lens[i])
         if secs > budget_s:
             break
     per_elem = 2.0 if cfg.dtype == 0 else 34.0 / 32.0
@@ -453,12 +465,17 @@ def run_reference(args):
     def one(i):
         q = wl.q[i:i + 1, heads]
         O.decode_attention(cfg.dtype, q, kd, vd, ks, vs, wl.block_table[i:i + 1],
-                           wl.seq_lens[i:i + 1], wl.num_pages, cfg.n_kv_heads, wl.scale)
+                           wl.seq_lens[i:i + 1], wl.num_pages, cfg.n_kv_heads, wl.scale,
+                           window=args.window)
 
     per_elem = 2.0 if cfg.dtype == 0 else 34.0 / 32.0
 
+    def row_tokens(i):
+        L = int(wl.seq_lens[i])
+        return min(L, args.window) if args.window > 0 else L
+
     def row_bytes(i, frac):
-        return frac * (int(wl.seq_lens[i]) * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem
+        return frac * (row_tokens(i) * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem
                        + 2 * cfg.n_q_heads * 128 * 4)
 
     mid = order[len(order) // 2]
@@ -479,7 +496,7 @@ def run_reference(args):
         one(i)
         secs += time.perf_counter() - t0
         nbytes += row_bytes(i, frac)
-        tokens += frac * int(wl.seq_lens[i])
+        tokens += frac * row_tokens(i)
     value = nbytes / secs / 1e9
     return {
         "impl": "reference",
@@ -488,7 +505,8 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": round(secs * 1e3 / args.steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic: same seeded workload, pool encoded by the oracle",
-        "config": {"workload": cfg.name, "description": cfg.description, "sample": sample},
+        "config": {"workload": cfg.name, "description": cfg.description, "sample": sample,
+                   **({"window": args.window} if args.window else {})},
         "rows_tokens_per_s": round(tokens / secs, 1),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": O.num_threads(),
                          "kind": "oracle", "sample": sample},

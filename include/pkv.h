@@ -116,6 +116,16 @@ pkv_status kv_pool_create(pkv_pool **out, int num_layers, int num_pages, int n_k
 /* Free a descriptor (not the caller's arrays).  NULL is allowed. */
 void kv_pool_destroy(pkv_pool *pool);
 
+/* Sliding window of a layer (Leone, "Capabilities": sliding-window KV
+ * caches).  With window W > 0, every attention call on the layer lets a row
+ * of L tokens attend to its last W tokens, [max(0, L - W), L), the token
+ * appended this step included, and reads only the pages holding them:
+ * block-table entries floor(max(0, L - W) / 16) onwards.  W = 0 (the
+ * default) attends to all L tokens.  Host-side descriptor state, read when a
+ * call is queued; kv_append is unaffected.  W < 0 -> PKV_ERR_INVALID_ARG. */
+pkv_status kv_pool_set_window(pkv_pool *pool, int layer, int window);
+pkv_status kv_pool_get_window(const pkv_pool *pool, int layer, int *window);
+
 /* Wait for `stream`, copy the pool's device status word into *status and
  * reset it to 0.  This call synchronises; it is not part of the decode path.
  * Without a status word, *status = 0. */
@@ -171,7 +181,9 @@ size_t paged_decode_workspace_bytes(int max_rows, int n_q_heads, int n_kv_heads,
  * (when it holds a whole (row, KV head)) or a partial state (m2, l, acc) to
  * slot chunk + row * n_kv_heads + head of the workspace.  The last CTA to
  * finish a piece of a split (row, KV head) merges all its pieces into the
- * output.  Rows with seq_lens[i] == 0 get zeros.  One launch, no host
+ * output.  Rows with seq_lens[i] == 0 get zeros.  A layer with a sliding
+ * window (kv_pool_set_window) attends to each row's last `window` tokens and
+ * counts only the pages holding them.  One launch, no host
  * synchronisation. */
 pkv_status paged_decode_attention(const pkv_pool *pool, int layer, const float *q,
                                   const int32_t *block_table, int bt_stride,
@@ -192,14 +204,17 @@ pkv_status paged_decode_split(const pkv_pool *pool, int layer, const float *q,
 
 /* paged_decode_plan — the work split paged_decode_attention uses, written out
  * for inspection.  Units are (row, KV head, page) tiles in that order; row i
- * has ceil(seq_lens[i] / 16) pages; T = n_kv_heads * total pages; chunk k
- * covers units [floor(k T / C), floor((k + 1) T / C)) with C = num_chunks.
+ * reads the pages holding its attended tokens [a_i, L_i), a_i = max(0, L_i -
+ * window) (0 for window 0): ceil(L_i / 16) - floor(a_i / 16) pages;
+ * T = n_kv_heads * total pages; of C = num_chunks chunks min(C, T) are used,
+ * chunk k covering units [floor(k T / C'), floor((k + 1) T / C')), C' = min(C, T).
+ * `window` must be the layer's window of the call the plan describes.
  *   row_page_start  int32 [num_rows + 1]: exclusive prefix sum of pages
  *   seg_first_chunk, seg_last_chunk  int32 [num_rows * n_kv_heads]: first and
  *                   last chunk meeting segment (row, head) (-1 if empty)
  * One single-CTA launch. */
 pkv_status paged_decode_plan(const int32_t *seq_lens, int num_rows, int n_kv_heads,
-                             int bt_stride, int num_chunks, int32_t *row_page_start,
+                             int bt_stride, int window, int num_chunks, int32_t *row_page_start,
                              int32_t *seg_first_chunk, int32_t *seg_last_chunk, void *stream);
 
 /* paged_decode_combine — merge the base-2 partial states of every
@@ -208,11 +223,12 @@ pkv_status paged_decode_plan(const int32_t *seq_lens, int num_rows, int n_kv_hea
  * over the slots chunk + row * n_kv_heads + head of the chunks the plan
  * assigns to the segment.  Segments held whole by one chunk are left as they
  * are; rows with seq_lens[i] == 0 get zeros.  The workspace layout is the one
- * paged_decode_workspace_bytes describes.  One launch. */
+ * paged_decode_workspace_bytes describes; `window` is the layer's window of
+ * the paged_decode_split call being completed.  One launch. */
 pkv_status paged_decode_combine(const int32_t *seq_lens, int num_rows, int n_q_heads,
-                                int n_kv_heads, int head_dim, int bt_stride, int num_chunks,
-                                const void *workspace, size_t workspace_bytes, float *out,
-                                void *stream);
+                                int n_kv_heads, int head_dim, int bt_stride, int window,
+                                int num_chunks, const void *workspace, size_t workspace_bytes,
+                                float *out, void *stream);
 
 /* pkv_decode_step — one decode step of one layer: the new K/V token of every
  * row is stored as kv_append would store it, and attention runs over the

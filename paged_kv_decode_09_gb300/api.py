@@ -53,8 +53,10 @@ _SIGS = {
                                 _sz, _i, _vp], _i),
     "paged_decode_split": ([_vp, _i, _vp, _vp, _i, _vp, _i, _i, ctypes.c_float, _vp, _vp,
                             _sz, _i, _vp], _i),
-    "paged_decode_plan": ([_vp, _i, _i, _i, _i, _vp, _vp, _vp, _vp], _i),
-    "paged_decode_combine": ([_vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp], _i),
+    "paged_decode_plan": ([_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp], _i),
+    "paged_decode_combine": ([_vp, _i, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp], _i),
+    "kv_pool_set_window": ([_vp, _i, _i], _i),
+    "kv_pool_get_window": ([_vp, _i, ctypes.POINTER(_i)], _i),
     "pkv_decode_step": ([_vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, ctypes.c_float, _vp, _vp,
                          _sz, _i, _vp], _i),
     "pkv_status_string": ([_i], ctypes.c_char_p),
@@ -158,6 +160,16 @@ class KVPool:
         if h and _lib is not None:
             _lib.kv_pool_destroy(h)
             self.handle = None
+
+    def set_window(self, layer: int, window: int):
+        """Sliding window of `layer` (0: none): attention on the layer reads
+        each row's last `window` tokens only."""
+        _check(lib().kv_pool_set_window(self.handle, layer, window), "kv_pool_set_window")
+
+    def window(self, layer: int) -> int:
+        w = ctypes.c_int(0)
+        _check(lib().kv_pool_get_window(self.handle, layer, ctypes.byref(w)), "kv_pool_get_window")
+        return w.value
 
     def read_status(self, stream=None) -> int:
         """Synchronise and return (and clear) the device status word."""
@@ -270,7 +282,8 @@ def paged_decode_split(pool: KVPool, layer: int, q, block_table, seq_lens, scale
     return out
 
 
-def paged_decode_plan(seq_lens, n_kv_heads: int, bt_stride: int, num_chunks: int, stream=None):
+def paged_decode_plan(seq_lens, n_kv_heads: int, bt_stride: int, num_chunks: int, stream=None,
+                      window: int = 0):
     """(row_page_start [rows+1], seg_first_chunk, seg_last_chunk [rows*n_kv]) int32 tensors."""
     _need(seq_lens, torch.int32, "seq_lens")
     rows = seq_lens.shape[0]
@@ -278,20 +291,22 @@ def paged_decode_plan(seq_lens, n_kv_heads: int, bt_stride: int, num_chunks: int
     rps = torch.empty(rows + 1, dtype=torch.int32, device=dev)
     first = torch.empty(max(rows * n_kv_heads, 1), dtype=torch.int32, device=dev)
     last = torch.empty_like(first)
-    _check(lib().paged_decode_plan(_ptr(seq_lens), rows, n_kv_heads, bt_stride, num_chunks,
+    _check(lib().paged_decode_plan(_ptr(seq_lens), rows, n_kv_heads, bt_stride, window, num_chunks,
                                    _ptr(rps), _ptr(first), _ptr(last), _stream(stream)),
            "paged_decode_plan")
     return rps, first[:rows * n_kv_heads], last[:rows * n_kv_heads]
 
 
 def paged_decode_combine(seq_lens, n_q_heads: int, n_kv_heads: int, bt_stride: int,
-                         num_chunks: int, workspace: torch.Tensor, out, stream=None):
+                         num_chunks: int, workspace: torch.Tensor, out, stream=None,
+                         window: int = 0):
     """Merge partial states held in `workspace` (layout of paged_decode_workspace_bytes)."""
     _need(seq_lens, torch.int32, "seq_lens")
     _need(workspace, torch.uint8, "workspace")
     _need(out, torch.float32, "out")
     rows = seq_lens.shape[0]
     _check(lib().paged_decode_combine(_ptr(seq_lens), rows, n_q_heads, n_kv_heads, HEAD_DIM,
-                                      bt_stride, num_chunks, _ptr(workspace), workspace.numel(),
+                                      bt_stride, window, num_chunks, _ptr(workspace),
+                                      workspace.numel(),
                                       _ptr(out), _stream(stream)), "paged_decode_combine")
     return out

@@ -32,9 +32,11 @@ struct pkv_pool {
   pkv::TileMaps* maps;       // [num_layers]
   std::atomic<int>* ready;   // [num_layers]: 1 once maps[layer] is valid
   std::mutex maps_mutex;
+  int* window;               // [num_layers]: sliding window of the layer (0: none)
   ~pkv_pool() {
     delete[] maps;
     delete[] ready;
+    delete[] window;
   }
 };
 
@@ -199,6 +201,7 @@ pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q, const
   a.num_rows = num_rows;
   a.n_q = n_q;
   a.qscale = scale * 1.4426950408889634f;  // log2(e): base-2 softmax
+  a.window = pool->window[layer];
   a.out = out;
   a.part_ml = w.part_ml;
   a.part_acc = w.part_acc;
@@ -269,22 +272,43 @@ pkv_status kv_pool_create(pkv_pool** out, int num_layers, int num_pages, int n_k
   p->layer_scale_bytes = scale_bytes_per_layer(num_pages, n_kv_heads, head_dim, dtype);
   p->maps = nullptr;
   p->ready = nullptr;
+  p->window = nullptr;
   if (static_cast<long long>(num_pages) * n_kv_heads >= (1ll << 31)) {
     delete p;
     return fail(PKV_ERR_UNSUPPORTED, "num_pages * n_kv_heads must be below 2^31");
   }
   p->maps = new (std::nothrow) pkv::TileMaps[num_layers];
   p->ready = new (std::nothrow) std::atomic<int>[num_layers];
-  if (!p->maps || !p->ready) {
+  p->window = new (std::nothrow) int[num_layers];
+  if (!p->maps || !p->ready || !p->window) {
     delete p;
     return fail(PKV_ERR_INVALID_ARG, "out of host memory");
   }
-  for (int l = 0; l < num_layers; ++l) p->ready[l].store(0);
+  for (int l = 0; l < num_layers; ++l) {
+    p->ready[l].store(0);
+    p->window[l] = 0;
+  }
   *out = p;
   return PKV_OK;
 }
 
 void kv_pool_destroy(pkv_pool* pool) { delete pool; }
+
+pkv_status kv_pool_set_window(pkv_pool* pool, int layer, int window) {
+  pkv_status s = check_pool_layer(pool, layer);
+  if (s) return s;
+  if (window < 0) return fail(PKV_ERR_INVALID_ARG, "window < 0");
+  pool->window[layer] = window;
+  return PKV_OK;
+}
+
+pkv_status kv_pool_get_window(const pkv_pool* pool, int layer, int* window) {
+  pkv_status s = check_pool_layer(pool, layer);
+  if (s) return s;
+  if (!window) return fail(PKV_ERR_INVALID_ARG, "null window pointer");
+  *window = pool->window[layer];
+  return PKV_OK;
+}
 
 pkv_status kv_pool_read_status(const pkv_pool* pool, void* stream, int32_t* status) {
   if (!pool || !status) return fail(PKV_ERR_INVALID_ARG, "null pool or status pointer");
@@ -367,15 +391,16 @@ pkv_status paged_decode_split(const pkv_pool* pool, int layer, const float* q,
 }
 
 pkv_status paged_decode_plan(const int32_t* seq_lens, int num_rows, int n_kv_heads,
-                             int bt_stride, int num_chunks, int32_t* row_page_start,
+                             int bt_stride, int window, int num_chunks, int32_t* row_page_start,
                              int32_t* seg_first_chunk, int32_t* seg_last_chunk, void* stream) {
   pkv_status s = check_rows(num_rows, bt_stride, seq_lens, seq_lens);
   if (s) return s;
+  if (window < 0) return fail(PKV_ERR_INVALID_ARG, "window < 0");
   if (n_kv_heads <= 0 || num_chunks < 1)
     return fail(PKV_ERR_INVALID_ARG, "n_kv_heads and num_chunks must be positive");
   if (!row_page_start || (num_rows > 0 && (!seg_first_chunk || !seg_last_chunk)))
     return fail(PKV_ERR_INVALID_ARG, "null plan output");
-  pkv::PlanArgs a{seq_lens, num_rows, n_kv_heads, bt_stride, num_chunks,
+  pkv::PlanArgs a{seq_lens, window, num_rows, n_kv_heads, bt_stride, num_chunks,
                   row_page_start, seg_first_chunk, seg_last_chunk};
   cudaError_t e = pkv::launch_plan(a, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
@@ -383,11 +408,12 @@ pkv_status paged_decode_plan(const int32_t* seq_lens, int num_rows, int n_kv_hea
 }
 
 pkv_status paged_decode_combine(const int32_t* seq_lens, int num_rows, int n_q_heads,
-                                int n_kv_heads, int head_dim, int bt_stride, int num_chunks,
-                                const void* workspace, size_t workspace_bytes, float* out,
-                                void* stream) {
+                                int n_kv_heads, int head_dim, int bt_stride, int window,
+                                int num_chunks, const void* workspace, size_t workspace_bytes,
+                                float* out, void* stream) {
   pkv_status s = check_geometry(n_q_heads, n_kv_heads, head_dim);
   if (s) return s;
+  if (window < 0) return fail(PKV_ERR_INVALID_ARG, "window < 0");
   if ((s = check_rows(num_rows, bt_stride, seq_lens, seq_lens))) return s;
   if (num_chunks < 1) return fail(PKV_ERR_INVALID_ARG, "num_chunks < 1");
   if (num_rows > 0 && !out) return fail(PKV_ERR_INVALID_ARG, "null out");
@@ -401,6 +427,7 @@ pkv_status paged_decode_combine(const int32_t* seq_lens, int num_rows, int n_q_h
       workspace_parts(const_cast<void*>(workspace), num_rows, n_q_heads, n_kv_heads, num_chunks);
   pkv::CombineArgs c;
   c.seq_lens = seq_lens;
+  c.window = window;
   c.num_rows = num_rows;
   c.n_q = n_q_heads;
   c.n_kv = n_kv_heads;

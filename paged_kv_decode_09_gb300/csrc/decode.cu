@@ -271,14 +271,15 @@ __device__ __forceinline__ void load_query(const float* qrow, float qscale, int 
   S.qexp = ldexpf(1.0f, __shfl_sync(kFull, e2, 8 * tig));
 }
 
-// Process one staged (page, KV head) unit of nvalid tokens (1..16): tiles at
-// shared address `st` (K, then V at + kData), q8_0 scales at `sc` (K, then V
-// at + kScale).  Rows nvalid..15 of the tiles hold whatever the pool holds
-// there (possibly NaN): they are masked out of the scores, and f16 V rows are
-// zeroed before the values MMA.
+// Process one staged (page, KV head) unit whose attended tokens are slots
+// [tlo, nvalid) (0 <= tlo < nvalid <= 16; tlo > 0 only on the first page of
+// a sliding window): tiles at shared address `st` (K, then V at + kData),
+// q8_0 scales at `sc` (K, then V at + kScale).  The other rows hold whatever
+// the pool holds there (possibly NaN): they are masked out of the scores, and
+// f16 V rows are zeroed before the values MMA.
 template <int DT, int G>
-__device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int nvalid, int lane,
-                                             WarpState& S) {
+__device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int tlo, int nvalid,
+                                             int lane, WarpState& S) {
   using TL = Tiles<DT>;
   const int gid = lane >> 2, tig = lane & 3;
   // ldmatrix row addresses: lane 8j + r gives row r of matrix j = token
@@ -328,8 +329,8 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
       s1 = fmaf(ksc.y, c[2] + c[3], s1);
     }
   }
-  s0 = gid < nvalid ? s0 * S.qexp : -INFINITY;
-  s1 = gid + 8 < nvalid ? s1 * S.qexp : -INFINITY;
+  s0 = gid >= tlo && gid < nvalid ? s0 * S.qexp : -INFINITY;
+  s1 = gid + 8 >= tlo && gid + 8 < nvalid ? s1 * S.qexp : -INFINITY;
 
   // ---- online softmax of head tig over the page (its 8 lanes: xor 4, 8, 16)
   float mx = fmaxf(s0, s1);
@@ -363,9 +364,10 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
 
   // ---- values
   if constexpr (DT == PKV_KV_F16) {
-    if (nvalid < kPage) {  // zero the V rows past the valid tokens (NaN * 0 is NaN)
-      for (int x = lane; x < (kPage - nvalid) * 16; x += 32) {
-        const int t = nvalid + (x >> 4), c = x & 15;
+    if (tlo > 0 || nvalid < kPage) {  // zero the V rows of unattended slots (NaN * 0 is NaN)
+      const int n_out = kPage - (nvalid - tlo);
+      for (int x = lane; x < n_out * 16; x += 32) {
+        const int r = x >> 4, t = r < tlo ? r : nvalid + (r - tlo), c = x & 15;
         *reinterpret_cast<uint4*>(st + TL::kData + (c >> 3) * 2048 + t * 128 + (c & 7) * 16) =
             make_uint4(0u, 0u, 0u, 0u);
       }
@@ -384,11 +386,11 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
     // four f16 block scales of a token are 8 contiguous bytes
     uint4 va = *reinterpret_cast<const uint4*>(sc + TL::kScale + t0 * 8);
     uint4 vb = *reinterpret_cast<const uint4*>(sc + TL::kScale + (t0 + 8) * 8);
-    if (nvalid < kPage) {  // masked tokens have p = 0 but their scales may be NaN
-      if (t0 >= nvalid) va.x = va.y = 0u;
-      if (t0 + 1 >= nvalid) va.z = va.w = 0u;
-      if (t0 + 8 >= nvalid) vb.x = vb.y = 0u;
-      if (t0 + 9 >= nvalid) vb.z = vb.w = 0u;
+    if (tlo > 0 || nvalid < kPage) {  // masked tokens have p = 0 but their scales may be NaN
+      if (t0 < tlo || t0 >= nvalid) va.x = va.y = 0u;
+      if (t0 + 1 < tlo || t0 + 1 >= nvalid) va.z = va.w = 0u;
+      if (t0 + 8 < tlo || t0 + 8 >= nvalid) vb.x = vb.y = 0u;
+      if (t0 + 9 < tlo || t0 + 9 >= nvalid) vb.z = vb.w = 0u;
     }
     // the page's largest |scale|: non-negative f16 bit patterns order as integers
     uint32_t mb = __vmaxu2(__vmaxu2(va.x & 0x7fff7fffu, va.y & 0x7fff7fffu),
@@ -687,8 +689,8 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_F16 ? PKV_F16_CTAS_PER_
   // find room as ours exit).
   grid_dependency_wait();
   grid_launch_dependents();
-  plan_rows(a.seq_lens, a.num_rows, a.bt_stride, blockIdx.x == 0 ? a.status : nullptr, lens,
-            row_start);
+  plan_rows(a.seq_lens, a.num_rows, a.bt_stride, a.window, blockIdx.x == 0 ? a.status : nullptr,
+            lens, row_start);
 
   const long long T = static_cast<long long>(a.n_kv) * row_start[a.num_rows];
   const int C = used_chunks(T, gridDim.x), k = blockIdx.x;
@@ -722,8 +724,9 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_F16 ? PKV_F16_CTAS_PER_
       const int npg = row_start[i + 1] - row_start[i];
       const int off = static_cast<int>(x - static_cast<long long>(a.n_kv) * row_start[i]);
       hh = off / npg;
-      const int p = off - hh * npg;
-      int page = __ldg(a.block_table + static_cast<long long>(i) * a.bt_stride + p);
+      const int p = off - hh * npg;  // of the pages the row reads, from window_start / 16
+      int page = __ldg(a.block_table + static_cast<long long>(i) * a.bt_stride +
+                       window_start(lens[i], a.window) / kPage + p);
       last = (p == npg - 1) ? 1 : 0;
       if (page < 0 || page >= a.num_pages) {
         record_status(a.status, PKV_DEV_BAD_PAGE);
@@ -803,6 +806,8 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_F16 ? PKV_F16_CTAS_PER_
     const long long seg_end = seg_start + npg;
     const long long b = min(seg_end, c_end);
     const int L = lens[i];
+    const int ws = window_start(L, a.window);  // first attended token of the row
+    const int p0 = ws / kPage;                 // its page: the row's unit 0
     const long long j = static_cast<long long>(i) * a.n_kv + h;
     const int k0 = chunk_of(seg_start, T, C), k1 = chunk_of(seg_end - 1, T, C);
 
@@ -830,8 +835,10 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_F16 ? PKV_F16_CTAS_PER_
         continue;
       }
       consumed = u + 1;
-      const int nvalid = min(kPage, L - static_cast<int>(pos - seg_start) * kPage);
-      process_unit<DT, G>(ring + s * TL::kCodes, ring_sc + s * TL::kScales, nvalid, lane, S);
+      const int t_page = (p0 + static_cast<int>(pos - seg_start)) * kPage;  // page's first token
+      const int nvalid = min(kPage, L - t_page);
+      const int tlo = max(0, ws - t_page);
+      process_unit<DT, G>(ring + s * TL::kCodes, ring_sc + s * TL::kScales, tlo, nvalid, lane, S);
       if (issued < n_units) issue();
     }
 
@@ -968,7 +975,7 @@ __global__ void __launch_bounds__(kD) combine_kernel(const CombineArgs a) {
   extern __shared__ int csm[];
   int* row_start = csm;
   int* lens = csm + a.num_rows + 1;
-  plan_rows(a.seq_lens, a.num_rows, a.bt_stride, nullptr, lens, row_start);
+  plan_rows(a.seq_lens, a.num_rows, a.bt_stride, a.window, nullptr, lens, row_start);
   const int j = blockIdx.x, i = j / a.n_kv, h = j % a.n_kv, d = threadIdx.x;
   const int npg = row_start[i + 1] - row_start[i];
   float* o = a.out + (static_cast<long long>(i) * a.n_q + h * G) * kD;
@@ -990,7 +997,7 @@ __global__ void __launch_bounds__(256) plan_kernel(const PlanArgs a) {
   extern __shared__ int psm[];
   int* row_start = psm;
   int* lens = psm + a.num_rows + 1;
-  plan_rows(a.seq_lens, a.num_rows, a.bt_stride, nullptr, lens, row_start);
+  plan_rows(a.seq_lens, a.num_rows, a.bt_stride, a.window, nullptr, lens, row_start);
   for (int r = threadIdx.x; r <= a.num_rows; r += blockDim.x) a.row_page_start[r] = row_start[r];
   const long long T = static_cast<long long>(a.n_kv) * row_start[a.num_rows];
   const int C = used_chunks(T, a.num_chunks);

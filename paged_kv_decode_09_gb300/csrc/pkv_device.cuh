@@ -161,12 +161,20 @@ __device__ __forceinline__ void record_status(int32_t* status, uint32_t bits) {
 }
 
 // ---------------------------------------------------------------- plan ----
-// The per-CTA plan: validated lengths and the exclusive prefix sum of pages
-// per row, in shared memory.  lens[i] is seq_lens[i] clamped to
-// [0, 16 * bt_stride] (a clamp records PKV_DEV_BAD_LENGTH); row_start has
-// num_rows + 1 entries.  Warp 0 scans; every thread of the CTA must call it.
+// First attended token of a row of L tokens under a sliding window of W
+// tokens (W = 0: no window): the row attends to [window_start, L).
+__device__ __forceinline__ int window_start(int L, int window) {
+  return window > 0 && L > window ? L - window : 0;
+}
+
+// The per-CTA plan: validated lengths and the exclusive prefix sum of the
+// pages each row reads, in shared memory.  lens[i] is seq_lens[i] clamped to
+// [0, 16 * bt_stride] (a clamp records PKV_DEV_BAD_LENGTH); a row reads the
+// pages holding tokens [window_start, L), block-table entries
+// window_start / 16 onwards; row_start has num_rows + 1 entries.  Warp 0
+// scans; every thread of the CTA must call it.
 __device__ __forceinline__ void plan_rows(const int32_t* __restrict__ seq_lens, int num_rows,
-                                          int bt_stride, int32_t* status, int* lens,
+                                          int bt_stride, int window, int32_t* status, int* lens,
                                           int* row_start) {
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
@@ -184,7 +192,7 @@ __device__ __forceinline__ void plan_rows(const int32_t* __restrict__ seq_lens, 
         }
         lens[r] = L;
       }
-      int v = (L + kPage - 1) / kPage;
+      int v = L > 0 ? (L + kPage - 1) / kPage - window_start(L, window) / kPage : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int u = __shfl_up_sync(kFull, v, o);

@@ -29,6 +29,7 @@ struct DecodeArgs {
   int num_rows;
   int n_q;
   float qscale;  // softmax scale * log2(e): scores are kept in base 2
+  int window;    // > 0: each row attends to its last `window` tokens
   float* out;
   float* part_ml;   // [slots][G][2]
   float* part_acc;  // [slots][G][128]
@@ -38,6 +39,7 @@ struct DecodeArgs {
 
 struct CombineArgs {
   const int32_t* seq_lens;
+  int window;
   int num_rows;
   int n_q;
   int n_kv;
@@ -50,6 +52,7 @@ struct CombineArgs {
 
 struct PlanArgs {
   const int32_t* seq_lens;
+  int window;
   int num_rows;
   int n_kv;
   int bt_stride;

@@ -41,12 +41,12 @@ def encode_pool(wl: W.Workload, layer: int = 0, include_appended: bool = True,
     return kd, vd, ks, vs
 
 
-def oracle_decode(wl: W.Workload, pool, seq_lens=None, q=None, scale=None):
+def oracle_decode(wl: W.Workload, pool, seq_lens=None, q=None, scale=None, window=0):
     kd, vd, ks, vs = pool
     return O.decode_attention(wl.cfg.dtype, wl.q if q is None else q, kd, vd, ks, vs,
                               wl.block_table, wl.seq_lens if seq_lens is None else seq_lens,
                               wl.num_pages, wl.cfg.n_kv_heads,
-                              wl.scale if scale is None else scale)
+                              wl.scale if scale is None else scale, window=window)
 
 
 def stored_values_dense(dtype, data, scales):

@@ -28,7 +28,7 @@ MUTANTS = {
                          "return (double)((const int8_t *)data)[row * D + d];"),
     "wrong_q8_block_index": ("scales[row * (D / ORACLE_QBLOCK) + d / ORACLE_QBLOCK]",
                              "scales[row * (D / ORACLE_QBLOCK) + d % (D / ORACLE_QBLOCK)]"),
-    "softmax_sign": ("double p = exp(s[t] - m);", "double p = exp(m - s[t]);"),
+    "softmax_sign": ("double p = exp(s[t - a] - m);", "double p = exp(m - s[t - a]);"),
     "ties_to_odd": ("(rem == 0.5 && fmod(whole, 2.0) != 0.0)", "(rem == 0.5 && fmod(whole, 2.0) == 0.0)"),
     "ties_toward_plus_inf": ("return y < 0.0 ? -floor(-y + 0.5) : floor(y + 0.5);",
                              "return floor(y + 0.5);"),
