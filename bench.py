@@ -56,10 +56,13 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU baseline budget")
     p.add_argument("--window", type=int, default=0,
                    help="sliding window of every layer (0: none); bytes count attended tokens")
-    p.add_argument("--kernel", choices=["step", "append", "split_combine", "plan"], default="step",
+    p.add_argument("--kernel", choices=["step", "append", "split_combine", "plan", "alloc"],
+                   default="step",
                    help="step: the decode step (the benchmark); the others run --steps calls of\n"
                         "one other entry point on the workload and print its mean call time\n"
-                        "(for profiling those kernels alone; not the benchmark metric)")
+                        "(for profiling those kernels alone; not the benchmark metric);\n"
+                        "alloc: the host page allocator's work for one decode step of 256\n"
+                        "sequences (reserve 1, batch tables, commit 1)")
     return p.parse_args()
 
 
@@ -357,6 +360,40 @@ def run_ours(args, rank, world, local):
     return result
 
 
+def run_alloc(args):
+    """Host page allocator: per decode step, reserve one token for each of 256
+    sequences, write the batch's block tables and lengths, commit the token."""
+    from paged_kv_decode_09_gb300 import api
+    rows, stride = 256, 2048
+    a = api.PageAllocator(rows * stride, rows, stride)
+    seqs = []
+    for s in range(rows):
+        seqs.append(a.open())
+        a.reserve(seqs[-1], 4096)
+        a.commit(seqs[-1], 4096)
+    import numpy as np
+    ids = np.arange(rows, dtype=np.int32)
+    bt = np.empty((rows, stride), np.int32)
+    sl = np.empty(rows, np.int32)
+    L = api.lib()
+
+    def step():
+        L.pkv_alloc_reserve_many(a.handle, ids.ctypes.data, rows, 1)
+        L.pkv_alloc_batch(a.handle, ids.ctypes.data, rows, 1, bt.ctypes.data, stride,
+                          sl.ctypes.data)
+        L.pkv_alloc_commit_many(a.handle, ids.ctypes.data, rows, 1)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    return {"kernel": "alloc", "rows": rows, "bt_stride": stride, "calls": args.steps,
+            "mean_step_us": round(dt * 1e6, 2),
+            "note": "host allocator work per decode step through ctypes; not the benchmark metric"}
+
+
 def run_kernel(args, local):
     """--steps calls of one entry point other than the decode step, timed with
     events on the stream: kv_append (new K/V of every row), paged_decode_split
@@ -521,6 +558,9 @@ def main():
         # host-only: rank 0 alone times the oracle, the other ranks exit at once
         if int(os.environ.get("RANK", "0")) == 0:
             print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.kernel == "alloc":
+        print(json.dumps(run_alloc(args)), flush=True)
         return
     if args.kernel != "step":
         print(json.dumps(run_kernel(args, int(os.environ.get("LOCAL_RANK", "0")))), flush=True)

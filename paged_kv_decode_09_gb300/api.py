@@ -56,6 +56,22 @@ _SIGS = {
     "paged_decode_plan": ([_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp], _i),
     "paged_decode_combine": ([_vp, _i, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp], _i),
     "kv_pool_set_window": ([_vp, _i, _i], _i),
+    "pkv_alloc_create": ([ctypes.POINTER(_vp), _i, _i, _i], _i),
+    "pkv_alloc_destroy": ([_vp], None),
+    "pkv_alloc_open": ([_vp, ctypes.POINTER(_i)], _i),
+    "pkv_alloc_reserve": ([_vp, _i, _i], _i),
+    "pkv_alloc_commit": ([_vp, _i, _i], _i),
+    "pkv_alloc_reserve_many": ([_vp, _vp, _i, _i], _i),
+    "pkv_alloc_commit_many": ([_vp, _vp, _i, _i], _i),
+    "pkv_alloc_unreserve": ([_vp, _i, _i], _i),
+    "pkv_alloc_fork": ([_vp, _i, ctypes.POINTER(_i)], _i),
+    "pkv_alloc_release": ([_vp, _i], _i),
+    "pkv_alloc_seq_info": ([_vp, _i, ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i)],
+                           _i),
+    "pkv_alloc_block_table": ([_vp, _i, _vp, _i], _i),
+    "pkv_alloc_batch": ([_vp, _vp, _i, _i, _vp, _i, _vp], _i),
+    "pkv_alloc_stats": ([_vp, ctypes.POINTER(_i), ctypes.POINTER(_i), ctypes.POINTER(_i)], _i),
+    "pkv_alloc_page_refs": ([_vp, _i, ctypes.POINTER(_i)], _i),
     "kv_pool_get_window": ([_vp, _i, ctypes.POINTER(_i)], _i),
     "pkv_decode_step": ([_vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, ctypes.c_float, _vp, _vp,
                          _sz, _i, _vp], _i),
@@ -310,3 +326,90 @@ def paged_decode_combine(seq_lens, n_q_heads: int, n_kv_heads: int, bt_stride: i
                                       workspace.numel(),
                                       _ptr(out), _stream(stream)), "paged_decode_combine")
     return out
+
+
+class PageAllocator:
+    """The library's host page allocator (include/pkv_alloc.h): page ids of a
+    pool, sequences with block tables, reserve/commit/unreserve/fork/release.
+    Raises PkvError with status PKV_ERR_CAPACITY (3) on overload."""
+
+    def __init__(self, num_pages: int, max_seqs: int, max_pages_per_seq: int):
+        import numpy as np  # noqa: F401  (used by batch)
+        h = ctypes.c_void_p()
+        _check(lib().pkv_alloc_create(ctypes.byref(h), num_pages, max_seqs, max_pages_per_seq),
+               "pkv_alloc_create")
+        self.handle, self.num_pages, self.max_pages_per_seq = h, num_pages, max_pages_per_seq
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h and _lib is not None:
+            _lib.pkv_alloc_destroy(h)
+            self.handle = None
+
+    def open(self) -> int:
+        s = ctypes.c_int(0)
+        _check(lib().pkv_alloc_open(self.handle, ctypes.byref(s)), "pkv_alloc_open")
+        return s.value
+
+    def reserve(self, seq: int, n: int):
+        _check(lib().pkv_alloc_reserve(self.handle, seq, n), "pkv_alloc_reserve")
+
+    def commit(self, seq: int, n: int):
+        _check(lib().pkv_alloc_commit(self.handle, seq, n), "pkv_alloc_commit")
+
+    def reserve_many(self, seqs, n: int):
+        import numpy as np
+        ids = np.ascontiguousarray(seqs, np.int32)
+        _check(lib().pkv_alloc_reserve_many(self.handle, ids.ctypes.data, len(ids), n),
+               "pkv_alloc_reserve_many")
+
+    def commit_many(self, seqs, n: int):
+        import numpy as np
+        ids = np.ascontiguousarray(seqs, np.int32)
+        _check(lib().pkv_alloc_commit_many(self.handle, ids.ctypes.data, len(ids), n),
+               "pkv_alloc_commit_many")
+
+    def unreserve(self, seq: int, n: int):
+        _check(lib().pkv_alloc_unreserve(self.handle, seq, n), "pkv_alloc_unreserve")
+
+    def fork(self, parent: int) -> int:
+        c = ctypes.c_int(0)
+        _check(lib().pkv_alloc_fork(self.handle, parent, ctypes.byref(c)), "pkv_alloc_fork")
+        return c.value
+
+    def release(self, seq: int):
+        _check(lib().pkv_alloc_release(self.handle, seq), "pkv_alloc_release")
+
+    def info(self, seq: int):
+        c, r, p = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+        _check(lib().pkv_alloc_seq_info(self.handle, seq, ctypes.byref(c), ctypes.byref(r),
+                                        ctypes.byref(p)), "pkv_alloc_seq_info")
+        return c.value, r.value, p.value
+
+    def block_table(self, seq: int, stride: int):
+        import numpy as np
+        row = np.empty(stride, np.int32)
+        _check(lib().pkv_alloc_block_table(self.handle, seq, row.ctypes.data, stride),
+               "pkv_alloc_block_table")
+        return row
+
+    def batch(self, seqs, extra: int, stride: int):
+        """(block_table int32 [rows][stride], seq_lens int32 [rows]) host arrays."""
+        import numpy as np
+        ids = np.ascontiguousarray(seqs, np.int32)
+        bt = np.empty((len(ids), stride), np.int32)
+        sl = np.empty(len(ids), np.int32)
+        _check(lib().pkv_alloc_batch(self.handle, ids.ctypes.data, len(ids), extra, bt.ctypes.data,
+                                     stride, sl.ctypes.data), "pkv_alloc_batch")
+        return bt, sl
+
+    def stats(self):
+        f, u, s = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+        _check(lib().pkv_alloc_stats(self.handle, ctypes.byref(f), ctypes.byref(u),
+                                     ctypes.byref(s)), "pkv_alloc_stats")
+        return f.value, u.value, s.value
+
+    def page_refs(self, page: int) -> int:
+        r = ctypes.c_int(0)
+        _check(lib().pkv_alloc_page_refs(self.handle, page, ctypes.byref(r)), "pkv_alloc_page_refs")
+        return r.value

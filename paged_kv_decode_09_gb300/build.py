@@ -32,7 +32,8 @@ def sources():
 
 def _deps():
     return sources() + [os.path.join(CSRC, f) for f in os.listdir(CSRC)
-                        if f.endswith((".cuh", ".h"))] + [os.path.join(INCLUDE, "pkv.h")]
+                        if f.endswith((".cuh", ".h"))] + \
+        [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
 
 
 def _stale() -> bool:

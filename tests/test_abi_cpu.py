@@ -1,5 +1,5 @@
 """The C ABI without a GPU: libpkv.so builds and loads, exports every function
-include/pkv.h declares, and rejects bad arguments on the host before any CUDA
+the headers under include/ declare, and rejects bad arguments on the host before any CUDA
 call (so these calls are safe on a machine without a device)."""
 import ctypes
 import os
@@ -24,7 +24,9 @@ def lib():
 
 
 def _declared():
-    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    inc = os.path.join(ROOT, "include")
+    text = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc))
+                   if f.endswith(".h"))
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)) -
                   {"if", "sizeof", "defined"})
@@ -34,7 +36,7 @@ def test_every_declared_function_is_exported(lib):
     names = _declared()
     assert {"kv_pool_create", "kv_append", "paged_decode_attention"} <= set(names)
     for n in names:
-        assert hasattr(lib, n), f"{n} declared in pkv.h but not exported"
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
 
 
 def test_pool_bytes(lib):
