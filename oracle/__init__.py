@@ -24,7 +24,7 @@ import numpy as np
 
 from . import build as _build
 
-F16, Q8_0 = 0, 1
+F16, Q8_0, BF16 = 0, 1, 2
 PAGE = 16
 QBLOCK = 32
 
@@ -61,6 +61,12 @@ def lib():
             L.oracle_q8_0_encode.restype = None
             L.oracle_f16_encode.argtypes = [_f32p, ctypes.c_int64, _u16p]
             L.oracle_f16_encode.restype = None
+            L.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
+            L.oracle_bf16_to_f64.restype = ctypes.c_double
+            L.oracle_bf16_from_f32.argtypes = [ctypes.c_float]
+            L.oracle_bf16_from_f32.restype = ctypes.c_uint16
+            L.oracle_bf16_encode.argtypes = [_f32p, ctypes.c_int64, _u16p]
+            L.oracle_bf16_encode.restype = None
             L.oracle_kv_append.argtypes = [_i, _i, _i, _i, _f32p, _f32p, _i32p, _i, _i32p, _i,
                                            _vp, _vp, _vp, _vp]
             L.oracle_kv_append.restype = _i
@@ -115,6 +121,24 @@ def f16_decode(bits: np.ndarray) -> np.ndarray:
     return f(np.asarray(bits, np.uint16))
 
 
+def bf16_from_f32(x: float) -> int:
+    """Bits of the bfloat16 nearest to fp32 x, ties to even."""
+    return int(lib().oracle_bf16_from_f32(float(np.float32(x))))
+
+
+def bf16_to_f64(bits: int) -> float:
+    """Exact value of a bfloat16 bit pattern."""
+    return float(lib().oracle_bf16_to_f64(int(bits) & 0xFFFF))
+
+
+def bf16_encode(x: np.ndarray) -> np.ndarray:
+    """Elementwise bfloat16 bits (uint16) of an fp32 array, ties to even."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, np.uint16)
+    lib().oracle_bf16_encode(x.reshape(-1), x.size, out.reshape(-1))
+    return out
+
+
 # ----------------------------------------------------------------- q8_0 ----
 def q8_0_encode_block(x: np.ndarray):
     """(codes int8[32], scale bits uint16, fp32 d) of one 32-value block."""
@@ -139,10 +163,12 @@ def q8_0_encode(x: np.ndarray):
 def encode_pool(dtype: int, values: np.ndarray):
     """Store fp32 values [pages][n_kv][16][D] in the pool dtype: (data, scales).
 
-    f16: data uint16 bits, scales None.  q8_0: data int8 codes, scales uint16
-    [pages][n_kv][16][D/32]."""
+    f16 / bf16: data uint16 bits, scales None.  q8_0: data int8 codes, scales
+    uint16 [pages][n_kv][16][D/32]."""
     if dtype == F16:
         return f16_encode(values), None
+    if dtype == BF16:
+        return bf16_encode(values), None
     return q8_0_encode(values)
 
 

@@ -12,7 +12,8 @@
  *     provides" (a runner-owned physical KV page pool with a logical block
  *     table per active sequence) and "Known limitations" (16-token pages).
  *   - KV storage as f16 and q8/q8_0: Leone, "What ships" (f32, f16 and q8 KV
- *     storage); LeatEngine, "Run" (--cache-type q8_0 keeps the KV cache the
+ *     storage); tinyllm, "The repository currently provides" (BF16/F32 KV
+ *     caching); LeatEngine, "Run" (--cache-type q8_0 keeps the KV cache the
  *     way llama.cpp's q8_0 cache does, in about half the memory of f16).
  *     q8_0 here: blocks of 32 consecutive head_dim values, one f16 scale per
  *     block, d = amax/127, codes round(x/d) with ties away from zero.
@@ -61,7 +62,7 @@
 #define ORACLE_PAGE 16 /* tokens per physical page (tinyllm, Known limitations) */
 #define ORACLE_QBLOCK 32 /* q8_0 block length along head_dim */
 
-enum { ORACLE_F16 = 0, ORACLE_Q8_0 = 1 };
+enum { ORACLE_F16 = 0, ORACLE_Q8_0 = 1, ORACLE_BF16 = 2 };
 enum { ORACLE_OK = 0, ORACLE_BAD_ARG = 1, ORACLE_BAD_PAGE = 2 };
 
 int oracle_num_threads(void) {
@@ -125,6 +126,62 @@ uint16_t oracle_f16_from_f32(float xf) {
     return (uint16_t)(sign | (expo << 10) | frac);
 }
 
+/* ----------------------------------------------------------------- bf16 --- */
+
+/* Exact value of a bfloat16 bit pattern (the high half of a binary32: 1 sign
+ * bit, 8 exponent bits with bias 127, 7 fraction bits), widened to double. */
+double oracle_bf16_to_f64(uint16_t b) {
+    int sign = (b >> 15) & 1;
+    int expo = (b >> 7) & 0xff;
+    int frac = b & 0x7f;
+    double mag;
+    if (expo == 0)
+        mag = ldexp((double)frac, -133); /* subnormal: frac * 2^(1-127-7) */
+    else if (expo == 255)
+        mag = frac ? NAN : INFINITY;
+    else
+        mag = ldexp((double)(128 + frac), expo - 134); /* (1.frac) * 2^(expo-127) */
+    return sign ? -mag : mag;
+}
+
+/* Round an fp32 value to the nearest bfloat16, ties to even, returning its
+ * bit pattern; written from the definition like the binary16 rounding above:
+ * 8 significant bits, spacing 2^-133 below 2^-126, and magnitudes that round
+ * to 2^128 (the midpoint (2 - 2^-8) * 2^127 included: it ties to the even
+ * side, the infinity) overflow to infinity. */
+uint16_t oracle_bf16_from_f32(float xf) {
+    double x = (double)xf; /* exact */
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (isnan(x)) return (uint16_t)(sign | 0x7fc0);
+    if (a >= ldexp(2.0 - ldexp(1.0, -8), 127)) return (uint16_t)(sign | 0x7f80);
+    double ulp;
+    if (a < ldexp(1.0, -126)) {
+        ulp = ldexp(1.0, -133);
+    } else {
+        int e;
+        frexp(a, &e);            /* a in [2^(e-1), 2^e) */
+        ulp = ldexp(1.0, e - 8); /* 8 significant bits */
+    }
+    double n = a / ulp;
+    double whole = floor(n);
+    double rem = n - whole;
+    if (rem > 0.5 || (rem == 0.5 && fmod(whole, 2.0) != 0.0)) whole += 1.0;
+    double r = whole * ulp;
+    if (r == 0.0) return sign;
+    if (r < ldexp(1.0, -126)) return (uint16_t)(sign | (uint16_t)(r / ldexp(1.0, -133)));
+    int e;
+    double m = frexp(r, &e);     /* r = m * 2^e, m in [0.5, 1) */
+    int expo = e - 1 + 127;
+    int frac = (int)((2.0 * m - 1.0) * 128.0);
+    return (uint16_t)(sign | (expo << 7) | frac);
+}
+
+/* Encode n fp32 values to bfloat16 bit patterns. */
+void oracle_bf16_encode(const float *x, int64_t n, uint16_t *out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_from_f32(x[i]);
+}
+
 /* ----------------------------------------------------------------- q8_0 --- */
 
 /* Round half away from zero, on a value whose magnitude is far below 2^52. */
@@ -171,14 +228,16 @@ void oracle_f16_encode(const float *x, int64_t n, uint16_t *out) {
 /* ------------------------------------------------------------ the pool --- */
 
 /* Stored value of element d of slot `slot` of (page, kv_head), widened to
- * double.  f16: the binary16 value.  q8_0: f16 scale of the element's block
- * times its int8 code.  Layout per layer (a reading; the pages fix none):
- *   data   [num_pages][n_kv][16][D]        (f16 bits, or int8 codes)
+ * double.  f16 / bf16: the binary16 / bfloat16 value.  q8_0: f16 scale of
+ * the element's block times its int8 code.  Layout per layer (a reading; the
+ * pages fix none):
+ *   data   [num_pages][n_kv][16][D]        (f16 or bf16 bits, or int8 codes)
  *   scales [num_pages][n_kv][16][D / 32]   (f16 bits; q8_0 only)           */
 static double stored(int dtype, const void *data, const uint16_t *scales, int n_kv,
                      int D, int64_t page, int kvh, int slot, int d) {
     int64_t row = (page * n_kv + kvh) * ORACLE_PAGE + slot;
     if (dtype == ORACLE_F16) return oracle_f16_to_f64(((const uint16_t *)data)[row * D + d]);
+    if (dtype == ORACLE_BF16) return oracle_bf16_to_f64(((const uint16_t *)data)[row * D + d]);
     double sc = oracle_f16_to_f64(scales[row * (D / ORACLE_QBLOCK) + d / ORACLE_QBLOCK]);
     return sc * (double)((const int8_t *)data)[row * D + d];
 }
@@ -213,6 +272,9 @@ int oracle_kv_append(int dtype, int num_rows, int n_kv, int D, const float *k_ne
             if (dtype == ORACLE_F16) {
                 oracle_f16_encode(kx, D, (uint16_t *)k_data + row * D);
                 oracle_f16_encode(vx, D, (uint16_t *)v_data + row * D);
+            } else if (dtype == ORACLE_BF16) {
+                oracle_bf16_encode(kx, D, (uint16_t *)k_data + row * D);
+                oracle_bf16_encode(vx, D, (uint16_t *)v_data + row * D);
             } else {
                 oracle_q8_0_encode(kx, D, (int8_t *)k_data + row * D,
                                    k_scales + row * (D / ORACLE_QBLOCK));

@@ -27,8 +27,8 @@ from dataclasses import dataclass, field
 import numpy as np
 
 PAGE = 16
-F16, Q8_0 = 0, 1
-DTYPE_NAMES = {F16: "f16", Q8_0: "q8_0"}
+F16, Q8_0, BF16 = 0, 1, 2
+DTYPE_NAMES = {F16: "f16", Q8_0: "q8_0", BF16: "bf16"}
 
 
 @dataclass(frozen=True)

@@ -12,6 +12,7 @@ import oracle as O
 from paged_kv_decode_09_gb300 import workloads as W
 
 F16_NAN = np.uint16(0x7E00)
+BF16_NAN = np.uint16(0x7FC0)
 
 
 def encode_pool(wl: W.Workload, layer: int = 0, include_appended: bool = True,
@@ -33,6 +34,9 @@ def encode_pool(wl: W.Workload, layer: int = 0, include_appended: bool = True,
         if cfg.dtype == W.F16:
             kd[sel] = F16_NAN
             vd[sel] = F16_NAN
+        elif cfg.dtype == W.BF16:
+            kd[sel] = BF16_NAN
+            vd[sel] = BF16_NAN
         else:
             ks[sel] = F16_NAN
             vs[sel] = F16_NAN
@@ -54,6 +58,8 @@ def stored_values_dense(dtype, data, scales):
     widening (a route independent of the oracle's)."""
     if dtype == W.F16:
         return data.view(np.float16).astype(np.float64)
+    if dtype == W.BF16:  # the high half of a binary32
+        return (data.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     sc = scales.view(np.float16).astype(np.float64)
     return np.repeat(sc, 32, axis=-1) * data.astype(np.float64)
 

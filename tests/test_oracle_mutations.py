@@ -13,7 +13,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "pkv_oracle.c")
-PINS = ["tests/test_oracle_f16.py", "tests/test_oracle_q8_0.py",
+PINS = ["tests/test_oracle_f16.py", "tests/test_oracle_q8_0.py", "tests/test_oracle_bf16.py",
         "tests/test_oracle_attention.py", "tests/test_oracle_plan_append.py"]
 
 MUTANTS = {
@@ -38,6 +38,10 @@ MUTANTS = {
                       "int64_t a = (int64_t)n_kv * row_page_start[i] + h, b = a + npg;"),
     "append_slot": ("int slot = pos % ORACLE_PAGE;", "int slot = L % ORACLE_PAGE;"),
     "partial_base_e": ("double p = exp2(s[t - t0] - m);", "double p = exp(s[t - t0] - m);"),
+    "bf16_eight_fraction_bits": ("ulp = ldexp(1.0, e - 8); /* 8 significant bits */",
+                                 "ulp = ldexp(1.0, e - 9); /* 8 significant bits */"),
+    "bf16_exponent_bias": ("mag = ldexp((double)(128 + frac), expo - 134);",
+                           "mag = ldexp((double)(128 + frac), expo - 133);"),
     "window_one_too_short": ("return window > 0 && L > window ? L - window : 0;",
                              "return window > 0 && L > window ? L - window + 1 : 0;"),
     "window_first_page_rounded_up": (
