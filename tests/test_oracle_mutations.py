@@ -29,7 +29,10 @@ MUTANTS = {
     "wrong_q8_block_index": ("scales[row * (D / ORACLE_QBLOCK) + d / ORACLE_QBLOCK]",
                              "scales[row * (D / ORACLE_QBLOCK) + d % (D / ORACLE_QBLOCK)]"),
     "softmax_sign": ("double p = exp(s[t - a] - m);", "double p = exp(m - s[t - a]);"),
-    "ties_to_odd": ("(rem == 0.5 && fmod(whole, 2.0) != 0.0)", "(rem == 0.5 && fmod(whole, 2.0) == 0.0)"),
+    "ties_to_odd": ("double rem = n - whole;  /* exact */\n    if (rem > 0.5 || (rem == 0.5 && fmod(whole, 2.0) != 0.0))",
+                    "double rem = n - whole;  /* exact */\n    if (rem > 0.5 || (rem == 0.5 && fmod(whole, 2.0) == 0.0))"),
+    "bf16_ties_to_odd": ("double rem = n - whole;\n    if (rem > 0.5 || (rem == 0.5 && fmod(whole, 2.0) != 0.0))",
+                         "double rem = n - whole;\n    if (rem > 0.5 || (rem == 0.5 && fmod(whole, 2.0) == 0.0))"),
     "ties_toward_plus_inf": ("return y < 0.0 ? -floor(-y + 0.5) : floor(y + 0.5);",
                              "return floor(y + 0.5);"),
     "q8_scale_126": ("float d = fdiv32(amax, 127.0f);", "float d = fdiv32(amax, 126.0f);"),
