@@ -85,15 +85,20 @@ typedef enum pkv_status {
 #define PKV_DEV_BAD_LENGTH 2u /* seq_lens[i] < 0 or > 16 * bt_stride: clamped */
 #define PKV_DEV_TIMEOUT 4u    /* a bounded wait on a shared-memory barrier gave up */
 
+/* Stored KV formats: binary16; q8_0 (int8 codes + one binary16 scale per 32
+ * values along head_dim); bfloat16 (tinyllm, "The repository currently
+ * provides": BF16/F32 KV caching), rounded to nearest even. */
 typedef enum pkv_kv_dtype {
     PKV_KV_F16 = 0,
     PKV_KV_Q8_0 = 1,
+    PKV_KV_BF16 = 2,
 } pkv_kv_dtype;
 
 typedef struct pkv_pool pkv_pool;
 
 /* Bytes of one pool array for all layers: which = 0 the data array (K or V),
- * which = 1 the q8_0 scale array (0 for f16).  Returns 0 for invalid sizes. */
+ * which = 1 the q8_0 scale array (0 for f16 and bf16).  Returns 0 for
+ * invalid sizes. */
 size_t kv_pool_bytes(int num_layers, int num_pages, int n_kv_heads, int head_dim,
                      pkv_kv_dtype dtype, int which);
 

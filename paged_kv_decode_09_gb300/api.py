@@ -14,7 +14,8 @@ import threading
 
 import torch
 
-F16, Q8_0 = 0, 1
+F16, Q8_0, BF16 = 0, 1, 2
+_TORCH_DTYPE = {F16: torch.float16, Q8_0: torch.int8, BF16: torch.bfloat16}
 PAGE = 16
 HEAD_DIM = 128
 Q8_BLOCK = 32
@@ -134,7 +135,8 @@ def _need(t, dtype, name, shape=None, device=None):
 class KVPool:
     """A caller-owned paged KV pool (torch tensors) and its library descriptor.
 
-    k_data / v_data: [layers][pages][n_kv][16][128] float16 (f16) or int8 (q8_0);
+    k_data / v_data: [layers][pages][n_kv][16][128] float16 (f16), int8 (q8_0) or
+    bfloat16 (bf16);
     k_scales / v_scales (q8_0): [layers][pages][n_kv][16][4] float16;
     status: int32 [1] device status word."""
 
@@ -148,7 +150,7 @@ class KVPool:
         shape = (num_layers, num_pages, n_kv_heads, PAGE, head_dim)
         sshape = (num_layers, num_pages, n_kv_heads, PAGE, head_dim // Q8_BLOCK)
         if tensors is None:
-            tdt = torch.float16 if dtype == F16 else torch.int8
+            tdt = _TORCH_DTYPE[dtype]
             tensors = [torch.empty(shape, dtype=tdt, device=self.device),
                        torch.empty(shape, dtype=tdt, device=self.device)]
             if dtype == Q8_0:
@@ -157,7 +159,7 @@ class KVPool:
         self.k_data, self.v_data = tensors[0], tensors[1]
         self.k_scales = tensors[2] if dtype == Q8_0 else None
         self.v_scales = tensors[3] if dtype == Q8_0 else None
-        tdt = torch.float16 if dtype == F16 else torch.int8
+        tdt = _TORCH_DTYPE[dtype]
         for name in ("k_data", "v_data"):
             _need(getattr(self, name), tdt, name, shape, self.device)
         if dtype == Q8_0:

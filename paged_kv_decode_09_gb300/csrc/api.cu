@@ -62,7 +62,7 @@ cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 size_t data_bytes_per_layer(int num_pages, int n_kv, int head_dim, pkv_kv_dtype dtype) {
   const size_t elems = static_cast<size_t>(num_pages) * n_kv * PKV_PAGE_TOKENS * head_dim;
-  return dtype == PKV_KV_F16 ? elems * 2 : elems;
+  return dtype == PKV_KV_Q8_0 ? elems : elems * 2;  // f16, bf16: 2 bytes
 }
 
 size_t scale_bytes_per_layer(int num_pages, int n_kv, int head_dim, pkv_kv_dtype dtype) {
@@ -227,7 +227,8 @@ extern "C" {
 size_t kv_pool_bytes(int num_layers, int num_pages, int n_kv_heads, int head_dim,
                      pkv_kv_dtype dtype, int which) {
   if (num_layers <= 0 || num_pages <= 0 || n_kv_heads <= 0 || head_dim <= 0 ||
-      head_dim % PKV_Q8_BLOCK || (dtype != PKV_KV_F16 && dtype != PKV_KV_Q8_0))
+      head_dim % PKV_Q8_BLOCK ||
+      (dtype != PKV_KV_F16 && dtype != PKV_KV_Q8_0 && dtype != PKV_KV_BF16))
     return 0;
   const size_t per = which == 0 ? data_bytes_per_layer(num_pages, n_kv_heads, head_dim, dtype)
                                 : scale_bytes_per_layer(num_pages, n_kv_heads, head_dim, dtype);
@@ -241,7 +242,7 @@ pkv_status kv_pool_create(pkv_pool** out, int num_layers, int num_pages, int n_k
   *out = nullptr;
   if (num_layers <= 0 || num_pages <= 0 || n_kv_heads <= 0)
     return fail(PKV_ERR_INVALID_ARG, "pool sizes must be positive");
-  if (dtype != PKV_KV_F16 && dtype != PKV_KV_Q8_0)
+  if (dtype != PKV_KV_F16 && dtype != PKV_KV_Q8_0 && dtype != PKV_KV_BF16)
     return fail(PKV_ERR_INVALID_ARG, "unknown KV dtype %d", static_cast<int>(dtype));
   if (head_dim != PKV_HEAD_DIM) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d != 128", head_dim);
   if (!k_data || !v_data) return fail(PKV_ERR_INVALID_ARG, "null K or V data");
@@ -252,7 +253,7 @@ pkv_status kv_pool_create(pkv_pool** out, int num_layers, int num_pages, int n_k
     if (!aligned(k_scales, 16) || !aligned(v_scales, 16))
       return fail(PKV_ERR_INVALID_ARG, "scale arrays not 16-byte aligned");
   } else if (k_scales || v_scales) {
-    return fail(PKV_ERR_INVALID_ARG, "f16 pool takes no scale arrays");
+    return fail(PKV_ERR_INVALID_ARG, "f16 and bf16 pools take no scale arrays");
   }
   if (device_status && !aligned(device_status, 4))
     return fail(PKV_ERR_INVALID_ARG, "status word not 4-byte aligned");

@@ -110,6 +110,8 @@ struct Tiles<PKV_KV_F16> {
   static constexpr int kRing = PKV_F16_RING;  // stages per warp
 };
 template <>
+struct Tiles<PKV_KV_BF16> : Tiles<PKV_KV_F16> {};  // same geometry: 16-bit values
+template <>
 struct Tiles<PKV_KV_Q8_0> {
   static constexpr uint32_t kData = kPage * kD;                   // 2048 codes
   static constexpr uint32_t kScale = kPage * (kD / kQBlock) * 2;  // 128 bytes of f16 scales
@@ -146,7 +148,7 @@ struct Smem {
 // keep dims 64..127 in a second 2 KiB half.
 template <int DT>
 __device__ __forceinline__ uint32_t tile_offset(int t, int c) {
-  if constexpr (DT == PKV_KV_F16)
+  if constexpr (DT != PKV_KV_Q8_0)
     return (c >> 3) * 2048 + t * 128 + (((c & 7) ^ (t & 7)) << 4);
   else
     return t * 128 + ((c ^ (t & 7)) << 4);
@@ -165,6 +167,13 @@ __device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t u) {
 }
 constexpr uint32_t kSelB01 = 0x4140, kSelB23 = 0x4342, kSelB02 = 0x4240, kSelB13 = 0x4341;
 
+// The tf32 part of x (`lo` false: its rounding; true: the rounding of the
+// remainder), as an fp32 bit pattern.
+__device__ __forceinline__ uint32_t tf32_part(float x, bool lo) {
+  const uint32_t h = to_tf32(x);
+  return lo ? to_tf32(x - __uint_as_float(h)) : h;
+}
+
 // The f16 part (`lo` false: the rounding of x; true: the rounding of the
 // remainder) of a pair, low half x0.
 __device__ __forceinline__ uint32_t split_f16x2(float x0, float x1, bool lo) {
@@ -177,8 +186,10 @@ __device__ __forceinline__ uint32_t split_f16x2(float x0, float x1, bool lo) {
 }
 
 // Per-warp online softmax state for one piece.
+template <int DT>
 struct WarpState {
-  uint32_t qb[8][2];  // B operand of the scores per k-step: column gid (head gid/2, part gid%2)
+  static constexpr int kSteps = DT == PKV_KV_BF16 ? 16 : 8;  // score k-steps (tf32: 8 dims)
+  uint32_t qb[kSteps][2];  // B operand of the scores per k-step: column gid (head gid/2, part gid%2)
   float qexp;         // 2^e of head tig: undoes its power-of-two normalisation
   float m;            // running max (base 2) of head tig, equal on its 8 lanes
   float l;            // this lane's share of head tig's sum of probabilities
@@ -197,9 +208,11 @@ __device__ __forceinline__ float pow2i(int e) {  // 2^e for -126 <= e <= 127
   return __int_as_float((127 + e) << 23);
 }
 template <int DT>
-__device__ __forceinline__ float o_scale(const WarpState& S) {
+__device__ __forceinline__ float o_scale(const WarpState<DT>& S) {
   if constexpr (DT == PKV_KV_F16)
     return 1.0f / (1 << kPShift);
+  else if constexpr (DT == PKV_KV_BF16)
+    return 1.0f;  // tf32 parts have the fp32 exponent range: no scaling
   else
     return pow2i(S.vx - kPShift);
 }
@@ -208,7 +221,7 @@ __device__ __forceinline__ float o_scale(const WarpState& S) {
 // 4 gid + tig.
 template <int DT>
 __device__ __forceinline__ int dim_of(int r, int e, int gid) {
-  if constexpr (DT == PKV_KV_F16)
+  if constexpr (DT != PKV_KV_Q8_0)
     return 16 * r + gid + (e ? 8 : 0);
   else
     return 16 * r + 2 * gid + (e ? 1 : 0);
@@ -221,54 +234,66 @@ __device__ __forceinline__ int dim_of(int r, int e, int gid) {
 // largest |q| lies in [2^13, 2^14) and both f16 parts stay normal.
 template <int DT, int G>
 __device__ __forceinline__ void load_query(const float* qrow, float qscale, int lane,
-                                           WarpState& S) {
+                                           WarpState<DT>& S) {
   const int gid = lane >> 2, tig = lane & 3, g2 = gid >> 1;
   const bool lo = (gid & 1) != 0;
-  float v[32];
+  if constexpr (DT == PKV_KV_BF16) {
+    // tf32 k-steps of 8 dims: k = tig <- dim 8ks + 2tig, k = tig + 4 <- dim 8ks + 2tig + 1
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    if (g2 < G) {
-      const float* qh = qrow + g2 * kD;
-      if constexpr (DT == PKV_KV_F16) {
-        const float2 x = __ldg(reinterpret_cast<const float2*>(qh + 16 * ks + 2 * tig));
-        const float2 y = __ldg(reinterpret_cast<const float2*>(qh + 16 * ks + 8 + 2 * tig));
-        v[4 * ks] = x.x;
-        v[4 * ks + 1] = x.y;
-        v[4 * ks + 2] = y.x;
-        v[4 * ks + 3] = y.y;
-      } else {
-        const float4 x = __ldg(reinterpret_cast<const float4*>(qh + 16 * ks + 4 * tig));
-        v[4 * ks] = x.x;
-        v[4 * ks + 1] = x.y;
-        v[4 * ks + 2] = x.z;
-        v[4 * ks + 3] = x.w;
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) v[4 * ks + e] = 0.f;
+    for (int ks = 0; ks < 16; ++ks) {
+      float2 x = make_float2(0.f, 0.f);
+      if (g2 < G) x = __ldg(reinterpret_cast<const float2*>(qrow + g2 * kD + 8 * ks + 2 * tig));
+      S.qb[ks][0] = tf32_part(x.x * qscale, lo);
+      S.qb[ks][1] = tf32_part(x.y * qscale, lo);
     }
+    S.qexp = 1.0f;
+  } else {
+    float v[32];
+  #pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      if (g2 < G) {
+        const float* qh = qrow + g2 * kD;
+        if constexpr (DT == PKV_KV_F16) {
+          const float2 x = __ldg(reinterpret_cast<const float2*>(qh + 16 * ks + 2 * tig));
+          const float2 y = __ldg(reinterpret_cast<const float2*>(qh + 16 * ks + 8 + 2 * tig));
+          v[4 * ks] = x.x;
+          v[4 * ks + 1] = x.y;
+          v[4 * ks + 2] = y.x;
+          v[4 * ks + 3] = y.y;
+        } else {
+          const float4 x = __ldg(reinterpret_cast<const float4*>(qh + 16 * ks + 4 * tig));
+          v[4 * ks] = x.x;
+          v[4 * ks + 1] = x.y;
+          v[4 * ks + 2] = x.z;
+          v[4 * ks + 3] = x.w;
+        }
+      } else {
+  #pragma unroll
+        for (int e = 0; e < 4; ++e) v[4 * ks + e] = 0.f;
+      }
+    }
+    float amax = 0.f;
+  #pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      v[e] *= qscale;
+      amax = fmaxf(amax, fabsf(v[e]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+    int e2 = 0;
+    if (amax > 0.f && amax <= 3.0e38f) {
+      int ex;
+      frexpf(amax, &ex);  // amax in [2^(ex-1), 2^ex)
+      e2 = ex - 14;
+    }
+  #pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      S.qb[ks][0] = split_f16x2(ldexpf(v[4 * ks], -e2), ldexpf(v[4 * ks + 1], -e2), lo);
+      S.qb[ks][1] = split_f16x2(ldexpf(v[4 * ks + 2], -e2), ldexpf(v[4 * ks + 3], -e2), lo);
+    }
+    // lane 8 tig holds head tig (gid = 2 tig)
+    S.qexp = ldexpf(1.0f, __shfl_sync(kFull, e2, 8 * tig));
   }
-  float amax = 0.f;
-#pragma unroll
-  for (int e = 0; e < 32; ++e) {
-    v[e] *= qscale;
-    amax = fmaxf(amax, fabsf(v[e]));
-  }
-  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));
-  amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
-  int e2 = 0;
-  if (amax > 0.f && amax <= 3.0e38f) {
-    int ex;
-    frexpf(amax, &ex);  // amax in [2^(ex-1), 2^ex)
-    e2 = ex - 14;
-  }
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    S.qb[ks][0] = split_f16x2(ldexpf(v[4 * ks], -e2), ldexpf(v[4 * ks + 1], -e2), lo);
-    S.qb[ks][1] = split_f16x2(ldexpf(v[4 * ks + 2], -e2), ldexpf(v[4 * ks + 3], -e2), lo);
-  }
-  // lane 8 tig holds head tig (gid = 2 tig)
-  S.qexp = ldexpf(1.0f, __shfl_sync(kFull, e2, 8 * tig));
 }
 
 // Process one staged (page, KV head) unit whose attended tokens are slots
@@ -279,7 +304,7 @@ __device__ __forceinline__ void load_query(const float* qrow, float qscale, int 
 // f16 V rows are zeroed before the values MMA.
 template <int DT, int G>
 __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int tlo, int nvalid,
-                                             int lane, WarpState& S) {
+                                             int lane, WarpState<DT>& S) {
   using TL = Tiles<DT>;
   const int gid = lane >> 2, tig = lane & 3;
   // ldmatrix row addresses: lane 8j + r gives row r of matrix j = token
@@ -290,7 +315,22 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
 
   // ---- scores
   float s0, s1;
-  if constexpr (DT == PKV_KV_F16) {
+  if constexpr (DT == PKV_KV_BF16) {
+    // bf16 pairs of an ldmatrix row widen to tf32 exactly: the low value is
+    // the word shifted up, the high one the word with its low half cleared
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c2 = 0; c2 < 8; ++c2) {
+      uint32_t w0, w1, w2, w3;  // tokens gid, gid+8 of chunk 2c2; the same of chunk 2c2+1
+      ldsm_x4(kt + tile_offset<DT>(ld_tok, 2 * c2 + ld_chunk), w0, w1, w2, w3);
+      mma_1688_tf32(c, w0 << 16, w1 << 16, w0 & 0xffff0000u, w1 & 0xffff0000u,
+                    S.qb[2 * c2][0], S.qb[2 * c2][1]);
+      mma_1688_tf32(c, w2 << 16, w3 << 16, w2 & 0xffff0000u, w3 & 0xffff0000u,
+                    S.qb[2 * c2 + 1][0], S.qb[2 * c2 + 1][1]);
+    }
+    s0 = c[0] + c[1];
+    s1 = c[2] + c[3];
+  } else if constexpr (DT == PKV_KV_F16) {
     float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
@@ -363,7 +403,7 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
   const int t0 = 2 * tig;
 
   // ---- values
-  if constexpr (DT == PKV_KV_F16) {
+  if constexpr (DT != PKV_KV_Q8_0) {
     if (tlo > 0 || nvalid < kPage) {  // zero the V rows of unattended slots (NaN * 0 is NaN)
       const int n_out = kPage - (nvalid - tlo);
       for (int x = lane; x < n_out * 16; x += 32) {
@@ -373,13 +413,27 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
       }
       __syncwarp();
     }
-    constexpr float kUp = static_cast<float>(1 << kPShift);
-    const uint32_t b0 = split_f16x2(pa * kUp, pb * kUp, lo), b1 = split_f16x2(pc * kUp, pd * kUp, lo);
+    if constexpr (DT == PKV_KV_F16) {
+      constexpr float kUp = static_cast<float>(1 << kPShift);
+      const uint32_t b0 = split_f16x2(pa * kUp, pb * kUp, lo);
+      const uint32_t b1 = split_f16x2(pc * kUp, pd * kUp, lo);
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      uint32_t w0, w1, w2, w3;  // (tokens 0-7 | 8-15) x (chunk 2mt | 2mt+1), transposed
-      ldsm_x4_trans(vt + tile_offset<DT>(ld_tok, 2 * mt + ld_chunk), w0, w1, w2, w3);
-      mma_16816(S.o[mt], w0, w2, w1, w3, b0, b1);
+      for (int mt = 0; mt < 8; ++mt) {
+        uint32_t w0, w1, w2, w3;  // (tokens 0-7 | 8-15) x (chunk 2mt | 2mt+1), transposed
+        ldsm_x4_trans(vt + tile_offset<DT>(ld_tok, 2 * mt + ld_chunk), w0, w1, w2, w3);
+        mma_16816(S.o[mt], w0, w2, w1, w3, b0, b1);
+      }
+    } else {
+      // tf32 k-steps of 8 tokens: k = tig <- token 2tig, k = tig + 4 <- token 2tig + 1
+      const uint32_t b_t0 = tf32_part(pa, lo), b_t1 = tf32_part(pb, lo);
+      const uint32_t b_t8 = tf32_part(pc, lo), b_t9 = tf32_part(pd, lo);
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        uint32_t w0, w1, w2, w3;  // dims (16mt + gid | + 8) x tokens (2tig, 2tig+1 | + 8)
+        ldsm_x4_trans(vt + tile_offset<DT>(ld_tok, 2 * mt + ld_chunk), w0, w1, w2, w3);
+        mma_1688_tf32(S.o[mt], w0 << 16, w2 << 16, w0 & 0xffff0000u, w2 & 0xffff0000u, b_t0, b_t1);
+        mma_1688_tf32(S.o[mt], w1 << 16, w3 << 16, w1 & 0xffff0000u, w3 & 0xffff0000u, b_t8, b_t9);
+      }
     }
   } else {
     // V block scales of tokens 2tig, 2tig+1 (va) and 2tig+8, 2tig+9 (vb): the
@@ -511,6 +565,12 @@ __device__ __forceinline__ void append_token(const DecodeArgs& a, int i, int h, 
     uint8_t* data = which ? a.v_data : a.k_data;
     if constexpr (DT == PKV_KV_F16) {
       const __half2 lo = __floats2half2_rn(x.x, x.y), hi = __floats2half2_rn(x.z, x.w);
+      uint2 w;
+      w.x = *reinterpret_cast<const uint32_t*>(&lo);
+      w.y = *reinterpret_cast<const uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(data + tile * TL::kData + slot * (kD * 2) + lane * 8) = w;
+    } else if constexpr (DT == PKV_KV_BF16) {
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
       uint2 w;
       w.x = *reinterpret_cast<const uint32_t*>(&lo);
       w.y = *reinterpret_cast<const uint32_t*>(&hi);
@@ -652,7 +712,7 @@ __device__ __forceinline__ bool wait_merge_buffer(volatile int* ctl, int piece) 
 
 // --------------------------------------------------------------- kernel ----
 template <int DT, int G>
-__global__ void __launch_bounds__(kThreads, DT == PKV_KV_F16 ? PKV_F16_CTAS_PER_SM
+__global__ void __launch_bounds__(kThreads, DT != PKV_KV_Q8_0 ? PKV_F16_CTAS_PER_SM
                                                               : PKV_Q8_CTAS_PER_SM)
     paged_decode_kernel(const __grid_constant__ DecodeArgs a,
                         const __grid_constant__ TileMaps maps) {
@@ -771,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_F16 ? PKV_F16_CTAS_PER_
       const uint32_t dst = smem_addr(ring + s * TL::kCodes);
       const int z = pg * a.n_kv + hh;  // tile index (the host checks num_pages * n_kv < 2^31)
       mbar_arrive_expect_tx(bar, TL::kTx);
-      if constexpr (DT == PKV_KV_F16) {
+      if constexpr (DT != PKV_KV_Q8_0) {
         tma_load_3d(dst, &maps.k, 0, 0, z, bar, policy);
         tma_load_3d(dst + 2048, &maps.k, 64, 0, z, bar, policy);
         tma_load_3d(dst + TL::kData, &maps.v, 0, 0, z, bar, policy);
@@ -794,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_F16 ? PKV_F16_CTAS_PER_
   float* mrg_ml = reinterpret_cast<float*>(smem + SM::kMrgMl);
   bool aborted = false;
   int consumed = 0;
-  WarpState S;
+  WarpState<DT> S;
 
   int piece = 0;
   for (long long x = c_begin; x < c_end; ++piece) {
@@ -917,7 +977,7 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_F16 ? PKV_F16_CTAS_PER_
       named_barrier(1, kThreads);
       if (ctl[1]) {
         __threadfence();
-        merge_segment<G, DT == PKV_KV_F16 ? PKV_MERGE_BATCH : PKV_MERGE_BATCH / 2>(
+        merge_segment<G, DT != PKV_KV_Q8_0 ? PKV_MERGE_BATCH : PKV_MERGE_BATCH / 2>(
             a.part_ml, a.part_acc, j, k0, k1, out_seg, d);
         if (d == 0) a.counters[j] = 0;  // ready for the next call
       }
@@ -1038,14 +1098,17 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 static cudaError_t encode_tile_map(CUtensorMap* m, int dtype, void* base, long long tiles) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  const bool f16 = dtype == PKV_KV_F16;
+  const bool f16 = dtype != PKV_KV_Q8_0;  // 16-bit values (f16, bf16)
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(kPage),
                               static_cast<cuuint64_t>(tiles)};
   const cuuint64_t strides[2] = {f16 ? 256u : 128u, f16 ? 4096u : 2048u};  // bytes
   const cuuint32_t box[3] = {f16 ? 64u : 128u, static_cast<cuuint32_t>(kPage), 1u};
   const cuuint32_t estride[3] = {1u, 1u, 1u};
   const CUresult r =
-      fn(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims,
+      fn(m, dtype == PKV_KV_F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+            : dtype == PKV_KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+         3, base, dims,
          strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -1118,6 +1181,10 @@ static cudaError_t occupancy_t(int rows, int* blocks) {
       if ((G_) == 1) return CALL(0, 1);      \
       if ((G_) == 2) return CALL(0, 2);      \
       if ((G_) == 4) return CALL(0, 4);      \
+    } else if ((DT_) == PKV_KV_BF16) {       \
+      if ((G_) == 1) return CALL(2, 1);      \
+      if ((G_) == 2) return CALL(2, 2);      \
+      if ((G_) == 4) return CALL(2, 4);      \
     } else {                                 \
       if ((G_) == 1) return CALL(1, 1);      \
       if ((G_) == 2) return CALL(1, 2);      \

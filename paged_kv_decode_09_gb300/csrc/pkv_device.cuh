@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "pkv.h"
@@ -131,6 +132,25 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       "{%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D = A B + D with tf32 operands (fp32 bit patterns, the low 13 fraction bits
+// ignored): A 16x8 (row), B 8x8 (column), D 16x8 f32.  Lane t = 4 gid + tig
+// holds A rows gid / gid + 8 at column tig (a0 / a1) and tig + 4 (a2 / a3),
+// B rows tig (b0) and tig + 4 (b1) of column gid, and D as for mma_16816.
+__device__ __forceinline__ void mma_1688_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// fp32 rounded to tf32 (10 fraction bits), to nearest with ties away.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
 }
 
 // The KV stream is read once per call: mark it first to leave L2.

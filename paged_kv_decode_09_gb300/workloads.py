@@ -69,6 +69,10 @@ CONFIGS = {
                model_layers=32,
                description="64 rows: one at 40960, 63 at L~U[16,512], 32q/8kv, f16, "
                            "append fused before attention"),
+        # the 8B shape with bfloat16 KV (tinyllm's BF16 KV caching)
+        Config("llama8b_bf16", 8, ("uniform", 1024, 8192), 32, 8, 128, BF16, ("spare", 0.10), 5,
+               model_layers=32,
+               description="8B layer: 8 rows, L~U[1024,8192], 32q/8kv, bf16, shuffled pages"),
     ]
 }
 CONFIG_ORDER = ["tiny", "qwen3_0p6b_layer", "llama8b_f16", "llama8b_q8_0", "skewed"]

@@ -77,11 +77,12 @@ def device_pool(wl: W.Workload, host_pool, num_layers: int = 1, layer: int = 0):
     cfg = wl.cfg
     pool = api.KVPool(num_layers, wl.num_pages, cfg.n_kv_heads, cfg.dtype, device="cuda")
     kd, vd, ks, vs = host_pool
-    if cfg.dtype == W.F16:
+    if cfg.dtype in (W.F16, W.BF16):  # 16-bit patterns copied as int16
+        nan = 0x7E00 if cfg.dtype == W.F16 else 0x7FC0
         for t in (pool.k_data, pool.v_data):
-            t.view(torch.int16).fill_(0x7E00)
-        pool.k_data[layer].copy_(torch.from_numpy(kd.view(np.float16)))
-        pool.v_data[layer].copy_(torch.from_numpy(vd.view(np.float16)))
+            t.view(torch.int16).fill_(nan)
+        pool.k_data[layer].view(torch.int16).copy_(torch.from_numpy(kd.view(np.int16)))
+        pool.v_data[layer].view(torch.int16).copy_(torch.from_numpy(vd.view(np.int16)))
     else:
         for t in (pool.k_scales, pool.v_scales):
             t.view(torch.int16).fill_(0x7E00)
@@ -97,7 +98,7 @@ def device_pool(wl: W.Workload, host_pool, num_layers: int = 1, layer: int = 0):
 def host_arrays(pool, layer: int = 0):
     """(k_data, v_data, k_scales, v_scales) numpy copies of one layer of a device pool."""
     import torch
-    if pool.dtype == W.F16:
+    if pool.dtype in (W.F16, W.BF16):
         return (pool.k_data[layer].cpu().view(torch.int16).numpy().view(np.uint16),
                 pool.v_data[layer].cpu().view(torch.int16).numpy().view(np.uint16), None, None)
     return (pool.k_data[layer].cpu().numpy(), pool.v_data[layer].cpu().numpy(),

@@ -31,7 +31,7 @@ def _append_case(cfg_name, dtype=None, scale_new=1.0, layer=1, layers=3):
     return wl, pool, got, want
 
 
-@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0])
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16])
 @pytest.mark.parametrize("cfg_name", ["tiny", "skewed"])
 def test_append_bit_exact(cfg_name, dtype):
     _, pool, got, want = _append_case(cfg_name, dtype)

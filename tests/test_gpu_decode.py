@@ -36,7 +36,7 @@ def _run(wl, pool, layer=0, num_chunks=0, q=None, seq_lens=None):
     return out.cpu().numpy()
 
 
-@pytest.mark.parametrize("cfg_name", ["tiny", "qwen3_0p6b_layer", "llama8b_f16"])
+@pytest.mark.parametrize("cfg_name", ["tiny", "qwen3_0p6b_layer", "llama8b_f16", "llama8b_bf16"])
 def test_attention_matches_oracle(cfg_name):
     wl = W.draw(cfg_name)
     host = encode_pool(wl)
@@ -74,7 +74,7 @@ def test_skewed_decode_step_appends_then_attends():
     _check(out.cpu().numpy(), oracle_decode(wl, want))
 
 
-@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0])
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16])
 def test_split_invariance(dtype):
     """Any chunk count gives the same output: 1 chunk (no merge), many chunks
     (every (row, head) split, one page per piece at the extreme)."""
@@ -91,7 +91,7 @@ def test_split_invariance(dtype):
 
 
 @pytest.mark.parametrize("group,n_kv", [(1, 4), (2, 8), (4, 8), (4, 2)])
-@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0])
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16])
 def test_gqa_groups(group, n_kv, dtype):
     cfg = W.Config("gqa", 5, ("uniform", 1, 300), n_kv * group, n_kv, 128, dtype,
                    ("spare", 0.3), 40 + group)
@@ -153,7 +153,7 @@ def test_host_validation_errors():
     assert out.shape == q.shape
 
 
-@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0])
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16])
 def test_fused_step_append_is_bit_exact(dtype):
     """pkv_decode_step stores each row's token inside the attention kernel:
     the pool afterwards must equal the oracle's append byte for byte."""
@@ -177,7 +177,7 @@ def test_fused_step_append_is_bit_exact(dtype):
     _check(out.cpu().numpy()[rows], ref)
 
 
-@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0])
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16])
 def test_split_then_combine_equals_merged(dtype):
     wl = W.draw("llama8b_f16")
     wl.cfg = W.Config(**{**wl.cfg.__dict__, "dtype": dtype})
