@@ -168,7 +168,7 @@ def step_bytes(wl, window=0) -> int:
     """Algorithmic bytes of one decode call: K and V of every attended token
     (f16: 2 bytes per element; q8_0: 34 bytes per 32 elements), q and out."""
     cfg = wl.cfg
-    per_elem = 2.0 if cfg.dtype == 0 else 34.0 / 32.0
+    per_elem = 34.0 / 32.0 if cfg.dtype == 1 else 2.0  # q8_0; f16 and bf16
     kv = attended_tokens(wl, window) * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem
     qo = 2 * wl.rows * cfg.n_q_heads * cfg.head_dim * 4
     return int(kv + qo)
@@ -450,7 +450,7 @@ def cpu_baseline(wl, pool, budget_s, window=0):
 
     import oracle as O
     cfg = wl.cfg
-    if cfg.dtype == 0:
+    if cfg.dtype != 1:  # 16-bit patterns (f16, bf16)
         kd = pool.k_data[0].cpu().view(torch.int16).numpy().view(np.uint16)
         vd = pool.v_data[0].cpu().view(torch.int16).numpy().view(np.uint16)
         ks = vs = None
@@ -470,7 +470,7 @@ def cpu_baseline(wl, pool, budget_s, window=0):
         done += min(int(wl.seq_lens[i]), window) if window > 0 else int(wl.seq_lens[i])
         if secs > budget_s:
             break
-    per_elem = 2.0 if cfg.dtype == 0 else 34.0 / 32.0
+    per_elem = 34.0 / 32.0 if cfg.dtype == 1 else 2.0  # q8_0; f16 and bf16
     nbytes = done * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem + 2 * len(rows) * cfg.n_q_heads * 128 * 4
     return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": O.num_threads(),
             "kind": "oracle",
@@ -505,7 +505,7 @@ def run_reference(args):
                            wl.seq_lens[i:i + 1], wl.num_pages, cfg.n_kv_heads, wl.scale,
                            window=args.window)
 
-    per_elem = 2.0 if cfg.dtype == 0 else 34.0 / 32.0
+    per_elem = 34.0 / 32.0 if cfg.dtype == 1 else 2.0  # q8_0; f16 and bf16
 
     def row_tokens(i):
         L = int(wl.seq_lens[i])
