@@ -74,6 +74,13 @@ def lib():
                                                   _i32p, _i, _i32p, _i, ctypes.c_double, _i,
                                                   _f64p]
             L.oracle_decode_attention.restype = _i
+            L.oracle_decode_attention_mq.argtypes = [_i, _i, _i, _i, _i, _i, _f32p, _vp, _vp, _vp,
+                                                     _vp, _i32p, _i, _i32p, _i, ctypes.c_double,
+                                                     _i, _f64p]
+            L.oracle_decode_attention_mq.restype = _i
+            L.oracle_kv_append_mq.argtypes = [_i, _i, _i, _i, _i, _f32p, _f32p, _i32p, _i, _i32p,
+                                              _i, _vp, _vp, _vp, _vp]
+            L.oracle_kv_append_mq.restype = _i
             L.oracle_attention_partial.argtypes = [
                 _i, _i, _i, _i, _f32p, _vp, _vp, _vp, _vp, _i32p, _i, _i, _i, _i,
                 ctypes.c_double, _i, _i, ctypes.POINTER(ctypes.c_double),
@@ -211,6 +218,41 @@ def decode_attention(dtype, q, k_data, v_data, k_scales, v_scales, block_table, 
     if st:
         raise ValueError(f"oracle_decode_attention: status {st}")
     return out
+
+
+def decode_attention_mq(dtype, q, k_data, v_data, k_scales, v_scales, block_table, seq_lens,
+                        num_pages, n_kv, scale, window=0):
+    """Several queries per row: q [rows][q_len][n_q][D]; query j of row i sits
+    at position L - q_len + j (L = seq_lens[i]) and attends causally to
+    [max(0, P + 1 - window), P + 1).  float64 [rows][q_len][n_q][D]."""
+    q = np.ascontiguousarray(q, np.float32)
+    bt = np.ascontiguousarray(block_table, np.int32)
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    rows, q_len, n_q, D = q.shape
+    out = np.zeros((rows, q_len, n_q, D), np.float64)
+    st = lib().oracle_decode_attention_mq(dtype, rows, q_len, n_q, n_kv, D, q.reshape(-1),
+                                          _ptr(k_data), _ptr(v_data), _ptr(k_scales),
+                                          _ptr(v_scales), bt.reshape(-1), bt.shape[1], sl,
+                                          num_pages, float(scale), int(window), out.reshape(-1))
+    if st:
+        raise ValueError(f"oracle_decode_attention_mq: status {st}")
+    return out
+
+
+def kv_append_mq(dtype, k_new, v_new, block_table, seq_lens, num_pages, k_data, v_data,
+                 k_scales=None, v_scales=None):
+    """Store q_len new tokens per row (k_new, v_new [rows][q_len][n_kv][D]) at
+    positions L - q_len + j, in place."""
+    k_new = np.ascontiguousarray(k_new, np.float32)
+    v_new = np.ascontiguousarray(v_new, np.float32)
+    bt = np.ascontiguousarray(block_table, np.int32)
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    rows, q_len, n_kv, D = k_new.shape
+    st = lib().oracle_kv_append_mq(dtype, rows, q_len, n_kv, D, k_new.reshape(-1),
+                                   v_new.reshape(-1), bt.reshape(-1), bt.shape[1], sl, num_pages,
+                                   _ptr(k_data), _ptr(v_data), _ptr(k_scales), _ptr(v_scales))
+    if st:
+        raise ValueError(f"oracle_kv_append_mq: status {st}")
 
 
 def attention_partial(dtype, q_row, k_data, v_data, k_scales, v_scales, block_table, num_pages,

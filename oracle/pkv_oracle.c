@@ -31,6 +31,12 @@
  *   - Sliding-window KV caches: Leone, "Capabilities".  Reading: with a
  *     window W > 0 a row of L tokens attends to its last W tokens,
  *     [max(0, L - W), L), the new token included; W = 0 means all L.
+ *   - Several query tokens per row (Leone, "What ships": chunked prefill and
+ *     exact speculative verification; LeatEngine, "Capabilities": chunked
+ *     prefill, speculative decoding).  Reading: a row of L tokens whose last
+ *     q_len are new has one query per new token; query j sits at position
+ *     P = L - q_len + j and attends causally to [a, P + 1), a = max(0,
+ *     P + 1 - W) under a window W (0 otherwise).
  *
  * Readings where the pages are silent (each is restated where it is used):
  *   - GQA head map: query head g reads KV head g / (n_q_heads / n_kv_heads).
@@ -249,6 +255,53 @@ static int64_t page_of(const int32_t *block_table, int bt_stride, int i, int t, 
     return (p >= 0 && p < num_pages) ? p : -1;
 }
 
+/* Store one fp32 K and V vector (D values each) of KV head h at position pos
+ * of row i. */
+static int store_token(int dtype, int n_kv, int D, const float *kx, const float *vx,
+                       const int32_t *block_table, int bt_stride, int i, int h, int pos,
+                       int num_pages, void *k_data, void *v_data, uint16_t *k_scales,
+                       uint16_t *v_scales) {
+    if (pos / ORACLE_PAGE >= bt_stride) return ORACLE_BAD_PAGE;
+    int64_t page = page_of(block_table, bt_stride, i, pos, num_pages);
+    if (page < 0) return ORACLE_BAD_PAGE;
+    int64_t row = (page * n_kv + h) * ORACLE_PAGE + pos % ORACLE_PAGE;
+    if (dtype == ORACLE_F16) {
+        oracle_f16_encode(kx, D, (uint16_t *)k_data + row * D);
+        oracle_f16_encode(vx, D, (uint16_t *)v_data + row * D);
+    } else if (dtype == ORACLE_BF16) {
+        oracle_bf16_encode(kx, D, (uint16_t *)k_data + row * D);
+        oracle_bf16_encode(vx, D, (uint16_t *)v_data + row * D);
+    } else {
+        oracle_q8_0_encode(kx, D, (int8_t *)k_data + row * D, k_scales + row * (D / ORACLE_QBLOCK));
+        oracle_q8_0_encode(vx, D, (int8_t *)v_data + row * D, v_scales + row * (D / ORACLE_QBLOCK));
+    }
+    return ORACLE_OK;
+}
+
+/* Several new tokens per row: k_new, v_new fp32 [rows][q_len][n_kv][D];
+ * token j of row i (L = seq_lens[i] >= q_len, the length after the step)
+ * goes to position L - q_len + j.  Rows with L <= 0 write nothing. */
+int oracle_kv_append_mq(int dtype, int num_rows, int q_len, int n_kv, int D, const float *k_new,
+                        const float *v_new, const int32_t *block_table, int bt_stride,
+                        const int32_t *seq_lens, int num_pages, void *k_data, void *v_data,
+                        uint16_t *k_scales, uint16_t *v_scales) {
+    if (D % ORACLE_QBLOCK || q_len < 1) return ORACLE_BAD_ARG;
+    for (int i = 0; i < num_rows; ++i) {
+        int L = seq_lens[i];
+        if (L <= 0) continue;
+        if (L < q_len) return ORACLE_BAD_ARG;
+        for (int j = 0; j < q_len; ++j)
+            for (int h = 0; h < n_kv; ++h) {
+                int64_t src = (((int64_t)i * q_len + j) * n_kv + h) * D;
+                int st = store_token(dtype, n_kv, D, k_new + src, v_new + src, block_table,
+                                     bt_stride, i, h, L - q_len + j, num_pages, k_data, v_data,
+                                     k_scales, v_scales);
+                if (st != ORACLE_OK) return st;
+            }
+    }
+    return ORACLE_OK;
+}
+
 /* kv_append: write each row's new K and V token (fp32 [rows][n_kv][D]) into
  * page block_table[i][(L-1)/16], slot (L-1)%16, with L = seq_lens[i] (the
  * length after this token).  Rows with L <= 0 write nothing. */
@@ -306,6 +359,37 @@ static int scores(int dtype, const void *k_data, const uint16_t *k_scales, int n
 /* First attended token of a row of L tokens under a window W (0: none). */
 static int window_start(int L, int window) { return window > 0 && L > window ? L - window : 0; }
 
+/* Attention of one query vector q (D values) of row i over KV head h's
+ * tokens [a, b), b > a: o = sum_t softmax_t(scale <q, K_t>) V_t, in double
+ * with the maximum subtracted before exp. */
+static int attend(int dtype, const void *k_data, const void *v_data, const uint16_t *k_scales,
+                  const uint16_t *v_scales, int n_kv, int D, const int32_t *block_table,
+                  int bt_stride, int num_pages, int i, int h, const float *q, double scale,
+                  int a, int b, double *o) {
+    const int n = b - a;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    double *s = (double *)malloc(sizeof(double) * (size_t)n);
+    if (!s) return ORACLE_BAD_ARG;
+    if (scores(dtype, k_data, k_scales, n_kv, D, block_table, bt_stride, num_pages, i, h, q,
+               scale, a, b, s) != ORACLE_OK) {
+        free(s);
+        return ORACLE_BAD_PAGE;
+    }
+    double m = -INFINITY;
+    for (int t = 0; t < n; ++t) m = s[t] > m ? s[t] : m;
+    double l = 0.0;
+    for (int t = a; t < b; ++t) {
+        double p = exp(s[t - a] - m);
+        l += p;
+        int64_t page = page_of(block_table, bt_stride, i, t, num_pages);
+        for (int d = 0; d < D; ++d)
+            o[d] += p * stored(dtype, v_data, v_scales, n_kv, D, page, h, t % ORACLE_PAGE, d);
+    }
+    for (int d = 0; d < D; ++d) o[d] /= l;
+    free(s);
+    return ORACLE_OK;
+}
+
 /* Decode attention for every row and query head:
  *   out[i][g] = sum_{a_i <= t < L_i} softmax_t(scale * <q[i][g], K[i][h][t]>) V[i][h][t]
  * with h = g / (n_q / n_kv), a_i = max(0, L_i - window) (a_i = 0 for window
@@ -329,27 +413,49 @@ int oracle_decode_attention(int dtype, int num_rows, int n_q, int n_kv, int D, c
         double *o = out + ig * D;
         for (int d = 0; d < D; ++d) o[d] = 0.0;
         if (L <= 0) continue;
-        const int a = window_start(L, window), n = L - a;
-        double *s = (double *)malloc(sizeof(double) * (size_t)n);
-        if (!s || scores(dtype, k_data, k_scales, n_kv, D, block_table, bt_stride, num_pages,
-                         i, h, q + ig * D, scale, a, L, s) != ORACLE_OK) {
+        if (attend(dtype, k_data, v_data, k_scales, v_scales, n_kv, D, block_table, bt_stride,
+                   num_pages, i, h, q + ig * D, scale, window_start(L, window), L, o) != ORACLE_OK) {
 #pragma omp atomic write
             status = ORACLE_BAD_PAGE;
-            free(s);
-            continue;
         }
-        double m = -INFINITY;
-        for (int t = 0; t < n; ++t) m = s[t] > m ? s[t] : m;
-        double l = 0.0;
-        for (int t = a; t < L; ++t) {
-            double p = exp(s[t - a] - m);
-            l += p;
-            int64_t page = page_of(block_table, bt_stride, i, t, num_pages);
-            for (int d = 0; d < D; ++d)
-                o[d] += p * stored(dtype, v_data, v_scales, n_kv, D, page, h, t % ORACLE_PAGE, d);
+    }
+    return status;
+}
+
+/* Several queries per row: q and out are [rows][q_len][n_q][D]; query j of
+ * row i (L = seq_lens[i] >= q_len) sits at position P = L - q_len + j and
+ * attends to tokens [max(0, P + 1 - window) (0 for window 0), P + 1) of KV
+ * head g / (n_q / n_kv).  Rows with L <= 0 produce zeros; 0 < L < q_len is
+ * an error.  out is double. */
+int oracle_decode_attention_mq(int dtype, int num_rows, int q_len, int n_q, int n_kv, int D,
+                               const float *q, const void *k_data, const void *v_data,
+                               const uint16_t *k_scales, const uint16_t *v_scales,
+                               const int32_t *block_table, int bt_stride,
+                               const int32_t *seq_lens, int num_pages, double scale, int window,
+                               double *out) {
+    if (n_kv <= 0 || n_q % n_kv || D % ORACLE_QBLOCK || window < 0 || q_len < 1)
+        return ORACLE_BAD_ARG;
+    for (int i = 0; i < num_rows; ++i)
+        if (seq_lens[i] > (int64_t)bt_stride * ORACLE_PAGE ||
+            (seq_lens[i] > 0 && seq_lens[i] < q_len))
+            return ORACLE_BAD_ARG;
+    const int group = n_q / n_kv;
+    int status = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t x = 0; x < (int64_t)num_rows * q_len * n_q; ++x) {
+        int i = (int)(x / ((int64_t)q_len * n_q));
+        int j = (int)((x / n_q) % q_len), g = (int)(x % n_q), h = g / group;
+        int L = seq_lens[i];
+        double *o = out + x * D;
+        for (int d = 0; d < D; ++d) o[d] = 0.0;
+        if (L <= 0) continue;
+        int P = L - q_len + j;
+        if (attend(dtype, k_data, v_data, k_scales, v_scales, n_kv, D, block_table, bt_stride,
+                   num_pages, i, h, q + x * D, scale, window_start(P + 1, window), P + 1,
+                   o) != ORACLE_OK) {
+#pragma omp atomic write
+            status = ORACLE_BAD_PAGE;
         }
-        for (int d = 0; d < D; ++d) o[d] /= l;
-        free(s);
     }
     return status;
 }

@@ -14,7 +14,8 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "pkv_oracle.c")
 PINS = ["tests/test_oracle_f16.py", "tests/test_oracle_q8_0.py", "tests/test_oracle_bf16.py",
-        "tests/test_oracle_attention.py", "tests/test_oracle_plan_append.py"]
+        "tests/test_oracle_attention.py", "tests/test_oracle_plan_append.py",
+        "tests/test_oracle_mq.py"]
 
 MUTANTS = {
     "no_normalisation": ("for (int d = 0; d < D; ++d) o[d] /= l;", ""),
@@ -45,6 +46,9 @@ MUTANTS = {
                                  "ulp = ldexp(1.0, e - 9); /* 8 significant bits */"),
     "bf16_exponent_bias": ("mag = ldexp((double)(128 + frac), expo - 134);",
                            "mag = ldexp((double)(128 + frac), expo - 133);"),
+    "mq_query_one_late": ("int P = L - q_len + j;", "int P = L - q_len + j + (j > 0);"),
+    "mq_append_position": ("bt_stride, i, h, L - q_len + j, num_pages, k_data, v_data,",
+                           "bt_stride, i, h, L - q_len + j - (j > 0), num_pages, k_data, v_data,"),
     "window_one_too_short": ("return window > 0 && L > window ? L - window : 0;",
                              "return window > 0 && L > window ? L - window + 1 : 0;"),
     "window_first_page_rounded_up": (
