@@ -19,7 +19,10 @@ PINS = ["tests/test_oracle_f16.py", "tests/test_oracle_q8_0.py", "tests/test_ora
 
 MUTANTS = {
     "no_normalisation": ("for (int d = 0; d < D; ++d) o[d] /= l;", ""),
-    "interleaved_gqa": ("h = g / group;", "h = g % n_kv;"),
+    "interleaved_gqa": ("int i = (int)(ig / n_q), g = (int)(ig % n_q), h = g / group;",
+                        "int i = (int)(ig / n_q), g = (int)(ig % n_q), h = g % n_kv;"),
+    "mq_interleaved_gqa": ("int j = (int)((x / n_q) % q_len), g = (int)(x % n_q), h = g / group;",
+                           "int j = (int)((x / n_q) % q_len), g = (int)(x % n_q), h = g % n_kv;"),
     "slot_as_page": ("block_table[(int64_t)i * bt_stride + t / ORACLE_PAGE]",
                      "block_table[(int64_t)i * bt_stride + t % ORACLE_PAGE]"),
     "transposed_page_head": ("int64_t row = (page * n_kv + kvh) * ORACLE_PAGE + slot;",
