@@ -247,6 +247,56 @@ pkv_status pkv_decode_step(const pkv_pool *pool, int layer, const float *q, cons
                            float *out, void *workspace, size_t workspace_bytes, int num_chunks,
                            void *stream);
 
+/* Several queries per row: the verification step of speculative decoding and
+ * short chunks of chunked prefill (Leone, "What ships": chunked prefill and
+ * exact speculative verification; LeatEngine, "Capabilities": chunked
+ * prefill, speculative decoding).
+ *
+ * Each row i has q_len (1 .. PKV_MAX_Q_LEN) new tokens, the last q_len of its
+ * L = seq_lens[i] >= q_len tokens.  Query j (0 <= j < q_len) sits at position
+ * P = L - q_len + j and attends causally to [max(0, P + 1 - W), P + 1), W the
+ * layer's window (0: [0, P + 1)):
+ *
+ *     out[i][j][g] = sum_{t in that range} softmax_t(scale * <q[i][j][g], K[i][h][t]>) V[i][h][t]
+ *
+ *   q, out        fp32 [num_rows][q_len][n_q_heads][128], 16-byte aligned
+ *   k_new, v_new  fp32 [num_rows][q_len][n_kv_heads][128] (pkv_decode_step_mq):
+ *                 token j of row i is stored at position L - q_len + j
+ * Rows with L == 0 get zeros; rows with 0 < L < q_len get zeros and set
+ * PKV_DEV_BAD_LENGTH.  A row reads the pages holding [L - q_len + 1 - W, L)
+ * (all of [0, L) without a window), split into chunks as in
+ * paged_decode_attention.  Every page is read once per pass: a pass carries
+ * up to 8 (query, query head) pairs of a KV head for f16 and q8_0 (4 for
+ * bf16), i.e. ceil(q_len * G / 8) passes (ceil(q_len * G / 4) for bf16), each
+ * one launch on `stream`.  pkv_decode_step_mq stores the new tokens in the
+ * first pass, just before their pages are read; the last q_len positions'
+ * pages must not be shared with another row.
+ * Workspace (paged_decode_workspace_bytes_mq): as paged_decode_attention's
+ * with 8 partial-state columns per slot instead of G:
+ *     counters int32 [num_rows * n_kv_heads]
+ *     part_ml  float [S][8][2];  part_acc float [S][8][head_dim]
+ * zero-filled once before first use; not shared by concurrent calls. */
+#define PKV_MAX_Q_LEN 64
+
+size_t paged_decode_workspace_bytes_mq(int max_rows, int n_q_heads, int n_kv_heads, int head_dim,
+                                       int num_chunks);
+
+/* Chunks (resident CTAs of the several-query kernel) that fill this GPU. */
+pkv_status paged_decode_default_chunks_mq(const pkv_pool *pool, int n_q_heads, int max_rows,
+                                          int *chunks);
+
+pkv_status paged_decode_attention_mq(const pkv_pool *pool, int layer, const float *q,
+                                     const int32_t *block_table, int bt_stride,
+                                     const int32_t *seq_lens, int num_rows, int q_len,
+                                     int n_q_heads, float scale, float *out, void *workspace,
+                                     size_t workspace_bytes, int num_chunks, void *stream);
+
+pkv_status pkv_decode_step_mq(const pkv_pool *pool, int layer, const float *q, const float *k_new,
+                              const float *v_new, const int32_t *block_table, int bt_stride,
+                              const int32_t *seq_lens, int num_rows, int q_len, int n_q_heads,
+                              float scale, float *out, void *workspace, size_t workspace_bytes,
+                              int num_chunks, void *stream);
+
 /* Bytes of scratch held by paged_decode_attention_static (per GPU that
  * loads the library, for the life of the process). */
 #define PKV_STATIC_SCRATCH_BYTES (8u << 20)

@@ -76,6 +76,12 @@ _SIGS = {
     "kv_pool_get_window": ([_vp, _i, ctypes.POINTER(_i)], _i),
     "pkv_decode_step": ([_vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, ctypes.c_float, _vp, _vp,
                          _sz, _i, _vp], _i),
+    "paged_decode_workspace_bytes_mq": ([_i, _i, _i, _i, _i], _sz),
+    "paged_decode_default_chunks_mq": ([_vp, _i, _i, ctypes.POINTER(_i)], _i),
+    "paged_decode_attention_mq": ([_vp, _i, _vp, _vp, _i, _vp, _i, _i, _i, ctypes.c_float, _vp,
+                                   _vp, _sz, _i, _vp], _i),
+    "pkv_decode_step_mq": ([_vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, ctypes.c_float,
+                            _vp, _vp, _sz, _i, _vp], _i),
     "pkv_status_string": ([_i], ctypes.c_char_p),
     "pkv_last_error_message": ([], ctypes.c_char_p),
 }
@@ -283,6 +289,71 @@ def decode_step(pool: KVPool, layer: int, q, k_new, v_new, block_table, seq_lens
                                  _ptr(block_table), stride, _ptr(seq_lens), rows, n_q,
                                  float(scale), _ptr(out), _ptr(workspace.tensor),
                                  workspace.nbytes, chunks, _stream(stream)), "pkv_decode_step")
+    return out
+
+
+class WorkspaceMQ:
+    """Device scratch for the several-query calls (8 partial-state columns per
+    slot), zero-filled as the library requires before first use."""
+
+    def __init__(self, pool: KVPool, n_q_heads: int, max_rows: int, num_chunks: int = 0):
+        if not num_chunks:
+            c = ctypes.c_int(0)
+            _check(lib().paged_decode_default_chunks_mq(pool.handle, n_q_heads, max_rows,
+                                                        ctypes.byref(c)),
+                   "paged_decode_default_chunks_mq")
+            num_chunks = c.value
+        self.num_chunks = num_chunks
+        self.nbytes = lib().paged_decode_workspace_bytes_mq(max_rows, n_q_heads, pool.n_kv,
+                                                            pool.head_dim, num_chunks)
+        if self.nbytes == 0 and max_rows > 0:
+            raise PkvError(1, "paged_decode_workspace_bytes_mq", "invalid sizes")
+        self.tensor = torch.zeros(max(self.nbytes, 256), dtype=torch.uint8, device=pool.device)
+
+
+def _mq_args(pool, q, block_table, seq_lens, out, workspace, num_chunks):
+    rows, stride = _rows(block_table, seq_lens, pool.device)
+    _need(q, torch.float32, "q", device=pool.device)
+    if q.dim() != 4 or q.shape[0] != rows or q.shape[3] != pool.head_dim:
+        raise ValueError("q must be [rows][q_len][n_q_heads][128]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.float32, "out", q.shape, pool.device)
+    if workspace is None:
+        workspace = WorkspaceMQ(pool, q.shape[2], max(rows, 1), num_chunks)
+    return rows, stride, out, workspace, num_chunks or workspace.num_chunks
+
+
+def paged_decode_attention_mq(pool: KVPool, layer: int, q, block_table, seq_lens, scale: float,
+                              out=None, workspace: WorkspaceMQ | None = None, num_chunks: int = 0,
+                              stream=None):
+    """Several queries per row: q [rows][q_len][n_q][128]; query j of a row of
+    L tokens sits at position L - q_len + j and attends causally."""
+    rows, stride, out, workspace, chunks = _mq_args(pool, q, block_table, seq_lens, out,
+                                                    workspace, num_chunks)
+    _check(lib().paged_decode_attention_mq(pool.handle, layer, _ptr(q), _ptr(block_table), stride,
+                                           _ptr(seq_lens), rows, q.shape[1], q.shape[2],
+                                           float(scale), _ptr(out), _ptr(workspace.tensor),
+                                           workspace.nbytes, chunks, _stream(stream)),
+           "paged_decode_attention_mq")
+    return out
+
+
+def decode_step_mq(pool: KVPool, layer: int, q, k_new, v_new, block_table, seq_lens,
+                   scale: float, out=None, workspace: WorkspaceMQ | None = None,
+                   num_chunks: int = 0, stream=None):
+    """Store each row's q_len new tokens (k_new, v_new [rows][q_len][n_kv][128])
+    at positions L - q_len .. L - 1, then attend (pkv_decode_step_mq)."""
+    rows, stride, out, workspace, chunks = _mq_args(pool, q, block_table, seq_lens, out,
+                                                    workspace, num_chunks)
+    shape = (rows, q.shape[1], pool.n_kv, pool.head_dim)
+    _need(k_new, torch.float32, "k_new", shape, pool.device)
+    _need(v_new, torch.float32, "v_new", shape, pool.device)
+    _check(lib().pkv_decode_step_mq(pool.handle, layer, _ptr(q), _ptr(k_new), _ptr(v_new),
+                                    _ptr(block_table), stride, _ptr(seq_lens), rows, q.shape[1],
+                                    q.shape[2], float(scale), _ptr(out), _ptr(workspace.tensor),
+                                    workspace.nbytes, chunks, _stream(stream)),
+           "pkv_decode_step_mq")
     return out
 
 

@@ -202,6 +202,9 @@ pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q, const
   a.n_q = n_q;
   a.qscale = scale * 1.4426950408889634f;  // log2(e): base-2 softmax
   a.window = pool->window[layer];
+  a.q_len = 1;
+  a.q0 = 0;
+  a.nq = 1;
   a.out = out;
   a.part_ml = w.part_ml;
   a.part_acc = w.part_acc;
@@ -212,6 +215,91 @@ pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q, const
   cudaError_t e = pkv::launch_paged_decode(pool->dtype, g, a, *maps, num_chunks,
                                            as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "paged decode launch");
+  return PKV_OK;
+}
+
+
+// ------------------------------------------------- several queries per row
+size_t workspace_needed_mq(int num_rows, int n_kv, int num_chunks) {
+  const long long slots = partial_slots(num_chunks, num_rows, n_kv);
+  return pkv::counter_bytes(static_cast<long long>(num_rows) * n_kv) +
+         pkv::part_ml_bytes(slots, pkv::kMqCols) + pkv::part_acc_bytes(slots, pkv::kMqCols);
+}
+
+pkv_status default_chunks_mq(const pkv_pool* p, int rows, int* chunks) {
+  int dev = 0, sms = 0, blocks = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  e = pkv::paged_decode_mq_blocks_per_sm(p->dtype, rows, &blocks);
+  if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+  if (blocks < 1) return fail(PKV_ERR_UNSUPPORTED, "attention kernel does not fit on an SM");
+  *chunks = sms * blocks;
+  return PKV_OK;
+}
+
+// ceil(q_len * G / columns) launches over the same plan; the first appends.
+pkv_status attention_mq_impl(const pkv_pool* pool, int layer, const float* q, const float* k_new,
+                             const float* v_new, const int32_t* block_table, int bt_stride,
+                             const int32_t* seq_lens, int num_rows, int q_len, int n_q,
+                             float scale, float* out, void* workspace, size_t workspace_bytes,
+                             int num_chunks, void* stream) {
+  pkv_status s = check_pool_layer(pool, layer);
+  if (s) return s;
+  if ((s = check_geometry(n_q, pool->n_kv, pool->head_dim))) return s;
+  if ((s = check_rows(num_rows, bt_stride, block_table, seq_lens))) return s;
+  if (q_len < 1 || q_len > PKV_MAX_Q_LEN)
+    return fail(PKV_ERR_UNSUPPORTED, "q_len %d outside [1, %d]", q_len, PKV_MAX_Q_LEN);
+  if (num_rows > 0 && (!q || !out)) return fail(PKV_ERR_INVALID_ARG, "null q or out");
+  if (!aligned(q, 16) || !aligned(out, 16))
+    return fail(PKV_ERR_INVALID_ARG, "q / out not 16-byte aligned");
+  if (num_chunks < 0) return fail(PKV_ERR_INVALID_ARG, "num_chunks < 0");
+  if (num_rows == 0) return PKV_OK;
+  if (num_chunks == 0 && (s = default_chunks_mq(pool, num_rows, &num_chunks))) return s;
+  const size_t need = workspace_needed_mq(num_rows, pool->n_kv, num_chunks);
+  if (!workspace || workspace_bytes < need)
+    return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
+  if (!aligned(workspace, 256)) return fail(PKV_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+
+  const int g = n_q / pool->n_kv;
+  const long long slots = partial_slots(num_chunks, num_rows, pool->n_kv);
+  uint8_t* wp = static_cast<uint8_t*>(workspace);
+  pkv::DecodeArgs a;
+  a.counters = reinterpret_cast<int32_t*>(wp);
+  wp += pkv::counter_bytes(static_cast<long long>(num_rows) * pool->n_kv);
+  a.part_ml = reinterpret_cast<float*>(wp);
+  wp += pkv::part_ml_bytes(slots, pkv::kMqCols);
+  a.part_acc = reinterpret_cast<float*>(wp);
+  a.k_data = pool->k_data + layer * pool->layer_data_bytes;
+  a.v_data = pool->v_data + layer * pool->layer_data_bytes;
+  a.k_scales = pool->k_scales ? pool->k_scales + layer * pool->layer_scale_bytes : nullptr;
+  a.v_scales = pool->v_scales ? pool->v_scales + layer * pool->layer_scale_bytes : nullptr;
+  a.num_pages = pool->num_pages;
+  a.n_kv = pool->n_kv;
+  a.q = q;
+  a.block_table = block_table;
+  a.bt_stride = bt_stride;
+  a.seq_lens = seq_lens;
+  a.num_rows = num_rows;
+  a.n_q = n_q;
+  a.qscale = scale * 1.4426950408889634f;  // log2(e): base-2 softmax
+  a.window = pool->window[layer];
+  a.q_len = q_len;
+  a.out = out;
+  a.status = pool->status;
+  const pkv::TileMaps* maps = nullptr;
+  if ((s = layer_maps(pool, layer, &maps))) return s;
+  const int per_pass = pkv::mq_pass_queries(pool->dtype, g);
+  for (int q0 = 0; q0 < q_len; q0 += per_pass) {
+    a.q0 = q0;
+    a.nq = q_len - q0 < per_pass ? q_len - q0 : per_pass;
+    a.k_new = q0 == 0 ? k_new : nullptr;  // the new tokens are stored once, in the first pass
+    a.v_new = q0 == 0 ? v_new : nullptr;
+    cudaError_t e = pkv::launch_paged_decode_mq(pool->dtype, g, a, *maps, num_chunks,
+                                                as_stream(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "paged decode (several queries) launch");
+  }
   return PKV_OK;
 }
 
@@ -455,6 +543,47 @@ pkv_status pkv_decode_step(const pkv_pool* pool, int layer, const float* q, cons
   return attention_impl(pool, layer, q, k_new, v_new, block_table, bt_stride, seq_lens, num_rows,
                         n_q_heads, scale, out, workspace, workspace_bytes, num_chunks, stream,
                         Mode::kMerged);
+}
+
+size_t paged_decode_workspace_bytes_mq(int max_rows, int n_q_heads, int n_kv_heads, int head_dim,
+                                       int num_chunks) {
+  if (max_rows < 0 || num_chunks < 1 || n_kv_heads <= 0 || n_q_heads <= 0 ||
+      n_q_heads % n_kv_heads || head_dim != PKV_HEAD_DIM)
+    return 0;
+  return workspace_needed_mq(max_rows, n_kv_heads, num_chunks);
+}
+
+pkv_status paged_decode_default_chunks_mq(const pkv_pool* pool, int n_q_heads, int max_rows,
+                                          int* chunks) {
+  if (!pool || !chunks) return fail(PKV_ERR_INVALID_ARG, "null pool or output pointer");
+  pkv_status s = check_geometry(n_q_heads, pool->n_kv, pool->head_dim);
+  if (s) return s;
+  if (max_rows < 1 || max_rows > PKV_MAX_ROWS)
+    return fail(PKV_ERR_UNSUPPORTED, "max_rows %d outside [1, %d]", max_rows, PKV_MAX_ROWS);
+  return default_chunks_mq(pool, max_rows, chunks);
+}
+
+pkv_status paged_decode_attention_mq(const pkv_pool* pool, int layer, const float* q,
+                                     const int32_t* block_table, int bt_stride,
+                                     const int32_t* seq_lens, int num_rows, int q_len,
+                                     int n_q_heads, float scale, float* out, void* workspace,
+                                     size_t workspace_bytes, int num_chunks, void* stream) {
+  return attention_mq_impl(pool, layer, q, nullptr, nullptr, block_table, bt_stride, seq_lens,
+                           num_rows, q_len, n_q_heads, scale, out, workspace, workspace_bytes,
+                           num_chunks, stream);
+}
+
+pkv_status pkv_decode_step_mq(const pkv_pool* pool, int layer, const float* q, const float* k_new,
+                              const float* v_new, const int32_t* block_table, int bt_stride,
+                              const int32_t* seq_lens, int num_rows, int q_len, int n_q_heads,
+                              float scale, float* out, void* workspace, size_t workspace_bytes,
+                              int num_chunks, void* stream) {
+  if (num_rows > 0 && (!k_new || !v_new)) return fail(PKV_ERR_INVALID_ARG, "null k_new or v_new");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16))
+    return fail(PKV_ERR_INVALID_ARG, "k_new / v_new not 16-byte aligned");
+  return attention_mq_impl(pool, layer, q, k_new, v_new, block_table, bt_stride, seq_lens,
+                           num_rows, q_len, n_q_heads, scale, out, workspace, workspace_bytes,
+                           num_chunks, stream);
 }
 
 const char* pkv_status_string(pkv_status s) {

@@ -62,64 +62,11 @@
 
 #include <cudaTypedefs.h>
 
+#include "decode_common.cuh"
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
-
-// Build-time knobs (defaults are the tuned values): shared-memory stages per
-// warp and the CTAs per SM the register allocation must allow, for each
-// dtype (q8_0 is bound by instruction issue: more warps hide more latency),
-// programmatic dependent launch of the decode kernel (1 on), and the partial
-// states a merge loads per round trip.
-#ifndef PKV_F16_RING
-#define PKV_F16_RING 2
-#endif
-#ifndef PKV_Q8_RING
-#define PKV_Q8_RING 2
-#endif
-#ifndef PKV_F16_CTAS_PER_SM
-#define PKV_F16_CTAS_PER_SM 3
-#endif
-#ifndef PKV_Q8_CTAS_PER_SM
-#define PKV_Q8_CTAS_PER_SM 4
-#endif
-#ifndef PKV_PDL
-#define PKV_PDL 1
-#endif
-#ifndef PKV_MERGE_BATCH
-#define PKV_MERGE_BATCH 8  // 4 for q8_0, whose 4 CTAs per SM leave 128 registers a thread
-#endif
-
-constexpr int kWarps = 4;  // warps per CTA; the final piece merge gives each thread one dim
-constexpr int kThreads = kWarps * 32;
-static_assert(kThreads == kD, "the final piece merge maps one thread to one dim");
-
-// Shared-memory stage of one unit: the K tile then the V tile of one
-// (page, KV head), each [16 tokens][128 dims] under the 128-byte swizzle
-// (f16: two 2 KiB halves of 64 dims); q8_0 block scales in a separate area.
-template <int DT>
-struct Tiles;
-template <>
-struct Tiles<PKV_KV_F16> {
-  static constexpr uint32_t kData = kPage * kD * 2;  // 4096 bytes of one K or V tile
-  static constexpr uint32_t kScale = 0;
-  static constexpr uint32_t kCodes = 2 * kData;  // K and V tiles of a stage
-  static constexpr uint32_t kScales = 0;
-  static constexpr uint32_t kTx = kCodes;  // bytes a stage's barrier waits for
-  static constexpr int kRing = PKV_F16_RING;  // stages per warp
-};
-template <>
-struct Tiles<PKV_KV_BF16> : Tiles<PKV_KV_F16> {};  // same geometry: 16-bit values
-template <>
-struct Tiles<PKV_KV_Q8_0> {
-  static constexpr uint32_t kData = kPage * kD;                   // 2048 codes
-  static constexpr uint32_t kScale = kPage * (kD / kQBlock) * 2;  // 128 bytes of f16 scales
-  static constexpr uint32_t kCodes = 2 * kData;
-  static constexpr uint32_t kScales = 2 * kScale;  // K scales then V scales
-  static constexpr uint32_t kTx = kCodes + kScales;
-  static constexpr int kRing = PKV_Q8_RING;  // stages per warp
-};
 
 // Offsets from a 1024-byte aligned base.  The tiles come first (the swizzle
 // atom is 1024 bytes), then scales, barriers, the merge buffer, control
@@ -142,49 +89,6 @@ struct Smem {
                 "vector accesses need 16-byte aligned regions");
 };
 
-// ------------------------------------------------------------ operands ----
-// Byte offset of the 16-byte chunk c (8 f16 or 16 int8 values) of token row t
-// in a swizzled tile: 128-byte rows, chunk index xor (row mod 8); f16 tiles
-// keep dims 64..127 in a second 2 KiB half.
-template <int DT>
-__device__ __forceinline__ uint32_t tile_offset(int t, int c) {
-  if constexpr (DT != PKV_KV_Q8_0)
-    return (c >> 3) * 2048 + t * 128 + (((c & 7) ^ (t & 7)) << 4);
-  else
-    return t * 128 + ((c ^ (t & 7)) << 4);
-}
-
-// Two signed 8-bit codes of `u` (the word xor 0x80808080, i.e. code + 128 in
-// each byte) as an exact f16 pair: the bytes chosen by `sel` go into the low
-// mantissa byte of 1024 (0x64xx = 1024 + code + 128), then 1152 is
-// subtracted in f16.
-template <uint32_t kSel>
-__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t u) {
-  const uint32_t biased = __byte_perm(u, 0x64646464u, kSel);
-  const __half2 r = __hsub2(*reinterpret_cast<const __half2*>(&biased),
-                            __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480)));
-  return *reinterpret_cast<const uint32_t*>(&r);
-}
-constexpr uint32_t kSelB01 = 0x4140, kSelB23 = 0x4342, kSelB02 = 0x4240, kSelB13 = 0x4341;
-
-// The tf32 part of x (`lo` false: its rounding; true: the rounding of the
-// remainder), as an fp32 bit pattern.
-__device__ __forceinline__ uint32_t tf32_part(float x, bool lo) {
-  const uint32_t h = to_tf32(x);
-  return lo ? to_tf32(x - __uint_as_float(h)) : h;
-}
-
-// The f16 part (`lo` false: the rounding of x; true: the rounding of the
-// remainder) of a pair, low half x0.
-__device__ __forceinline__ uint32_t split_f16x2(float x0, float x1, bool lo) {
-  __half2 h = __floats2half2_rn(x0, x1);
-  if (lo) {
-    const float2 f = __half22float2(h);
-    h = __floats2half2_rn(x0 - f.x, x1 - f.y);
-  }
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
 // Per-warp online softmax state for one piece.
 template <int DT>
 struct WarpState {
@@ -197,16 +101,6 @@ struct WarpState {
   int vx;             // q8_0: every V block scale of the piece so far is below 2^vx
 };
 
-// The P operand is scaled by a power of two so that its f16 parts stay
-// normal: f16 KV by 2^7 (p <= 2^8, so P <= 2^15); q8_0, where P carries the V
-// block scale, by 2^(7 - vx) with 2^vx above every V scale of the piece so
-// far (raised, with the accumulators rescaled, when a page exceeds it).  O
-// holds the scaled sums; o_scale() undoes it.
-constexpr int kPShift = 7;
-constexpr int kNoScale = -64;  // vx before the piece's first page
-__device__ __forceinline__ float pow2i(int e) {  // 2^e for -126 <= e <= 127
-  return __int_as_float((127 + e) << 23);
-}
 template <int DT>
 __device__ __forceinline__ float o_scale(const WarpState<DT>& S) {
   if constexpr (DT == PKV_KV_F16)
@@ -492,115 +386,6 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
   __syncwarp();
 }
 
-// ---------------------------------------------------------------- merge ----
-// Merge the base-2 partial states of segment j held in slots k + j for the
-// chunks k0..k1 that meet it; one thread per dim d, all G heads:
-//   M = max_k m2_k,  out = sum_k 2^(m2_k - M) acc_k / sum_k 2^(m2_k - M) l_k,
-// evaluated batch by batch with a running maximum (the sums are rescaled when
-// it grows).  Loads go through L2 (other CTAs wrote the slots in this
-// launch); a batch of pieces costs one round trip.
-template <int G, int kBatch = PKV_MERGE_BATCH>  // kBatch: pieces loaded per round trip
-__device__ __forceinline__ void merge_segment(const float* part_ml, const float* part_acc,
-                                              long long j, int k0, int k1, float* o, int d) {
-  float M[G], Ls[G], A[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    M[g] = -INFINITY;
-    Ls[g] = 0.f;
-    A[g] = 0.f;
-  }
-  for (int kk = k0; kk <= k1; kk += kBatch) {
-    float m[kBatch][G], l[kBatch][G], x[kBatch][G];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const bool in = kk + u <= k1;
-      const long long slot = kk + u + j;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        m[u][g] = in ? __ldcg(part_ml + (slot * G + g) * 2) : -INFINITY;
-        l[u][g] = in ? __ldcg(part_ml + (slot * G + g) * 2 + 1) : 0.f;
-        x[u][g] = in ? __ldcg(part_acc + (slot * G + g) * kD + d) : 0.f;
-      }
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float bm = M[g];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) bm = fmaxf(bm, m[u][g]);
-      const float sc = exp2f(M[g] - bm);  // 0 on the first batch (M = -inf)
-      Ls[g] *= sc;
-      A[g] *= sc;
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const float w = exp2f(m[u][g] - bm);
-        Ls[g] = fmaf(w, l[u][g], Ls[g]);
-        A[g] = fmaf(w, x[u][g], A[g]);
-      }
-      M[g] = bm;
-    }
-  }
-#pragma unroll
-  for (int g = 0; g < G; ++g) o[g * kD + d] = A[g] / Ls[g];
-}
-
-// Chunks actually used for T units when C are launched: min(C, T), so that
-// no chunk is empty.
-__device__ __forceinline__ int used_chunks(long long T, int C) {
-  return static_cast<int>(T < C ? T : C);
-}
-
-// ------------------------------------------------------------- append ----
-// A warp stores row i's new K and V token of KV head h into slot (L - 1) % 16
-// of tile (page, h) just before it bulk-copies that tile: 4 dims per lane;
-// q8_0 blocks of 32 dims span 8 lanes.  Same encoding as kv_append.
-template <int DT>
-__device__ __forceinline__ void append_token(const DecodeArgs& a, int i, int h, int page,
-                                                   int slot, int lane) {
-  using TL = Tiles<DT>;
-  const size_t tile = static_cast<size_t>(page) * a.n_kv + h;
-  const long long src = (static_cast<long long>(i) * a.n_kv + h) * kD + lane * 4;
-#pragma unroll
-  for (int which = 0; which < 2; ++which) {
-    const float4 x = __ldg(reinterpret_cast<const float4*>((which ? a.v_new : a.k_new) + src));
-    uint8_t* data = which ? a.v_data : a.k_data;
-    if constexpr (DT == PKV_KV_F16) {
-      const __half2 lo = __floats2half2_rn(x.x, x.y), hi = __floats2half2_rn(x.z, x.w);
-      uint2 w;
-      w.x = *reinterpret_cast<const uint32_t*>(&lo);
-      w.y = *reinterpret_cast<const uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(data + tile * TL::kData + slot * (kD * 2) + lane * 8) = w;
-    } else if constexpr (DT == PKV_KV_BF16) {
-      const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
-      uint2 w;
-      w.x = *reinterpret_cast<const uint32_t*>(&lo);
-      w.y = *reinterpret_cast<const uint32_t*>(&hi);
-      *reinterpret_cast<uint2*>(data + tile * TL::kData + slot * (kD * 2) + lane * 8) = w;
-    } else {
-      float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
-      const float dq = amax / 127.0f;
-      const float v[4] = {x.x, x.y, x.z, x.w};
-      uint32_t packed = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float c = dq != 0.0f ? fminf(fmaxf(roundf(v[e] / dq), -127.0f), 127.0f) : 0.0f;
-        packed |= (static_cast<uint32_t>(static_cast<int>(c)) & 0xffu) << (8 * e);
-      }
-      *reinterpret_cast<uint32_t*>(data + tile * TL::kData + slot * kD + lane * 4) = packed;
-      if ((lane & 7) == 0) {
-        uint8_t* sc = which ? a.v_scales : a.k_scales;
-        reinterpret_cast<__half*>(sc + tile * TL::kScale)[slot * (kD / kQBlock) + (lane >> 3)] =
-            __float2half_rn(dq);
-      }
-    }
-  }
-  // The tile is read next by the async proxy (bulk copy): order these generic
-  // writes before it.
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-  __syncwarp();
-}
-
 // ------------------------------------------------------------ piece merge ----
 // The warp that arrives last at the end of a piece combines the four warps'
 // states from shared memory: lane l owns dims 4l..4l+3 of every head.  A
@@ -638,76 +423,6 @@ __device__ __forceinline__ void piece_merge(const float* mrg_acc, const float* m
       }
     }
   }
-}
-
-// The same merge as merge_segment, done by one warp (lane l: dims 4l..4l+3).
-template <int G>
-__device__ __forceinline__ void merge_segment_warp(const float* part_ml, const float* part_acc,
-                                                   long long j, int k0, int k1, float* o, int lane) {
-  constexpr int kBatch = 2;
-  float M[G], Ls[G];
-  float4 A[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    M[g] = -INFINITY;
-    Ls[g] = 0.f;
-    A[g] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-  for (int kk = k0; kk <= k1; kk += kBatch) {
-    float m[kBatch][G], l[kBatch][G];
-    float4 x[kBatch][G];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const bool in = kk + u <= k1;
-      const long long slot = kk + u + j;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        m[u][g] = in ? __ldcg(part_ml + (slot * G + g) * 2) : -INFINITY;
-        l[u][g] = in ? __ldcg(part_ml + (slot * G + g) * 2 + 1) : 0.f;
-        x[u][g] = in ? __ldcg(reinterpret_cast<const float4*>(part_acc + (slot * G + g) * kD) + lane)
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float bm = M[g];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) bm = fmaxf(bm, m[u][g]);
-      const float sc = exp2f(M[g] - bm);
-      Ls[g] *= sc;
-      A[g].x *= sc;
-      A[g].y *= sc;
-      A[g].z *= sc;
-      A[g].w *= sc;
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const float w = exp2f(m[u][g] - bm);
-        Ls[g] = fmaf(w, l[u][g], Ls[g]);
-        A[g].x = fmaf(w, x[u][g].x, A[g].x);
-        A[g].y = fmaf(w, x[u][g].y, A[g].y);
-        A[g].z = fmaf(w, x[u][g].z, A[g].z);
-        A[g].w = fmaf(w, x[u][g].w, A[g].w);
-      }
-      M[g] = bm;
-    }
-  }
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-    *reinterpret_cast<float4*>(o + g * kD + lane * 4) =
-        make_float4(A[g].x / Ls[g], A[g].y / Ls[g], A[g].z / Ls[g], A[g].w / Ls[g]);
-}
-
-// Spin (bounded) until the shared merge buffer has been released for piece
-// `piece`; false on timeout or abort.
-__device__ __forceinline__ bool wait_merge_buffer(volatile int* ctl, int piece) {
-  if (ctl[2] >= piece) return true;
-  const unsigned long long t0 = global_ns();
-  while (ctl[2] < piece) {
-    if (ctl[0]) return false;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
-    __nanosleep(32);
-  }
-  return true;
 }
 
 // --------------------------------------------------------------- kernel ----
@@ -820,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, DT != PKV_KV_Q8_0 ? PKV_F16_CTAS_PER
     const int hh = __shfl_sync(kFull, c_h, jj);
     if (a.k_new != nullptr && __shfl_sync(kFull, c_last, jj)) {
       const int row = __shfl_sync(kFull, c_row, jj);
-      append_token<DT>(a, row, hh, pg, (lens[row] - 1) % kPage, lane);
+      append_token<DT>(a, row, hh, pg, (lens[row] - 1) % kPage, lane);  // row's k_new/v_new
     }
     // The warp's earlier reads of this stage come before the copy rewrites it.
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -191,11 +191,13 @@ __device__ __forceinline__ int window_start(int L, int window) {
 // pages each row reads, in shared memory.  lens[i] is seq_lens[i] clamped to
 // [0, 16 * bt_stride] (a clamp records PKV_DEV_BAD_LENGTH); a row reads the
 // pages holding tokens [window_start, L), block-table entries
-// window_start / 16 onwards; row_start has num_rows + 1 entries.  Warp 0
-// scans; every thread of the CTA must call it.
+// window_start / 16 onwards; row_start has num_rows + 1 entries.  Rows
+// shorter than min_len (the queries of a several-query step) read nothing
+// and record PKV_DEV_BAD_LENGTH.  Warp 0 scans; every thread of the CTA must
+// call it.
 __device__ __forceinline__ void plan_rows(const int32_t* __restrict__ seq_lens, int num_rows,
                                           int bt_stride, int window, int32_t* status, int* lens,
-                                          int* row_start) {
+                                          int* row_start, int min_len = 1) {
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     int carry = 0;
@@ -211,6 +213,11 @@ __device__ __forceinline__ void plan_rows(const int32_t* __restrict__ seq_lens, 
           L = L < 0 ? 0 : cap;
         }
         lens[r] = L;
+      }
+      if (L > 0 && L < min_len) {  // fewer tokens than the step's queries: nothing read
+        record_status(status, PKV_DEV_BAD_LENGTH);
+        L = 0;
+        lens[r] = 0;
       }
       int v = L > 0 ? (L + kPage - 1) / kPage - window_start(L, window) / kPage : 0;
 #pragma unroll

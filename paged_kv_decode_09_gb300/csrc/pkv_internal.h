@@ -30,6 +30,8 @@ struct DecodeArgs {
   int n_q;
   float qscale;  // softmax scale * log2(e): scores are kept in base 2
   int window;    // > 0: each row attends to its last `window` tokens
+  int q_len;     // queries (new tokens) per row; q, out [rows][q_len][n_q][128]
+  int q0, nq;    // several-query kernel: this pass's queries q0 .. q0 + nq - 1
   float* out;
   float* part_ml;   // [slots][G][2]
   float* part_acc;  // [slots][G][128]
@@ -107,6 +109,13 @@ cudaError_t encode_tile_maps(int dtype, void* k_data, void* v_data, long long ti
 cudaError_t launch_paged_decode(int dtype, int group, const DecodeArgs& a, const TileMaps& maps,
                                 int chunks, cudaStream_t stream);
 cudaError_t paged_decode_blocks_per_sm(int dtype, int group, int rows, int* blocks);
+// The several-query kernel: one pass of up to mq_pass_queries(dtype, group)
+// queries (a.q0, a.nq) over the same plan.
+int mq_pass_queries(int dtype, int group);
+cudaError_t launch_paged_decode_mq(int dtype, int group, const DecodeArgs& a, const TileMaps& maps,
+                                   int chunks, cudaStream_t stream);
+cudaError_t paged_decode_mq_blocks_per_sm(int dtype, int rows, int* blocks);
+constexpr int kMqCols = 8;  // partial-state columns of a several-query workspace slot
 cudaError_t launch_combine(int group, const CombineArgs& a, cudaStream_t stream);
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
 cudaError_t launch_append(int dtype, const AppendArgs& a, cudaStream_t stream);

@@ -210,3 +210,16 @@ def used_slots(wl: Workload, include_appended: bool = True) -> np.ndarray:
         t = np.arange(n)
         mask[wl.block_table[i, t // PAGE], t % PAGE] = True
     return mask
+
+
+def mq_inputs(wl: Workload, q_len: int, seed: int = 0):
+    """Queries and new K/V of a step with q_len new tokens per row (the
+    verification of q_len - 1 drafted tokens, or a prefill chunk of q_len):
+    q fp32 [rows][q_len][n_q][D], k_new and v_new fp32 [rows][q_len][n_kv][D],
+    N(0, 1), from a stream seeded by (config seed, q_len, seed)."""
+    cfg = wl.cfg
+    rng = np.random.default_rng([cfg.seed, 1000 + q_len, seed])
+    q = rng.standard_normal((wl.rows, q_len, cfg.n_q_heads, cfg.head_dim), dtype=np.float32)
+    k_new = rng.standard_normal((wl.rows, q_len, cfg.n_kv_heads, cfg.head_dim), dtype=np.float32)
+    v_new = rng.standard_normal((wl.rows, q_len, cfg.n_kv_heads, cfg.head_dim), dtype=np.float32)
+    return q, k_new, v_new
