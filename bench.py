@@ -56,6 +56,8 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU baseline budget")
     p.add_argument("--window", type=int, default=0,
                    help="sliding window of every layer (0: none); bytes count attended tokens")
+    p.add_argument("--q-len", type=int, default=1,
+                   help="new tokens (queries) per row: > 1 times the several-query step")
     p.add_argument("--kernel", choices=["step", "append", "split_combine", "plan", "alloc"],
                    default="step",
                    help="step: the decode step (the benchmark); the others run --steps calls of\n"
@@ -159,18 +161,25 @@ def read_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def attended_tokens(wl, window=0) -> int:
-    """Tokens attended by one decode call: L per row, min(L, window) with a window."""
-    return int(sum(min(int(L), window) if window > 0 else int(L) for L in wl.seq_lens))
+def row_tokens(L: int, window=0, q_len=1) -> int:
+    """Tokens a row of L tokens needs in one call: all L, or with a window W the
+    union of its q_len queries' windows, the last min(L, W + q_len - 1)."""
+    return min(L, window + q_len - 1) if window > 0 else L
 
 
-def step_bytes(wl, window=0) -> int:
-    """Algorithmic bytes of one decode call: K and V of every attended token
-    (f16: 2 bytes per element; q8_0: 34 bytes per 32 elements), q and out."""
+def attended_tokens(wl, window=0, q_len=1) -> int:
+    """Tokens read once by one decode call, summed over rows (see row_tokens)."""
+    return int(sum(row_tokens(int(L), window, q_len) for L in wl.seq_lens))
+
+
+def step_bytes(wl, window=0, q_len=1) -> int:
+    """Algorithmic bytes of one decode call: K and V of every needed token read
+    once (f16, bf16: 2 bytes per element; q8_0: 34 bytes per 32 elements),
+    q and out (fp32, q_len queries per row)."""
     cfg = wl.cfg
     per_elem = 34.0 / 32.0 if cfg.dtype == 1 else 2.0  # q8_0; f16 and bf16
-    kv = attended_tokens(wl, window) * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem
-    qo = 2 * wl.rows * cfg.n_q_heads * cfg.head_dim * 4
+    kv = attended_tokens(wl, window, q_len) * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem
+    qo = 2 * wl.rows * q_len * cfg.n_q_heads * cfg.head_dim * 4
     return int(kv + qo)
 
 
@@ -234,10 +243,19 @@ def run_ours(args, rank, world, local):
         pool.set_window(layer, args.window)
 
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
-    q, k_new, v_new = t(wl.q), t(wl.k_new), t(wl.v_new)
+    QL = args.q_len
+    if QL > 1:  # verification / chunk step: q_len new tokens per row
+        hq_np, hk_np, hv_np = W.mq_inputs(wl, QL)
+        q, k_new, v_new = t(hq_np), t(hk_np), t(hv_np)
+        ws = api.WorkspaceMQ(pool, cfg.n_q_heads, wl.rows, args.chunks)
+        per_pass = (4 if cfg.dtype == W.BF16 else 8) // cfg.group
+        passes = -(-QL // per_pass)
+    else:
+        q, k_new, v_new = t(wl.q), t(wl.k_new), t(wl.v_new)
+        ws = api.Workspace(pool, cfg.n_q_heads, wl.rows, args.chunks)
+        passes = 1
     bt, sl = t(wl.block_table), t(wl.seq_lens)
     out = torch.empty_like(q)
-    ws = api.Workspace(pool, cfg.n_q_heads, wl.rows, args.chunks)
     L = api.lib()
     stream = torch.cuda.current_stream(dev)
     sp = ctypes.c_void_p(stream.cuda_stream)
@@ -251,8 +269,12 @@ def run_ours(args, rank, world, local):
             raise api.PkvError(st, what, L.pkv_last_error_message().decode())
 
     def step(layer):
-        chk(L.pkv_decode_step(H, layer, a_q, a_k, a_v, a_bt, S, a_sl, R, NQ, scale, a_out, a_ws,
-                              ws.nbytes, CH, sp), "pkv_decode_step")
+        if QL > 1:
+            chk(L.pkv_decode_step_mq(H, layer, a_q, a_k, a_v, a_bt, S, a_sl, R, QL, NQ, scale,
+                                     a_out, a_ws, ws.nbytes, CH, sp), "pkv_decode_step_mq")
+        else:
+            chk(L.pkv_decode_step(H, layer, a_q, a_k, a_v, a_bt, S, a_sl, R, NQ, scale, a_out,
+                                  a_ws, ws.nbytes, CH, sp), "pkv_decode_step")
 
     for w in range(args.warmup):
         step(w % layers)
@@ -277,7 +299,9 @@ def run_ours(args, rank, world, local):
     clock_info = clocks.stop()
     barrier(world)
     total_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    launch_ms = total_ms / K  # the only kernel in the timed region: its mean launch-to-launch time
+    # the only kernel in the timed region: a step is `passes` back-to-back
+    # launches of it; the roofline takes the step (all passes) as the unit
+    launch_ms = total_ms / K
     assert pool.read_status() == 0, "device status word set during the timed steps"
 
     # ---- end to end through the C ABI: pinned host inputs in, output out
@@ -290,8 +314,7 @@ def run_ours(args, rank, world, local):
     def e2e_step(layer):
         for d_, h_ in ((q, hq), (k_new, hk), (v_new, hv), (bt, hbt), (sl, hsl)):
             d_.copy_(h_, non_blocking=True)
-        chk(L.pkv_decode_step(H, layer, a_q, a_k, a_v, a_bt, S, a_sl, R, NQ, scale, a_out, a_ws,
-                              ws.nbytes, CH, sp), "pkv_decode_step")
+        step(layer)
         hout.copy_(out, non_blocking=True)
 
     Ke = min(K, 2000)
@@ -308,12 +331,13 @@ def run_ours(args, rank, world, local):
     barrier(world)
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world)
 
-    nbytes = step_bytes(wl, args.window)
+    nbytes = step_bytes(wl, args.window, QL)
     peak, peak_src = read_peak()
     step_s = total_ms / 1e3 / K
     value = world * nbytes / step_s / 1e9
     achieved = nbytes / (launch_ms / 1e3) / 1e9
-    tokens = attended_tokens(wl, args.window)
+    tokens = attended_tokens(wl, args.window, QL)
+    kname = "paged_decode_mq_kernel" if QL > 1 else "paged_decode_kernel"
     result = {
         "metric": "paged decode-attn KV GB/s & % of GB300 HBM peak; rows*tokens/s at 1 GPU",
         "value": round(value, 2),
@@ -336,27 +360,28 @@ def run_ours(args, rank, world, local):
                   f"{layer_bytes / 2**20:.0f} MiB rotated (> 4x the 126 MiB L2)",
             "chunks": CH, "bytes_per_step": nbytes, "parallelism": f"replicas x{world}",
             **({"window": args.window} if args.window else {}),
+            **({"q_len": QL, "launches_per_step": passes} if QL > 1 else {}),
         },
         "frac_of_hbm_peak": round(value / world / peak, 4),
         "rows_tokens_per_s": round(world * tokens / step_s, 1),
         "rows_per_s": round(world * wl.rows / step_s, 1),
         "roofline": {
-            "bound": "hbm", "kernel": f"paged_decode_kernel<{W.DTYPE_NAMES[cfg.dtype]}, G="
-                                      f"{cfg.group}>",
+            "bound": "hbm", "kernel": f"{kname}<{W.DTYPE_NAMES[cfg.dtype]}, G={cfg.group}>",
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (copy bandwidth)",
-            "traffic": None if args.window else profile_traffic(cfg.name),
+            "traffic": None if args.window or QL > 1 else profile_traffic(cfg.name),
             "mean_launch_us": round(launch_ms * 1e3, 3),
             "timing": "events around the K back-to-back launches of the timed region",
         },
         "e2e": {"value": round(world * nbytes / (e2e_ms / 1e3 / Ke) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
                 "ms_per_step": round(e2e_ms / Ke, 6)},
-        "gpu_launches": K,
+        "gpu_launches": K * passes,
         "clocks": clock_info,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(wl, pool, args.cpu_seconds, args.window)
+        result["cpu_baseline"] = cpu_baseline(wl, pool, args.cpu_seconds, args.window, QL,
+                                              q.cpu().numpy())
     return result
 
 
@@ -443,7 +468,7 @@ def run_kernel(args, local):
             "note": "per-entry-point timing for profiling; not the benchmark metric"}
 
 
-def cpu_baseline(wl, pool, budget_s, window=0):
+def cpu_baseline(wl, pool, budget_s, window=0, q_len=1, q=None):
     """The FP64 oracle, as it stands, on a bounded sample of rows of layer 0."""
     import numpy as np
     import torch
@@ -462,16 +487,22 @@ def cpu_baseline(wl, pool, budget_s, window=0):
     done, secs, rows = 0, 0.0, []
     for i in order:
         t0 = time.perf_counter()
-        O.decode_attention(cfg.dtype, wl.q[i:i + 1], kd, vd, ks, vs, wl.block_table[i:i + 1],
-                           wl.seq_lens[i:i + 1], wl.num_pages, cfg.n_kv_heads, wl.scale,
-                           window=window)
+        if q_len > 1:
+            O.decode_attention_mq(cfg.dtype, q[i:i + 1], kd, vd, ks, vs, wl.block_table[i:i + 1],
+                                  wl.seq_lens[i:i + 1], wl.num_pages, cfg.n_kv_heads, wl.scale,
+                                  window=window)
+        else:
+            O.decode_attention(cfg.dtype, wl.q[i:i + 1], kd, vd, ks, vs, wl.block_table[i:i + 1],
+                               wl.seq_lens[i:i + 1], wl.num_pages, cfg.n_kv_heads, wl.scale,
+                               window=window)
         secs += time.perf_counter() - t0
         rows.append(int(i))
-        done += min(int(wl.seq_lens[i]), window) if window > 0 else int(wl.seq_lens[i])
+        done += row_tokens(int(wl.seq_lens[i]), window, q_len)
         if secs > budget_s:
             break
     per_elem = 34.0 / 32.0 if cfg.dtype == 1 else 2.0  # q8_0; f16 and bf16
-    nbytes = done * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem + 2 * len(rows) * cfg.n_q_heads * 128 * 4
+    nbytes = done * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem + \
+        2 * len(rows) * q_len * cfg.n_q_heads * 128 * 4
     return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": O.num_threads(),
             "kind": "oracle",
             "sample": f"{len(rows)} of {wl.rows} rows ({done} attended tokens) of one layer, "
@@ -498,8 +529,15 @@ def run_reference(args):
     # G-th query head of one row, i.e. one query head per KV head: 1/G of the
     # row's work, with the same per-head computation.
     heads = slice(None)
+    QL = args.q_len
+    q_mq = W.mq_inputs(wl, QL)[0] if QL > 1 else None
 
     def one(i):
+        if q_mq is not None:
+            O.decode_attention_mq(cfg.dtype, q_mq[i:i + 1, :, heads], kd, vd, ks, vs,
+                                  wl.block_table[i:i + 1], wl.seq_lens[i:i + 1], wl.num_pages,
+                                  cfg.n_kv_heads, wl.scale, window=args.window)
+            return
         q = wl.q[i:i + 1, heads]
         O.decode_attention(cfg.dtype, q, kd, vd, ks, vs, wl.block_table[i:i + 1],
                            wl.seq_lens[i:i + 1], wl.num_pages, cfg.n_kv_heads, wl.scale,
@@ -507,13 +545,12 @@ def run_reference(args):
 
     per_elem = 34.0 / 32.0 if cfg.dtype == 1 else 2.0  # q8_0; f16 and bf16
 
-    def row_tokens(i):
-        L = int(wl.seq_lens[i])
-        return min(L, args.window) if args.window > 0 else L
+    def tokens_of(i):
+        return row_tokens(int(wl.seq_lens[i]), args.window, QL)
 
     def row_bytes(i, frac):
-        return frac * (row_tokens(i) * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem
-                       + 2 * cfg.n_q_heads * 128 * 4)
+        return frac * (tokens_of(i) * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem
+                       + 2 * QL * cfg.n_q_heads * 128 * 4)
 
     mid = order[len(order) // 2]
     t0 = time.perf_counter()
@@ -533,7 +570,7 @@ def run_reference(args):
         one(i)
         secs += time.perf_counter() - t0
         nbytes += row_bytes(i, frac)
-        tokens += frac * row_tokens(i)
+        tokens += frac * tokens_of(i)
     value = nbytes / secs / 1e9
     return {
         "impl": "reference",
@@ -543,7 +580,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic: same seeded workload, pool encoded by the oracle",
         "config": {"workload": cfg.name, "description": cfg.description, "sample": sample,
-                   **({"window": args.window} if args.window else {})},
+                   **({"window": args.window} if args.window else {}),
+                   **({"q_len": QL} if QL > 1 else {})},
         "rows_tokens_per_s": round(tokens / secs, 1),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": O.num_threads(),
                          "kind": "oracle", "sample": sample},
