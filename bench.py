@@ -183,22 +183,32 @@ def step_bytes(wl, window=0, q_len=1) -> int:
     return int(kv + qo)
 
 
-def profile_traffic(workload: str):
-    """DRAM bytes per split-KV launch from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
+KERNEL_SOURCES = {  # the files each decode kernel is compiled from (besides headers of the ABI)
+    "paged_decode_kernel": ("decode.cu", "decode_common.cuh", "pkv_device.cuh"),
+    "paged_decode_mq_kernel": ("decode_mq.cu", "decode_common.cuh", "pkv_device.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
     src = os.path.join(ROOT, "paged_kv_decode_09_gb300", "csrc")
     h = hashlib.sha256()
-    for name in ("decode.cu", "pkv_device.cuh"):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(src, name), "rb") as f:
             h.update(f.read())
-    digest = h.hexdigest()[:16]
-    path = os.path.join(ROOT, "profiles", f"paged_decode_kernel_{workload}.md")
+    return h.hexdigest()[:16]
+
+
+def profile_traffic(workload: str, kernel: str = "paged_decode_kernel", q_len: int = 1):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, if it was taken on the current kernel source (else None)."""
+    suffix = f"_q{q_len}" if q_len > 1 else ""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}{suffix}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*(\d+)\s+source_sha256_16:\s*([0-9a-f]{16})", text)
-    if not m or m.group(2) != digest:
+    if not m or m.group(2) != kernel_source_hash(kernel):
         return None
     return int(m.group(1))
 
@@ -247,9 +257,13 @@ def run_ours(args, rank, world, local):
     if QL > 1:  # verification / chunk step: q_len new tokens per row
         hq_np, hk_np, hv_np = W.mq_inputs(wl, QL)
         q, k_new, v_new = t(hq_np), t(hk_np), t(hv_np)
-        ws = api.WorkspaceMQ(pool, cfg.n_q_heads, wl.rows, args.chunks)
-        per_pass = (4 if cfg.dtype == W.BF16 else 8) // cfg.group
-        passes = -(-QL // per_pass)
+        ws = api.WorkspaceMQ(pool, cfg.n_q_heads, wl.rows, QL, args.chunks)
+        cols = QL * cfg.group  # (query, head) columns; the kernel's pass width follows them
+        if cfg.dtype == W.Q8_0 or cols <= (4 if cfg.dtype == W.BF16 else 8):
+            width = min(cols, 8)
+        else:
+            width = 16 if cfg.dtype == W.BF16 or cols <= 16 else 32
+        passes = -(-QL // max(1, width // cfg.group))
     else:
         q, k_new, v_new = t(wl.q), t(wl.k_new), t(wl.v_new)
         ws = api.Workspace(pool, cfg.n_q_heads, wl.rows, args.chunks)
@@ -369,7 +383,9 @@ def run_ours(args, rank, world, local):
             "bound": "hbm", "kernel": f"{kname}<{W.DTYPE_NAMES[cfg.dtype]}, G={cfg.group}>",
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (copy bandwidth)",
-            "traffic": None if args.window or QL > 1 else profile_traffic(cfg.name),
+            # DRAM bytes of one launch (one pass: a step of the several-query
+            # kernel is `launches_per_step` of them)
+            "traffic": None if args.window else profile_traffic(cfg.name, kname, QL),
             "mean_launch_us": round(launch_ms * 1e3, 3),
             "timing": "events around the K back-to-back launches of the timed region",
         },

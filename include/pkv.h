@@ -265,25 +265,30 @@ pkv_status pkv_decode_step(const pkv_pool *pool, int layer, const float *q, cons
  * Rows with L == 0 get zeros; rows with 0 < L < q_len get zeros and set
  * PKV_DEV_BAD_LENGTH.  A row reads the pages holding [L - q_len + 1 - W, L)
  * (all of [0, L) without a window), split into chunks as in
- * paged_decode_attention.  Every page is read once per pass: a pass carries
- * up to 8 (query, query head) pairs of a KV head for f16 and q8_0 (4 for
- * bf16), i.e. ceil(q_len * G / 8) passes (ceil(q_len * G / 4) for bf16), each
- * one launch on `stream`.  pkv_decode_step_mq stores the new tokens in the
- * first pass, just before their pages are read; the last q_len positions'
- * pages must not be shared with another row.
+ * paged_decode_attention.  Every page is read once per pass; a pass carries
+ * the (query, query head) pairs of a KV head, C = q_len * G in all:
+ *     C <= 8 (bf16: 4), and q8_0: passes of 8 pairs (bf16: 4), the CTA's
+ *     warps reading different pages;
+ *     otherwise passes of 16 pairs (C <= 16, and bf16) or 32 (f16), the
+ *     CTA's four warps reading every page together, a quarter each;
+ * each pass one launch on `stream`.  pkv_decode_step_mq stores the new tokens
+ * in the first pass, just before their pages are read; the last q_len
+ * positions' pages must not be shared with another row.
  * Workspace (paged_decode_workspace_bytes_mq): as paged_decode_attention's
- * with 8 partial-state columns per slot instead of G:
- *     counters int32 [num_rows * n_kv_heads]
- *     part_ml  float [S][8][2];  part_acc float [S][8][head_dim]
+ * with 32 partial-state columns per slot instead of G and 4 counters per
+ * (row, KV head):
+ *     counters int32 [num_rows * n_kv_heads * 4]
+ *     part_ml  float [S][32][2];  part_acc float [S][32][head_dim]
  * zero-filled once before first use; not shared by concurrent calls. */
 #define PKV_MAX_Q_LEN 64
 
 size_t paged_decode_workspace_bytes_mq(int max_rows, int n_q_heads, int n_kv_heads, int head_dim,
                                        int num_chunks);
 
-/* Chunks (resident CTAs of the several-query kernel) that fill this GPU. */
+/* Chunks (resident CTAs of the several-query kernel that q_len selects) that
+ * fill this GPU. */
 pkv_status paged_decode_default_chunks_mq(const pkv_pool *pool, int n_q_heads, int max_rows,
-                                          int *chunks);
+                                          int q_len, int *chunks);
 
 pkv_status paged_decode_attention_mq(const pkv_pool *pool, int layer, const float *q,
                                      const int32_t *block_table, int bt_stride,

@@ -77,7 +77,7 @@ _SIGS = {
     "pkv_decode_step": ([_vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, ctypes.c_float, _vp, _vp,
                          _sz, _i, _vp], _i),
     "paged_decode_workspace_bytes_mq": ([_i, _i, _i, _i, _i], _sz),
-    "paged_decode_default_chunks_mq": ([_vp, _i, _i, ctypes.POINTER(_i)], _i),
+    "paged_decode_default_chunks_mq": ([_vp, _i, _i, _i, ctypes.POINTER(_i)], _i),
     "paged_decode_attention_mq": ([_vp, _i, _vp, _vp, _i, _vp, _i, _i, _i, ctypes.c_float, _vp,
                                    _vp, _sz, _i, _vp], _i),
     "pkv_decode_step_mq": ([_vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, ctypes.c_float,
@@ -293,13 +293,15 @@ def decode_step(pool: KVPool, layer: int, q, k_new, v_new, block_table, seq_lens
 
 
 class WorkspaceMQ:
-    """Device scratch for the several-query calls (8 partial-state columns per
-    slot), zero-filled as the library requires before first use."""
+    """Device scratch for the several-query calls (32 partial-state columns per
+    slot), zero-filled as the library requires before first use.  The default
+    chunk count depends on q_len (it selects the kernel)."""
 
-    def __init__(self, pool: KVPool, n_q_heads: int, max_rows: int, num_chunks: int = 0):
+    def __init__(self, pool: KVPool, n_q_heads: int, max_rows: int, q_len: int,
+                 num_chunks: int = 0):
         if not num_chunks:
             c = ctypes.c_int(0)
-            _check(lib().paged_decode_default_chunks_mq(pool.handle, n_q_heads, max_rows,
+            _check(lib().paged_decode_default_chunks_mq(pool.handle, n_q_heads, max_rows, q_len,
                                                         ctypes.byref(c)),
                    "paged_decode_default_chunks_mq")
             num_chunks = c.value
@@ -320,7 +322,7 @@ def _mq_args(pool, q, block_table, seq_lens, out, workspace, num_chunks):
         out = torch.empty_like(q)
     _need(out, torch.float32, "out", q.shape, pool.device)
     if workspace is None:
-        workspace = WorkspaceMQ(pool, q.shape[2], max(rows, 1), num_chunks)
+        workspace = WorkspaceMQ(pool, q.shape[2], max(rows, 1), max(q.shape[1], 1), num_chunks)
     return rows, stride, out, workspace, num_chunks or workspace.num_chunks
 
 

@@ -222,17 +222,17 @@ pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q, const
 // ------------------------------------------------- several queries per row
 size_t workspace_needed_mq(int num_rows, int n_kv, int num_chunks) {
   const long long slots = partial_slots(num_chunks, num_rows, n_kv);
-  return pkv::counter_bytes(static_cast<long long>(num_rows) * n_kv) +
+  return pkv::counter_bytes(static_cast<long long>(num_rows) * n_kv * pkv::kMqCounters) +
          pkv::part_ml_bytes(slots, pkv::kMqCols) + pkv::part_acc_bytes(slots, pkv::kMqCols);
 }
 
-pkv_status default_chunks_mq(const pkv_pool* p, int rows, int* chunks) {
+pkv_status default_chunks_mq(const pkv_pool* p, int group, int q_len, int rows, int* chunks) {
   int dev = 0, sms = 0, blocks = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  e = pkv::paged_decode_mq_blocks_per_sm(p->dtype, rows, &blocks);
+  e = pkv::paged_decode_mq_blocks_per_sm(p->dtype, group, q_len, rows, &blocks);
   if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
   if (blocks < 1) return fail(PKV_ERR_UNSUPPORTED, "attention kernel does not fit on an SM");
   *chunks = sms * blocks;
@@ -256,18 +256,18 @@ pkv_status attention_mq_impl(const pkv_pool* pool, int layer, const float* q, co
     return fail(PKV_ERR_INVALID_ARG, "q / out not 16-byte aligned");
   if (num_chunks < 0) return fail(PKV_ERR_INVALID_ARG, "num_chunks < 0");
   if (num_rows == 0) return PKV_OK;
-  if (num_chunks == 0 && (s = default_chunks_mq(pool, num_rows, &num_chunks))) return s;
+  const int g = n_q / pool->n_kv;
+  if (num_chunks == 0 && (s = default_chunks_mq(pool, g, q_len, num_rows, &num_chunks))) return s;
   const size_t need = workspace_needed_mq(num_rows, pool->n_kv, num_chunks);
   if (!workspace || workspace_bytes < need)
     return fail(PKV_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", workspace_bytes, need);
   if (!aligned(workspace, 256)) return fail(PKV_ERR_INVALID_ARG, "workspace not 256-byte aligned");
 
-  const int g = n_q / pool->n_kv;
   const long long slots = partial_slots(num_chunks, num_rows, pool->n_kv);
   uint8_t* wp = static_cast<uint8_t*>(workspace);
   pkv::DecodeArgs a;
   a.counters = reinterpret_cast<int32_t*>(wp);
-  wp += pkv::counter_bytes(static_cast<long long>(num_rows) * pool->n_kv);
+  wp += pkv::counter_bytes(static_cast<long long>(num_rows) * pool->n_kv * pkv::kMqCounters);
   a.part_ml = reinterpret_cast<float*>(wp);
   wp += pkv::part_ml_bytes(slots, pkv::kMqCols);
   a.part_acc = reinterpret_cast<float*>(wp);
@@ -290,7 +290,7 @@ pkv_status attention_mq_impl(const pkv_pool* pool, int layer, const float* q, co
   a.status = pool->status;
   const pkv::TileMaps* maps = nullptr;
   if ((s = layer_maps(pool, layer, &maps))) return s;
-  const int per_pass = pkv::mq_pass_queries(pool->dtype, g);
+  const int per_pass = pkv::mq_pass_queries(pool->dtype, g, q_len);
   for (int q0 = 0; q0 < q_len; q0 += per_pass) {
     a.q0 = q0;
     a.nq = q_len - q0 < per_pass ? q_len - q0 : per_pass;
@@ -554,13 +554,15 @@ size_t paged_decode_workspace_bytes_mq(int max_rows, int n_q_heads, int n_kv_hea
 }
 
 pkv_status paged_decode_default_chunks_mq(const pkv_pool* pool, int n_q_heads, int max_rows,
-                                          int* chunks) {
+                                          int q_len, int* chunks) {
   if (!pool || !chunks) return fail(PKV_ERR_INVALID_ARG, "null pool or output pointer");
   pkv_status s = check_geometry(n_q_heads, pool->n_kv, pool->head_dim);
   if (s) return s;
   if (max_rows < 1 || max_rows > PKV_MAX_ROWS)
     return fail(PKV_ERR_UNSUPPORTED, "max_rows %d outside [1, %d]", max_rows, PKV_MAX_ROWS);
-  return default_chunks_mq(pool, max_rows, chunks);
+  if (q_len < 1 || q_len > PKV_MAX_Q_LEN)
+    return fail(PKV_ERR_UNSUPPORTED, "q_len %d outside [1, %d]", q_len, PKV_MAX_Q_LEN);
+  return default_chunks_mq(pool, n_q_heads / pool->n_kv, q_len, max_rows, chunks);
 }
 
 pkv_status paged_decode_attention_mq(const pkv_pool* pool, int layer, const float* q,

@@ -36,14 +36,34 @@ namespace pkv {
 // Score n-tiles (4 columns each) per dtype: bf16 runs its scores as tf32
 // k-steps of 8 dims, whose query operands take twice the registers.
 template <int DT>
-constexpr int mq_tiles() {
+__host__ __device__ constexpr int mq_tiles() {
   return DT == PKV_KV_BF16 ? 1 : 2;
 }
 
-int mq_pass_queries(int dtype, int group) {
-  const int cols = dtype == PKV_KV_BF16 ? 4 : 8;
-  return cols / group > 0 ? cols / group : 1;
+// The kernel a call takes, by its q_len * G (query, head) columns: up to 8
+// (bf16: 4) the warps of a CTA read different pages (paged_decode_mq_kernel);
+// beyond, the four warps read every page together (paged_decode_mqt_kernel,
+// 4 columns a warp up to 16, else 8), in passes of 16 or 32 columns.  q8_0
+// always takes the first, in passes of 8 columns: its pages are converted
+// from int8 codes by the warp that reads them, so four warps sharing a page
+// would convert it four times (measured slower than a second pass).
+enum MqKind { kMqSingle = 0, kMqTeam1 = 1, kMqTeam2 = 2 };
+static int mq_kind(int dtype, int group, int q_len) {
+  const int cols = q_len * group;
+  if (dtype == PKV_KV_Q8_0) return kMqSingle;
+  if (dtype == PKV_KV_BF16) return cols <= 4 ? kMqSingle : kMqTeam1;
+  return cols <= 8 ? kMqSingle : cols <= 16 ? kMqTeam1 : kMqTeam2;
 }
+static int mq_kind_cols(int dtype, int kind) {
+  return kind == kMqSingle ? (dtype == PKV_KV_BF16 ? 4 : 8) : kind == kMqTeam1 ? 16 : 32;
+}
+
+int mq_pass_queries(int dtype, int group, int q_len) {
+  const int per = mq_kind_cols(dtype, mq_kind(dtype, group, q_len)) / group;
+  return per > 0 ? per : 1;
+}
+
+constexpr int kWarpCols = 8;  // (query, head) columns of one warp's state: 2 score n-tiles
 
 template <int DT>
 struct MqSmem {
@@ -52,17 +72,22 @@ struct MqSmem {
   static constexpr uint32_t kScl = kStages * Tiles<DT>::kCodes;
   static constexpr uint32_t kBar = kScl + kStages * Tiles<DT>::kScales;
   static constexpr uint32_t kMrgAcc = kBar + ((kStages * 8 + 15) / 16) * 16;  // f32 [warps][8][D]
-  static constexpr uint32_t kMrgMl = kMrgAcc + kWarps * kMqCols * kD * 4;      // f32 [warps][8][2]
-  static constexpr uint32_t kCtl = kMrgMl + kWarps * kMqCols * 2 * 4;
+  static constexpr uint32_t kMrgMl = kMrgAcc + kWarps * kWarpCols * kD * 4;    // f32 [warps][8][2]
+  static constexpr uint32_t kCtl = kMrgMl + kWarps * kWarpCols * 2 * 4;
   static constexpr uint32_t kRows = kCtl + 16;
   static size_t bytes(int rows) { return kAlign + kRows + (2 * static_cast<size_t>(rows) + 1) * 4; }
   static_assert(Tiles<DT>::kCodes % 1024 == 0, "tile stages keep the swizzle atom alignment");
 };
 
 template <int DT>
+__host__ __device__ constexpr int mq_steps() {  // k-steps over the 128 dims: f16 MMAs take 16 dims, tf32 MMAs 8
+  return DT == PKV_KV_BF16 ? 16 : 8;
+}
+
+template <int DT, int kTiles>
 struct MqState {
-  static constexpr int NT = mq_tiles<DT>();
-  static constexpr int kSteps = DT == PKV_KV_BF16 ? 16 : 8;
+  static constexpr int NT = kTiles;
+  static constexpr int kSteps = mq_steps<DT>();
   uint32_t qb[NT][kSteps][2];  // score B operands of n-tile t: column gid -> (4t + gid/2, part gid%2)
   float qexp[NT];              // 2^e of the lane's score column 4t + tig
   float m[NT], l[NT];          // softmax state of the lane's score columns
@@ -94,7 +119,7 @@ __device__ __forceinline__ int mq_dim(int r, int e, int gid) {
 // kernel, normalised by a power of two per column (f16, q8_0).
 template <int DT>
 __device__ __forceinline__ void mq_load_column(const float* qv, float qscale, bool lo, int tig,
-                                               uint32_t (&qb)[MqState<DT>::kSteps][2], int& e2) {
+                                               uint32_t (&qb)[mq_steps<DT>()][2], int& e2) {
   if constexpr (DT == PKV_KV_BF16) {
 #pragma unroll
     for (int ks = 0; ks < 16; ++ks) {
@@ -145,13 +170,12 @@ __device__ __forceinline__ void mq_load_column(const float* qv, float qscale, bo
 // Per-unit work of a pass: columns c < nc are (query q0 + c / G, head c % G);
 // pf is the page's first token; col_hi[t] / col_lo[t] bound the attended
 // positions of the lane's score column 4t + tig (empty for unused columns).
-template <int DT>
-__device__ __forceinline__ void mq_process_unit(uint8_t* st, const uint8_t* sc, int pf,
+template <int DT, int NT>
+__device__ __forceinline__ void mq_process_unit(const uint8_t* st, const uint8_t* sc, int pf,
                                                 const int (&col_lo)[2], const int (&col_hi)[2],
                                                 int slot_lo, int slot_hi, int nc, int lane,
-                                                MqState<DT>& S) {
+                                                MqState<DT, NT>& S) {
   using TL = Tiles<DT>;
-  constexpr int NT = MqState<DT>::NT;
   const int gid = lane >> 2, tig = lane & 3;
   const int ld_tok = (lane & 7) + ((lane >> 3) & 1) * 8;
   const int ld_chunk = lane >> 4;
@@ -296,15 +320,13 @@ __device__ __forceinline__ void mq_process_unit(uint8_t* st, const uint8_t* sc, 
 
   // ---- values: each part of P is its own B operand into the same accumulator
   if constexpr (DT != PKV_KV_Q8_0) {
-    if (slot_lo > 0 || slot_hi < kPage) {  // zero the V rows of slots no column attends
-      const int n_out = kPage - (slot_hi - slot_lo);
-      for (int x = lane; x < n_out * 16; x += 32) {
-        const int r = x >> 4, tt = r < slot_lo ? r : slot_hi + (r - slot_lo), c = x & 15;
-        *reinterpret_cast<uint4*>(st + TL::kData + (c >> 3) * 2048 + tt * 128 + (c & 7) * 16) =
-            make_uint4(0u, 0u, 0u, 0u);
-      }
-      __syncwarp();
-    }
+    // V values of slots no column attends may be anything (NaN * 0 is NaN):
+    // masked in the registers, the stage is shared by readers.  Fragment
+    // words hold tokens (2tig, 2tig + 1) [w0, w2] or (2tig + 8, 2tig + 9) [w1, w3].
+    auto ok = [&](int t) { return t >= slot_lo && t < slot_hi; };
+    const bool partial = slot_lo > 0 || slot_hi < kPage;  // warp-uniform
+    const uint32_t vm_lo = (ok(t0) ? 0x0000ffffu : 0u) | (ok(t0 + 1) ? 0xffff0000u : 0u);
+    const uint32_t vm_hi = (ok(t0 + 8) ? 0x0000ffffu : 0u) | (ok(t0 + 9) ? 0xffff0000u : 0u);
     if constexpr (DT == PKV_KV_F16) {
       constexpr float kUp = static_cast<float>(1 << kPShift);
       const uint32_t h0 = split_f16x2(pa * kUp, pb * kUp, false);
@@ -315,6 +337,12 @@ __device__ __forceinline__ void mq_process_unit(uint8_t* st, const uint8_t* sc, 
       for (int mt = 0; mt < 8; ++mt) {
         uint32_t w0, w1, w2, w3;
         ldsm_x4_trans(vt + tile_offset<DT>(ld_tok, 2 * mt + ld_chunk), w0, w1, w2, w3);
+        if (partial) {
+          w0 &= vm_lo;
+          w1 &= vm_hi;
+          w2 &= vm_lo;
+          w3 &= vm_hi;
+        }
         mma_16816(S.o[mt], w0, w2, w1, w3, h0, h1);
         mma_16816(S.o[mt], w0, w2, w1, w3, l0, l1);
       }
@@ -327,6 +355,12 @@ __device__ __forceinline__ void mq_process_unit(uint8_t* st, const uint8_t* sc, 
       for (int mt = 0; mt < 8; ++mt) {
         uint32_t w0, w1, w2, w3;
         ldsm_x4_trans(vt + tile_offset<DT>(ld_tok, 2 * mt + ld_chunk), w0, w1, w2, w3);
+        if (partial) {
+          w0 &= vm_lo;
+          w1 &= vm_hi;
+          w2 &= vm_lo;
+          w3 &= vm_hi;
+        }
         const uint32_t x0 = w0 << 16, x1 = w2 << 16, x2 = w0 & 0xffff0000u, x3 = w2 & 0xffff0000u;
         const uint32_t y0 = w1 << 16, y1 = w3 << 16, y2 = w1 & 0xffff0000u, y3 = w3 & 0xffff0000u;
         mma_1688_tf32(S.o[mt], x0, x1, x2, x3, h0, h1);
@@ -390,42 +424,73 @@ __device__ __forceinline__ void mq_process_unit(uint8_t* st, const uint8_t* sc, 
   __syncwarp();
 }
 
-// Merge the pieces k0..k1 of segment j (slots k + j, kMqCols columns each),
-// one warp, lane l: dims 4l..4l+3; column c of the pass goes to out_col(c).
-template <class OutCol>
+// Merge the pieces k0..k1 of segment j (slots k + j, kMqCols columns each)
+// for the columns c0 .. c0 + kCols - 1 that are below nc; one warp, lane l:
+// dims 4l..4l+3; column c goes to out_col(c).  The loads of kBatch pieces of
+// all kCols columns are issued together (one L2 round trip per batch).
+template <int kCols, int kBatch, class OutCol>
 __device__ __forceinline__ void mq_merge_segment_warp(const float* part_ml, const float* part_acc,
-                                                      long long j, int k0, int k1, int nc,
+                                                      long long j, int k0, int k1, int c0, int nc,
                                                       OutCol&& out_col, int lane) {
-  for (int c = 0; c < nc; ++c) {
-    float M = -INFINITY, Ls = 0.f;
-    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int kk = k0; kk <= k1; ++kk) {
-      const long long slot = (kk + j) * kMqCols + c;
-      const float m = __ldcg(part_ml + slot * 2), l = __ldcg(part_ml + slot * 2 + 1);
-      const float4 x = __ldcg(reinterpret_cast<const float4*>(part_acc + slot * kD) + lane);
-      const float bm = fmaxf(M, m);
-      if (bm == -INFINITY) continue;  // no token of this query in either
-      const float f0 = exp2f(M - bm), f1 = exp2f(m - bm);
-      Ls = Ls * f0 + l * f1;
-      A = make_float4(A.x * f0 + x.x * f1, A.y * f0 + x.y * f1, A.z * f0 + x.z * f1,
-                      A.w * f0 + x.w * f1);
-      M = bm;
+  float M[kCols], Ls[kCols];
+  float4 A[kCols];
+#pragma unroll
+  for (int u = 0; u < kCols; ++u) {
+    M[u] = -INFINITY;
+    Ls[u] = 0.f;
+    A[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int kk = k0; kk <= k1; kk += kBatch) {
+    float m[kBatch][kCols], l[kBatch][kCols];
+    float4 x[kBatch][kCols];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+      for (int u = 0; u < kCols; ++u) {
+        const bool in = kk + b <= k1 && c0 + u < nc;
+        const long long slot = (kk + b + j) * kMqCols + c0 + u;
+        m[b][u] = in ? __ldcg(part_ml + slot * 2) : -INFINITY;
+        l[b][u] = in ? __ldcg(part_ml + slot * 2 + 1) : 0.f;
+        x[b][u] = in ? __ldcg(reinterpret_cast<const float4*>(part_acc + slot * kD) + lane)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+    for (int u = 0; u < kCols; ++u) {
+      float bm = M[u];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) bm = fmaxf(bm, m[b][u]);
+      if (bm == -INFINITY) continue;  // no token of this query in any piece so far
+      const float sc = exp2f(M[u] - bm);
+      Ls[u] *= sc;
+      A[u] = make_float4(A[u].x * sc, A[u].y * sc, A[u].z * sc, A[u].w * sc);
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const float w = exp2f(m[b][u] - bm);
+        Ls[u] = fmaf(w, l[b][u], Ls[u]);
+        A[u] = make_float4(fmaf(w, x[b][u].x, A[u].x), fmaf(w, x[b][u].y, A[u].y),
+                           fmaf(w, x[b][u].z, A[u].z), fmaf(w, x[b][u].w, A[u].w));
+      }
+      M[u] = bm;
     }
-    const float inv = 1.0f / Ls;
-    *reinterpret_cast<float4*>(out_col(c) + lane * 4) =
-        make_float4(A.x * inv, A.y * inv, A.z * inv, A.w * inv);
+  }
+#pragma unroll
+  for (int u = 0; u < kCols; ++u) {
+    if (c0 + u >= nc) continue;
+    const float inv = 1.0f / Ls[u];
+    *reinterpret_cast<float4*>(out_col(c0 + u) + lane * 4) =
+        make_float4(A[u].x * inv, A[u].y * inv, A[u].z * inv, A[u].w * inv);
   }
 }
 
 // --------------------------------------------------------------- kernel ----
-template <int DT, int G>
+template <int DT>
 __global__ void __launch_bounds__(kThreads, 2)
     paged_decode_mq_kernel(const __grid_constant__ DecodeArgs a,
                            const __grid_constant__ TileMaps maps) {
   using TL = Tiles<DT>;
   using SM = MqSmem<DT>;
   constexpr int R = TL::kRing;
-  constexpr int NT = MqState<DT>::NT;
+  constexpr int NT = mq_tiles<DT>();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((SM::kAlign - (smem_addr(smem_raw) & (SM::kAlign - 1))) &
                               (SM::kAlign - 1));
@@ -439,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t bar0 = smem_addr(smem + SM::kBar) + warp * R * 8;
   uint8_t* ring = smem + static_cast<size_t>(warp) * R * TL::kCodes;
   uint8_t* ring_sc = smem + SM::kScl + static_cast<size_t>(warp) * R * TL::kScales;
+  const int G = a.n_q / a.n_kv;
   const int nc = a.nq * G;  // columns of this pass
   // the pages read cover the first query's window: [L - q_len + 1 - W, L)
   const int plan_window = a.window > 0 ? a.window + a.q_len - 1 : 0;
@@ -556,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* mrg_ml = reinterpret_cast<float*>(smem + SM::kMrgMl);
   bool aborted = false;
   int consumed = 0;
-  MqState<DT> S;
+  MqState<DT, NT> S;
 
   int piece = 0;
   for (long long x = c_begin; x < c_end; ++piece) {
@@ -622,12 +688,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       consumed = u + 1;
       const int pf = (p0 + static_cast<int>(pos - seg_start)) * kPage;  // page's first token
       const int slot_lo = max(0, pos_lo - pf), slot_hi = min(kPage, pos_hi - pf);
-      mq_process_unit<DT>(ring + s * TL::kCodes, ring_sc + s * TL::kScales, pf, col_lo, col_hi,
+      mq_process_unit<DT, NT>(ring + s * TL::kCodes, ring_sc + s * TL::kScales, pf, col_lo, col_hi,
                           slot_lo, slot_hi, nc, lane, S);
       if (issued < n_units) issue();
     }
 
-    // ---- piece end (as the single-query kernel, kMqCols columns)
+    // ---- piece end (as the single-query kernel, kWarpCols columns)
     float l_tot[NT];
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
@@ -652,8 +718,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         const int c = 4 * t + tig;
-        mrg_ml[(warp * kMqCols + c) * 2] = aborted ? -INFINITY : S.m[t];
-        mrg_ml[(warp * kMqCols + c) * 2 + 1] = l_tot[t];
+        mrg_ml[(warp * kWarpCols + c) * 2] = aborted ? -INFINITY : S.m[t];
+        mrg_ml[(warp * kWarpCols + c) * 2 + 1] = l_tot[t];
       }
     }
     {
@@ -663,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int c = 2 * tig + (e & 1);
-          mrg_acc[(warp * kMqCols + c) * kD + mq_dim<DT>(r, e & 2, gid)] = S.o[r][e] * osc;
+          mrg_acc[(warp * kWarpCols + c) * kD + mq_dim<DT>(r, e & 2, gid)] = S.o[r][e] * osc;
         }
     }
     const bool whole = (k0 == k1);
@@ -675,15 +741,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     auto merge_dim = [&](int c, int d, float& M, float& Ls, float& A) {
       M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mrg_ml[(w * kMqCols + c) * 2]);
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mrg_ml[(w * kWarpCols + c) * 2]);
       Ls = 0.f;
       A = 0.f;
       if (M == -INFINITY) return;  // no token of this query in the piece
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        const float f = exp2f(mrg_ml[(w * kMqCols + c) * 2] - M);
-        Ls = fmaf(f, mrg_ml[(w * kMqCols + c) * 2 + 1], Ls);
-        A = fmaf(f, mrg_acc[(w * kMqCols + c) * kD + d], A);
+        const float f = exp2f(mrg_ml[(w * kWarpCols + c) * 2] - M);
+        Ls = fmaf(f, mrg_ml[(w * kWarpCols + c) * 2 + 1], Ls);
+        A = fmaf(f, mrg_acc[(w * kWarpCols + c) * kD + d], A);
       }
     };
     auto write_piece_dim = [&](int c, int d, float M, float Ls, float A) {
@@ -720,10 +786,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         ctl[1] = seg_last;
       }
       named_barrier(1, kThreads);
-      if (ctl[1] && warp == 0) {
+      if (ctl[1]) {  // the CTA merges the segment: warp w takes columns 2w, 2w + 1
         __threadfence();
-        mq_merge_segment_warp(a.part_ml, a.part_acc, j, k0, k1, nc, out_col, lane);
-        if (lane == 0) a.counters[j] = 0;
+        mq_merge_segment_warp<2, 4>(a.part_ml, a.part_acc, j, k0, k1, 2 * warp, nc, out_col,
+                                    lane);
+        if (threadIdx.x == 0) a.counters[j] = 0;
       }
     } else {
       __syncwarp();
@@ -760,7 +827,8 @@ __global__ void __launch_bounds__(kThreads, 2)
           seg_last = __shfl_sync(kFull, seg_last, 0);
           if (seg_last) {
             __threadfence();
-            mq_merge_segment_warp(a.part_ml, a.part_acc, j, k0, k1, nc, out_col, lane);
+            mq_merge_segment_warp<kWarpCols, 1>(a.part_ml, a.part_acc, j, k0, k1, 0, nc, out_col,
+                                              lane);
             if (lane == 0) a.counters[j] = 0;
           }
         }
@@ -776,17 +844,351 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
+// -------------------------------------------------- shared-page kernel ----
+// With more than 8 (query, head) columns in a pass (more than 4 for bf16) the
+// four warps of a CTA read every page of the chunk together, warp w taking
+// columns [w CW, (w + 1) CW): a page is copied once for up to 4 CW columns.
+// The stages form one ring per CTA.  Unit v (the chunk's v-th page) is copied
+// by warp v mod 4 into stage v mod (stages), once all four warps have read
+// the unit that stage held before (an empty barrier of four arrivals).  Each
+// warp holds whole columns, so a piece end needs no merge inside the CTA: a
+// warp writes its columns (to the output, or to its workspace slot) and the
+// last piece of the segment to arrive for those columns merges them.
+// Stages of the CTA's ring, a multiple of kWarps (unit v + stages has v's
+// copier): as many as the shared memory of the CTAs an SM holds allows
+// (3 CTAs with 4 columns a warp, 2 with 8).
+__host__ __device__ constexpr int team_stages(int nt) { return nt == 1 ? 8 : 12; }
+
+template <int DT, int kStages>
+struct MqtSmem {
+  static constexpr uint32_t kAlign = 1024;
+  static constexpr uint32_t kScl = kStages * Tiles<DT>::kCodes;
+  static constexpr uint32_t kFull = kScl + kStages * Tiles<DT>::kScales;
+  static constexpr uint32_t kEmpty = kFull + kStages * 8;
+  static constexpr uint32_t kCtl = kEmpty + kStages * 8;
+  static constexpr uint32_t kRows = kCtl + 16;
+  static size_t bytes(int rows) { return kAlign + kRows + (2 * static_cast<size_t>(rows) + 1) * 4; }
+};
+
+template <int DT, int NT>
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2)
+    paged_decode_mqt_kernel(const __grid_constant__ DecodeArgs a,
+                            const __grid_constant__ TileMaps maps) {
+  using TL = Tiles<DT>;
+  constexpr int RS = team_stages(NT);
+  using SM = MqtSmem<DT, RS>;
+  constexpr int CW = 4 * NT;  // columns of one warp
+  static_assert(RS % kWarps == 0, "a unit and the unit RS later have the same copier");
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((SM::kAlign - (smem_addr(smem_raw) & (SM::kAlign - 1))) &
+                              (SM::kAlign - 1));
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  volatile int* ctl = reinterpret_cast<volatile int*>(smem + SM::kCtl);  // [0] abort
+  int* row_start = reinterpret_cast<int*>(smem + SM::kRows);
+  int* lens = row_start + a.num_rows + 1;
+  const uint32_t full0 = smem_addr(smem + SM::kFull), empty0 = smem_addr(smem + SM::kEmpty);
+  const int G = a.n_q / a.n_kv;
+  const int nc = a.nq * G;                             // columns of this pass
+  const int cbase = warp * CW;                         // this warp's first column
+  const int ncw = min(max(nc - cbase, 0), CW);         // and how many it has
+  const int plan_window = a.window > 0 ? a.window + a.q_len - 1 : 0;
+
+  if (threadIdx.x == 0) {
+    ctl[0] = 0;
+    for (int s = 0; s < RS; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kWarps);
+    }
+    fence_mbar_init();
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+  plan_rows(a.seq_lens, a.num_rows, a.bt_stride, plan_window,
+            blockIdx.x == 0 ? a.status : nullptr, lens, row_start, a.q_len);
+
+  const long long T = static_cast<long long>(a.n_kv) * row_start[a.num_rows];
+  const int C = used_chunks(T, gridDim.x), k = blockIdx.x;
+  const long long c_begin = k < C ? static_cast<long long>(k) * T / C : T;
+  const long long c_end = k < C ? static_cast<long long>(k + 1) * T / C : T;
+
+  if (k == 0) {  // rows without tokens (or shorter than q_len): zeros
+    for (int i = 0; i < a.num_rows; ++i)
+      if (row_start[i + 1] == row_start[i])
+        for (int jj = 0; jj < a.nq; ++jj)
+          for (int e = threadIdx.x; e < a.n_q * kD; e += kThreads)
+            a.out[((static_cast<long long>(i) * a.q_len + a.q0 + jj) * a.n_q) * kD + e] = 0.f;
+  }
+
+  const int n_units = static_cast<int>(c_end - c_begin);
+  // this warp copies the units v = warp + 4 u (u = 0, 1, ...)
+  const long long first = c_begin + warp;
+  const int n_mine = first < c_end ? static_cast<int>((c_end - first + kWarps - 1) / kWarps) : 0;
+
+  auto fetch = [&](int base, int& pg, int& hh, int& row, int& pidx) {
+    const int u = base + lane;
+    pg = hh = row = pidx = 0;
+    if (u < n_mine) {
+      const long long x = first + static_cast<long long>(u) * kWarps;
+      const int i = row_of(row_start, a.num_rows, a.n_kv, x);
+      const int npg = row_start[i + 1] - row_start[i];
+      const int off = static_cast<int>(x - static_cast<long long>(a.n_kv) * row_start[i]);
+      hh = off / npg;
+      const int p = off - hh * npg;
+      int pabs = window_start(lens[i], plan_window) / kPage + p;  // block-table entry
+      int page = __ldg(a.block_table + static_cast<long long>(i) * a.bt_stride + pabs);
+      if (page < 0 || page >= a.num_pages) {
+        record_status(a.status, PKV_DEV_BAD_PAGE);
+        page = 0;
+        pabs = -1;  // take no append
+      }
+      pg = page;
+      row = i;
+      pidx = pabs;
+    }
+  };
+  int c_pg, c_h, c_row, c_p, n_pg, n_h, n_row, n_p;
+  int batch = 0;
+  fetch(0, c_pg, c_h, c_row, c_p);
+  fetch(32, n_pg, n_h, n_row, n_p);
+  int issued = 0;  // units this warp has copied
+  const uint64_t policy = policy_evict_first();
+
+  auto issue = [&]() {  // this warp's next unit, v = warp + 4 issued
+    const int u = issued;
+    if (u >= batch + 32) {
+      c_pg = n_pg;
+      c_h = n_h;
+      c_row = n_row;
+      c_p = n_p;
+      batch += 32;
+      fetch(batch + 32, n_pg, n_h, n_row, n_p);
+    }
+    const int jj = u - batch;
+    const int pg = __shfl_sync(kFull, c_pg, jj);
+    const int hh = __shfl_sync(kFull, c_h, jj);
+    const int pabs = __shfl_sync(kFull, c_p, jj);
+    if (a.k_new != nullptr && pabs >= 0) {  // first pass: new tokens of this page first
+      const int row = __shfl_sync(kFull, c_row, jj);
+      const int L = lens[row], first_new = L - a.q_len;
+      const int lo = max(first_new, pabs * kPage), hi = min(L, pabs * kPage + kPage);
+      for (int pos = lo; pos < hi; ++pos)
+        append_token<DT>(a, static_cast<long long>(row) * a.q_len + (pos - first_new), hh, pg,
+                         pos % kPage, lane);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+      const int s = (warp + kWarps * u) % RS;
+      const uint32_t bar = full0 + 8 * s;
+      const uint32_t dst = smem_addr(smem + s * TL::kCodes);
+      const int z = pg * a.n_kv + hh;
+      mbar_arrive_expect_tx(bar, TL::kTx);
+      if constexpr (DT != PKV_KV_Q8_0) {
+        tma_load_3d(dst, &maps.k, 0, 0, z, bar, policy);
+        tma_load_3d(dst + 2048, &maps.k, 64, 0, z, bar, policy);
+        tma_load_3d(dst + TL::kData, &maps.v, 0, 0, z, bar, policy);
+        tma_load_3d(dst + TL::kData + 2048, &maps.v, 64, 0, z, bar, policy);
+      } else {
+        const uint32_t sdst = smem_addr(smem + SM::kScl + s * TL::kScales);
+        const size_t unit = static_cast<size_t>(z);
+        tma_load_3d(dst, &maps.k, 0, 0, z, bar, policy);
+        bulk_g2s(sdst, a.k_scales + unit * TL::kScale, TL::kScale, bar, policy);
+        tma_load_3d(dst + TL::kData, &maps.v, 0, 0, z, bar, policy);
+        bulk_g2s(sdst + TL::kScale, a.v_scales + unit * TL::kScale, TL::kScale, bar, policy);
+      }
+    }
+    ++issued;
+  };
+  while (issued < n_mine && warp + kWarps * issued < RS) issue();
+
+  bool aborted = false;
+  int consumed = 0;  // units [0, consumed) have landed (this warp waited for them)
+  auto fail = [&]() {
+    if (!aborted && lane == 0 && !ctl[0]) {
+      ctl[0] = 1;
+      record_status(a.status, PKV_DEV_TIMEOUT);
+    }
+    aborted = true;
+  };
+  MqState<DT, NT> S;
+
+  for (long long x = c_begin; x < c_end;) {
+    const int i = row_of(row_start, a.num_rows, a.n_kv, x);
+    const int npg = row_start[i + 1] - row_start[i];
+    const long long row_base = static_cast<long long>(a.n_kv) * row_start[i];
+    const int h = static_cast<int>((x - row_base) / npg);
+    const long long seg_start = row_base + static_cast<long long>(h) * npg;
+    const long long seg_end = seg_start + npg;
+    const long long b = min(seg_end, c_end);
+    const int L = lens[i];
+    const int p0 = window_start(L, plan_window) / kPage;
+    const long long j = static_cast<long long>(i) * a.n_kv + h;
+    const int k0 = chunk_of(seg_start, T, C), k1 = chunk_of(seg_end - 1, T, C);
+    const int P0 = L - a.q_len + a.q0;  // position of the pass's first query
+
+    // the lane's score columns cbase + 4t + tig: attended positions [col_lo, col_hi)
+    int col_lo[2] = {0, 0}, col_hi[2] = {0, 0};
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int c = 4 * t + tig;
+      if (c < ncw) {
+        const int P = P0 + (cbase + c) / G;
+        col_hi[t] = P + 1;
+        col_lo[t] = window_start(P + 1, a.window);
+      }
+    }
+    // slots any of the warp's columns attends, in any page
+    const int pos_lo = ncw > 0 ? window_start(P0 + cbase / G + 1, a.window) : 0;
+    const int pos_hi = ncw > 0 ? P0 + (cbase + ncw - 1) / G + 1 : 0;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      const int cq = 4 * t + (gid >> 1);  // the column whose query this lane loads
+      const float* qv = cq < ncw
+                            ? a.q + ((static_cast<long long>(i) * a.q_len + a.q0 + (cbase + cq) / G) *
+                                         a.n_q + h * G + (cbase + cq) % G) * kD
+                            : nullptr;
+      int e2;
+      mq_load_column<DT>(qv, a.qscale, (gid & 1) != 0, tig, S.qb[t], e2);
+      S.qexp[t] = ldexpf(1.0f, __shfl_sync(kFull, e2, 8 * tig));
+      S.m[t] = -INFINITY;
+      S.l[t] = 0.f;
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) S.o[r][e] = 0.f;
+    S.vx = kNoScale;
+
+    for (long long pos = x; pos < b; ++pos) {
+      const int v = static_cast<int>(pos - c_begin);
+      const int s = v % RS;
+      bool ok = !aborted && mbar_wait_bounded(full0 + 8 * s, (v / RS) & 1, ctl);
+      ok = __all_sync(kFull, ok);
+      if (!ok) {
+        fail();
+        continue;
+      }
+      consumed = v + 1;
+      if (ncw > 0) {
+        const int pf = (p0 + static_cast<int>(pos - seg_start)) * kPage;  // page's first token
+        const int slot_lo = max(0, pos_lo - pf), slot_hi = min(kPage, pos_hi - pf);
+        mq_process_unit<DT, NT>(smem + s * TL::kCodes, smem + SM::kScl + s * TL::kScales, pf,
+                                col_lo, col_hi, slot_lo, slot_hi, ncw, lane, S);
+      }
+      // done with the stage; its unit's copier refills it with unit v + RS
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      if ((v & (kWarps - 1)) == warp && v + RS < n_units) {
+        bool e_ok = mbar_wait_bounded(empty0 + 8 * s, (v / RS) & 1, ctl);
+        e_ok = __all_sync(kFull, e_ok);
+        if (!e_ok) {
+          fail();
+          continue;
+        }
+        issue();
+      }
+    }
+
+    // ---- piece end: this warp's columns are complete for the piece
+    if (!aborted && ncw > 0) {
+      float l_tot[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        float vsum = S.l[t];
+        vsum += __shfl_xor_sync(kFull, vsum, 4);
+        vsum += __shfl_xor_sync(kFull, vsum, 8);
+        vsum += __shfl_xor_sync(kFull, vsum, 16);
+        l_tot[t] = vsum;
+      }
+      // (m, l) of the lane's V-columns 2tig + e, from the score lanes
+      float mv[2], lv[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int cl = 2 * tig + e;
+        mv[e] = __shfl_sync(kFull, S.m[0], cl & 3);
+        lv[e] = __shfl_sync(kFull, l_tot[0], cl & 3);
+        if constexpr (NT == 2) {
+          const float m1 = __shfl_sync(kFull, S.m[1], cl & 3);
+          const float l1 = __shfl_sync(kFull, l_tot[1], cl & 3);
+          if (cl >= 4) {
+            mv[e] = m1;
+            lv[e] = l1;
+          }
+        }
+      }
+      const float osc = mq_o_scale<DT>(S.vx);
+      const bool whole = (k0 == k1);
+      auto out_col = [&](int c) {
+        return a.out + ((static_cast<long long>(i) * a.q_len + a.q0 + c / G) * a.n_q + h * G +
+                        c % G) * kD;
+      };
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int cl = 2 * tig + e;
+        if (cl >= ncw) continue;
+        if (whole) {
+          float* o = out_col(cbase + cl);
+          const float f = osc / lv[e];
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            o[mq_dim<DT>(r, 0, gid)] = S.o[r][e] * f;
+            o[mq_dim<DT>(r, 2, gid)] = S.o[r][e + 2] * f;
+          }
+        } else {
+          const long long slot = (k + j) * kMqCols + cbase + cl;
+          float* acc = a.part_acc + slot * kD;
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            acc[mq_dim<DT>(r, 0, gid)] = S.o[r][e] * osc;
+            acc[mq_dim<DT>(r, 2, gid)] = S.o[r][e + 2] * osc;
+          }
+          if (gid == 0) {
+            a.part_ml[slot * 2] = mv[e];
+            a.part_ml[slot * 2 + 1] = lv[e];
+          }
+        }
+      }
+      if (!whole && a.counters != nullptr) {
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          __threadfence();  // the warp's partial (ordered by __syncwarp) before its arrival
+          last = atomicAdd(a.counters + j * kWarps + warp, 1) == k1 - k0;
+        }
+        last = __shfl_sync(kFull, last, 0);
+        if (last) {
+          __threadfence();
+          mq_merge_segment_warp<CW, NT == 1 ? 2 : 1>(a.part_ml, a.part_acc, j, k0, k1, cbase, nc,
+                                                     out_col, lane);
+          if (lane == 0) a.counters[j * kWarps + warp] = 0;  // ready for the next call
+        }
+      }
+    }
+    x = b;
+  }
+
+  // Copies this warp issued that no wait saw land must land before the CTA exits.
+  if (aborted || ctl[0]) {
+    const int zero = 0;
+    for (int u = 0; u < issued; ++u) {
+      const int v = warp + kWarps * u;
+      if (v >= consumed) mbar_wait_bounded(full0 + 8 * (v % RS), (v / RS) & 1, &zero);
+    }
+  }
+}
+
 // ------------------------------------------------------------ launchers ----
-template <int DT, int G>
-static cudaError_t mq_ensure_smem(size_t smem) {
-  static std::atomic<size_t> granted[64];
+template <class K>
+static cudaError_t mq_ensure_smem(K kernel, std::atomic<size_t> (&granted)[64], size_t smem) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && granted[dev].load(std::memory_order_relaxed) >= smem)
     return cudaSuccess;
-  e = cudaFuncSetAttribute(paged_decode_mq_kernel<DT, G>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
   if (e == cudaSuccess && dev >= 0 && dev < 64) {
     size_t cur = granted[dev].load();
     while (cur < smem && !granted[dev].compare_exchange_weak(cur, smem)) {
@@ -795,11 +1197,31 @@ static cudaError_t mq_ensure_smem(size_t smem) {
   return e;
 }
 
-template <int DT, int G>
+// The kernel of (dtype, kind) and its dynamic shared memory for `rows` rows.
+template <int DT, int KIND>
+struct MqKernel {
+  static auto fn() {
+    if constexpr (KIND == kMqSingle)
+      return paged_decode_mq_kernel<DT>;
+    else
+      return paged_decode_mqt_kernel<DT, KIND == kMqTeam1 ? 1 : 2>;
+  }
+  static size_t smem(int rows) {
+    return KIND == kMqSingle ? MqSmem<DT>::bytes(rows)
+                             : MqtSmem<DT, team_stages(KIND == kMqTeam1 ? 1 : 2)>::bytes(rows);
+  }
+  static cudaError_t prepare(size_t smem) {
+    static std::atomic<size_t> granted[64];
+    return mq_ensure_smem(fn(), granted, smem);
+  }
+};
+
+template <int DT, int KIND>
 static cudaError_t launch_mq_t(const DecodeArgs& a, const TileMaps& maps, int chunks,
                                cudaStream_t st) {
-  const size_t smem = MqSmem<DT>::bytes(a.num_rows);
-  cudaError_t e = mq_ensure_smem<DT, G>(smem);
+  using K = MqKernel<DT, KIND>;
+  const size_t smem = K::smem(a.num_rows);
+  cudaError_t e = K::prepare(smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(chunks);
@@ -811,45 +1233,60 @@ static cudaError_t launch_mq_t(const DecodeArgs& a, const TileMaps& maps, int ch
   attr[0].val.programmaticStreamSerializationAllowed = PKV_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, paged_decode_mq_kernel<DT, G>, a, maps);
+  e = cudaLaunchKernelEx(&cfg, K::fn(), a, maps);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-template <int DT>
+template <int DT, int KIND>
 static cudaError_t mq_occupancy_t(int rows, int* blocks) {
-  const size_t smem = MqSmem<DT>::bytes(rows);
-  cudaError_t e = mq_ensure_smem<DT, 4>(smem);
+  using K = MqKernel<DT, KIND>;
+  const size_t smem = K::smem(rows);
+  cudaError_t e = K::prepare(smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, paged_decode_mq_kernel<DT, 4>,
-                                                       kThreads, smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, K::fn(), kThreads, smem);
+}
+
+template <int DT>
+static cudaError_t launch_mq_dt(int kind, const DecodeArgs& a, const TileMaps& maps, int chunks,
+                                cudaStream_t st) {
+  if constexpr (DT == PKV_KV_Q8_0) {
+    return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
+  } else {
+    if (kind == kMqSingle) return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
+    if constexpr (DT == PKV_KV_F16)
+      if (kind == kMqTeam2) return launch_mq_t<DT, kMqTeam2>(a, maps, chunks, st);
+    return launch_mq_t<DT, kMqTeam1>(a, maps, chunks, st);
+  }
+}
+
+template <int DT>
+static cudaError_t occupancy_mq_dt(int kind, int rows, int* blocks) {
+  if constexpr (DT == PKV_KV_Q8_0) {
+    return mq_occupancy_t<DT, kMqSingle>(rows, blocks);
+  } else {
+    if (kind == kMqSingle) return mq_occupancy_t<DT, kMqSingle>(rows, blocks);
+    if constexpr (DT == PKV_KV_F16)
+      if (kind == kMqTeam2) return mq_occupancy_t<DT, kMqTeam2>(rows, blocks);
+    return mq_occupancy_t<DT, kMqTeam1>(rows, blocks);
+  }
 }
 
 cudaError_t launch_paged_decode_mq(int dtype, int group, const DecodeArgs& a, const TileMaps& maps,
                                    int chunks, cudaStream_t st) {
-#define PKV_MQ(D, G_)                                   \
-  if (group == (G_)) return launch_mq_t<D, G_>(a, maps, chunks, st)
-  if (dtype == PKV_KV_F16) {
-    PKV_MQ(PKV_KV_F16, 1);
-    PKV_MQ(PKV_KV_F16, 2);
-    PKV_MQ(PKV_KV_F16, 4);
-  } else if (dtype == PKV_KV_BF16) {
-    PKV_MQ(PKV_KV_BF16, 1);
-    PKV_MQ(PKV_KV_BF16, 2);
-    PKV_MQ(PKV_KV_BF16, 4);
-  } else {
-    PKV_MQ(PKV_KV_Q8_0, 1);
-    PKV_MQ(PKV_KV_Q8_0, 2);
-    PKV_MQ(PKV_KV_Q8_0, 4);
-  }
-#undef PKV_MQ
-  return cudaErrorInvalidValue;
+  if (group != 1 && group != 2 && group != 4) return cudaErrorInvalidValue;
+  const int kind = mq_kind(dtype, group, a.q_len);
+  if (dtype == PKV_KV_F16) return launch_mq_dt<PKV_KV_F16>(kind, a, maps, chunks, st);
+  if (dtype == PKV_KV_BF16) return launch_mq_dt<PKV_KV_BF16>(kind, a, maps, chunks, st);
+  return launch_mq_dt<PKV_KV_Q8_0>(kind, a, maps, chunks, st);
 }
 
-cudaError_t paged_decode_mq_blocks_per_sm(int dtype, int rows, int* blocks) {
-  if (dtype == PKV_KV_F16) return mq_occupancy_t<PKV_KV_F16>(rows, blocks);
-  if (dtype == PKV_KV_BF16) return mq_occupancy_t<PKV_KV_BF16>(rows, blocks);
-  return mq_occupancy_t<PKV_KV_Q8_0>(rows, blocks);
+cudaError_t paged_decode_mq_blocks_per_sm(int dtype, int group, int q_len, int rows,
+                                          int* blocks) {
+  const int kind = mq_kind(dtype, group, q_len);
+  if (dtype == PKV_KV_F16) return occupancy_mq_dt<PKV_KV_F16>(kind, rows, blocks);
+  if (dtype == PKV_KV_BF16) return occupancy_mq_dt<PKV_KV_BF16>(kind, rows, blocks);
+  return occupancy_mq_dt<PKV_KV_Q8_0>(kind, rows, blocks);
 }
 
 }  // namespace pkv

@@ -109,13 +109,15 @@ cudaError_t encode_tile_maps(int dtype, void* k_data, void* v_data, long long ti
 cudaError_t launch_paged_decode(int dtype, int group, const DecodeArgs& a, const TileMaps& maps,
                                 int chunks, cudaStream_t stream);
 cudaError_t paged_decode_blocks_per_sm(int dtype, int group, int rows, int* blocks);
-// The several-query kernel: one pass of up to mq_pass_queries(dtype, group)
-// queries (a.q0, a.nq) over the same plan.
-int mq_pass_queries(int dtype, int group);
+// The several-query kernels: one pass of up to mq_pass_queries(dtype, group,
+// q_len) queries (a.q0, a.nq) over the same plan; the kernel is chosen by
+// q_len * group (the same for every pass of a call).
+int mq_pass_queries(int dtype, int group, int q_len);
 cudaError_t launch_paged_decode_mq(int dtype, int group, const DecodeArgs& a, const TileMaps& maps,
                                    int chunks, cudaStream_t stream);
-cudaError_t paged_decode_mq_blocks_per_sm(int dtype, int rows, int* blocks);
-constexpr int kMqCols = 8;  // partial-state columns of a several-query workspace slot
+cudaError_t paged_decode_mq_blocks_per_sm(int dtype, int group, int q_len, int rows, int* blocks);
+constexpr int kMqCols = 32;  // partial-state columns of a several-query workspace slot
+constexpr int kMqCounters = 4;  // arrival counters per (row, KV head): one per warp's columns
 cudaError_t launch_combine(int group, const CombineArgs& a, cudaStream_t stream);
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
 cudaError_t launch_append(int dtype, const AppendArgs& a, cudaStream_t stream);

@@ -111,9 +111,10 @@ def test_mq_window_matches_oracle_and_skips_earlier_pages(dtype, q_len, window):
 
 
 @pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16])
-def test_mq_split_invariance(dtype):
+@pytest.mark.parametrize("q_len", [2, 3, 6])  # G = 4: 8, 12 and 24 columns (each kernel)
+def test_mq_split_invariance(dtype, q_len):
     wl = _wl(dtype, n_q=32, n_kv=8)
-    q, _, _ = W.mq_inputs(wl, 6, seed=2)
+    q, _, _ = W.mq_inputs(wl, q_len, seed=2)
     host = encode_pool(wl)
     pool = device_pool(wl, host)
     ref = _oracle(wl, host, q)
