@@ -186,6 +186,7 @@ def step_bytes(wl, window=0, q_len=1) -> int:
 KERNEL_SOURCES = {  # the files each decode kernel is compiled from (besides headers of the ABI)
     "paged_decode_kernel": ("decode.cu", "decode_common.cuh", "pkv_device.cuh"),
     "paged_decode_mq_kernel": ("decode_mq.cu", "decode_common.cuh", "pkv_device.cuh"),
+    "paged_decode_mqt_kernel": ("decode_mq.cu", "decode_common.cuh", "pkv_device.cuh"),
 }
 
 
@@ -261,13 +262,16 @@ def run_ours(args, rank, world, local):
         cols = QL * cfg.group  # (query, head) columns; the kernel's pass width follows them
         if cfg.dtype == W.Q8_0 or cols <= (4 if cfg.dtype == W.BF16 else 8):
             width = min(cols, 8)
+            kname = "paged_decode_mq_kernel"  # the warps of a CTA read different pages
         else:
             width = 16 if cfg.dtype == W.BF16 or cols <= 16 else 32
+            kname = "paged_decode_mqt_kernel"  # the four warps share every page
         passes = -(-QL // max(1, width // cfg.group))
     else:
         q, k_new, v_new = t(wl.q), t(wl.k_new), t(wl.v_new)
         ws = api.Workspace(pool, cfg.n_q_heads, wl.rows, args.chunks)
         passes = 1
+        kname = "paged_decode_kernel"
     bt, sl = t(wl.block_table), t(wl.seq_lens)
     out = torch.empty_like(q)
     L = api.lib()
@@ -351,7 +355,6 @@ def run_ours(args, rank, world, local):
     value = world * nbytes / step_s / 1e9
     achieved = nbytes / (launch_ms / 1e3) / 1e9
     tokens = attended_tokens(wl, args.window, QL)
-    kname = "paged_decode_mq_kernel" if QL > 1 else "paged_decode_kernel"
     result = {
         "metric": "paged decode-attn KV GB/s & % of GB300 HBM peak; rows*tokens/s at 1 GPU",
         "value": round(value, 2),
@@ -380,7 +383,7 @@ def run_ours(args, rank, world, local):
         "rows_tokens_per_s": round(world * tokens / step_s, 1),
         "rows_per_s": round(world * wl.rows / step_s, 1),
         "roofline": {
-            "bound": "hbm", "kernel": f"{kname}<{W.DTYPE_NAMES[cfg.dtype]}, G={cfg.group}>",
+            "bound": "hbm", "kernel": f"{kname}<{W.DTYPE_NAMES[cfg.dtype]}>, G={cfg.group}",
             "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (copy bandwidth)",
             # DRAM bytes of one launch (one pass: a step of the several-query
