@@ -161,6 +161,11 @@ def read_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def bytes_per_value(dtype: int) -> float:
+    """Stored bytes per K or V value: q8_0 34 per 32, f32 4, f16 and bf16 2."""
+    return 34.0 / 32.0 if dtype == 1 else 4.0 if dtype == 3 else 2.0
+
+
 def row_tokens(L: int, window=0, q_len=1) -> int:
     """Tokens a row of L tokens needs in one call: all L, or with a window W the
     union of its q_len queries' windows, the last min(L, W + q_len - 1)."""
@@ -174,10 +179,9 @@ def attended_tokens(wl, window=0, q_len=1) -> int:
 
 def step_bytes(wl, window=0, q_len=1) -> int:
     """Algorithmic bytes of one decode call: K and V of every needed token read
-    once (f16, bf16: 2 bytes per element; q8_0: 34 bytes per 32 elements),
-    q and out (fp32, q_len queries per row)."""
+    once (bytes_per_value per element), q and out (fp32, q_len queries per row)."""
     cfg = wl.cfg
-    per_elem = 34.0 / 32.0 if cfg.dtype == 1 else 2.0  # q8_0; f16 and bf16
+    per_elem = bytes_per_value(cfg.dtype)
     kv = attended_tokens(wl, window, q_len) * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem
     qo = 2 * wl.rows * q_len * cfg.n_q_heads * cfg.head_dim * 4
     return int(kv + qo)
@@ -286,13 +290,13 @@ def run_ours(args, rank, world, local):
         if st:
             raise api.PkvError(st, what, L.pkv_last_error_message().decode())
 
-    def step(layer):
+    def step(layer, on=sp):
         if QL > 1:
             chk(L.pkv_decode_step_mq(H, layer, a_q, a_k, a_v, a_bt, S, a_sl, R, QL, NQ, scale,
-                                     a_out, a_ws, ws.nbytes, CH, sp), "pkv_decode_step_mq")
+                                     a_out, a_ws, ws.nbytes, CH, on), "pkv_decode_step_mq")
         else:
             chk(L.pkv_decode_step(H, layer, a_q, a_k, a_v, a_bt, S, a_sl, R, NQ, scale, a_out,
-                                  a_ws, ws.nbytes, CH, sp), "pkv_decode_step")
+                                  a_ws, ws.nbytes, CH, on), "pkv_decode_step")
 
     for w in range(args.warmup):
         step(w % layers)
@@ -321,6 +325,8 @@ def run_ours(args, rank, world, local):
     # launches of it; the roofline takes the step (all passes) as the unit
     launch_ms = total_ms / K
     assert pool.read_status() == 0, "device status word set during the timed steps"
+
+    graph = graph_timing(torch, dev, step, layers)
 
     # ---- end to end through the C ABI: pinned host inputs in, output out
     hq, hk, hv = (x.cpu().pin_memory() for x in (q, k_new, v_new))
@@ -396,12 +402,44 @@ def run_ours(args, rank, world, local):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
                 "ms_per_step": round(e2e_ms / Ke, 6)},
         "gpu_launches": K * passes,
+        "graph": graph,
         "clocks": clock_info,
     }
     if rank == 0 and not args.no_cpu_baseline:
         result["cpu_baseline"] = cpu_baseline(wl, pool, args.cpu_seconds, args.window, QL,
                                               q.cpu().numpy())
     return result
+
+
+def graph_timing(torch, dev, step, layers, calls=20, replays=50):
+    """Steps captured as a CUDA graph of `calls` calls (rotating the layer
+    pools as the timed loop does), replayed `replays` times with events
+    around each replay: per-call median, p10 and p90 in microseconds."""
+    import numpy as np
+    try:
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        with torch.cuda.graph(g, stream=cap):
+            on = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+            for c in range(calls):
+                step(c % layers, on)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(replays)]
+        for e0, e1 in ev:
+            e0.record()
+            g.replay()
+            e1.record()
+        torch.cuda.synchronize()
+        per_call = np.array([e0.elapsed_time(e1) * 1e3 / calls for e0, e1 in ev])
+        return {"calls_per_graph": calls, "replays": replays,
+                "median_us_per_call": round(float(np.median(per_call)), 3),
+                "p10_us_per_call": round(float(np.percentile(per_call, 10)), 3),
+                "p90_us_per_call": round(float(np.percentile(per_call, 90)), 3)}
+    except Exception as exc:  # reported, not fatal: the event-timed loop is the measurement
+        return {"error": f"{type(exc).__name__}: {str(exc)[:160]}"}
 
 
 def run_alloc(args):
@@ -494,7 +532,10 @@ def cpu_baseline(wl, pool, budget_s, window=0, q_len=1, q=None):
 
     import oracle as O
     cfg = wl.cfg
-    if cfg.dtype != 1:  # 16-bit patterns (f16, bf16)
+    if cfg.dtype == 3:  # f32 values
+        kd, vd = pool.k_data[0].cpu().numpy(), pool.v_data[0].cpu().numpy()
+        ks = vs = None
+    elif cfg.dtype != 1:  # 16-bit patterns (f16, bf16)
         kd = pool.k_data[0].cpu().view(torch.int16).numpy().view(np.uint16)
         vd = pool.v_data[0].cpu().view(torch.int16).numpy().view(np.uint16)
         ks = vs = None
@@ -519,7 +560,7 @@ def cpu_baseline(wl, pool, budget_s, window=0, q_len=1, q=None):
         done += row_tokens(int(wl.seq_lens[i]), window, q_len)
         if secs > budget_s:
             break
-    per_elem = 34.0 / 32.0 if cfg.dtype == 1 else 2.0  # q8_0; f16 and bf16
+    per_elem = bytes_per_value(cfg.dtype)
     nbytes = done * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem + \
         2 * len(rows) * q_len * cfg.n_q_heads * 128 * 4
     return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": O.num_threads(),
@@ -562,7 +603,7 @@ def run_reference(args):
                            wl.seq_lens[i:i + 1], wl.num_pages, cfg.n_kv_heads, wl.scale,
                            window=args.window)
 
-    per_elem = 34.0 / 32.0 if cfg.dtype == 1 else 2.0  # q8_0; f16 and bf16
+    per_elem = bytes_per_value(cfg.dtype)
 
     def tokens_of(i):
         return row_tokens(int(wl.seq_lens[i]), args.window, QL)

@@ -30,6 +30,8 @@
  *   - Pool, per layer, per K and per V (layer l starts at l times the
  *     per-layer size):
  *       f16 : data   [num_pages][n_kv_heads][16][head_dim]  binary16
+ *       bf16: data   [num_pages][n_kv_heads][16][head_dim]  bfloat16
+ *       f32 : data   [num_pages][n_kv_heads][16][head_dim]  binary32
  *       q8_0: data   [num_pages][n_kv_heads][16][head_dim]  int8 codes
  *             scales [num_pages][n_kv_heads][16][head_dim/32] binary16
  *     q8_0 value = scale of the element's 32-wide block (along head_dim)
@@ -86,12 +88,15 @@ typedef enum pkv_status {
 #define PKV_DEV_TIMEOUT 4u    /* a bounded wait on a shared-memory barrier gave up */
 
 /* Stored KV formats: binary16; q8_0 (int8 codes + one binary16 scale per 32
- * values along head_dim); bfloat16 (tinyllm, "The repository currently
- * provides": BF16/F32 KV caching), rounded to nearest even. */
+ * values along head_dim); bfloat16, rounded to nearest even, and binary32,
+ * stored as given (tinyllm, "The repository currently provides": BF16/F32 KV
+ * caching).  Data arrays hold 2 bytes per value (f16, bf16), 4 (f32) or 1
+ * (q8_0 codes). */
 typedef enum pkv_kv_dtype {
     PKV_KV_F16 = 0,
     PKV_KV_Q8_0 = 1,
     PKV_KV_BF16 = 2,
+    PKV_KV_F32 = 3,
 } pkv_kv_dtype;
 
 typedef struct pkv_pool pkv_pool;
@@ -106,7 +111,7 @@ size_t kv_pool_bytes(int num_layers, int num_pages, int n_kv_heads, int head_dim
  * provides": one runner-owned physical KV page pool).
  *   k_data, v_data     device arrays of kv_pool_bytes(..., 0) bytes, 16-byte aligned
  *   k_scales, v_scales q8_0: device arrays of kv_pool_bytes(..., 1) bytes,
- *                      16-byte aligned; f16: must be NULL
+ *                      16-byte aligned; f16, bf16, f32: must be NULL
  *   device_status      optional device int32 (NULL: none), zero before first
  *                      use; kernels OR PKV_DEV_* bits into it.
  * num_pages * n_kv_heads must be below 2^31 (PKV_ERR_UNSUPPORTED).  Creating
@@ -263,7 +268,8 @@ pkv_status pkv_decode_step(const pkv_pool *pool, int layer, const float *q, cons
  *   k_new, v_new  fp32 [num_rows][q_len][n_kv_heads][128] (pkv_decode_step_mq):
  *                 token j of row i is stored at position L - q_len + j
  * Rows with L == 0 get zeros; rows with 0 < L < q_len get zeros and set
- * PKV_DEV_BAD_LENGTH.  A row reads the pages holding [L - q_len + 1 - W, L)
+ * PKV_DEV_BAD_LENGTH.  f32 pools are not supported here (PKV_ERR_UNSUPPORTED).
+ * A row reads the pages holding [L - q_len + 1 - W, L)
  * (all of [0, L) without a window), split into chunks as in
  * paged_decode_attention.  Every page is read once per pass; a pass carries
  * the (query, query head) pairs of a KV head, C = q_len * G in all:

@@ -11,8 +11,8 @@ evaluates; the C source cites the pages it follows:
 * Leone, "What ships"; LeatEngine, "Run": f16 and q8_0 KV storage.
 
 Pool layout per layer (a reading; the pages fix none): data
-``[num_pages][n_kv][16][D]`` (f16 bits as uint16, or int8 codes), q8_0 scales
-``[num_pages][n_kv][16][D/32]`` (f16 bits as uint16).
+``[num_pages][n_kv][16][D]`` (f16 or bf16 bits as uint16, float32, or int8
+codes), q8_0 scales ``[num_pages][n_kv][16][D/32]`` (f16 bits as uint16).
 """
 from __future__ import annotations
 
@@ -24,7 +24,7 @@ import numpy as np
 
 from . import build as _build
 
-F16, Q8_0, BF16 = 0, 1, 2
+F16, Q8_0, BF16, F32 = 0, 1, 2, 3
 PAGE = 16
 QBLOCK = 32
 
@@ -170,12 +170,14 @@ def q8_0_encode(x: np.ndarray):
 def encode_pool(dtype: int, values: np.ndarray):
     """Store fp32 values [pages][n_kv][16][D] in the pool dtype: (data, scales).
 
-    f16 / bf16: data uint16 bits, scales None.  q8_0: data int8 codes, scales
-    uint16 [pages][n_kv][16][D/32]."""
+    f16 / bf16: data uint16 bits, scales None.  f32: the fp32 values as given,
+    scales None.  q8_0: data int8 codes, scales uint16 [pages][n_kv][16][D/32]."""
     if dtype == F16:
         return f16_encode(values), None
     if dtype == BF16:
         return bf16_encode(values), None
+    if dtype == F32:
+        return np.array(values, dtype=np.float32, copy=True), None
     return q8_0_encode(values)
 
 

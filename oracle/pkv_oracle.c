@@ -11,7 +11,7 @@
  *   - The KV page pool and block table: tinyllm, "The repository currently
  *     provides" (a runner-owned physical KV page pool with a logical block
  *     table per active sequence) and "Known limitations" (16-token pages).
- *   - KV storage as f16 and q8/q8_0: Leone, "What ships" (f32, f16 and q8 KV
+ *   - KV storage as f16, bf16, f32 and q8/q8_0: Leone, "What ships" (f32, f16 and q8 KV
  *     storage); tinyllm, "The repository currently provides" (BF16/F32 KV
  *     caching); LeatEngine, "Run" (--cache-type q8_0 keeps the KV cache the
  *     way llama.cpp's q8_0 cache does, in about half the memory of f16).
@@ -68,7 +68,7 @@
 #define ORACLE_PAGE 16 /* tokens per physical page (tinyllm, Known limitations) */
 #define ORACLE_QBLOCK 32 /* q8_0 block length along head_dim */
 
-enum { ORACLE_F16 = 0, ORACLE_Q8_0 = 1, ORACLE_BF16 = 2 };
+enum { ORACLE_F16 = 0, ORACLE_Q8_0 = 1, ORACLE_BF16 = 2, ORACLE_F32 = 3 };
 enum { ORACLE_OK = 0, ORACLE_BAD_ARG = 1, ORACLE_BAD_PAGE = 2 };
 
 int oracle_num_threads(void) {
@@ -234,16 +234,18 @@ void oracle_f16_encode(const float *x, int64_t n, uint16_t *out) {
 /* ------------------------------------------------------------ the pool --- */
 
 /* Stored value of element d of slot `slot` of (page, kv_head), widened to
- * double.  f16 / bf16: the binary16 / bfloat16 value.  q8_0: f16 scale of
- * the element's block times its int8 code.  Layout per layer (a reading; the
- * pages fix none):
- *   data   [num_pages][n_kv][16][D]        (f16 or bf16 bits, or int8 codes)
+ * double.  f16 / bf16: the binary16 / bfloat16 value.  f32: the binary32
+ * value (stored as given, no rounding).  q8_0: f16 scale of the element's
+ * block times its int8 code.  Layout per layer (a reading; the pages fix
+ * none):
+ *   data   [num_pages][n_kv][16][D]        (f16 or bf16 bits, binary32, or int8 codes)
  *   scales [num_pages][n_kv][16][D / 32]   (f16 bits; q8_0 only)           */
 static double stored(int dtype, const void *data, const uint16_t *scales, int n_kv,
                      int D, int64_t page, int kvh, int slot, int d) {
     int64_t row = (page * n_kv + kvh) * ORACLE_PAGE + slot;
     if (dtype == ORACLE_F16) return oracle_f16_to_f64(((const uint16_t *)data)[row * D + d]);
     if (dtype == ORACLE_BF16) return oracle_bf16_to_f64(((const uint16_t *)data)[row * D + d]);
+    if (dtype == ORACLE_F32) return (double)((const float *)data)[row * D + d];
     double sc = oracle_f16_to_f64(scales[row * (D / ORACLE_QBLOCK) + d / ORACLE_QBLOCK]);
     return sc * (double)((const int8_t *)data)[row * D + d];
 }
@@ -271,6 +273,9 @@ static int store_token(int dtype, int n_kv, int D, const float *kx, const float 
     } else if (dtype == ORACLE_BF16) {
         oracle_bf16_encode(kx, D, (uint16_t *)k_data + row * D);
         oracle_bf16_encode(vx, D, (uint16_t *)v_data + row * D);
+    } else if (dtype == ORACLE_F32) {  /* stored as given */
+        memcpy((float *)k_data + row * D, kx, (size_t)D * sizeof(float));
+        memcpy((float *)v_data + row * D, vx, (size_t)D * sizeof(float));
     } else {
         oracle_q8_0_encode(kx, D, (int8_t *)k_data + row * D, k_scales + row * (D / ORACLE_QBLOCK));
         oracle_q8_0_encode(vx, D, (int8_t *)v_data + row * D, v_scales + row * (D / ORACLE_QBLOCK));
@@ -328,6 +333,9 @@ int oracle_kv_append(int dtype, int num_rows, int n_kv, int D, const float *k_ne
             } else if (dtype == ORACLE_BF16) {
                 oracle_bf16_encode(kx, D, (uint16_t *)k_data + row * D);
                 oracle_bf16_encode(vx, D, (uint16_t *)v_data + row * D);
+            } else if (dtype == ORACLE_F32) {  /* the fp32 values, unrounded */
+                memcpy((float *)k_data + row * D, kx, (size_t)D * sizeof(float));
+                memcpy((float *)v_data + row * D, vx, (size_t)D * sizeof(float));
             } else {
                 oracle_q8_0_encode(kx, D, (int8_t *)k_data + row * D,
                                    k_scales + row * (D / ORACLE_QBLOCK));

@@ -62,7 +62,7 @@ cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
 size_t data_bytes_per_layer(int num_pages, int n_kv, int head_dim, pkv_kv_dtype dtype) {
   const size_t elems = static_cast<size_t>(num_pages) * n_kv * PKV_PAGE_TOKENS * head_dim;
-  return dtype == PKV_KV_Q8_0 ? elems : elems * 2;  // f16, bf16: 2 bytes
+  return dtype == PKV_KV_Q8_0 ? elems : dtype == PKV_KV_F32 ? elems * 4 : elems * 2;  // f16, bf16: 2
 }
 
 size_t scale_bytes_per_layer(int num_pages, int n_kv, int head_dim, pkv_kv_dtype dtype) {
@@ -251,6 +251,8 @@ pkv_status attention_mq_impl(const pkv_pool* pool, int layer, const float* q, co
   if ((s = check_rows(num_rows, bt_stride, block_table, seq_lens))) return s;
   if (q_len < 1 || q_len > PKV_MAX_Q_LEN)
     return fail(PKV_ERR_UNSUPPORTED, "q_len %d outside [1, %d]", q_len, PKV_MAX_Q_LEN);
+  if (pool->dtype == PKV_KV_F32)
+    return fail(PKV_ERR_UNSUPPORTED, "several queries per row on an f32 pool");
   if (num_rows > 0 && (!q || !out)) return fail(PKV_ERR_INVALID_ARG, "null q or out");
   if (!aligned(q, 16) || !aligned(out, 16))
     return fail(PKV_ERR_INVALID_ARG, "q / out not 16-byte aligned");
@@ -316,7 +318,8 @@ size_t kv_pool_bytes(int num_layers, int num_pages, int n_kv_heads, int head_dim
                      pkv_kv_dtype dtype, int which) {
   if (num_layers <= 0 || num_pages <= 0 || n_kv_heads <= 0 || head_dim <= 0 ||
       head_dim % PKV_Q8_BLOCK ||
-      (dtype != PKV_KV_F16 && dtype != PKV_KV_Q8_0 && dtype != PKV_KV_BF16))
+      (dtype != PKV_KV_F16 && dtype != PKV_KV_Q8_0 && dtype != PKV_KV_BF16 &&
+       dtype != PKV_KV_F32))
     return 0;
   const size_t per = which == 0 ? data_bytes_per_layer(num_pages, n_kv_heads, head_dim, dtype)
                                 : scale_bytes_per_layer(num_pages, n_kv_heads, head_dim, dtype);
@@ -330,7 +333,8 @@ pkv_status kv_pool_create(pkv_pool** out, int num_layers, int num_pages, int n_k
   *out = nullptr;
   if (num_layers <= 0 || num_pages <= 0 || n_kv_heads <= 0)
     return fail(PKV_ERR_INVALID_ARG, "pool sizes must be positive");
-  if (dtype != PKV_KV_F16 && dtype != PKV_KV_Q8_0 && dtype != PKV_KV_BF16)
+  if (dtype != PKV_KV_F16 && dtype != PKV_KV_Q8_0 && dtype != PKV_KV_BF16 &&
+      dtype != PKV_KV_F32)
     return fail(PKV_ERR_INVALID_ARG, "unknown KV dtype %d", static_cast<int>(dtype));
   if (head_dim != PKV_HEAD_DIM) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d != 128", head_dim);
   if (!k_data || !v_data) return fail(PKV_ERR_INVALID_ARG, "null K or V data");
@@ -341,7 +345,7 @@ pkv_status kv_pool_create(pkv_pool** out, int num_layers, int num_pages, int n_k
     if (!aligned(k_scales, 16) || !aligned(v_scales, 16))
       return fail(PKV_ERR_INVALID_ARG, "scale arrays not 16-byte aligned");
   } else if (k_scales || v_scales) {
-    return fail(PKV_ERR_INVALID_ARG, "f16 and bf16 pools take no scale arrays");
+    return fail(PKV_ERR_INVALID_ARG, "f16, bf16 and f32 pools take no scale arrays");
   }
   if (device_status && !aligned(device_status, 4))
     return fail(PKV_ERR_INVALID_ARG, "status word not 4-byte aligned");
@@ -562,6 +566,8 @@ pkv_status paged_decode_default_chunks_mq(const pkv_pool* pool, int n_q_heads, i
     return fail(PKV_ERR_UNSUPPORTED, "max_rows %d outside [1, %d]", max_rows, PKV_MAX_ROWS);
   if (q_len < 1 || q_len > PKV_MAX_Q_LEN)
     return fail(PKV_ERR_UNSUPPORTED, "q_len %d outside [1, %d]", q_len, PKV_MAX_Q_LEN);
+  if (pool->dtype == PKV_KV_F32)
+    return fail(PKV_ERR_UNSUPPORTED, "several queries per row on an f32 pool");
   return default_chunks_mq(pool, n_q_heads / pool->n_kv, q_len, max_rows, chunks);
 }
 

@@ -8,6 +8,7 @@
 // thread per dim; K and V in turn.
 //   f16 : binary16 rounded to nearest even.
 //   bf16: bfloat16 rounded to nearest even.
+//   f32 : the fp32 value itself.
 //   q8_0: each warp holds one 32-wide block: amax by warp reduction,
 //         d = amax / 127 (IEEE division), codes round(x / d) with ties away
 //         from zero (roundf), stored scale binary16(d); amax = 0 gives zeros.
@@ -43,6 +44,8 @@ __global__ void __launch_bounds__(kD) append_kernel(const AppendArgs a) {
       reinterpret_cast<__half*>(data)[slot_row * kD + d] = __float2half_rn(x);
     } else if constexpr (DT == PKV_KV_BF16) {
       reinterpret_cast<__nv_bfloat16*>(data)[slot_row * kD + d] = __float2bfloat16_rn(x);
+    } else if constexpr (DT == PKV_KV_F32) {
+      reinterpret_cast<float*>(data)[slot_row * kD + d] = x;
     } else {
       float amax = fabsf(x);
 #pragma unroll
@@ -67,6 +70,8 @@ cudaError_t launch_append(int dtype, const AppendArgs& a, cudaStream_t st) {
     append_kernel<PKV_KV_F16><<<grid, kD, 0, st>>>(a);
   else if (dtype == PKV_KV_BF16)
     append_kernel<PKV_KV_BF16><<<grid, kD, 0, st>>>(a);
+  else if (dtype == PKV_KV_F32)
+    append_kernel<PKV_KV_F32><<<grid, kD, 0, st>>>(a);
   else
     append_kernel<PKV_KV_Q8_0><<<grid, kD, 0, st>>>(a);
   return cudaGetLastError();

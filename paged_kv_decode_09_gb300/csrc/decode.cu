@@ -68,9 +68,13 @@
 
 namespace pkv {
 
+// f32 KV keeps each warp's scaled queries in shared memory, one head every
+// kQStride floats (the 16-byte pad puts the heads' chunks in different banks).
+constexpr int kQStride = kD + 4;
+
 // Offsets from a 1024-byte aligned base.  The tiles come first (the swizzle
-// atom is 1024 bytes), then scales, barriers, the merge buffer, control
-// words and the plan.
+// atom is 1024 bytes), then scales, barriers, the merge buffer, (f32 KV) the
+// queries, control words and the plan.
 template <int DT, int G>
 struct Smem {
   static constexpr int kStages = kWarps * Tiles<DT>::kRing;
@@ -79,34 +83,38 @@ struct Smem {
   static constexpr uint32_t kBar = kScl + kStages * Tiles<DT>::kScales;   // full[warp][ring]
   static constexpr uint32_t kMrgAcc = kBar + ((kStages * 8 + 15) / 16) * 16;  // f32 [warps][G][D]
   static constexpr uint32_t kMrgMl = kMrgAcc + kWarps * G * kD * 4;        // f32 [warps][G][2]
-  static constexpr uint32_t kCtl = kMrgMl + kWarps * G * 2 * 4;            // int [4]
+  static constexpr uint32_t kQ = kMrgMl + kWarps * G * 2 * 4;  // f32 KV: [warps][G][kQStride] q
+  static constexpr uint32_t kCtl =
+      kQ + (DT == PKV_KV_F32 ? kWarps * G * kQStride * 4 : 0);             // int [4]
   static constexpr uint32_t kRows = kCtl + 16;  // int row_start[rows + 1], lens[rows]
   static size_t bytes(int rows) {
     return kAlign + kRows + (2 * static_cast<size_t>(rows) + 1) * 4;  // kAlign: base alignment slack
   }
   static_assert(Tiles<DT>::kCodes % 1024 == 0, "tile stages keep the swizzle atom alignment");
-  static_assert(kMrgAcc % 16 == 0 && kMrgMl % 16 == 0 && kCtl % 16 == 0,
+  static_assert(kMrgAcc % 16 == 0 && kMrgMl % 16 == 0 && kQ % 16 == 0 && kCtl % 16 == 0,
                 "vector accesses need 16-byte aligned regions");
 };
 
 // Per-warp online softmax state for one piece.
 template <int DT>
 struct WarpState {
-  static constexpr int kSteps = DT == PKV_KV_BF16 ? 16 : 8;  // score k-steps (tf32: 8 dims)
+  // score k-steps (tf32: 8 dims; f32 KV: none, the products run on CUDA cores)
+  static constexpr int kSteps = DT == PKV_KV_BF16 ? 16 : DT == PKV_KV_F32 ? 1 : 8;
   uint32_t qb[kSteps][2];  // B operand of the scores per k-step: column gid (head gid/2, part gid%2)
   float qexp;         // 2^e of head tig: undoes its power-of-two normalisation
   float m;            // running max (base 2) of head tig, equal on its 8 lanes
   float l;            // this lane's share of head tig's sum of probabilities
   float o[8][4];      // O^T accumulators: dims (see dim_of) x columns (tig, hi), (tig, lo)
   int vx;             // q8_0: every V block scale of the piece so far is below 2^vx
+  float* qs;          // f32 KV: the warp's scaled queries [G][kQStride] in shared memory
 };
 
 template <int DT>
 __device__ __forceinline__ float o_scale(const WarpState<DT>& S) {
   if constexpr (DT == PKV_KV_F16)
     return 1.0f / (1 << kPShift);
-  else if constexpr (DT == PKV_KV_BF16)
-    return 1.0f;  // tf32 parts have the fp32 exponent range: no scaling
+  else if constexpr (DT == PKV_KV_BF16 || DT == PKV_KV_F32)
+    return 1.0f;  // tf32 parts have the fp32 exponent range; f32 products are plain fp32
   else
     return pow2i(S.vx - kPShift);
 }
@@ -115,7 +123,9 @@ __device__ __forceinline__ float o_scale(const WarpState<DT>& S) {
 // 4 gid + tig.
 template <int DT>
 __device__ __forceinline__ int dim_of(int r, int e, int gid) {
-  if constexpr (DT != PKV_KV_Q8_0)
+  if constexpr (DT == PKV_KV_F32)  // dims 32j + 4gid + {0,1,2,3}: o[2j][0, 2], o[2j+1][0, 2]
+    return 32 * (r >> 1) + 4 * gid + 2 * (r & 1) + (e ? 1 : 0);
+  else if constexpr (DT != PKV_KV_Q8_0)
     return 16 * r + gid + (e ? 8 : 0);
   else
     return 16 * r + 2 * gid + (e ? 1 : 0);
@@ -131,7 +141,19 @@ __device__ __forceinline__ void load_query(const float* qrow, float qscale, int 
                                            WarpState<DT>& S) {
   const int gid = lane >> 2, tig = lane & 3, g2 = gid >> 1;
   const bool lo = (gid & 1) != 0;
-  if constexpr (DT == PKV_KV_BF16) {
+  if constexpr (DT == PKV_KV_F32) {
+    // the G heads' q times scale * log2 e into the warp's buffer: lane l
+    // writes dims 4l .. 4l + 3 of every head
+    __syncwarp();  // the previous piece's reads are done
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(qrow + g * kD) + lane);
+      *reinterpret_cast<float4*>(S.qs + g * kQStride + 4 * lane) =
+          make_float4(x.x * qscale, x.y * qscale, x.z * qscale, x.w * qscale);
+    }
+    __syncwarp();
+    S.qexp = 1.0f;
+  } else if constexpr (DT == PKV_KV_BF16) {
     // tf32 k-steps of 8 dims: k = tig <- dim 8ks + 2tig, k = tig + 4 <- dim 8ks + 2tig + 1
 #pragma unroll
     for (int ks = 0; ks < 16; ++ks) {
@@ -209,7 +231,25 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
 
   // ---- scores
   float s0, s1;
-  if constexpr (DT == PKV_KV_BF16) {
+  if constexpr (DT == PKV_KV_F32) {
+    // CUDA cores, fp32: lane 4 gid + tig takes head tig (head 0 stands in for
+    // heads >= G, whose results are never used) and tokens gid, gid + 8;
+    // four partial sums per token shorten the FMA chains
+    const float* qh = S.qs + (tig < G ? tig : 0) * kQStride;
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+#pragma unroll 8
+    for (int c = 0; c < 32; ++c) {  // 16-byte chunks of the 128 dims
+      const float4 qv = *reinterpret_cast<const float4*>(qh + 4 * c);
+      const float4 k0 = *reinterpret_cast<const float4*>(st + tile_offset<DT>(gid, c));
+      const float4 k1 = *reinterpret_cast<const float4*>(st + tile_offset<DT>(gid + 8, c));
+      a0 = make_float4(fmaf(qv.x, k0.x, a0.x), fmaf(qv.y, k0.y, a0.y), fmaf(qv.z, k0.z, a0.z),
+                       fmaf(qv.w, k0.w, a0.w));
+      a1 = make_float4(fmaf(qv.x, k1.x, a1.x), fmaf(qv.y, k1.y, a1.y), fmaf(qv.z, k1.z, a1.z),
+                       fmaf(qv.w, k1.w, a1.w));
+    }
+    s0 = (a0.x + a0.y) + (a0.z + a0.w);
+    s1 = (a1.x + a1.y) + (a1.z + a1.w);
+  } else if constexpr (DT == PKV_KV_BF16) {
     // bf16 pairs of an ldmatrix row widen to tf32 exactly: the low value is
     // the word shifted up, the high one the word with its low half cleared
     float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -285,6 +325,32 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
   const float p0 = exp2f(s0 - S.m), p1 = exp2f(s1 - S.m);
   S.l += p0 + p1;
 
+  if constexpr (DT == PKV_KV_F32) {
+    // O += p_t V_t on CUDA cores: lane 4 gid + tig keeps head tig's output at
+    // dims 32 j + 4 gid + {0..3}; p_t of head tig comes from lane
+    // 4 (t mod 8) + tig.  Unattended slots are skipped (their V may be NaN).
+    const uint8_t* vs = st + TL::kData;
+    auto accumulate = [&](int t) {
+      const float pt = __shfl_sync(kFull, t < 8 ? p0 : p1, 4 * (t & 7) + tig);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 v = *reinterpret_cast<const float4*>(vs + tile_offset<DT>(t, 8 * j + gid));
+        S.o[2 * j][0] = fmaf(pt, v.x, S.o[2 * j][0]);
+        S.o[2 * j][2] = fmaf(pt, v.y, S.o[2 * j][2]);
+        S.o[2 * j + 1][0] = fmaf(pt, v.z, S.o[2 * j + 1][0]);
+        S.o[2 * j + 1][2] = fmaf(pt, v.w, S.o[2 * j + 1][2]);
+      }
+    };
+    if (tlo == 0 && nvalid == kPage) {
+#pragma unroll
+      for (int t = 0; t < kPage; ++t) accumulate(t);
+    } else {
+      for (int t = tlo; t < nvalid; ++t) accumulate(t);
+    }
+    __syncwarp();
+    return;
+  }
+
   // ---- P^T operand: column gid (head gid/2, part gid%2) at tokens 2tig,
   // 2tig+1 (b0) and 2tig+8, 2tig+9 (b1); lane 8 tig + g holds head g's
   // tokens 2tig and 2tig + 8, lane 8 tig + 4 + g tokens 2tig+1 and 2tig+9.
@@ -297,7 +363,7 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
   const int t0 = 2 * tig;
 
   // ---- values
-  if constexpr (DT != PKV_KV_Q8_0) {
+  if constexpr (DT == PKV_KV_F16 || DT == PKV_KV_BF16) {
     if (tlo > 0 || nvalid < kPage) {  // zero the V rows of unattended slots (NaN * 0 is NaN)
       const int n_out = kPage - (nvalid - tlo);
       for (int x = lane; x < n_out * 16; x += 32) {
@@ -427,8 +493,9 @@ __device__ __forceinline__ void piece_merge(const float* mrg_acc, const float* m
 
 // --------------------------------------------------------------- kernel ----
 template <int DT, int G>
-__global__ void __launch_bounds__(kThreads, DT != PKV_KV_Q8_0 ? PKV_F16_CTAS_PER_SM
-                                                              : PKV_Q8_CTAS_PER_SM)
+__global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PER_SM
+                                            : DT == PKV_KV_F32 ? PKV_F32_CTAS_PER_SM
+                                                               : PKV_F16_CTAS_PER_SM)
     paged_decode_kernel(const __grid_constant__ DecodeArgs a,
                         const __grid_constant__ TileMaps maps) {
   using TL = Tiles<DT>;
@@ -546,7 +613,13 @@ __global__ void __launch_bounds__(kThreads, DT != PKV_KV_Q8_0 ? PKV_F16_CTAS_PER
       const uint32_t dst = smem_addr(ring + s * TL::kCodes);
       const int z = pg * a.n_kv + hh;  // tile index (the host checks num_pages * n_kv < 2^31)
       mbar_arrive_expect_tx(bar, TL::kTx);
-      if constexpr (DT != PKV_KV_Q8_0) {
+      if constexpr (DT == PKV_KV_F32) {  // four boxes of 32 dims per tile
+#pragma unroll
+        for (int bx = 0; bx < 4; ++bx) {
+          tma_load_3d(dst + bx * 2048, &maps.k, 32 * bx, 0, z, bar, policy);
+          tma_load_3d(dst + TL::kData + bx * 2048, &maps.v, 32 * bx, 0, z, bar, policy);
+        }
+      } else if constexpr (DT != PKV_KV_Q8_0) {
         tma_load_3d(dst, &maps.k, 0, 0, z, bar, policy);
         tma_load_3d(dst + 2048, &maps.k, 64, 0, z, bar, policy);
         tma_load_3d(dst + TL::kData, &maps.v, 0, 0, z, bar, policy);
@@ -570,6 +643,7 @@ __global__ void __launch_bounds__(kThreads, DT != PKV_KV_Q8_0 ? PKV_F16_CTAS_PER
   bool aborted = false;
   int consumed = 0;
   WarpState<DT> S;
+  S.qs = reinterpret_cast<float*>(smem + SM::kQ) + warp * G * kQStride;  // f32 KV only
 
   int piece = 0;
   for (long long x = c_begin; x < c_end; ++piece) {
@@ -808,20 +882,21 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // A layer's K or V data as a 3-D tensor [tiles][16 tokens][128 dims] read in
-// [16][64] (f16) or [16][128] (q8_0 codes) boxes of 128-byte rows under the
-// 128-byte swizzle.
+// boxes of 16 rows of 128 bytes under the 128-byte swizzle: [16][64] (f16,
+// bf16), [16][32] (f32) or [16][128] (q8_0 codes).
 static cudaError_t encode_tile_map(CUtensorMap* m, int dtype, void* base, long long tiles) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  const bool f16 = dtype != PKV_KV_Q8_0;  // 16-bit values (f16, bf16)
+  const cuuint32_t esize = dtype == PKV_KV_F32 ? 4u : dtype == PKV_KV_Q8_0 ? 1u : 2u;  // bytes
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(kPage),
                               static_cast<cuuint64_t>(tiles)};
-  const cuuint64_t strides[2] = {f16 ? 256u : 128u, f16 ? 4096u : 2048u};  // bytes
-  const cuuint32_t box[3] = {f16 ? 64u : 128u, static_cast<cuuint32_t>(kPage), 1u};
+  const cuuint64_t strides[2] = {kD * esize, kD * kPage * esize};  // bytes
+  const cuuint32_t box[3] = {128u / esize, static_cast<cuuint32_t>(kPage), 1u};
   const cuuint32_t estride[3] = {1u, 1u, 1u};
   const CUresult r =
       fn(m, dtype == PKV_KV_F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
             : dtype == PKV_KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+            : dtype == PKV_KV_F32  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                    : CU_TENSOR_MAP_DATA_TYPE_UINT8,
          3, base, dims,
          strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -900,6 +975,10 @@ static cudaError_t occupancy_t(int rows, int* blocks) {
       if ((G_) == 1) return CALL(2, 1);      \
       if ((G_) == 2) return CALL(2, 2);      \
       if ((G_) == 4) return CALL(2, 4);      \
+    } else if ((DT_) == PKV_KV_F32) {        \
+      if ((G_) == 1) return CALL(3, 1);      \
+      if ((G_) == 2) return CALL(3, 2);      \
+      if ((G_) == 4) return CALL(3, 4);      \
     } else {                                 \
       if ((G_) == 1) return CALL(1, 1);      \
       if ((G_) == 2) return CALL(1, 2);      \

@@ -32,6 +32,9 @@ namespace pkv {
 #ifndef PKV_PDL
 #define PKV_PDL 1
 #endif
+#ifndef PKV_F32_CTAS_PER_SM
+#define PKV_F32_CTAS_PER_SM 2  // 16 KiB stages, one per warp: the shared memory of 2 CTAs
+#endif
 #ifndef PKV_MERGE_BATCH
 #define PKV_MERGE_BATCH 8  // 4 for q8_0, whose 4 CTAs per SM leave 128 registers a thread
 #endif
@@ -57,6 +60,15 @@ struct Tiles<PKV_KV_F16> {
 template <>
 struct Tiles<PKV_KV_BF16> : Tiles<PKV_KV_F16> {};  // same geometry: 16-bit values
 template <>
+struct Tiles<PKV_KV_F32> {
+  static constexpr uint32_t kData = kPage * kD * 4;  // 8 KiB of one K or V tile: four 2 KiB boxes
+  static constexpr uint32_t kScale = 0;
+  static constexpr uint32_t kCodes = 2 * kData;
+  static constexpr uint32_t kScales = 0;
+  static constexpr uint32_t kTx = kCodes;
+  static constexpr int kRing = 1;  // one 16 KiB stage per warp
+};
+template <>
 struct Tiles<PKV_KV_Q8_0> {
   static constexpr uint32_t kData = kPage * kD;                   // 2048 codes
   static constexpr uint32_t kScale = kPage * (kD / kQBlock) * 2;  // 128 bytes of f16 scales
@@ -67,9 +79,10 @@ struct Tiles<PKV_KV_Q8_0> {
 };
 
 // ------------------------------------------------------------ operands ----
-// Byte offset of the 16-byte chunk c (8 f16 or 16 int8 values) of token row t
-// in a swizzled tile: 128-byte rows, chunk index xor (row mod 8); f16 tiles
-// keep dims 64..127 in a second 2 KiB half.
+// Byte offset of the 16-byte chunk c (8 f16 / bf16, 4 f32 or 16 int8 values)
+// of token row t in a swizzled tile: 128-byte rows, chunk index xor (row mod
+// 8); 16-bit tiles keep dims 64..127 in a second 2 KiB box, f32 tiles hold
+// four 2 KiB boxes of 32 dims.
 template <int DT>
 __device__ __forceinline__ uint32_t tile_offset(int t, int c) {
   if constexpr (DT != PKV_KV_Q8_0)
@@ -268,6 +281,8 @@ __device__ __forceinline__ void append_token(const DecodeArgs& a, long long src_
       w.x = *reinterpret_cast<const uint32_t*>(&lo);
       w.y = *reinterpret_cast<const uint32_t*>(&hi);
       *reinterpret_cast<uint2*>(data + tile * TL::kData + slot * (kD * 2) + lane * 8) = w;
+    } else if constexpr (DT == PKV_KV_F32) {
+      *reinterpret_cast<float4*>(data + tile * TL::kData + slot * (kD * 4) + lane * 16) = x;
     } else if constexpr (DT == PKV_KV_BF16) {
       const __nv_bfloat162 lo = __floats2bfloat162_rn(x.x, x.y), hi = __floats2bfloat162_rn(x.z, x.w);
       uint2 w;

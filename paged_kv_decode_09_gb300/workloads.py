@@ -27,8 +27,8 @@ from dataclasses import dataclass, field
 import numpy as np
 
 PAGE = 16
-F16, Q8_0, BF16 = 0, 1, 2
-DTYPE_NAMES = {F16: "f16", Q8_0: "q8_0", BF16: "bf16"}
+F16, Q8_0, BF16, F32 = 0, 1, 2, 3
+DTYPE_NAMES = {F16: "f16", Q8_0: "q8_0", BF16: "bf16", F32: "f32"}
 
 
 @dataclass(frozen=True)
@@ -73,6 +73,10 @@ CONFIGS = {
         Config("llama8b_bf16", 8, ("uniform", 1024, 8192), 32, 8, 128, BF16, ("spare", 0.10), 5,
                model_layers=32,
                description="8B layer: 8 rows, L~U[1024,8192], 32q/8kv, bf16, shuffled pages"),
+        # and with fp32 KV (tinyllm's F32 KV caching)
+        Config("llama8b_f32", 8, ("uniform", 1024, 8192), 32, 8, 128, F32, ("spare", 0.10), 6,
+               model_layers=32,
+               description="8B layer: 8 rows, L~U[1024,8192], 32q/8kv, f32, shuffled pages"),
     ]
 }
 CONFIG_ORDER = ["tiny", "qwen3_0p6b_layer", "llama8b_f16", "llama8b_q8_0", "skewed"]
@@ -83,8 +87,11 @@ def pages_for(length: int) -> int:
 
 
 def page_bytes_all_heads(cfg: Config) -> int:
-    """Bytes of one page across all KV heads, K and V (f16 or q8_0)."""
-    per_token_head = cfg.head_dim * 2 if cfg.dtype == F16 else cfg.head_dim + cfg.head_dim // 32 * 2
+    """Bytes of one page across all KV heads, K and V."""
+    if cfg.dtype == Q8_0:
+        per_token_head = cfg.head_dim + cfg.head_dim // 32 * 2
+    else:
+        per_token_head = cfg.head_dim * (4 if cfg.dtype == F32 else 2)
     return 2 * cfg.n_kv_heads * PAGE * per_token_head
 
 

@@ -2,7 +2,7 @@
 encoder, poison unused slots, and small utilities shared by the tests.
 
 Pool arrays per layer (the library's documented layout): data
-[num_pages][n_kv][16][D] (uint16 f16 bits or int8 q8_0 codes), q8_0 scales
+[num_pages][n_kv][16][D] (uint16 f16 / bf16 bits, float32, or int8 q8_0 codes), q8_0 scales
 [num_pages][n_kv][16][D/32] (uint16 f16 bits)."""
 from __future__ import annotations
 
@@ -13,6 +13,7 @@ from paged_kv_decode_09_gb300 import workloads as W
 
 F16_NAN = np.uint16(0x7E00)
 BF16_NAN = np.uint16(0x7FC0)
+F32_NAN = np.float32(np.nan)
 
 
 def encode_pool(wl: W.Workload, layer: int = 0, include_appended: bool = True,
@@ -37,6 +38,9 @@ def encode_pool(wl: W.Workload, layer: int = 0, include_appended: bool = True,
         elif cfg.dtype == W.BF16:
             kd[sel] = BF16_NAN
             vd[sel] = BF16_NAN
+        elif cfg.dtype == W.F32:
+            kd[sel] = F32_NAN
+            vd[sel] = F32_NAN
         else:
             ks[sel] = F16_NAN
             vs[sel] = F16_NAN
@@ -60,6 +64,8 @@ def stored_values_dense(dtype, data, scales):
         return data.view(np.float16).astype(np.float64)
     if dtype == W.BF16:  # the high half of a binary32
         return (data.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    if dtype == W.F32:
+        return data.astype(np.float64)
     sc = scales.view(np.float16).astype(np.float64)
     return np.repeat(sc, 32, axis=-1) * data.astype(np.float64)
 
@@ -83,6 +89,11 @@ def device_pool(wl: W.Workload, host_pool, num_layers: int = 1, layer: int = 0):
             t.view(torch.int16).fill_(nan)
         pool.k_data[layer].view(torch.int16).copy_(torch.from_numpy(kd.view(np.int16)))
         pool.v_data[layer].view(torch.int16).copy_(torch.from_numpy(vd.view(np.int16)))
+    elif cfg.dtype == W.F32:
+        for t in (pool.k_data, pool.v_data):
+            t.fill_(float("nan"))
+        pool.k_data[layer].copy_(torch.from_numpy(np.ascontiguousarray(kd, np.float32)))
+        pool.v_data[layer].copy_(torch.from_numpy(np.ascontiguousarray(vd, np.float32)))
     else:
         for t in (pool.k_scales, pool.v_scales):
             t.view(torch.int16).fill_(0x7E00)
@@ -101,6 +112,8 @@ def host_arrays(pool, layer: int = 0):
     if pool.dtype in (W.F16, W.BF16):
         return (pool.k_data[layer].cpu().view(torch.int16).numpy().view(np.uint16),
                 pool.v_data[layer].cpu().view(torch.int16).numpy().view(np.uint16), None, None)
+    if pool.dtype == W.F32:
+        return pool.k_data[layer].cpu().numpy(), pool.v_data[layer].cpu().numpy(), None, None
     return (pool.k_data[layer].cpu().numpy(), pool.v_data[layer].cpu().numpy(),
             pool.k_scales[layer].cpu().view(torch.int16).numpy().view(np.uint16),
             pool.v_scales[layer].cpu().view(torch.int16).numpy().view(np.uint16))

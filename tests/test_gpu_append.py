@@ -31,7 +31,7 @@ def _append_case(cfg_name, dtype=None, scale_new=1.0, layer=1, layers=3):
     return wl, pool, got, want
 
 
-@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16])
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16, W.F32])
 @pytest.mark.parametrize("cfg_name", ["tiny", "skewed"])
 def test_append_bit_exact(cfg_name, dtype):
     _, pool, got, want = _append_case(cfg_name, dtype)
@@ -40,7 +40,7 @@ def test_append_bit_exact(cfg_name, dtype):
             np.testing.assert_array_equal(g, w)
     # other layers untouched
     other = host_arrays(pool, 0)
-    assert np.array_equal(other[0], host_arrays(pool, 2)[0])
+    assert np.array_equal(other[0].view(np.uint8), host_arrays(pool, 2)[0].view(np.uint8))
 
 
 @pytest.mark.parametrize("scale_new", [1e-3, 1e3, 3e4])

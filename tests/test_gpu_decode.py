@@ -36,7 +36,8 @@ def _run(wl, pool, layer=0, num_chunks=0, q=None, seq_lens=None):
     return out.cpu().numpy()
 
 
-@pytest.mark.parametrize("cfg_name", ["tiny", "qwen3_0p6b_layer", "llama8b_f16", "llama8b_bf16"])
+@pytest.mark.parametrize("cfg_name", ["tiny", "qwen3_0p6b_layer", "llama8b_f16", "llama8b_bf16",
+                                      "llama8b_f32"])
 def test_attention_matches_oracle(cfg_name):
     wl = W.draw(cfg_name)
     host = encode_pool(wl)
@@ -74,7 +75,7 @@ def test_skewed_decode_step_appends_then_attends():
     _check(out.cpu().numpy(), oracle_decode(wl, want))
 
 
-@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16])
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16, W.F32])
 def test_split_invariance(dtype):
     """Any chunk count gives the same output: 1 chunk (no merge), many chunks
     (every (row, head) split, one page per piece at the extreme)."""
@@ -91,7 +92,7 @@ def test_split_invariance(dtype):
 
 
 @pytest.mark.parametrize("group,n_kv", [(1, 4), (2, 8), (4, 8), (4, 2)])
-@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16])
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16, W.F32])
 def test_gqa_groups(group, n_kv, dtype):
     cfg = W.Config("gqa", 5, ("uniform", 1, 300), n_kv * group, n_kv, 128, dtype,
                    ("spare", 0.3), 40 + group)
@@ -101,10 +102,11 @@ def test_gqa_groups(group, n_kv, dtype):
     _check(_run(wl, pool, num_chunks=37), oracle_decode(wl, host))
 
 
-def test_peaked_scores():
+@pytest.mark.parametrize("cfg_name", ["llama8b_f16", "llama8b_f32"])
+def test_peaked_scores(cfg_name):
     """q scaled by 8: near one-hot softmax, so one wrong key or value would
     dominate the output."""
-    wl = W.draw("llama8b_f16")
+    wl = W.draw(cfg_name)
     host = encode_pool(wl)
     pool = device_pool(wl, host)
     q = (wl.q * 8).astype(np.float32)
@@ -153,7 +155,7 @@ def test_host_validation_errors():
     assert out.shape == q.shape
 
 
-@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16])
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16, W.F32])
 def test_fused_step_append_is_bit_exact(dtype):
     """pkv_decode_step stores each row's token inside the attention kernel:
     the pool afterwards must equal the oracle's append byte for byte."""
@@ -177,7 +179,7 @@ def test_fused_step_append_is_bit_exact(dtype):
     _check(out.cpu().numpy()[rows], ref)
 
 
-@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16])
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16, W.F32])
 def test_split_then_combine_equals_merged(dtype):
     wl = W.draw("llama8b_f16")
     wl.cfg = W.Config(**{**wl.cfg.__dict__, "dtype": dtype})

@@ -210,3 +210,14 @@ def test_mq_validation():
     with pytest.raises(ValueError):  # 3-D q
         api.paged_decode_attention_mq(pool, 0, torch.zeros((wl.rows, 16, 128), device="cuda"),
                                       bt, sl, wl.scale)
+
+
+def test_mq_f32_pool_is_unsupported():
+    """Several queries per row are not built for f32 KV: a typed error, no launch."""
+    wl = _wl(W.F32, n_q=32, n_kv=8)
+    pool = device_pool(wl, encode_pool(wl))
+    q, _, _ = W.mq_inputs(wl, 2)
+    with pytest.raises(api.PkvError) as e:
+        api.paged_decode_attention_mq(pool, 0, to_dev(q), to_dev(wl.block_table),
+                                      to_dev(wl.seq_lens), wl.scale)
+    assert e.value.status == 2

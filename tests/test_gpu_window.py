@@ -91,7 +91,7 @@ def test_window_per_layer(cfg_name):
     _check(_attend(wl, pool, layer=1), oracle_decode(wl, host, window=20))
 
 
-@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16])
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16, W.F32])
 def test_window_split_invariance(dtype):
     """Windows starting mid-page, rows shorter than the window, an empty row."""
     wl = W.draw("tiny", lengths=[1, 17, 33, 100, 16, 250, 0, 31])

@@ -36,8 +36,11 @@ def _scatter_rows(rng, dtype, dense_k, dense_v, lens, n_kv, D, extra_pages=3, or
     bt = np.full((len(lens), stride), -1, np.int32)
     q8 = dtype == O.Q8_0
     nan16 = 0x7FC0 if dtype == O.BF16 else 0x7E00  # NaN in the stored 16-bit format
-    kd = np.full((num_pages, n_kv, PAGE, D), nan16 if not q8 else 127,
-                 np.uint16 if not q8 else np.int8)
+    if dtype == O.F32:
+        kd = np.full((num_pages, n_kv, PAGE, D), np.nan, np.float32)
+    else:
+        kd = np.full((num_pages, n_kv, PAGE, D), nan16 if not q8 else 127,
+                     np.uint16 if not q8 else np.int8)
     vd = kd.copy()
     ks = np.full((num_pages, n_kv, PAGE, D // 32), 0x7E00, np.uint16) if q8 else None
     vs = ks.copy() if q8 else None
@@ -83,7 +86,7 @@ def _brute(dtype, q, dk, dv, lens, n_q, n_kv, scale):
     return out
 
 
-@pytest.mark.parametrize("dtype", [O.F16, O.Q8_0, O.BF16])
+@pytest.mark.parametrize("dtype", [O.F16, O.Q8_0, O.BF16, O.F32])
 @pytest.mark.parametrize("shape", [(4, 4, 32), (4, 2, 64), (8, 2, 128), (2, 2, 32)])
 def test_against_dense_brute_force(dtype, shape):
     n_q, n_kv, D = shape
@@ -95,7 +98,7 @@ def test_against_dense_brute_force(dtype, shape):
     np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
 
 
-@pytest.mark.parametrize("dtype", [O.F16, O.Q8_0, O.BF16])
+@pytest.mark.parametrize("dtype", [O.F16, O.Q8_0, O.BF16, O.F32])
 def test_contiguous_equals_paged(dtype):
     lens, n_q, n_kv, D = [5, 16, 47, 70], 4, 2, 128
     a = _case(3, dtype, lens, n_q, n_kv, D, order="contiguous")
@@ -120,7 +123,7 @@ def test_page_permutation_invariance():
     np.testing.assert_array_equal(base, got)
 
 
-@pytest.mark.parametrize("dtype", [O.F16, O.Q8_0, O.BF16])
+@pytest.mark.parametrize("dtype", [O.F16, O.Q8_0, O.BF16, O.F32])
 def test_single_token_returns_v(dtype):
     q, dk, dv, pool, bt, num_pages = _case(6, dtype, [1, 1], 4, 2, 128)
     out = O.decode_attention(dtype, q, *pool, bt, np.array([1, 1], np.int32), num_pages, 2, 0.3)

@@ -26,7 +26,7 @@ def _mq_case(seed, dtype, lens, q_len, n_q, n_kv, D):
     return q, dk, dv, pool, bt, num_pages
 
 
-@pytest.mark.parametrize("dtype", [O.F16, O.Q8_0, O.BF16])
+@pytest.mark.parametrize("dtype", [O.F16, O.Q8_0, O.BF16, O.F32])
 def test_one_query_is_the_single_query_call(dtype):
     lens, n_q, n_kv, D = [3, 17, 40], 4, 2, 64
     q, dk, dv, pool, bt, num_pages = _mq_case(5, dtype, lens, 1, n_q, n_kv, D)
@@ -38,7 +38,7 @@ def test_one_query_is_the_single_query_call(dtype):
         np.testing.assert_array_equal(mq[:, 0], single)
 
 
-@pytest.mark.parametrize("dtype", [O.F16, O.Q8_0, O.BF16])
+@pytest.mark.parametrize("dtype", [O.F16, O.Q8_0, O.BF16, O.F32])
 @pytest.mark.parametrize("window", [0, 5, 16, 33])
 def test_each_query_is_single_query_attention_over_its_prefix(dtype, window):
     lens, q_len, n_q, n_kv, D = [8, 20, 47, 64], 6, 4, 2, 64
@@ -90,7 +90,7 @@ def test_causality_later_tokens_do_not_matter():
             assert np.isnan(got[:, j + 1:]).any()  # later queries do see the poisoned tokens
 
 
-@pytest.mark.parametrize("dtype", [O.F16, O.Q8_0, O.BF16])
+@pytest.mark.parametrize("dtype", [O.F16, O.Q8_0, O.BF16, O.F32])
 def test_multi_token_append_is_sequential_appends(dtype):
     rng = np.random.default_rng(13)
     rows, q_len, n_kv, D, num_pages = 3, 5, 2, 64, 12
@@ -98,7 +98,7 @@ def test_multi_token_append_is_sequential_appends(dtype):
     bt = rng.permutation(num_pages)[:9].reshape(rows, 3).astype(np.int32)
     q8 = dtype == O.Q8_0
     shape = (num_pages, n_kv, 16, D)
-    kd = np.zeros(shape, np.int8 if q8 else np.uint16)
+    kd = np.zeros(shape, np.int8 if q8 else np.float32 if dtype == O.F32 else np.uint16)
     ks = np.zeros((num_pages, n_kv, 16, D // 32), np.uint16) if q8 else None
     pools = [[kd.copy(), kd.copy(), None if ks is None else ks.copy(), None if ks is None else ks.copy()]
              for _ in range(2)]

@@ -52,6 +52,12 @@ MUTANTS = {
     "mq_query_one_late": ("int P = L - q_len + j;", "int P = L - q_len + j + (j > 0);"),
     "mq_append_position": ("bt_stride, i, h, L - q_len + j, num_pages, k_data, v_data,",
                            "bt_stride, i, h, L - q_len + j - (j > 0), num_pages, k_data, v_data,"),
+    "f32_neighbour_value": ("if (dtype == ORACLE_F32) return (double)((const float *)data)[row * D + d];",
+                            "if (dtype == ORACLE_F32) return (double)((const float *)data)[row * D + (d ^ 1)];"),
+    "f32_append_swaps_k_v": ("/* the fp32 values, unrounded */\n                memcpy((float *)k_data + row * D, kx,",
+                             "/* the fp32 values, unrounded */\n                memcpy((float *)k_data + row * D, vx,"),
+    "f32_mq_append_swaps_k_v": ("/* stored as given */\n        memcpy((float *)k_data + row * D, kx,",
+                                "/* stored as given */\n        memcpy((float *)k_data + row * D, vx,"),
     "window_one_too_short": ("return window > 0 && L > window ? L - window : 0;",
                              "return window > 0 && L > window ? L - window + 1 : 0;"),
     "window_first_page_rounded_up": (

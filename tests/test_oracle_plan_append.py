@@ -153,3 +153,26 @@ def test_append_rejects_page_outside_pool():
     with pytest.raises(ValueError):
         O.kv_append(W.F16, np.zeros((1, 1, 32), np.float32), np.zeros((1, 1, 32), np.float32),
                     bt, np.array([3], np.int32), 4, kd, kd.copy())
+
+
+def test_append_f32_stores_the_values_unrounded():
+    """f32 KV (tinyllm, "The repository currently provides": BF16/F32 KV
+    caching) keeps the fp32 inputs as they are: the slot holds k_new and v_new
+    bit for bit, in the K and V arrays respectively, and nothing else moves."""
+    rng = np.random.default_rng(23)
+    rows, n_kv, D, num_pages = 3, 2, 64, 8
+    lens = np.array([1, 18, 32], np.int32)
+    bt = rng.permutation(num_pages)[:6].reshape(rows, 2).astype(np.int32)
+    kd = rng.standard_normal((num_pages, n_kv, 16, D)).astype(np.float32)
+    vd = rng.standard_normal((num_pages, n_kv, 16, D)).astype(np.float32)
+    k0, v0 = kd.copy(), vd.copy()
+    k_new = rng.standard_normal((rows, n_kv, D)).astype(np.float32)
+    v_new = rng.standard_normal((rows, n_kv, D)).astype(np.float32)
+    O.kv_append(O.F32, k_new, v_new, bt, lens, num_pages, kd, vd)
+    for i, L in enumerate(lens):
+        page, slot = bt[i, (L - 1) // 16], (L - 1) % 16
+        np.testing.assert_array_equal(kd[page, :, slot].view(np.uint32), k_new[i].view(np.uint32))
+        np.testing.assert_array_equal(vd[page, :, slot].view(np.uint32), v_new[i].view(np.uint32))
+        k0[page, :, slot], v0[page, :, slot] = k_new[i], v_new[i]
+    np.testing.assert_array_equal(kd, k0)
+    np.testing.assert_array_equal(vd, v0)
