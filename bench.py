@@ -56,6 +56,8 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU baseline budget")
     p.add_argument("--window", type=int, default=0,
                    help="sliding window of every layer (0: none); bytes count attended tokens")
+    p.add_argument("--no-graph", action="store_true",
+                   help="skip the CUDA-graph replay timing (shorter runs under a profiler)")
     p.add_argument("--q-len", type=int, default=1,
                    help="new tokens (queries) per row: > 1 times the several-query step")
     p.add_argument("--kernel", choices=["step", "append", "split_combine", "plan", "alloc"],
@@ -326,7 +328,7 @@ def run_ours(args, rank, world, local):
     launch_ms = total_ms / K
     assert pool.read_status() == 0, "device status word set during the timed steps"
 
-    graph = graph_timing(torch, dev, step, layers)
+    graph = None if args.no_graph else graph_timing(torch, dev, step, layers)
 
     # ---- end to end through the C ABI: pinned host inputs in, output out
     hq, hk, hv = (x.cpu().pin_memory() for x in (q, k_new, v_new))
