@@ -266,7 +266,7 @@ def run_ours(args, rank, world, local):
         q, k_new, v_new = t(hq_np), t(hk_np), t(hv_np)
         ws = api.WorkspaceMQ(pool, cfg.n_q_heads, wl.rows, QL, args.chunks)
         cols = QL * cfg.group  # (query, head) columns; the kernel's pass width follows them
-        if cfg.dtype == W.Q8_0 or cols <= (4 if cfg.dtype == W.BF16 else 8):
+        if cfg.dtype in (W.Q8_0, W.F32) or cols <= (4 if cfg.dtype == W.BF16 else 8):
             width = min(cols, 8)
             kname = "paged_decode_mq_kernel"  # the warps of a CTA read different pages
         else:

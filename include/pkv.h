@@ -268,13 +268,12 @@ pkv_status pkv_decode_step(const pkv_pool *pool, int layer, const float *q, cons
  *   k_new, v_new  fp32 [num_rows][q_len][n_kv_heads][128] (pkv_decode_step_mq):
  *                 token j of row i is stored at position L - q_len + j
  * Rows with L == 0 get zeros; rows with 0 < L < q_len get zeros and set
- * PKV_DEV_BAD_LENGTH.  f32 pools are not supported here (PKV_ERR_UNSUPPORTED).
- * A row reads the pages holding [L - q_len + 1 - W, L)
+ * PKV_DEV_BAD_LENGTH.  A row reads the pages holding [L - q_len + 1 - W, L)
  * (all of [0, L) without a window), split into chunks as in
  * paged_decode_attention.  Every page is read once per pass; a pass carries
  * the (query, query head) pairs of a KV head, C = q_len * G in all:
- *     C <= 8 (bf16: 4), and q8_0: passes of 8 pairs (bf16: 4), the CTA's
- *     warps reading different pages;
+ *     C <= 8 (bf16: 4), and q8_0 and f32: passes of 8 pairs (bf16: 4), the
+ *     CTA's warps reading different pages;
  *     otherwise passes of 16 pairs (C <= 16, and bf16) or 32 (f16), the
  *     CTA's four warps reading every page together, a quarter each;
  * each pass one launch on `stream`.  pkv_decode_step_mq stores the new tokens

@@ -251,8 +251,6 @@ pkv_status attention_mq_impl(const pkv_pool* pool, int layer, const float* q, co
   if ((s = check_rows(num_rows, bt_stride, block_table, seq_lens))) return s;
   if (q_len < 1 || q_len > PKV_MAX_Q_LEN)
     return fail(PKV_ERR_UNSUPPORTED, "q_len %d outside [1, %d]", q_len, PKV_MAX_Q_LEN);
-  if (pool->dtype == PKV_KV_F32)
-    return fail(PKV_ERR_UNSUPPORTED, "several queries per row on an f32 pool");
   if (num_rows > 0 && (!q || !out)) return fail(PKV_ERR_INVALID_ARG, "null q or out");
   if (!aligned(q, 16) || !aligned(out, 16))
     return fail(PKV_ERR_INVALID_ARG, "q / out not 16-byte aligned");
@@ -566,8 +564,6 @@ pkv_status paged_decode_default_chunks_mq(const pkv_pool* pool, int n_q_heads, i
     return fail(PKV_ERR_UNSUPPORTED, "max_rows %d outside [1, %d]", max_rows, PKV_MAX_ROWS);
   if (q_len < 1 || q_len > PKV_MAX_Q_LEN)
     return fail(PKV_ERR_UNSUPPORTED, "q_len %d outside [1, %d]", q_len, PKV_MAX_Q_LEN);
-  if (pool->dtype == PKV_KV_F32)
-    return fail(PKV_ERR_UNSUPPORTED, "several queries per row on an f32 pool");
   return default_chunks_mq(pool, n_q_heads / pool->n_kv, q_len, max_rows, chunks);
 }
 

@@ -46,11 +46,12 @@ __host__ __device__ constexpr int mq_tiles() {
 // 4 columns a warp up to 16, else 8), in passes of 16 or 32 columns.  q8_0
 // always takes the first, in passes of 8 columns: its pages are converted
 // from int8 codes by the warp that reads them, so four warps sharing a page
-// would convert it four times (measured slower than a second pass).
+// would convert it four times (measured slower than a second pass).  f32
+// pages (CUDA cores) take the first as well.
 enum MqKind { kMqSingle = 0, kMqTeam1 = 1, kMqTeam2 = 2 };
 static int mq_kind(int dtype, int group, int q_len) {
   const int cols = q_len * group;
-  if (dtype == PKV_KV_Q8_0) return kMqSingle;
+  if (dtype == PKV_KV_Q8_0 || dtype == PKV_KV_F32) return kMqSingle;
   if (dtype == PKV_KV_BF16) return cols <= 4 ? kMqSingle : kMqTeam1;
   return cols <= 8 ? kMqSingle : cols <= 16 ? kMqTeam1 : kMqTeam2;
 }
@@ -64,6 +65,9 @@ int mq_pass_queries(int dtype, int group, int q_len) {
 }
 
 constexpr int kWarpCols = 8;  // (query, head) columns of one warp's state: 2 score n-tiles
+// f32 KV keeps a warp's scaled queries in shared memory, one column every
+// kQStride floats (the 16-byte pad puts the columns' chunks in different banks).
+constexpr int kQStride = kD + 4;
 
 template <int DT>
 struct MqSmem {
@@ -73,7 +77,9 @@ struct MqSmem {
   static constexpr uint32_t kBar = kScl + kStages * Tiles<DT>::kScales;
   static constexpr uint32_t kMrgAcc = kBar + ((kStages * 8 + 15) / 16) * 16;  // f32 [warps][8][D]
   static constexpr uint32_t kMrgMl = kMrgAcc + kWarps * kWarpCols * kD * 4;    // f32 [warps][8][2]
-  static constexpr uint32_t kCtl = kMrgMl + kWarps * kWarpCols * 2 * 4;
+  static constexpr uint32_t kQ = kMrgMl + kWarps * kWarpCols * 2 * 4;  // f32 KV: [warps][8][kQStride] q
+  static constexpr uint32_t kCtl =
+      kQ + (DT == PKV_KV_F32 ? kWarps * kWarpCols * kQStride * 4 : 0);
   static constexpr uint32_t kRows = kCtl + 16;
   static size_t bytes(int rows) { return kAlign + kRows + (2 * static_cast<size_t>(rows) + 1) * 4; }
   static_assert(Tiles<DT>::kCodes % 1024 == 0, "tile stages keep the swizzle atom alignment");
@@ -81,7 +87,7 @@ struct MqSmem {
 
 template <int DT>
 __host__ __device__ constexpr int mq_steps() {  // k-steps over the 128 dims: f16 MMAs take 16 dims, tf32 MMAs 8
-  return DT == PKV_KV_BF16 ? 16 : 8;
+  return DT == PKV_KV_BF16 ? 16 : DT == PKV_KV_F32 ? 1 : 8;  // f32: CUDA cores, no fragments
 }
 
 template <int DT, int kTiles>
@@ -93,13 +99,14 @@ struct MqState {
   float m[NT], l[NT];          // softmax state of the lane's score columns
   float o[8][4];               // O^T: dims x V-columns 2tig (o[.][0, 2]) and 2tig + 1 (o[.][1, 3])
   int vx;                      // q8_0: bound on the piece's V block scales (as decode.cu)
+  float* qs;                   // f32 KV: the warp's scaled queries [8][kQStride] in shared memory
 };
 
 template <int DT>
 __device__ __forceinline__ float mq_o_scale(int vx) {
   if constexpr (DT == PKV_KV_F16)
     return 1.0f / (1 << kPShift);
-  else if constexpr (DT == PKV_KV_BF16)
+  else if constexpr (DT == PKV_KV_BF16 || DT == PKV_KV_F32)
     return 1.0f;
   else
     return pow2i(vx - kPShift);
@@ -108,7 +115,9 @@ __device__ __forceinline__ float mq_o_scale(int vx) {
 // Dim of O row r, element e (0: c0/c1, 2: c2/c3) in lane 4 gid + tig (as decode.cu).
 template <int DT>
 __device__ __forceinline__ int mq_dim(int r, int e, int gid) {
-  if constexpr (DT != PKV_KV_Q8_0)
+  if constexpr (DT == PKV_KV_F32)  // dims 32j + 4gid + {0..3} (CUDA-core accumulation)
+    return 32 * (r >> 1) + 4 * gid + 2 * (r & 1) + (e ? 1 : 0);
+  else if constexpr (DT != PKV_KV_Q8_0)
     return 16 * r + gid + (e ? 8 : 0);
   else
     return 16 * r + 2 * gid + (e ? 1 : 0);
@@ -183,7 +192,31 @@ __device__ __forceinline__ void mq_process_unit(const uint8_t* st, const uint8_t
 
   // ---- scores of the lane's columns 4t + tig, tokens gid and gid + 8
   float s[NT][2];
-  if constexpr (DT == PKV_KV_BF16) {
+  if constexpr (DT == PKV_KV_F32) {
+    // CUDA cores, fp32: dot products of the column's q (shared buffer) with K
+    // rows gid and gid + 8, four partial sums each
+    float4 acc[NT][2];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int c = 0; c < 32; ++c) {  // 16-byte chunks of the 128 dims
+      const float4 k0 = *reinterpret_cast<const float4*>(st + tile_offset<DT>(gid, c));
+      const float4 k1 = *reinterpret_cast<const float4*>(st + tile_offset<DT>(gid + 8, c));
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const float4 qv = *reinterpret_cast<const float4*>(S.qs + (4 * t + tig) * kQStride + 4 * c);
+        acc[t][0] = make_float4(fmaf(qv.x, k0.x, acc[t][0].x), fmaf(qv.y, k0.y, acc[t][0].y),
+                                fmaf(qv.z, k0.z, acc[t][0].z), fmaf(qv.w, k0.w, acc[t][0].w));
+        acc[t][1] = make_float4(fmaf(qv.x, k1.x, acc[t][1].x), fmaf(qv.y, k1.y, acc[t][1].y),
+                                fmaf(qv.z, k1.z, acc[t][1].z), fmaf(qv.w, k1.w, acc[t][1].w));
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      s[t][0] = (acc[t][0].x + acc[t][0].y) + (acc[t][0].z + acc[t][0].w);
+      s[t][1] = (acc[t][1].x + acc[t][1].y) + (acc[t][1].z + acc[t][1].w);
+    }
+  } else if constexpr (DT == PKV_KV_BF16) {
     float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int c2 = 0; c2 < 8; ++c2) {
@@ -297,6 +330,51 @@ __device__ __forceinline__ void mq_process_unit(const uint8_t* st, const uint8_t
     S.l[t] += p[t][0] + p[t][1];
   }
 
+  if constexpr (DT == PKV_KV_F32) {
+    // O += p_t V_t on CUDA cores: lane 4 gid + tig keeps V-columns 2tig + e
+    // (e = 0, 1) at dims 32 j + 4 gid + {0..3}.  Column c's p_t sits in lane
+    // 4 (t mod 8) + (c mod 4), score tile c / 4 (one shuffle per tile, then a
+    // select).  Slots no column attends are skipped (their V may be NaN).
+    const uint8_t* vs = st + TL::kData;
+    const int c0 = 2 * tig, c1 = 2 * tig + 1;
+    auto accumulate = [&](int t) {
+      const int hi = t >> 3;
+      float pe[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int c = e ? c1 : c0;
+        const int src = 4 * (t & 7) + (c & 3);
+        float v = __shfl_sync(kFull, hi ? p[0][1] : p[0][0], src);
+        if constexpr (NT == 2) {
+          const float v1 = __shfl_sync(kFull, hi ? p[1][1] : p[1][0], src);
+          if (c >= 4) v = v1;
+        } else {
+          if (c >= 4) v = 0.f;  // 4 columns: V-columns 4..7 unused
+        }
+        pe[e] = c < nc ? v : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 x = *reinterpret_cast<const float4*>(vs + tile_offset<DT>(t, 8 * j + gid));
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          S.o[2 * j][e] = fmaf(pe[e], x.x, S.o[2 * j][e]);
+          S.o[2 * j][e + 2] = fmaf(pe[e], x.y, S.o[2 * j][e + 2]);
+          S.o[2 * j + 1][e] = fmaf(pe[e], x.z, S.o[2 * j + 1][e]);
+          S.o[2 * j + 1][e + 2] = fmaf(pe[e], x.w, S.o[2 * j + 1][e + 2]);
+        }
+      }
+    };
+    if (slot_lo == 0 && slot_hi == kPage) {
+#pragma unroll
+      for (int t = 0; t < kPage; ++t) accumulate(t);
+    } else {
+      for (int t = slot_lo; t < slot_hi; ++t) accumulate(t);
+    }
+    __syncwarp();
+    return;
+  }
+
   // ---- P^T operands: V-column gid = score column gid (n-tile gid / 4, lanes
   // tig' = gid % 4): tokens 2tig, 2tig+1 from lanes 8 tig + gid % 4 and
   // 8 tig + 4 + gid % 4, tokens + 8 from their second scores
@@ -319,7 +397,7 @@ __device__ __forceinline__ void mq_process_unit(const uint8_t* st, const uint8_t
   const int t0 = 2 * tig;
 
   // ---- values: each part of P is its own B operand into the same accumulator
-  if constexpr (DT != PKV_KV_Q8_0) {
+  if constexpr (DT == PKV_KV_F16 || DT == PKV_KV_BF16) {
     // V values of slots no column attends may be anything (NaN * 0 is NaN):
     // masked in the registers, the stage is shared by readers.  Fragment
     // words hold tokens (2tig, 2tig + 1) [w0, w2] or (2tig + 8, 2tig + 9) [w1, w3].
@@ -369,7 +447,7 @@ __device__ __forceinline__ void mq_process_unit(const uint8_t* st, const uint8_t
         mma_1688_tf32(S.o[mt], y0, y1, y2, y3, l8, l9);
       }
     }
-  } else {
+  } else if constexpr (DT == PKV_KV_Q8_0) {
     uint4 va = *reinterpret_cast<const uint4*>(sc + TL::kScale + t0 * 8);
     uint4 vb = *reinterpret_cast<const uint4*>(sc + TL::kScale + (t0 + 8) * 8);
     if (slot_lo > 0 || slot_hi < kPage) {  // unattended slots: P = 0, scales may be NaN
@@ -600,7 +678,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint32_t dst = smem_addr(ring + s * TL::kCodes);
       const int z = pg * a.n_kv + hh;
       mbar_arrive_expect_tx(bar, TL::kTx);
-      if constexpr (DT != PKV_KV_Q8_0) {
+      if constexpr (DT == PKV_KV_F32) {  // four boxes of 32 dims per tile
+#pragma unroll
+        for (int bx = 0; bx < 4; ++bx) {
+          tma_load_3d(dst + bx * 2048, &maps.k, 32 * bx, 0, z, bar, policy);
+          tma_load_3d(dst + TL::kData + bx * 2048, &maps.v, 32 * bx, 0, z, bar, policy);
+        }
+      } else if constexpr (DT != PKV_KV_Q8_0) {
         tma_load_3d(dst, &maps.k, 0, 0, z, bar, policy);
         tma_load_3d(dst + 2048, &maps.k, 64, 0, z, bar, policy);
         tma_load_3d(dst + TL::kData, &maps.v, 0, 0, z, bar, policy);
@@ -623,6 +707,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   bool aborted = false;
   int consumed = 0;
   MqState<DT, NT> S;
+  S.qs = reinterpret_cast<float*>(smem + SM::kQ) + warp * kWarpCols * kQStride;  // f32 KV only
 
   int piece = 0;
   for (long long x = c_begin; x < c_end; ++piece) {
@@ -652,18 +737,41 @@ __global__ void __launch_bounds__(kThreads, 2)
     // the warp's slots of interest in any page: union of the pass's columns
     const int pos_lo = window_start(L - a.q_len + a.q0 + 1, a.window);
     const int pos_hi = L - a.q_len + a.q0 + a.nq;  // last query of the pass + 1
+    if constexpr (DT == PKV_KV_F32) {
+      // the pass's columns times scale * log2 e into the warp's buffer (zeros
+      // for unused columns): lane l writes dims 4l .. 4l + 3 of each
+      __syncwarp();  // the previous piece's reads are done
 #pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const int cq = 4 * t + (gid >> 1);  // the column whose query this lane loads
-      const float* qv = cq < nc
-                            ? a.q + ((static_cast<long long>(i) * a.q_len + a.q0 + cq / G) * a.n_q +
-                                     h * G + cq % G) * kD
-                            : nullptr;
-      int e2;
-      mq_load_column<DT>(qv, a.qscale, (gid & 1) != 0, tig, S.qb[t], e2);
-      S.qexp[t] = ldexpf(1.0f, __shfl_sync(kFull, e2, 8 * tig));  // lane 8 tig loads column 4t + tig
-      S.m[t] = -INFINITY;
-      S.l[t] = 0.f;
+      for (int c = 0; c < kWarpCols; ++c) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < nc)
+          x = __ldg(reinterpret_cast<const float4*>(
+                        a.q + ((static_cast<long long>(i) * a.q_len + a.q0 + c / G) * a.n_q + h * G +
+                               c % G) * kD) + lane);
+        *reinterpret_cast<float4*>(S.qs + c * kQStride + 4 * lane) =
+            make_float4(x.x * a.qscale, x.y * a.qscale, x.z * a.qscale, x.w * a.qscale);
+      }
+      __syncwarp();
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        S.qexp[t] = 1.0f;
+        S.m[t] = -INFINITY;
+        S.l[t] = 0.f;
+      }
+    } else {
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int cq = 4 * t + (gid >> 1);  // the column whose query this lane loads
+        const float* qv = cq < nc
+                              ? a.q + ((static_cast<long long>(i) * a.q_len + a.q0 + cq / G) * a.n_q +
+                                       h * G + cq % G) * kD
+                              : nullptr;
+        int e2;
+        mq_load_column<DT>(qv, a.qscale, (gid & 1) != 0, tig, S.qb[t], e2);
+        S.qexp[t] = ldexpf(1.0f, __shfl_sync(kFull, e2, 8 * tig));  // lane 8 tig: column 4t + tig
+        S.m[t] = -INFINITY;
+        S.l[t] = 0.f;
+      }
     }
 #pragma unroll
     for (int r = 0; r < 8; ++r)
@@ -1250,7 +1358,7 @@ static cudaError_t mq_occupancy_t(int rows, int* blocks) {
 template <int DT>
 static cudaError_t launch_mq_dt(int kind, const DecodeArgs& a, const TileMaps& maps, int chunks,
                                 cudaStream_t st) {
-  if constexpr (DT == PKV_KV_Q8_0) {
+  if constexpr (DT == PKV_KV_Q8_0 || DT == PKV_KV_F32) {
     return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
   } else {
     if (kind == kMqSingle) return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
@@ -1262,7 +1370,7 @@ static cudaError_t launch_mq_dt(int kind, const DecodeArgs& a, const TileMaps& m
 
 template <int DT>
 static cudaError_t occupancy_mq_dt(int kind, int rows, int* blocks) {
-  if constexpr (DT == PKV_KV_Q8_0) {
+  if constexpr (DT == PKV_KV_Q8_0 || DT == PKV_KV_F32) {
     return mq_occupancy_t<DT, kMqSingle>(rows, blocks);
   } else {
     if (kind == kMqSingle) return mq_occupancy_t<DT, kMqSingle>(rows, blocks);
@@ -1278,6 +1386,7 @@ cudaError_t launch_paged_decode_mq(int dtype, int group, const DecodeArgs& a, co
   const int kind = mq_kind(dtype, group, a.q_len);
   if (dtype == PKV_KV_F16) return launch_mq_dt<PKV_KV_F16>(kind, a, maps, chunks, st);
   if (dtype == PKV_KV_BF16) return launch_mq_dt<PKV_KV_BF16>(kind, a, maps, chunks, st);
+  if (dtype == PKV_KV_F32) return launch_mq_dt<PKV_KV_F32>(kind, a, maps, chunks, st);
   return launch_mq_dt<PKV_KV_Q8_0>(kind, a, maps, chunks, st);
 }
 
@@ -1286,6 +1395,7 @@ cudaError_t paged_decode_mq_blocks_per_sm(int dtype, int group, int q_len, int r
   const int kind = mq_kind(dtype, group, q_len);
   if (dtype == PKV_KV_F16) return occupancy_mq_dt<PKV_KV_F16>(kind, rows, blocks);
   if (dtype == PKV_KV_BF16) return occupancy_mq_dt<PKV_KV_BF16>(kind, rows, blocks);
+  if (dtype == PKV_KV_F32) return occupancy_mq_dt<PKV_KV_F32>(kind, rows, blocks);
   return occupancy_mq_dt<PKV_KV_Q8_0>(kind, rows, blocks);
 }
 

@@ -16,8 +16,8 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import (ATOL_STATED, BF16_NAN, F16_NAN, device_pool, encode_pool, host_arrays,
-                     tight_tol, to_dev)
+from helpers import (ATOL_STATED, BF16_NAN, F16_NAN, F32_NAN, device_pool, encode_pool,
+                     host_arrays, tight_tol, to_dev)
 from paged_kv_decode_09_gb300 import api
 from paged_kv_decode_09_gb300 import workloads as W
 
@@ -42,10 +42,10 @@ def _check(out, ref):
 
 
 def _poison(wl, host, positions_of_row):
-    """NaN into the slots positions_of_row(i, L) of every row (f16/bf16 data,
-    q8_0 scales)."""
+    """NaN into the slots positions_of_row(i, L) of every row (f16/bf16/f32
+    data, q8_0 scales)."""
     kd, vd, ks, vs = [None if a is None else a.copy() for a in host]
-    nan = {W.F16: F16_NAN, W.BF16: BF16_NAN}.get(wl.cfg.dtype)
+    nan = {W.F16: F16_NAN, W.BF16: BF16_NAN, W.F32: F32_NAN}.get(wl.cfg.dtype)
     for i, L in enumerate(wl.seq_lens):
         for t in positions_of_row(i, int(L)):
             page, slot = wl.block_table[i, t // W.PAGE], t % W.PAGE
@@ -82,7 +82,7 @@ def _attend(wl, pool, q, num_chunks=0, seq_lens=None):
     return out.cpu().numpy()
 
 
-@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16])
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16, W.F32])
 @pytest.mark.parametrize("q_len", [1, 2, 3, 5, 8, 13])
 @pytest.mark.parametrize("group", [1, 2, 4])
 def test_mq_matches_oracle(dtype, q_len, group):
@@ -95,7 +95,7 @@ def test_mq_matches_oracle(dtype, q_len, group):
     _check(out, _oracle(wl, host, q))
 
 
-@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16])
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16, W.F32])
 @pytest.mark.parametrize("q_len,window", [(1, 1), (2, 1), (4, 5), (8, 16), (3, 17), (8, 40),
                                           (13, 100), (5, 1000)])
 def test_mq_window_matches_oracle_and_skips_earlier_pages(dtype, q_len, window):
@@ -110,7 +110,7 @@ def test_mq_window_matches_oracle_and_skips_earlier_pages(dtype, q_len, window):
     _check(out, ref)
 
 
-@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16])
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16, W.F32])
 @pytest.mark.parametrize("q_len", [2, 3, 6])  # G = 4: 8, 12 and 24 columns (each kernel)
 def test_mq_split_invariance(dtype, q_len):
     wl = _wl(dtype, n_q=32, n_kv=8)
@@ -124,7 +124,7 @@ def test_mq_split_invariance(dtype, q_len):
         assert float(np.max(np.abs(o - outs[0]))) <= 1e-6
 
 
-@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16])
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16, W.F32])
 @pytest.mark.parametrize("q_len,window", [(1, 0), (4, 0), (7, 0), (8, 30)])
 def test_mq_decode_step_appends_then_attends(dtype, q_len, window):
     """pkv_decode_step_mq: the q_len new tokens of every row land bit-exact
@@ -182,7 +182,7 @@ def test_mq_short_row_reports_bad_length():
 
 
 @pytest.mark.parametrize("cfg_name,q_len", [("llama8b_f16", 4), ("llama8b_bf16", 3),
-                                            ("llama8b_q8_0", 2)])
+                                            ("llama8b_q8_0", 2), ("llama8b_f32", 5)])
 def test_mq_full_size(cfg_name, q_len):
     """The 8B shapes: every row of f16 and bf16, every fourth row of q8_0."""
     wl = W.draw(cfg_name)
@@ -211,13 +211,3 @@ def test_mq_validation():
         api.paged_decode_attention_mq(pool, 0, torch.zeros((wl.rows, 16, 128), device="cuda"),
                                       bt, sl, wl.scale)
 
-
-def test_mq_f32_pool_is_unsupported():
-    """Several queries per row are not built for f32 KV: a typed error, no launch."""
-    wl = _wl(W.F32, n_q=32, n_kv=8)
-    pool = device_pool(wl, encode_pool(wl))
-    q, _, _ = W.mq_inputs(wl, 2)
-    with pytest.raises(api.PkvError) as e:
-        api.paged_decode_attention_mq(pool, 0, to_dev(q), to_dev(wl.block_table),
-                                      to_dev(wl.seq_lens), wl.scale)
-    assert e.value.status == 2
