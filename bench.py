@@ -269,9 +269,12 @@ def run_ours(args, rank, world, local):
         if cfg.dtype in (W.Q8_0, W.F32) or cols <= (4 if cfg.dtype == W.BF16 else 8):
             width = min(cols, 8)
             kname = "paged_decode_mq_kernel"  # the warps of a CTA read different pages
-        else:
-            width = 16 if cfg.dtype == W.BF16 or cols <= 16 else 32
-            kname = "paged_decode_mqt_kernel"  # the four warps share every page
+        else:  # teams of 2 or 4 warps share every page
+            if cfg.dtype == W.BF16:
+                width = 8 if cols <= 8 else 16
+            else:
+                width = 16 if cols <= 16 else 32  # four warps of 4 or of 8 columns
+            kname = "paged_decode_mqt_kernel"
         passes = -(-QL // max(1, width // cfg.group))
     else:
         q, k_new, v_new = t(wl.q), t(wl.k_new), t(wl.v_new)

@@ -274,8 +274,10 @@ pkv_status pkv_decode_step(const pkv_pool *pool, int layer, const float *q, cons
  * the (query, query head) pairs of a KV head, C = q_len * G in all:
  *     C <= 8 (bf16: 4), and q8_0 and f32: passes of 8 pairs (bf16: 4), the
  *     CTA's warps reading different pages;
- *     otherwise passes of 16 pairs (C <= 16, and bf16) or 32 (f16), the
- *     CTA's four warps reading every page together, a quarter each;
+ *     otherwise teams of warps reading every page together, each warp a
+ *     share of the pairs: f16 passes of 16 (C <= 16) or 32 (four warps);
+ *     bf16 one pass for C <= 8 (two warps), passes of 16 beyond (four
+ *     warps);
  * each pass one launch on `stream`.  pkv_decode_step_mq stores the new tokens
  * in the first pass, just before their pages are read; the last q_len
  * positions' pages must not be shared with another row.

@@ -205,6 +205,7 @@ pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q, const
   a.q_len = 1;
   a.q0 = 0;
   a.nq = 1;
+  a.vchunks = num_chunks;
   a.out = out;
   a.part_ml = w.part_ml;
   a.part_acc = w.part_acc;
@@ -286,6 +287,7 @@ pkv_status attention_mq_impl(const pkv_pool* pool, int layer, const float* q, co
   a.qscale = scale * 1.4426950408889634f;  // log2(e): base-2 softmax
   a.window = pool->window[layer];
   a.q_len = q_len;
+  a.vchunks = num_chunks;
   a.out = out;
   a.status = pool->status;
   const pkv::TileMaps* maps = nullptr;

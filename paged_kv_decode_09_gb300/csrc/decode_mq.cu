@@ -42,22 +42,34 @@ __host__ __device__ constexpr int mq_tiles() {
 
 // The kernel a call takes, by its q_len * G (query, head) columns: up to 8
 // (bf16: 4) the warps of a CTA read different pages (paged_decode_mq_kernel);
-// beyond, the four warps read every page together (paged_decode_mqt_kernel,
-// 4 columns a warp up to 16, else 8), in passes of 16 or 32 columns.  q8_0
-// always takes the first, in passes of 8 columns: its pages are converted
-// from int8 codes by the warp that reads them, so four warps sharing a page
-// would convert it four times (measured slower than a second pass).  f32
-// pages (CUDA cores) take the first as well.
-enum MqKind { kMqSingle = 0, kMqTeam1 = 1, kMqTeam2 = 2 };
+// beyond, teams of warps read every page together (paged_decode_mqt_kernel):
+// f16 four warps of 4 columns up to 16, four of 8 beyond (passes of 32); bf16
+// (4 columns a warp) two warps up to 8 columns, four beyond (passes of 16), so
+// that no warp of a team idles.  (f16 pairs of 8-column warps were measured
+// slower than four warps of 4 columns: fewer warps per page leave the page's
+// latency chain exposed.)  q8_0 always takes the first, in
+// passes of 8 columns: its pages are converted from int8 codes by the warp
+// that reads them, so warps sharing a page would convert it several times
+// (measured slower than a second pass).  f32 pages (CUDA cores) take the
+// first as well.
+enum MqKind { kMqSingle = 0, kMqPair1, kMqTeam1, kMqTeam2 };
 static int mq_kind(int dtype, int group, int q_len) {
   const int cols = q_len * group;
   if (dtype == PKV_KV_Q8_0 || dtype == PKV_KV_F32) return kMqSingle;
-  if (dtype == PKV_KV_BF16) return cols <= 4 ? kMqSingle : kMqTeam1;
+  if (dtype == PKV_KV_BF16) return cols <= 4 ? kMqSingle : cols <= 8 ? kMqPair1 : kMqTeam1;
   return cols <= 8 ? kMqSingle : cols <= 16 ? kMqTeam1 : kMqTeam2;
 }
 static int mq_kind_cols(int dtype, int kind) {
-  return kind == kMqSingle ? (dtype == PKV_KV_BF16 ? 4 : 8) : kind == kMqTeam1 ? 16 : 32;
+  switch (kind) {
+    case kMqSingle: return dtype == PKV_KV_BF16 ? 4 : 8;
+    case kMqPair1: return 8;
+    case kMqTeam1: return 16;
+    default: return 32;
+  }
 }
+// score n-tiles (4 columns each) of a warp, and warps per page, of a kind
+__host__ __device__ constexpr int kind_nt(int kind) { return kind == kMqTeam2 ? 2 : 1; }
+__host__ __device__ constexpr int kind_ts(int kind) { return kind == kMqPair1 ? 2 : 4; }
 
 int mq_pass_queries(int dtype, int group, int q_len) {
   const int per = mq_kind_cols(dtype, mq_kind(dtype, group, q_len)) / group;
@@ -953,19 +965,26 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 // -------------------------------------------------- shared-page kernel ----
-// With more than 8 (query, head) columns in a pass (more than 4 for bf16) the
-// four warps of a CTA read every page of the chunk together, warp w taking
-// columns [w CW, (w + 1) CW): a page is copied once for up to 4 CW columns.
-// The stages form one ring per CTA.  Unit v (the chunk's v-th page) is copied
-// by warp v mod 4 into stage v mod (stages), once all four warps have read
-// the unit that stage held before (an empty barrier of four arrivals).  Each
-// warp holds whole columns, so a piece end needs no merge inside the CTA: a
-// warp writes its columns (to the output, or to its workspace slot) and the
-// last piece of the segment to arrive for those columns merges them.
-// Stages of the CTA's ring, a multiple of kWarps (unit v + stages has v's
-// copier): as many as the shared memory of the CTAs an SM holds allows
-// (3 CTAs with 4 columns a warp, 2 with 8).
-__host__ __device__ constexpr int team_stages(int nt) { return nt == 1 ? 8 : 12; }
+// With more than 8 (query, head) columns in a pass (more than 4 for bf16) a
+// team of TS warps (2 or 4) reads every page of its chunk together, warp w of
+// the team taking columns [w CW, (w + 1) CW): a page is copied once for up to
+// TS * CW columns.  A CTA holds 4 / TS teams, each with its own chunk (chunk
+// b * teams + team of the a.vchunks) and its own ring of stages.  Unit v of
+// a team's chunk is copied by its warp v mod TS into the team's stage v mod
+// (stages), once all TS warps have read the unit that stage held before (an
+// empty barrier of TS arrivals).  Each warp holds whole columns, so a piece
+// end needs no merge inside the CTA: a warp writes its columns (to the output,
+// or to its workspace slot) and the last piece of the segment to arrive for
+// those columns merges them.
+// CTAs per SM of the kernel with 8 columns a warp (4 columns a warp: 3).
+#ifndef PKV_MQT2_CTAS
+#define PKV_MQT2_CTAS 3
+#endif
+__host__ __device__ constexpr int team_ctas(int nt) { return nt == 1 ? 3 : PKV_MQT2_CTAS; }
+// Stages of a CTA (its teams' rings together, each a multiple of the team's
+// warps: unit v + stages has v's copier): as many as the shared memory of the
+// CTAs an SM holds allows.
+__host__ __device__ constexpr int team_stages(int nt) { return team_ctas(nt) == 3 ? 8 : 12; }
 
 template <int DT, int kStages>
 struct MqtSmem {
@@ -978,36 +997,43 @@ struct MqtSmem {
   static size_t bytes(int rows) { return kAlign + kRows + (2 * static_cast<size_t>(rows) + 1) * 4; }
 };
 
-template <int DT, int NT>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2)
+template <int DT, int NT, int TS>
+__global__ void __launch_bounds__(kThreads, team_ctas(NT))
     paged_decode_mqt_kernel(const __grid_constant__ DecodeArgs a,
                             const __grid_constant__ TileMaps maps) {
   using TL = Tiles<DT>;
-  constexpr int RS = team_stages(NT);
+  constexpr int RS = team_stages(NT);  // stages of the CTA
   using SM = MqtSmem<DT, RS>;
-  constexpr int CW = 4 * NT;  // columns of one warp
-  static_assert(RS % kWarps == 0, "a unit and the unit RS later have the same copier");
+  constexpr int kTeams = kWarps / TS;
+  constexpr int RT = RS / kTeams;      // stages of a team
+  constexpr int CW = 4 * NT;           // columns of one warp
+  static_assert(RT % TS == 0, "a unit and the unit RT later have the same copier");
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((SM::kAlign - (smem_addr(smem_raw) & (SM::kAlign - 1))) &
                               (SM::kAlign - 1));
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
+  const int team = warp / TS, wt = warp % TS;          // team, and warp within it
   volatile int* ctl = reinterpret_cast<volatile int*>(smem + SM::kCtl);  // [0] abort
   int* row_start = reinterpret_cast<int*>(smem + SM::kRows);
   int* lens = row_start + a.num_rows + 1;
-  const uint32_t full0 = smem_addr(smem + SM::kFull), empty0 = smem_addr(smem + SM::kEmpty);
+  const uint32_t full0 = smem_addr(smem + SM::kFull) + team * RT * 8;    // the team's barriers
+  const uint32_t empty0 = smem_addr(smem + SM::kEmpty) + team * RT * 8;
+  uint8_t* ring = smem + static_cast<size_t>(team) * RT * TL::kCodes;    // and stages
+  uint8_t* ring_sc = smem + SM::kScl + static_cast<size_t>(team) * RT * TL::kScales;
   const int G = a.n_q / a.n_kv;
   const int nc = a.nq * G;                             // columns of this pass
-  const int cbase = warp * CW;                         // this warp's first column
+  const int cbase = wt * CW;                           // this warp's first column
   const int ncw = min(max(nc - cbase, 0), CW);         // and how many it has
   const int plan_window = a.window > 0 ? a.window + a.q_len - 1 : 0;
 
   if (threadIdx.x == 0) {
     ctl[0] = 0;
+    const uint32_t f = smem_addr(smem + SM::kFull), e = smem_addr(smem + SM::kEmpty);
     for (int s = 0; s < RS; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, kWarps);
+      mbar_init(f + 8 * s, 1);
+      mbar_init(e + 8 * s, TS);
     }
     fence_mbar_init();
   }
@@ -1017,11 +1043,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2)
             blockIdx.x == 0 ? a.status : nullptr, lens, row_start, a.q_len);
 
   const long long T = static_cast<long long>(a.n_kv) * row_start[a.num_rows];
-  const int C = used_chunks(T, gridDim.x), k = blockIdx.x;
+  const int C = used_chunks(T, a.vchunks), k = blockIdx.x * kTeams + team;
   const long long c_begin = k < C ? static_cast<long long>(k) * T / C : T;
   const long long c_end = k < C ? static_cast<long long>(k + 1) * T / C : T;
 
-  if (k == 0) {  // rows without tokens (or shorter than q_len): zeros
+  if (blockIdx.x == 0) {  // rows without tokens (or shorter than q_len): zeros
     for (int i = 0; i < a.num_rows; ++i)
       if (row_start[i + 1] == row_start[i])
         for (int jj = 0; jj < a.nq; ++jj)
@@ -1030,15 +1056,15 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2)
   }
 
   const int n_units = static_cast<int>(c_end - c_begin);
-  // this warp copies the units v = warp + 4 u (u = 0, 1, ...)
-  const long long first = c_begin + warp;
-  const int n_mine = first < c_end ? static_cast<int>((c_end - first + kWarps - 1) / kWarps) : 0;
+  // this warp copies the units v = wt + TS u (u = 0, 1, ...) of its team's chunk
+  const long long first = c_begin + wt;
+  const int n_mine = first < c_end ? static_cast<int>((c_end - first + TS - 1) / TS) : 0;
 
   auto fetch = [&](int base, int& pg, int& hh, int& row, int& pidx) {
     const int u = base + lane;
     pg = hh = row = pidx = 0;
     if (u < n_mine) {
-      const long long x = first + static_cast<long long>(u) * kWarps;
+      const long long x = first + static_cast<long long>(u) * TS;
       const int i = row_of(row_start, a.num_rows, a.n_kv, x);
       const int npg = row_start[i + 1] - row_start[i];
       const int off = static_cast<int>(x - static_cast<long long>(a.n_kv) * row_start[i]);
@@ -1063,7 +1089,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2)
   int issued = 0;  // units this warp has copied
   const uint64_t policy = policy_evict_first();
 
-  auto issue = [&]() {  // this warp's next unit, v = warp + 4 issued
+  auto issue = [&]() {  // this warp's next unit, v = wt + TS issued
     const int u = issued;
     if (u >= batch + 32) {
       c_pg = n_pg;
@@ -1088,9 +1114,9 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (lane == 0) {
-      const int s = (warp + kWarps * u) % RS;
+      const int s = (wt + TS * u) % RT;
       const uint32_t bar = full0 + 8 * s;
-      const uint32_t dst = smem_addr(smem + s * TL::kCodes);
+      const uint32_t dst = smem_addr(ring + s * TL::kCodes);
       const int z = pg * a.n_kv + hh;
       mbar_arrive_expect_tx(bar, TL::kTx);
       if constexpr (DT != PKV_KV_Q8_0) {
@@ -1099,7 +1125,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2)
         tma_load_3d(dst + TL::kData, &maps.v, 0, 0, z, bar, policy);
         tma_load_3d(dst + TL::kData + 2048, &maps.v, 64, 0, z, bar, policy);
       } else {
-        const uint32_t sdst = smem_addr(smem + SM::kScl + s * TL::kScales);
+        const uint32_t sdst = smem_addr(ring_sc + s * TL::kScales);
         const size_t unit = static_cast<size_t>(z);
         tma_load_3d(dst, &maps.k, 0, 0, z, bar, policy);
         bulk_g2s(sdst, a.k_scales + unit * TL::kScale, TL::kScale, bar, policy);
@@ -1109,7 +1135,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2)
     }
     ++issued;
   };
-  while (issued < n_mine && warp + kWarps * issued < RS) issue();
+  while (issued < n_mine && wt + TS * issued < RT) issue();
 
   bool aborted = false;
   int consumed = 0;  // units [0, consumed) have landed (this warp waited for them)
@@ -1171,8 +1197,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2)
 
     for (long long pos = x; pos < b; ++pos) {
       const int v = static_cast<int>(pos - c_begin);
-      const int s = v % RS;
-      bool ok = !aborted && mbar_wait_bounded(full0 + 8 * s, (v / RS) & 1, ctl);
+      const int s = v % RT;
+      bool ok = !aborted && mbar_wait_bounded(full0 + 8 * s, (v / RT) & 1, ctl);
       ok = __all_sync(kFull, ok);
       if (!ok) {
         fail();
@@ -1182,14 +1208,14 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2)
       if (ncw > 0) {
         const int pf = (p0 + static_cast<int>(pos - seg_start)) * kPage;  // page's first token
         const int slot_lo = max(0, pos_lo - pf), slot_hi = min(kPage, pos_hi - pf);
-        mq_process_unit<DT, NT>(smem + s * TL::kCodes, smem + SM::kScl + s * TL::kScales, pf,
-                                col_lo, col_hi, slot_lo, slot_hi, ncw, lane, S);
+        mq_process_unit<DT, NT>(ring + s * TL::kCodes, ring_sc + s * TL::kScales, pf, col_lo,
+                                col_hi, slot_lo, slot_hi, ncw, lane, S);
       }
-      // done with the stage; its unit's copier refills it with unit v + RS
+      // done with the stage; its unit's copier refills it with unit v + RT
       __syncwarp();
       if (lane == 0) mbar_arrive(empty0 + 8 * s);
-      if ((v & (kWarps - 1)) == warp && v + RS < n_units) {
-        bool e_ok = mbar_wait_bounded(empty0 + 8 * s, (v / RS) & 1, ctl);
+      if (v % TS == wt && v + RT < n_units) {
+        bool e_ok = mbar_wait_bounded(empty0 + 8 * s, (v / RT) & 1, ctl);
         e_ok = __all_sync(kFull, e_ok);
         if (!e_ok) {
           fail();
@@ -1263,14 +1289,14 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2)
         int last = 0;
         if (lane == 0) {
           __threadfence();  // the warp's partial (ordered by __syncwarp) before its arrival
-          last = atomicAdd(a.counters + j * kWarps + warp, 1) == k1 - k0;
+          last = atomicAdd(a.counters + j * kMqCounters + wt, 1) == k1 - k0;
         }
         last = __shfl_sync(kFull, last, 0);
         if (last) {
           __threadfence();
           mq_merge_segment_warp<CW, NT == 1 ? 2 : 1>(a.part_ml, a.part_acc, j, k0, k1, cbase, nc,
                                                      out_col, lane);
-          if (lane == 0) a.counters[j * kWarps + warp] = 0;  // ready for the next call
+          if (lane == 0) a.counters[j * kMqCounters + wt] = 0;  // ready for the next call
         }
       }
     }
@@ -1281,8 +1307,8 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 3 : 2)
   if (aborted || ctl[0]) {
     const int zero = 0;
     for (int u = 0; u < issued; ++u) {
-      const int v = warp + kWarps * u;
-      if (v >= consumed) mbar_wait_bounded(full0 + 8 * (v % RS), (v / RS) & 1, &zero);
+      const int v = wt + TS * u;
+      if (v >= consumed) mbar_wait_bounded(full0 + 8 * (v % RT), (v / RT) & 1, &zero);
     }
   }
 }
@@ -1305,18 +1331,20 @@ static cudaError_t mq_ensure_smem(K kernel, std::atomic<size_t> (&granted)[64], 
   return e;
 }
 
-// The kernel of (dtype, kind) and its dynamic shared memory for `rows` rows.
+// The kernel of (dtype, kind), its dynamic shared memory for `rows` rows and
+// the chunks one CTA holds.
 template <int DT, int KIND>
 struct MqKernel {
+  static constexpr int kTeams = KIND == kMqSingle ? 1 : kWarps / kind_ts(KIND);
   static auto fn() {
     if constexpr (KIND == kMqSingle)
       return paged_decode_mq_kernel<DT>;
     else
-      return paged_decode_mqt_kernel<DT, KIND == kMqTeam1 ? 1 : 2>;
+      return paged_decode_mqt_kernel<DT, kind_nt(KIND), kind_ts(KIND)>;
   }
   static size_t smem(int rows) {
     return KIND == kMqSingle ? MqSmem<DT>::bytes(rows)
-                             : MqtSmem<DT, team_stages(KIND == kMqTeam1 ? 1 : 2)>::bytes(rows);
+                             : MqtSmem<DT, team_stages(kind_nt(KIND))>::bytes(rows);
   }
   static cudaError_t prepare(size_t smem) {
     static std::atomic<size_t> granted[64];
@@ -1332,7 +1360,7 @@ static cudaError_t launch_mq_t(const DecodeArgs& a, const TileMaps& maps, int ch
   cudaError_t e = K::prepare(smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(chunks);
+  cfg.gridDim = dim3((chunks + K::kTeams - 1) / K::kTeams);  // a CTA holds kTeams chunks
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
@@ -1346,13 +1374,16 @@ static cudaError_t launch_mq_t(const DecodeArgs& a, const TileMaps& maps, int ch
   return cudaGetLastError();
 }
 
+// Chunks per SM: resident CTAs times the chunks a CTA holds.
 template <int DT, int KIND>
 static cudaError_t mq_occupancy_t(int rows, int* blocks) {
   using K = MqKernel<DT, KIND>;
   const size_t smem = K::smem(rows);
   cudaError_t e = K::prepare(smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, K::fn(), kThreads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, K::fn(), kThreads, smem);
+  *blocks *= K::kTeams;
+  return e;
 }
 
 template <int DT>
@@ -1360,11 +1391,14 @@ static cudaError_t launch_mq_dt(int kind, const DecodeArgs& a, const TileMaps& m
                                 cudaStream_t st) {
   if constexpr (DT == PKV_KV_Q8_0 || DT == PKV_KV_F32) {
     return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
+  } else if constexpr (DT == PKV_KV_BF16) {
+    if (kind == kMqSingle) return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
+    if (kind == kMqPair1) return launch_mq_t<DT, kMqPair1>(a, maps, chunks, st);
+    return launch_mq_t<DT, kMqTeam1>(a, maps, chunks, st);
   } else {
     if (kind == kMqSingle) return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
-    if constexpr (DT == PKV_KV_F16)
-      if (kind == kMqTeam2) return launch_mq_t<DT, kMqTeam2>(a, maps, chunks, st);
-    return launch_mq_t<DT, kMqTeam1>(a, maps, chunks, st);
+    if (kind == kMqTeam1) return launch_mq_t<DT, kMqTeam1>(a, maps, chunks, st);
+    return launch_mq_t<DT, kMqTeam2>(a, maps, chunks, st);
   }
 }
 
@@ -1372,11 +1406,14 @@ template <int DT>
 static cudaError_t occupancy_mq_dt(int kind, int rows, int* blocks) {
   if constexpr (DT == PKV_KV_Q8_0 || DT == PKV_KV_F32) {
     return mq_occupancy_t<DT, kMqSingle>(rows, blocks);
+  } else if constexpr (DT == PKV_KV_BF16) {
+    if (kind == kMqSingle) return mq_occupancy_t<DT, kMqSingle>(rows, blocks);
+    if (kind == kMqPair1) return mq_occupancy_t<DT, kMqPair1>(rows, blocks);
+    return mq_occupancy_t<DT, kMqTeam1>(rows, blocks);
   } else {
     if (kind == kMqSingle) return mq_occupancy_t<DT, kMqSingle>(rows, blocks);
-    if constexpr (DT == PKV_KV_F16)
-      if (kind == kMqTeam2) return mq_occupancy_t<DT, kMqTeam2>(rows, blocks);
-    return mq_occupancy_t<DT, kMqTeam1>(rows, blocks);
+    if (kind == kMqTeam1) return mq_occupancy_t<DT, kMqTeam1>(rows, blocks);
+    return mq_occupancy_t<DT, kMqTeam2>(rows, blocks);
   }
 }
 

@@ -32,6 +32,7 @@ struct DecodeArgs {
   int window;    // > 0: each row attends to its last `window` tokens
   int q_len;     // queries (new tokens) per row; q, out [rows][q_len][n_q][128]
   int q0, nq;    // several-query kernel: this pass's queries q0 .. q0 + nq - 1
+  int vchunks;   // chunks of the work split (several-query kernels: a CTA may hold 2)
   float* out;
   float* part_ml;   // [slots][G][2]
   float* part_acc;  // [slots][G][128]
