@@ -53,7 +53,7 @@ def parse_args():
     p.add_argument("--layers", type=int, default=0, help="layer pools to rotate (0: auto)")
     p.add_argument("--chunks", type=int, default=0, help="work chunks (0: one per resident CTA)")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--cpu-seconds", type=float, default=15.0, help="CPU baseline budget")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU baseline budget")
     p.add_argument("--window", type=int, default=0,
                    help="sliding window of every layer (0: none); bytes count attended tokens")
     p.add_argument("--no-graph", action="store_true",
@@ -531,7 +531,8 @@ def run_kernel(args, local):
 
 
 def cpu_baseline(wl, pool, budget_s, window=0, q_len=1, q=None):
-    """The FP64 oracle, as it stands, on a bounded sample of rows of layer 0."""
+    """The FP64 oracle, as it stands, on a bounded sample of the batch of layer
+    0: on all the host's cores (the reported value) and on one core."""
     import numpy as np
     import torch
 
@@ -548,31 +549,64 @@ def cpu_baseline(wl, pool, budget_s, window=0, q_len=1, q=None):
         kd, vd = pool.k_data[0].cpu().numpy(), pool.v_data[0].cpu().numpy()
         ks = pool.k_scales[0].cpu().view(torch.int16).numpy().view(np.uint16)
         vs = pool.v_scales[0].cpu().view(torch.int16).numpy().view(np.uint16)
-    order = np.argsort(wl.seq_lens)  # shortest rows first, to bound the sample
-    done, secs, rows = 0, 0.0, []
-    for i in order:
-        t0 = time.perf_counter()
-        if q_len > 1:
-            O.decode_attention_mq(cfg.dtype, q[i:i + 1], kd, vd, ks, vs, wl.block_table[i:i + 1],
-                                  wl.seq_lens[i:i + 1], wl.num_pages, cfg.n_kv_heads, wl.scale,
-                                  window=window)
-        else:
-            O.decode_attention(cfg.dtype, wl.q[i:i + 1], kd, vd, ks, vs, wl.block_table[i:i + 1],
-                               wl.seq_lens[i:i + 1], wl.num_pages, cfg.n_kv_heads, wl.scale,
-                               window=window)
-        secs += time.perf_counter() - t0
-        rows.append(int(i))
-        done += row_tokens(int(wl.seq_lens[i]), window, q_len)
-        if secs > budget_s:
-            break
     per_elem = bytes_per_value(cfg.dtype)
-    nbytes = done * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem + \
-        2 * len(rows) * q_len * cfg.n_q_heads * 128 * 4
-    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": O.num_threads(),
-            "kind": "oracle",
-            "sample": f"{len(rows)} of {wl.rows} rows ({done} attended tokens) of one layer, "
-                      f"attention only, {secs:.1f} s",
-            "rows_tokens_per_s": round(done / secs, 1)}
+
+    def sample(budget):
+        # shortest rows first; the batch is cycled until the budget is spent,
+        # stopping on a whole pass once half of it is
+        order = np.argsort(wl.seq_lens)
+        done, secs, rows = 0, 0.0, 0
+        for n in range(1 << 30):
+            if n >= len(order) and n % len(order) == 0 and secs > 0.5 * budget:
+                break
+            i = order[n % len(order)]
+            t0 = time.perf_counter()
+            if q_len > 1:
+                O.decode_attention_mq(cfg.dtype, q[i:i + 1], kd, vd, ks, vs,
+                                      wl.block_table[i:i + 1], wl.seq_lens[i:i + 1], wl.num_pages,
+                                      cfg.n_kv_heads, wl.scale, window=window)
+            else:
+                O.decode_attention(cfg.dtype, wl.q[i:i + 1], kd, vd, ks, vs,
+                                   wl.block_table[i:i + 1], wl.seq_lens[i:i + 1], wl.num_pages,
+                                   cfg.n_kv_heads, wl.scale, window=window)
+            secs += time.perf_counter() - t0
+            rows += 1
+            done += row_tokens(int(wl.seq_lens[i]), window, q_len)
+            if secs > budget:
+                break
+        nbytes = done * cfg.n_kv_heads * cfg.head_dim * 2 * per_elem + \
+            2 * rows * q_len * cfg.n_q_heads * 128 * 4
+        what = (f"{rows} of {wl.rows} rows" if rows < wl.rows
+                else f"{rows / wl.rows:g} passes over the {wl.rows} rows")
+        return nbytes / secs / 1e9, done / secs, f"{what} ({done} attended tokens), {secs:.1f} s"
+
+    cores = O.num_threads()
+    value, tps, text = sample(0.7 * budget_s)
+    O.set_num_threads(1)
+    try:
+        value1, tps1, text1 = sample(0.3 * budget_s)
+    finally:
+        O.set_num_threads(cores)
+    return {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{text} of one layer, attention only",
+            "rows_tokens_per_s": round(tps, 1),
+            "single_core": {"value": round(value1, 4), "unit": "GB/s", "cores": 1,
+                            "sample": f"{text1} of one layer, attention only",
+                            "rows_tokens_per_s": round(tps1, 1)},
+            "cpu": cpu_model()}
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (or architecture) as the system reports it."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.machine()
 
 
 # ------------------------------------------------------------- reference ----

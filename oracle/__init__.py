@@ -51,6 +51,8 @@ def lib():
             path = os.environ.get("PKV_ORACLE_LIB") or _build.build()
             L = ctypes.CDLL(path)
             L.oracle_num_threads.restype = _i
+            L.oracle_set_num_threads.argtypes = [_i]
+            L.oracle_set_num_threads.restype = None
             L.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
             L.oracle_f16_to_f64.restype = ctypes.c_double
             L.oracle_f16_from_f32.argtypes = [ctypes.c_float]
@@ -97,6 +99,11 @@ def lib():
 def num_threads() -> int:
     """Threads the oracle's parallel loop uses (OpenMP), 1 without OpenMP."""
     return lib().oracle_num_threads()
+
+
+def set_num_threads(n: int):
+    """Threads for the oracle's parallel loops from now on (timing only)."""
+    lib().oracle_set_num_threads(int(n))
 
 
 def _ptr(a):

@@ -79,6 +79,16 @@ int oracle_num_threads(void) {
 #endif
 }
 
+/* Threads for the following parallel loops (timing only: results do not
+ * depend on it, every output element is computed by one thread). */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------ f16 --- */
 
 /* Exact value of an IEEE binary16 bit pattern, widened to double.
