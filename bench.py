@@ -266,14 +266,14 @@ def run_ours(args, rank, world, local):
         q, k_new, v_new = t(hq_np), t(hk_np), t(hv_np)
         ws = api.WorkspaceMQ(pool, cfg.n_q_heads, wl.rows, QL, args.chunks)
         cols = QL * cfg.group  # (query, head) columns; the kernel's pass width follows them
-        if cfg.dtype in (W.Q8_0, W.F32) or cols <= (4 if cfg.dtype == W.BF16 else 8):
+        if cfg.dtype == W.F32 or cols <= (4 if cfg.dtype == W.BF16 else 8):
             width = min(cols, 8)
             kname = "paged_decode_mq_kernel"  # the warps of a CTA read different pages
         else:  # teams of 2 or 4 warps share every page
             if cfg.dtype == W.BF16:
                 width = 8 if cols <= 8 else 16
-            else:
-                width = 16 if cols <= 16 else 32  # four warps of 4 or of 8 columns
+            else:  # f16: four warps of 4 or 8 columns; q8_0: two or four of 8
+                width = 16 if cols <= 16 else 32
             kname = "paged_decode_mqt_kernel"
         passes = -(-QL // max(1, width // cfg.group))
     else:

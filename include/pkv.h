@@ -272,12 +272,12 @@ pkv_status pkv_decode_step(const pkv_pool *pool, int layer, const float *q, cons
  * (all of [0, L) without a window), split into chunks as in
  * paged_decode_attention.  Every page is read once per pass; a pass carries
  * the (query, query head) pairs of a KV head, C = q_len * G in all:
- *     C <= 8 (bf16: 4), and q8_0 and f32: passes of 8 pairs (bf16: 4), the
- *     CTA's warps reading different pages;
+ *     C <= 8 (bf16: 4), and f32: passes of 8 pairs (bf16: 4), the CTA's
+ *     warps reading different pages;
  *     otherwise teams of warps reading every page together, each warp a
  *     share of the pairs: f16 passes of 16 (C <= 16) or 32 (four warps);
- *     bf16 one pass for C <= 8 (two warps), passes of 16 beyond (four
- *     warps);
+ *     q8_0 passes of 16 (C <= 16, two warps) or 32 (four warps); bf16 one
+ *     pass for C <= 8 (two warps), passes of 16 beyond (four warps);
  * each pass one launch on `stream`.  pkv_decode_step_mq stores the new tokens
  * in the first pass, just before their pages are read; the last q_len
  * positions' pages must not be shared with another row.

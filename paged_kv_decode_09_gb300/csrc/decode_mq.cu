@@ -52,10 +52,11 @@ __host__ __device__ constexpr int mq_tiles() {
 // that reads them, so warps sharing a page would convert it several times
 // (measured slower than a second pass).  f32 pages (CUDA cores) take the
 // first as well.
-enum MqKind { kMqSingle = 0, kMqPair1, kMqTeam1, kMqTeam2 };
+enum MqKind { kMqSingle = 0, kMqPair1, kMqPair2, kMqTeam1, kMqTeam2 };
 static int mq_kind(int dtype, int group, int q_len) {
   const int cols = q_len * group;
-  if (dtype == PKV_KV_Q8_0 || dtype == PKV_KV_F32) return kMqSingle;
+  if (dtype == PKV_KV_F32) return kMqSingle;
+  if (dtype == PKV_KV_Q8_0) return cols <= 8 ? kMqSingle : cols <= 16 ? kMqPair2 : kMqTeam2;
   if (dtype == PKV_KV_BF16) return cols <= 4 ? kMqSingle : cols <= 8 ? kMqPair1 : kMqTeam1;
   return cols <= 8 ? kMqSingle : cols <= 16 ? kMqTeam1 : kMqTeam2;
 }
@@ -63,13 +64,17 @@ static int mq_kind_cols(int dtype, int kind) {
   switch (kind) {
     case kMqSingle: return dtype == PKV_KV_BF16 ? 4 : 8;
     case kMqPair1: return 8;
-    case kMqTeam1: return 16;
+    case kMqPair2: case kMqTeam1: return 16;
     default: return 32;
   }
 }
 // score n-tiles (4 columns each) of a warp, and warps per page, of a kind
-__host__ __device__ constexpr int kind_nt(int kind) { return kind == kMqTeam2 ? 2 : 1; }
-__host__ __device__ constexpr int kind_ts(int kind) { return kind == kMqPair1 ? 2 : 4; }
+__host__ __device__ constexpr int kind_nt(int kind) {
+  return kind == kMqTeam2 || kind == kMqPair2 ? 2 : 1;
+}
+__host__ __device__ constexpr int kind_ts(int kind) {
+  return kind == kMqPair1 || kind == kMqPair2 ? 2 : 4;
+}
 
 int mq_pass_queries(int dtype, int group, int q_len) {
   const int per = mq_kind_cols(dtype, mq_kind(dtype, group, q_len)) / group;
@@ -1389,8 +1394,12 @@ static cudaError_t mq_occupancy_t(int rows, int* blocks) {
 template <int DT>
 static cudaError_t launch_mq_dt(int kind, const DecodeArgs& a, const TileMaps& maps, int chunks,
                                 cudaStream_t st) {
-  if constexpr (DT == PKV_KV_Q8_0 || DT == PKV_KV_F32) {
+  if constexpr (DT == PKV_KV_F32) {
     return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
+  } else if constexpr (DT == PKV_KV_Q8_0) {
+    if (kind == kMqSingle) return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
+    if (kind == kMqPair2) return launch_mq_t<DT, kMqPair2>(a, maps, chunks, st);
+    return launch_mq_t<DT, kMqTeam2>(a, maps, chunks, st);
   } else if constexpr (DT == PKV_KV_BF16) {
     if (kind == kMqSingle) return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
     if (kind == kMqPair1) return launch_mq_t<DT, kMqPair1>(a, maps, chunks, st);
@@ -1404,8 +1413,12 @@ static cudaError_t launch_mq_dt(int kind, const DecodeArgs& a, const TileMaps& m
 
 template <int DT>
 static cudaError_t occupancy_mq_dt(int kind, int rows, int* blocks) {
-  if constexpr (DT == PKV_KV_Q8_0 || DT == PKV_KV_F32) {
+  if constexpr (DT == PKV_KV_F32) {
     return mq_occupancy_t<DT, kMqSingle>(rows, blocks);
+  } else if constexpr (DT == PKV_KV_Q8_0) {
+    if (kind == kMqSingle) return mq_occupancy_t<DT, kMqSingle>(rows, blocks);
+    if (kind == kMqPair2) return mq_occupancy_t<DT, kMqPair2>(rows, blocks);
+    return mq_occupancy_t<DT, kMqTeam2>(rows, blocks);
   } else if constexpr (DT == PKV_KV_BF16) {
     if (kind == kMqSingle) return mq_occupancy_t<DT, kMqSingle>(rows, blocks);
     if (kind == kMqPair1) return mq_occupancy_t<DT, kMqPair1>(rows, blocks);
