@@ -7,20 +7,28 @@
 // A row of L tokens whose last q_len are new has one query per new token:
 // query j sits at position P = L - q_len + j and attends causally to
 // [max(0, P + 1 - W), P + 1) under a window W (all of [0, P + 1) without
-// one).  Every (row, KV head) page is read once per pass for all the pass's
-// queries: a pass carries up to 8 (query, head) columns (f16, q8_0; 4 for
-// bf16), so a step with q_len * G larger than that takes several passes over
-// the same plan, each reading the pages again.  The new tokens are appended
-// in the first pass, by the warp that reads their page, before its copy.
+// one).  The (query, query head) pairs of a KV head are the "columns" of a
+// call, C = q_len * G of them; each page of a (row, KV head) is read once per
+// pass for all the pass's columns, and a call takes as many passes as its
+// kernel's pass width requires (below).  The new tokens are stored in the
+// first pass, by the warp that copies their page, just before the copy.
 //
-// The work split, the warps' rings, the tensor copies and the merges are the
-// single-query kernel's (decode.cu); what differs is the page's MMA layout:
-//   scores: S[16 tokens][cols] = K Q^T as there, with the columns split over
-//     NT score n-tiles of 4 (query, head) columns x {hi, lo} parts; lane
-//     4 gid + tig ends with the scores of columns tig and 4 + tig.
+// Two kernels:
+//   paged_decode_mq_kernel: the single-query kernel's structure (decode.cu):
+//     the four warps of a CTA stream different pages of its chunk, each for
+//     all (up to 8) columns, and merge their states at piece ends.
+//   paged_decode_mqt_kernel: a team of 2 or 4 warps streams every page of
+//     its chunk together, each warp owning a share of the columns (up to 32
+//     in all), so a page is copied once for all of them.
+// The page's MMA layout is the same in both:
+//   scores: S[16 tokens][cols] = K Q^T as in the single-query kernel, with
+//     the columns split over NT score n-tiles of 4 (query, head) columns x
+//     {hi, lo} parts; lane 4 gid + tig ends with the scores of columns tig
+//     and 4 + tig.
 //   values: O^T[128 dims][cols] += V^T P^T with one B operand per part of P
 //     (two MMAs into the same accumulator), so the 8 columns of an n-tile are
 //     8 (query, head) pairs and O stays 32 registers a lane.
+// f32 pages run the same lanes on CUDA cores (as in the single-query kernel).
 // A query whose causal range does not reach a page sees only masked scores
 // there: its probabilities are 0 and its running state is left alone.
 #include <atomic>
@@ -40,18 +48,19 @@ __host__ __device__ constexpr int mq_tiles() {
   return DT == PKV_KV_BF16 ? 1 : 2;
 }
 
-// The kernel a call takes, by its q_len * G (query, head) columns: up to 8
-// (bf16: 4) the warps of a CTA read different pages (paged_decode_mq_kernel);
-// beyond, teams of warps read every page together (paged_decode_mqt_kernel):
-// f16 four warps of 4 columns up to 16, four of 8 beyond (passes of 32); bf16
-// (4 columns a warp) two warps up to 8 columns, four beyond (passes of 16), so
-// that no warp of a team idles.  (f16 pairs of 8-column warps were measured
-// slower than four warps of 4 columns: fewer warps per page leave the page's
-// latency chain exposed.)  q8_0 always takes the first, in
-// passes of 8 columns: its pages are converted from int8 codes by the warp
-// that reads them, so warps sharing a page would convert it several times
-// (measured slower than a second pass).  f32 pages (CUDA cores) take the
-// first as well.
+// The kernel a call takes, by its C = q_len * G columns:
+//   f16 : C <= 8 paged_decode_mq_kernel; C <= 16 four warps of 4 columns per
+//         page; beyond, four warps of 8 (passes of 32).  (Pairs of 8-column
+//         warps were measured slower than four warps of 4: fewer warps per
+//         page leave the page's latency chain exposed.)
+//   bf16: C <= 4 paged_decode_mq_kernel; C <= 8 two warps of 4 columns (four
+//         would leave two idle); beyond, four warps of 4 (passes of 16).
+//   q8_0: C <= 8 paged_decode_mq_kernel; C <= 16 two warps of 8 columns;
+//         beyond, four warps of 8 (passes of 32).  Every warp that reads a
+//         page converts its int8 codes, so the fewer warps per page the
+//         better: two passes of 8 columns cost more than one page read by two
+//         warps, four warps of 4 columns more still.
+//   f32 : paged_decode_mq_kernel, passes of 8 columns (CUDA cores).
 enum MqKind { kMqSingle = 0, kMqPair1, kMqPair2, kMqTeam1, kMqTeam2 };
 static int mq_kind(int dtype, int group, int q_len) {
   const int cols = q_len * group;
