@@ -85,3 +85,52 @@ def test_host_validation_without_device(lib):
                                       4, None) == 2                          # too many rows
     lib.kv_pool_destroy(h)
     assert api.status_string(4) == "PKV_ERR_WORKSPACE"
+
+
+def test_pool_bytes_bf16_f32(lib):
+    assert lib.kv_pool_bytes(2, 10, 8, 128, 2, 0) == 2 * 10 * 8 * 16 * 128 * 2  # bf16
+    assert lib.kv_pool_bytes(2, 10, 8, 128, 3, 0) == 2 * 10 * 8 * 16 * 128 * 4  # f32
+    assert lib.kv_pool_bytes(2, 10, 8, 128, 3, 1) == 0
+    assert lib.kv_pool_bytes(2, 10, 8, 128, 4, 0) == 0  # no such format
+
+
+def test_workspace_bytes_several_queries(lib):
+    # 32 partial-state columns per slot, 4 arrival counters per (row, KV head)
+    chunks, rows, n_q, n_kv = 304, 8, 32, 8
+    slots = chunks + rows * n_kv
+    cnt = (rows * n_kv * 4 * 4 + 255) // 256 * 256
+    ml = (slots * 32 * 2 * 4 + 255) // 256 * 256
+    acc = (slots * 32 * 128 * 4 + 255) // 256 * 256
+    assert lib.paged_decode_workspace_bytes_mq(rows, n_q, n_kv, 128, chunks) == cnt + ml + acc
+    assert lib.paged_decode_workspace_bytes_mq(rows, n_q, n_kv, 128, 0) == 0
+
+
+def test_several_query_host_validation_without_device(lib):
+    h = ctypes.c_void_p()
+    fake = ctypes.c_void_p(1 << 20)
+    bt = ctypes.c_void_p(1 << 21)
+    assert lib.kv_pool_create(ctypes.byref(h), 1, 4, 8, 128, 0, fake, fake, None, None, None) == 0
+    args = (h, 0, fake, bt, 1, bt, 4)
+    # q_len outside [1, 64] -> PKV_ERR_UNSUPPORTED, before any CUDA call
+    assert lib.paged_decode_attention_mq(*args, 0, 32, 0.1, fake, fake, 1 << 24, 4, None) == 2
+    assert lib.paged_decode_attention_mq(*args, 65, 32, 0.1, fake, fake, 1 << 24, 4, None) == 2
+    # GQA group 3 -> PKV_ERR_UNSUPPORTED
+    assert lib.paged_decode_attention_mq(*args, 2, 24, 0.1, fake, fake, 1 << 24, 4, None) == 2
+    # null q -> PKV_ERR_INVALID_ARG
+    assert lib.paged_decode_attention_mq(h, 0, None, bt, 1, bt, 4, 2, 32, 0.1, fake, fake,
+                                         1 << 24, 4, None) == 1
+    # workspace too small -> PKV_ERR_WORKSPACE
+    assert lib.paged_decode_attention_mq(*args, 2, 32, 0.1, fake, fake, 256, 4, None) == 4
+    # the fused step also needs its new tokens
+    assert lib.pkv_decode_step_mq(h, 0, fake, None, fake, bt, 1, bt, 4, 2, 32, 0.1, fake, fake,
+                                  1 << 24, 4, None) == 1
+    lib.kv_pool_destroy(h)
+
+
+def test_missing_library_raises(monkeypatch):
+    """The product path has no fallback: without libpkv.so every call raises."""
+    from paged_kv_decode_09_gb300 import api
+    monkeypatch.setattr(api, "_LIB_PATH", os.path.join(ROOT, "no_such_dir", "libpkv.so"))
+    monkeypatch.setattr(api, "_lib", None)
+    with pytest.raises(api.PkvError, match="missing"):
+        api.lib()
