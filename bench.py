@@ -449,6 +449,16 @@ def run_ours(args, rank, world, local):
             "chunks": CH, "bytes_per_step": nbytes, "parallelism": f"replicas x{world}",
             **({"window": args.window} if args.window else {}),
             **({"q_len": QL, "launches_per_step": passes} if QL > 1 else {}),
+            "workspace_bytes": ws.nbytes,
+            # traffic beyond the algorithmic bytes and not counted in them: the
+            # block-table entries of the attended pages (once per launch; a
+            # window that does not start on a page boundary touches one more
+            # page), and at most every workspace byte written once and read once
+            "uncounted_bytes": {"block_table": 4 * passes * int(sum(
+                                    W.pages_for(row_tokens(int(L), args.window, QL))
+                                    + (1 if args.window and int(L) else 0)
+                                    for L in wl.seq_lens)),
+                                "workspace_max": 2 * ws.nbytes},
         },
         "frac_of_hbm_peak": round(value / world / peak, 4),
         "rows_tokens_per_s": round(world * tokens / step_s, 1),

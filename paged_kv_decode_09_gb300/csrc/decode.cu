@@ -757,15 +757,13 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
       named_barrier(1, kThreads);
       if (threadIdx.x == 0) {
         int seg_last = 0;
-        if (counted) {
-          __threadfence();  // the CTA's partial (ordered by the barrier) before the arrival
-          seg_last = atomicAdd(a.counters + j, 1) == k1 - k0;
-        }
+        // the CTA's partial (ordered by the barrier) is released by the
+        // arrival; the last to arrive acquires every other piece's
+        if (counted) seg_last = atomic_add_acq_rel(a.counters + j, 1) == k1 - k0;
         ctl[1] = seg_last;
       }
       named_barrier(1, kThreads);
-      if (ctl[1]) {
-        __threadfence();
+      if (ctl[1]) {  // thread 0's acquire, ordered for the CTA by the barrier
         merge_segment<G, DT != PKV_KV_Q8_0 ? PKV_MERGE_BATCH : PKV_MERGE_BATCH / 2>(
             a.part_ml, a.part_acc, j, k0, k1, out_seg, d);
         if (d == 0) a.counters[j] = 0;  // ready for the next call
@@ -792,13 +790,11 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
         if (live && !whole && a.counters != nullptr) {
           __syncwarp();
           int seg_last = 0;
-          if (lane == 0) {
-            __threadfence();  // the warp's partial (ordered by __syncwarp) before the arrival
-            seg_last = atomicAdd(a.counters + j, 1) == k1 - k0;
-          }
+          // the warp's partial (ordered by __syncwarp) is released by the arrival
+          if (lane == 0) seg_last = atomic_add_acq_rel(a.counters + j, 1) == k1 - k0;
           seg_last = __shfl_sync(kFull, seg_last, 0);
           if (seg_last) {
-            __threadfence();
+            __syncwarp();  // lane 0's acquire, ordered for the warp
             merge_segment_warp<G>(a.part_ml, a.part_acc, j, k0, k1, out_seg, lane);
             if (lane == 0) a.counters[j] = 0;  // ready for the next call
           }

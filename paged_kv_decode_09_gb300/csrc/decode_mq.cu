@@ -913,15 +913,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       named_barrier(1, kThreads);
       if (threadIdx.x == 0) {
         int seg_last = 0;
-        if (counted) {
-          __threadfence();
-          seg_last = atomicAdd(a.counters + j, 1) == k1 - k0;
-        }
+        // the CTA's partial (ordered by the barrier) is released by the
+        // arrival; the last to arrive acquires every other piece's
+        if (counted) seg_last = atomic_add_acq_rel(a.counters + j, 1) == k1 - k0;
         ctl[1] = seg_last;
       }
       named_barrier(1, kThreads);
       if (ctl[1]) {  // the CTA merges the segment: warp w takes columns 2w, 2w + 1
-        __threadfence();
         mq_merge_segment_warp<2, 4>(a.part_ml, a.part_acc, j, k0, k1, 2 * warp, nc, out_col,
                                     lane);
         if (threadIdx.x == 0) a.counters[j] = 0;
@@ -954,13 +952,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         if (live && !whole && a.counters != nullptr) {
           __syncwarp();
           int seg_last = 0;
-          if (lane == 0) {
-            __threadfence();
-            seg_last = atomicAdd(a.counters + j, 1) == k1 - k0;
-          }
+          // the warp's partial (ordered by __syncwarp) is released by the arrival
+          if (lane == 0) seg_last = atomic_add_acq_rel(a.counters + j, 1) == k1 - k0;
           seg_last = __shfl_sync(kFull, seg_last, 0);
           if (seg_last) {
-            __threadfence();
+            __syncwarp();  // lane 0's acquire, ordered for the warp
             mq_merge_segment_warp<kWarpCols, 1>(a.part_ml, a.part_acc, j, k0, k1, 0, nc, out_col,
                                               lane);
             if (lane == 0) a.counters[j] = 0;
@@ -1301,13 +1297,11 @@ __global__ void __launch_bounds__(kThreads, team_ctas(NT))
       if (!whole && a.counters != nullptr) {
         __syncwarp();
         int last = 0;
-        if (lane == 0) {
-          __threadfence();  // the warp's partial (ordered by __syncwarp) before its arrival
-          last = atomicAdd(a.counters + j * kMqCounters + wt, 1) == k1 - k0;
-        }
+        // the warp's partial (ordered by __syncwarp) is released by its arrival
+        if (lane == 0) last = atomic_add_acq_rel(a.counters + j * kMqCounters + wt, 1) == k1 - k0;
         last = __shfl_sync(kFull, last, 0);
         if (last) {
-          __threadfence();
+          __syncwarp();  // lane 0's acquire, ordered for the warp
           mq_merge_segment_warp<CW, NT == 1 ? 2 : 1>(a.part_ml, a.part_acc, j, k0, k1, cbase, nc,
                                                      out_col, lane);
           if (lane == 0) a.counters[j * kMqCounters + wt] = 0;  // ready for the next call

@@ -176,6 +176,19 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Atomic add at GPU scope with acquire-release order: the writes ordered
+// before it in the caller (including other threads' writes ordered by a
+// barrier) are visible to whoever acquires the value it writes, and the
+// caller sees every write released before the value it reads.
+__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void record_status(int32_t* status, uint32_t bits) {
   if (status) atomicOr(reinterpret_cast<unsigned int*>(status), bits);
 }
