@@ -584,9 +584,10 @@ def run_kernel(args, local):
         elif args.kernel == "split_combine":
             api.paged_decode_split(pool, i % layers, q, bt, sl, wl.scale, out, ws)
             api.paged_decode_combine(sl, cfg.n_q_heads, cfg.n_kv_heads, wl.bt_stride,
-                                     ws.num_chunks, ws.tensor, out)
+                                     ws.num_chunks, ws.tensor, out, kv_dtype=cfg.dtype)
         else:
-            api.paged_decode_plan(sl, cfg.n_kv_heads, wl.bt_stride, ws.num_chunks)
+            api.paged_decode_plan(sl, cfg.n_kv_heads, wl.bt_stride, ws.num_chunks,
+                                  kv_dtype=cfg.dtype)
 
     for i in range(args.warmup):
         call(i)

@@ -72,6 +72,7 @@ extern "C" {
 #define PKV_HEAD_DIM 128
 #define PKV_Q8_BLOCK 32
 #define PKV_MAX_ROWS 2048 /* rows per call (per-CTA row tables live in shared memory) */
+#define PKV_MAX_CHUNKS (1 << 24) /* work chunks per call (PKV_ERR_UNSUPPORTED above) */
 
 typedef enum pkv_status {
     PKV_OK = 0,
@@ -184,9 +185,9 @@ size_t paged_decode_workspace_bytes(int max_rows, int n_q_heads, int n_kv_heads,
  *   workspace    device scratch of paged_decode_workspace_bytes(num_rows ...)
  *                bytes, 256-byte aligned, zero-filled before its first use
  *   num_chunks   work chunks (0: paged_decode_default_chunks for num_rows)
- * The T (row, KV head, page) tiles of the batch are split into
- * min(num_chunks, T) equal contiguous chunks, one per CTA; a CTA streams its
- * tiles through shared memory, keeps a base-2 online softmax in fp32 for the
+ * The T (row, KV head, page) tiles of the batch are split into at most
+ * num_chunks contiguous chunks, one per CTA, as paged_decode_plan describes;
+ * a CTA streams its tiles through shared memory, keeps a base-2 online softmax in fp32 for the
  * G query heads of the tile's KV head, and writes either the final output
  * (when it holds a whole (row, KV head)) or a partial state (m2, l, acc) to
  * slot chunk + row * n_kv_heads + head of the workspace.  The last CTA to
@@ -212,20 +213,35 @@ pkv_status paged_decode_split(const pkv_pool *pool, int layer, const float *q,
                               void *workspace, size_t workspace_bytes, int num_chunks,
                               void *stream);
 
-/* paged_decode_plan — the work split paged_decode_attention uses, written out
- * for inspection.  Units are (row, KV head, page) tiles in that order; row i
- * reads the pages holding its attended tokens [a_i, L_i), a_i = max(0, L_i -
- * window) (0 for window 0): ceil(L_i / 16) - floor(a_i / 16) pages;
- * T = n_kv_heads * total pages; of C = num_chunks chunks min(C, T) are used,
- * chunk k covering units [floor(k T / C'), floor((k + 1) T / C')), C' = min(C, T).
+/* paged_decode_plan — the work split paged_decode_attention uses on a pool of
+ * KV format kv_dtype, written out for inspection.  Units are (row, KV head,
+ * page) tiles in that order; row i reads the pages holding its attended
+ * tokens [a_i, L_i), a_i = max(0, L_i - window) (0 for window 0):
+ * npg_i = ceil(L_i / 16) - floor(a_i / 16) pages; the units of one (row, KV
+ * head) form a segment; T = n_kv_heads * total pages; C = num_chunks.
+ *   Aligned split (f16 and bf16 KV, when it balances): for a cap of t
+ *   units a chunk, a row with npg_i >= t gives each of its segments
+ *   c = ceil(npg_i / t) chunks, the q-th covering the segment's pages
+ *   [floor(q npg_i / c), floor((q + 1) npg_i / c)); a row with npg_i < t gives
+ *   ceil(n_kv_heads / m) chunks of m = floor(t / npg_i) whole segments (the
+ *   last fewer).  Chunks are numbered in unit order.  t is the smallest
+ *   integer from ceil(T / C) for which all rows need at most C chunks; the
+ *   split is used when t <= floor(11 T / (10 C)), floor(11 T / (10 C)) >
+ *   ceil(T / C) and T < 2^31.  No segment split over several chunks ends
+ *   inside a chunk.
+ *   Uniform split (q8_0 and f32 KV, or when the aligned one does not
+ *   balance): of C
+ *   chunks C' = min(C, T) are used, chunk k covering units
+ *   [floor(k T / C'), floor((k + 1) T / C')).
  * `window` must be the layer's window of the call the plan describes.
  *   row_page_start  int32 [num_rows + 1]: exclusive prefix sum of pages
  *   seg_first_chunk, seg_last_chunk  int32 [num_rows * n_kv_heads]: first and
  *                   last chunk meeting segment (row, head) (-1 if empty)
  * One single-CTA launch. */
 pkv_status paged_decode_plan(const int32_t *seq_lens, int num_rows, int n_kv_heads,
-                             int bt_stride, int window, int num_chunks, int32_t *row_page_start,
-                             int32_t *seg_first_chunk, int32_t *seg_last_chunk, void *stream);
+                             int bt_stride, int window, int num_chunks, pkv_kv_dtype kv_dtype,
+                             int32_t *row_page_start, int32_t *seg_first_chunk,
+                             int32_t *seg_last_chunk, void *stream);
 
 /* paged_decode_combine — merge the base-2 partial states of every
  * (row, query head) split over several chunks:
@@ -233,12 +249,13 @@ pkv_status paged_decode_plan(const int32_t *seq_lens, int num_rows, int n_kv_hea
  * over the slots chunk + row * n_kv_heads + head of the chunks the plan
  * assigns to the segment.  Segments held whole by one chunk are left as they
  * are; rows with seq_lens[i] == 0 get zeros.  The workspace layout is the one
- * paged_decode_workspace_bytes describes; `window` is the layer's window of
- * the paged_decode_split call being completed.  One launch. */
+ * paged_decode_workspace_bytes describes; `window` is the layer's window and
+ * kv_dtype the pool's KV format of the paged_decode_split call being
+ * completed.  One launch. */
 pkv_status paged_decode_combine(const int32_t *seq_lens, int num_rows, int n_q_heads,
                                 int n_kv_heads, int head_dim, int bt_stride, int window,
-                                int num_chunks, const void *workspace, size_t workspace_bytes,
-                                float *out, void *stream);
+                                int num_chunks, pkv_kv_dtype kv_dtype, const void *workspace,
+                                size_t workspace_bytes, float *out, void *stream);
 
 /* pkv_decode_step — one decode step of one layer: the new K/V token of every
  * row is stored as kv_append would store it, and attention runs over the

@@ -90,8 +90,10 @@ def lib():
             L.oracle_attention_partial.restype = _i
             L.oracle_combine.argtypes = [_i, _f32p, _f32p, _f32p, _i, _f64p]
             L.oracle_combine.restype = None
-            L.oracle_plan.argtypes = [_i, _i32p, _i, _i, _i, _i32p, _i32p, _i32p, _i64p]
+            L.oracle_plan.argtypes = [_i, _i32p, _i, _i, _i, _i, _i32p, _i32p, _i32p, _i64p]
             L.oracle_plan.restype = _i
+            L.oracle_chunk_ranges.argtypes = [_i, _i32p, _i, _i, _i, _i, _i64p, _i64p, _i64p]
+            L.oracle_chunk_ranges.restype = _i
             _lib = L
     return _lib
 
@@ -296,8 +298,23 @@ def combine(m2, l, acc):
     return out
 
 
-def plan(seq_lens, n_kv, num_chunks, window=0):
-    """Work split of one decode call (see oracle_plan in the C source):
+def chunk_ranges(seq_lens, n_kv, num_chunks, window=0, aligned=False):
+    """(lo, hi): unit ranges [lo[k], hi[k]) of the chunks that hold units, in the split
+    `plan` describes."""
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    lo = np.zeros(num_chunks, np.int64)
+    hi = np.zeros(num_chunks, np.int64)
+    used = np.zeros(1, np.int64)
+    st = lib().oracle_chunk_ranges(sl.shape[0], sl, n_kv, num_chunks, int(window),
+                                   int(bool(aligned)), lo, hi, used)
+    if st:
+        raise ValueError(f"oracle_chunk_ranges: status {st}")
+    return lo[:used[0]], hi[:used[0]]
+
+
+def plan(seq_lens, n_kv, num_chunks, window=0, aligned=False):
+    """Work split of one decode call (see oracle_plan in the C source); `aligned`: the call
+    allows the segment-aligned split (f16 and bf16 KV):
     (row_page_start[rows+1], seg_first_chunk[rows*n_kv], seg_last_chunk[...], T)."""
     sl = np.ascontiguousarray(seq_lens, np.int32)
     rows = sl.shape[0]
@@ -305,7 +322,8 @@ def plan(seq_lens, n_kv, num_chunks, window=0):
     first = np.zeros(max(rows * n_kv, 1), np.int32)
     last = np.zeros(max(rows * n_kv, 1), np.int32)
     total = np.zeros(1, np.int64)
-    st = lib().oracle_plan(rows, sl, n_kv, num_chunks, int(window), rps, first, last, total)
+    st = lib().oracle_plan(rows, sl, n_kv, num_chunks, int(window), int(bool(aligned)), rps, first,
+                           last, total)
     if st:
         raise ValueError(f"oracle_plan: status {st}")
     return rps, first[:rows * n_kv], last[:rows * n_kv], int(total[0])

@@ -544,37 +544,118 @@ void oracle_combine(int n, const float *m2, const float *l, const float *acc, in
  * its page p < npg_i is block-table entry floor(a_i / 16) + p.  Units are numbered in the order
  * (row, KV head, page): segment j = i * n_kv + h holds the npg_i units of
  * (row i, head h) starting at seg_start(j) = n_kv * sum_{r<i} npg_r + h * npg_i.
- * With T = n_kv * sum_i npg_i units and C chunks requested, Ce = min(C, T)
- * chunks are used (so none is empty) and chunk k < Ce covers units
- * [floor(k T / Ce), floor((k + 1) T / Ce)).  A segment's pieces are its
- * intersections with the chunks; first/last chunk record which chunks they
- * are (-1, -1 for an empty segment).
+ * With T = n_kv * sum_i npg_i units and C chunks requested, the chunks are:
+ *   aligned (only when `aligned` is set): walking the rows in order, a row
+ *   with npg_i >= t gives, head by head, c = ceil(npg_i / t) chunks of the
+ *   head's segment, the q-th holding its pages [floor(q npg_i / c),
+ *   floor((q + 1) npg_i / c)); a row with 0 < npg_i < t gives chunks of
+ *   m = floor(t / npg_i) consecutive whole segments (the last one what is
+ *   left).  t is the first cap, counting up from ceil(T / C) to
+ *   floor(11 T / (10 C)), for which this walk makes at most C chunks; if that
+ *   range holds a single cap or none, if no cap fits, or if T >= 2^31, the
+ *   split is uniform;
+ *   uniform: Ce = min(C, T) chunks (so none is empty), chunk k < Ce covering
+ *   units [floor(k T / Ce), floor((k + 1) T / Ce)).
+ * A segment's pieces are its intersections with the chunks; first/last
+ * chunk record which chunks they are (-1, -1 for an empty segment).
  *
  * Outputs: row_page_start[rows + 1] (exclusive prefix sum of npg),
  * seg_first_chunk[rows * n_kv], seg_last_chunk[rows * n_kv], *total = T. */
-int oracle_plan(int num_rows, const int32_t *seq_lens, int n_kv, int num_chunks, int window,
-                int32_t *row_page_start, int32_t *seg_first_chunk, int32_t *seg_last_chunk,
-                int64_t *total) {
-    if (num_rows < 0 || n_kv <= 0 || num_chunks <= 0 || window < 0) return ORACLE_BAD_ARG;
-    row_page_start[0] = 0;
+
+/* The aligned walk for cap t: the number of chunks it makes, and their unit
+ * ranges in lo/hi while they fit in `cap_chunks` entries (lo may be NULL). */
+static int64_t aligned_walk(int num_rows, const int32_t *rps, int n_kv, int64_t t,
+                            int64_t *lo, int64_t *hi, int64_t cap_chunks) {
+    int64_t n = 0;
+    for (int i = 0; i < num_rows; ++i) {
+        int64_t npg = rps[i + 1] - rps[i], base = (int64_t)n_kv * rps[i];
+        if (npg == 0) continue;
+        if (npg >= t) {
+            int64_t c = (npg + t - 1) / t;
+            for (int h = 0; h < n_kv; ++h)
+                for (int64_t q = 0; q < c; ++q, ++n)
+                    if (lo && n < cap_chunks) {
+                        lo[n] = base + h * npg + q * npg / c;
+                        hi[n] = base + h * npg + (q + 1) * npg / c;
+                    }
+        } else {
+            int64_t m = t / npg;
+            for (int64_t h = 0; h < n_kv; h += m, ++n)
+                if (lo && n < cap_chunks) {
+                    lo[n] = base + h * npg;
+                    hi[n] = base + (h + m < n_kv ? h + m : n_kv) * npg;
+                }
+        }
+    }
+    return n;
+}
+
+/* The chunks' unit ranges [lo[k], hi[k]) for k < the returned count (at most
+ * num_chunks entries are written), for pages per row given by rps. */
+static int64_t split_chunks(int num_rows, const int32_t *rps, int n_kv, int num_chunks,
+                            int aligned, int64_t *lo, int64_t *hi) {
+    int64_t T = (int64_t)n_kv * rps[num_rows];
+    if (aligned && T > 0 && T < ((int64_t)1 << 31)) {
+        int64_t t0 = (T + num_chunks - 1) / num_chunks, t1 = 11 * T / (10 * (int64_t)num_chunks);
+        for (int64_t t = t0; t1 > t0 && t <= t1; ++t)
+            if (aligned_walk(num_rows, rps, n_kv, t, NULL, NULL, 0) <= num_chunks)
+                return aligned_walk(num_rows, rps, n_kv, t, lo, hi, num_chunks);
+    }
+    int64_t nch = T < num_chunks ? T : num_chunks;
+    for (int64_t k = 0; k < nch; ++k) {
+        lo[k] = k * T / nch;
+        hi[k] = (k + 1) * T / nch;
+    }
+    return nch;
+}
+
+static void page_counts(int num_rows, const int32_t *seq_lens, int window, int32_t *rps) {
+    rps[0] = 0;
     for (int i = 0; i < num_rows; ++i) {
         int L = seq_lens[i] > 0 ? seq_lens[i] : 0;
         int npg = L > 0 ? (L + ORACLE_PAGE - 1) / ORACLE_PAGE - window_start(L, window) / ORACLE_PAGE
                         : 0;
-        row_page_start[i + 1] = row_page_start[i] + npg;
+        rps[i + 1] = rps[i] + npg;
     }
+}
+
+/* The chunk ranges of the split oracle_plan describes: lo/hi [num_chunks],
+ * *used = the chunks holding units. */
+int oracle_chunk_ranges(int num_rows, const int32_t *seq_lens, int n_kv, int num_chunks,
+                        int window, int aligned, int64_t *lo, int64_t *hi, int64_t *used) {
+    if (num_rows < 0 || n_kv <= 0 || num_chunks <= 0 || window < 0) return ORACLE_BAD_ARG;
+    int32_t *rps = malloc(sizeof(int32_t) * ((size_t)num_rows + 1));
+    if (!rps) return ORACLE_BAD_ARG;
+    page_counts(num_rows, seq_lens, window, rps);
+    *used = split_chunks(num_rows, rps, n_kv, num_chunks, aligned, lo, hi);
+    free(rps);
+    return ORACLE_OK;
+}
+
+int oracle_plan(int num_rows, const int32_t *seq_lens, int n_kv, int num_chunks, int window,
+                int aligned, int32_t *row_page_start, int32_t *seg_first_chunk,
+                int32_t *seg_last_chunk, int64_t *total) {
+    if (num_rows < 0 || n_kv <= 0 || num_chunks <= 0 || window < 0) return ORACLE_BAD_ARG;
+    page_counts(num_rows, seq_lens, window, row_page_start);
     int64_t T = (int64_t)n_kv * row_page_start[num_rows];
     *total = T;
+    /* the chunks' unit ranges */
+    int64_t *lo = malloc(sizeof(int64_t) * (size_t)num_chunks);
+    int64_t *hi = malloc(sizeof(int64_t) * (size_t)num_chunks);
+    if (!lo || !hi) {
+        free(lo);
+        free(hi);
+        return ORACLE_BAD_ARG;
+    }
+    const int64_t nch = split_chunks(num_rows, row_page_start, n_kv, num_chunks, aligned, lo, hi);
     for (int i = 0; i < num_rows; ++i) {
         int64_t npg = row_page_start[i + 1] - row_page_start[i];
         for (int h = 0; h < n_kv; ++h) {
             int64_t j = (int64_t)i * n_kv + h;
             int64_t a = (int64_t)n_kv * row_page_start[i] + h * npg, b = a + npg;
             int32_t first = -1, last = -1;
-            const int64_t Ce = T < num_chunks ? T : num_chunks;
-            for (int64_t k = 0; k < Ce; ++k) {
-                int64_t c0 = k * T / Ce, c1 = (k + 1) * T / Ce;
-                if (a < b && c0 < c1 && c0 < b && a < c1) { /* non-empty overlap */
+            for (int64_t k = 0; k < nch; ++k) {
+                if (a < b && lo[k] < hi[k] && lo[k] < b && a < hi[k]) { /* non-empty overlap */
                     if (first < 0) first = (int32_t)k;
                     last = (int32_t)k;
                 }
@@ -583,5 +664,7 @@ int oracle_plan(int num_rows, const int32_t *seq_lens, int n_kv, int num_chunks,
             seg_last_chunk[j] = last;
         }
     }
+    free(lo);
+    free(hi);
     return ORACLE_OK;
 }

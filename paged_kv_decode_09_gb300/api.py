@@ -54,8 +54,8 @@ _SIGS = {
                                 _sz, _i, _vp], _i),
     "paged_decode_split": ([_vp, _i, _vp, _vp, _i, _vp, _i, _i, ctypes.c_float, _vp, _vp,
                             _sz, _i, _vp], _i),
-    "paged_decode_plan": ([_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp], _i),
-    "paged_decode_combine": ([_vp, _i, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp], _i),
+    "paged_decode_plan": ([_vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp], _i),
+    "paged_decode_combine": ([_vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp], _i),
     "kv_pool_set_window": ([_vp, _i, _i], _i),
     "pkv_alloc_create": ([ctypes.POINTER(_vp), _i, _i, _i], _i),
     "pkv_alloc_destroy": ([_vp], None),
@@ -374,8 +374,9 @@ def paged_decode_split(pool: KVPool, layer: int, q, block_table, seq_lens, scale
 
 
 def paged_decode_plan(seq_lens, n_kv_heads: int, bt_stride: int, num_chunks: int, stream=None,
-                      window: int = 0):
-    """(row_page_start [rows+1], seg_first_chunk, seg_last_chunk [rows*n_kv]) int32 tensors."""
+                      window: int = 0, *, kv_dtype: int):
+    """(row_page_start [rows+1], seg_first_chunk, seg_last_chunk [rows*n_kv]) int32 tensors:
+    the split an attention call on a pool of KV format kv_dtype uses."""
     _need(seq_lens, torch.int32, "seq_lens")
     rows = seq_lens.shape[0]
     dev = seq_lens.device
@@ -383,21 +384,22 @@ def paged_decode_plan(seq_lens, n_kv_heads: int, bt_stride: int, num_chunks: int
     first = torch.empty(max(rows * n_kv_heads, 1), dtype=torch.int32, device=dev)
     last = torch.empty_like(first)
     _check(lib().paged_decode_plan(_ptr(seq_lens), rows, n_kv_heads, bt_stride, window, num_chunks,
-                                   _ptr(rps), _ptr(first), _ptr(last), _stream(stream)),
+                                   kv_dtype, _ptr(rps), _ptr(first), _ptr(last), _stream(stream)),
            "paged_decode_plan")
     return rps, first[:rows * n_kv_heads], last[:rows * n_kv_heads]
 
 
 def paged_decode_combine(seq_lens, n_q_heads: int, n_kv_heads: int, bt_stride: int,
                          num_chunks: int, workspace: torch.Tensor, out, stream=None,
-                         window: int = 0):
-    """Merge partial states held in `workspace` (layout of paged_decode_workspace_bytes)."""
+                         window: int = 0, *, kv_dtype: int):
+    """Merge partial states held in `workspace` (layout of paged_decode_workspace_bytes) left
+    by paged_decode_split on a pool of KV format kv_dtype."""
     _need(seq_lens, torch.int32, "seq_lens")
     _need(workspace, torch.uint8, "workspace")
     _need(out, torch.float32, "out")
     rows = seq_lens.shape[0]
     _check(lib().paged_decode_combine(_ptr(seq_lens), rows, n_q_heads, n_kv_heads, HEAD_DIM,
-                                      bt_stride, window, num_chunks, _ptr(workspace),
+                                      bt_stride, window, num_chunks, kv_dtype, _ptr(workspace),
                                       workspace.numel(),
                                       _ptr(out), _stream(stream)), "paged_decode_combine")
     return out

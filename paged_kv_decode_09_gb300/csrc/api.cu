@@ -80,6 +80,16 @@ pkv_status check_geometry(int n_q, int n_kv, int head_dim) {
   return PKV_OK;
 }
 
+bool known_dtype(pkv_kv_dtype d) {
+  return d == PKV_KV_F16 || d == PKV_KV_Q8_0 || d == PKV_KV_BF16 || d == PKV_KV_F32;
+}
+
+// Whether the single-query split may align its chunks to segments for this
+// KV format: the 16-bit formats.  q8_0 chunks finish by launch order
+// (instruction issue), not by the pieces they hold, and f32 chunks are twice
+// as long, so for both equal chunks serve better.
+int split_may_align(pkv_kv_dtype d) { return d == PKV_KV_F16 || d == PKV_KV_BF16; }
+
 pkv_status check_rows(int num_rows, int bt_stride, const int32_t* bt, const int32_t* sl,
                       int max_rows = PKV_MAX_ROWS) {
   if (num_rows < 0) return fail(PKV_ERR_INVALID_ARG, "num_rows < 0");
@@ -176,6 +186,7 @@ pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q, const
   if (!aligned(q, 16) || !aligned(out, 16))
     return fail(PKV_ERR_INVALID_ARG, "q / out not 16-byte aligned");
   if (num_chunks < 0) return fail(PKV_ERR_INVALID_ARG, "num_chunks < 0");
+  if (num_chunks > PKV_MAX_CHUNKS) return fail(PKV_ERR_UNSUPPORTED, "num_chunks > %d", PKV_MAX_CHUNKS);
   if (num_rows == 0) return PKV_OK;
   if (num_chunks == 0 && (s = default_chunks(pool, n_q, num_rows, &num_chunks))) return s;
   const size_t need = workspace_needed(num_rows, n_q, pool->n_kv, num_chunks);
@@ -206,6 +217,7 @@ pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q, const
   a.q0 = 0;
   a.nq = 1;
   a.vchunks = num_chunks;
+  a.aligned_split = split_may_align(pool->dtype);
   a.out = out;
   a.part_ml = w.part_ml;
   a.part_acc = w.part_acc;
@@ -256,6 +268,7 @@ pkv_status attention_mq_impl(const pkv_pool* pool, int layer, const float* q, co
   if (!aligned(q, 16) || !aligned(out, 16))
     return fail(PKV_ERR_INVALID_ARG, "q / out not 16-byte aligned");
   if (num_chunks < 0) return fail(PKV_ERR_INVALID_ARG, "num_chunks < 0");
+  if (num_chunks > PKV_MAX_CHUNKS) return fail(PKV_ERR_UNSUPPORTED, "num_chunks > %d", PKV_MAX_CHUNKS);
   if (num_rows == 0) return PKV_OK;
   const int g = n_q / pool->n_kv;
   if (num_chunks == 0 && (s = default_chunks_mq(pool, g, q_len, num_rows, &num_chunks))) return s;
@@ -288,6 +301,7 @@ pkv_status attention_mq_impl(const pkv_pool* pool, int layer, const float* q, co
   a.window = pool->window[layer];
   a.q_len = q_len;
   a.vchunks = num_chunks;
+  a.aligned_split = 0;
   a.out = out;
   a.status = pool->status;
   const pkv::TileMaps* maps = nullptr;
@@ -457,7 +471,7 @@ pkv_status paged_decode_default_chunks(const pkv_pool* pool, int n_q_heads, int 
 
 size_t paged_decode_workspace_bytes(int max_rows, int n_q_heads, int n_kv_heads, int head_dim,
                                     int num_chunks) {
-  if (max_rows < 0 || num_chunks < 1 || n_kv_heads <= 0 || n_q_heads <= 0 ||
+  if (max_rows < 0 || num_chunks < 1 || num_chunks > PKV_MAX_CHUNKS || n_kv_heads <= 0 || n_q_heads <= 0 ||
       n_q_heads % n_kv_heads || head_dim != PKV_HEAD_DIM)
     return 0;
   return workspace_needed(max_rows, n_q_heads, n_kv_heads, num_chunks);
@@ -484,17 +498,21 @@ pkv_status paged_decode_split(const pkv_pool* pool, int layer, const float* q,
 }
 
 pkv_status paged_decode_plan(const int32_t* seq_lens, int num_rows, int n_kv_heads,
-                             int bt_stride, int window, int num_chunks, int32_t* row_page_start,
-                             int32_t* seg_first_chunk, int32_t* seg_last_chunk, void* stream) {
+                             int bt_stride, int window, int num_chunks, pkv_kv_dtype kv_dtype,
+                             int32_t* row_page_start, int32_t* seg_first_chunk,
+                             int32_t* seg_last_chunk, void* stream) {
   pkv_status s = check_rows(num_rows, bt_stride, seq_lens, seq_lens);
   if (s) return s;
+  if (!known_dtype(kv_dtype)) return fail(PKV_ERR_INVALID_ARG, "unknown KV dtype %d", static_cast<int>(kv_dtype));
   if (window < 0) return fail(PKV_ERR_INVALID_ARG, "window < 0");
   if (n_kv_heads <= 0 || num_chunks < 1)
     return fail(PKV_ERR_INVALID_ARG, "n_kv_heads and num_chunks must be positive");
+  if (num_chunks > PKV_MAX_CHUNKS) return fail(PKV_ERR_UNSUPPORTED, "num_chunks > %d", PKV_MAX_CHUNKS);
   if (!row_page_start || (num_rows > 0 && (!seg_first_chunk || !seg_last_chunk)))
     return fail(PKV_ERR_INVALID_ARG, "null plan output");
-  pkv::PlanArgs a{seq_lens, window, num_rows, n_kv_heads, bt_stride, num_chunks,
-                  row_page_start, seg_first_chunk, seg_last_chunk};
+  pkv::PlanArgs a{seq_lens,  window,         num_rows,        n_kv_heads,     bt_stride,
+                  num_chunks, split_may_align(kv_dtype), row_page_start, seg_first_chunk,
+                  seg_last_chunk};
   cudaError_t e = pkv::launch_plan(a, as_stream(stream));
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   return PKV_OK;
@@ -502,13 +520,15 @@ pkv_status paged_decode_plan(const int32_t* seq_lens, int num_rows, int n_kv_hea
 
 pkv_status paged_decode_combine(const int32_t* seq_lens, int num_rows, int n_q_heads,
                                 int n_kv_heads, int head_dim, int bt_stride, int window,
-                                int num_chunks, const void* workspace, size_t workspace_bytes,
-                                float* out, void* stream) {
+                                int num_chunks, pkv_kv_dtype kv_dtype, const void* workspace,
+                                size_t workspace_bytes, float* out, void* stream) {
   pkv_status s = check_geometry(n_q_heads, n_kv_heads, head_dim);
   if (s) return s;
+  if (!known_dtype(kv_dtype)) return fail(PKV_ERR_INVALID_ARG, "unknown KV dtype %d", static_cast<int>(kv_dtype));
   if (window < 0) return fail(PKV_ERR_INVALID_ARG, "window < 0");
   if ((s = check_rows(num_rows, bt_stride, seq_lens, seq_lens))) return s;
   if (num_chunks < 1) return fail(PKV_ERR_INVALID_ARG, "num_chunks < 1");
+  if (num_chunks > PKV_MAX_CHUNKS) return fail(PKV_ERR_UNSUPPORTED, "num_chunks > %d", PKV_MAX_CHUNKS);
   if (num_rows > 0 && !out) return fail(PKV_ERR_INVALID_ARG, "null out");
   const size_t need = workspace_needed(num_rows, n_q_heads, n_kv_heads, num_chunks);
   if (!workspace || workspace_bytes < need)
@@ -526,6 +546,7 @@ pkv_status paged_decode_combine(const int32_t* seq_lens, int num_rows, int n_q_h
   c.n_kv = n_kv_heads;
   c.bt_stride = bt_stride;
   c.num_chunks = num_chunks;
+  c.aligned_split = split_may_align(kv_dtype);
   c.part_ml = w.part_ml;
   c.part_acc = w.part_acc;
   c.out = out;
@@ -551,7 +572,7 @@ pkv_status pkv_decode_step(const pkv_pool* pool, int layer, const float* q, cons
 
 size_t paged_decode_workspace_bytes_mq(int max_rows, int n_q_heads, int n_kv_heads, int head_dim,
                                        int num_chunks) {
-  if (max_rows < 0 || num_chunks < 1 || n_kv_heads <= 0 || n_q_heads <= 0 ||
+  if (max_rows < 0 || num_chunks < 1 || num_chunks > PKV_MAX_CHUNKS || n_kv_heads <= 0 || n_q_heads <= 0 ||
       n_q_heads % n_kv_heads || head_dim != PKV_HEAD_DIM)
     return 0;
   return workspace_needed_mq(max_rows, n_kv_heads, num_chunks);

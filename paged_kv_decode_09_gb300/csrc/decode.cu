@@ -86,9 +86,10 @@ struct Smem {
   static constexpr uint32_t kQ = kMrgMl + kWarps * G * 2 * 4;  // f32 KV: [warps][G][kQStride] q
   static constexpr uint32_t kCtl =
       kQ + (DT == PKV_KV_F32 ? kWarps * G * kQStride * 4 : 0);             // int [4]
-  static constexpr uint32_t kRows = kCtl + 16;  // int row_start[rows + 1], lens[rows]
+  static constexpr uint32_t kSplit = kCtl + 16;  // the work split
+  static constexpr uint32_t kRows = kSplit + 16;  // int row_start[rows + 1], lens[rows], pc[rows + 1]
   static size_t bytes(int rows) {
-    return kAlign + kRows + (2 * static_cast<size_t>(rows) + 1) * 4;  // kAlign: base alignment slack
+    return kAlign + kRows + plan_ints(rows) * 4;  // kAlign: base alignment slack
   }
   static_assert(Tiles<DT>::kCodes % 1024 == 0, "tile stages keep the swizzle atom alignment");
   static_assert(kMrgAcc % 16 == 0 && kMrgMl % 16 == 0 && kQ % 16 == 0 && kCtl % 16 == 0,
@@ -511,6 +512,8 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
   volatile int* ctl = reinterpret_cast<volatile int*>(smem + SM::kCtl);
   int* row_start = reinterpret_cast<int*>(smem + SM::kRows);
   int* lens = row_start + a.num_rows + 1;
+  int* pc = lens + a.num_rows;  // chunks before each row (aligned split)
+  Split* split = reinterpret_cast<Split*>(smem + SM::kSplit);
   const uint32_t bar0 = smem_addr(smem + SM::kBar) + warp * R * 8;  // this warp's barriers
   uint8_t* ring = smem + static_cast<size_t>(warp) * R * TL::kCodes;  // this warp's tiles
   uint8_t* ring_sc = smem + SM::kScl + static_cast<size_t>(warp) * R * TL::kScales;  // q8_0 scales
@@ -534,10 +537,11 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
   plan_rows(a.seq_lens, a.num_rows, a.bt_stride, a.window, blockIdx.x == 0 ? a.status : nullptr,
             lens, row_start);
 
-  const long long T = static_cast<long long>(a.n_kv) * row_start[a.num_rows];
-  const int C = used_chunks(T, gridDim.x), k = blockIdx.x;
-  const long long c_begin = k < C ? static_cast<long long>(k) * T / C : T;
-  const long long c_end = k < C ? static_cast<long long>(k + 1) * T / C : T;
+  plan_split(row_start, a.num_rows, a.n_kv, gridDim.x, a.aligned_split, split, pc);
+  const Split sp = *split;
+  const int k = blockIdx.x;
+  long long c_begin, c_end;
+  chunk_range(sp, k, row_start, pc, a.num_rows, a.n_kv, c_begin, c_end);
 
   // Rows without tokens attend to nothing: their output is zero.
   if (k == 0) {
@@ -658,7 +662,8 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
     const int ws = window_start(L, a.window);  // first attended token of the row
     const int p0 = ws / kPage;                 // its page: the row's unit 0
     const long long j = static_cast<long long>(i) * a.n_kv + h;
-    const int k0 = chunk_of(seg_start, T, C), k1 = chunk_of(seg_end - 1, T, C);
+    int k0, k1;
+    segment_chunks(sp, i, h, row_start, pc, a.num_rows, a.n_kv, k0, k1);
 
     load_query<DT, G>(a.q + (static_cast<long long>(i) * a.n_q + h * G) * kD, a.qscale, lane, S);
 #pragma unroll
@@ -818,9 +823,12 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
 template <int G>
 __global__ void __launch_bounds__(kD) combine_kernel(const CombineArgs a) {
   extern __shared__ int csm[];
+  __shared__ Split split;
   int* row_start = csm;
   int* lens = csm + a.num_rows + 1;
+  int* pc = lens + a.num_rows;
   plan_rows(a.seq_lens, a.num_rows, a.bt_stride, a.window, nullptr, lens, row_start);
+  plan_split(row_start, a.num_rows, a.n_kv, a.num_chunks, a.aligned_split, &split, pc);
   const int j = blockIdx.x, i = j / a.n_kv, h = j % a.n_kv, d = threadIdx.x;
   const int npg = row_start[i + 1] - row_start[i];
   float* o = a.out + (static_cast<long long>(i) * a.n_q + h * G) * kD;
@@ -829,10 +837,8 @@ __global__ void __launch_bounds__(kD) combine_kernel(const CombineArgs a) {
     for (int g = 0; g < G; ++g) o[g * kD + d] = 0.f;
     return;
   }
-  const long long T = static_cast<long long>(a.n_kv) * row_start[a.num_rows];
-  const int C = used_chunks(T, a.num_chunks);
-  const long long s0 = static_cast<long long>(a.n_kv) * row_start[i] + static_cast<long long>(h) * npg;
-  const int k0 = chunk_of(s0, T, C), k1 = chunk_of(s0 + npg - 1, T, C);
+  int k0, k1;
+  segment_chunks(split, i, h, row_start, pc, a.num_rows, a.n_kv, k0, k1);
   if (k0 == k1) return;  // one piece: the attention kernel wrote the output
   merge_segment<G>(a.part_ml, a.part_acc, j, k0, k1, o, d);
 }
@@ -840,21 +846,18 @@ __global__ void __launch_bounds__(kD) combine_kernel(const CombineArgs a) {
 // ----------------------------------------------------------------- plan ----
 __global__ void __launch_bounds__(256) plan_kernel(const PlanArgs a) {
   extern __shared__ int psm[];
+  __shared__ Split split;
   int* row_start = psm;
   int* lens = psm + a.num_rows + 1;
+  int* pc = lens + a.num_rows;
   plan_rows(a.seq_lens, a.num_rows, a.bt_stride, a.window, nullptr, lens, row_start);
+  plan_split(row_start, a.num_rows, a.n_kv, a.num_chunks, a.aligned_split, &split, pc);
   for (int r = threadIdx.x; r <= a.num_rows; r += blockDim.x) a.row_page_start[r] = row_start[r];
-  const long long T = static_cast<long long>(a.n_kv) * row_start[a.num_rows];
-  const int C = used_chunks(T, a.num_chunks);
   for (int j = threadIdx.x; j < a.num_rows * a.n_kv; j += blockDim.x) {
     const int i = j / a.n_kv, h = j % a.n_kv;
     const int npg = row_start[i + 1] - row_start[i];
     int f = -1, l = -1;
-    if (npg > 0) {
-      const long long s0 = static_cast<long long>(a.n_kv) * row_start[i] + static_cast<long long>(h) * npg;
-      f = chunk_of(s0, T, C);
-      l = chunk_of(s0 + npg - 1, T, C);
-    }
+    if (npg > 0) segment_chunks(split, i, h, row_start, pc, a.num_rows, a.n_kv, f, l);
     a.seg_first_chunk[j] = f;
     a.seg_last_chunk[j] = l;
   }
@@ -999,7 +1002,7 @@ cudaError_t paged_decode_blocks_per_sm(int dtype, int group, int rows, int* bloc
 cudaError_t launch_combine(int group, const CombineArgs& a, cudaStream_t st) {
   const int segs = a.num_rows * a.n_kv;
   if (segs == 0) return cudaSuccess;
-  const size_t smem = (2 * static_cast<size_t>(a.num_rows) + 1) * sizeof(int);
+  const size_t smem = plan_ints(a.num_rows) * sizeof(int);
   if (group == 1)
     combine_kernel<1><<<segs, kD, smem, st>>>(a);
   else if (group == 2)
@@ -1012,7 +1015,7 @@ cudaError_t launch_combine(int group, const CombineArgs& a, cudaStream_t st) {
 }
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t st) {
-  const size_t smem = (2 * static_cast<size_t>(a.num_rows) + 1) * sizeof(int);
+  const size_t smem = plan_ints(a.num_rows) * sizeof(int);
   plan_kernel<<<1, 256, smem, st>>>(a);
   return cudaGetLastError();
 }

@@ -267,4 +267,175 @@ __device__ __forceinline__ int row_of(const int* row_start, int num_rows, int n_
   return lo;
 }
 
+// ---------------------------------------------------------------- split ----
+// The work split of T (row, KV head, page) units into at most C chunks.
+// Uniform: chunk k covers [floor(k T / C'), floor((k + 1) T / C')), C' =
+// min(C, T).  Aligned to the (row, KV head) segments, for a cap of t units a
+// chunk: a row of npg >= t pages gives each of its n_kv segments cps =
+// ceil(npg / t) chunks, chunk q of a segment covering its pages
+// [floor(q npg / cps), floor((q + 1) npg / cps)); a shorter row gives
+// ceil(n_kv / m) chunks of m = floor(t / npg) whole segments (the last one
+// fewer).  A segment split over several chunks then always ends where a chunk
+// ends, so no chunk stops in the middle of its units to hand a partial state
+// on.  t is the smallest cap from ceil(T / C) to floor(1.1 T / C) for which the
+// rows need at most C chunks; the aligned split is taken when the call allows
+// it, that range holds more than one cap and one of them fits, else the
+// uniform one.
+struct Split {
+  int aligned;  // 1: aligned with cap t; 0: uniform
+  int t;
+  int used;     // chunks holding units: C' (uniform) or the rows' total (aligned)
+  int pad;
+};
+
+// Choose the split for the rows planned by plan_rows (row_start), write it
+// to *sp and, when aligned, the exclusive prefix sum of the rows' chunk
+// counts to pc[0 .. num_rows].  Every thread of the CTA (at least 128) must
+// call it; it ends with __syncthreads.
+//
+// The counts are monotone in the cap, so the cap is the first of
+// lo0, lo0 + 1, .. hi0 whose count fits.  The CTA tests eight caps at a time:
+// sixteen lanes a cap, each over every sixteenth row, a shuffle sum in the
+// half warp, the eight counts in shared memory.
+__device__ __forceinline__ void plan_split(const int* row_start, int num_rows, int n_kv, int C,
+                                           bool allow_aligned, Split* sp, int* pc) {
+  __shared__ int counts[8];
+  const long long T = static_cast<long long>(n_kv) * row_start[num_rows];
+  int aligned = 0, t = 0;
+  // 32-bit arithmetic throughout; batches of 2^31 units or more take the
+  // uniform split.
+  if (allow_aligned && T > 0 && T < (1ll << 31) && C > 0) {
+    const int T32 = static_cast<int>(T);
+    const int Cs = C < (1 << 29) ? C : (1 << 29);  // counts saturate at Cs + 1
+    const int lo0 = T32 / Cs + (T32 % Cs != 0);
+    const int hi0 = T32 < (1 << 27) ? (11 * T32) / (10 * Cs) : static_cast<int>((11ll * T32) / (10ll * Cs));
+    // only when the cap may exceed ceil(T / C) (about 10 units a chunk or more)
+    const int cand = threadIdx.x >> 4, sub = threadIdx.x & 15;  // 8 caps x 16 lanes
+    for (int base = lo0; hi0 > lo0 && base <= hi0; base += 8) {
+      if (threadIdx.x < 128) {
+        const int cap = base + cand;
+        int c = 0;
+        for (int r = sub; r < num_rows; r += 16) {
+          const int npg = row_start[r + 1] - row_start[r];
+          int x = 0;
+          if (npg > 0) {
+            if (npg >= cap) {
+              x = n_kv * ((npg + cap - 1) / cap);
+            } else {
+              const int m = cap / npg;
+              x = (n_kv + m - 1) / m;
+            }
+          }
+          c = min(c + x, Cs + 1);
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) c = min(c + __shfl_xor_sync(kFull, c, o), Cs + 1);
+        if (sub == 0) counts[cand] = c;
+      }
+      __syncthreads();
+      int found = 0;
+#pragma unroll
+      for (int u = 7; u >= 0; --u)
+        if (base + u <= hi0 && counts[u] <= Cs) found = base + u;
+      __syncthreads();  // counts[] is rewritten by the next round
+      if (found) {
+        aligned = 1;
+        t = found;
+        break;
+      }
+    }
+  }
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int used;
+    if (aligned) {
+      int carry = 0;
+      if (lane == 0) pc[0] = 0;
+      for (int base = 0; base < num_rows; base += 32) {
+        const int r = base + lane;
+        const int npg = r < num_rows ? row_start[r + 1] - row_start[r] : 0;
+        int v = 0;
+        if (npg > 0) v = npg >= t ? n_kv * ((npg + t - 1) / t) : (n_kv + t / npg - 1) / (t / npg);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(kFull, v, o);
+          if (lane >= o) v += u;
+        }
+        if (r < num_rows) pc[r + 1] = carry + v;
+        carry += __shfl_sync(kFull, v, 31);
+      }
+      used = carry;
+    } else {
+      used = static_cast<int>(T < C ? T : C);
+    }
+    if (lane == 0) {
+      sp->aligned = aligned;
+      sp->t = t;
+      sp->used = used;
+    }
+  }
+  __syncthreads();
+}
+
+// Units [b, e) of chunk k (empty, b = e = T, for k >= sp.used).
+__device__ __forceinline__ void chunk_range(const Split& sp, int k, const int* row_start,
+                                            const int* pc, int num_rows, int n_kv,
+                                            long long& b, long long& e) {
+  const long long T = static_cast<long long>(n_kv) * row_start[num_rows];
+  if (k >= sp.used) {
+    b = e = T;
+    return;
+  }
+  if (!sp.aligned) {
+    b = static_cast<long long>(k) * T / sp.used;
+    e = static_cast<long long>(k + 1) * T / sp.used;
+    return;
+  }
+  int lo = 0, hi = num_rows;  // pc[lo] <= k < pc[hi]: the row is the largest such lo
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pc[mid] <= k)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const int l = k - pc[lo], npg = row_start[lo + 1] - row_start[lo];
+  const long long base = static_cast<long long>(n_kv) * row_start[lo];
+  if (npg >= sp.t) {
+    const int cps = (npg + sp.t - 1) / sp.t, h = l / cps, q = l - h * cps;
+    const long long seg = base + static_cast<long long>(h) * npg;
+    if (npg < 46340) {  // (q + 1) * npg < 2^31
+      b = seg + q * npg / cps;
+      e = seg + (q + 1) * npg / cps;
+    } else {
+      b = seg + static_cast<long long>(q) * npg / cps;
+      e = seg + static_cast<long long>(q + 1) * npg / cps;
+    }
+  } else {
+    const int m = sp.t / npg;
+    const int h1 = (l + 1) * m < n_kv ? (l + 1) * m : n_kv;
+    b = base + static_cast<long long>(l) * m * npg;
+    e = base + static_cast<long long>(h1) * npg;
+  }
+}
+
+// First and last chunk meeting segment (row i, KV head h) of npg > 0 pages.
+__device__ __forceinline__ void segment_chunks(const Split& sp, int i, int h, const int* row_start,
+                                               const int* pc, int num_rows, int n_kv, int& k0,
+                                               int& k1) {
+  const int npg = row_start[i + 1] - row_start[i];
+  if (!sp.aligned) {
+    const long long T = static_cast<long long>(n_kv) * row_start[num_rows];
+    const long long s0 = static_cast<long long>(n_kv) * row_start[i] + static_cast<long long>(h) * npg;
+    k0 = chunk_of(s0, T, sp.used);
+    k1 = chunk_of(s0 + npg - 1, T, sp.used);
+  } else if (npg >= sp.t) {
+    const int cps = (npg + sp.t - 1) / sp.t;
+    k0 = pc[i] + h * cps;
+    k1 = k0 + cps - 1;
+  } else {
+    k0 = k1 = pc[i] + h / (sp.t / npg);
+  }
+}
+
 }  // namespace pkv

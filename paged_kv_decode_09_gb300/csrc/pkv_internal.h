@@ -33,6 +33,7 @@ struct DecodeArgs {
   int q_len;     // queries (new tokens) per row; q, out [rows][q_len][n_q][128]
   int q0, nq;    // several-query kernel: this pass's queries q0 .. q0 + nq - 1
   int vchunks;   // chunks of the work split (several-query kernels: a CTA may hold 2)
+  int aligned_split;  // 1: the split may align chunks to segments (single-query kernel)
   float* out;
   float* part_ml;   // [slots][G][2]
   float* part_acc;  // [slots][G][128]
@@ -48,6 +49,7 @@ struct CombineArgs {
   int n_kv;
   int bt_stride;
   int num_chunks;
+  int aligned_split;  // the attention call's split (see DecodeArgs)
   const float* part_ml;
   const float* part_acc;
   float* out;
@@ -60,6 +62,7 @@ struct PlanArgs {
   int n_kv;
   int bt_stride;
   int num_chunks;
+  int aligned_split;
   int32_t* row_page_start;
   int32_t* seg_first_chunk;
   int32_t* seg_last_chunk;
@@ -84,6 +87,9 @@ struct AppendArgs {
 // Workspace layout (see paged_decode_workspace_bytes): arrival counters,
 // then the partial states.
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+// ints of a single-query CTA's plan in shared memory: row_start[rows + 1],
+// lens[rows] and the chunks before each row pc[rows + 1]
+inline size_t plan_ints(int rows) { return 3 * static_cast<size_t>(rows) + 2; }
 inline size_t counter_bytes(long long segments) {
   return align256(static_cast<size_t>(segments) * sizeof(int32_t));
 }

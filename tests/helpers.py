@@ -106,6 +106,12 @@ def device_pool(wl: W.Workload, host_pool, num_layers: int = 1, layer: int = 0):
     return pool
 
 
+def split_aligned(dtype) -> bool:
+    """Whether attention calls on a pool of this KV format may use the segment-aligned split
+    (the oracle plan's `aligned` flag): the 16-bit formats."""
+    return dtype in (W.F16, W.BF16)
+
+
 def host_arrays(pool, layer: int = 0):
     """(k_data, v_data, k_scales, v_scales) numpy copies of one layer of a device pool."""
     import torch

@@ -57,6 +57,20 @@ def test_workspace_bytes(lib):
     assert lib.paged_decode_workspace_bytes(rows, n_q, n_kv, 128, chunks) == cnt + ml + acc
     assert lib.paged_decode_workspace_bytes(rows, 30, 8, 128, chunks) == 0   # 30 % 8 != 0
     assert lib.paged_decode_workspace_bytes(rows, 32, 8, 64, chunks) == 0    # head_dim 64
+    assert lib.paged_decode_workspace_bytes(rows, n_q, n_kv, 128, (1 << 24) + 1) == 0  # chunks
+
+
+def test_plan_and_combine_reject_bad_split_arguments(lib):
+    """The plan and the combine describe the split of one KV format: an unknown
+    format, or more than 2^24 chunks, is rejected on the host."""
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.paged_decode_plan(fake, 1, 8, 4, 0, 16, 7, fake, fake, fake, None) == 1
+    assert lib.paged_decode_plan(fake, 1, 8, 4, 0, (1 << 24) + 1, 0, fake, fake, fake,
+                                 None) == 2
+    assert lib.paged_decode_combine(fake, 1, 32, 8, 128, 4, 0, 16, 9, fake, 1 << 20, fake,
+                                    None) == 1
+    assert lib.paged_decode_combine(fake, 1, 32, 8, 128, 4, 0, (1 << 24) + 1, 0, fake, 1 << 30,
+                                    fake, None) == 2
 
 
 def test_host_validation_without_device(lib):

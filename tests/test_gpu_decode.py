@@ -191,7 +191,7 @@ def test_split_then_combine_equals_merged(dtype):
     out = torch.full_like(q, float("nan"))
     api.paged_decode_split(pool, 0, q, bt, sl, wl.scale, out, ws)
     api.paged_decode_combine(sl, wl.cfg.n_q_heads, wl.cfg.n_kv_heads, wl.bt_stride,
-                             ws.num_chunks, ws.tensor, out)
+                             ws.num_chunks, ws.tensor, out, kv_dtype=pool.dtype)
     torch.cuda.synchronize()
     # the two merges batch the pieces differently: same sums, other rounding order
     np.testing.assert_allclose(out.cpu().numpy(), merged, rtol=0, atol=1e-6)

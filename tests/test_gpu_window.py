@@ -13,7 +13,8 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import ATOL_STATED, F16_NAN, device_pool, encode_pool, oracle_decode, tight_tol, to_dev
+from helpers import (ATOL_STATED, F16_NAN, device_pool, encode_pool, oracle_decode, split_aligned,
+                     tight_tol, to_dev)
 from paged_kv_decode_09_gb300 import api
 from paged_kv_decode_09_gb300 import workloads as W
 
@@ -135,12 +136,13 @@ def test_window_split_combine_and_plan():
     out = torch.full_like(q, float("nan"))
     api.paged_decode_split(pool, 0, q, bt, sl, wl.scale, out, ws)
     api.paged_decode_combine(sl, cfg.n_q_heads, cfg.n_kv_heads, wl.bt_stride, chunks, ws.tensor,
-                             out, window=window)
+                             out, window=window, kv_dtype=pool.dtype)
     torch.cuda.synchronize()
     _check(out.cpu().numpy(), oracle_decode(wl, host, window=window))
     rps, first, last = api.paged_decode_plan(sl, cfg.n_kv_heads, wl.bt_stride, chunks,
-                                             window=window)
-    o_rps, o_first, o_last, _ = O.plan(wl.seq_lens, cfg.n_kv_heads, chunks, window=window)
+                                             window=window, kv_dtype=pool.dtype)
+    o_rps, o_first, o_last, _ = O.plan(wl.seq_lens, cfg.n_kv_heads, chunks, window=window,
+                                       aligned=split_aligned(pool.dtype))
     np.testing.assert_array_equal(rps.cpu().numpy(), o_rps)
     np.testing.assert_array_equal(first.cpu().numpy(), o_first)
     np.testing.assert_array_equal(last.cpu().numpy(), o_last)

@@ -44,6 +44,13 @@ MUTANTS = {
     "segment_start": ("int64_t a = (int64_t)n_kv * row_page_start[i] + h * npg, b = a + npg;",
                       "int64_t a = (int64_t)n_kv * row_page_start[i] + h, b = a + npg;"),
     "append_slot": ("int slot = pos % ORACLE_PAGE;", "int slot = L % ORACLE_PAGE;"),
+    "aligned_chunk_end": ("hi[n] = base + h * npg + (q + 1) * npg / c;",
+                          "hi[n] = base + h * npg + (q + 1) * npg / c + (q + 1 < c);"),
+    "aligned_balance_bound": ("t1 = 11 * T / (10 * (int64_t)num_chunks);",
+                              "t1 = 12 * T / (10 * (int64_t)num_chunks);"),
+    "aligned_without_room": ("for (int64_t t = t0; t1 > t0 && t <= t1; ++t)",
+                             "for (int64_t t = t0; t1 >= t0 && t <= t1; ++t)"),
+    "aligned_group_size": ("int64_t m = t / npg;", "int64_t m = (t + npg - 1) / npg;"),
     "partial_base_e": ("double p = exp2(s[t - t0] - m);", "double p = exp(s[t - t0] - m);"),
     "bf16_eight_fraction_bits": ("ulp = ldexp(1.0, e - 8); /* 8 significant bits */",
                                  "ulp = ldexp(1.0, e - 9); /* 8 significant bits */"),

@@ -1,10 +1,11 @@
 """Pins for the oracle's work split (plan) and its kv_append.
 
-Plan: units are (row, KV head, page) tiles in that order; of C chunks asked
-for, Ce = min(C, T) are used, chunk k covering [floor(k T / Ce),
-floor((k + 1) T / Ce)), so none is empty; a segment (row, head) is split into
-pieces by the chunks it meets.  Pinned to hand-derived fixtures and to a
-brute-force enumeration of every unit.
+Plan: units are (row, KV head, page) tiles in that order; in the uniform
+split, of C chunks asked for, Ce = min(C, T) are used, chunk k covering
+[floor(k T / Ce), floor((k + 1) T / Ce)), so none is empty; a segment (row,
+head) is split into pieces by the chunks it meets.  Pinned to hand-derived
+fixtures and to a brute-force enumeration of every unit.  The segment-aligned
+split is pinned to hand-derived cases and to its structure.
 
 Append (tinyllm, "The repository currently provides": block table per active
 sequence; "Known limitations": 16-token pages): row i's new token goes to page
@@ -103,6 +104,106 @@ def test_windowed_plan_matches_unit_enumeration(seed):
             for L, p in zip(lens, pages):  # contiguous run starting at floor(a / 16)
                 if p:
                     assert p == list(range(max(0, int(L) - window) // 16, p[-1] + 1))
+
+
+# The segment-aligned split (f16 and bf16 KV).  For a cap of t units a
+# chunk, a row of npg >= t pages cuts each KV head's segment into
+# c = ceil(npg / t) chunks (chunk q: pages [floor(q npg / c), floor((q+1) npg / c))),
+# a shorter row groups m = floor(t / npg) whole segments a chunk; t is the
+# first cap from ceil(T / C) to floor(1.1 T / C) whose chunks number at most
+# C; with a single cap in that range, or none fitting, the split is uniform.
+
+def test_aligned_split_hand_worked():
+    """Rows of 470 and 70 tokens = 30 and 5 pages, 2 KV heads, 5 chunks:
+    T = 70, caps 14 .. 15.  Cap 14: row 0 needs 2 * ceil(30 / 14) = 6 > 5.
+    Cap 15: 2 * 2 chunks of 15 pages for row 0, and row 1 (5 < 15) groups
+    floor(15 / 5) = 3 >= 2 heads in one chunk: 5 chunks."""
+    lens = np.array([470, 70], np.int32)
+    lo, hi = O.chunk_ranges(lens, 2, 5, aligned=True)
+    np.testing.assert_array_equal(lo, [0, 15, 30, 45, 60])
+    np.testing.assert_array_equal(hi, [15, 30, 45, 60, 70])
+    rps, first, last, T = O.plan(lens, 2, 5, aligned=True)
+    assert T == 70
+    np.testing.assert_array_equal(first, [0, 2, 4, 4])
+    np.testing.assert_array_equal(last, [1, 3, 4, 4])
+    # the uniform split of the same call: [0,14) [14,28) [28,42) [42,56) [56,70)
+    rps, first, last, T = O.plan(lens, 2, 5, aligned=False)
+    np.testing.assert_array_equal(first, [0, 2, 4, 4])
+    np.testing.assert_array_equal(last, [2, 4, 4, 4])
+
+
+def test_aligned_split_whole_segments_of_a_long_and_a_short_row():
+    """30 and 3 pages, 8 KV heads, 9 chunks: T = 264, caps 30 .. 32.  Cap 30:
+    row 0 gives each head one chunk (30 >= 30, ceil(30 / 30) = 1), row 1
+    groups floor(30 / 3) = 10 >= 8 heads in one chunk: 9 chunks."""
+    lens = np.array([480, 48], np.int32)
+    lo, hi = O.chunk_ranges(lens, 8, 9, aligned=True)
+    np.testing.assert_array_equal(lo, [0, 30, 60, 90, 120, 150, 180, 210, 240])
+    np.testing.assert_array_equal(hi, [30, 60, 90, 120, 150, 180, 210, 240, 264])
+    rps, first, last, T = O.plan(lens, 8, 9, aligned=True)
+    np.testing.assert_array_equal(first, list(range(8)) + [8] * 8)
+    np.testing.assert_array_equal(last, list(range(8)) + [8] * 8)
+
+
+def _same_plan(lens, n_kv, C):
+    for a, b in zip(O.plan(lens, n_kv, C, aligned=True), O.plan(lens, n_kv, C, aligned=False)):
+        np.testing.assert_array_equal(a, b)
+    lo, hi = O.chunk_ranges(lens, n_kv, C, aligned=True)
+    T = n_kv * int(sum((int(L) + 15) // 16 for L in lens))
+    np.testing.assert_array_equal(lo, [k * T // C for k in range(C)])
+
+
+def test_aligned_split_falls_back_when_no_cap_fits():
+    """30 and 4 pages, 8 KV heads, 10 chunks: T = 272, caps 28 .. 29.  Row 0
+    alone needs 8 * ceil(30 / 28) = 8 * ceil(30 / 29) = 16 > 10 chunks."""
+    _same_plan(np.array([480, 64], np.int32), 8, 10)
+
+
+def test_aligned_split_needs_room_above_the_even_share():
+    """6, 1 and 1 pages, 2 KV heads, 6 chunks: T = 16, ceil(T / C) = 3 but
+    floor(1.1 T / C) = 2: a single cap (none above the even share), so the
+    split is uniform although cap 3 would need only 6 chunks."""
+    _same_plan(np.array([90, 5, 1], np.int32), 2, 6)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_aligned_split_structure(seed):
+    """Whatever split comes out tiles [0, T) with non-empty chunks, at most C
+    of them; when it is not the uniform one, every chunk lies inside one
+    segment or is whole segments of one row, a segment split over several
+    chunks starts and ends on chunk boundaries, and no chunk holds more than
+    max(ceil(T / C), floor(1.1 T / C)) units."""
+    rng = np.random.default_rng(300 + seed)
+    rows = int(rng.integers(1, 40))
+    lens = rng.integers(0, 3000, rows).astype(np.int32)
+    lens[rng.integers(0, rows, 2)] = 0
+    n_kv = int(rng.choice([1, 2, 4, 8]))
+    for C in (1, 4, 37, 152, 456, 5000):
+        rps, first, last, T = O.plan(lens, n_kv, C, aligned=True)
+        lo, hi = O.chunk_ranges(lens, n_kv, C, aligned=True)
+        if T == 0:
+            assert len(lo) == 0
+            continue
+        assert lo[0] == 0 and hi[-1] == T and np.all(hi > lo) and np.all(lo[1:] == hi[:-1])
+        assert len(lo) <= C
+        ulo, uhi = O.chunk_ranges(lens, n_kv, C, aligned=False)
+        if len(lo) == len(ulo) and np.array_equal(lo, ulo):
+            continue  # the uniform split (possibly also what alignment gives)
+        npg = np.diff(rps)
+        seg_start = np.concatenate([[0], np.cumsum(np.repeat(npg, n_kv))])
+        seg_row = np.repeat(np.arange(rows), n_kv)
+        bounds = set(lo.tolist()) | {T}
+        for a, b in zip(lo, hi):
+            j0 = np.searchsorted(seg_start, a, "right") - 1
+            j1 = np.searchsorted(seg_start, b, "left") - 1
+            if j0 != j1:  # several segments: all whole, of one row
+                assert seg_start[j0] == a and seg_start[j1 + 1] == b
+                assert seg_row[j0] == seg_row[j1]
+        for j in range(rows * n_kv):
+            if first[j] >= 0 and first[j] != last[j]:
+                assert seg_start[j] in bounds and seg_start[j + 1] in bounds
+        assert 11 * T // (10 * C) > -(-T // C)  # room above the even share
+        assert np.max(hi - lo) <= 11 * T // (10 * C)
 
 
 @pytest.mark.parametrize("dtype", [W.F16, W.Q8_0])
