@@ -301,7 +301,7 @@ pkv_status attention_mq_impl(const pkv_pool* pool, int layer, const float* q, co
   a.window = pool->window[layer];
   a.q_len = q_len;
   a.vchunks = num_chunks;
-  a.aligned_split = 0;
+  a.aligned_split = split_may_align(pool->dtype);
   a.out = out;
   a.status = pool->status;
   const pkv::TileMaps* maps = nullptr;

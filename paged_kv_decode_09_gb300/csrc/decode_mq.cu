@@ -106,8 +106,9 @@ struct MqSmem {
   static constexpr uint32_t kQ = kMrgMl + kWarps * kWarpCols * 2 * 4;  // f32 KV: [warps][8][kQStride] q
   static constexpr uint32_t kCtl =
       kQ + (DT == PKV_KV_F32 ? kWarps * kWarpCols * kQStride * 4 : 0);
-  static constexpr uint32_t kRows = kCtl + 16;
-  static size_t bytes(int rows) { return kAlign + kRows + (2 * static_cast<size_t>(rows) + 1) * 4; }
+  static constexpr uint32_t kSplit = kCtl + 16;  // the work split
+  static constexpr uint32_t kRows = kSplit + 16;  // row_start, lens, chunks before each row
+  static size_t bytes(int rows) { return kAlign + kRows + plan_ints(rows) * 4; }
   static_assert(Tiles<DT>::kCodes % 1024 == 0, "tile stages keep the swizzle atom alignment");
 };
 
@@ -626,11 +627,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   grid_launch_dependents();
   plan_rows(a.seq_lens, a.num_rows, a.bt_stride, plan_window,
             blockIdx.x == 0 ? a.status : nullptr, lens, row_start, a.q_len);
-
-  const long long T = static_cast<long long>(a.n_kv) * row_start[a.num_rows];
-  const int C = used_chunks(T, gridDim.x), k = blockIdx.x;
-  const long long c_begin = k < C ? static_cast<long long>(k) * T / C : T;
-  const long long c_end = k < C ? static_cast<long long>(k + 1) * T / C : T;
+  int* pc = lens + a.num_rows;
+  plan_split(row_start, a.num_rows, a.n_kv, gridDim.x, a.aligned_split,
+             reinterpret_cast<Split*>(smem + SM::kSplit), pc);
+  // read from shared memory where used (at each piece): no registers held across the loop
+  const Split* sp = reinterpret_cast<const Split*>(smem + SM::kSplit);
+  const int k = blockIdx.x;
+  long long c_begin, c_end;
+  chunk_range(*sp, k, row_start, pc, a.num_rows, a.n_kv, c_begin, c_end);
 
   // Rows without tokens (or shorter than q_len): zero outputs for this pass.
   if (k == 0) {
@@ -747,7 +751,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int L = lens[i];
     const int p0 = window_start(L, plan_window) / kPage;
     const long long j = static_cast<long long>(i) * a.n_kv + h;
-    const int k0 = chunk_of(seg_start, T, C), k1 = chunk_of(seg_end - 1, T, C);
+    int k0, k1;
+    segment_chunks(*sp, i, h, row_start, pc, a.num_rows, a.n_kv, k0, k1);
 
     // the lane's score columns 4t + tig: attended positions [col_lo, col_hi)
     int col_lo[2] = {0, 0}, col_hi[2] = {0, 0};
@@ -1003,8 +1008,9 @@ struct MqtSmem {
   static constexpr uint32_t kFull = kScl + kStages * Tiles<DT>::kScales;
   static constexpr uint32_t kEmpty = kFull + kStages * 8;
   static constexpr uint32_t kCtl = kEmpty + kStages * 8;
-  static constexpr uint32_t kRows = kCtl + 16;
-  static size_t bytes(int rows) { return kAlign + kRows + (2 * static_cast<size_t>(rows) + 1) * 4; }
+  static constexpr uint32_t kSplit = kCtl + 16;  // the work split
+  static constexpr uint32_t kRows = kSplit + 16;  // row_start, lens, chunks before each row
+  static size_t bytes(int rows) { return kAlign + kRows + plan_ints(rows) * 4; }
 };
 
 template <int DT, int NT, int TS>
@@ -1051,11 +1057,14 @@ __global__ void __launch_bounds__(kThreads, team_ctas(NT))
   grid_launch_dependents();
   plan_rows(a.seq_lens, a.num_rows, a.bt_stride, plan_window,
             blockIdx.x == 0 ? a.status : nullptr, lens, row_start, a.q_len);
-
-  const long long T = static_cast<long long>(a.n_kv) * row_start[a.num_rows];
-  const int C = used_chunks(T, a.vchunks), k = blockIdx.x * kTeams + team;
-  const long long c_begin = k < C ? static_cast<long long>(k) * T / C : T;
-  const long long c_end = k < C ? static_cast<long long>(k + 1) * T / C : T;
+  int* pc = lens + a.num_rows;
+  plan_split(row_start, a.num_rows, a.n_kv, a.vchunks, a.aligned_split,
+             reinterpret_cast<Split*>(smem + SM::kSplit), pc);
+  // read from shared memory where used (at each piece): no registers held across the loop
+  const Split* sp = reinterpret_cast<const Split*>(smem + SM::kSplit);
+  const int k = blockIdx.x * kTeams + team;
+  long long c_begin, c_end;
+  chunk_range(*sp, k, row_start, pc, a.num_rows, a.n_kv, c_begin, c_end);
 
   if (blockIdx.x == 0) {  // rows without tokens (or shorter than q_len): zeros
     for (int i = 0; i < a.num_rows; ++i)
@@ -1169,7 +1178,8 @@ __global__ void __launch_bounds__(kThreads, team_ctas(NT))
     const int L = lens[i];
     const int p0 = window_start(L, plan_window) / kPage;
     const long long j = static_cast<long long>(i) * a.n_kv + h;
-    const int k0 = chunk_of(seg_start, T, C), k1 = chunk_of(seg_end - 1, T, C);
+    int k0, k1;
+    segment_chunks(*sp, i, h, row_start, pc, a.num_rows, a.n_kv, k0, k1);
     const int P0 = L - a.q_len + a.q0;  // position of the pass's first query
 
     // the lane's score columns cbase + 4t + tig: attended positions [col_lo, col_hi)
