@@ -196,13 +196,31 @@ KERNEL_SOURCES = {  # the files each decode kernel is compiled from (besides hea
 }
 
 
-def kernel_source_hash(kernel: str) -> str:
-    src = os.path.join(ROOT, "paged_kv_decode_09_gb300", "csrc")
+_TOKEN = re.compile(r'"(?:\\.|[^"\\\n])*"|/\*.*?\*/|//[^\n]*', re.S)
+
+
+def code_only(text: str) -> str:
+    """A C++/CUDA source without its comments and with its whitespace collapsed
+    (string literals kept as they are): what decides the compiled kernel."""
+    stripped = _TOKEN.sub(lambda m: m.group(0) if m.group(0).startswith('"') else " ", text)
+    return " ".join(stripped.split())
+
+
+def code_hash(paths) -> str:
+    """Hash of the code of these files (comments and layout ignored)."""
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(src, name), "rb") as f:
-            h.update(f.read())
+    for path in paths:
+        with open(path, encoding="utf-8") as f:
+            h.update(code_only(f.read()).encode())
+        h.update(b"\0")
     return h.hexdigest()[:16]
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Identifies the code a decode kernel is compiled from: a profile taken on
+    it stays valid through edits of comments, not of code."""
+    src = os.path.join(ROOT, "paged_kv_decode_09_gb300", "csrc")
+    return code_hash(os.path.join(src, name) for name in KERNEL_SOURCES[kernel])
 
 
 def profile_traffic(workload: str, kernel: str = "paged_decode_kernel", q_len: int = 1):

@@ -9,11 +9,13 @@
 // Here the pages are read in place.
 //
 // Work split.  The batch is a list of T = n_kv * sum_i ceil(L_i/16) units,
-// one per (row, KV head, page) in that order.  With C = min(grid, T) chunks,
-// CTA k < C takes units [floor(kT/C), floor((k+1)T/C)) (never empty; CTAs
-// k >= C idle), so every CTA streams the same number of
-// 4 KiB (f16) or 2176-byte (q8_0) tiles whatever the length mix: one 40k-token
-// row and many 16-token rows keep all SMs equally busy.  The units of one
+// one per (row, KV head, page) in that order, cut into contiguous chunks of
+// nearly equal size, one per CTA (plan_split): uniform for q8_0 and f32 KV
+// (CTA k < min(grid, T) takes [floor(kT/C), floor((k+1)T/C))), aligned to the
+// (row, KV head) segments for f16 and bf16 (a split segment ends where a
+// chunk ends); CTAs beyond the chunks idle.  Every CTA thus streams about the
+// same number of 4 KiB (f16) or 2176-byte (q8_0) tiles whatever the length
+// mix: one 40k-token row and many 16-token rows keep all SMs busy.  The units of one
 // (row, head) that fall in one CTA form a "piece"; a piece that is the whole
 // segment writes the output, otherwise it writes a partial state to slot
 // k + (i * n_kv + h) (pieces in unit order increase k, j or both, so the slot

@@ -50,3 +50,21 @@ def test_row_tokens_edges():
     assert bench.row_tokens(500, 100, 1) == 100
     assert bench.row_tokens(500, 100, 8) == 107
     assert bench.row_tokens(np.int32(37)) == 37
+
+
+def test_source_hash_follows_code_not_comments(tmp_path):
+    """A profile stays valid through edits of comments and layout, and not
+    through an edit of code: string literals (inline PTX) count as code."""
+    base = 'int f(int a) {  // doubles\n  return 2 * a; /* fast */\n}\nconst char* s = "x // y";\n'
+    same = '/* header */\nint f(int a)\n{\n    return 2 * a;\n}\nconst char* s = "x // y";  // ptx\n'
+    other = 'int f(int a) { return 3 * a; }\nconst char* s = "x // y";\n'
+    lit = 'int f(int a) { return 2 * a; }\nconst char* s = "x // z";\n'
+    paths = {}
+    for name, text in (("base", base), ("same", same), ("other", other), ("lit", lit)):
+        paths[name] = tmp_path / f"{name}.cu"
+        paths[name].write_text(text)
+    h = {k: bench.code_hash([str(p)]) for k, p in paths.items()}
+    assert h["base"] == h["same"]
+    assert h["base"] != h["other"]
+    assert h["base"] != h["lit"]
+    assert bench.code_only(base) == 'int f(int a) { return 2 * a; } const char* s = "x // y";'
