@@ -4,10 +4,12 @@
 A step is one pass of the whole hot path over one batch for one layer's pool:
 pkv_decode_step, which stores each row's new token (kv_append's encoding) and
 runs split-KV paged decode attention with its in-kernel merge over lengths
-that include the token -- one kernel launch.  Default workload: the 8B layer
-shape with f16 KV (8 rows, L ~ U[1024, 8192], 32 q / 8 KV heads, head_dim 128).
-Steps rotate over several layer pools whose total size is more than 4x the
-L2 cache, so every step reads KV from HBM.
+that include the token -- one kernel launch.  Default workload: the largest
+single-GPU one, the 8B layer shape with q8_0 KV (32 rows, L ~ U[4096, 32768],
+32 q / 8 KV heads, head_dim 128); the 8B f16 layer (8 rows, L ~ U[1024, 8192])
+is timed the same way in the same run and reported under "also".  Steps rotate
+over several layer pools whose total size is more than 4x the L2 cache, so
+every step reads KV from HBM.
 
 Metric (bytes counted per step: K and V of every attended token, q, out):
   value      KV GB/s, device-resident inputs, CUDA events on the stream
@@ -48,7 +50,14 @@ def parse_args():
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=5000)
     p.add_argument("--warmup", type=int, default=20)
-    p.add_argument("--workload", default="llama8b_f16")
+    p.add_argument("--workload", default="llama8b_q8_0",
+                   help="the workload of the reported value (default: the largest, 8B q8_0)")
+    p.add_argument("--also", default="llama8b_f16",
+                   help="comma-separated workloads timed the same way after the main one and\n"
+                        "reported under \"also\" (\"\" for none)")
+    p.add_argument("--lead-seconds", type=float, default=0.25,
+                   help="untimed steps run straight into the timed ones (clock samples under\n"
+                        "load; the start event fires on a busy stream)")
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--layers", type=int, default=0, help="layer pools to rotate (0: auto)")
     p.add_argument("--chunks", type=int, default=0, help="work chunks (0: one per resident CTA)")
@@ -258,106 +267,248 @@ def fill_pool(api, pool, layers, seed):
     torch.cuda.synchronize()
 
 
+class StepSetup:
+    """One workload's pool, inputs and decode-step call, ready to time."""
+
+    def __init__(self, args, name, rank, dev):
+        import numpy as np
+        import torch
+
+        from paged_kv_decode_09_gb300 import api
+        from paged_kv_decode_09_gb300 import workloads as W
+
+        self.torch, self.api, self.W = torch, api, W
+        wl = W.draw(name)
+        cfg = wl.cfg
+        self.wl, self.cfg = wl, cfg
+        layer_bytes = 2 * api.KVPool.bytes(1, wl.num_pages, cfg.n_kv_heads, cfg.dtype, 0) + \
+            2 * api.KVPool.bytes(1, wl.num_pages, cfg.n_kv_heads, cfg.dtype, 1)
+        self.layer_bytes = layer_bytes
+        layers = args.layers or max(2, min(cfg.model_layers, -(-4 * L2_BYTES // layer_bytes)))
+        self.layers = layers
+        pool = api.KVPool(layers, wl.num_pages, cfg.n_kv_heads, cfg.dtype, device=dev)
+        fill_pool(api, pool, layers, seed=1234 + rank)
+        for layer in range(layers):
+            pool.set_window(layer, args.window)
+        self.pool = pool
+
+        t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+        QL = args.q_len
+        self.QL = QL
+        if QL > 1:  # verification / chunk step: q_len new tokens per row
+            hq_np, hk_np, hv_np = W.mq_inputs(wl, QL)
+            q, k_new, v_new = t(hq_np), t(hk_np), t(hv_np)
+            ws = api.WorkspaceMQ(pool, cfg.n_q_heads, wl.rows, QL, args.chunks)
+            cols = QL * cfg.group  # (query, head) columns; the kernel's pass width follows them
+            if cfg.dtype == W.F32 or cols <= (4 if cfg.dtype == W.BF16 else 8):
+                width = min(cols, 8)
+                kname = "paged_decode_mq_kernel"  # the warps of a CTA read different pages
+            else:  # teams of 2 or 4 warps share every page
+                if cfg.dtype == W.BF16:
+                    width = 8 if cols <= 8 else 16
+                else:  # f16: four warps of 4 or 8 columns; q8_0: two or four of 8
+                    width = 16 if cols <= 16 else 32
+                kname = "paged_decode_mqt_kernel"
+            passes = -(-QL // max(1, width // cfg.group))
+        else:
+            q, k_new, v_new = t(wl.q), t(wl.k_new), t(wl.v_new)
+            ws = api.Workspace(pool, cfg.n_q_heads, wl.rows, args.chunks)
+            passes = 1
+            kname = "paged_decode_kernel"
+        self.passes, self.kname, self.ws = passes, kname, ws
+        bt, sl = t(wl.block_table), t(wl.seq_lens)
+        out = torch.empty_like(q)
+        self.q, self.k_new, self.v_new, self.bt, self.sl, self.out = q, k_new, v_new, bt, sl, out
+        self.L = L = api.lib()
+        self.stream = torch.cuda.current_stream(dev)
+        self.sp = ctypes.c_void_p(self.stream.cuda_stream)
+        P = lambda x: ctypes.c_void_p(x.data_ptr())  # noqa: E731
+        self.a_q, self.a_k, self.a_v, self.a_bt, self.a_sl, self.a_out, self.a_ws = map(
+            P, (q, k_new, v_new, bt, sl, out, ws.tensor))
+        self.scale = ctypes.c_float(wl.scale)
+        self.nbytes = step_bytes(wl, args.window, QL)
+        self.tokens = attended_tokens(wl, args.window, QL)
+
+    def chk(self, st, what):
+        if st:
+            raise self.api.PkvError(st, what, self.L.pkv_last_error_message().decode())
+
+    def call(self, layer, pq, pk, pv, pbt, psl, pout, on):
+        """One decode step through the C ABI (the step's inputs at these pointers)."""
+        L, wl, cfg, ws = self.L, self.wl, self.cfg, self.ws
+        H, R, NQ, S, CH = self.pool.handle, wl.rows, cfg.n_q_heads, wl.bt_stride, ws.num_chunks
+        if self.QL > 1:
+            self.chk(L.pkv_decode_step_mq(H, layer, pq, pk, pv, pbt, S, psl, R, self.QL, NQ,
+                                          self.scale, pout, self.a_ws, ws.nbytes, CH, on),
+                     "pkv_decode_step_mq")
+        else:
+            self.chk(L.pkv_decode_step(H, layer, pq, pk, pv, pbt, S, psl, R, NQ, self.scale, pout,
+                                       self.a_ws, ws.nbytes, CH, on), "pkv_decode_step")
+
+    def step(self, layer, on=None):
+        self.call(layer, self.a_q, self.a_k, self.a_v, self.a_bt, self.a_sl, self.a_out,
+                  self.sp if on is None else on)
+
+    def time_steps(self, K, warmup, world, local, lead_s):
+        """Mean time of K back-to-back steps (max over ranks), with the clocks
+        sampled meanwhile.
+
+        Untimed lead steps run first, for lead_s seconds, straight into the
+        timed ones: the clock sampler sees the GPU under this load, and the
+        start event fires on a busy stream, so the timed region holds the K
+        steps and not the latency of the first launch.  The two events are
+        the only ones in the region: an event between launches would add its
+        own gap and break the programmatic dependent launch."""
+        torch = self.torch
+        for w in range(warmup):
+            self.step(w % self.layers)
+        torch.cuda.synchronize()
+        assert self.pool.read_status() == 0, "device status word set during warm-up"
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        clocks = ClockSampler(local)
+        barrier(world)
+        torch.cuda.synchronize()
+        clocks.start()
+        n = 0
+        t_end = time.perf_counter() + lead_s
+        while n < 3 or time.perf_counter() < t_end:
+            self.step(n % self.layers)
+            n += 1
+        e0.record(self.stream)
+        for s in range(K):
+            self.step((n + s) % self.layers)
+        e1.record(self.stream)
+        torch.cuda.synchronize()
+        clock_info = clocks.stop()
+        barrier(world)
+        total_ms = max_over_ranks(e0.elapsed_time(e1), world)
+        assert self.pool.read_status() == 0, "device status word set during the timed steps"
+        return total_ms, clock_info, n
+
+    def roofline(self, launch_ms, peak, peak_src, window):
+        W = self.W
+        achieved = self.nbytes / (launch_ms / 1e3) / 1e9
+        return {
+            "bound": "hbm", "kernel": f"{self.kname}<{W.DTYPE_NAMES[self.cfg.dtype]}>, G={self.cfg.group}",
+            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (copy bandwidth)",
+            # DRAM bytes of one launch (one pass: a step of the several-query
+            # kernel is `launches_per_step` of them)
+            "traffic": None if window else profile_traffic(self.cfg.name, self.kname, self.QL),
+            "mean_launch_us": round(launch_ms * 1e3, 3),
+            "timing": "events around the K back-to-back launches of the timed region, "
+                      "after untimed lead steps on the same stream",
+        }
+
+    def config(self, args, world):
+        wl, cfg, W, ws = self.wl, self.cfg, self.W, self.ws
+        QL, passes = self.QL, self.passes
+        return {
+            "workload": cfg.name, "description": cfg.description, "rows": wl.rows,
+            "n_q_heads": cfg.n_q_heads, "n_kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim,
+            "kv_dtype": W.DTYPE_NAMES[cfg.dtype], "tokens_attended": self.tokens,
+            "pages_per_layer": wl.num_pages, "layers_rotated": self.layers,
+            "l2": f"inputs larger than L2: {self.layers} layer pools of "
+                  f"{self.layer_bytes / 2**20:.0f} MiB rotated (> 4x the 126 MiB L2)",
+            "chunks": ws.num_chunks, "bytes_per_step": self.nbytes,
+            "parallelism": f"replicas x{world}",
+            **({"window": args.window} if args.window else {}),
+            **({"q_len": QL, "launches_per_step": passes} if QL > 1 else {}),
+            "workspace_bytes": ws.nbytes,
+            # traffic beyond the algorithmic bytes and not counted in them: the
+            # block-table entries of the attended pages (once per launch; a
+            # window that does not start on a page boundary touches one more
+            # page), and at most every workspace byte written once and read once
+            "uncounted_bytes": {"block_table": 4 * passes * int(sum(
+                                    W.pages_for(row_tokens(int(L), args.window, QL))
+                                    + (1 if args.window and int(L) else 0)
+                                    for L in wl.seq_lens)),
+                                "workspace_max": 2 * ws.nbytes},
+        }
+
+
 def run_ours(args, rank, world, local):
-    import numpy as np
     import torch
 
-    from paged_kv_decode_09_gb300 import api
     from paged_kv_decode_09_gb300 import workloads as W
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl = W.draw(args.workload)
-    cfg = wl.cfg
-    layer_bytes = 2 * api.KVPool.bytes(1, wl.num_pages, cfg.n_kv_heads, cfg.dtype, 0) + \
-        2 * api.KVPool.bytes(1, wl.num_pages, cfg.n_kv_heads, cfg.dtype, 1)
-    layers = args.layers or max(2, min(cfg.model_layers, -(-4 * L2_BYTES // layer_bytes)))
-    pool = api.KVPool(layers, wl.num_pages, cfg.n_kv_heads, cfg.dtype, device=dev)
-    fill_pool(api, pool, layers, seed=1234 + rank)
-    for layer in range(layers):
-        pool.set_window(layer, args.window)
-
-    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
-    QL = args.q_len
-    if QL > 1:  # verification / chunk step: q_len new tokens per row
-        hq_np, hk_np, hv_np = W.mq_inputs(wl, QL)
-        q, k_new, v_new = t(hq_np), t(hk_np), t(hv_np)
-        ws = api.WorkspaceMQ(pool, cfg.n_q_heads, wl.rows, QL, args.chunks)
-        cols = QL * cfg.group  # (query, head) columns; the kernel's pass width follows them
-        if cfg.dtype == W.F32 or cols <= (4 if cfg.dtype == W.BF16 else 8):
-            width = min(cols, 8)
-            kname = "paged_decode_mq_kernel"  # the warps of a CTA read different pages
-        else:  # teams of 2 or 4 warps share every page
-            if cfg.dtype == W.BF16:
-                width = 8 if cols <= 8 else 16
-            else:  # f16: four warps of 4 or 8 columns; q8_0: two or four of 8
-                width = 16 if cols <= 16 else 32
-            kname = "paged_decode_mqt_kernel"
-        passes = -(-QL // max(1, width // cfg.group))
-    else:
-        q, k_new, v_new = t(wl.q), t(wl.k_new), t(wl.v_new)
-        ws = api.Workspace(pool, cfg.n_q_heads, wl.rows, args.chunks)
-        passes = 1
-        kname = "paged_decode_kernel"
-    bt, sl = t(wl.block_table), t(wl.seq_lens)
-    out = torch.empty_like(q)
-    L = api.lib()
-    stream = torch.cuda.current_stream(dev)
-    sp = ctypes.c_void_p(stream.cuda_stream)
-    P = lambda x: ctypes.c_void_p(x.data_ptr())  # noqa: E731
-    a_q, a_k, a_v, a_bt, a_sl, a_out, a_ws = map(P, (q, k_new, v_new, bt, sl, out, ws.tensor))
-    H, R, NQ, S, CH = pool.handle, wl.rows, cfg.n_q_heads, wl.bt_stride, ws.num_chunks
-    scale = ctypes.c_float(wl.scale)
-
-    def chk(st, what):
-        if st:
-            raise api.PkvError(st, what, L.pkv_last_error_message().decode())
-
-    def step(layer, on=sp):
-        if QL > 1:
-            chk(L.pkv_decode_step_mq(H, layer, a_q, a_k, a_v, a_bt, S, a_sl, R, QL, NQ, scale,
-                                     a_out, a_ws, ws.nbytes, CH, on), "pkv_decode_step_mq")
-        else:
-            chk(L.pkv_decode_step(H, layer, a_q, a_k, a_v, a_bt, S, a_sl, R, NQ, scale, a_out,
-                                  a_ws, ws.nbytes, CH, on), "pkv_decode_step")
-
-    for w in range(args.warmup):
-        step(w % layers)
-    torch.cuda.synchronize()
-    assert pool.read_status() == 0, "device status word set during warm-up"
-
-    # The timed steps are back-to-back launches of the decode kernel on one
-    # stream, bracketed by one pair of events (an event between launches would
-    # add its own gap and break the programmatic dependent launch).
+    peak, peak_src = read_peak()
+    st = StepSetup(args, args.workload, rank, dev)
+    wl, cfg = st.wl, st.cfg
     K = args.steps
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local)
-    barrier(world)
-    torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.1)
-    e0.record(stream)
-    for s in range(K):
-        step(s % layers)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    clock_info = clocks.stop()
-    barrier(world)
-    total_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    total_ms, clock_info, lead = st.time_steps(K, args.warmup, world, local, args.lead_seconds)
     # the only kernel in the timed region: a step is `passes` back-to-back
     # launches of it; the roofline takes the step (all passes) as the unit
     launch_ms = total_ms / K
-    assert pool.read_status() == 0, "device status word set during the timed steps"
+    graph = None if args.no_graph else graph_timing(torch, dev, st.step, st.layers)
+    e2e = e2e_timing(st, K, args.warmup, world, dev)
 
-    graph = None if args.no_graph else graph_timing(torch, dev, step, layers)
+    nbytes = st.nbytes
+    step_s = total_ms / 1e3 / K
+    value = world * nbytes / step_s / 1e9
+    result = {
+        "metric": "paged decode-attn KV GB/s & % of GB300 HBM peak; rows*tokens/s at 1 GPU",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / K, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": W.DTYPE_NAMES[cfg.dtype] + " KV, f32 compute",
+        "data": "synthetic: seeded lengths/block tables/q; KV N(0,1) stored by kv_append",
+        "config": {**st.config(args, world), "lead_steps": lead},
+        "frac_of_hbm_peak": round(value / world / peak, 4),
+        "rows_tokens_per_s": round(world * st.tokens / step_s, 1),
+        "rows_per_s": round(world * wl.rows / step_s, 1),
+        "roofline": st.roofline(launch_ms, peak, peak_src, args.window),
+        "e2e": e2e,
+        "gpu_launches": K * st.passes,
+        "graph": graph,
+        "clocks": clock_info,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(wl, st.pool, args.cpu_seconds, args.window,
+                                              args.q_len, st.q.cpu().numpy())
+    # The other workloads of the 70% bar (the 8B f16 layer beside the 8B q8_0
+    # headline), each timed the same way and reported with its own roofline.
+    also = {}
+    for name in [x for x in args.also.split(",") if x and x != args.workload]:
+        del st
+        torch.cuda.empty_cache()
+        st = StepSetup(args, name, rank, dev)
+        t_ms, clk, n_lead = st.time_steps(K, args.warmup, world, local, args.lead_seconds)
+        g = None if args.no_graph else graph_timing(torch, dev, st.step, st.layers)
+        s_ = t_ms / 1e3 / K
+        v_ = world * st.nbytes / s_ / 1e9
+        also[name] = {
+            "value": round(v_, 2), "unit": "GB/s", "steps": K, "ms_per_step": round(t_ms / K, 6),
+            "dtype": W.DTYPE_NAMES[st.cfg.dtype] + " KV, f32 compute",
+            "config": {**st.config(args, world), "lead_steps": n_lead},
+            "frac_of_hbm_peak": round(v_ / world / peak, 4),
+            "rows_tokens_per_s": round(world * st.tokens / s_, 1),
+            "roofline": st.roofline(t_ms / K, peak, peak_src, args.window),
+            "gpu_launches": K * st.passes, "graph": g, "clocks": clk,
+        }
+        result["gpu_launches"] += K * st.passes
+    if also:
+        result["also"] = also
+    return result
 
-    # ---- end to end through the C ABI: every step copies its inputs from
-    # pinned host memory and its output back.  As a serving loop would, the
-    # inputs sit in one packed buffer (one copy per step each way) and are
-    # double-buffered: the copy of step s + 1's inputs (on a copy stream)
-    # overlaps step s's kernel, the copy of step s's output (on another)
-    # overlaps step s + 1's.
-    parts = (q, k_new, v_new, bt, sl)
+
+def e2e_timing(st, K, warmup, world, dev):
+    """The same metric end to end through the C ABI: every step copies its
+    inputs from pinned host memory and its output back.  As a serving loop
+    would, the inputs sit in one packed buffer (one copy per step each way) and
+    are double-buffered: the copy of step s + 1's inputs (on a copy stream)
+    overlaps step s's kernel, the copy of step s's output (on another)
+    overlaps step s + 1's."""
+    torch = st.torch
+    parts = (st.q, st.k_new, st.v_new, st.bt, st.sl)
     offs, size = [], 0
     for x in parts:
         offs.append(size)
@@ -366,10 +517,10 @@ def run_ours(args, rank, world, local):
     for x, o in zip(parts, offs):
         hpack[o:o + x.numel() * x.element_size()].copy_(x.cpu().contiguous().view(-1).view(torch.uint8))
     dpack = [torch.empty(size, dtype=torch.uint8, device=dev) for _ in range(2)]
-    douts = [torch.empty_like(out) for _ in range(2)]
-    hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    douts = [torch.empty_like(st.out) for _ in range(2)]
+    hout = [torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory() for _ in range(2)]
     h2d = sum(x.numel() * x.element_size() for x in parts)
-    d2h = out.numel() * out.element_size()
+    d2h = st.out.numel() * st.out.element_size()
     ptrs = [[ctypes.c_void_p(d.data_ptr() + o) for o in offs] for d in dpack]
     s_h2d, s_d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     # The copies and the stream edges go straight to the CUDA driver (the
@@ -391,12 +542,13 @@ def run_ours(args, rank, world, local):
         return e_
 
     ev_in, ev_done, ev_out = ([new_event() for _ in range(2)] for _ in range(3))
+    stream = st.stream
     c_st, c_h2d, c_d2h = (ctypes.c_void_p(x.cuda_stream) for x in (stream, s_h2d, s_d2h))
     hsrc = ctypes.c_void_p(hpack.data_ptr())
     dsts = [d.data_ptr() for d in dpack]
     oh = [ctypes.c_void_p(x.data_ptr()) for x in hout]
+    po_ = [ctypes.c_void_p(x.data_ptr()) for x in douts]
     od = [x.data_ptr() for x in douts]
-    po_ = [ctypes.c_void_p(x) for x in od]
 
     def e2e_step(s_, layer):
         b = s_ % 2
@@ -408,103 +560,36 @@ def run_ours(args, rank, world, local):
         if s_ >= 2:
             cu.cuStreamWaitEvent(c_st, ev_out[b], 0)  # step s - 2's output left this buffer
         pq, pk, pv, pbt, psl = ptrs[b]
-        if QL > 1:
-            chk(L.pkv_decode_step_mq(H, layer, pq, pk, pv, pbt, S, psl, R, QL, NQ, scale,
-                                     po_[b], a_ws, ws.nbytes, CH, sp), "pkv_decode_step_mq")
-        else:
-            chk(L.pkv_decode_step(H, layer, pq, pk, pv, pbt, S, psl, R, NQ, scale, po_[b], a_ws,
-                                  ws.nbytes, CH, sp), "pkv_decode_step")
+        st.call(layer, pq, pk, pv, pbt, psl, po_[b], st.sp)
         cu.cuEventRecord(ev_done[b], c_st)
         cu.cuStreamWaitEvent(c_d2h, ev_done[b], 0)
         cu_ok(cu.cuMemcpyDtoHAsync_v2(oh[b], od[b], d2h, c_d2h), "D2H")
         cu.cuEventRecord(ev_out[b], c_d2h)
 
     Ke = min(K, 2000)
-    for w in range(args.warmup):
-        e2e_step(w, w % layers)
+    for w in range(warmup):
+        e2e_step(w, w % st.layers)
     torch.cuda.synchronize()
     barrier(world)
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
     h0 = time.perf_counter()
     for s_ in range(Ke):
-        e2e_step(s_, s_ % layers)
+        e2e_step(s_, s_ % st.layers)
     host_us = (time.perf_counter() - h0) * 1e6 / Ke  # issue time per step on the host
     stream.wait_stream(s_d2h)  # the last output is on the host
     f1.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), world)
-    assert pool.read_status() == 0, "device status word set during the end-to-end steps"
+    assert st.pool.read_status() == 0, "device status word set during the end-to-end steps"
     torch.testing.assert_close(hout[(Ke - 1) % 2], douts[(Ke - 1) % 2].cpu(), rtol=0, atol=0)
-
-    nbytes = step_bytes(wl, args.window, QL)
-    peak, peak_src = read_peak()
-    step_s = total_ms / 1e3 / K
-    value = world * nbytes / step_s / 1e9
-    achieved = nbytes / (launch_ms / 1e3) / 1e9
-    tokens = attended_tokens(wl, args.window, QL)
-    result = {
-        "metric": "paged decode-attn KV GB/s & % of GB300 HBM peak; rows*tokens/s at 1 GPU",
-        "value": round(value, 2),
-        "unit": "GB/s",
-        "n_gpus": world,
-        "steps": K,
-        "warmup": args.warmup,
-        "ms_per_step": round(total_ms / K, 6),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": W.DTYPE_NAMES[cfg.dtype] + " KV, f32 compute",
-        "data": "synthetic: seeded lengths/block tables/q; KV N(0,1) stored by kv_append",
-        "config": {
-            "workload": cfg.name, "description": cfg.description, "rows": wl.rows,
-            "n_q_heads": cfg.n_q_heads, "n_kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim,
-            "kv_dtype": W.DTYPE_NAMES[cfg.dtype], "tokens_attended": tokens,
-            "pages_per_layer": wl.num_pages, "layers_rotated": layers,
-            "l2": f"inputs larger than L2: {layers} layer pools of "
-                  f"{layer_bytes / 2**20:.0f} MiB rotated (> 4x the 126 MiB L2)",
-            "chunks": CH, "bytes_per_step": nbytes, "parallelism": f"replicas x{world}",
-            **({"window": args.window} if args.window else {}),
-            **({"q_len": QL, "launches_per_step": passes} if QL > 1 else {}),
-            "workspace_bytes": ws.nbytes,
-            # traffic beyond the algorithmic bytes and not counted in them: the
-            # block-table entries of the attended pages (once per launch; a
-            # window that does not start on a page boundary touches one more
-            # page), and at most every workspace byte written once and read once
-            "uncounted_bytes": {"block_table": 4 * passes * int(sum(
-                                    W.pages_for(row_tokens(int(L), args.window, QL))
-                                    + (1 if args.window and int(L) else 0)
-                                    for L in wl.seq_lens)),
-                                "workspace_max": 2 * ws.nbytes},
-        },
-        "frac_of_hbm_peak": round(value / world / peak, 4),
-        "rows_tokens_per_s": round(world * tokens / step_s, 1),
-        "rows_per_s": round(world * wl.rows / step_s, 1),
-        "roofline": {
-            "bound": "hbm", "kernel": f"{kname}<{W.DTYPE_NAMES[cfg.dtype]}>, G={cfg.group}",
-            "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "peak_source": f"{peak_src} (copy bandwidth)",
-            # DRAM bytes of one launch (one pass: a step of the several-query
-            # kernel is `launches_per_step` of them)
-            "traffic": None if args.window else profile_traffic(cfg.name, kname, QL),
-            "mean_launch_us": round(launch_ms * 1e3, 3),
-            "timing": "events around the K back-to-back launches of the timed region",
-        },
-        "e2e": {"value": round(world * nbytes / (e2e_ms / 1e3 / Ke) / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
-                "ms_per_step": round(e2e_ms / Ke, 6),
-                "copies": "one packed pinned H2D and one D2H per step, double-buffered on two "
-                          "copy streams overlapping the kernels",
-                "host_issue_us_per_step": round(host_us, 2)},
-        "gpu_launches": K * passes,
-        "graph": graph,
-        "clocks": clock_info,
-    }
-    if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(wl, pool, args.cpu_seconds, args.window, QL,
-                                              q.cpu().numpy())
-    return result
+    return {"value": round(world * st.nbytes / (e2e_ms / 1e3 / Ke) / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": Ke,
+            "ms_per_step": round(e2e_ms / Ke, 6),
+            "copies": "one packed pinned H2D and one D2H per step, double-buffered on two "
+                      "copy streams overlapping the kernels",
+            "host_issue_us_per_step": round(host_us, 2)}
 
 
 def graph_timing(torch, dev, step, layers, calls=20, replays=50):
@@ -702,6 +787,28 @@ def cpu_model() -> str:
 
 
 # ------------------------------------------------------------- reference ----
+def encoded_pool(O, W, wl, layer=0):
+    """The oracle's encoding of one layer's context values, (k_data, v_data,
+    k_scales, v_scales), built block by block so that the fp32 values of only
+    one block are held at a time."""
+    import numpy as np
+    kd = vd = ks = vs = None
+    for lo, k, v in W.context_value_blocks(wl, layer):
+        kb, ksb = O.encode_pool(wl.cfg.dtype, k)
+        vb, vsb = O.encode_pool(wl.cfg.dtype, v)
+        if kd is None:
+            kd = np.empty((wl.num_pages,) + kb.shape[1:], kb.dtype)
+            vd = np.empty_like(kd)
+            if ksb is not None:
+                ks = np.empty((wl.num_pages,) + ksb.shape[1:], ksb.dtype)
+                vs = np.empty_like(ks)
+        hi = lo + kb.shape[0]
+        kd[lo:hi], vd[lo:hi] = kb, vb
+        if ksb is not None:
+            ks[lo:hi], vs[lo:hi] = ksb, vsb
+    return kd, vd, ks, vs
+
+
 def run_reference(args):
     """The FP64 oracle on the host cores, each step one row of the batch."""
     import numpy as np
@@ -710,10 +817,7 @@ def run_reference(args):
     from paged_kv_decode_09_gb300 import workloads as W
     wl = W.draw(args.workload)
     cfg = wl.cfg
-    k, v = W.context_values(wl)
-    kd, ks = O.encode_pool(cfg.dtype, k)
-    vd, vs = O.encode_pool(cfg.dtype, v)
-    del k, v
+    kd, vd, ks, vs = encoded_pool(O, W, wl)
     order = np.argsort(wl.seq_lens)
     G = cfg.group
     # A step is one row, or (when K rows would overrun the time budget) every
