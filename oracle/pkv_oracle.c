@@ -28,7 +28,7 @@
  *   - Variable-length batched decode: tinyllm, "The repository currently
  *     provides" (variable-length batched decode for several active
  *     sequences); Leone, "What ships" (continuous decode batching).
- *   - Sliding-window KV caches: Leone, "Capabilities".  Reading: with a
+ *   - Sliding-window KV caches: LeatEngine, "Capabilities".  Reading: with a
  *     window W > 0 a row of L tokens attends to its last W tokens,
  *     [max(0, L - W), L), the new token included; W = 0 means all L.
  *   - Several query tokens per row (Leone, "What ships": chunked prefill and

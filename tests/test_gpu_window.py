@@ -1,4 +1,4 @@
-"""Sliding-window decode (Leone, "Capabilities": sliding-window KV caches) on
+"""Sliding-window decode (LeatEngine, "Capabilities": sliding-window KV caches) on
 the GPU against the FP64 oracle, through the C ABI.
 
 Reading: with window W a row of L tokens attends to [max(0, L - W), L), and

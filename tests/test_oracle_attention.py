@@ -258,7 +258,7 @@ def test_merge_is_invariant_to_rescaled_partials():
 
 
 # ---------------------------------------------------------------------------
-# Sliding window (Leone, "Capabilities": sliding-window KV caches).  Reading:
+# Sliding window (LeatEngine, "Capabilities": sliding-window KV caches).  Reading:
 # with W > 0 a row of L tokens attends to [max(0, L - W), L).
 
 def _brute_window(dtype, q, dk, dv, lens, n_q, n_kv, scale, window):
