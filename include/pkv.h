@@ -88,6 +88,10 @@ typedef enum pkv_status {
 #define PKV_DEV_BAD_LENGTH 2u /* seq_lens[i] < 0 or > 16 * bt_stride: clamped */
 #define PKV_DEV_TIMEOUT 4u    /* a bounded wait on a shared-memory barrier gave up */
 
+/* How long (ns) a warp of the attention kernels waits for one of its tile
+ * copies before the kernel gives up (see kv_pool_set_wait_limit). */
+#define PKV_DEFAULT_WAIT_NS (1ull << 30)
+
 /* Stored KV formats: binary16; q8_0 (int8 codes + one binary16 scale per 32
  * values along head_dim); bfloat16, rounded to nearest even, and binary32,
  * stored as given (tinyllm, "The repository currently provides": BF16/F32 KV
@@ -127,7 +131,7 @@ pkv_status kv_pool_create(pkv_pool **out, int num_layers, int num_pages, int n_k
 /* Free a descriptor (not the caller's arrays).  NULL is allowed. */
 void kv_pool_destroy(pkv_pool *pool);
 
-/* Sliding window of a layer (Leone, "Capabilities": sliding-window KV
+/* Sliding window of a layer (LeatEngine, "Capabilities": sliding-window KV
  * caches).  With window W > 0, every attention call on the layer lets a row
  * of L tokens attend to its last W tokens, [max(0, L - W), L), the token
  * appended this step included, and reads only the pages holding them:
@@ -136,6 +140,20 @@ void kv_pool_destroy(pkv_pool *pool);
  * call is queued; kv_append is unaffected.  W < 0 -> PKV_ERR_INVALID_ARG. */
 pkv_status kv_pool_set_window(pkv_pool *pool, int layer, int window);
 pkv_status kv_pool_get_window(const pkv_pool *pool, int layer, int *window);
+
+/* Limit of the attention kernels' waits on their tile copies, for calls
+ * queued on this descriptor from now on (host-side state; default
+ * PKV_DEFAULT_WAIT_NS, about 1.07 s).  Not part of the method: it exists so
+ * that the kernels' give-up path can be tested on a real GPU without a hang
+ * or a fault.  When a warp has waited longer than wait_ns for a copy (with 0:
+ * when a copy it waits for has not landed yet), its CTA stops reading, ORs
+ * PKV_DEV_TIMEOUT into the status word, waits (up to PKV_DEFAULT_WAIT_NS) for
+ * every copy it has in flight to land, and returns; the call's outputs are
+ * then undefined, and its workspace may hold non-zero arrival counters, so
+ * zero the workspace before the next call uses it.  Waits on anything other
+ * than a tile copy keep the default limit.  Setting it while calls are being
+ * queued from another thread is a data race. */
+pkv_status kv_pool_set_wait_limit(pkv_pool *pool, unsigned long long wait_ns);
 
 /* Wait for `stream`, copy the pool's device status word into *status and
  * reset it to 0.  This call synchronises; it is not part of the decode path.
@@ -344,7 +362,11 @@ pkv_status pkv_decode_step_mq(const pkv_pool *pool, int layer, const float *q, c
  *     a GB300, a few hundred rows of 8 KV heads fit).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is kept with the id of the
+ *     CUDA context it belongs to: after a device reset, the first call in
+ *     the new context looks it up again (also before any capture).
+ *   - Every argument is checked as paged_decode_attention checks it before
+ *     the array is touched, so a rejected call leaves it as it was.
  *   - Every call on a device shares the one array, which keeps the last
  *     call's partial states; each call clears the arrival counters first
  *     (one cudaMemsetAsync on `stream`).  Calls that overlap on the GPU

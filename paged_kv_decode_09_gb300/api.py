@@ -20,6 +20,7 @@ PAGE = 16
 HEAD_DIM = 128
 Q8_BLOCK = 32
 MAX_ROWS = 2048
+DEFAULT_WAIT_NS = 1 << 30
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libpkv.so")
@@ -57,6 +58,7 @@ _SIGS = {
     "paged_decode_plan": ([_vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp], _i),
     "paged_decode_combine": ([_vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp], _i),
     "kv_pool_set_window": ([_vp, _i, _i], _i),
+    "kv_pool_set_wait_limit": ([_vp, ctypes.c_ulonglong], _i),
     "pkv_alloc_create": ([ctypes.POINTER(_vp), _i, _i, _i], _i),
     "pkv_alloc_destroy": ([_vp], None),
     "pkv_alloc_open": ([_vp, ctypes.POINTER(_i)], _i),
@@ -189,6 +191,11 @@ class KVPool:
         """Sliding window of `layer` (0: none): attention on the layer reads
         each row's last `window` tokens only."""
         _check(lib().kv_pool_set_window(self.handle, layer, window), "kv_pool_set_window")
+
+    def set_wait_limit(self, wait_ns: int):
+        """Limit (ns) of the attention kernels' waits on their tile copies
+        (a test hook: see kv_pool_set_wait_limit in pkv.h)."""
+        _check(lib().kv_pool_set_wait_limit(self.handle, int(wait_ns)), "kv_pool_set_wait_limit")
 
     def window(self, layer: int) -> int:
         w = ctypes.c_int(0)

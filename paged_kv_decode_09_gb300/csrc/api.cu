@@ -33,6 +33,7 @@ struct pkv_pool {
   std::atomic<int>* ready;   // [num_layers]: 1 once maps[layer] is valid
   std::mutex maps_mutex;
   int* window;               // [num_layers]: sliding window of the layer (0: none)
+  unsigned long long wait_ns = PKV_DEFAULT_WAIT_NS;  // limit of a wait on a tile copy
   ~pkv_pool() {
     delete[] maps;
     delete[] ready;
@@ -173,11 +174,10 @@ enum class Mode { kMerged, kSplitOnly };
 // One launch of the decode kernel: kMerged merges split segments in-kernel
 // (arrival counters) and, given k_new/v_new, appends the new tokens first;
 // kSplitOnly leaves the partial states for paged_decode_combine.
-pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q, const float* k_new,
-                          const float* v_new, const int32_t* block_table, int bt_stride,
-                          const int32_t* seq_lens, int num_rows, int n_q, float scale, float* out,
-                          void* workspace, size_t workspace_bytes, int num_chunks, void* stream,
-                          Mode mode) {
+// The checks of an attention call's arguments other than the workspace.
+pkv_status check_attention(const pkv_pool* pool, int layer, const float* q,
+                           const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                           int num_rows, int n_q, const float* out, int num_chunks) {
   pkv_status s = check_pool_layer(pool, layer);
   if (s) return s;
   if ((s = check_geometry(n_q, pool->n_kv, pool->head_dim))) return s;
@@ -187,6 +187,17 @@ pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q, const
     return fail(PKV_ERR_INVALID_ARG, "q / out not 16-byte aligned");
   if (num_chunks < 0) return fail(PKV_ERR_INVALID_ARG, "num_chunks < 0");
   if (num_chunks > PKV_MAX_CHUNKS) return fail(PKV_ERR_UNSUPPORTED, "num_chunks > %d", PKV_MAX_CHUNKS);
+  return PKV_OK;
+}
+
+pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q, const float* k_new,
+                          const float* v_new, const int32_t* block_table, int bt_stride,
+                          const int32_t* seq_lens, int num_rows, int n_q, float scale, float* out,
+                          void* workspace, size_t workspace_bytes, int num_chunks, void* stream,
+                          Mode mode) {
+  pkv_status s =
+      check_attention(pool, layer, q, block_table, bt_stride, seq_lens, num_rows, n_q, out, num_chunks);
+  if (s) return s;
   if (num_rows == 0) return PKV_OK;
   if (num_chunks == 0 && (s = default_chunks(pool, n_q, num_rows, &num_chunks))) return s;
   const size_t need = workspace_needed(num_rows, n_q, pool->n_kv, num_chunks);
@@ -223,6 +234,7 @@ pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q, const
   a.part_acc = w.part_acc;
   a.counters = mode == Mode::kMerged ? w.counters : nullptr;
   a.status = pool->status;
+  a.wait_ns = pool->wait_ns;
   const pkv::TileMaps* maps = nullptr;
   if ((s = layer_maps(pool, layer, &maps))) return s;
   cudaError_t e = pkv::launch_paged_decode(pool->dtype, g, a, *maps, num_chunks,
@@ -304,6 +316,7 @@ pkv_status attention_mq_impl(const pkv_pool* pool, int layer, const float* q, co
   a.aligned_split = split_may_align(pool->dtype);
   a.out = out;
   a.status = pool->status;
+  a.wait_ns = pool->wait_ns;
   const pkv::TileMaps* maps = nullptr;
   if ((s = layer_maps(pool, layer, &maps))) return s;
   const int per_pass = pkv::mq_pass_queries(pool->dtype, g, q_len);
@@ -323,6 +336,13 @@ pkv_status attention_mq_impl(const pkv_pool* pool, int layer, const float* q, co
 
 namespace pkv {
 int pool_kv_heads(const pkv_pool* pool) { return pool ? pool->n_kv : 0; }
+pkv_status check_attention_args(const pkv_pool* pool, int layer, const float* q,
+                                const int32_t* block_table, int bt_stride,
+                                const int32_t* seq_lens, int num_rows, int n_q_heads,
+                                const float* out, int num_chunks) {
+  return check_attention(pool, layer, q, block_table, bt_stride, seq_lens, num_rows, n_q_heads, out,
+                         num_chunks);
+}
 pkv_status record_error(pkv_status s, const char* msg) { return fail(s, "%s", msg); }
 }  // namespace pkv
 
@@ -414,6 +434,12 @@ pkv_status kv_pool_get_window(const pkv_pool* pool, int layer, int* window) {
   if (s) return s;
   if (!window) return fail(PKV_ERR_INVALID_ARG, "null window pointer");
   *window = pool->window[layer];
+  return PKV_OK;
+}
+
+pkv_status kv_pool_set_wait_limit(pkv_pool* pool, unsigned long long wait_ns) {
+  if (!pool) return fail(PKV_ERR_INVALID_ARG, "null pool");
+  pool->wait_ns = wait_ns;
   return PKV_OK;
 }
 

@@ -680,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
     for (long long pos = x + ((warp - r + kWarps) % kWarps); pos < b; pos += kWarps) {
       const int u = static_cast<int>((pos - first) / kWarps);
       const int s = u % R;
-      bool ok = !aborted && mbar_wait_bounded(bar0 + 8 * s, (u / R) & 1, ctl);
+      bool ok = !aborted && mbar_wait_bounded(bar0 + 8 * s, (u / R) & 1, ctl, a.wait_ns);
       ok = __all_sync(kFull, ok);
       if (!ok) {
         if (!aborted && lane == 0 && !ctl[0]) {

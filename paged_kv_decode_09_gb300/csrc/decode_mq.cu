@@ -814,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (long long pos = x + ((warp - r0 + kWarps) % kWarps); pos < b; pos += kWarps) {
       const int u = static_cast<int>((pos - first) / kWarps);
       const int s = u % R;
-      bool ok = !aborted && mbar_wait_bounded(bar0 + 8 * s, (u / R) & 1, ctl);
+      bool ok = !aborted && mbar_wait_bounded(bar0 + 8 * s, (u / R) & 1, ctl, a.wait_ns);
       ok = __all_sync(kFull, ok);
       if (!ok) {
         if (!aborted && lane == 0 && !ctl[0]) {
@@ -1218,7 +1218,7 @@ __global__ void __launch_bounds__(kThreads, team_ctas(NT))
     for (long long pos = x; pos < b; ++pos) {
       const int v = static_cast<int>(pos - c_begin);
       const int s = v % RT;
-      bool ok = !aborted && mbar_wait_bounded(full0 + 8 * s, (v / RT) & 1, ctl);
+      bool ok = !aborted && mbar_wait_bounded(full0 + 8 * s, (v / RT) & 1, ctl, a.wait_ns);
       ok = __all_sync(kFull, ok);
       if (!ok) {
         fail();

@@ -14,10 +14,15 @@
 // Host code cannot use the array's name as a device address (on the host it
 // names a stand-in object), so the first call on each device, with that
 // device current, looks the address up with cudaGetSymbolAddress and keeps
-// it; that first call should come before any stream capture.
+// it; that first call should come before any stream capture.  The address
+// is kept together with the id of the CUDA context it belongs to: after a
+// device reset the runtime creates a new context, loads the module again
+// (the array may then sit elsewhere), and the next call looks it up anew.
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
+
+#include <cudaTypedefs.h>
 
 #include "pkv.h"
 #include "pkv_internal.h"
@@ -29,8 +34,36 @@ static __device__ __align__(256) unsigned char g_scratch[PKV_STATIC_SCRATCH_BYTE
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 void* g_addr[kMaxDevices] = {};
+unsigned long long g_ctx[kMaxDevices] = {};  // id of the context g_addr[dev] belongs to
 
 thread_local char g_static_error[160] = "";
+
+// The id of the calling thread's current CUDA context, through the driver
+// (reached via the runtime, no link against the driver library); false if
+// there is none yet or the driver cannot say.
+bool current_context_id(unsigned long long* id) {
+  static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  static PFN_cuCtxGetId_v12000 get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+  });
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 }  // namespace
 
@@ -39,9 +72,11 @@ extern "C" pkv_status paged_decode_attention_static(const pkv_pool* pool, int la
                                                     int bt_stride, const int32_t* seq_lens,
                                                     int num_rows, int n_q_heads, float scale,
                                                     float* out, int num_chunks, void* stream) {
-  if (!pool) return pkv::record_error(PKV_ERR_INVALID_ARG, "null pool");
-  if (num_rows < 0 || num_rows > PKV_MAX_ROWS)
-    return pkv::record_error(PKV_ERR_UNSUPPORTED, "num_rows outside [0, PKV_MAX_ROWS]");
+  // Every check of the regular entry point comes first: a call that will not
+  // launch leaves the shared array alone.
+  pkv_status st = pkv::check_attention_args(pool, layer, q, block_table, bt_stride, seq_lens,
+                                            num_rows, n_q_heads, out, num_chunks);
+  if (st != PKV_OK) return st;
   if (num_rows == 0)
     return paged_decode_attention(pool, layer, q, block_table, bt_stride, seq_lens, 0, n_q_heads,
                                   scale, out, nullptr, 0, num_chunks, stream);
@@ -51,14 +86,22 @@ extern "C" pkv_status paged_decode_attention_static(const pkv_pool* pool, int la
   void* base = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_addr[dev]) {
+    unsigned long long id = 0;
+    const bool known = current_context_id(&id);
+    if (!g_addr[dev] || !known || g_ctx[dev] != id) {
       void* p = nullptr;
+      // also creates the device's context if the thread has none yet
       if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p)
         return pkv::record_error(PKV_ERR_CUDA,
                                  "paged_decode_attention_static: cudaGetSymbolAddress failed");
-      g_addr[dev] = p;
+      // without a context id from the driver, nothing is kept (the next call
+      // looks the address up again)
+      g_addr[dev] = current_context_id(&id) ? p : nullptr;
+      g_ctx[dev] = id;
+      base = p;
+    } else {
+      base = g_addr[dev];
     }
-    base = g_addr[dev];
   }
   // The chunk count fixes the workspace size; resolve the default here.
   if (num_chunks == 0) {

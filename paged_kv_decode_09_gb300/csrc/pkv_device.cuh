@@ -18,8 +18,10 @@ constexpr int kQBlock = PKV_Q8_BLOCK;   // q8_0 block along head_dim
 constexpr unsigned kFull = 0xffffffffu;
 
 // A wait on a shared-memory barrier gives up after this long (the whole
-// decode of a batch takes well under a millisecond).
-constexpr unsigned long long kWaitLimitNs = 1ull << 30;  // ~1.07 s
+// decode of a batch takes well under a millisecond).  The attention kernels
+// take the limit of their waits on tile copies as an argument (this value
+// unless kv_pool_set_wait_limit changed it); every other wait uses it as is.
+constexpr unsigned long long kWaitLimitNs = PKV_DEFAULT_WAIT_NS;  // ~1.07 s
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -55,6 +57,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Whether the phase of `bar` with the given parity has completed, without
+// waiting.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -62,9 +78,12 @@ __device__ __forceinline__ unsigned long long global_ns() {
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Returns
-// false, without waiting further, once *abort is set or after kWaitLimitNs.
+// false, without waiting further, once *abort is set or after `limit_ns`;
+// with limit_ns = 0, unless the phase has already completed.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  const volatile int* abort) {
+                                                  const volatile int* abort,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
+  if (limit_ns == 0) return mbar_test_wait(bar, parity);
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (true) {
@@ -72,7 +91,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -39,6 +39,7 @@ struct DecodeArgs {
   float* part_acc;  // [slots][G][128]
   int32_t* counters;  // non-null: [rows * n_kv] arrival counters, merge in-kernel
   int32_t* status;  // optional device status word
+  unsigned long long wait_ns;  // limit of a wait on a tile copy (kv_pool_set_wait_limit)
 };
 
 struct CombineArgs {
@@ -102,6 +103,12 @@ inline size_t part_acc_bytes(long long slots, int group) {
 
 // Helpers the C-ABI layer exports to the other translation units.
 int pool_kv_heads(const pkv_pool* pool);                 // n_kv_heads of a pool descriptor
+// The host-side checks of paged_decode_attention's arguments other than the
+// workspace (PKV_OK, or the status that call would return).
+pkv_status check_attention_args(const pkv_pool* pool, int layer, const float* q,
+                                const int32_t* block_table, int bt_stride,
+                                const int32_t* seq_lens, int num_rows, int n_q_heads,
+                                const float* out, int num_chunks);
 pkv_status record_error(pkv_status s, const char* msg);  // sets pkv_last_error_message
 
 // Tensor maps of one layer's K and V data, [tiles][16 tokens][128 dims]

@@ -2,8 +2,7 @@
 FP64 oracle, through the C ABI.
 
 Every workload shape (tiny, Qwen3-0.6B layer, 8B f16, 8B q8_0, skewed batch)
-runs at its full size; the oracle checks every output of the smaller ones and
-a sample of rows of the q8_0 batch.  Unused pool slots are poisoned with NaN,
+runs at its full size, and the oracle checks every output.  Unused pool slots are poisoned with NaN,
 so any read outside a row's tokens shows up.  Bounds: max abs error <= 2e-3
 (the stated bound) and <= 1e-4 * max(1, max|ref|) (internal)."""
 import numpy as np
@@ -11,11 +10,24 @@ import pytest
 import torch
 
 import oracle as O
-from helpers import (ATOL_STATED, device_pool, encode_pool, oracle_decode, tight_tol, to_dev)
+from helpers import (ATOL_STATED, device_pool, encode_pool, host_arrays, oracle_decode,
+                     tight_tol, to_dev)
 from paged_kv_decode_09_gb300 import api
 from paged_kv_decode_09_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
+
+
+_HOST_POOLS = {}
+
+
+def _host_pool(wl, include_appended=True):
+    """encode_pool of a full-size workload, kept for the module's other tests
+    (encoding the 8B q8_0 pool takes a while; the arrays are only read)."""
+    key = (wl.cfg.name, include_appended)
+    if key not in _HOST_POOLS:
+        _HOST_POOLS[key] = encode_pool(wl, include_appended=include_appended)
+    return _HOST_POOLS[key]
 
 
 def _check(out, ref):
@@ -46,18 +58,37 @@ def test_attention_matches_oracle(cfg_name):
     _check(_run(wl, pool, layer=1), ref)
 
 
-def test_attention_q8_0_full_batch_sampled_rows():
+def test_attention_q8_0_full_batch_every_row():
     """The 8B q8_0 batch at full size (32 rows up to 32768 tokens) in the
-    launch configuration the benchmark times; the oracle checks 6 rows."""
+    launch configuration the benchmark times; the oracle checks every row."""
     wl = W.draw("llama8b_q8_0")
-    host = encode_pool(wl)
+    host = _host_pool(wl)
     pool = device_pool(wl, host)
     out = _run(wl, pool)
-    rows = np.random.default_rng(0).choice(wl.rows, 6, replace=False)
-    rows[0] = int(np.argmax(wl.seq_lens))  # the longest row is always checked
-    ref = O.decode_attention(W.Q8_0, wl.q[rows], *host, wl.block_table[rows], wl.seq_lens[rows],
-                             wl.num_pages, wl.cfg.n_kv_heads, wl.scale)
-    _check(out[rows], ref)
+    _check(out, oracle_decode(wl, host))
+
+
+@pytest.mark.parametrize("cfg_name", ["llama8b_f16", "llama8b_q8_0"])
+def test_benchmarked_decode_step(cfg_name):
+    """The call the benchmark times: pkv_decode_step on the full 8B batch at
+    the default chunk count, the new token of every row stored by the fused
+    append.  The pool must then equal the oracle's append bit for bit, and the
+    output must match the oracle's attention over it."""
+    wl = W.draw(cfg_name)
+    host = _host_pool(wl, include_appended=False)
+    pool = device_pool(wl, host)
+    out = api.decode_step(pool, 0, to_dev(wl.q), to_dev(wl.k_new), to_dev(wl.v_new),
+                          to_dev(wl.block_table), to_dev(wl.seq_lens), wl.scale)
+    torch.cuda.synchronize()
+    assert pool.read_status() == 0
+    want = [None if a is None else a.copy() for a in host]
+    O.kv_append(wl.cfg.dtype, wl.k_new, wl.v_new, wl.block_table, wl.seq_lens, wl.num_pages,
+                *want)
+    got = host_arrays(pool, 0)
+    for g, w in zip(got, want):
+        if w is not None:
+            assert np.array_equal(g, w), "fused append differs from the oracle's encoding"
+    _check(out.cpu().numpy(), oracle_decode(wl, want))
 
 
 def test_skewed_decode_step_appends_then_attends():
@@ -102,12 +133,13 @@ def test_gqa_groups(group, n_kv, dtype):
     _check(_run(wl, pool, num_chunks=37), oracle_decode(wl, host))
 
 
-@pytest.mark.parametrize("cfg_name", ["llama8b_f16", "llama8b_f32"])
+@pytest.mark.parametrize("cfg_name", ["llama8b_f16", "llama8b_f32", "llama8b_bf16",
+                                      "llama8b_q8_0"])
 def test_peaked_scores(cfg_name):
     """q scaled by 8: near one-hot softmax, so one wrong key or value would
     dominate the output."""
     wl = W.draw(cfg_name)
-    host = encode_pool(wl)
+    host = _host_pool(wl)
     pool = device_pool(wl, host)
     q = (wl.q * 8).astype(np.float32)
     _check(_run(wl, pool, q=q), oracle_decode(wl, host, q=q))

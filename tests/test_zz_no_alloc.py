@@ -39,7 +39,7 @@ def _call_static(pool, q, bt, sl, n_q, scale, out, chunks=0):
                         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
 
-@pytest.mark.parametrize("cfg_name", ["llama8b_f16", "skewed"])
+@pytest.mark.parametrize("cfg_name", ["llama8b_f16", "skewed", "llama8b_q8_0"])
 def test_static_scratch_matches_workspace_entry_point(cfg_name):
     wl = W.draw(cfg_name)
     host = encode_pool(wl)
@@ -70,3 +70,50 @@ def test_static_scratch_rejects_calls_that_do_not_fit():
     st = _call_static(pool, q, bt, sl, 32, 0.1, out, chunks=304)
     assert st == 4  # PKV_ERR_WORKSPACE
     assert b"static array" in api.lib().pkv_last_error_message()
+
+
+def _scratch_bytes():
+    """PKV_STATIC_SCRATCH_BYTES as include/pkv.h defines it."""
+    import os
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    text = open(os.path.join(root, "include", "pkv.h")).read()
+    m = re.search(r"#define PKV_STATIC_SCRATCH_BYTES \((\d+)u << (\d+)\)", text)
+    return int(m.group(1)) << int(m.group(2))
+
+
+def _largest_fitting_rows(pool, n_q):
+    """The most rows whose workspace, at the default chunk count for that
+    many rows, fits the static array."""
+    best = 0
+    for rows in range(1, api.MAX_ROWS + 1):
+        need = api.workspace_bytes(rows, n_q, pool.n_kv, api.default_chunks(pool, n_q, rows))
+        if need > _scratch_bytes():
+            break
+        best = rows
+    return best
+
+
+@pytest.mark.parametrize("dtype", [W.F16, W.Q8_0])
+def test_static_scratch_size_limit_is_exact(dtype):
+    """At the largest row count that fits, the call succeeds and matches the
+    workspace entry point; with one row more it is refused."""
+    cfg = W.Config("limit", 1, ("fixed", (1,)), 32, 8, 128, dtype, ("spare", 0.1), 21)
+    probe = api.KVPool(1, 64, 8, dtype)
+    n = _largest_fitting_rows(probe, 32)
+    assert 0 < n < api.MAX_ROWS
+    lengths = [1 + (7 * i) % 40 for i in range(n + 1)]  # short rows, 1 to 40 tokens
+    wl = W.draw(cfg, lengths=lengths)
+    host = encode_pool(wl)
+    pool = device_pool(wl, host)
+    q, bt, sl = to_dev(wl.q), to_dev(wl.block_table), to_dev(wl.seq_lens)
+    qn, sln = q[:n].contiguous(), sl[:n].contiguous()
+    btn = bt[:n].contiguous()
+    ref = api.paged_decode_attention(pool, 0, qn, btn, sln, wl.scale).cpu().numpy()
+    out = torch.full_like(qn, float("nan"))
+    assert _call_static(pool, qn, btn, sln, 32, wl.scale, out) == 0
+    torch.cuda.synchronize()
+    assert float(np.max(np.abs(out.cpu().numpy() - ref))) <= TOL
+    out1 = torch.zeros_like(q)
+    assert _call_static(pool, q, bt, sl, 32, wl.scale, out1) == 4  # PKV_ERR_WORKSPACE
+    assert pool.read_status() == 0
