@@ -88,8 +88,8 @@ typedef enum pkv_status {
 #define PKV_DEV_BAD_LENGTH 2u /* seq_lens[i] < 0 or > 16 * bt_stride: clamped */
 #define PKV_DEV_TIMEOUT 4u    /* a bounded wait on a shared-memory barrier gave up */
 
-/* How long (ns) a warp of the attention kernels waits for one of its tile
- * copies before the kernel gives up (see kv_pool_set_wait_limit). */
+/* How long (ns) a warp of the attention kernels waits on a shared-memory
+ * barrier (a tile copy, a peer warp) before the kernel gives up. */
 #define PKV_DEFAULT_WAIT_NS (1ull << 30)
 
 /* Stored KV formats: binary16; q8_0 (int8 codes + one binary16 scale per 32
@@ -141,19 +141,20 @@ void kv_pool_destroy(pkv_pool *pool);
 pkv_status kv_pool_set_window(pkv_pool *pool, int layer, int window);
 pkv_status kv_pool_get_window(const pkv_pool *pool, int layer, int *window);
 
-/* Limit of the attention kernels' waits on their tile copies, for calls
- * queued on this descriptor from now on (host-side state; default
- * PKV_DEFAULT_WAIT_NS, about 1.07 s).  Not part of the method: it exists so
- * that the kernels' give-up path can be tested on a real GPU without a hang
- * or a fault.  When a warp has waited longer than wait_ns for a copy (with 0:
- * when a copy it waits for has not landed yet), its CTA stops reading, ORs
- * PKV_DEV_TIMEOUT into the status word, waits (up to PKV_DEFAULT_WAIT_NS) for
- * every copy it has in flight to land, and returns; the call's outputs are
- * then undefined, and its workspace may hold non-zero arrival counters, so
- * zero the workspace before the next call uses it.  Waits on anything other
- * than a tile copy keep the default limit.  Setting it while calls are being
- * queued from another thread is a data race. */
-pkv_status kv_pool_set_wait_limit(pkv_pool *pool, unsigned long long wait_ns);
+/* Test hook, not part of the method: it lets the kernels' give-up path be
+ * run on a real GPU, with no hang and no fault.  With stall_ns > 0, every
+ * attention call queued on this descriptor from now on makes each warp of
+ * the kernel, once it has queued its first tile copies, wait up to stall_ns
+ * on a barrier that nothing completes, as it would on a copy that never
+ * lands.  That wait runs out, and the kernel gives up as on a real timeout:
+ * it stops reading, ORs PKV_DEV_TIMEOUT into the status word, waits for the
+ * copies it has in flight to land (each up to PKV_DEFAULT_WAIT_NS), and
+ * returns.  The call's outputs are then undefined and its workspace may hold
+ * non-zero arrival counters: zero the workspace before the next call uses
+ * it.  stall_ns = 0 (the default) turns the hook off; values above
+ * PKV_DEFAULT_WAIT_NS return PKV_ERR_INVALID_ARG.  Host-side descriptor
+ * state; setting it while another thread queues calls is a data race. */
+pkv_status kv_pool_set_test_stall(pkv_pool *pool, unsigned long long stall_ns);
 
 /* Wait for `stream`, copy the pool's device status word into *status and
  * reset it to 0.  This call synchronises; it is not part of the decode path.
@@ -180,14 +181,17 @@ pkv_status paged_decode_default_chunks(const pkv_pool *pool, int n_q_heads, int 
                                        int *chunks);
 
 /* Workspace bytes paged_decode_attention needs for up to max_rows rows with
- * num_chunks chunks.  Layout for a call of num_rows rows, in parts that each
- * start on a 256-byte boundary, with S = num_chunks + num_rows * n_kv_heads
- * partial slots and G = n_q / n_kv:
- *     counters int32 [num_rows * n_kv_heads]  arrival count per (row, KV head)
+ * num_chunks chunks.  Layout for a call of num_rows rows, with S = num_chunks
+ * + num_rows * n_kv_heads partial slots and G = n_q / n_kv, from the start:
  *     part_ml  float [S][G][2]  (m2, l) per slot and query head of the group
- *     part_acc float [S][G][head_dim]
- * The workspace must be zero-filled once before its first use (the counters
- * must start at 0); every call that completes leaves the counters at 0 again.
+ *     part_acc float [S][G][head_dim]  (at the next 256-byte boundary)
+ * and down from the end E (workspace_bytes rounded down to a multiple of 256),
+ * int32 flags: the arrival count of (row, KV head) j at E - 4 (2j + 1), and
+ * the ready flag of slot s (its partial state is complete) at E - 4 (2s + 2).
+ * The flags keep their places whatever the call's rows and chunks, so one
+ * workspace sized for the largest call serves every smaller call.  It must
+ * be zero-filled once before its first use (the flags must start at 0);
+ * every call that completes leaves them at 0 again.
  * After a call that reported PKV_DEV_TIMEOUT, zero it again.  Calls that
  * share a workspace must not run concurrently.  Returns 0 for invalid sizes. */
 size_t paged_decode_workspace_bytes(int max_rows, int n_q_heads, int n_kv_heads, int head_dim,

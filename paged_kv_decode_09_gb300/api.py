@@ -58,7 +58,7 @@ _SIGS = {
     "paged_decode_plan": ([_vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp], _i),
     "paged_decode_combine": ([_vp, _i, _i, _i, _i, _i, _i, _i, _i, _vp, _sz, _vp, _vp], _i),
     "kv_pool_set_window": ([_vp, _i, _i], _i),
-    "kv_pool_set_wait_limit": ([_vp, ctypes.c_ulonglong], _i),
+    "kv_pool_set_test_stall": ([_vp, ctypes.c_ulonglong], _i),
     "pkv_alloc_create": ([ctypes.POINTER(_vp), _i, _i, _i], _i),
     "pkv_alloc_destroy": ([_vp], None),
     "pkv_alloc_open": ([_vp, ctypes.POINTER(_i)], _i),
@@ -192,10 +192,11 @@ class KVPool:
         each row's last `window` tokens only."""
         _check(lib().kv_pool_set_window(self.handle, layer, window), "kv_pool_set_window")
 
-    def set_wait_limit(self, wait_ns: int):
-        """Limit (ns) of the attention kernels' waits on their tile copies
-        (a test hook: see kv_pool_set_wait_limit in pkv.h)."""
-        _check(lib().kv_pool_set_wait_limit(self.handle, int(wait_ns)), "kv_pool_set_wait_limit")
+    def set_test_stall(self, stall_ns: int):
+        """Test hook (kv_pool_set_test_stall in pkv.h): with stall_ns > 0 the
+        attention kernels stall on a barrier nothing completes, give up after
+        stall_ns and take their timeout path; 0 turns it off."""
+        _check(lib().kv_pool_set_test_stall(self.handle, int(stall_ns)), "kv_pool_set_test_stall")
 
     def window(self, layer: int) -> int:
         w = ctypes.c_int(0)

@@ -33,7 +33,7 @@ struct pkv_pool {
   std::atomic<int>* ready;   // [num_layers]: 1 once maps[layer] is valid
   std::mutex maps_mutex;
   int* window;               // [num_layers]: sliding window of the layer (0: none)
-  unsigned long long wait_ns = PKV_DEFAULT_WAIT_NS;  // limit of a wait on a tile copy
+  unsigned long long test_stall_ns = 0;  // test hook (kv_pool_set_test_stall); 0: off
   ~pkv_pool() {
     delete[] maps;
     delete[] ready;
@@ -117,25 +117,23 @@ long long partial_slots(int num_chunks, int num_rows, int n_kv) {
 size_t workspace_needed(int num_rows, int n_q, int n_kv, int num_chunks) {
   const long long slots = partial_slots(num_chunks, num_rows, n_kv);
   const int g = n_q / n_kv;
-  return pkv::counter_bytes(static_cast<long long>(num_rows) * n_kv) +
-         pkv::part_ml_bytes(slots, g) + pkv::part_acc_bytes(slots, g);
+  return pkv::part_ml_bytes(slots, g) + pkv::part_acc_bytes(slots, g) + pkv::flag_bytes(slots);
 }
 
-// Workspace parts for a call: counters, part_ml, part_acc.
+// Workspace parts for a call: part_ml, part_acc, and the end the flags hang from.
 struct WsParts {
-  int32_t* counters;
   float* part_ml;
   float* part_acc;
+  int32_t* flags;
 };
-WsParts workspace_parts(void* ws, int num_rows, int n_q, int n_kv, int num_chunks) {
+WsParts workspace_parts(void* ws, size_t bytes, int num_rows, int n_q, int n_kv, int num_chunks) {
   const long long slots = partial_slots(num_chunks, num_rows, n_kv);
   uint8_t* p = static_cast<uint8_t*>(ws);
   WsParts w;
-  w.counters = reinterpret_cast<int32_t*>(p);
-  p += pkv::counter_bytes(static_cast<long long>(num_rows) * n_kv);
   w.part_ml = reinterpret_cast<float*>(p);
   p += pkv::part_ml_bytes(slots, n_q / n_kv);
   w.part_acc = reinterpret_cast<float*>(p);
+  w.flags = pkv::flags_end(ws, bytes);
   return w;
 }
 
@@ -206,7 +204,7 @@ pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q, const
   if (!aligned(workspace, 256)) return fail(PKV_ERR_INVALID_ARG, "workspace not 256-byte aligned");
 
   const int g = n_q / pool->n_kv;
-  const WsParts w = workspace_parts(workspace, num_rows, n_q, pool->n_kv, num_chunks);
+  const WsParts w = workspace_parts(workspace, workspace_bytes, num_rows, n_q, pool->n_kv, num_chunks);
   pkv::DecodeArgs a;
   a.k_data = pool->k_data + layer * pool->layer_data_bytes;
   a.v_data = pool->v_data + layer * pool->layer_data_bytes;
@@ -232,9 +230,9 @@ pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q, const
   a.out = out;
   a.part_ml = w.part_ml;
   a.part_acc = w.part_acc;
-  a.counters = mode == Mode::kMerged ? w.counters : nullptr;
+  a.flags = mode == Mode::kMerged ? w.flags : nullptr;
   a.status = pool->status;
-  a.wait_ns = pool->wait_ns;
+  a.test_stall_ns = pool->test_stall_ns;
   const pkv::TileMaps* maps = nullptr;
   if ((s = layer_maps(pool, layer, &maps))) return s;
   cudaError_t e = pkv::launch_paged_decode(pool->dtype, g, a, *maps, num_chunks,
@@ -247,8 +245,8 @@ pkv_status attention_impl(const pkv_pool* pool, int layer, const float* q, const
 // ------------------------------------------------- several queries per row
 size_t workspace_needed_mq(int num_rows, int n_kv, int num_chunks) {
   const long long slots = partial_slots(num_chunks, num_rows, n_kv);
-  return pkv::counter_bytes(static_cast<long long>(num_rows) * n_kv * pkv::kMqCounters) +
-         pkv::part_ml_bytes(slots, pkv::kMqCols) + pkv::part_acc_bytes(slots, pkv::kMqCols);
+  return pkv::part_ml_bytes(slots, pkv::kMqCols) + pkv::part_acc_bytes(slots, pkv::kMqCols) +
+         pkv::mq_flag_bytes(static_cast<long long>(num_rows) * n_kv);
 }
 
 pkv_status default_chunks_mq(const pkv_pool* p, int group, int q_len, int rows, int* chunks) {
@@ -292,8 +290,7 @@ pkv_status attention_mq_impl(const pkv_pool* pool, int layer, const float* q, co
   const long long slots = partial_slots(num_chunks, num_rows, pool->n_kv);
   uint8_t* wp = static_cast<uint8_t*>(workspace);
   pkv::DecodeArgs a;
-  a.counters = reinterpret_cast<int32_t*>(wp);
-  wp += pkv::counter_bytes(static_cast<long long>(num_rows) * pool->n_kv * pkv::kMqCounters);
+  a.flags = pkv::flags_end(workspace, workspace_bytes);
   a.part_ml = reinterpret_cast<float*>(wp);
   wp += pkv::part_ml_bytes(slots, pkv::kMqCols);
   a.part_acc = reinterpret_cast<float*>(wp);
@@ -316,7 +313,7 @@ pkv_status attention_mq_impl(const pkv_pool* pool, int layer, const float* q, co
   a.aligned_split = split_may_align(pool->dtype);
   a.out = out;
   a.status = pool->status;
-  a.wait_ns = pool->wait_ns;
+  a.test_stall_ns = pool->test_stall_ns;
   const pkv::TileMaps* maps = nullptr;
   if ((s = layer_maps(pool, layer, &maps))) return s;
   const int per_pass = pkv::mq_pass_queries(pool->dtype, g, q_len);
@@ -437,9 +434,11 @@ pkv_status kv_pool_get_window(const pkv_pool* pool, int layer, int* window) {
   return PKV_OK;
 }
 
-pkv_status kv_pool_set_wait_limit(pkv_pool* pool, unsigned long long wait_ns) {
+pkv_status kv_pool_set_test_stall(pkv_pool* pool, unsigned long long stall_ns) {
   if (!pool) return fail(PKV_ERR_INVALID_ARG, "null pool");
-  pool->wait_ns = wait_ns;
+  if (stall_ns > PKV_DEFAULT_WAIT_NS)
+    return fail(PKV_ERR_INVALID_ARG, "stall_ns above PKV_DEFAULT_WAIT_NS");
+  pool->test_stall_ns = stall_ns;
   return PKV_OK;
 }
 
@@ -562,8 +561,8 @@ pkv_status paged_decode_combine(const int32_t* seq_lens, int num_rows, int n_q_h
   if (!aligned(workspace, 256)) return fail(PKV_ERR_INVALID_ARG, "workspace not 256-byte aligned");
   if (num_rows == 0) return PKV_OK;
   const int g = n_q_heads / n_kv_heads;
-  const WsParts w =
-      workspace_parts(const_cast<void*>(workspace), num_rows, n_q_heads, n_kv_heads, num_chunks);
+  const WsParts w = workspace_parts(const_cast<void*>(workspace), workspace_bytes, num_rows,
+                                    n_q_heads, n_kv_heads, num_chunks);
   pkv::CombineArgs c;
   c.seq_lens = seq_lens;
   c.window = window;

@@ -88,7 +88,8 @@ struct Smem {
   static constexpr uint32_t kQ = kMrgMl + kWarps * G * 2 * 4;  // f32 KV: [warps][G][kQStride] q
   static constexpr uint32_t kCtl =
       kQ + (DT == PKV_KV_F32 ? kWarps * G * kQStride * 4 : 0);             // int [4]
-  static constexpr uint32_t kSplit = kCtl + 16;  // the work split
+  static constexpr uint32_t kStall = kCtl + 16;  // the test hook's barrier (nothing completes it)
+  static constexpr uint32_t kSplit = kCtl + 32;  // the work split
   static constexpr uint32_t kRows = kSplit + 16;  // int row_start[rows + 1], lens[rows], pc[rows + 1]
   static size_t bytes(int rows) {
     return kAlign + kRows + plan_ints(rows) * 4;  // kAlign: base alignment slack
@@ -521,9 +522,13 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
   uint8_t* ring_sc = smem + SM::kScl + static_cast<size_t>(warp) * R * TL::kScales;  // q8_0 scales
 
   if (threadIdx.x == 0) {
+    // the tensor maps are kernel parameters, not written by an earlier kernel
+    prefetch_tensormap(&maps.k);
+    prefetch_tensormap(&maps.v);
     ctl[0] = 0;
     ctl[1] = 0;
     ctl[2] = 0;
+    mbar_init(smem_addr(smem + SM::kStall), 1);
   }
   if (lane == 0) {
     for (int s = 0; s < R; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -539,6 +544,7 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
   plan_rows(a.seq_lens, a.num_rows, a.bt_stride, a.window, blockIdx.x == 0 ? a.status : nullptr,
             lens, row_start);
 
+  const bool stalled = test_stall(smem_addr(smem + SM::kStall), a.test_stall_ns, ctl, a.status);
   plan_split(row_start, a.num_rows, a.n_kv, gridDim.x, a.aligned_split, split, pc);
   const Split sp = *split;
   const int k = blockIdx.x;
@@ -588,7 +594,6 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
   int c_pg, c_h, c_row, c_last, n_pg, n_h, n_row, n_last;
   int batch = 0;
   fetch(0, c_pg, c_h, c_row, c_last);
-  fetch(32, n_pg, n_h, n_row, n_last);
   int issued = 0;
   const uint64_t policy = policy_evict_first();
 
@@ -619,35 +624,26 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
       const uint32_t dst = smem_addr(ring + s * TL::kCodes);
       const int z = pg * a.n_kv + hh;  // tile index (the host checks num_pages * n_kv < 2^31)
       mbar_arrive_expect_tx(bar, TL::kTx);
-      if constexpr (DT == PKV_KV_F32) {  // four boxes of 32 dims per tile
-#pragma unroll
-        for (int bx = 0; bx < 4; ++bx) {
-          tma_load_3d(dst + bx * 2048, &maps.k, 32 * bx, 0, z, bar, policy);
-          tma_load_3d(dst + TL::kData + bx * 2048, &maps.v, 32 * bx, 0, z, bar, policy);
-        }
-      } else if constexpr (DT != PKV_KV_Q8_0) {
-        tma_load_3d(dst, &maps.k, 0, 0, z, bar, policy);
-        tma_load_3d(dst + 2048, &maps.k, 64, 0, z, bar, policy);
-        tma_load_3d(dst + TL::kData, &maps.v, 0, 0, z, bar, policy);
-        tma_load_3d(dst + TL::kData + 2048, &maps.v, 64, 0, z, bar, policy);
-      } else {
+      tma_load_tile<DT>(dst, &maps.k, z, bar, policy);
+      tma_load_tile<DT>(dst + TL::kData, &maps.v, z, bar, policy);
+      if constexpr (DT == PKV_KV_Q8_0) {
         const uint32_t sdst = smem_addr(ring_sc + s * TL::kScales);
         const size_t unit = static_cast<size_t>(z);
-        tma_load_3d(dst, &maps.k, 0, 0, z, bar, policy);
         bulk_g2s(sdst, a.k_scales + unit * TL::kScale, TL::kScale, bar, policy);
-        tma_load_3d(dst + TL::kData, &maps.v, 0, 0, z, bar, policy);
         bulk_g2s(sdst + TL::kScale, a.v_scales + unit * TL::kScale, TL::kScale, bar, policy);
       }
     }
     ++issued;
   };
   while (issued < n_units && issued < R) issue();
+  // the next batch of descriptors, once the first copies are on their way
+  fetch(32, n_pg, n_h, n_row, n_last);
 
   const int gid = lane >> 2, tig = lane & 3;
   float* mrg_acc = reinterpret_cast<float*>(smem + SM::kMrgAcc);
   float* mrg_ml = reinterpret_cast<float*>(smem + SM::kMrgMl);
-  bool aborted = false;
   int consumed = 0;
+  bool aborted = stalled;
   WarpState<DT> S;
   S.qs = reinterpret_cast<float*>(smem + SM::kQ) + warp * G * kQStride;  // f32 KV only
 
@@ -656,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
     const int i = row_of(row_start, a.num_rows, a.n_kv, x);
     const int npg = row_start[i + 1] - row_start[i];
     const long long row_base = static_cast<long long>(a.n_kv) * row_start[i];
-    const int h = static_cast<int>((x - row_base) / npg);
+    const int h = static_cast<int>(x - row_base) / npg;  // x - row_base < n_kv * npg < 2^31
     const long long seg_start = row_base + static_cast<long long>(h) * npg;
     const long long seg_end = seg_start + npg;
     const long long b = min(seg_end, c_end);
@@ -680,7 +676,7 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
     for (long long pos = x + ((warp - r + kWarps) % kWarps); pos < b; pos += kWarps) {
       const int u = static_cast<int>((pos - first) / kWarps);
       const int s = u % R;
-      bool ok = !aborted && mbar_wait_bounded(bar0 + 8 * s, (u / R) & 1, ctl, a.wait_ns);
+      bool ok = !aborted && mbar_wait_bounded(bar0 + 8 * s, (u / R) & 1, ctl);
       ok = __all_sync(kFull, ok);
       if (!ok) {
         if (!aborted && lane == 0 && !ctl[0]) {
@@ -736,44 +732,89 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
       named_barrier(1, kThreads);
       const bool live = !ctl[0];
       const int d = threadIdx.x;  // one dim per thread, all heads
-      if (live) {
+      const bool split = live && !whole && a.flags != nullptr;
+      // Aligned split: every piece of a split segment is the final piece of
+      // its chunk, and arrives first, with a relaxed add, while its own merge
+      // runs; the last arrival merges, and the others publish their partials
+      // afterwards through their ready flags.  Uniform split: the segment's
+      // other pieces may have ended inside their chunks, merged by one warp
+      // with a release arrival (below), so this piece does the same, but first
+      // asks whether the others have all arrived (then it is the last).
+      // (q8_0 and f32 always take the uniform split: the aligned protocol is
+      // compiled only for the 16-bit formats.)
+      constexpr bool kAlignable = DT == PKV_KV_F16 || DT == PKV_KV_BF16;
+      const bool aligned = kAlignable && sp.aligned;
+      int arrived = -1;
+      if (split && threadIdx.x == 0)
+        arrived = aligned ? atomicAdd(seg_counter(a.flags, j), 1)
+                          : load_acquire(seg_counter(a.flags, j));
+      float M[G], Ls[G], A[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float M = -INFINITY;
+      for (int g = 0; g < G; ++g) {
+        M[g] = -INFINITY;
 #pragma unroll
-          for (int w = 0; w < kWarps; ++w) M = fmaxf(M, mrg_ml[(w * G + g) * 2]);
-          float Ls = 0.f, A = 0.f;
+        for (int w = 0; w < kWarps; ++w) M[g] = fmaxf(M[g], mrg_ml[(w * G + g) * 2]);
+        Ls[g] = 0.f;
+        A[g] = 0.f;
 #pragma unroll
-          for (int w = 0; w < kWarps; ++w) {
-            const float f = exp2f(mrg_ml[(w * G + g) * 2] - M);
-            Ls = fmaf(f, mrg_ml[(w * G + g) * 2 + 1], Ls);
-            A = fmaf(f, mrg_acc[(w * G + g) * kD + d], A);
-          }
-          if (whole) {
-            out_seg[g * kD + d] = A / Ls;
-          } else {
-            a.part_acc[((k + j) * G + g) * kD + d] = A;
-            if (d == 0) {
-              a.part_ml[((k + j) * G + g) * 2] = M;
-              a.part_ml[((k + j) * G + g) * 2 + 1] = Ls;
-            }
-          }
+        for (int w = 0; w < kWarps; ++w) {
+          const float f = exp2f(mrg_ml[(w * G + g) * 2] - M[g]);
+          Ls[g] = fmaf(f, mrg_ml[(w * G + g) * 2 + 1], Ls[g]);
+          A[g] = fmaf(f, mrg_acc[(w * G + g) * kD + d], A[g]);
         }
       }
-      const bool counted = live && !whole && a.counters != nullptr;
-      named_barrier(1, kThreads);
-      if (threadIdx.x == 0) {
-        int seg_last = 0;
-        // the CTA's partial (ordered by the barrier) is released by the
-        // arrival; the last to arrive acquires every other piece's
-        if (counted) seg_last = atomic_add_acq_rel(a.counters + j, 1) == k1 - k0;
-        ctl[1] = seg_last;
+      if (live && whole) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) out_seg[g * kD + d] = A[g] / Ls[g];
       }
-      named_barrier(1, kThreads);
-      if (ctl[1]) {  // thread 0's acquire, ordered for the CTA by the barrier
-        merge_segment<G, DT != PKV_KV_Q8_0 ? PKV_MERGE_BATCH : PKV_MERGE_BATCH / 2>(
-            a.part_ml, a.part_acc, j, k0, k1, out_seg, d);
-        if (d == 0) a.counters[j] = 0;  // ready for the next call
+      auto write_partial = [&]() {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          a.part_acc[((k + j) * G + g) * kD + d] = A[g];
+          if (d == 0) {
+            a.part_ml[((k + j) * G + g) * 2] = M[g];
+            a.part_ml[((k + j) * G + g) * 2 + 1] = Ls[g];
+          }
+        }
+      };
+      if (split && aligned) {
+        if (threadIdx.x == 0) ctl[1] = arrived == k1 - k0;
+        named_barrier(1, kThreads);  // also: the merge buffer is read
+        if (ctl[1]) {  // the last arrival: merge from this piece's registers
+          merge_segment_cta_ready<G, DT == PKV_KV_Q8_0 ? 2 : 3>(
+              a.part_ml, a.part_acc, a.flags, j, k0, k1, k, M, Ls, A, mrg_acc, mrg_ml, out_seg,
+              ctl, a.status);
+          if (d == 0) *seg_counter(a.flags, j) = 0;  // ready for the next call
+        } else {
+          write_partial();
+          named_barrier(1, kThreads);  // every thread's stores ordered before thread 0's release
+          if (threadIdx.x == 0) store_release(slot_ready(a.flags, k + j), 1);
+        }
+      } else if (split) {
+        // The last piece of a segment to finish merges it.  Every piece
+        // stores its partial (the stores go out while the counter load is in
+        // flight).  If the others had all arrived when asked, this piece is
+        // the last one: it merges from its registers, with no arrival to
+        // make (thread 0's acquire, passed on by the barrier, orders the
+        // loads of the other partials).  Otherwise it arrives, releasing its
+        // partial; the arrival that completes the count merges.
+        write_partial();
+        if (threadIdx.x == 0) ctl[1] = arrived == k1 - k0;
+        named_barrier(1, kThreads);  // also: the merge buffer is read, the partial stored
+        bool last = ctl[1] != 0;
+        if (!last) {
+          if (threadIdx.x == 0)  // the CTA's partial (ordered by the barrier) is released
+            ctl[1] = atomic_add_acq_rel(seg_counter(a.flags, j), 1) == k1 - k0;
+          named_barrier(1, kThreads);
+          last = ctl[1] != 0;
+        }
+        if (last) {
+          merge_segment_cta<G, DT == PKV_KV_Q8_0 ? 2 : 3>(a.part_ml, a.part_acc, j, k0, k1, k, M,
+                                                           Ls, A, mrg_acc, mrg_ml, out_seg);
+          if (d == 0) *seg_counter(a.flags, j) = 0;  // ready for the next call
+        }
+      } else if (live && !whole) {
+        write_partial();  // for the combine launch
       }
     } else {
       __syncwarp();
@@ -794,16 +835,16 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
           __threadfence_block();
           ctl[2] = piece + 1;
         }
-        if (live && !whole && a.counters != nullptr) {
+        if (live && !whole && a.flags != nullptr) {
           __syncwarp();
           int seg_last = 0;
           // the warp's partial (ordered by __syncwarp) is released by the arrival
-          if (lane == 0) seg_last = atomic_add_acq_rel(a.counters + j, 1) == k1 - k0;
+          if (lane == 0) seg_last = atomic_add_acq_rel(seg_counter(a.flags, j), 1) == k1 - k0;
           seg_last = __shfl_sync(kFull, seg_last, 0);
           if (seg_last) {
             __syncwarp();  // lane 0's acquire, ordered for the warp
             merge_segment_warp<G>(a.part_ml, a.part_acc, j, k0, k1, out_seg, lane);
-            if (lane == 0) a.counters[j] = 0;  // ready for the next call
+            if (lane == 0) *seg_counter(a.flags, j) = 0;  // ready for the next call
           }
         }
       }
@@ -882,26 +923,44 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// A layer's K or V data as a 3-D tensor [tiles][16 tokens][128 dims] read in
-// boxes of 16 rows of 128 bytes under the 128-byte swizzle: [16][64] (f16,
-// bf16), [16][32] (f32) or [16][128] (q8_0 codes).
+// A layer's K or V data, [tiles][16 tokens][128 dims], as the tensor map a
+// tile copy reads through (tma_load_tile), under the 128-byte swizzle:
+//   f16, bf16: 4-D {64 dims, 16 tokens, 2 halves, tiles}, strides {256, 128,
+//     4096} bytes, box {64, 16, 2, 1}: shared memory [half][16][64];
+//   f32: 4-D {32 dims, 16 tokens, 4 quarters, tiles}, strides {512, 128,
+//     8192}, box {32, 16, 4, 1}: [quarter][16][32];
+//   q8_0: 3-D {128 codes, 16 tokens, tiles}, box {128, 16, 1}: [16][128].
+// Each is 16 token rows of 128 bytes per box, the layout the swizzled tile
+// addressing (tile_offset) reads.
 static cudaError_t encode_tile_map(CUtensorMap* m, int dtype, void* base, long long tiles) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   const cuuint32_t esize = dtype == PKV_KV_F32 ? 4u : dtype == PKV_KV_Q8_0 ? 1u : 2u;  // bytes
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(kPage),
-                              static_cast<cuuint64_t>(tiles)};
-  const cuuint64_t strides[2] = {kD * esize, kD * kPage * esize};  // bytes
-  const cuuint32_t box[3] = {128u / esize, static_cast<cuuint32_t>(kPage), 1u};
-  const cuuint32_t estride[3] = {1u, 1u, 1u};
-  const CUresult r =
-      fn(m, dtype == PKV_KV_F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-            : dtype == PKV_KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-            : dtype == PKV_KV_F32  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                   : CU_TENSOR_MAP_DATA_TYPE_UINT8,
-         3, base, dims,
-         strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const cuuint32_t row = 128u / esize;   // elements in a 128-byte row
+  const cuuint32_t parts = kD / row;     // rows of a token: 1 (q8_0), 2 (16-bit), 4 (f32)
+  const cuuint64_t tok = static_cast<cuuint64_t>(kD) * esize;  // bytes of a token
+  const cuuint32_t estride[4] = {1u, 1u, 1u, 1u};
+  const CUtensorMapDataType type = dtype == PKV_KV_F16    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                   : dtype == PKV_KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : dtype == PKV_KV_F32  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                          : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUresult r;
+  if (parts == 1) {
+    const cuuint64_t dims[3] = {row, static_cast<cuuint64_t>(kPage), static_cast<cuuint64_t>(tiles)};
+    const cuuint64_t strides[2] = {tok, tok * kPage};
+    const cuuint32_t box[3] = {row, static_cast<cuuint32_t>(kPage), 1u};
+    r = fn(m, type, 3, base, dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const cuuint64_t dims[4] = {row, static_cast<cuuint64_t>(kPage), parts,
+                                static_cast<cuuint64_t>(tiles)};
+    const cuuint64_t strides[3] = {tok, 128u, tok * kPage};
+    const cuuint32_t box[4] = {row, static_cast<cuuint32_t>(kPage), parts, 1u};
+    r = fn(m, type, 4, base, dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 

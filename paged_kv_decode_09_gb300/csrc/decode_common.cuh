@@ -78,6 +78,22 @@ struct Tiles<PKV_KV_Q8_0> {
   static constexpr int kRing = PKV_Q8_RING;  // stages per warp
 };
 
+// Copy tile z (one (page, KV head) of K or V) into a stage: one tensor copy
+// for every format.  The 16-bit and f32 tiles go through 4-D maps whose box
+// lists the dims of a 128-byte row, the 16 tokens, then the row's place in
+// the 256-byte (512-byte) token, so the copy lands as 2 (4) swizzled boxes
+// of [16 tokens][128 bytes]; q8_0 tiles are one such box.  One copy per tile
+// instead of 2 (16-bit) or 4 (f32): fewer copies to queue at the start of a
+// step, when every warp of the GPU queues its first stages at once.
+template <int DT>
+__device__ __forceinline__ void tma_load_tile(uint32_t dst, const void* tmap, int z, uint32_t bar,
+                                              uint64_t policy) {
+  if constexpr (DT == PKV_KV_Q8_0)
+    tma_load_3d(dst, tmap, 0, 0, z, bar, policy);
+  else
+    tma_load_4d(dst, tmap, 0, 0, 0, z, bar, policy);
+}
+
 // ------------------------------------------------------------ operands ----
 // Byte offset of the 16-byte chunk c (8 f16 / bf16, 4 f32 or 16 int8 values)
 // of token row t in a swizzled tile: 128-byte rows, chunk index xor (row mod
@@ -134,6 +150,13 @@ __device__ __forceinline__ float pow2i(int e) {  // 2^e for -126 <= e <= 127
   return __int_as_float((127 + e) << 23);
 }
 // ---------------------------------------------------------------- merge ----
+// The merge's flags below the end of the workspace (DecodeArgs::flags).
+__device__ __forceinline__ int* seg_counter(int32_t* flags, long long j) { return flags - 1 - 2 * j; }
+__device__ __forceinline__ int* slot_ready(int32_t* flags, long long s) { return flags - 2 - 2 * s; }
+__device__ __forceinline__ int* mq_counter(int32_t* flags, long long j, int w) {
+  return flags - 1 - (static_cast<long long>(kMqCounters) * j + w);
+}
+
 // Merge the base-2 partial states of segment j held in slots k + j for the
 // chunks k0..k1 that meet it; one thread per dim d, all G heads:
 //   M = max_k m2_k,  out = sum_k 2^(m2_k - M) acc_k / sum_k 2^(m2_k - M) l_k,
@@ -245,6 +268,210 @@ __device__ __forceinline__ void merge_segment_warp(const float* part_ml, const f
   for (int g = 0; g < G; ++g)
     *reinterpret_cast<float4*>(o + g * kD + lane * 4) =
         make_float4(A[g].x / Ls[g], A[g].y / Ls[g], A[g].z / Ls[g], A[g].w / Ls[g]);
+}
+
+// The merge of segment j by the CTA that finishes its last piece: the CTA's
+// own piece state, in registers (thread d holds M, Ls, A of dim d for the G
+// heads), and the partial states of the segment's other pieces (slots
+// kk + j for kk in [k0, k1], kk != k).  The four warps load the other pieces
+// together, kPpw pieces a warp per L2 round trip (4 kPpw a trip for the CTA),
+// lane l taking dims 4l .. 4l + 3; each warp folds its pieces into one state,
+// leaves it in the shared merge buffer, and after a CTA barrier thread d
+// combines its own state with the four warps' and writes the output.  Every
+// thread of the CTA calls it; the merge buffer must be free.
+template <int G, int kPpw>
+__device__ __forceinline__ void merge_segment_cta(const float* part_ml, const float* part_acc,
+                                                  long long j, int k0, int k1, int k,
+                                                  const float (&M)[G], const float (&Ls)[G],
+                                                  const float (&A)[G], float* mrg_acc,
+                                                  float* mrg_ml, float* o) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_other = k1 - k0;
+  float wm[G], wl[G];
+  float4 wa[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    wm[g] = -INFINITY;
+    wl[g] = 0.f;
+    wa[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  for (int base = 0; base < n_other; base += 4 * kPpw) {
+    float m[kPpw][G], l[kPpw][G];
+    float4 x[kPpw][G];
+#pragma unroll
+    for (int u = 0; u < kPpw; ++u) {
+      const int p = base + warp + 4 * u;
+      const bool in = p < n_other;
+      const int kk = k0 + p + (k0 + p >= k ? 1 : 0);  // the p-th piece other than k
+      const long long slot = kk + j;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        m[u][g] = in ? __ldcg(part_ml + (slot * G + g) * 2) : -INFINITY;
+        l[u][g] = in ? __ldcg(part_ml + (slot * G + g) * 2 + 1) : 0.f;
+        x[u][g] = in ? __ldcg(reinterpret_cast<const float4*>(part_acc + (slot * G + g) * kD) + lane)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float bm = wm[g];
+#pragma unroll
+      for (int u = 0; u < kPpw; ++u) bm = fmaxf(bm, m[u][g]);
+      if (bm == -INFINITY) continue;  // no piece for this warp yet
+      const float sc = exp2f(wm[g] - bm);  // 0 while wm is -inf
+      wl[g] *= sc;
+      wa[g].x *= sc;
+      wa[g].y *= sc;
+      wa[g].z *= sc;
+      wa[g].w *= sc;
+#pragma unroll
+      for (int u = 0; u < kPpw; ++u) {
+        const float f = exp2f(m[u][g] - bm);  // 0 for a missing piece
+        wl[g] = fmaf(f, l[u][g], wl[g]);
+        wa[g].x = fmaf(f, x[u][g].x, wa[g].x);
+        wa[g].y = fmaf(f, x[u][g].y, wa[g].y);
+        wa[g].z = fmaf(f, x[u][g].z, wa[g].z);
+        wa[g].w = fmaf(f, x[u][g].w, wa[g].w);
+      }
+      wm[g] = bm;
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    if (lane == 0) {
+      mrg_ml[(warp * G + g) * 2] = wm[g];
+      mrg_ml[(warp * G + g) * 2 + 1] = wl[g];
+    }
+    *reinterpret_cast<float4*>(mrg_acc + (warp * G + g) * kD + lane * 4) = wa[g];
+  }
+  named_barrier(1, kThreads);
+  const int d = threadIdx.x;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float Mx = M[g];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) Mx = fmaxf(Mx, mrg_ml[(w * G + g) * 2]);
+    const float f0 = exp2f(M[g] - Mx);
+    float L = f0 * Ls[g], Ax = f0 * A[g];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = exp2f(mrg_ml[(w * G + g) * 2] - Mx);  // 0 for a warp without pieces
+      L = fmaf(f, mrg_ml[(w * G + g) * 2 + 1], L);
+      Ax = fmaf(f, mrg_acc[(w * G + g) * kD + d], Ax);
+    }
+    o[g * kD + d] = Ax / L;
+  }
+}
+
+// merge_segment_cta for pieces that publish their partials through ready
+// flags (slot_ready): before a warp loads a piece's partial, one of its lanes
+// waits for that piece's flag (acquire, bounded; the piece's CTA has already
+// arrived, so it is running and publishes without waiting on anything) and
+// clears it for the next call.  Returns false, without writing the output,
+// if a wait gave up (then *abort is set and PKV_DEV_TIMEOUT recorded).
+template <int G, int kPpw>
+__device__ __forceinline__ bool merge_segment_cta_ready(const float* part_ml, const float* part_acc,
+                                                        int32_t* flags, long long j, int k0, int k1,
+                                                        int k, const float (&M)[G],
+                                                        const float (&Ls)[G], const float (&A)[G],
+                                                        float* mrg_acc, float* mrg_ml, float* o,
+                                                        volatile int* abort, int32_t* status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_other = k1 - k0;
+  float wm[G], wl[G];
+  float4 wa[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    wm[g] = -INFINITY;
+    wl[g] = 0.f;
+    wa[g] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  bool ok = true;
+  for (int base = 0; base < n_other; base += 4 * kPpw) {
+    // lane u < kPpw waits for the flag of the warp's piece u of this round
+    if (lane < kPpw) {
+      const int p = base + warp + 4 * lane;
+      if (p < n_other) {
+        int* f = slot_ready(flags, k0 + p + (k0 + p >= k ? 1 : 0) + j);
+        if (wait_flag(f, abort))
+          *f = 0;  // ready for the next call
+        else
+          ok = false;
+      }
+    }
+    ok = __all_sync(kFull, ok);
+    if (!ok) break;
+    __syncwarp();  // the lanes' acquires, ordered for the warp
+    float m[kPpw][G], l[kPpw][G];
+    float4 x[kPpw][G];
+#pragma unroll
+    for (int u = 0; u < kPpw; ++u) {
+      const int p = base + warp + 4 * u;
+      const bool in = p < n_other;
+      const long long slot = k0 + p + (k0 + p >= k ? 1 : 0) + j;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        m[u][g] = in ? __ldcg(part_ml + (slot * G + g) * 2) : -INFINITY;
+        l[u][g] = in ? __ldcg(part_ml + (slot * G + g) * 2 + 1) : 0.f;
+        x[u][g] = in ? __ldcg(reinterpret_cast<const float4*>(part_acc + (slot * G + g) * kD) + lane)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float bm = wm[g];
+#pragma unroll
+      for (int u = 0; u < kPpw; ++u) bm = fmaxf(bm, m[u][g]);
+      if (bm == -INFINITY) continue;
+      const float sc = exp2f(wm[g] - bm);
+      wl[g] *= sc;
+      wa[g].x *= sc;
+      wa[g].y *= sc;
+      wa[g].z *= sc;
+      wa[g].w *= sc;
+#pragma unroll
+      for (int u = 0; u < kPpw; ++u) {
+        const float f = exp2f(m[u][g] - bm);
+        wl[g] = fmaf(f, l[u][g], wl[g]);
+        wa[g].x = fmaf(f, x[u][g].x, wa[g].x);
+        wa[g].y = fmaf(f, x[u][g].y, wa[g].y);
+        wa[g].z = fmaf(f, x[u][g].z, wa[g].z);
+        wa[g].w = fmaf(f, x[u][g].w, wa[g].w);
+      }
+      wm[g] = bm;
+    }
+  }
+  if (!ok && lane == 0 && !abort[0]) {
+    abort[0] = 1;
+    record_status(status, PKV_DEV_TIMEOUT);
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    if (lane == 0) {
+      mrg_ml[(warp * G + g) * 2] = wm[g];
+      mrg_ml[(warp * G + g) * 2 + 1] = wl[g];
+    }
+    *reinterpret_cast<float4*>(mrg_acc + (warp * G + g) * kD + lane * 4) = wa[g];
+  }
+  named_barrier(1, kThreads);
+  if (abort[0]) return false;
+  const int d = threadIdx.x;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float Mx = M[g];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) Mx = fmaxf(Mx, mrg_ml[(w * G + g) * 2]);
+    const float f0 = exp2f(M[g] - Mx);
+    float L = f0 * Ls[g], Ax = f0 * A[g];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = exp2f(mrg_ml[(w * G + g) * 2] - Mx);
+      L = fmaf(f, mrg_ml[(w * G + g) * 2 + 1], L);
+      Ax = fmaf(f, mrg_acc[(w * G + g) * kD + d], Ax);
+    }
+    o[g * kD + d] = Ax / L;
+  }
+  return true;
 }
 
 // Spin (bounded) until the shared merge buffer has been released for piece

@@ -106,7 +106,8 @@ struct MqSmem {
   static constexpr uint32_t kQ = kMrgMl + kWarps * kWarpCols * 2 * 4;  // f32 KV: [warps][8][kQStride] q
   static constexpr uint32_t kCtl =
       kQ + (DT == PKV_KV_F32 ? kWarps * kWarpCols * kQStride * 4 : 0);
-  static constexpr uint32_t kSplit = kCtl + 16;  // the work split
+  static constexpr uint32_t kStall = kCtl + 16;  // the test hook's barrier (nothing completes it)
+  static constexpr uint32_t kSplit = kCtl + 32;  // the work split
   static constexpr uint32_t kRows = kSplit + 16;  // row_start, lens, chunks before each row
   static size_t bytes(int rows) { return kAlign + kRows + plan_ints(rows) * 4; }
   static_assert(Tiles<DT>::kCodes % 1024 == 0, "tile stages keep the swizzle atom alignment");
@@ -615,9 +616,13 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int plan_window = a.window > 0 ? a.window + a.q_len - 1 : 0;
 
   if (threadIdx.x == 0) {
+    // the tensor maps are kernel parameters, not written by an earlier kernel
+    prefetch_tensormap(&maps.k);
+    prefetch_tensormap(&maps.v);
     ctl[0] = 0;
     ctl[1] = 0;
     ctl[2] = 0;
+    mbar_init(smem_addr(smem + SM::kStall), 1);
   }
   if (lane == 0) {
     for (int s = 0; s < R; ++s) mbar_init(bar0 + 8 * s, 1);
@@ -627,6 +632,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   grid_launch_dependents();
   plan_rows(a.seq_lens, a.num_rows, a.bt_stride, plan_window,
             blockIdx.x == 0 ? a.status : nullptr, lens, row_start, a.q_len);
+  const bool stalled = test_stall(smem_addr(smem + SM::kStall), a.test_stall_ns, ctl, a.status);
   int* pc = lens + a.num_rows;
   plan_split(row_start, a.num_rows, a.n_kv, gridDim.x, a.aligned_split,
              reinterpret_cast<Split*>(smem + SM::kSplit), pc);
@@ -674,7 +680,6 @@ __global__ void __launch_bounds__(kThreads, 2)
   int c_pg, c_h, c_row, c_p, n_pg, n_h, n_row, n_p;
   int batch = 0;
   fetch(0, c_pg, c_h, c_row, c_p);
-  fetch(32, n_pg, n_h, n_row, n_p);
   int issued = 0;
   const uint64_t policy = policy_evict_first();
 
@@ -708,34 +713,24 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint32_t dst = smem_addr(ring + s * TL::kCodes);
       const int z = pg * a.n_kv + hh;
       mbar_arrive_expect_tx(bar, TL::kTx);
-      if constexpr (DT == PKV_KV_F32) {  // four boxes of 32 dims per tile
-#pragma unroll
-        for (int bx = 0; bx < 4; ++bx) {
-          tma_load_3d(dst + bx * 2048, &maps.k, 32 * bx, 0, z, bar, policy);
-          tma_load_3d(dst + TL::kData + bx * 2048, &maps.v, 32 * bx, 0, z, bar, policy);
-        }
-      } else if constexpr (DT != PKV_KV_Q8_0) {
-        tma_load_3d(dst, &maps.k, 0, 0, z, bar, policy);
-        tma_load_3d(dst + 2048, &maps.k, 64, 0, z, bar, policy);
-        tma_load_3d(dst + TL::kData, &maps.v, 0, 0, z, bar, policy);
-        tma_load_3d(dst + TL::kData + 2048, &maps.v, 64, 0, z, bar, policy);
-      } else {
+      tma_load_tile<DT>(dst, &maps.k, z, bar, policy);
+      tma_load_tile<DT>(dst + TL::kData, &maps.v, z, bar, policy);
+      if constexpr (DT == PKV_KV_Q8_0) {
         const uint32_t sdst = smem_addr(ring_sc + s * TL::kScales);
         const size_t unit = static_cast<size_t>(z);
-        tma_load_3d(dst, &maps.k, 0, 0, z, bar, policy);
         bulk_g2s(sdst, a.k_scales + unit * TL::kScale, TL::kScale, bar, policy);
-        tma_load_3d(dst + TL::kData, &maps.v, 0, 0, z, bar, policy);
         bulk_g2s(sdst + TL::kScale, a.v_scales + unit * TL::kScale, TL::kScale, bar, policy);
       }
     }
     ++issued;
   };
   while (issued < n_units && issued < R) issue();
+  fetch(32, n_pg, n_h, n_row, n_p);  // the next batch, once the first copies are on their way
 
   float* mrg_acc = reinterpret_cast<float*>(smem + SM::kMrgAcc);
   float* mrg_ml = reinterpret_cast<float*>(smem + SM::kMrgMl);
-  bool aborted = false;
   int consumed = 0;
+  bool aborted = stalled;
   MqState<DT, NT> S;
   S.qs = reinterpret_cast<float*>(smem + SM::kQ) + warp * kWarpCols * kQStride;  // f32 KV only
 
@@ -744,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int i = row_of(row_start, a.num_rows, a.n_kv, x);
     const int npg = row_start[i + 1] - row_start[i];
     const long long row_base = static_cast<long long>(a.n_kv) * row_start[i];
-    const int h = static_cast<int>((x - row_base) / npg);
+    const int h = static_cast<int>(x - row_base) / npg;  // x - row_base < n_kv * npg < 2^31
     const long long seg_start = row_base + static_cast<long long>(h) * npg;
     const long long seg_end = seg_start + npg;
     const long long b = min(seg_end, c_end);
@@ -814,7 +809,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (long long pos = x + ((warp - r0 + kWarps) % kWarps); pos < b; pos += kWarps) {
       const int u = static_cast<int>((pos - first) / kWarps);
       const int s = u % R;
-      bool ok = !aborted && mbar_wait_bounded(bar0 + 8 * s, (u / R) & 1, ctl, a.wait_ns);
+      bool ok = !aborted && mbar_wait_bounded(bar0 + 8 * s, (u / R) & 1, ctl);
       ok = __all_sync(kFull, ok);
       if (!ok) {
         if (!aborted && lane == 0 && !ctl[0]) {
@@ -914,20 +909,20 @@ __global__ void __launch_bounds__(kThreads, 2)
           write_piece_dim(c, d, M, Ls, A);
         }
       }
-      const bool counted = live && !whole && a.counters != nullptr;
+      const bool counted = live && !whole && a.flags != nullptr;
       named_barrier(1, kThreads);
       if (threadIdx.x == 0) {
         int seg_last = 0;
         // the CTA's partial (ordered by the barrier) is released by the
         // arrival; the last to arrive acquires every other piece's
-        if (counted) seg_last = atomic_add_acq_rel(a.counters + j, 1) == k1 - k0;
+        if (counted) seg_last = atomic_add_acq_rel(mq_counter(a.flags, j, 0), 1) == k1 - k0;
         ctl[1] = seg_last;
       }
       named_barrier(1, kThreads);
       if (ctl[1]) {  // the CTA merges the segment: warp w takes columns 2w, 2w + 1
         mq_merge_segment_warp<2, 4>(a.part_ml, a.part_acc, j, k0, k1, 2 * warp, nc, out_col,
                                     lane);
-        if (threadIdx.x == 0) a.counters[j] = 0;
+        if (threadIdx.x == 0) *mq_counter(a.flags, j, 0) = 0;
       }
     } else {
       __syncwarp();
@@ -954,17 +949,17 @@ __global__ void __launch_bounds__(kThreads, 2)
           __threadfence_block();
           ctl[2] = piece + 1;
         }
-        if (live && !whole && a.counters != nullptr) {
+        if (live && !whole && a.flags != nullptr) {
           __syncwarp();
           int seg_last = 0;
           // the warp's partial (ordered by __syncwarp) is released by the arrival
-          if (lane == 0) seg_last = atomic_add_acq_rel(a.counters + j, 1) == k1 - k0;
+          if (lane == 0) seg_last = atomic_add_acq_rel(mq_counter(a.flags, j, 0), 1) == k1 - k0;
           seg_last = __shfl_sync(kFull, seg_last, 0);
           if (seg_last) {
             __syncwarp();  // lane 0's acquire, ordered for the warp
             mq_merge_segment_warp<kWarpCols, 1>(a.part_ml, a.part_acc, j, k0, k1, 0, nc, out_col,
                                               lane);
-            if (lane == 0) a.counters[j] = 0;
+            if (lane == 0) *mq_counter(a.flags, j, 0) = 0;
           }
         }
       }
@@ -1008,7 +1003,8 @@ struct MqtSmem {
   static constexpr uint32_t kFull = kScl + kStages * Tiles<DT>::kScales;
   static constexpr uint32_t kEmpty = kFull + kStages * 8;
   static constexpr uint32_t kCtl = kEmpty + kStages * 8;
-  static constexpr uint32_t kSplit = kCtl + 16;  // the work split
+  static constexpr uint32_t kStall = kCtl + 16;  // the test hook's barrier (nothing completes it)
+  static constexpr uint32_t kSplit = kCtl + 32;  // the work split
   static constexpr uint32_t kRows = kSplit + 16;  // row_start, lens, chunks before each row
   static size_t bytes(int rows) { return kAlign + kRows + plan_ints(rows) * 4; }
 };
@@ -1045,7 +1041,10 @@ __global__ void __launch_bounds__(kThreads, team_ctas(NT))
   const int plan_window = a.window > 0 ? a.window + a.q_len - 1 : 0;
 
   if (threadIdx.x == 0) {
+    prefetch_tensormap(&maps.k);  // kernel parameters, not written by an earlier kernel
+    prefetch_tensormap(&maps.v);
     ctl[0] = 0;
+    mbar_init(smem_addr(smem + SM::kStall), 1);
     const uint32_t f = smem_addr(smem + SM::kFull), e = smem_addr(smem + SM::kEmpty);
     for (int s = 0; s < RS; ++s) {
       mbar_init(f + 8 * s, 1);
@@ -1057,6 +1056,7 @@ __global__ void __launch_bounds__(kThreads, team_ctas(NT))
   grid_launch_dependents();
   plan_rows(a.seq_lens, a.num_rows, a.bt_stride, plan_window,
             blockIdx.x == 0 ? a.status : nullptr, lens, row_start, a.q_len);
+  const bool stalled = test_stall(smem_addr(smem + SM::kStall), a.test_stall_ns, ctl, a.status);
   int* pc = lens + a.num_rows;
   plan_split(row_start, a.num_rows, a.n_kv, a.vchunks, a.aligned_split,
              reinterpret_cast<Split*>(smem + SM::kSplit), pc);
@@ -1104,7 +1104,6 @@ __global__ void __launch_bounds__(kThreads, team_ctas(NT))
   int c_pg, c_h, c_row, c_p, n_pg, n_h, n_row, n_p;
   int batch = 0;
   fetch(0, c_pg, c_h, c_row, c_p);
-  fetch(32, n_pg, n_h, n_row, n_p);
   int issued = 0;  // units this warp has copied
   const uint64_t policy = policy_evict_first();
 
@@ -1138,26 +1137,22 @@ __global__ void __launch_bounds__(kThreads, team_ctas(NT))
       const uint32_t dst = smem_addr(ring + s * TL::kCodes);
       const int z = pg * a.n_kv + hh;
       mbar_arrive_expect_tx(bar, TL::kTx);
-      if constexpr (DT != PKV_KV_Q8_0) {
-        tma_load_3d(dst, &maps.k, 0, 0, z, bar, policy);
-        tma_load_3d(dst + 2048, &maps.k, 64, 0, z, bar, policy);
-        tma_load_3d(dst + TL::kData, &maps.v, 0, 0, z, bar, policy);
-        tma_load_3d(dst + TL::kData + 2048, &maps.v, 64, 0, z, bar, policy);
-      } else {
+      tma_load_tile<DT>(dst, &maps.k, z, bar, policy);
+      tma_load_tile<DT>(dst + TL::kData, &maps.v, z, bar, policy);
+      if constexpr (DT == PKV_KV_Q8_0) {
         const uint32_t sdst = smem_addr(ring_sc + s * TL::kScales);
         const size_t unit = static_cast<size_t>(z);
-        tma_load_3d(dst, &maps.k, 0, 0, z, bar, policy);
         bulk_g2s(sdst, a.k_scales + unit * TL::kScale, TL::kScale, bar, policy);
-        tma_load_3d(dst + TL::kData, &maps.v, 0, 0, z, bar, policy);
         bulk_g2s(sdst + TL::kScale, a.v_scales + unit * TL::kScale, TL::kScale, bar, policy);
       }
     }
     ++issued;
   };
-  while (issued < n_mine && wt + TS * issued < RT) issue();
+  while (issued < n_mine && wt + TS * issued < RT) issue();  // at most 32 units: batch 0
+  fetch(32, n_pg, n_h, n_row, n_p);  // the next batch, once the first copies are on their way
 
-  bool aborted = false;
   int consumed = 0;  // units [0, consumed) have landed (this warp waited for them)
+  bool aborted = stalled;
   auto fail = [&]() {
     if (!aborted && lane == 0 && !ctl[0]) {
       ctl[0] = 1;
@@ -1171,7 +1166,7 @@ __global__ void __launch_bounds__(kThreads, team_ctas(NT))
     const int i = row_of(row_start, a.num_rows, a.n_kv, x);
     const int npg = row_start[i + 1] - row_start[i];
     const long long row_base = static_cast<long long>(a.n_kv) * row_start[i];
-    const int h = static_cast<int>((x - row_base) / npg);
+    const int h = static_cast<int>(x - row_base) / npg;  // x - row_base < n_kv * npg < 2^31
     const long long seg_start = row_base + static_cast<long long>(h) * npg;
     const long long seg_end = seg_start + npg;
     const long long b = min(seg_end, c_end);
@@ -1218,7 +1213,7 @@ __global__ void __launch_bounds__(kThreads, team_ctas(NT))
     for (long long pos = x; pos < b; ++pos) {
       const int v = static_cast<int>(pos - c_begin);
       const int s = v % RT;
-      bool ok = !aborted && mbar_wait_bounded(full0 + 8 * s, (v / RT) & 1, ctl, a.wait_ns);
+      bool ok = !aborted && mbar_wait_bounded(full0 + 8 * s, (v / RT) & 1, ctl);
       ok = __all_sync(kFull, ok);
       if (!ok) {
         fail();
@@ -1304,17 +1299,17 @@ __global__ void __launch_bounds__(kThreads, team_ctas(NT))
           }
         }
       }
-      if (!whole && a.counters != nullptr) {
+      if (!whole && a.flags != nullptr) {
         __syncwarp();
         int last = 0;
         // the warp's partial (ordered by __syncwarp) is released by its arrival
-        if (lane == 0) last = atomic_add_acq_rel(a.counters + j * kMqCounters + wt, 1) == k1 - k0;
+        if (lane == 0) last = atomic_add_acq_rel(mq_counter(a.flags, j, wt), 1) == k1 - k0;
         last = __shfl_sync(kFull, last, 0);
         if (last) {
           __syncwarp();  // lane 0's acquire, ordered for the warp
           mq_merge_segment_warp<CW, NT == 1 ? 2 : 1>(a.part_ml, a.part_acc, j, k0, k1, cbase, nc,
                                                      out_col, lane);
-          if (lane == 0) a.counters[j * kMqCounters + wt] = 0;  // ready for the next call
+          if (lane == 0) *mq_counter(a.flags, j, wt) = 0;  // ready for the next call
         }
       }
     }

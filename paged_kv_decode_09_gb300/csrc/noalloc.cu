@@ -118,12 +118,14 @@ extern "C" pkv_status paged_decode_attention_static(const pkv_pool* pool, int la
              need, static_cast<unsigned>(PKV_STATIC_SCRATCH_BYTES));
     return pkv::record_error(PKV_ERR_WORKSPACE, g_static_error);
   }
-  // The arrival counters must start at zero.  Completed calls leave them at
-  // zero, but a call that timed out may not have: clear them every time.
+  // The merge's flags (arrival counters and ready flags, at the end of the
+  // array) must start at zero.  Completed calls leave them at zero, but a call
+  // that timed out may not have: clear this call's flags every time.
   if (need > 0) {
-    const size_t counters =
-        pkv::counter_bytes(static_cast<long long>(num_rows) * n_kv);
-    if (cudaMemsetAsync(base, 0, counters, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    const long long slots = static_cast<long long>(num_chunks) + static_cast<long long>(num_rows) * n_kv;
+    const size_t flags = pkv::flag_bytes(slots);
+    uint8_t* end = reinterpret_cast<uint8_t*>(pkv::flags_end(base, PKV_STATIC_SCRATCH_BYTES));
+    if (cudaMemsetAsync(end - flags, 0, flags, static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return pkv::record_error(PKV_ERR_CUDA, "paged_decode_attention_static: clearing counters");
   }
   // need == 0 means invalid geometry: the regular entry point reports it.

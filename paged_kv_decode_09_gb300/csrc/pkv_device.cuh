@@ -18,9 +18,7 @@ constexpr int kQBlock = PKV_Q8_BLOCK;   // q8_0 block along head_dim
 constexpr unsigned kFull = 0xffffffffu;
 
 // A wait on a shared-memory barrier gives up after this long (the whole
-// decode of a batch takes well under a millisecond).  The attention kernels
-// take the limit of their waits on tile copies as an argument (this value
-// unless kv_pool_set_wait_limit changed it); every other wait uses it as is.
+// decode of a batch takes well under a millisecond).
 constexpr unsigned long long kWaitLimitNs = PKV_DEFAULT_WAIT_NS;  // ~1.07 s
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -57,20 +55,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Whether the phase of `bar` with the given parity has completed, without
-// waiting.
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -78,12 +62,10 @@ __device__ __forceinline__ unsigned long long global_ns() {
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Returns
-// false, without waiting further, once *abort is set or after `limit_ns`;
-// with limit_ns = 0, unless the phase has already completed.
+// false, without waiting further, once *abort is set or after `limit_ns`.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   const volatile int* abort,
                                                   unsigned long long limit_ns = kWaitLimitNs) {
-  if (limit_ns == 0) return mbar_test_wait(bar, parity);
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   while (true) {
@@ -118,6 +100,23 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int 
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// Fetch a tensor map (the generic address of a kernel parameter) into the
+// cache the tensor copies read it from, ahead of the first copy.
+__device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+// 4-D tiled bulk tensor copy global -> shared (as tma_load_3d, one more
+// coordinate).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int x, int y, int z,
+                                            int w, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy)
       : "memory");
 }
 
@@ -190,6 +189,25 @@ __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// The kernels' test hook (kv_pool_set_test_stall): with stall_ns > 0, each
+// warp waits up to stall_ns on `bar`, a barrier that nothing completes, as
+// it would on a copy that never lands.  The wait runs out and the warp gives
+// up: it sets the CTA's abort flag and PKV_DEV_TIMEOUT, and the kernel then
+// queues its first copies, reads nothing, drains them and returns, as after
+// a real timeout.  Called early in the kernel, where few registers are live.
+// Returns true if the warp gave up.  Warp-uniform.
+__device__ __forceinline__ bool test_stall(uint32_t bar, unsigned long long stall_ns,
+                                           volatile int* ctl, int32_t* status) {
+  if (stall_ns == 0) return false;
+  bool ok = mbar_wait_bounded(bar, 0, ctl, stall_ns);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok && (threadIdx.x & 31) == 0 && !ctl[0]) {
+    ctl[0] = 1;
+    if (status) atomicOr(reinterpret_cast<unsigned int*>(status), PKV_DEV_TIMEOUT);
+  }
+  return !ok;
+}
+
 // Named barrier over `count` threads (id 0 is __syncthreads).
 __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -206,6 +224,35 @@ __device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
                : "l"(p), "r"(v)
                : "memory");
   return old;
+}
+
+// Load with acquire order at GPU scope: the caller sees every write released
+// before the value it reads.
+__device__ __forceinline__ int load_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Store with release order at GPU scope: the writes ordered before it in the
+// caller (including other threads' writes ordered by a barrier) are visible
+// to whoever acquires the value it stores.
+__device__ __forceinline__ void store_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait (bounded) until *p is non-zero, reading it with acquire order; false
+// after kWaitLimitNs or once *abort is set.
+__device__ __forceinline__ bool wait_flag(const int* p, const volatile int* abort) {
+  if (load_acquire(p)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i)
+      if (load_acquire(p)) return true;
+    if (*abort) return false;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
 }
 
 __device__ __forceinline__ void record_status(int32_t* status, uint32_t bits) {
@@ -264,10 +311,32 @@ __device__ __forceinline__ void plan_rows(const int32_t* __restrict__ seq_lens, 
   __syncthreads();
 }
 
+// floor(x / y) for 0 <= x and 0 < y, for the work-split search.  Integer
+// division is a long dependent sequence on the GPU, and the search runs a
+// chain of them before a CTA can queue its first copy; for operands below
+// 2^21 the quotient is estimated in fp32 (x times an approximate reciprocal
+// of y: the estimate is within one of the quotient) and corrected by the
+// sign of the remainder.  Larger operands take the plain division.  (Measured
+// per CTA on the 8B f16 batch: the search 2059 -> 1830 cycles; elsewhere the
+// plain 32-bit division was as fast or faster, so it is kept there.)
+__device__ __forceinline__ int udiv(int x, int y) {
+  if ((x | y) < (1 << 21)) {
+    const int q = __float2int_rz(__fdividef(__int2float_rn(x), __int2float_rn(y)));
+    const int r = x - q * y;
+    return q + (r >= y ? 1 : 0) - (r < 0 ? 1 : 0);
+  }
+  return x / y;
+}
+
 // Chunk holding unit x (0 <= x < T) when T units are split into C chunks
 // [floor(kT/C), floor((k+1)T/C)): the largest k with floor(kT/C) <= x, which
-// is ceil((x + 1) C / T) - 1.
+// is ceil((x + 1) C / T) - 1.  In 32-bit arithmetic when T (C + 1) < 2^31
+// (a 64-bit division is a long software routine on the GPU).
 __device__ __forceinline__ int chunk_of(long long x, long long T, int C) {
+  if (T * (C + 1) < (1ll << 31)) {
+    const int xi = static_cast<int>(x), Ti = static_cast<int>(T);
+    return ((xi + 1) * C + Ti - 1) / Ti - 1;
+  }
   return static_cast<int>(((x + 1) * C + T - 1) / T - 1);
 }
 
@@ -326,8 +395,9 @@ __device__ __forceinline__ void plan_split(const int* row_start, int num_rows, i
   if (allow_aligned && T > 0 && T < (1ll << 31) && C > 0) {
     const int T32 = static_cast<int>(T);
     const int Cs = C < (1 << 29) ? C : (1 << 29);  // counts saturate at Cs + 1
-    const int lo0 = T32 / Cs + (T32 % Cs != 0);
-    const int hi0 = T32 < (1 << 27) ? (11 * T32) / (10 * Cs) : static_cast<int>((11ll * T32) / (10ll * Cs));
+    const int q0 = udiv(T32, Cs);
+    const int lo0 = q0 + (T32 - q0 * Cs != 0);  // ceil(T / C)
+    const int hi0 = T32 < (1 << 27) ? udiv(11 * T32, 10 * Cs) : static_cast<int>((11ll * T32) / (10ll * Cs));
     // only when the cap may exceed ceil(T / C) (about 10 units a chunk or more)
     const int cand = threadIdx.x >> 4, sub = threadIdx.x & 15;  // 8 caps x 16 lanes
     for (int base = lo0; hi0 > lo0 && base <= hi0; base += 8) {
@@ -339,10 +409,10 @@ __device__ __forceinline__ void plan_split(const int* row_start, int num_rows, i
           int x = 0;
           if (npg > 0) {
             if (npg >= cap) {
-              x = n_kv * ((npg + cap - 1) / cap);
+              x = n_kv * udiv(npg + cap - 1, cap);
             } else {
-              const int m = cap / npg;
-              x = (n_kv + m - 1) / m;
+              const int m = udiv(cap, npg);
+              x = udiv(n_kv + m - 1, m);
             }
           }
           c = min(c + x, Cs + 1);
@@ -374,7 +444,14 @@ __device__ __forceinline__ void plan_split(const int* row_start, int num_rows, i
         const int r = base + lane;
         const int npg = r < num_rows ? row_start[r + 1] - row_start[r] : 0;
         int v = 0;
-        if (npg > 0) v = npg >= t ? n_kv * ((npg + t - 1) / t) : (n_kv + t / npg - 1) / (t / npg);
+        if (npg > 0) {
+          if (npg >= t) {
+            v = n_kv * udiv(npg + t - 1, t);
+          } else {
+            const int m = udiv(t, npg);
+            v = udiv(n_kv + m - 1, m);
+          }
+        }
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
           const int u = __shfl_up_sync(kFull, v, o);
@@ -406,8 +483,14 @@ __device__ __forceinline__ void chunk_range(const Split& sp, int k, const int* r
     return;
   }
   if (!sp.aligned) {
-    b = static_cast<long long>(k) * T / sp.used;
-    e = static_cast<long long>(k + 1) * T / sp.used;
+    if (T * (sp.used + 1) < (1ll << 31)) {  // 32-bit arithmetic when it cannot overflow
+      const int Ti = static_cast<int>(T);
+      b = k * Ti / sp.used;
+      e = (k + 1) * Ti / sp.used;
+    } else {
+      b = static_cast<long long>(k) * T / sp.used;
+      e = static_cast<long long>(k + 1) * T / sp.used;
+    }
     return;
   }
   int lo = 0, hi = num_rows;  // pc[lo] <= k < pc[hi]: the row is the largest such lo

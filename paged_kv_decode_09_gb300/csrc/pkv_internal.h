@@ -37,9 +37,15 @@ struct DecodeArgs {
   float* out;
   float* part_ml;   // [slots][G][2]
   float* part_acc;  // [slots][G][128]
-  int32_t* counters;  // non-null: [rows * n_kv] arrival counters, merge in-kernel
+  // Non-null: merge in-kernel, and the end of the workspace.  The merge's
+  // flags sit below it at places that do not depend on the call's rows or
+  // chunks (see flag_bytes): the arrival counter of segment j at flags[-1 - 2j]
+  // and the ready flag of partial slot s at flags[-2 - 2s] (single-query
+  // kernel); the counter of (segment j, column group w) at
+  // flags[-1 - (kMqCounters j + w)] (several-query kernels).
+  int32_t* flags;
   int32_t* status;  // optional device status word
-  unsigned long long wait_ns;  // limit of a wait on a tile copy (kv_pool_set_wait_limit)
+  unsigned long long test_stall_ns;  // test hook (kv_pool_set_test_stall); 0: off
 };
 
 struct CombineArgs {
@@ -85,14 +91,23 @@ struct AppendArgs {
   int32_t* status;
 };
 
-// Workspace layout (see paged_decode_workspace_bytes): arrival counters,
-// then the partial states.
+// Workspace layout (see paged_decode_workspace_bytes): the partial states
+// from the start (part_ml, then part_acc), and the merge's int32 flags down
+// from the end.  The flags of a segment or slot keep their place whatever
+// the call's shape, so a workspace sized for the largest call serves calls of
+// any smaller shape: no call's partial states land on another call's flags.
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // ints of a single-query CTA's plan in shared memory: row_start[rows + 1],
 // lens[rows] and the chunks before each row pc[rows + 1]
 inline size_t plan_ints(int rows) { return 3 * static_cast<size_t>(rows) + 2; }
-inline size_t counter_bytes(long long segments) {
-  return align256(static_cast<size_t>(segments) * sizeof(int32_t));
+// the single-query flags of a call with `slots` partial slots (segments <=
+// slots): a counter and a ready flag interleaved per index
+inline size_t flag_bytes(long long slots) {
+  return align256(static_cast<size_t>(slots) * 2 * sizeof(int32_t));
+}
+// the end of a workspace of `bytes` bytes, where the flags start (downwards)
+inline int32_t* flags_end(void* ws, size_t bytes) {
+  return reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + (bytes & ~size_t(255)));
 }
 inline size_t part_ml_bytes(long long slots, int group) {
   return align256(static_cast<size_t>(slots) * group * 2 * sizeof(float));
@@ -132,6 +147,9 @@ cudaError_t launch_paged_decode_mq(int dtype, int group, const DecodeArgs& a, co
 cudaError_t paged_decode_mq_blocks_per_sm(int dtype, int group, int q_len, int rows, int* blocks);
 constexpr int kMqCols = 32;  // partial-state columns of a several-query workspace slot
 constexpr int kMqCounters = 4;  // arrival counters per (row, KV head): one per warp's columns
+inline size_t mq_flag_bytes(long long segments) {
+  return align256(static_cast<size_t>(segments) * kMqCounters * sizeof(int32_t));
+}
 cudaError_t launch_combine(int group, const CombineArgs& a, cudaStream_t stream);
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
 cudaError_t launch_append(int dtype, const AppendArgs& a, cudaStream_t stream);

@@ -51,10 +51,10 @@ def test_pool_bytes(lib):
 def test_workspace_bytes(lib):
     chunks, rows, n_q, n_kv = 456, 8, 32, 8
     slots, G = chunks + rows * n_kv, n_q // n_kv
-    cnt = (rows * n_kv * 4 + 255) // 256 * 256
+    flags = (slots * 2 * 4 + 255) // 256 * 256  # a counter and a ready flag per slot index
     ml = (slots * G * 2 * 4 + 255) // 256 * 256
     acc = (slots * G * 128 * 4 + 255) // 256 * 256
-    assert lib.paged_decode_workspace_bytes(rows, n_q, n_kv, 128, chunks) == cnt + ml + acc
+    assert lib.paged_decode_workspace_bytes(rows, n_q, n_kv, 128, chunks) == ml + acc + flags
     assert lib.paged_decode_workspace_bytes(rows, 30, 8, 128, chunks) == 0   # 30 % 8 != 0
     assert lib.paged_decode_workspace_bytes(rows, 32, 8, 64, chunks) == 0    # head_dim 64
     assert lib.paged_decode_workspace_bytes(rows, n_q, n_kv, 128, (1 << 24) + 1) == 0  # chunks

@@ -245,4 +245,33 @@ def test_workspace_reuse_across_calls_and_shapes():
         sub = api.paged_decode_attention(pool, 0, q[:3].contiguous(), bt[:3].contiguous(),
                                          sl[:3].contiguous(), wl.scale, workspace=ws)
         _check(sub.cpu().numpy(), ref[:3])
-    assert int(ws.tensor[:wl.rows * wl.cfg.n_kv_heads * 4].view(torch.int32).abs().sum()) == 0
+    assert _flags_clear(ws, wl.rows)
+
+
+def _flags_clear(ws, max_rows, n_kv=8):
+    """The merge's flags (down from the end of the workspace) are all zero."""
+    slots = ws.num_chunks + max_rows * n_kv
+    up = (slots * 8 + 255) // 256 * 256
+    return int(ws.tensor[ws.nbytes - up:ws.nbytes].view(torch.int32).abs().sum()) == 0
+
+
+@pytest.mark.parametrize("chunks", [456, 97])
+def test_workspace_reuse_across_batch_sizes(chunks):
+    """A workspace sized for the largest batch serves batches of every size in
+    any order, as in continuous batching: rows come and go between steps.  A
+    small call's partial states must not be read as a later large call's
+    arrival counters or ready flags."""
+    wl = W.draw("skewed")
+    host = encode_pool(wl)
+    pool = device_pool(wl, host)
+    ws = api.Workspace(pool, wl.cfg.n_q_heads, wl.rows, chunks)
+    ref = oracle_decode(wl, host)
+    q, bt, sl = to_dev(wl.q), to_dev(wl.block_table), to_dev(wl.seq_lens)
+    for rows in (64, 4, 64, 17, 64, 1, 40, 64):
+        out = api.paged_decode_attention(pool, 0, q[:rows].contiguous(), bt[:rows].contiguous(),
+                                         sl[:rows].contiguous(), wl.scale, workspace=ws,
+                                         num_chunks=chunks)
+        torch.cuda.synchronize()
+        _check(out.cpu().numpy(), ref[:rows])
+    assert pool.read_status() == 0
+    assert _flags_clear(ws, wl.rows)

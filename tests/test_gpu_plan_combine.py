@@ -99,11 +99,11 @@ def test_combine_of_oracle_partials(lengths, chunks, kv_dtype):
     assert merged.sum() >= 5 or chunks == 200
     nbytes = api.workspace_bytes(wl.rows, cfg.n_q_heads, cfg.n_kv_heads, chunks)
     ws = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
-    # layout: counters [rows * n_kv] int32, part_ml, part_acc; each part 256-byte aligned
+    # layout: part_ml, part_acc (256-byte aligned), then the merge's flags down from the end
     up = lambda n: (n + 255) // 256 * 256  # noqa: E731
-    ml_at = up(wl.rows * cfg.n_kv_heads * 4)
+    ml_at = 0
     acc_at = ml_at + up(slots * G * 2 * 4)
-    assert acc_at + up(part_acc.nbytes) == nbytes
+    assert acc_at + up(part_acc.nbytes) + up(slots * 2 * 4) == nbytes
     ws[ml_at:ml_at + part_ml.nbytes] = torch.from_numpy(part_ml.view(np.uint8).reshape(-1)).cuda()
     ws[acc_at:acc_at + part_acc.nbytes] = torch.from_numpy(
         part_acc.view(np.uint8).reshape(-1)).cuda()
