@@ -202,6 +202,7 @@ KERNEL_SOURCES = {  # the files each decode kernel is compiled from (besides hea
     "paged_decode_kernel": ("decode.cu", "decode_common.cuh", "pkv_device.cuh"),
     "paged_decode_mq_kernel": ("decode_mq.cu", "decode_common.cuh", "pkv_device.cuh"),
     "paged_decode_mqt_kernel": ("decode_mq.cu", "decode_common.cuh", "pkv_device.cuh"),
+    "paged_decode_mqtc_kernel": ("decode_mqtc.cu", "decode_common.cuh", "pkv_device.cuh"),
 }
 
 
@@ -303,10 +304,13 @@ class StepSetup:
             if cfg.dtype == W.F32 or cols <= (4 if cfg.dtype == W.BF16 else 8):
                 width = min(cols, 8)
                 kname = "paged_decode_mq_kernel"  # the warps of a CTA read different pages
+            elif cfg.dtype == W.F16:  # blocks of 8 pages on the tensor cores, passes of 32
+                width = 32
+                kname = "paged_decode_mqtc_kernel"
             else:  # teams of 2 or 4 warps share every page
                 if cfg.dtype == W.BF16:
                     width = 8 if cols <= 8 else 16
-                else:  # f16: four warps of 4 or 8 columns; q8_0: two or four of 8
+                else:  # q8_0: two or four warps of 8 columns
                     width = 16 if cols <= 16 else 32
                 kname = "paged_decode_mqt_kernel"
             passes = -(-QL // max(1, width // cfg.group))

@@ -49,10 +49,11 @@ __host__ __device__ constexpr int mq_tiles() {
 }
 
 // The kernel a call takes, by its C = q_len * G columns:
-//   f16 : C <= 8 paged_decode_mq_kernel; C <= 16 four warps of 4 columns per
-//         page; beyond, four warps of 8 (passes of 32).  (Pairs of 8-column
-//         warps were measured slower than four warps of 4: fewer warps per
-//         page leave the page's latency chain exposed.)
+//   f16 : C <= 8 paged_decode_mq_kernel; beyond, the tensor-core kernel
+//         (decode_mqtc.cu, passes of 32 columns): 49.2 and 51.6 us for 16
+//         and 32 columns on the 8B f16 layer, where the warp-level team
+//         kernels below (four warps of 4 or 8 columns per page, which took
+//         this range before) measured 54.2 and 68.2 us.
 //   bf16: C <= 4 paged_decode_mq_kernel; C <= 8 two warps of 4 columns (four
 //         would leave two idle); beyond, four warps of 4 (passes of 16).
 //   q8_0: C <= 8 paged_decode_mq_kernel; C <= 16 two warps of 8 columns;
@@ -61,20 +62,20 @@ __host__ __device__ constexpr int mq_tiles() {
 //         better: two passes of 8 columns cost more than one page read by two
 //         warps, four warps of 4 columns more still.
 //   f32 : paged_decode_mq_kernel, passes of 8 columns (CUDA cores).
-enum MqKind { kMqSingle = 0, kMqPair1, kMqPair2, kMqTeam1, kMqTeam2 };
+enum MqKind { kMqSingle = 0, kMqPair1, kMqPair2, kMqTeam1, kMqTeam2, kMqTc };
 static int mq_kind(int dtype, int group, int q_len) {
   const int cols = q_len * group;
   if (dtype == PKV_KV_F32) return kMqSingle;
   if (dtype == PKV_KV_Q8_0) return cols <= 8 ? kMqSingle : cols <= 16 ? kMqPair2 : kMqTeam2;
   if (dtype == PKV_KV_BF16) return cols <= 4 ? kMqSingle : cols <= 8 ? kMqPair1 : kMqTeam1;
-  return cols <= 8 ? kMqSingle : cols <= 16 ? kMqTeam1 : kMqTeam2;
+  return cols <= 8 ? kMqSingle : kMqTc;
 }
 static int mq_kind_cols(int dtype, int kind) {
   switch (kind) {
     case kMqSingle: return dtype == PKV_KV_BF16 ? 4 : 8;
     case kMqPair1: return 8;
     case kMqPair2: case kMqTeam1: return 16;
-    default: return 32;
+    default: return 32;  // kMqTeam2, kMqTc
   }
 }
 // score n-tiles (4 columns each) of a warp, and warps per page, of a kind
@@ -1412,10 +1413,8 @@ static cudaError_t launch_mq_dt(int kind, const DecodeArgs& a, const TileMaps& m
     if (kind == kMqSingle) return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
     if (kind == kMqPair1) return launch_mq_t<DT, kMqPair1>(a, maps, chunks, st);
     return launch_mq_t<DT, kMqTeam1>(a, maps, chunks, st);
-  } else {
-    if (kind == kMqSingle) return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
-    if (kind == kMqTeam1) return launch_mq_t<DT, kMqTeam1>(a, maps, chunks, st);
-    return launch_mq_t<DT, kMqTeam2>(a, maps, chunks, st);
+  } else {  // f16: wider passes take the tensor-core kernel (launch_paged_decode_mq)
+    return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
   }
 }
 
@@ -1431,10 +1430,8 @@ static cudaError_t occupancy_mq_dt(int kind, int rows, int* blocks) {
     if (kind == kMqSingle) return mq_occupancy_t<DT, kMqSingle>(rows, blocks);
     if (kind == kMqPair1) return mq_occupancy_t<DT, kMqPair1>(rows, blocks);
     return mq_occupancy_t<DT, kMqTeam1>(rows, blocks);
-  } else {
-    if (kind == kMqSingle) return mq_occupancy_t<DT, kMqSingle>(rows, blocks);
-    if (kind == kMqTeam1) return mq_occupancy_t<DT, kMqTeam1>(rows, blocks);
-    return mq_occupancy_t<DT, kMqTeam2>(rows, blocks);
+  } else {  // f16
+    return mq_occupancy_t<DT, kMqSingle>(rows, blocks);
   }
 }
 
@@ -1442,6 +1439,7 @@ cudaError_t launch_paged_decode_mq(int dtype, int group, const DecodeArgs& a, co
                                    int chunks, cudaStream_t st) {
   if (group != 1 && group != 2 && group != 4) return cudaErrorInvalidValue;
   const int kind = mq_kind(dtype, group, a.q_len);
+  if (kind == kMqTc) return launch_paged_decode_mqtc(a, maps, chunks, st);
   if (dtype == PKV_KV_F16) return launch_mq_dt<PKV_KV_F16>(kind, a, maps, chunks, st);
   if (dtype == PKV_KV_BF16) return launch_mq_dt<PKV_KV_BF16>(kind, a, maps, chunks, st);
   if (dtype == PKV_KV_F32) return launch_mq_dt<PKV_KV_F32>(kind, a, maps, chunks, st);
@@ -1451,6 +1449,7 @@ cudaError_t launch_paged_decode_mq(int dtype, int group, const DecodeArgs& a, co
 cudaError_t paged_decode_mq_blocks_per_sm(int dtype, int group, int q_len, int rows,
                                           int* blocks) {
   const int kind = mq_kind(dtype, group, q_len);
+  if (kind == kMqTc) return paged_decode_mqtc_blocks_per_sm(rows, blocks);
   if (dtype == PKV_KV_F16) return occupancy_mq_dt<PKV_KV_F16>(kind, rows, blocks);
   if (dtype == PKV_KV_BF16) return occupancy_mq_dt<PKV_KV_BF16>(kind, rows, blocks);
   if (dtype == PKV_KV_F32) return occupancy_mq_dt<PKV_KV_F32>(kind, rows, blocks);

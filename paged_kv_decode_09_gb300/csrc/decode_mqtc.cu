@@ -1,0 +1,905 @@
+// decode_mqtc.cu — several queries per row on the fifth-generation tensor
+// cores (tcgen05, accumulators in tensor memory), f16 KV: the verification
+// step of speculative decoding and small chunks of chunked prefill (Leone,
+// "What ships": chunked prefill, exact speculative verification; LeatEngine,
+// "Capabilities": chunked prefill, speculative decoding).
+//
+// The operation is that of decode_mq.cu: query j of a row of L tokens whose
+// last q_len are new sits at P = L - q_len + j and attends causally to
+// [max(0, P + 1 - W), P + 1); the (query, query head) pairs of a KV head are
+// a pass's columns, here up to 32 of them.  What differs is how a page's
+// products run: a block of 8 pages of one (row, KV head) is one matrix
+// product per step, issued by one thread:
+//   scores  S[128 tokens][32] = K[128 tokens][128 dims] (Qhi + Qlo)^T: K
+//           straight from the staged tiles (A, K-major, 128-byte swizzle);
+//           Qhi^T, the f16 rounding of the 32 columns' queries (times scale *
+//           log2 e, normalised per column by a power of two), and Qlo^T, the
+//           f16 rounding of the remainder, are two operands in shared memory
+//           whose products accumulate into the same columns, so a score keeps
+//           about 22 significant bits (as in the other kernels);
+//   softmax one thread per (token, 16 columns), reading its row of S from
+//           tensor memory: base 2, masks per column (causal, window, length),
+//           the running maximum raised only when a block exceeds it by more
+//           than 8 (a vote of the softmax warps), P scaled by 2^7 and split
+//           into its leading 11 bits (Phi) and the f16 rounding of the rest
+//           (Plo), written as [Phi | Plo] [128 tokens][64] to shared memory,
+//           a token's 16 columns in two 16-byte stores per part;
+//   values  O^T[128 dims][64] += V^T [Phi | Plo]: V read in place from the
+//           staged tiles and [Phi | Plo] both as MN-major operands; the hi
+//           and lo halves of O^T, added at the end, stay in tensor memory for
+//           the whole piece.
+//
+// The warps have one job each, and the blocks flow through them as a
+// pipeline.  Warps 8 and 10 fetch block-table entries, store the new tokens
+// of the first pass (K, V) and queue the tensor copies of [16 tokens][64
+// dims] halves of K and of V into rings of two 32 KiB slots each (8 pages);
+// warp 9 issues the products, the scores of block b + 2 before the values of
+// block b; warps 0..7 run the softmax of block b while the copies of later
+// blocks land and the products of the neighbouring blocks run.  A K slot is
+// free again once its scores are computed, well before the block's values,
+// so K copies run about two blocks ahead of the softmax; V copies, needed
+// last, follow their own ring.  S is double-buffered in tensor memory, and
+// P and Q^T in shared memory.  Shared-memory barriers carry every
+// hand-over:
+//   kfull[s], vfull[s]  copies of K or V slot s landed (transaction bytes)
+//   kempty[s]  the scores of K slot s computed  (product commit)
+//   vempty[s]  the values of V slot s computed  (product commit)
+//   sfull[x]  scores in S buffer x             (product commit)
+//   sfree[x]  S buffer x read                  (softmax warps, 8 arrivals)
+//   pready[x] P buffer x written               (softmax warps, 8 arrivals)
+//   pvdone[x] the values product from P x done (product commit)
+//   qready[x] Q^T buffer x written             (softmax warps, 8 arrivals)
+// Every wait is bounded; the warp that gives up sets the CTA's abort flag,
+// which ends every other wait, and the CTA drains its copies and products
+// before it releases the tensor memory.  One CTA per SM; the work split, the
+// partial states and the merge of split segments are those of the other
+// several-query kernels (workspace slots of 32 columns).
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+
+#include "decode_common.cuh"
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kSwWarps = 8;                          // softmax warps 0..7
+constexpr int kSwThreads = kSwWarps * 32;            // 256
+constexpr int kKWarp = 8, kMmaWarp = 9, kVWarp = 10;  // warp 11 only fills the warpgroup
+constexpr int kTcThreads = 384;
+constexpr int kSwBar = 1;                            // named barrier of the softmax warps
+constexpr int kBlockPages = 8;                       // pages of a block: the products' M = 128 tokens
+constexpr int kTcStages = 2;                         // slots of the K ring and of the V ring
+constexpr uint32_t kHalfBytes = kBlockPages * 2048;  // one 64-dim half of K or V for 8 pages
+constexpr uint32_t kSlotBytes = 2 * kHalfBytes;      // a ring slot: both halves, 32 KiB
+constexpr uint32_t kTmemCols = 128;                  // S0: 0..31, S1: 32..63, O^T: 64..127
+constexpr uint32_t kTmemO = 64;
+constexpr float kPUp = 128.0f;                       // P is stored times 2^7 (as kPShift)
+constexpr float kNoMax = -1e30f;                     // a column's m before its first score
+
+// Shared memory, from a 1024-byte aligned base.
+struct TcSmem {
+  static constexpr uint32_t kAlign = 1024;
+  static constexpr uint32_t kV = kTcStages * kSlotBytes;      // K ring from 0, then the V ring
+  static constexpr uint32_t kQ = 2 * kTcStages * kSlotBytes;  // Q^T x2: [2 halves][64 rows][128 B]
+  static constexpr uint32_t kP = kQ + 2 * 16384;           // P x2: [128 tokens][64 columns]
+  static constexpr uint32_t kRed = kP + 2 * 16384;         // float [2][4][32] block maxima, [4][32] sums
+  static constexpr uint32_t kQexp = kRed + 3 * 4 * 32 * 4; // float [2][32]: 2^e of each column's q
+  static constexpr uint32_t kBar = kQexp + 2 * 32 * 4;     // 19 barriers, 8 bytes each
+  static constexpr uint32_t kCtl = kBar + 20 * 8;          // int [4]: [0] abort, [1] last arrival
+  static constexpr uint32_t kTmem = kCtl + 16;             // uint32: tensor-memory base
+  static constexpr uint32_t kSplit = kTmem + 16;
+  static constexpr uint32_t kRows = kSplit + 16;
+  static size_t bytes(int rows) { return kAlign + kRows + plan_ints(rows) * 4; }
+};
+// barrier indices
+constexpr int kBKfull = 0, kBKempty = 2, kBVfull = 4, kBVempty = 6, kBSfull = 8, kBSfree = 10,
+              kBPready = 12, kBPvdone = 14, kBQready = 16, kBStall = 18, kNumBars = 19;
+
+// --------------------------------------------------------- tcgen05 PTX ----
+// Shared-memory matrix descriptor: 128-byte swizzle, start address and the
+// two byte offsets in units of 16 bytes.  K-major operands (rows of 64
+// elements, 8 rows per 1024-byte atom): sbo = 1024, lbo unused.  The MN-major
+// V^T operand: lbo = bytes between the 64-element halves of M, sbo = bytes
+// between groups of 8 rows along K.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor of kind::f16 with f32 accumulation, f16 A and B.
+__host__ __device__ constexpr uint32_t tc_idesc(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | (a_mn_major ? (1u << 15) : 0u) | (b_mn_major ? (1u << 16) : 0u) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       int accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` once every product this thread has issued is complete.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// 16 consecutive 32-bit columns of the warp's 32 lanes (lane = thread).
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int u = 0; u < 16; ++u) v[u] = __uint_as_float(r[u]);
+}
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+// 2^x by the hardware approximation (about 22 correct bits; 2^-inf = 0,
+// results below 2^-126 flushed to 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Named barrier of `count` threads that also ORs `pred` over them.
+__device__ __forceinline__ bool barrier_or(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
+// A wait of one lane of the warp, its outcome given to every lane
+// (warp-uniform: the tensor-memory loads that follow are warp-collective).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
+                                          int lane) {
+  int ok = 1;
+  if (lane == 0) ok = mbar_wait_bounded(bar, parity, abort) ? 1 : 0;
+  return __shfl_sync(kFull, ok, 0) != 0;
+}
+
+// A block: the units [x, x + n) of one (row, KV head) segment, n <= 8.
+struct Blk {
+  int i, h, n, L, pfirst;  // row, KV head, pages, row length, first page's index in the row
+  long long x, seg_end;
+};
+
+}  // namespace
+
+template <int DT>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    paged_decode_mqtc_kernel(const __grid_constant__ DecodeArgs a,
+                             const __grid_constant__ TileMaps maps) {
+  static_assert(DT == PKV_KV_F16, "the tensor-core several-query kernel takes f16 KV");
+  using SM = TcSmem;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((SM::kAlign - (smem_addr(smem_raw) & (SM::kAlign - 1))) &
+                              (SM::kAlign - 1));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  volatile int* ctl = reinterpret_cast<volatile int*>(smem + SM::kCtl);
+  int* row_start = reinterpret_cast<int*>(smem + SM::kRows);
+  int* lens = row_start + a.num_rows + 1;
+  int* pc = lens + a.num_rows;
+  const uint32_t bars = smem_addr(smem + SM::kBar);
+  auto bar = [&](int b, int x) { return bars + 8u * static_cast<uint32_t>(b + x); };
+  const uint32_t sQ = smem_addr(smem + SM::kQ), sP = smem_addr(smem + SM::kP);
+  const int G = a.n_q / a.n_kv;
+  const int nc = a.nq * G;  // columns of this pass, <= 32
+  const int plan_window = a.window > 0 ? a.window + a.q_len - 1 : 0;
+
+  if (tid == 0) {
+    prefetch_tensormap(&maps.kh);  // kernel parameters, not written by an earlier kernel
+    prefetch_tensormap(&maps.vh);
+    ctl[0] = 0;
+    ctl[1] = 0;
+    for (int b = 0; b < kNumBars; ++b) {
+      const bool sw = b >= kBSfree && b < kBSfree + 2;
+      const bool sw2 = b >= kBPready && b < kBPready + 2;
+      const bool sw3 = b >= kBQready && b < kBQready + 2;
+      mbar_init(bars + 8u * b, (sw || sw2 || sw3) ? kSwWarps : 1);
+    }
+    fence_mbar_init();
+  }
+  // Q^T and P start zeroed: Q^T rows of columns beyond nc stay zero
+  for (int e = tid; e < 65536 / 16; e += kTcThreads)
+    reinterpret_cast<uint4*>(smem + SM::kQ)[e] = make_uint4(0u, 0u, 0u, 0u);
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(smem + SM::kTmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    tc_fence_before();
+  }
+  grid_dependency_wait();
+  grid_launch_dependents();
+  plan_rows(a.seq_lens, a.num_rows, a.bt_stride, plan_window, blockIdx.x == 0 ? a.status : nullptr,
+            lens, row_start, a.q_len);  // ends with __syncthreads
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM::kTmem);
+  const bool stalled = test_stall(bar(kBStall, 0), a.test_stall_ns, ctl, a.status);
+  plan_split(row_start, a.num_rows, a.n_kv, a.vchunks, a.aligned_split,
+             reinterpret_cast<Split*>(smem + SM::kSplit), pc);
+  const Split* sp = reinterpret_cast<const Split*>(smem + SM::kSplit);
+  const int k = blockIdx.x;
+  long long c_begin, c_end;
+  chunk_range(*sp, k, row_start, pc, a.num_rows, a.n_kv, c_begin, c_end);
+
+  if (blockIdx.x == 0) {  // rows without tokens (or shorter than q_len): zeros
+    for (int i = 0; i < a.num_rows; ++i)
+      if (row_start[i + 1] == row_start[i])
+        for (int jj = 0; jj < a.nq; ++jj)
+          for (int e = tid; e < a.n_q * kD; e += kTcThreads)
+            a.out[((static_cast<long long>(i) * a.q_len + a.q0 + jj) * a.n_q) * kD + e] = 0.f;
+  }
+
+  // The block starting at unit x (x < c_end): up to 8 units of x's segment.
+  auto block_at = [&](long long x, Blk& bk) {
+    const int i = row_of(row_start, a.num_rows, a.n_kv, x);
+    const int npg = row_start[i + 1] - row_start[i];
+    const long long row_base = static_cast<long long>(a.n_kv) * row_start[i];
+    bk.i = i;
+    bk.h = static_cast<int>(x - row_base) / npg;
+    const long long seg_start = row_base + static_cast<long long>(bk.h) * npg;
+    bk.seg_end = seg_start + npg;
+    const long long e = min(min(bk.seg_end, c_end), x + kBlockPages);
+    bk.n = static_cast<int>(e - x);
+    bk.x = x;
+    bk.L = lens[i];
+    bk.pfirst = window_start(bk.L, plan_window) / kPage + static_cast<int>(x - seg_start);
+  };
+
+  const int zero = 0;
+  if (warp == kKWarp || warp == kVWarp) {
+    // ------------------------------------------------------------ copies ----
+    // K (warp 8) or V (warp 10): slot b % 2 of the ring for block b, once the
+    // product that read the slot's previous block is done.
+    const bool is_v = warp == kVWarp;
+    const CUtensorMap* map = is_v ? &maps.vh : &maps.kh;
+    const uint32_t ring = smem_addr(smem) + (is_v ? SM::kV : 0u);
+    const int bfull = is_v ? kBVfull : kBKfull, bempty = is_v ? kBVempty : kBKempty;
+    const float* src_new = is_v ? a.v_new : a.k_new;
+    uint8_t* data = is_v ? a.v_data : a.k_data;
+    const uint64_t policy = policy_evict_first();
+    int b = 0;
+    bool failed = stalled;
+    for (long long x = c_begin; x < c_end && !failed; ++b) {
+      Blk bk;
+      block_at(x, bk);
+      const int st = b % kTcStages;
+      int pg = 0;
+      bool ok_pg = false;
+      if (lane < bk.n) {  // the entry is read before the wait for the slot
+        pg = __ldg(a.block_table + static_cast<long long>(bk.i) * a.bt_stride + bk.pfirst + lane);
+        ok_pg = pg >= 0 && pg < a.num_pages;
+      }
+      if (b >= kTcStages && !warp_wait(bar(bempty, st), ((b / kTcStages) - 1) & 1, ctl, lane)) {
+        failed = true;
+        break;
+      }
+      if (lane < bk.n && !ok_pg) {
+        if (!is_v) record_status(a.status, PKV_DEV_BAD_PAGE);
+        pg = 0;
+      }
+      if (src_new != nullptr) {  // the new tokens of the block's pages, before their copies
+        const int first_new = bk.L - a.q_len;
+        const int lo = max(first_new, bk.pfirst * kPage);
+        const int hi = min(bk.L, (bk.pfirst + bk.n) * kPage);
+        for (int pos = lo; pos < hi; ++pos) {
+          const int q = pos / kPage - bk.pfirst;
+          const int pgq = __shfl_sync(kFull, pg, q);
+          if (__shfl_sync(kFull, ok_pg ? 1 : 0, q)) {
+            // the kv_append encoding of one f16 token: 4 dims per lane
+            const long long src_row = static_cast<long long>(bk.i) * a.q_len + (pos - first_new);
+            const float4 v4 = __ldg(reinterpret_cast<const float4*>(
+                src_new + (src_row * a.n_kv + bk.h) * kD + lane * 4));
+            const __half2 h01 = __floats2half2_rn(v4.x, v4.y), h23 = __floats2half2_rn(v4.z, v4.w);
+            uint2 w;
+            w.x = *reinterpret_cast<const uint32_t*>(&h01);
+            w.y = *reinterpret_cast<const uint32_t*>(&h23);
+            const size_t tile = static_cast<size_t>(pgq) * a.n_kv + bk.h;
+            *reinterpret_cast<uint2*>(data + tile * (kPage * kD * 2) + (pos % kPage) * (kD * 2) +
+                                      lane * 8) = w;
+          }
+        }
+        // the tiles are read next by the async proxy (tensor copies)
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __syncwarp();
+      }
+      const uint32_t dst0 = ring + st * kSlotBytes;
+      if (lane == 0) mbar_arrive_expect_tx(bar(bfull, st), static_cast<uint32_t>(bk.n) * 2u * 2048u);
+      __syncwarp();
+      if (lane < bk.n) {
+        const int z = pg * a.n_kv + bk.h;
+        tma_load_3d(dst0 + lane * 2048, map, 0, 0, z, bar(bfull, st), policy);
+        tma_load_3d(dst0 + kHalfBytes + lane * 2048, map, 64, 0, z, bar(bfull, st), policy);
+      }
+      x += bk.n;
+    }
+    // drain: the copies of the last slots land before the CTA exits
+    for (int bb = max(0, b - kTcStages); bb < b; ++bb)
+      if (lane == 0) mbar_wait_bounded(bar(bfull, bb % kTcStages), (bb / kTcStages) & 1, &zero);
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------- products ----
+    if (lane == 0) {
+      const uint32_t id_s = tc_idesc(128, 32, false, false), id_pv = tc_idesc(128, 64, true, true);
+      int b = 0, p = 0;
+      // the values products still to issue, oldest first: up to two blocks
+      // (the scores run two blocks ahead of the values)
+      int pv_cnt = 0, pv_b[2] = {0, 0}, pv_n[2] = {0, 0};
+      bool pv_first[2] = {false, false};
+      int last_bar = -1;        // barrier of the last commit, and its parity
+      uint32_t last_par = 0;
+      bool failed = stalled;
+      auto fail = [&]() {
+        if (!failed && !ctl[0]) {
+          ctl[0] = 1;
+          record_status(a.status, PKV_DEV_TIMEOUT);
+        }
+        failed = true;
+      };
+      auto issue_pv = [&]() {  // the oldest pending values product
+        const int vb = pv_b[0], vn = pv_n[0];
+        const bool vfirst = pv_first[0];
+        pv_b[0] = pv_b[1];
+        pv_n[0] = pv_n[1];
+        pv_first[0] = pv_first[1];
+        --pv_cnt;
+        if (!mbar_wait_bounded(bar(kBPready, vb & 1), (vb >> 1) & 1, ctl) ||
+            !mbar_wait_bounded(bar(kBVfull, vb % kTcStages), (vb / kTcStages) & 1, ctl)) {
+          fail();
+          return;
+        }
+        tc_fence_after();
+        const uint32_t vbase = smem_addr(smem) + SM::kV + (vb % kTcStages) * kSlotBytes;
+        const uint32_t pbase = sP + (vb & 1) * 16384;
+        for (int kk = 0; kk < vn; ++kk) {  // 16 tokens a step: P rows 16 kk .., N-major
+          const uint64_t ad = sw128_desc(vbase + kk * 2048, kHalfBytes, 1024);
+          const uint64_t bd = sw128_desc(pbase + kk * 2048, 16384, 1024);
+          tc_mma(tmem + kTmemO, ad, bd, id_pv, (!vfirst || kk > 0) ? 1 : 0);
+        }
+        tc_commit(bar(kBVempty, vb % kTcStages));
+        tc_commit(bar(kBPvdone, vb & 1));
+        last_bar = kBPvdone + (vb & 1);
+        last_par = (vb >> 1) & 1;
+      };
+      for (long long x = c_begin; x < c_end && !failed; ++p) {
+        Blk pb;
+        block_at(x, pb);
+        const long long b_piece = min(pb.seg_end, c_end);
+        if (!mbar_wait_bounded(bar(kBQready, p & 1), (p >> 1) & 1, ctl)) {
+          fail();
+          break;
+        }
+        const uint32_t qbase = sQ + (p & 1) * 16384;
+        bool first = true;
+        for (long long xb = x; xb < b_piece; ++b) {
+          const int n = static_cast<int>(min(b_piece - xb, static_cast<long long>(kBlockPages)));
+          const int st = b % kTcStages;
+          if (!mbar_wait_bounded(bar(kBKfull, st), (b / kTcStages) & 1, ctl) ||
+              (b >= 2 && !mbar_wait_bounded(bar(kBSfree, b & 1), ((b - 2) >> 1) & 1, ctl))) {
+            fail();
+            break;
+          }
+          tc_fence_after();
+          const uint32_t kbase = smem_addr(smem) + st * kSlotBytes;
+          const uint32_t tS = tmem + (b & 1) * 32;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {  // 16 dims a step: half kk / 4, 32 bytes in
+            const uint64_t ad = sw128_desc(kbase + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+            const uint32_t qb = qbase + (kk >> 2) * 8192 + (kk & 3) * 32;
+            tc_mma(tS, ad, sw128_desc(qb, 16, 1024), id_s, kk > 0);       // Qhi^T rows 0..31
+            tc_mma(tS, ad, sw128_desc(qb + 4096, 16, 1024), id_s, 1);    // Qlo^T rows 32..63
+          }
+          tc_commit(bar(kBKempty, st));
+          tc_commit(bar(kBSfull, b & 1));
+          last_bar = kBSfull + (b & 1);
+          last_par = (b >> 1) & 1;
+          if (pv_cnt == 2) {
+            issue_pv();
+            if (failed) break;
+          }
+          if (pv_cnt == 0) {
+            pv_b[0] = b;
+            pv_n[0] = n;
+            pv_first[0] = first;
+          } else {
+            pv_b[1] = b;
+            pv_n[1] = n;
+            pv_first[1] = first;
+          }
+          ++pv_cnt;
+          first = false;
+          xb += n;
+        }
+        x = b_piece;
+      }
+      while (!failed && pv_cnt > 0) issue_pv();
+      // drain: every product issued completes before the tensor memory goes
+      if (last_bar >= 0) mbar_wait_bounded(bars + 8u * last_bar, last_par, &zero);
+    }
+    __syncwarp();
+  } else if (warp == kVWarp + 1) {
+    // fills the warpgroup; nothing to do
+  } else {
+    // ----------------------------------------------------------- softmax ----
+    const int qw = warp & 3, hc = warp >> 2;  // tensor-memory lane quarter, column half
+    const int t = 32 * qw + lane;             // this thread's token row of a block (and dim of O)
+    const uint32_t lane_off = static_cast<uint32_t>(32 * qw) << 16;
+    float* red = reinterpret_cast<float*>(smem + SM::kRed);
+    float* qexp_s = reinterpret_cast<float*>(smem + SM::kQexp);
+    bool failed = stalled;
+    auto fail = [&]() {
+      if (!failed && !ctl[0]) {
+        ctl[0] = 1;
+        record_status(a.status, PKV_DEV_TIMEOUT);
+      }
+      failed = true;
+    };
+    // Q^T of the piece at unit x into buffer qb: thread tid takes column
+    // tid / 8, dims 16 (tid % 8) ..
+    auto write_q = [&](long long x, int qb) {
+      Blk pb;
+      block_at(x, pb);
+      const int c = tid >> 3, d0 = (tid & 7) * 16;
+      float v[16];
+      const bool in = c < nc;
+      const float* qv = in ? a.q + ((static_cast<long long>(pb.i) * a.q_len + a.q0 + c / G) * a.n_q +
+                                    pb.h * G + c % G) * kD + d0
+                           : nullptr;
+      float amax = 0.f;
+#pragma unroll
+      for (int e = 0; e < 16; e += 4) {
+        float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (in) x4 = __ldg(reinterpret_cast<const float4*>(qv + e));
+        v[e] = x4.x * a.qscale;
+        v[e + 1] = x4.y * a.qscale;
+        v[e + 2] = x4.z * a.qscale;
+        v[e + 3] = x4.w * a.qscale;
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) amax = fmaxf(amax, fabsf(v[e]));
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 1));  // the column's 8 threads
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
+      amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
+      int e2 = 0;
+      if (amax > 0.f && amax <= 3.0e38f) {
+        int ex;
+        frexpf(amax, &ex);
+        e2 = ex - 14;  // largest |q| in [2^13, 2^14): both f16 parts normal
+      }
+      if (in) {
+        // rows c (hi) and 32 + c (lo); dims d0 .. d0 + 15 = two 16-byte chunks
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+          const int row = part * 32 + c;
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              w[e] = split_f16x2(ldexpf(v[8 * ch + 2 * e], -e2), ldexpf(v[8 * ch + 2 * e + 1], -e2),
+                                 part == 1);
+            const int d = d0 + 8 * ch;
+            const uint32_t off = qb * 16384 + (d >> 6) * 8192 + row * 128 +
+                                 ((((d & 63) >> 3) ^ (row & 7)) << 4);
+            *reinterpret_cast<uint4*>(smem + SM::kQ + off) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        if ((tid & 7) == 0) qexp_s[qb * 32 + c] = ldexpf(1.0f, e2);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q^T for the tensor cores
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBQready, qb));
+    };
+    // the query of the thread's column 16 hc + u: qbase + 4 bits u of qoff
+    const int qbase = (16 * hc) / G;
+    uint64_t qoff = 0;
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      qoff |= static_cast<uint64_t>((16 * hc + u) / G - qbase) << (4 * u);
+
+    int b = 0, p = 0, rb = 0;
+    if (tid < 64) qexp_s[tid] = 0.f;  // columns beyond nc keep 0
+    named_barrier(kSwBar, kSwThreads);
+    // Q^T of piece p + 2 goes into the buffer of piece p once the scores of
+    // p's last block are read (all of p's score products are then done): the
+    // product thread, two blocks ahead, may need it before this piece ends.
+    // Pieces 0 and 1 are written here.
+    auto piece_end = [&](long long x) {  // end of the piece starting at unit x
+      Blk pb;
+      block_at(x, pb);
+      return min(pb.seg_end, c_end);
+    };
+    if (c_begin < c_end && !failed) {
+      write_q(c_begin, 0);
+      const long long e0 = piece_end(c_begin);
+      if (e0 < c_end) write_q(e0, 1);
+    }
+    named_barrier(kSwBar, kSwThreads);  // qexp of pieces 0 and 1
+    for (long long x = c_begin; x < c_end; ++p) {
+      Blk pb;
+      block_at(x, pb);
+      const long long b_piece = min(pb.seg_end, c_end);
+      const long long next2 = b_piece < c_end ? piece_end(b_piece) : c_end;  // start of piece p + 2
+      const int i = pb.i, h = pb.h, L = pb.L;
+      const long long j = static_cast<long long>(i) * a.n_kv + h;
+      int k0, k1;
+      segment_chunks(*sp, i, h, row_start, pc, a.num_rows, a.n_kv, k0, k1);
+      const int P0 = L - a.q_len + a.q0;  // position of the pass's first query
+      // tokens every used column attends: [all_lo, P0]
+      const int all_lo = window_start(P0 + (nc - 1) / G + 1, a.window);
+      const float4* qexp4 = reinterpret_cast<const float4*>(qexp_s + (p & 1) * 32 + 16 * hc);
+      // per column: m = the running maximum minus 7 (so that 2^(s - m) is P
+      // times 2^7), l = the sum of the thread's 2^(s - m).  Before a column's
+      // first score m is -1e30, a finite stand-in for -inf: s - m is then -inf
+      // for a masked score and above the raise threshold for any other.
+      float m[16], l[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        m[u] = kNoMax;
+        l[u] = 0.f;
+      }
+      bool first = true;
+      long long xb = x;
+      for (; xb < b_piece; ++b) {
+        const int n = static_cast<int>(min(b_piece - xb, static_cast<long long>(kBlockPages)));
+        const int pfirst = pb.pfirst + static_cast<int>(xb - x);
+        // ---- scores of block b from S buffer b & 1: d = s - m, masked to -inf
+        const int t0 = pfirst * kPage;
+        const bool fast = t0 >= all_lo && t0 + n * kPage <= P0 + 1;  // every token, every column
+        const bool in_blk = t < n * kPage;  // rows of pages past n: stale stage data
+        const int pos = t0 + t;
+        // score of column u, from S and the column's scale (masked to -inf)
+        auto score = [&](int u, float sv, float qe) {
+          bool ok = in_blk;
+          if (!fast) {
+            const int P = P0 + qbase + static_cast<int>((qoff >> (4 * u)) & 15);
+            ok = ok && pos < L && 16 * hc + u < nc && pos <= P && pos >= window_start(P + 1, a.window);
+          }
+          return ok ? sv * qe : -INFINITY;
+        };
+        float d[16];
+        if (!failed && !warp_wait(bar(kBSfull, b & 1), (b >> 1) & 1, ctl, lane)) fail();
+        const uint32_t tS = tmem + lane_off + (b & 1) * 32 + 16 * hc;
+        bool up = false;
+        if (!failed) {
+          tc_fence_after();
+          float sv[16];
+          tc_ld16(tS, sv);
+          tc_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 q4 = qexp4[e];
+            const float qe[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int u = 4 * e + k;
+              const float sc = score(u, sv[u], qe[k]);
+              d[u] = sc - m[u];  // -inf when masked (m is finite)
+              up = up || d[u] > 15.0f;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 16; ++u) d[u] = -INFINITY;
+        }
+        // ---- the running maximum: raised (by a vote of the softmax warps)
+        // only when the block exceeds it by more than 8
+        if (barrier_or(kSwBar, kSwThreads, up || failed)) {
+          if (barrier_or(kSwBar, kSwThreads, failed)) {
+            failed = true;
+            break;
+          }
+          // the scores again (S buffer b is not released yet)
+          float sc[16];
+          {
+            float sv[16];
+            tc_ld16(tS, sv);
+            tc_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float4 q4 = qexp4[e];
+              const float qe[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) sc[4 * e + k] = score(4 * e + k, sv[4 * e + k], qe[k]);
+            }
+          }
+          float* rr = red + rb * 128;
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            float v = sc[u];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+            if (lane == 0) rr[qw * 32 + 16 * hc + u] = v;
+          }
+          named_barrier(kSwBar, kSwThreads);
+          rb ^= 1;  // the next raise writes the other buffer (a vote lies between)
+          float my_al = 1.0f;  // lane u % 16 keeps alpha of column 16 hc + u % 16
+          bool any_scale = false;
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            const int c = 16 * hc + u;
+            const float b4 = fmaxf(fmaxf(rr[c], rr[32 + c]), fmaxf(rr[64 + c], rr[96 + c]));
+            const float mn = b4 > m[u] + 15.0f ? b4 - 7.0f : m[u];
+            const float al = mn == m[u] ? 1.0f : exp2f(m[u] - mn);  // 0 from the stand-in
+            if ((lane & 15) == u) my_al = al;
+            any_scale = any_scale || al != 1.0f;
+            l[u] *= al;
+            m[u] = mn;
+            d[u] = sc[u] == -INFINITY ? -INFINITY : sc[u] - mn;
+          }
+          // O^T columns of the warp's 16 columns (hi and lo parts), times
+          // alpha, once the values product of block b - 1 is done (not in a
+          // piece's first block: its values product overwrites O^T)
+          if (!first && any_scale) {
+            if (!warp_wait(bar(kBPvdone, (b - 1) & 1), ((b - 1) >> 1) & 1, ctl, lane)) {
+              fail();
+            } else {
+              tc_fence_after();
+#pragma unroll
+              for (int part = 0; part < 2; ++part) {
+                const uint32_t tO = tmem + lane_off + kTmemO + 32 * part + 16 * hc;
+                float ov[16];
+                tc_ld16(tO, ov);
+                tc_wait_ld();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) ov[u] *= __shfl_sync(kFull, my_al, u);
+                tc_st16(tO, ov);
+                tc_wait_st();
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0 && !failed) mbar_arrive(bar(kBSfree, b & 1));
+        if (xb + n >= b_piece && next2 < c_end && !failed) write_q(next2, p & 1);
+        // ---- probabilities into P buffer b & 1 once the values product of
+        // block b - 2 has read it: row t (token) of [128 tokens][64], columns
+        // 0..31 Phi (pu's leading 11 bits, exact in f16 from 2^-14 up), 32..63
+        // Plo (the f16 rounding of the rest), 128-byte swizzle
+        if (!failed && b >= 2 && !warp_wait(bar(kBPvdone, b & 1), ((b - 2) >> 1) & 1, ctl, lane))
+          fail();
+        if (!failed) {
+          uint8_t* prow = smem + SM::kP + (b & 1) * 16384 + t * 128;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {  // columns 16 hc + 8 e .. + 7
+            uint32_t wh[4], wl[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int u = 8 * e + 2 * k;
+              const float p0 = ex2_approx(d[u]), p1 = ex2_approx(d[u + 1]);  // P times 2^7
+              l[u] += p0;
+              l[u + 1] += p1;
+              const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFFFE000u);
+              const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFFFE000u);
+              const __half2 hh = __floats2half2_rn(h0, h1), ll = __floats2half2_rn(p0 - h0, p1 - h1);
+              wh[k] = *reinterpret_cast<const uint32_t*>(&hh);
+              wl[k] = *reinterpret_cast<const uint32_t*>(&ll);
+            }
+            const int ch = 2 * hc + e;  // 16-byte chunk of the hi columns; lo: ch + 4
+            *reinterpret_cast<uint4*>(prow + ((ch ^ (t & 7)) << 4)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+            *reinterpret_cast<uint4*>(prow + (((ch + 4) ^ (t & 7)) << 4)) =
+                make_uint4(wl[0], wl[1], wl[2], wl[3]);
+          }
+          // V rows of slots past the row's length in a page the block reads:
+          // the pool may hold anything there (NaN * 0 is NaN).  Zeroed once
+          // the block's V copies have landed.
+          const int q = t / kPage, slot = t % kPage;
+          const bool zero_v = hc == 0 && q < n && pos >= L;
+          if (__any_sync(kFull, zero_v)) {
+            if (!warp_wait(bar(kBVfull, b % kTcStages), (b / kTcStages) & 1, ctl, lane)) {
+              fail();
+            } else if (zero_v) {
+#pragma unroll
+              for (int hv = 0; hv < 2; ++hv) {
+                uint4* row = reinterpret_cast<uint4*>(smem + SM::kV + (b % kTcStages) * kSlotBytes +
+                                                      hv * kHalfBytes + q * 2048 + slot * 128);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) row[e] = make_uint4(0u, 0u, 0u, 0u);
+              }
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // P, zeroed V rows
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBPready, b & 1));
+        }
+        first = false;
+        xb += n;
+      }
+      // ---- piece end: the values product of the piece's last block done
+      if (!failed && !warp_wait(bar(kBPvdone, (b - 1) & 1), ((b - 1) >> 1) & 1, ctl, lane)) fail();
+      if (barrier_or(kSwBar, kSwThreads, failed)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      float o[16];  // O^T (hi + lo columns) and the sums carry P's factor 2^7: removed here
+      {
+        float olo[16];
+        tc_ld16(tmem + lane_off + kTmemO + 16 * hc, o);
+        tc_ld16(tmem + lane_off + kTmemO + 32 + 16 * hc, olo);
+        tc_wait_ld();
+#pragma unroll
+        for (int u = 0; u < 16; ++u) o[u] = (o[u] + olo[u]) * (1.0f / kPUp);
+      }
+      tc_fence_before();  // O^T read before the next piece's first values product
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        float v = l[u];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
+        l[u] = v;
+      }
+      float* rs = red + 256;
+      if (lane == 0)
+#pragma unroll
+        for (int u = 0; u < 16; ++u) rs[qw * 32 + 16 * hc + u] = l[u];
+      named_barrier(kSwBar, kSwThreads);
+      float Ls[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int c = 16 * hc + u;
+        Ls[u] = ((rs[c] + rs[32 + c]) + (rs[64 + c] + rs[96 + c])) * (1.0f / kPUp);
+      }
+      const bool whole = (k0 == k1);
+      auto out_col = [&](int c) {
+        return a.out + ((static_cast<long long>(i) * a.q_len + a.q0 + c / G) * a.n_q + h * G +
+                        c % G) * kD;
+      };
+      const int d = t;  // O^T lane = dim
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int c = 16 * hc + u;
+        if (c >= nc) continue;
+        if (whole) {
+          out_col(c)[d] = o[u] / Ls[u];
+        } else {
+          const long long slot = (k + j) * kMqCols + c;
+          a.part_acc[slot * kD + d] = o[u];
+          if (qw == 0 && lane == 0) {
+            // the running maximum (-inf: no token of the column in the piece)
+            a.part_ml[slot * 2] = Ls[u] > 0.f ? m[u] + static_cast<float>(kPShift) : -INFINITY;
+            a.part_ml[slot * 2 + 1] = Ls[u];
+          }
+        }
+      }
+      if (!whole && a.flags != nullptr) {
+        named_barrier(kSwBar, kSwThreads);  // the CTA's partial, ordered before thread 0's release
+        if (tid == 0) ctl[1] = atomic_add_acq_rel(mq_counter(a.flags, j, 0), 1) == k1 - k0;
+        named_barrier(kSwBar, kSwThreads);
+        if (ctl[1]) {  // the last piece of the segment: merge all its pieces (thread 0's acquire)
+          const int c = tid >> 3, dd = (tid & 7) * 16;
+          if (c < nc) {
+            float Mx = -INFINITY, Lx = 0.f, Ax[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) Ax[e] = 0.f;
+            for (int kk = k0; kk <= k1; ++kk) {
+              const long long slot = (kk + j) * kMqCols + c;
+              const float mk = __ldcg(a.part_ml + slot * 2), lk = __ldcg(a.part_ml + slot * 2 + 1);
+              const float4* src = reinterpret_cast<const float4*>(a.part_acc + slot * kD + dd);
+              float4 xs[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) xs[e] = __ldcg(src + e);
+              if (mk == -INFINITY) continue;  // no token of this query in the piece
+              const float mn = fmaxf(Mx, mk);
+              const float f0 = exp2f(Mx - mn), f1 = exp2f(mk - mn);
+              Lx = Lx * f0 + lk * f1;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                Ax[4 * e] = Ax[4 * e] * f0 + xs[e].x * f1;
+                Ax[4 * e + 1] = Ax[4 * e + 1] * f0 + xs[e].y * f1;
+                Ax[4 * e + 2] = Ax[4 * e + 2] * f0 + xs[e].z * f1;
+                Ax[4 * e + 3] = Ax[4 * e + 3] * f0 + xs[e].w * f1;
+              }
+              Mx = mn;
+            }
+            float* oc = out_col(c) + dd;
+            const float inv = 1.0f / Lx;
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              reinterpret_cast<float4*>(oc)[e] =
+                  make_float4(Ax[4 * e] * inv, Ax[4 * e + 1] * inv, Ax[4 * e + 2] * inv,
+                              Ax[4 * e + 3] * inv);
+          }
+          if (tid == 0) *mq_counter(a.flags, j, 0) = 0;  // ready for the next call
+        }
+      }
+      named_barrier(kSwBar, kSwThreads);  // red and the merge flag are free for the next piece
+      x = b_piece;
+    }
+    tc_fence_before();
+  }
+
+  // ---- teardown: every role has drained its copies and products
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------ launchers ----
+static cudaError_t mqtc_prepare(size_t smem) {
+  static std::atomic<size_t> granted[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && granted[dev].load(std::memory_order_relaxed) >= smem)
+    return cudaSuccess;
+  e = cudaFuncSetAttribute(paged_decode_mqtc_kernel<PKV_KV_F16>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e == cudaSuccess && dev >= 0 && dev < 64) {
+    size_t cur = granted[dev].load();
+    while (cur < smem && !granted[dev].compare_exchange_weak(cur, smem)) {
+    }
+  }
+  return e;
+}
+
+cudaError_t launch_paged_decode_mqtc(const DecodeArgs& a, const TileMaps& maps, int chunks,
+                                     cudaStream_t st) {
+  const size_t smem = TcSmem::bytes(a.num_rows);
+  cudaError_t e = mqtc_prepare(smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(chunks);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = PKV_PDL;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, paged_decode_mqtc_kernel<PKV_KV_F16>, a, maps);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t paged_decode_mqtc_blocks_per_sm(int rows, int* blocks) {
+  const size_t smem = TcSmem::bytes(rows);
+  cudaError_t e = mqtc_prepare(smem);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, paged_decode_mqtc_kernel<PKV_KV_F16>,
+                                                       kTcThreads, smem);
+}
+
+}  // namespace pkv

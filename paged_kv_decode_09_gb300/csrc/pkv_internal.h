@@ -131,6 +131,10 @@ pkv_status record_error(pkv_status s, const char* msg);  // sets pkv_last_error_
 struct TileMaps {
   CUtensorMap k;
   CUtensorMap v;
+  // 16-bit formats also: one 64-dim half of a tile per copy, box [16][64]
+  // (the tensor-core several-query kernel places the halves of 8 pages apart)
+  CUtensorMap kh;
+  CUtensorMap vh;
 };
 cudaError_t encode_tile_maps(int dtype, void* k_data, void* v_data, long long tiles,
                              TileMaps* maps);
@@ -145,6 +149,10 @@ int mq_pass_queries(int dtype, int group, int q_len);
 cudaError_t launch_paged_decode_mq(int dtype, int group, const DecodeArgs& a, const TileMaps& maps,
                                    int chunks, cudaStream_t stream);
 cudaError_t paged_decode_mq_blocks_per_sm(int dtype, int group, int q_len, int rows, int* blocks);
+// The tensor-core several-query kernel (f16 KV, passes of up to 32 columns).
+cudaError_t launch_paged_decode_mqtc(const DecodeArgs& a, const TileMaps& maps, int chunks,
+                                     cudaStream_t stream);
+cudaError_t paged_decode_mqtc_blocks_per_sm(int rows, int* blocks);
 constexpr int kMqCols = 32;  // partial-state columns of a several-query workspace slot
 constexpr int kMqCounters = 4;  // arrival counters per (row, KV head): one per warp's columns
 inline size_t mq_flag_bytes(long long segments) {
