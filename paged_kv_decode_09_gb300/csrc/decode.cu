@@ -964,18 +964,21 @@ static cudaError_t encode_tile_map(CUtensorMap* m, int dtype, void* base, long l
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// A 16-bit layer's K or V data read one 64-dim half at a time.
-static cudaError_t encode_half_map(CUtensorMap* m, int dtype, void* base, long long tiles) {
+// A 16-bit layer's K or V data as 5-D tiles [2 token groups][2 halves][8
+// tokens][64 dims] (strides 2048, 128, 256 bytes): one copy lands a tile as
+// four 1 KiB blocks, each 8 tokens of one 64-dim half under the 128-byte
+// swizzle, so that the 8-token groups of consecutive tiles of one half sit a
+// uniform 2 KiB apart in shared memory.
+static cudaError_t encode_page_map(CUtensorMap* m, int dtype, void* base, long long tiles) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(kPage),
-                              static_cast<cuuint64_t>(tiles)};
-  const cuuint64_t strides[2] = {kD * 2, kD * kPage * 2};
-  const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(kPage), 1u};
-  const cuuint32_t estride[3] = {1u, 1u, 1u};
+  const cuuint64_t dims[5] = {64u, 8u, 2u, 2u, static_cast<cuuint64_t>(tiles)};
+  const cuuint64_t strides[4] = {kD * 2, 128u, 8 * kD * 2, kD * kPage * 2};
+  const cuuint32_t box[5] = {64u, 8u, 2u, 2u, 1u};
+  const cuuint32_t estride[5] = {1u, 1u, 1u, 1u, 1u};
   const CUresult r = fn(m, dtype == PKV_KV_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                               : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                        3, base, dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        5, base, dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
@@ -987,11 +990,11 @@ cudaError_t encode_tile_maps(int dtype, void* k_data, void* v_data, long long ti
   cudaError_t e = encode_tile_map(&maps->k, dtype, k_data, tiles);
   if (e == cudaSuccess) e = encode_tile_map(&maps->v, dtype, v_data, tiles);
   if (dtype == PKV_KV_F16 || dtype == PKV_KV_BF16) {
-    if (e == cudaSuccess) e = encode_half_map(&maps->kh, dtype, k_data, tiles);
-    if (e == cudaSuccess) e = encode_half_map(&maps->vh, dtype, v_data, tiles);
+    if (e == cudaSuccess) e = encode_page_map(&maps->kp, dtype, k_data, tiles);
+    if (e == cudaSuccess) e = encode_page_map(&maps->vp, dtype, v_data, tiles);
   } else {
-    maps->kh = maps->k;
-    maps->vh = maps->v;
+    maps->kp = maps->k;
+    maps->vp = maps->v;
   }
   return e;
 }

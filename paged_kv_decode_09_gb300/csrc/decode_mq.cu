@@ -50,10 +50,12 @@ __host__ __device__ constexpr int mq_tiles() {
 
 // The kernel a call takes, by its C = q_len * G columns:
 //   f16 : C <= 8 paged_decode_mq_kernel; beyond, the tensor-core kernel
-//         (decode_mqtc.cu, passes of 32 columns): 49.2 and 51.6 us for 16
-//         and 32 columns on the 8B f16 layer, where the warp-level team
-//         kernels below (four warps of 4 or 8 columns per page, which took
-//         this range before) measured 54.2 and 68.2 us.
+//         (decode_mqtc.cu, passes of 32 columns) for calls of up to
+//         paged_decode_mqtc_max_rows() rows (its plan tables share the CTA's
+//         shared memory with its rings: 2055 rows with 227 KiB), else four
+//         warps of 4 columns per page up to 16 columns, of 8 beyond (passes
+//         of 32).  On the 8B f16 layer at 16 and 32 columns the tensor-core
+//         kernel measured 39.3 and 40.4 us, the team kernels 54.2 and 68.2.
 //   bf16: C <= 4 paged_decode_mq_kernel; C <= 8 two warps of 4 columns (four
 //         would leave two idle); beyond, four warps of 4 (passes of 16).
 //   q8_0: C <= 8 paged_decode_mq_kernel; C <= 16 two warps of 8 columns;
@@ -1413,8 +1415,10 @@ static cudaError_t launch_mq_dt(int kind, const DecodeArgs& a, const TileMaps& m
     if (kind == kMqSingle) return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
     if (kind == kMqPair1) return launch_mq_t<DT, kMqPair1>(a, maps, chunks, st);
     return launch_mq_t<DT, kMqTeam1>(a, maps, chunks, st);
-  } else {  // f16: wider passes take the tensor-core kernel (launch_paged_decode_mq)
-    return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
+  } else {  // f16 (the tensor-core kernel is launched by launch_paged_decode_mq)
+    if (kind == kMqSingle) return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
+    if (kind == kMqTeam1) return launch_mq_t<DT, kMqTeam1>(a, maps, chunks, st);
+    return launch_mq_t<DT, kMqTeam2>(a, maps, chunks, st);
   }
 }
 
@@ -1431,14 +1435,24 @@ static cudaError_t occupancy_mq_dt(int kind, int rows, int* blocks) {
     if (kind == kMqPair1) return mq_occupancy_t<DT, kMqPair1>(rows, blocks);
     return mq_occupancy_t<DT, kMqTeam1>(rows, blocks);
   } else {  // f16
-    return mq_occupancy_t<DT, kMqSingle>(rows, blocks);
+    if (kind == kMqSingle) return mq_occupancy_t<DT, kMqSingle>(rows, blocks);
+    if (kind == kMqTeam1) return mq_occupancy_t<DT, kMqTeam1>(rows, blocks);
+    return mq_occupancy_t<DT, kMqTeam2>(rows, blocks);
   }
+}
+
+// The kernel of a call of `rows` rows: the tensor-core kernel's calls of
+// more rows than it takes go to the team kernels.
+static int mq_kind_rows(int dtype, int group, int q_len, int rows) {
+  const int kind = mq_kind(dtype, group, q_len);
+  if (kind != kMqTc || rows <= paged_decode_mqtc_max_rows()) return kind;
+  return q_len * group <= 16 ? kMqTeam1 : kMqTeam2;
 }
 
 cudaError_t launch_paged_decode_mq(int dtype, int group, const DecodeArgs& a, const TileMaps& maps,
                                    int chunks, cudaStream_t st) {
   if (group != 1 && group != 2 && group != 4) return cudaErrorInvalidValue;
-  const int kind = mq_kind(dtype, group, a.q_len);
+  const int kind = mq_kind_rows(dtype, group, a.q_len, a.num_rows);
   if (kind == kMqTc) return launch_paged_decode_mqtc(a, maps, chunks, st);
   if (dtype == PKV_KV_F16) return launch_mq_dt<PKV_KV_F16>(kind, a, maps, chunks, st);
   if (dtype == PKV_KV_BF16) return launch_mq_dt<PKV_KV_BF16>(kind, a, maps, chunks, st);
@@ -1448,7 +1462,7 @@ cudaError_t launch_paged_decode_mq(int dtype, int group, const DecodeArgs& a, co
 
 cudaError_t paged_decode_mq_blocks_per_sm(int dtype, int group, int q_len, int rows,
                                           int* blocks) {
-  const int kind = mq_kind(dtype, group, q_len);
+  const int kind = mq_kind_rows(dtype, group, q_len, rows);
   if (kind == kMqTc) return paged_decode_mqtc_blocks_per_sm(rows, blocks);
   if (dtype == PKV_KV_F16) return occupancy_mq_dt<PKV_KV_F16>(kind, rows, blocks);
   if (dtype == PKV_KV_BF16) return occupancy_mq_dt<PKV_KV_BF16>(kind, rows, blocks);

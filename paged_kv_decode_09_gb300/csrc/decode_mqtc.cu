@@ -31,16 +31,18 @@
 //
 // The warps have one job each, and the blocks flow through them as a
 // pipeline.  Warps 8 and 10 fetch block-table entries, store the new tokens
-// of the first pass (K, V) and queue the tensor copies of [16 tokens][64
-// dims] halves of K and of V into rings of two 32 KiB slots each (8 pages);
-// warp 9 issues the products, the scores of block b + 2 before the values of
-// block b; warps 0..7 run the softmax of block b while the copies of later
-// blocks land and the products of the neighbouring blocks run.  A K slot is
-// free again once its scores are computed, well before the block's values,
-// so K copies run about two blocks ahead of the softmax; V copies, needed
-// last, follow their own ring.  S is double-buffered in tensor memory, and
-// P and Q^T in shared memory.  Shared-memory barriers carry every
-// hand-over:
+// of the first pass (K, V) one block ahead of their copies, and queue one
+// tensor copy per tile of K and of V into rings of 32 KiB slots (8 pages;
+// three for K, two for V).  A tile lands as [2 token groups][2 halves][8
+// tokens][64 dims], so the 8-token groups of a slot's 8 tiles sit a uniform 2
+// KiB apart for either half: the operand layout the products read.  Warp 9
+// (one elected lane) issues the products, the scores of block b + 2 before
+// the values of block b.  Warps 0..7 run the softmax of block b meanwhile.
+// A K slot is free again once its scores are computed, well before the
+// block's values, so K copies run ahead of the softmax; V copies, needed
+// last, follow their own ring.  S is double-buffered in tensor memory and P
+// in shared memory; Q^T, one buffer, is replaced once a piece's last scores
+// are read.  Shared-memory barriers carry every hand-over:
 //   kfull[s], vfull[s]  copies of K or V slot s landed (transaction bytes)
 //   kempty[s]  the scores of K slot s computed  (product commit)
 //   vempty[s]  the values of V slot s computed  (product commit)
@@ -48,12 +50,19 @@
 //   sfree[x]  S buffer x read                  (softmax warps, 8 arrivals)
 //   pready[x] P buffer x written               (softmax warps, 8 arrivals)
 //   pvdone[x] the values product from P x done (product commit)
-//   qready[x] Q^T buffer x written             (softmax warps, 8 arrivals)
+//   qready    Q^T of the next piece written    (softmax warps, 8 arrivals)
 // Every wait is bounded; the warp that gives up sets the CTA's abort flag,
 // which ends every other wait, and the CTA drains its copies and products
-// before it releases the tensor memory.  One CTA per SM; the work split, the
-// partial states and the merge of split segments are those of the other
-// several-query kernels (workspace slots of 32 columns).
+// before it releases the tensor memory.
+//
+// One CTA per SM.  The work split is the uniform split of the (row, KV head,
+// page) units with a price per piece (kPiecePenalty), so that a chunk that
+// crosses into another segment reads fewer pages.  A segment split over
+// chunks leaves a partial state per piece in the workspace (slots of 32
+// columns); the piece that takes the segment's last arrival ticket (taken as
+// its last block starts) merges them once the others have published theirs
+// (a release add to the segment's count of pieces written), staging two
+// pieces' accumulators at a time in shared memory by bulk copies.
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -71,32 +80,34 @@ constexpr int kKWarp = 8, kMmaWarp = 9, kVWarp = 10;  // warp 11 only fills the 
 constexpr int kTcThreads = 384;
 constexpr int kSwBar = 1;                            // named barrier of the softmax warps
 constexpr int kBlockPages = 8;                       // pages of a block: the products' M = 128 tokens
-constexpr int kTcStages = 2;                         // slots of the K ring and of the V ring
-constexpr uint32_t kHalfBytes = kBlockPages * 2048;  // one 64-dim half of K or V for 8 pages
-constexpr uint32_t kSlotBytes = 2 * kHalfBytes;      // a ring slot: both halves, 32 KiB
+constexpr int kKStages = 3, kVStages = 2;            // slots of the K ring and of the V ring
+constexpr uint32_t kSlotBytes = kBlockPages * 4096;  // a ring slot: 8 tiles of K or V, 32 KiB
 constexpr uint32_t kTmemCols = 128;                  // S0: 0..31, S1: 32..63, O^T: 64..127
 constexpr uint32_t kTmemO = 64;
 constexpr float kPUp = 128.0f;                       // P is stored times 2^7 (as kPShift)
 constexpr float kNoMax = -1e30f;                     // a column's m before its first score
+// The work split's price of a piece, in units (pages): a chunk that a
+// segment starts in pays it (measured on the 8B layer at 32 columns: one more
+// piece costs about as long as 40 pages of its blocks).
+constexpr int kPiecePenalty = 40;
 
 // Shared memory, from a 1024-byte aligned base.
 struct TcSmem {
   static constexpr uint32_t kAlign = 1024;
-  static constexpr uint32_t kV = kTcStages * kSlotBytes;      // K ring from 0, then the V ring
-  static constexpr uint32_t kQ = 2 * kTcStages * kSlotBytes;  // Q^T x2: [2 halves][64 rows][128 B]
-  static constexpr uint32_t kP = kQ + 2 * 16384;           // P x2: [128 tokens][64 columns]
+  static constexpr uint32_t kV = kKStages * kSlotBytes;       // K ring from 0, then the V ring
+  static constexpr uint32_t kQ = kV + kVStages * kSlotBytes;  // Q^T: [2 halves][64 rows][128 B]
+  static constexpr uint32_t kP = kQ + 16384;               // P x2: [128 tokens][64 columns]
   static constexpr uint32_t kRed = kP + 2 * 16384;         // float [2][4][32] block maxima, [4][32] sums
   static constexpr uint32_t kQexp = kRed + 3 * 4 * 32 * 4; // float [2][32]: 2^e of each column's q
-  static constexpr uint32_t kBar = kQexp + 2 * 32 * 4;     // 19 barriers, 8 bytes each
-  static constexpr uint32_t kCtl = kBar + 20 * 8;          // int [4]: [0] abort, [1] last arrival
+  static constexpr uint32_t kBar = kQexp + 2 * 32 * 4;     // 21 barriers, 8 bytes each
+  static constexpr uint32_t kCtl = kBar + 22 * 8;          // int [4]: [0] abort, [1] last arrival
   static constexpr uint32_t kTmem = kCtl + 16;             // uint32: tensor-memory base
-  static constexpr uint32_t kSplit = kTmem + 16;
-  static constexpr uint32_t kRows = kSplit + 16;
-  static size_t bytes(int rows) { return kAlign + kRows + plan_ints(rows) * 4; }
+  static constexpr uint32_t kRows = kTmem + 16;             // int row_start[rows + 1], lens[rows]
+  static size_t bytes(int rows) { return kAlign + kRows + (2 * static_cast<size_t>(rows) + 1) * 4; }
 };
 // barrier indices
-constexpr int kBKfull = 0, kBKempty = 2, kBVfull = 4, kBVempty = 6, kBSfull = 8, kBSfree = 10,
-              kBPready = 12, kBPvdone = 14, kBQready = 16, kBStall = 18, kNumBars = 19;
+constexpr int kBKfull = 0, kBKempty = 3, kBVfull = 6, kBVempty = 8, kBSfull = 10, kBSfree = 12,
+              kBPready = 14, kBPvdone = 16, kBQready = 18, kBStall = 19, kBMerge = 20, kNumBars = 21;
 
 // --------------------------------------------------------- tcgen05 PTX ----
 // Shared-memory matrix descriptor: 128-byte swizzle, start address and the
@@ -181,12 +192,86 @@ __device__ __forceinline__ bool barrier_or(int id, int count, bool pred) {
   return r != 0;
 }
 
-// A wait of one lane of the warp, its outcome given to every lane
+// Tensor copy of the 5-D box at {0, 0, 0, 0, v} (a whole tile) into shared
+// memory, completing on `bar`, with an L2 eviction-priority hint.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* tmap, int v, uint32_t bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %2, %2, %2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(tmap), "r"(0), "r"(v), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// The maximum (kMax) or sum over the warp's 32 lanes of each of a lane's 16
+// values, by a butterfly that halves the values a lane keeps at each step
+// (8, 4, 2, 1 exchanges, then one more): 16 shuffles.  Lane l returns value
+// (l >> 1) & 15's result; v is overwritten.
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int half = 8 >> s, bit = 16 >> s;
+    const bool upper = (lane & bit) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      const float recv = __shfl_xor_sync(kFull, send, bit);
+      v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  const float r = __shfl_xor_sync(kFull, v[0], 1);
+  return kMax ? fmaxf(v[0], r) : v[0] + r;
+}
+
+// Atomic add at GPU scope with release order, no value returned: the writes
+// ordered before it (including other threads' writes ordered by a CTA-scope
+// barrier) are visible to whoever acquires the sum.
+__device__ __forceinline__ void red_release_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// True in one lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// Whether the phase of `bar` with the given parity has completed (does not
+// suspend the thread).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// A wait of one lane of the warp, polling without suspending (each hand-over
+// of the pipeline is on its critical path), its outcome given to every lane
 // (warp-uniform: the tensor-memory loads that follow are warp-collective).
+// Gives up, as mbar_wait_bounded does, once *abort is set or after
+// kWaitLimitNs.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
                                           int lane) {
   int ok = 1;
-  if (lane == 0) ok = mbar_wait_bounded(bar, parity, abort) ? 1 : 0;
+  if (lane == 0 && !mbar_test_wait(bar, parity)) {
+    const unsigned long long t0 = global_ns();
+    ok = 0;
+    while (!ok) {
+#pragma unroll 1
+      for (int i = 0; i < 64 && !ok; ++i) ok = mbar_test_wait(bar, parity) ? 1 : 0;
+      if (!ok && (*abort || global_ns() - t0 > kWaitLimitNs)) break;
+    }
+  }
   return __shfl_sync(kFull, ok, 0) != 0;
 }
 
@@ -211,7 +296,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int* ctl = reinterpret_cast<volatile int*>(smem + SM::kCtl);
   int* row_start = reinterpret_cast<int*>(smem + SM::kRows);
   int* lens = row_start + a.num_rows + 1;
-  int* pc = lens + a.num_rows;
   const uint32_t bars = smem_addr(smem + SM::kBar);
   auto bar = [&](int b, int x) { return bars + 8u * static_cast<uint32_t>(b + x); };
   const uint32_t sQ = smem_addr(smem + SM::kQ), sP = smem_addr(smem + SM::kP);
@@ -220,20 +304,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int plan_window = a.window > 0 ? a.window + a.q_len - 1 : 0;
 
   if (tid == 0) {
-    prefetch_tensormap(&maps.kh);  // kernel parameters, not written by an earlier kernel
-    prefetch_tensormap(&maps.vh);
+    prefetch_tensormap(&maps.kp);  // kernel parameters, not written by an earlier kernel
+    prefetch_tensormap(&maps.vp);
     ctl[0] = 0;
     ctl[1] = 0;
     for (int b = 0; b < kNumBars; ++b) {
       const bool sw = b >= kBSfree && b < kBSfree + 2;
       const bool sw2 = b >= kBPready && b < kBPready + 2;
-      const bool sw3 = b >= kBQready && b < kBQready + 2;
+      const bool sw3 = b == kBQready;
       mbar_init(bars + 8u * b, (sw || sw2 || sw3) ? kSwWarps : 1);
     }
     fence_mbar_init();
   }
   // Q^T and P start zeroed: Q^T rows of columns beyond nc stay zero
-  for (int e = tid; e < 65536 / 16; e += kTcThreads)
+  for (int e = tid; e < 49152 / 16; e += kTcThreads)
     reinterpret_cast<uint4*>(smem + SM::kQ)[e] = make_uint4(0u, 0u, 0u, 0u);
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -250,12 +334,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + SM::kTmem);
   const bool stalled = test_stall(bar(kBStall, 0), a.test_stall_ns, ctl, a.status);
-  plan_split(row_start, a.num_rows, a.n_kv, a.vchunks, a.aligned_split,
-             reinterpret_cast<Split*>(smem + SM::kSplit), pc);
-  const Split* sp = reinterpret_cast<const Split*>(smem + SM::kSplit);
+  // ---- the work split: the uniform split of the (row, KV head, page) units
+  // over virtual units, in which every segment is preceded by kPiecePenalty
+  // units that no chunk reads.  A chunk that a segment starts in gets that
+  // many fewer units: the cost of one more piece (its end, partial state
+  // and merge, and the next piece's start).  Segment s = (row i, head h),
+  // real units [r_s, r_s + npg), sits at virtual [r_s + P (s + 1), ...).
+  const long long T = static_cast<long long>(a.n_kv) * row_start[a.num_rows];
+  const long long Tv = T + static_cast<long long>(kPiecePenalty) * a.n_kv * a.num_rows;
+  // chunks of at least one virtual unit: a chunk inside a segment then holds
+  // at least one of its units (chunks past C are empty)
+  const int C = static_cast<int>(min(static_cast<long long>(a.vchunks), Tv));
+  auto vrow = [&](int r) {  // virtual start of row r (its first penalty)
+    return static_cast<long long>(a.n_kv) * (row_start[r] + static_cast<long long>(kPiecePenalty) * r);
+  };
+  auto vreal = [&](long long vb) -> long long {  // the first unit at virtual position >= vb
+    if (vb >= Tv) return T;
+    int lo = 0, hi = a.num_rows;  // vrow(lo) <= vb < vrow(hi)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (vrow(mid) <= vb)
+        lo = mid;
+      else
+        hi = mid;
+    }
+    const int npg = row_start[lo + 1] - row_start[lo];
+    const long long base = static_cast<long long>(a.n_kv) * row_start[lo];
+    if (npg == 0) return base;
+    const long long r = vb - vrow(lo);
+    const long long h = r / (npg + kPiecePenalty);
+    const long long off = r - h * (npg + kPiecePenalty) - kPiecePenalty;
+    return base + h * npg + (off > 0 ? off : 0);
+  };
+  // first and last chunk of segment (i, h) of npg > 0 pages
+  auto seg_chunks = [&](int i, int h, int& k0, int& k1) {
+    const int npg = row_start[i + 1] - row_start[i];
+    const long long v0 = static_cast<long long>(a.n_kv) * row_start[i] + static_cast<long long>(h) * npg +
+                         static_cast<long long>(kPiecePenalty) * (static_cast<long long>(i) * a.n_kv + h + 1);
+    k0 = chunk_of(v0, Tv, C);
+    k1 = chunk_of(v0 + npg - 1, Tv, C);
+  };
   const int k = blockIdx.x;
-  long long c_begin, c_end;
-  chunk_range(*sp, k, row_start, pc, a.num_rows, a.n_kv, c_begin, c_end);
+  const long long c_begin = k < C ? vreal(static_cast<long long>(k) * Tv / C) : T;
+  const long long c_end = k < C ? vreal(static_cast<long long>(k + 1) * Tv / C) : T;
 
   if (blockIdx.x == 0) {  // rows without tokens (or shorter than q_len): zeros
     for (int i = 0; i < a.num_rows; ++i)
@@ -287,170 +408,218 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // K (warp 8) or V (warp 10): slot b % 2 of the ring for block b, once the
     // product that read the slot's previous block is done.
     const bool is_v = warp == kVWarp;
-    const CUtensorMap* map = is_v ? &maps.vh : &maps.kh;
+    const CUtensorMap* map = is_v ? &maps.vp : &maps.kp;
     const uint32_t ring = smem_addr(smem) + (is_v ? SM::kV : 0u);
     const int bfull = is_v ? kBVfull : kBKfull, bempty = is_v ? kBVempty : kBKempty;
+    const int ns = is_v ? kVStages : kKStages;
     const float* src_new = is_v ? a.v_new : a.k_new;
     uint8_t* data = is_v ? a.v_data : a.k_data;
     const uint64_t policy = policy_evict_first();
+    // lane q < n: the block-table entry of the block's page q, read one
+    // block ahead (while the slot of the block before is awaited)
+    auto entry = [&](const Blk& bk) {
+      return lane < bk.n
+                 ? __ldg(a.block_table + static_cast<long long>(bk.i) * a.bt_stride + bk.pfirst + lane)
+                 : 0;
+    };
+    // The new tokens (first pass) in block bk's pages, in the kv_append
+    // encoding, before the block's copies: 4 dims per lane, the loads of 8
+    // tokens issued before their stores.
+    auto append_block = [&](const Blk& bk, int pg) {
+      const int first_new = bk.L - a.q_len;
+      const int lo = max(first_new, bk.pfirst * kPage);
+      const int hi = min(bk.L, (bk.pfirst + bk.n) * kPage);
+      const bool ok_pg = lane < bk.n && pg >= 0 && pg < a.num_pages;
+      for (int p0 = lo; p0 < hi; p0 += 8) {
+        float4 v4[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const long long src_row = static_cast<long long>(bk.i) * a.q_len + (p0 + e - first_new);
+          if (p0 + e < hi)
+            v4[e] = __ldg(reinterpret_cast<const float4*>(src_new + (src_row * a.n_kv + bk.h) * kD +
+                                                           lane * 4));
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int pos = p0 + e;
+          if (pos < hi) {
+            const int q = pos / kPage - bk.pfirst;
+            const int pgq = __shfl_sync(kFull, pg, q);
+            if (__shfl_sync(kFull, ok_pg ? 1 : 0, q)) {
+              const __half2 h01 = __floats2half2_rn(v4[e].x, v4[e].y);
+              const __half2 h23 = __floats2half2_rn(v4[e].z, v4[e].w);
+              uint2 w;
+              w.x = *reinterpret_cast<const uint32_t*>(&h01);
+              w.y = *reinterpret_cast<const uint32_t*>(&h23);
+              const size_t tile = static_cast<size_t>(pgq) * a.n_kv + bk.h;
+              *reinterpret_cast<uint2*>(data + tile * (kPage * kD * 2) + (pos % kPage) * (kD * 2) +
+                                        lane * 8) = w;
+            }
+          }
+        }
+      }
+      // the tiles are read next by the async proxy (tensor copies)
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __syncwarp();
+    };
     int b = 0;
     bool failed = stalled;
+    Blk bk;
+    int pg = 0;
+    if (c_begin < c_end) {
+      block_at(c_begin, bk);
+      pg = entry(bk);
+      if (src_new != nullptr && !failed) append_block(bk, pg);
+    }
     for (long long x = c_begin; x < c_end && !failed; ++b) {
-      Blk bk;
-      block_at(x, bk);
-      const int st = b % kTcStages;
-      int pg = 0;
-      bool ok_pg = false;
-      if (lane < bk.n) {  // the entry is read before the wait for the slot
-        pg = __ldg(a.block_table + static_cast<long long>(bk.i) * a.bt_stride + bk.pfirst + lane);
-        ok_pg = pg >= 0 && pg < a.num_pages;
+      const long long xn = x + bk.n;
+      Blk bn;
+      int pgn = 0;
+      if (xn < c_end) {
+        block_at(xn, bn);
+        pgn = entry(bn);
       }
-      if (b >= kTcStages && !warp_wait(bar(bempty, st), ((b / kTcStages) - 1) & 1, ctl, lane)) {
+      const int st = b % ns;
+      if (b >= ns && !warp_wait(bar(bempty, st), ((b / ns) - 1) & 1, ctl, lane)) {
         failed = true;
         break;
       }
+      const bool ok_pg = lane < bk.n && pg >= 0 && pg < a.num_pages;
       if (lane < bk.n && !ok_pg) {
         if (!is_v) record_status(a.status, PKV_DEV_BAD_PAGE);
         pg = 0;
       }
-      if (src_new != nullptr) {  // the new tokens of the block's pages, before their copies
-        const int first_new = bk.L - a.q_len;
-        const int lo = max(first_new, bk.pfirst * kPage);
-        const int hi = min(bk.L, (bk.pfirst + bk.n) * kPage);
-        for (int pos = lo; pos < hi; ++pos) {
-          const int q = pos / kPage - bk.pfirst;
-          const int pgq = __shfl_sync(kFull, pg, q);
-          if (__shfl_sync(kFull, ok_pg ? 1 : 0, q)) {
-            // the kv_append encoding of one f16 token: 4 dims per lane
-            const long long src_row = static_cast<long long>(bk.i) * a.q_len + (pos - first_new);
-            const float4 v4 = __ldg(reinterpret_cast<const float4*>(
-                src_new + (src_row * a.n_kv + bk.h) * kD + lane * 4));
-            const __half2 h01 = __floats2half2_rn(v4.x, v4.y), h23 = __floats2half2_rn(v4.z, v4.w);
-            uint2 w;
-            w.x = *reinterpret_cast<const uint32_t*>(&h01);
-            w.y = *reinterpret_cast<const uint32_t*>(&h23);
-            const size_t tile = static_cast<size_t>(pgq) * a.n_kv + bk.h;
-            *reinterpret_cast<uint2*>(data + tile * (kPage * kD * 2) + (pos % kPage) * (kD * 2) +
-                                      lane * 8) = w;
-          }
-        }
-        // the tiles are read next by the async proxy (tensor copies)
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        __syncwarp();
-      }
       const uint32_t dst0 = ring + st * kSlotBytes;
-      if (lane == 0) mbar_arrive_expect_tx(bar(bfull, st), static_cast<uint32_t>(bk.n) * 2u * 2048u);
+      if (lane == 0) mbar_arrive_expect_tx(bar(bfull, st), static_cast<uint32_t>(bk.n) * 4096u);
       __syncwarp();
-      if (lane < bk.n) {
-        const int z = pg * a.n_kv + bk.h;
-        tma_load_3d(dst0 + lane * 2048, map, 0, 0, z, bar(bfull, st), policy);
-        tma_load_3d(dst0 + kHalfBytes + lane * 2048, map, 64, 0, z, bar(bfull, st), policy);
-      }
-      x += bk.n;
+      if (lane < bk.n)  // page q of the block at 4 KiB * q: one copy of the whole tile
+        tma_load_5d(dst0 + lane * 4096, map, pg * a.n_kv + bk.h, bar(bfull, st), policy);
+      // the next block's new tokens, while its slot is still in use
+      if (src_new != nullptr && xn < c_end) append_block(bn, pgn);
+      x = xn;
+      bk = bn;
+      pg = pgn;
     }
     // drain: the copies of the last slots land before the CTA exits
-    for (int bb = max(0, b - kTcStages); bb < b; ++bb)
-      if (lane == 0) mbar_wait_bounded(bar(bfull, bb % kTcStages), (bb / kTcStages) & 1, &zero);
+    for (int bb = max(0, b - ns); bb < b; ++bb)
+      if (lane == 0) mbar_wait_bounded(bar(bfull, bb % ns), (bb / ns) & 1, &zero);
     __syncwarp();
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- products ----
-    if (lane == 0) {
-      const uint32_t id_s = tc_idesc(128, 32, false, false), id_pv = tc_idesc(128, 64, true, true);
-      int b = 0, p = 0;
-      // the values products still to issue, oldest first: up to two blocks
-      // (the scores run two blocks ahead of the values)
-      int pv_cnt = 0, pv_b[2] = {0, 0}, pv_n[2] = {0, 0};
-      bool pv_first[2] = {false, false};
-      int last_bar = -1;        // barrier of the last commit, and its parity
-      uint32_t last_par = 0;
-      bool failed = stalled;
-      auto fail = [&]() {
-        if (!failed && !ctl[0]) {
-          ctl[0] = 1;
-          record_status(a.status, PKV_DEV_TIMEOUT);
-        }
-        failed = true;
-      };
-      auto issue_pv = [&]() {  // the oldest pending values product
-        const int vb = pv_b[0], vn = pv_n[0];
-        const bool vfirst = pv_first[0];
-        pv_b[0] = pv_b[1];
-        pv_n[0] = pv_n[1];
-        pv_first[0] = pv_first[1];
-        --pv_cnt;
-        if (!mbar_wait_bounded(bar(kBPready, vb & 1), (vb >> 1) & 1, ctl) ||
-            !mbar_wait_bounded(bar(kBVfull, vb % kTcStages), (vb / kTcStages) & 1, ctl)) {
-          fail();
-          return;
-        }
-        tc_fence_after();
-        const uint32_t vbase = smem_addr(smem) + SM::kV + (vb % kTcStages) * kSlotBytes;
-        const uint32_t pbase = sP + (vb & 1) * 16384;
-        for (int kk = 0; kk < vn; ++kk) {  // 16 tokens a step: P rows 16 kk .., N-major
-          const uint64_t ad = sw128_desc(vbase + kk * 2048, kHalfBytes, 1024);
-          const uint64_t bd = sw128_desc(pbase + kk * 2048, 16384, 1024);
-          tc_mma(tmem + kTmemO, ad, bd, id_pv, (!vfirst || kk > 0) ? 1 : 0);
-        }
-        tc_commit(bar(kBVempty, vb % kTcStages));
+    // The whole warp runs this loop (its waits are warp-uniform); one elected
+    // lane issues the products and their commits.
+    const bool leader = elect_one();
+    const uint32_t id_s = tc_idesc(128, 32, false, false), id_pv = tc_idesc(128, 64, true, true);
+    int b = 0, p = 0;
+    // the values products still to issue, oldest first: up to two blocks
+    // (the scores run two blocks ahead of the values)
+    int pv_cnt = 0, pv_b[2] = {0, 0}, pv_n[2] = {0, 0};
+    bool pv_first[2] = {false, false};
+    int last_bar = -1;  // barrier of the last commit, and its parity
+    uint32_t last_par = 0;
+    bool failed = stalled;
+    auto fail = [&]() {
+      if (!failed && lane == 0 && !ctl[0]) {
+        ctl[0] = 1;
+        record_status(a.status, PKV_DEV_TIMEOUT);
+      }
+      failed = true;
+    };
+    auto issue_pv = [&]() {  // the oldest pending values product
+      const int vb = pv_b[0], vn = pv_n[0];
+      const bool vfirst = pv_first[0];
+      pv_b[0] = pv_b[1];
+      pv_n[0] = pv_n[1];
+      pv_first[0] = pv_first[1];
+      --pv_cnt;
+      if (!warp_wait(bar(kBPready, vb & 1), (vb >> 1) & 1, ctl, lane) ||
+          !warp_wait(bar(kBVfull, vb % kVStages), (vb / kVStages) & 1, ctl, lane)) {
+        fail();
+        return;
+      }
+      tc_fence_after();
+      // 16 tokens (page kk, 4 KiB kk into the slot) a step: V^T rows (dims)
+      // in halves 1 KiB apart, 8-token groups 2 KiB apart; P rows 16 kk ..
+      // (N-major)
+      const uint64_t ad0 = sw128_desc(smem_addr(smem) + SM::kV + (vb % kVStages) * kSlotBytes,
+                                      1024, 2048);
+      const uint64_t bd0 = sw128_desc(sP + (vb & 1) * 16384, 16384, 1024);
+      if (leader) {
+        for (int kk = 0; kk < vn; ++kk)
+          tc_mma(tmem + kTmemO, ad0 + kk * (4096 >> 4), bd0 + kk * (2048 >> 4), id_pv,
+                 (!vfirst || kk > 0) ? 1 : 0);
+        tc_commit(bar(kBVempty, vb % kVStages));
         tc_commit(bar(kBPvdone, vb & 1));
-        last_bar = kBPvdone + (vb & 1);
-        last_par = (vb >> 1) & 1;
-      };
-      for (long long x = c_begin; x < c_end && !failed; ++p) {
-        Blk pb;
-        block_at(x, pb);
-        const long long b_piece = min(pb.seg_end, c_end);
-        if (!mbar_wait_bounded(bar(kBQready, p & 1), (p >> 1) & 1, ctl)) {
+      }
+      __syncwarp();
+      last_bar = kBPvdone + (vb & 1);
+      last_par = (vb >> 1) & 1;
+    };
+    for (long long x = c_begin; x < c_end && !failed; ++p) {
+      Blk pb;
+      block_at(x, pb);
+      const long long b_piece = min(pb.seg_end, c_end);
+      // a new piece: its Q^T is written once the softmax warps have read the
+      // scores of the last block before it, which may wait for the values
+      // products still pending here
+      while (!failed && pv_cnt > 0) issue_pv();
+      if (failed) break;
+      if (!warp_wait(bar(kBQready, 0), p & 1, ctl, lane)) {
+        fail();
+        break;
+      }
+      const uint64_t qd0 = sw128_desc(sQ, 16, 1024);
+      bool first = true;
+      for (long long xb = x; xb < b_piece; ++b) {
+        const int n = static_cast<int>(min(b_piece - xb, static_cast<long long>(kBlockPages)));
+        const int st = b % kKStages;
+        if (!warp_wait(bar(kBKfull, st), (b / kKStages) & 1, ctl, lane) ||
+            (b >= 2 && !warp_wait(bar(kBSfree, b & 1), ((b - 2) >> 1) & 1, ctl, lane))) {
           fail();
           break;
         }
-        const uint32_t qbase = sQ + (p & 1) * 16384;
-        bool first = true;
-        for (long long xb = x; xb < b_piece; ++b) {
-          const int n = static_cast<int>(min(b_piece - xb, static_cast<long long>(kBlockPages)));
-          const int st = b % kTcStages;
-          if (!mbar_wait_bounded(bar(kBKfull, st), (b / kTcStages) & 1, ctl) ||
-              (b >= 2 && !mbar_wait_bounded(bar(kBSfree, b & 1), ((b - 2) >> 1) & 1, ctl))) {
-            fail();
-            break;
-          }
-          tc_fence_after();
-          const uint32_t kbase = smem_addr(smem) + st * kSlotBytes;
+        tc_fence_after();
+        // 16 dims a step: K half kk / 4 (1 KiB further), 32 bytes in, its
+        // 8-token groups 2 KiB apart; Qhi^T rows 0..31, Qlo^T rows 32..63
+        // (4096 bytes further)
+        const uint64_t kd0 = sw128_desc(smem_addr(smem) + st * kSlotBytes, 16, 2048);
+        if (leader) {
           const uint32_t tS = tmem + (b & 1) * 32;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {  // 16 dims a step: half kk / 4, 32 bytes in
-            const uint64_t ad = sw128_desc(kbase + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-            const uint32_t qb = qbase + (kk >> 2) * 8192 + (kk & 3) * 32;
-            tc_mma(tS, ad, sw128_desc(qb, 16, 1024), id_s, kk > 0);       // Qhi^T rows 0..31
-            tc_mma(tS, ad, sw128_desc(qb + 4096, 16, 1024), id_s, 1);    // Qlo^T rows 32..63
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
+            const uint32_t qoff16 = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+            tc_mma(tS, kd0 + off, qd0 + qoff16, id_s, kk > 0);
+            tc_mma(tS, kd0 + off, qd0 + qoff16 + (4096 >> 4), id_s, 1);
           }
           tc_commit(bar(kBKempty, st));
           tc_commit(bar(kBSfull, b & 1));
-          last_bar = kBSfull + (b & 1);
-          last_par = (b >> 1) & 1;
-          if (pv_cnt == 2) {
-            issue_pv();
-            if (failed) break;
-          }
-          if (pv_cnt == 0) {
-            pv_b[0] = b;
-            pv_n[0] = n;
-            pv_first[0] = first;
-          } else {
-            pv_b[1] = b;
-            pv_n[1] = n;
-            pv_first[1] = first;
-          }
-          ++pv_cnt;
-          first = false;
-          xb += n;
         }
-        x = b_piece;
+        __syncwarp();
+        last_bar = kBSfull + (b & 1);
+        last_par = (b >> 1) & 1;
+        if (pv_cnt == 2) {
+          issue_pv();
+          if (failed) break;
+        }
+        if (pv_cnt == 0) {
+          pv_b[0] = b;
+          pv_n[0] = n;
+          pv_first[0] = first;
+        } else {
+          pv_b[1] = b;
+          pv_n[1] = n;
+          pv_first[1] = first;
+        }
+        ++pv_cnt;
+        first = false;
+        xb += n;
       }
-      while (!failed && pv_cnt > 0) issue_pv();
-      // drain: every product issued completes before the tensor memory goes
-      if (last_bar >= 0) mbar_wait_bounded(bars + 8u * last_bar, last_par, &zero);
+      x = b_piece;
     }
+    while (!failed && pv_cnt > 0) issue_pv();
+    // drain: every product issued completes before the tensor memory goes
+    if (lane == 0 && last_bar >= 0) mbar_wait_bounded(bars + 8u * last_bar, last_par, &zero);
     __syncwarp();
   } else if (warp == kVWarp + 1) {
     // fills the warpgroup; nothing to do
@@ -469,8 +638,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       failed = true;
     };
-    // Q^T of the piece at unit x into buffer qb: thread tid takes column
-    // tid / 8, dims 16 (tid % 8) ..
+    // Q^T of the piece at unit x, and its columns' scales into qexp buffer
+    // qb: thread tid takes column tid / 8, dims 16 (tid % 8) ..
     auto write_q = [&](long long x, int qb) {
       Blk pb;
       block_at(x, pb);
@@ -514,7 +683,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               w[e] = split_f16x2(ldexpf(v[8 * ch + 2 * e], -e2), ldexpf(v[8 * ch + 2 * e + 1], -e2),
                                  part == 1);
             const int d = d0 + 8 * ch;
-            const uint32_t off = qb * 16384 + (d >> 6) * 8192 + row * 128 +
+            const uint32_t off = (d >> 6) * 8192 + row * 128 +
                                  ((((d & 63) >> 3) ^ (row & 7)) << 4);
             *reinterpret_cast<uint4*>(smem + SM::kQ + off) = make_uint4(w[0], w[1], w[2], w[3]);
           }
@@ -523,7 +692,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // Q^T for the tensor cores
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBQready, qb));
+      if (lane == 0) mbar_arrive(bar(kBQready, 0));
     };
     // the query of the thread's column 16 hc + u: qbase + 4 bits u of qoff
     const int qbase = (16 * hc) / G;
@@ -533,32 +702,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       qoff |= static_cast<uint64_t>((16 * hc + u) / G - qbase) << (4 * u);
 
     int b = 0, p = 0, rb = 0;
+    int nmerge = 0;  // merge rounds staged so far (parity of the merge barrier)
     if (tid < 64) qexp_s[tid] = 0.f;  // columns beyond nc keep 0
     named_barrier(kSwBar, kSwThreads);
-    // Q^T of piece p + 2 goes into the buffer of piece p once the scores of
-    // p's last block are read (all of p's score products are then done): the
-    // product thread, two blocks ahead, may need it before this piece ends.
-    // Pieces 0 and 1 are written here.
-    auto piece_end = [&](long long x) {  // end of the piece starting at unit x
-      Blk pb;
-      block_at(x, pb);
-      return min(pb.seg_end, c_end);
-    };
-    if (c_begin < c_end && !failed) {
-      write_q(c_begin, 0);
-      const long long e0 = piece_end(c_begin);
-      if (e0 < c_end) write_q(e0, 1);
-    }
-    named_barrier(kSwBar, kSwThreads);  // qexp of pieces 0 and 1
+    // Q^T of piece p + 1 replaces p's as soon as the scores of p's last block
+    // are read (all of p's score products are then done), right after that
+    // block's vote: the product thread, two blocks ahead, waits for it.
+    if (c_begin < c_end && !failed) write_q(c_begin, 0);
+    named_barrier(kSwBar, kSwThreads);  // qexp of piece 0
     for (long long x = c_begin; x < c_end; ++p) {
       Blk pb;
       block_at(x, pb);
       const long long b_piece = min(pb.seg_end, c_end);
-      const long long next2 = b_piece < c_end ? piece_end(b_piece) : c_end;  // start of piece p + 2
       const int i = pb.i, h = pb.h, L = pb.L;
       const long long j = static_cast<long long>(i) * a.n_kv + h;
       int k0, k1;
-      segment_chunks(*sp, i, h, row_start, pc, a.num_rows, a.n_kv, k0, k1);
+      seg_chunks(i, h, k0, k1);
       const int P0 = L - a.q_len + a.q0;  // position of the pass's first query
       // tokens every used column attends: [all_lo, P0]
       const int all_lo = window_start(P0 + (nc - 1) / G + 1, a.window);
@@ -575,9 +734,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       bool first = true;
       long long xb = x;
+      const bool whole = (k0 == k1);
+      // the piece's arrival ticket (thread 0), taken when its last block
+      // starts: the round trip overlaps the block
+      int ticket = 0;
       for (; xb < b_piece; ++b) {
         const int n = static_cast<int>(min(b_piece - xb, static_cast<long long>(kBlockPages)));
         const int pfirst = pb.pfirst + static_cast<int>(xb - x);
+        if (tid == 0 && !whole && xb + n >= b_piece) ticket = atomicAdd(mq_counter(a.flags, j, 0), 1);
         // ---- scores of block b from S buffer b & 1: d = s - m, masked to -inf
         const int t0 = pfirst * kPage;
         const bool fast = t0 >= all_lo && t0 + n * kPage <= P0 + 1;  // every token, every column
@@ -592,7 +756,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           return ok ? sv * qe : -INFINITY;
         };
-        float d[16];
+        float sc[16];  // the scores (-inf when masked)
         if (!failed && !warp_wait(bar(kBSfull, b & 1), (b >> 1) & 1, ctl, lane)) fail();
         const uint32_t tS = tmem + lane_off + (b & 1) * 32 + 16 * hc;
         bool up = false;
@@ -601,6 +765,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           float sv[16];
           tc_ld16(tS, sv);
           tc_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBSfree, b & 1));  // S buffer b & 1 read
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float4 q4 = qexp4[e];
@@ -608,43 +775,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int u = 4 * e + k;
-              const float sc = score(u, sv[u], qe[k]);
-              d[u] = sc - m[u];  // -inf when masked (m is finite)
-              up = up || d[u] > 15.0f;
+              sc[u] = score(u, sv[u], qe[k]);
+              up = up || sc[u] - m[u] > 15.0f;  // -inf when masked (m is finite)
             }
           }
         } else {
 #pragma unroll
-          for (int u = 0; u < 16; ++u) d[u] = -INFINITY;
+          for (int u = 0; u < 16; ++u) sc[u] = -INFINITY;
         }
         // ---- the running maximum: raised (by a vote of the softmax warps)
         // only when the block exceeds it by more than 8
-        if (barrier_or(kSwBar, kSwThreads, up || failed)) {
+        const bool vote = barrier_or(kSwBar, kSwThreads, up || failed);
+        if (xb + n >= b_piece && b_piece < c_end && !failed) write_q(b_piece, (p + 1) & 1);
+        if (vote) {
           if (barrier_or(kSwBar, kSwThreads, failed)) {
             failed = true;
             break;
           }
-          // the scores again (S buffer b is not released yet)
-          float sc[16];
-          {
-            float sv[16];
-            tc_ld16(tS, sv);
-            tc_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float4 q4 = qexp4[e];
-              const float qe[4] = {q4.x, q4.y, q4.z, q4.w};
-#pragma unroll
-              for (int k = 0; k < 4; ++k) sc[4 * e + k] = score(4 * e + k, sv[4 * e + k], qe[k]);
-            }
-          }
           float* rr = red + rb * 128;
+          {
+            float v[16];
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            float v = sc[u];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
-            if (lane == 0) rr[qw * 32 + 16 * hc + u] = v;
+            for (int u = 0; u < 16; ++u) v[u] = sc[u];
+            const float mx = warp_reduce16<true>(v, lane);  // column (lane >> 1) & 15
+            if ((lane & 1) == 0) rr[qw * 32 + 16 * hc + ((lane >> 1) & 15)] = mx;
           }
           named_barrier(kSwBar, kSwThreads);
           rb ^= 1;  // the next raise writes the other buffer (a vote lies between)
@@ -655,12 +809,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int c = 16 * hc + u;
             const float b4 = fmaxf(fmaxf(rr[c], rr[32 + c]), fmaxf(rr[64 + c], rr[96 + c]));
             const float mn = b4 > m[u] + 15.0f ? b4 - 7.0f : m[u];
-            const float al = mn == m[u] ? 1.0f : exp2f(m[u] - mn);  // 0 from the stand-in
+            const float al = mn == m[u] ? 1.0f : ex2_approx(m[u] - mn);  // 0 from the stand-in
             if ((lane & 15) == u) my_al = al;
             any_scale = any_scale || al != 1.0f;
             l[u] *= al;
             m[u] = mn;
-            d[u] = sc[u] == -INFINITY ? -INFINITY : sc[u] - mn;
           }
           // O^T columns of the warp's 16 columns (hi and lo parts), times
           // alpha, once the values product of block b - 1 is done (not in a
@@ -684,10 +837,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0 && !failed) mbar_arrive(bar(kBSfree, b & 1));
-        if (xb + n >= b_piece && next2 < c_end && !failed) write_q(next2, p & 1);
         // ---- probabilities into P buffer b & 1 once the values product of
         // block b - 2 has read it: row t (token) of [128 tokens][64], columns
         // 0..31 Phi (pu's leading 11 bits, exact in f16 from 2^-14 up), 32..63
@@ -702,7 +851,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int u = 8 * e + 2 * k;
-              const float p0 = ex2_approx(d[u]), p1 = ex2_approx(d[u + 1]);  // P times 2^7
+              // P times 2^7 (2^-inf = 0 for masked scores; m is finite)
+              const float p0 = ex2_approx(sc[u] - m[u]), p1 = ex2_approx(sc[u + 1] - m[u + 1]);
               l[u] += p0;
               l[u + 1] += p1;
               const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFFFE000u);
@@ -722,13 +872,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int q = t / kPage, slot = t % kPage;
           const bool zero_v = hc == 0 && q < n && pos >= L;
           if (__any_sync(kFull, zero_v)) {
-            if (!warp_wait(bar(kBVfull, b % kTcStages), (b / kTcStages) & 1, ctl, lane)) {
+            if (!warp_wait(bar(kBVfull, b % kVStages), (b / kVStages) & 1, ctl, lane)) {
               fail();
             } else if (zero_v) {
 #pragma unroll
               for (int hv = 0; hv < 2; ++hv) {
-                uint4* row = reinterpret_cast<uint4*>(smem + SM::kV + (b % kTcStages) * kSlotBytes +
-                                                      hv * kHalfBytes + q * 2048 + slot * 128);
+                uint4* row = reinterpret_cast<uint4*>(smem + SM::kV + (b % kVStages) * kSlotBytes +
+                                                      q * 4096 + (slot >> 3) * 2048 + hv * 1024 +
+                                                      (slot & 7) * 128);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) row[e] = make_uint4(0u, 0u, 0u, 0u);
               }
@@ -759,17 +910,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int u = 0; u < 16; ++u) o[u] = (o[u] + olo[u]) * (1.0f / kPUp);
       }
       tc_fence_before();  // O^T read before the next piece's first values product
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        float v = l[u];
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(kFull, v, off);
-        l[u] = v;
-      }
       float* rs = red + 256;
-      if (lane == 0)
-#pragma unroll
-        for (int u = 0; u < 16; ++u) rs[qw * 32 + 16 * hc + u] = l[u];
+      {
+        const float ls = warp_reduce16<false>(l, lane);  // column (lane >> 1) & 15
+        if ((lane & 1) == 0) rs[qw * 32 + 16 * hc + ((lane >> 1) & 15)] = ls;
+      }
       named_barrier(kSwBar, kSwThreads);
       float Ls[16];
 #pragma unroll
@@ -777,7 +922,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int c = 16 * hc + u;
         Ls[u] = ((rs[c] + rs[32 + c]) + (rs[64 + c] + rs[96 + c])) * (1.0f / kPUp);
       }
-      const bool whole = (k0 == k1);
       auto out_col = [&](int c) {
         return a.out + ((static_cast<long long>(i) * a.q_len + a.q0 + c / G) * a.n_q + h * G +
                         c % G) * kD;
@@ -799,36 +943,90 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
-      if (!whole && a.flags != nullptr) {
-        named_barrier(kSwBar, kSwThreads);  // the CTA's partial, ordered before thread 0's release
-        if (tid == 0) ctl[1] = atomic_add_acq_rel(mq_counter(a.flags, j, 0), 1) == k1 - k0;
-        named_barrier(kSwBar, kSwThreads);
-        if (ctl[1]) {  // the last piece of the segment: merge all its pieces (thread 0's acquire)
-          const int c = tid >> 3, dd = (tid & 7) * 16;
-          if (c < nc) {
-            float Mx = -INFINITY, Lx = 0.f, Ax[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e) Ax[e] = 0.f;
-            for (int kk = k0; kk <= k1; ++kk) {
-              const long long slot = (kk + j) * kMqCols + c;
-              const float mk = __ldcg(a.part_ml + slot * 2), lk = __ldcg(a.part_ml + slot * 2 + 1);
-              const float4* src = reinterpret_cast<const float4*>(a.part_acc + slot * kD + dd);
-              float4 xs[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) xs[e] = __ldcg(src + e);
-              if (mk == -INFINITY) continue;  // no token of this query in the piece
-              const float mn = fmaxf(Mx, mk);
-              const float f0 = exp2f(Mx - mn), f1 = exp2f(mk - mn);
-              Lx = Lx * f0 + lk * f1;
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                Ax[4 * e] = Ax[4 * e] * f0 + xs[e].x * f1;
-                Ax[4 * e + 1] = Ax[4 * e + 1] * f0 + xs[e].y * f1;
-                Ax[4 * e + 2] = Ax[4 * e + 2] * f0 + xs[e].z * f1;
-                Ax[4 * e + 3] = Ax[4 * e + 3] * f0 + xs[e].w * f1;
+      if (!whole) {
+        // The last-ticketed piece merges the segment; every other piece
+        // publishes its partial state by a release add to the segment's
+        // count of pieces written, which the merging piece acquires.
+        if (tid == 0) ctl[1] = ticket == k1 - k0;
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // the partial, for bulk copies
+        named_barrier(kSwBar, kSwThreads);  // the CTA's partial written; ctl[1]
+        const bool last = ctl[1] != 0;
+        if (tid == 0) {
+          if (!last) {
+            red_release_add(mq_counter(a.flags, j, 1), 1);
+          } else {  // bounded wait (acquire) for the other k1 - k0 pieces
+            const int* cnt = mq_counter(a.flags, j, 1);
+            if (load_acquire(cnt) < k1 - k0) {
+              const unsigned long long t0w = global_ns();
+              while (load_acquire(cnt) < k1 - k0) {
+                if (ctl[0] || global_ns() - t0w > kWaitLimitNs) {
+                  fail();
+                  break;
+                }
               }
-              Mx = mn;
             }
+          }
+        }
+        if (barrier_or(kSwBar, kSwThreads, failed)) {
+          failed = true;
+          break;
+        }
+        if (last) {
+          // Merge the pieces (thread 0's acquire, passed on by the barrier),
+          // two per round: their accumulators [32 columns][128] (16 KiB a
+          // piece) staged in the P buffers by bulk copies, their (m, l) read
+          // directly.  Thread tid: column tid / 8, dims 16 (tid % 8) ..
+          const int c = tid >> 3, dd = (tid & 7) * 16;
+          float Mx = -INFINITY, Lx = 0.f, Ax[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) Ax[e] = 0.f;
+          const uint64_t keep = policy_evict_first();
+          for (int kb = k0; kb <= k1; kb += 2) {
+            const int np = min(2, k1 - kb + 1);
+            if (tid == 0) {
+              asm volatile("fence.proxy.async.global;" ::: "memory");  // after the acquire
+              mbar_arrive_expect_tx(bar(kBMerge, 0), static_cast<uint32_t>(np) * 16384u);
+              for (int u = 0; u < np; ++u)
+                bulk_g2s(sP + u * 16384,
+                         a.part_acc + (static_cast<long long>(kb + u) + j) * kMqCols * kD, 16384u,
+                         bar(kBMerge, 0), keep);
+            }
+            float mk[2], lk[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              mk[u] = -INFINITY;
+              lk[u] = 0.f;
+              if (u < np && c < nc) {
+                const long long slot = (static_cast<long long>(kb + u) + j) * kMqCols + c;
+                mk[u] = __ldcg(a.part_ml + slot * 2);
+                lk[u] = __ldcg(a.part_ml + slot * 2 + 1);
+              }
+            }
+            if (!warp_wait(bar(kBMerge, 0), nmerge & 1, ctl, lane)) fail();
+            ++nmerge;
+            if (!failed && c < nc) {
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                if (mk[u] == -INFINITY) continue;  // no token of this query in the piece (or none)
+                const float4* src =
+                    reinterpret_cast<const float4*>(smem + SM::kP + u * 16384 + (c * kD + dd) * 4);
+                const float mn = fmaxf(Mx, mk[u]);
+                const float f0 = exp2f(Mx - mn), f1 = exp2f(mk[u] - mn);
+                Lx = Lx * f0 + lk[u] * f1;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float4 x4 = src[e];
+                  Ax[4 * e] = Ax[4 * e] * f0 + x4.x * f1;
+                  Ax[4 * e + 1] = Ax[4 * e + 1] * f0 + x4.y * f1;
+                  Ax[4 * e + 2] = Ax[4 * e + 2] * f0 + x4.z * f1;
+                  Ax[4 * e + 3] = Ax[4 * e + 3] * f0 + x4.w * f1;
+                }
+                Mx = mn;
+              }
+            }
+            named_barrier(kSwBar, kSwThreads);  // the staged pieces read
+          }
+          if (c < nc) {
             float* oc = out_col(c) + dd;
             const float inv = 1.0f / Lx;
 #pragma unroll
@@ -837,7 +1035,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                   make_float4(Ax[4 * e] * inv, Ax[4 * e + 1] * inv, Ax[4 * e + 2] * inv,
                               Ax[4 * e + 3] * inv);
           }
-          if (tid == 0) *mq_counter(a.flags, j, 0) = 0;  // ready for the next call
+          if (tid == 0) {  // ready for the next call
+            *mq_counter(a.flags, j, 0) = 0;
+            *mq_counter(a.flags, j, 1) = 0;
+          }
         }
       }
       named_barrier(kSwBar, kSwThreads);  // red and the merge flag are free for the next piece
@@ -889,9 +1090,22 @@ cudaError_t launch_paged_decode_mqtc(const DecodeArgs& a, const TileMaps& maps, 
   attr[0].val.programmaticStreamSerializationAllowed = PKV_PDL;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, paged_decode_mqtc_kernel<PKV_KV_F16>, a, maps);
+  // One chunk per SM: the segment-aligned split needs more chunks than that
+  // for any batch of a few long rows, and trying it costs the kernel's start.
+  DecodeArgs au = a;
+  au.aligned_split = 0;
+  e = cudaLaunchKernelEx(&cfg, paged_decode_mqtc_kernel<PKV_KV_F16>, au, maps);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+int paged_decode_mqtc_max_rows() {
+  int dev = 0, optin = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return 0;
+  const long long fixed = TcSmem::kAlign + TcSmem::kRows + 4;  // 2 rows + 1 ints of plan
+  return optin > fixed ? static_cast<int>((optin - fixed) / 8) : 0;
 }
 
 cudaError_t paged_decode_mqtc_blocks_per_sm(int rows, int* blocks) {

@@ -131,10 +131,10 @@ pkv_status record_error(pkv_status s, const char* msg);  // sets pkv_last_error_
 struct TileMaps {
   CUtensorMap k;
   CUtensorMap v;
-  // 16-bit formats also: one 64-dim half of a tile per copy, box [16][64]
-  // (the tensor-core several-query kernel places the halves of 8 pages apart)
-  CUtensorMap kh;
-  CUtensorMap vh;
+  // 16-bit formats also: a tile as [2 token groups][2 halves][8 tokens][64
+  // dims], one copy per tile (the tensor-core several-query kernel)
+  CUtensorMap kp;
+  CUtensorMap vp;
 };
 cudaError_t encode_tile_maps(int dtype, void* k_data, void* v_data, long long tiles,
                              TileMaps* maps);
@@ -153,6 +153,7 @@ cudaError_t paged_decode_mq_blocks_per_sm(int dtype, int group, int q_len, int r
 cudaError_t launch_paged_decode_mqtc(const DecodeArgs& a, const TileMaps& maps, int chunks,
                                      cudaStream_t stream);
 cudaError_t paged_decode_mqtc_blocks_per_sm(int rows, int* blocks);
+int paged_decode_mqtc_max_rows();  // rows per call the tensor-core kernel takes
 constexpr int kMqCols = 32;  // partial-state columns of a several-query workspace slot
 constexpr int kMqCounters = 4;  // arrival counters per (row, KV head): one per warp's columns
 inline size_t mq_flag_bytes(long long segments) {

@@ -124,6 +124,25 @@ def test_mq_split_invariance(dtype, q_len):
         assert float(np.max(np.abs(o - outs[0]))) <= 1e-6
 
 
+@pytest.mark.parametrize("rows", [1300, 2048])
+def test_mq_many_rows(rows):
+    """f16 at 32 columns with many short rows of mixed lengths (many pieces
+    per CTA, whole and split): the tensor-core kernel keeps its plan tables in
+    shared memory beside its rings and takes every row count the API allows
+    (2048); a GPU with less shared memory would route the larger calls to the
+    team kernels."""
+    lengths = [8 + (7 * i) % 29 for i in range(rows)]
+    cfg = W.Config(**{**W.CONFIGS["tiny"].__dict__, "rows": rows, "n_q_heads": 32,
+                      "pool": ("spare", 0.10)})
+    wl = W.draw(cfg, seed=3, lengths=lengths)
+    q, _, _ = W.mq_inputs(wl, 8, seed=3)
+    host = encode_pool(wl)
+    pool = device_pool(wl, host)
+    out = _attend(wl, pool, q)
+    assert pool.read_status() == 0
+    _check(out, _oracle(wl, host, q))
+
+
 @pytest.mark.parametrize("dtype", [W.F16, W.Q8_0, W.BF16, W.F32])
 @pytest.mark.parametrize("q_len,window", [(1, 0), (4, 0), (7, 0), (8, 30)])
 def test_mq_decode_step_appends_then_attends(dtype, q_len, window):
