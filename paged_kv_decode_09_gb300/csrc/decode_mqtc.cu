@@ -87,9 +87,11 @@ constexpr uint32_t kTmemO = 64;
 constexpr float kPUp = 128.0f;                       // P is stored times 2^7 (as kPShift)
 constexpr float kNoMax = -1e30f;                     // a column's m before its first score
 // The work split's price of a piece, in units (pages): a chunk that a
-// segment starts in pays it (measured on the 8B layer at 32 columns: one more
-// piece costs about as long as 40 pages of its blocks).
-constexpr int kPiecePenalty = 40;
+// segment starts in pays it.  One more piece (its end, partial state and
+// merge, and the next piece's start) costs about as long as 50 pages of
+// blocks; on the 8B layer at 32 columns 40, 52 and 64 measured 40.6, 39.3
+// and 39.3 us, at 16 columns 39.4, 38.6 and 39.2 us.
+constexpr int kPiecePenalty = 52;
 
 // Shared memory, from a 1024-byte aligned base.
 struct TcSmem {
