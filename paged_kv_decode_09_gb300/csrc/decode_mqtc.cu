@@ -707,9 +707,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int nmerge = 0;  // merge rounds staged so far (parity of the merge barrier)
     if (tid < 64) qexp_s[tid] = 0.f;  // columns beyond nc keep 0
     named_barrier(kSwBar, kSwThreads);
-    // Q^T of piece p + 1 replaces p's as soon as the scores of p's last block
-    // are read (all of p's score products are then done), right after that
-    // block's vote: the product thread, two blocks ahead, waits for it.
+    // Q^T of piece p + 1 replaces p's once the scores of p's last block are
+    // read (all of p's score products are then done), after that block's
+    // probabilities: the product thread, two blocks ahead, waits for it.
     if (c_begin < c_end && !failed) write_q(c_begin, 0);
     named_barrier(kSwBar, kSwThreads);  // qexp of piece 0
     for (long long x = c_begin; x < c_end; ++p) {
@@ -788,7 +788,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ---- the running maximum: raised (by a vote of the softmax warps)
         // only when the block exceeds it by more than 8
         const bool vote = barrier_or(kSwBar, kSwThreads, up || failed);
-        if (xb + n >= b_piece && b_piece < c_end && !failed) write_q(b_piece, (p + 1) & 1);
         if (vote) {
           if (barrier_or(kSwBar, kSwThreads, failed)) {
             failed = true;
@@ -811,7 +810,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int c = 16 * hc + u;
             const float b4 = fmaxf(fmaxf(rr[c], rr[32 + c]), fmaxf(rr[64 + c], rr[96 + c]));
             const float mn = b4 > m[u] + 15.0f ? b4 - 7.0f : m[u];
-            const float al = mn == m[u] ? 1.0f : ex2_approx(m[u] - mn);  // 0 from the stand-in
+            // 0 from the stand-in; not needed in a piece's first block (l is 0
+            // and the block's values product overwrites O^T)
+            const float al = (first || mn == m[u]) ? 1.0f : ex2_approx(m[u] - mn);
             if ((lane & 15) == u) my_al = al;
             any_scale = any_scale || al != 1.0f;
             l[u] *= al;
@@ -891,6 +892,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kBPready, b & 1));
+          // the next piece's Q^T once this piece's last scores are read: it
+          // overlaps the wait for this block's values product at the piece end
+          if (xb + n >= b_piece && b_piece < c_end) write_q(b_piece, (p + 1) & 1);
         }
         first = false;
         xb += n;
