@@ -304,8 +304,8 @@ class StepSetup:
             if cfg.dtype == W.F32 or cols <= (4 if cfg.dtype == W.BF16 else 8):
                 width = min(cols, 8)
                 kname = "paged_decode_mq_kernel"  # the warps of a CTA read different pages
-            elif cfg.dtype == W.F16:  # blocks of 8 pages on the tensor cores, passes of 32
-                width = 32
+            elif cfg.dtype == W.F16 or (cfg.dtype == W.BF16 and cols > 8):
+                width = 32  # blocks of 8 pages on the tensor cores, passes of 32
                 kname = "paged_decode_mqtc_kernel"
             else:  # teams of 2 or 4 warps share every page
                 if cfg.dtype == W.BF16:

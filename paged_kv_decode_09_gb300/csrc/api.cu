@@ -316,7 +316,7 @@ pkv_status attention_mq_impl(const pkv_pool* pool, int layer, const float* q, co
   a.test_stall_ns = pool->test_stall_ns;
   const pkv::TileMaps* maps = nullptr;
   if ((s = layer_maps(pool, layer, &maps))) return s;
-  const int per_pass = pkv::mq_pass_queries(pool->dtype, g, q_len);
+  const int per_pass = pkv::mq_pass_queries(pool->dtype, g, q_len, num_rows);
   for (int q0 = 0; q0 < q_len; q0 += per_pass) {
     a.q0 = q0;
     a.nq = q_len - q0 < per_pass ? q_len - q0 : per_pass;

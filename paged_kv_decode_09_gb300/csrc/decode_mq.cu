@@ -51,13 +51,15 @@ __host__ __device__ constexpr int mq_tiles() {
 // The kernel a call takes, by its C = q_len * G columns:
 //   f16 : C <= 8 paged_decode_mq_kernel; beyond, the tensor-core kernel
 //         (decode_mqtc.cu, passes of 32 columns) for calls of up to
-//         paged_decode_mqtc_max_rows() rows (its plan tables share the CTA's
+//         paged_decode_mqtc_max_rows(f16) rows (its plan tables share the CTA's
 //         shared memory with its rings: 2055 rows with 227 KiB), else four
 //         warps of 4 columns per page up to 16 columns, of 8 beyond (passes
 //         of 32).  On the 8B f16 layer at 16 and 32 columns the tensor-core
 //         kernel measured 38.1 and 38.9 us, the team kernels 54.2 and 68.2.
 //   bf16: C <= 4 paged_decode_mq_kernel; C <= 8 two warps of 4 columns (four
-//         would leave two idle); beyond, four warps of 4 (passes of 16).
+//         would leave two idle); beyond, the tensor-core kernel (passes of
+//         32, three bf16 parts of q and P) up to paged_decode_mqtc_max_rows()
+//         rows, else four warps of 4 (passes of 16).
 //   q8_0: C <= 8 paged_decode_mq_kernel; C <= 16 two warps of 8 columns;
 //         beyond, four warps of 8 (passes of 32).  Every warp that reads a
 //         page converts its int8 codes, so the fewer warps per page the
@@ -69,8 +71,15 @@ static int mq_kind(int dtype, int group, int q_len) {
   const int cols = q_len * group;
   if (dtype == PKV_KV_F32) return kMqSingle;
   if (dtype == PKV_KV_Q8_0) return cols <= 8 ? kMqSingle : cols <= 16 ? kMqPair2 : kMqTeam2;
-  if (dtype == PKV_KV_BF16) return cols <= 4 ? kMqSingle : cols <= 8 ? kMqPair1 : kMqTeam1;
+  if (dtype == PKV_KV_BF16) return cols <= 4 ? kMqSingle : cols <= 8 ? kMqPair1 : kMqTc;
   return cols <= 8 ? kMqSingle : kMqTc;
+}
+// The kernel of a call of `rows` rows: the tensor-core kernel's calls of
+// more rows than its plan tables hold go to the team kernels.
+static int mq_kind_rows(int dtype, int group, int q_len, int rows) {
+  const int kind = mq_kind(dtype, group, q_len);
+  if (kind != kMqTc || rows <= paged_decode_mqtc_max_rows(dtype)) return kind;
+  return dtype == PKV_KV_BF16 || q_len * group <= 16 ? kMqTeam1 : kMqTeam2;
 }
 static int mq_kind_cols(int dtype, int kind) {
   switch (kind) {
@@ -88,8 +97,8 @@ __host__ __device__ constexpr int kind_ts(int kind) {
   return kind == kMqPair1 || kind == kMqPair2 ? 2 : 4;
 }
 
-int mq_pass_queries(int dtype, int group, int q_len) {
-  const int per = mq_kind_cols(dtype, mq_kind(dtype, group, q_len)) / group;
+int mq_pass_queries(int dtype, int group, int q_len, int rows) {
+  const int per = mq_kind_cols(dtype, mq_kind_rows(dtype, group, q_len, rows)) / group;
   return per > 0 ? per : 1;
 }
 
@@ -1411,7 +1420,7 @@ static cudaError_t launch_mq_dt(int kind, const DecodeArgs& a, const TileMaps& m
     if (kind == kMqSingle) return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
     if (kind == kMqPair2) return launch_mq_t<DT, kMqPair2>(a, maps, chunks, st);
     return launch_mq_t<DT, kMqTeam2>(a, maps, chunks, st);
-  } else if constexpr (DT == PKV_KV_BF16) {
+  } else if constexpr (DT == PKV_KV_BF16) {  // (the tensor-core kernel: launch_paged_decode_mq)
     if (kind == kMqSingle) return launch_mq_t<DT, kMqSingle>(a, maps, chunks, st);
     if (kind == kMqPair1) return launch_mq_t<DT, kMqPair1>(a, maps, chunks, st);
     return launch_mq_t<DT, kMqTeam1>(a, maps, chunks, st);
@@ -1441,19 +1450,11 @@ static cudaError_t occupancy_mq_dt(int kind, int rows, int* blocks) {
   }
 }
 
-// The kernel of a call of `rows` rows: the tensor-core kernel's calls of
-// more rows than it takes go to the team kernels.
-static int mq_kind_rows(int dtype, int group, int q_len, int rows) {
-  const int kind = mq_kind(dtype, group, q_len);
-  if (kind != kMqTc || rows <= paged_decode_mqtc_max_rows()) return kind;
-  return q_len * group <= 16 ? kMqTeam1 : kMqTeam2;
-}
-
 cudaError_t launch_paged_decode_mq(int dtype, int group, const DecodeArgs& a, const TileMaps& maps,
                                    int chunks, cudaStream_t st) {
   if (group != 1 && group != 2 && group != 4) return cudaErrorInvalidValue;
   const int kind = mq_kind_rows(dtype, group, a.q_len, a.num_rows);
-  if (kind == kMqTc) return launch_paged_decode_mqtc(a, maps, chunks, st);
+  if (kind == kMqTc) return launch_paged_decode_mqtc(dtype, a, maps, chunks, st);
   if (dtype == PKV_KV_F16) return launch_mq_dt<PKV_KV_F16>(kind, a, maps, chunks, st);
   if (dtype == PKV_KV_BF16) return launch_mq_dt<PKV_KV_BF16>(kind, a, maps, chunks, st);
   if (dtype == PKV_KV_F32) return launch_mq_dt<PKV_KV_F32>(kind, a, maps, chunks, st);
@@ -1463,7 +1464,7 @@ cudaError_t launch_paged_decode_mq(int dtype, int group, const DecodeArgs& a, co
 cudaError_t paged_decode_mq_blocks_per_sm(int dtype, int group, int q_len, int rows,
                                           int* blocks) {
   const int kind = mq_kind_rows(dtype, group, q_len, rows);
-  if (kind == kMqTc) return paged_decode_mqtc_blocks_per_sm(rows, blocks);
+  if (kind == kMqTc) return paged_decode_mqtc_blocks_per_sm(dtype, rows, blocks);
   if (dtype == PKV_KV_F16) return occupancy_mq_dt<PKV_KV_F16>(kind, rows, blocks);
   if (dtype == PKV_KV_BF16) return occupancy_mq_dt<PKV_KV_BF16>(kind, rows, blocks);
   if (dtype == PKV_KV_F32) return occupancy_mq_dt<PKV_KV_F32>(kind, rows, blocks);

@@ -1,33 +1,37 @@
 // decode_mqtc.cu — several queries per row on the fifth-generation tensor
-// cores (tcgen05, accumulators in tensor memory), f16 KV: the verification
-// step of speculative decoding and small chunks of chunked prefill (Leone,
-// "What ships": chunked prefill, exact speculative verification; LeatEngine,
-// "Capabilities": chunked prefill, speculative decoding).
+// cores (tcgen05, accumulators in tensor memory), f16 and bf16 KV: the
+// verification step of speculative decoding and small chunks of chunked
+// prefill (Leone, "What ships": chunked prefill, exact speculative
+// verification; LeatEngine, "Capabilities": chunked prefill, speculative
+// decoding).
 //
 // The operation is that of decode_mq.cu: query j of a row of L tokens whose
 // last q_len are new sits at P = L - q_len + j and attends causally to
 // [max(0, P + 1 - W), P + 1); the (query, query head) pairs of a KV head are
 // a pass's columns, here up to 32 of them.  What differs is how a page's
 // products run: a block of 8 pages of one (row, KV head) is one matrix
-// product per step, issued by one thread:
-//   scores  S[128 tokens][32] = K[128 tokens][128 dims] (Qhi + Qlo)^T: K
-//           straight from the staged tiles (A, K-major, 128-byte swizzle);
-//           Qhi^T, the f16 rounding of the 32 columns' queries (times scale *
-//           log2 e, normalised per column by a power of two), and Qlo^T, the
-//           f16 rounding of the remainder, are two operands in shared memory
-//           whose products accumulate into the same columns, so a score keeps
-//           about 22 significant bits (as in the other kernels);
+// product per step, issued by one thread.  q and P are split into parts in
+// the KV format, whose products accumulate: f16 takes two (the rounding and
+// the rounding of the remainder, 11 significant bits each), bf16 three (8
+// bits each), so a product keeps about 22 or 24 significant bits (as in the
+// other kernels):
+//   scores  S[128 tokens][32] = K[128 tokens][128 dims] (sum of the parts of
+//           Q)^T: K straight from the staged tiles (A, K-major, 128-byte
+//           swizzle); the parts of Q^T (the 32 columns' queries times scale *
+//           log2 e; f16 normalised per column by a power of two) 32 rows each
+//           in shared memory, one product per part into the same columns;
 //   softmax one thread per (token, 16 columns), reading its row of S from
 //           tensor memory: base 2, masks per column (causal, window, length),
 //           the running maximum raised only when a block exceeds it by more
 //           than 8 (a vote of the softmax warps), P scaled by 2^7 and split
-//           into its leading 11 bits (Phi) and the f16 rounding of the rest
-//           (Plo), written as [Phi | Plo] [128 tokens][64] to shared memory,
-//           a token's 16 columns in two 16-byte stores per part;
-//   values  O^T[128 dims][64] += V^T [Phi | Plo]: V read in place from the
-//           staged tiles and [Phi | Plo] both as MN-major operands; the hi
-//           and lo halves of O^T, added at the end, stay in tensor memory for
-//           the whole piece.
+//           into its parts (f16: the leading 11 bits and the rounding of the
+//           rest; bf16: 8, 8 and the rounding of the rest), written as
+//           [P1 | P2 (| P3)] [128 tokens][32 a part] to shared memory, a
+//           token's 16 columns in two 16-byte stores per part;
+//   values  O^T[128 dims][32 a part] += V^T [P1 | P2 (| P3)]: V read in place
+//           from the staged tiles and P both as MN-major operands; the parts'
+//           columns of O^T, added at the end, stay in tensor memory for the
+//           whole piece.
 //
 // The warps have one job each, and the blocks flow through them as a
 // pipeline.  Warps 8 and 10 fetch block-table entries, store the new tokens
@@ -80,10 +84,9 @@ constexpr int kKWarp = 8, kMmaWarp = 9, kVWarp = 10;  // warp 11 only fills the 
 constexpr int kTcThreads = 384;
 constexpr int kSwBar = 1;                            // named barrier of the softmax warps
 constexpr int kBlockPages = 8;                       // pages of a block: the products' M = 128 tokens
-constexpr int kKStages = 3, kVStages = 2;            // slots of the K ring and of the V ring
+constexpr int kVStages = 2;                          // slots of the V ring
 constexpr uint32_t kSlotBytes = kBlockPages * 4096;  // a ring slot: 8 tiles of K or V, 32 KiB
-constexpr uint32_t kTmemCols = 128;                  // S0: 0..31, S1: 32..63, O^T: 64..127
-constexpr uint32_t kTmemO = 64;
+constexpr uint32_t kTmemO = 64;                      // S0: 0..31, S1: 32..63, O^T from 64
 constexpr float kPUp = 128.0f;                       // P is stored times 2^7 (as kPShift)
 constexpr float kNoMax = -1e30f;                     // a column's m before its first score
 // The work split's price of a piece, in units (pages): a chunk that a
@@ -93,13 +96,39 @@ constexpr float kNoMax = -1e30f;                     // a column's m before its 
 // and 39.3 us, at 16 columns 39.4, 38.6 and 39.2 us.
 constexpr int kPiecePenalty = 52;
 
+// The KV formats: f16 parts of q and P keep 11 significant bits each, so
+// two of them hold the ~22 bits the other kernels keep; bf16 parts keep 8,
+// so three (~24 bits).  bf16's larger Q^T and P leave room for 2 K slots.
+template <int DT>
+struct TcFmt;
+template <>
+struct TcFmt<PKV_KV_F16> {
+  static constexpr int kParts = 2;
+  static constexpr int kKStages = 3;
+  static constexpr uint32_t kFormat = 0;     // operand type in the instruction descriptor
+  static constexpr uint32_t kTmemCols = 128;
+};
+template <>
+struct TcFmt<PKV_KV_BF16> {
+  static constexpr int kParts = 3;
+  static constexpr int kKStages = 2;
+  static constexpr uint32_t kFormat = 1;
+  static constexpr uint32_t kTmemCols = 256;
+};
+
 // Shared memory, from a 1024-byte aligned base.
+template <int DT>
 struct TcSmem {
+  using F = TcFmt<DT>;
   static constexpr uint32_t kAlign = 1024;
-  static constexpr uint32_t kV = kKStages * kSlotBytes;       // K ring from 0, then the V ring
-  static constexpr uint32_t kQ = kV + kVStages * kSlotBytes;  // Q^T: [2 halves][64 rows][128 B]
-  static constexpr uint32_t kP = kQ + 16384;               // P x2: [128 tokens][64 columns]
-  static constexpr uint32_t kRed = kP + 2 * 16384;         // float [2][4][32] block maxima, [4][32] sums
+  static constexpr uint32_t kQRows = 32 * F::kParts;           // Q^T rows: 32 columns a part
+  static constexpr uint32_t kQHalf = kQRows * 128;             // one 64-dim half of Q^T
+  static constexpr uint32_t kPCols = 32 * F::kParts;           // P columns: 32 a part
+  static constexpr uint32_t kPBuf = (kPCols + 63) / 64 * 16384;  // 64-column planes [128][128 B]
+  static constexpr uint32_t kV = F::kKStages * kSlotBytes;     // K ring from 0, then the V ring
+  static constexpr uint32_t kQ = kV + kVStages * kSlotBytes;   // Q^T: [2 halves][kQRows][128 B]
+  static constexpr uint32_t kP = kQ + 2 * kQHalf;              // P x2: [planes][128 tokens][128 B]
+  static constexpr uint32_t kRed = kP + 2 * kPBuf;         // float [2][4][32] block maxima, [4][32] sums
   static constexpr uint32_t kQexp = kRed + 3 * 4 * 32 * 4; // float [2][32]: 2^e of each column's q
   static constexpr uint32_t kBar = kQexp + 2 * 32 * 4;     // 21 barriers, 8 bytes each
   static constexpr uint32_t kCtl = kBar + 22 * 8;          // int [4]: [0] abort, [1] last arrival
@@ -122,10 +151,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
          (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
-// Instruction descriptor of kind::f16 with f32 accumulation, f16 A and B.
-__host__ __device__ constexpr uint32_t tc_idesc(int M, int N, bool a_mn_major, bool b_mn_major) {
-  return (1u << 4) | (a_mn_major ? (1u << 15) : 0u) | (b_mn_major ? (1u << 16) : 0u) |
-         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+// Instruction descriptor of kind::f16 with f32 accumulation; A and B both f16
+// (format 0) or both bf16 (format 1).
+__host__ __device__ constexpr uint32_t tc_idesc(int M, int N, bool a_mn_major, bool b_mn_major,
+                                                uint32_t format) {
+  return (1u << 4) | (format << 7) | (format << 10) | (a_mn_major ? (1u << 15) : 0u) |
+         (b_mn_major ? (1u << 16) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
 }
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                        int accumulate) {
@@ -234,6 +266,45 @@ __device__ __forceinline__ void red_release_add(int* p, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// A pair of fp32 values as the kParts parts of the format, each packed as a
+// pair: f16: the rounding and the rounding of the remainder; bf16: the
+// leading 8 bits, the next 8, and the rounding of the rest (x0 in the low
+// half of each word).
+template <int DT>
+__device__ __forceinline__ void split_parts(float x0, float x1, uint32_t (&w)[TcFmt<DT>::kParts]) {
+  if constexpr (DT == PKV_KV_F16) {
+    w[0] = split_f16x2(x0, x1, false);
+    w[1] = split_f16x2(x0, x1, true);
+  } else {
+    const float a0 = __uint_as_float(__float_as_uint(x0) & 0xFFFF0000u);
+    const float a1 = __uint_as_float(__float_as_uint(x1) & 0xFFFF0000u);
+    const float r0 = x0 - a0, r1 = x1 - a1;  // exact
+    const float b0 = __uint_as_float(__float_as_uint(r0) & 0xFFFF0000u);
+    const float b1 = __uint_as_float(__float_as_uint(r1) & 0xFFFF0000u);
+    const __nv_bfloat162 pa = __floats2bfloat162_rn(a0, a1), pb = __floats2bfloat162_rn(b0, b1);
+    const __nv_bfloat162 pc = __floats2bfloat162_rn(r0 - b0, r1 - b1);
+    w[0] = *reinterpret_cast<const uint32_t*>(&pa);
+    w[1] = *reinterpret_cast<const uint32_t*>(&pb);
+    w[2] = *reinterpret_cast<const uint32_t*>(&pc);
+  }
+}
+
+// A pair of probabilities (times 2^7, at most 2^15) as the parts of the
+// format: f16: the leading 11 bits (exact in f16 from 2^-14 up) and the
+// rounding of the rest, one packed conversion each; bf16 as split_parts.
+template <int DT>
+__device__ __forceinline__ void split_p(float p0, float p1, uint32_t (&w)[TcFmt<DT>::kParts]) {
+  if constexpr (DT == PKV_KV_F16) {
+    const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFFFE000u);
+    const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFFFE000u);
+    const __half2 hh = __floats2half2_rn(h0, h1), ll = __floats2half2_rn(p0 - h0, p1 - h1);
+    w[0] = *reinterpret_cast<const uint32_t*>(&hh);
+    w[1] = *reinterpret_cast<const uint32_t*>(&ll);
+  } else {
+    split_parts<DT>(p0, p1, w);
+  }
+}
+
 // True in one lane of the (converged) warp.
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred;
@@ -289,8 +360,12 @@ template <int DT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     paged_decode_mqtc_kernel(const __grid_constant__ DecodeArgs a,
                              const __grid_constant__ TileMaps maps) {
-  static_assert(DT == PKV_KV_F16, "the tensor-core several-query kernel takes f16 KV");
-  using SM = TcSmem;
+  static_assert(DT == PKV_KV_F16 || DT == PKV_KV_BF16,
+                "the tensor-core several-query kernel takes 16-bit KV");
+  using F = TcFmt<DT>;
+  using SM = TcSmem<DT>;
+  constexpr int kKStages = F::kKStages;
+  constexpr int kParts = F::kParts;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((SM::kAlign - (smem_addr(smem_raw) & (SM::kAlign - 1))) &
                               (SM::kAlign - 1));
@@ -319,12 +394,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     fence_mbar_init();
   }
   // Q^T and P start zeroed: Q^T rows of columns beyond nc stay zero
-  for (int e = tid; e < 49152 / 16; e += kTcThreads)
+  for (int e = tid; e < static_cast<int>((SM::kRed - SM::kQ) / 16); e += kTcThreads)
     reinterpret_cast<uint4*>(smem + SM::kQ)[e] = make_uint4(0u, 0u, 0u, 0u);
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(smem + SM::kTmem)),
-                 "r"(kTmemCols)
+                 "r"(F::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     tc_fence_before();
@@ -448,11 +523,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int q = pos / kPage - bk.pfirst;
             const int pgq = __shfl_sync(kFull, pg, q);
             if (__shfl_sync(kFull, ok_pg ? 1 : 0, q)) {
-              const __half2 h01 = __floats2half2_rn(v4[e].x, v4[e].y);
-              const __half2 h23 = __floats2half2_rn(v4[e].z, v4[e].w);
-              uint2 w;
-              w.x = *reinterpret_cast<const uint32_t*>(&h01);
-              w.y = *reinterpret_cast<const uint32_t*>(&h23);
+              uint2 w;  // 4 dims in the format (round to nearest even)
+              if constexpr (DT == PKV_KV_F16) {
+                const __half2 h01 = __floats2half2_rn(v4[e].x, v4[e].y);
+                const __half2 h23 = __floats2half2_rn(v4[e].z, v4[e].w);
+                w.x = *reinterpret_cast<const uint32_t*>(&h01);
+                w.y = *reinterpret_cast<const uint32_t*>(&h23);
+              } else {
+                const __nv_bfloat162 h01 = __floats2bfloat162_rn(v4[e].x, v4[e].y);
+                const __nv_bfloat162 h23 = __floats2bfloat162_rn(v4[e].z, v4[e].w);
+                w.x = *reinterpret_cast<const uint32_t*>(&h01);
+                w.y = *reinterpret_cast<const uint32_t*>(&h23);
+              }
               const size_t tile = static_cast<size_t>(pgq) * a.n_kv + bk.h;
               *reinterpret_cast<uint2*>(data + tile * (kPage * kD * 2) + (pos % kPage) * (kD * 2) +
                                         lane * 8) = w;
@@ -511,7 +593,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // The whole warp runs this loop (its waits are warp-uniform); one elected
     // lane issues the products and their commits.
     const bool leader = elect_one();
-    const uint32_t id_s = tc_idesc(128, 32, false, false), id_pv = tc_idesc(128, 64, true, true);
+    const uint32_t id_s = tc_idesc(128, 32, false, false, F::kFormat);
+    const uint32_t id_pv = tc_idesc(128, SM::kPCols, true, true, F::kFormat);
     int b = 0, p = 0;
     // the values products still to issue, oldest first: up to two blocks
     // (the scores run two blocks ahead of the values)
@@ -545,7 +628,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // (N-major)
       const uint64_t ad0 = sw128_desc(smem_addr(smem) + SM::kV + (vb % kVStages) * kSlotBytes,
                                       1024, 2048);
-      const uint64_t bd0 = sw128_desc(sP + (vb & 1) * 16384, 16384, 1024);
+      const uint64_t bd0 = sw128_desc(sP + (vb & 1) * SM::kPBuf, 16384, 1024);
       if (leader) {
         for (int kk = 0; kk < vn; ++kk)
           tc_mma(tmem + kTmemO, ad0 + kk * (4096 >> 4), bd0 + kk * (2048 >> 4), id_pv,
@@ -582,17 +665,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         tc_fence_after();
         // 16 dims a step: K half kk / 4 (1 KiB further), 32 bytes in, its
-        // 8-token groups 2 KiB apart; Qhi^T rows 0..31, Qlo^T rows 32..63
-        // (4096 bytes further)
+        // 8-token groups 2 KiB apart; the parts of Q^T, each 32 rows, accumulate
+        // into the same columns
         const uint64_t kd0 = sw128_desc(smem_addr(smem) + st * kSlotBytes, 16, 2048);
         if (leader) {
           const uint32_t tS = tmem + (b & 1) * 32;
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = ((kk >> 2) * 1024 + (kk & 3) * 32) >> 4;
-            const uint32_t qoff16 = ((kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-            tc_mma(tS, kd0 + off, qd0 + qoff16, id_s, kk > 0);
-            tc_mma(tS, kd0 + off, qd0 + qoff16 + (4096 >> 4), id_s, 1);
+            const uint32_t qoff16 = ((kk >> 2) * SM::kQHalf + (kk & 3) * 32) >> 4;
+#pragma unroll
+            for (int q = 0; q < kParts; ++q)  // part q of Q^T: rows 32 q .. (4096 bytes a part)
+              tc_mma(tS, kd0 + off, qd0 + qoff16 + q * (4096 >> 4), id_s, (kk > 0 || q > 0) ? 1 : 0);
           }
           tc_commit(bar(kBKempty, st));
           tc_commit(bar(kBSfull, b & 1));
@@ -667,12 +751,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 2));
       amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, 4));
       int e2 = 0;
-      if (amax > 0.f && amax <= 3.0e38f) {
+      if (DT == PKV_KV_F16 && amax > 0.f && amax <= 3.0e38f) {
         int ex;
         frexpf(amax, &ex);
         e2 = ex - 14;  // largest |q| in [2^13, 2^14): both f16 parts normal
       }
-      if (in) {
+      if (in && DT == PKV_KV_F16) {
         // rows c (hi) and 32 + c (lo); dims d0 .. d0 + 15 = two 16-byte chunks
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
@@ -685,9 +769,32 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               w[e] = split_f16x2(ldexpf(v[8 * ch + 2 * e], -e2), ldexpf(v[8 * ch + 2 * e + 1], -e2),
                                  part == 1);
             const int d = d0 + 8 * ch;
-            const uint32_t off = (d >> 6) * 8192 + row * 128 +
+            const uint32_t off = (d >> 6) * SM::kQHalf + row * 128 +
                                  ((((d & 63) >> 3) ^ (row & 7)) << 4);
             *reinterpret_cast<uint4*>(smem + SM::kQ + off) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+        if ((tid & 7) == 0) qexp_s[qb * 32 + c] = ldexpf(1.0f, e2);
+      } else if (in) {
+        // bf16: part q in row 32 q + c (no scaling: bf16 has fp32's range)
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          uint32_t w[kParts][4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint32_t pw[kParts];
+            split_parts<DT>(v[8 * ch + 2 * e], v[8 * ch + 2 * e + 1], pw);
+#pragma unroll
+            for (int q = 0; q < kParts; ++q) w[q][e] = pw[q];
+          }
+          const int d = d0 + 8 * ch;
+#pragma unroll
+          for (int q = 0; q < kParts; ++q) {
+            const int row = q * 32 + c;
+            const uint32_t off = (d >> 6) * SM::kQHalf + row * 128 +
+                                 ((((d & 63) >> 3) ^ (row & 7)) << 4);
+            *reinterpret_cast<uint4*>(smem + SM::kQ + off) =
+                make_uint4(w[q][0], w[q][1], w[q][2], w[q][3]);
           }
         }
         if ((tid & 7) == 0) qexp_s[qb * 32 + c] = ldexpf(1.0f, e2);
@@ -827,7 +934,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             } else {
               tc_fence_after();
 #pragma unroll
-              for (int part = 0; part < 2; ++part) {
+              for (int part = 0; part < kParts; ++part) {
                 const uint32_t tO = tmem + lane_off + kTmemO + 32 * part + 16 * hc;
                 float ov[16];
                 tc_ld16(tO, ov);
@@ -847,10 +954,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!failed && b >= 2 && !warp_wait(bar(kBPvdone, b & 1), ((b - 2) >> 1) & 1, ctl, lane))
           fail();
         if (!failed) {
-          uint8_t* prow = smem + SM::kP + (b & 1) * 16384 + t * 128;
+          uint8_t* prow = smem + SM::kP + (b & 1) * SM::kPBuf + t * 128;
 #pragma unroll
           for (int e = 0; e < 2; ++e) {  // columns 16 hc + 8 e .. + 7
-            uint32_t wh[4], wl[4];
+            uint32_t w[kParts][4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               const int u = 8 * e + 2 * k;
@@ -858,16 +965,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const float p0 = ex2_approx(sc[u] - m[u]), p1 = ex2_approx(sc[u + 1] - m[u + 1]);
               l[u] += p0;
               l[u + 1] += p1;
-              const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFFFE000u);
-              const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFFFE000u);
-              const __half2 hh = __floats2half2_rn(h0, h1), ll = __floats2half2_rn(p0 - h0, p1 - h1);
-              wh[k] = *reinterpret_cast<const uint32_t*>(&hh);
-              wl[k] = *reinterpret_cast<const uint32_t*>(&ll);
+              uint32_t pw[kParts];
+              split_p<DT>(p0, p1, pw);
+#pragma unroll
+              for (int q = 0; q < kParts; ++q) w[q][k] = pw[q];
             }
-            const int ch = 2 * hc + e;  // 16-byte chunk of the hi columns; lo: ch + 4
-            *reinterpret_cast<uint4*>(prow + ((ch ^ (t & 7)) << 4)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+            // part q: columns 32 q + 16 hc + 8 e ..: 16-byte chunk ch of the
+            // row, in plane ch / 8 (parts 0 and 1 in plane 0)
+            const int ch = 2 * hc + e;
+            *reinterpret_cast<uint4*>(prow + ((ch ^ (t & 7)) << 4)) =
+                make_uint4(w[0][0], w[0][1], w[0][2], w[0][3]);
             *reinterpret_cast<uint4*>(prow + (((ch + 4) ^ (t & 7)) << 4)) =
-                make_uint4(wl[0], wl[1], wl[2], wl[3]);
+                make_uint4(w[1][0], w[1][1], w[1][2], w[1][3]);
+            if constexpr (kParts == 3)
+              *reinterpret_cast<uint4*>(prow + 16384 + ((ch ^ (t & 7)) << 4)) =
+                  make_uint4(w[2][0], w[2][1], w[2][2], w[2][3]);
           }
           // V rows of slots past the row's length in a page the block reads:
           // the pool may hold anything there (NaN * 0 is NaN).  Zeroed once
@@ -906,14 +1018,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      float o[16];  // O^T (hi + lo columns) and the sums carry P's factor 2^7: removed here
-      {
+      float o[16];  // O^T (its parts' columns added) and the sums carry P's factor 2^7: removed here
+      if constexpr (kParts == 2) {
         float olo[16];
         tc_ld16(tmem + lane_off + kTmemO + 16 * hc, o);
         tc_ld16(tmem + lane_off + kTmemO + 32 + 16 * hc, olo);
         tc_wait_ld();
 #pragma unroll
         for (int u = 0; u < 16; ++u) o[u] = (o[u] + olo[u]) * (1.0f / kPUp);
+      } else {
+        tc_ld16(tmem + lane_off + kTmemO + 16 * hc, o);
+#pragma unroll
+        for (int q = 1; q < kParts; ++q) {
+          float oq[16];
+          tc_ld16(tmem + lane_off + kTmemO + 32 * q + 16 * hc, oq);
+          tc_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 16; ++u) o[u] += oq[u];
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) o[u] *= 1.0f / kPUp;
       }
       tc_fence_before();  // O^T read before the next piece's first values product
       float* rs = red + 256;
@@ -1058,12 +1182,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 0) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTmemCols)
+                 "r"(F::kTmemCols)
                  : "memory");
   }
 }
 
 // ------------------------------------------------------------ launchers ----
+template <int DT>
 static cudaError_t mqtc_prepare(size_t smem) {
   static std::atomic<size_t> granted[64];
   int dev = 0;
@@ -1071,8 +1196,8 @@ static cudaError_t mqtc_prepare(size_t smem) {
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && granted[dev].load(std::memory_order_relaxed) >= smem)
     return cudaSuccess;
-  e = cudaFuncSetAttribute(paged_decode_mqtc_kernel<PKV_KV_F16>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  e = cudaFuncSetAttribute(paged_decode_mqtc_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem));
   if (e == cudaSuccess && dev >= 0 && dev < 64) {
     size_t cur = granted[dev].load();
     while (cur < smem && !granted[dev].compare_exchange_weak(cur, smem)) {
@@ -1081,10 +1206,11 @@ static cudaError_t mqtc_prepare(size_t smem) {
   return e;
 }
 
-cudaError_t launch_paged_decode_mqtc(const DecodeArgs& a, const TileMaps& maps, int chunks,
-                                     cudaStream_t st) {
-  const size_t smem = TcSmem::bytes(a.num_rows);
-  cudaError_t e = mqtc_prepare(smem);
+template <int DT>
+static cudaError_t launch_mqtc_t(const DecodeArgs& a, const TileMaps& maps, int chunks,
+                                 cudaStream_t st) {
+  const size_t smem = TcSmem<DT>::bytes(a.num_rows);
+  cudaError_t e = mqtc_prepare<DT>(smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(chunks);
@@ -1100,26 +1226,47 @@ cudaError_t launch_paged_decode_mqtc(const DecodeArgs& a, const TileMaps& maps, 
   // for any batch of a few long rows, and trying it costs the kernel's start.
   DecodeArgs au = a;
   au.aligned_split = 0;
-  e = cudaLaunchKernelEx(&cfg, paged_decode_mqtc_kernel<PKV_KV_F16>, au, maps);
+  e = cudaLaunchKernelEx(&cfg, paged_decode_mqtc_kernel<DT>, au, maps);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-int paged_decode_mqtc_max_rows() {
+cudaError_t launch_paged_decode_mqtc(int dtype, const DecodeArgs& a, const TileMaps& maps,
+                                     int chunks, cudaStream_t st) {
+  if (dtype == PKV_KV_F16) return launch_mqtc_t<PKV_KV_F16>(a, maps, chunks, st);
+  if (dtype == PKV_KV_BF16) return launch_mqtc_t<PKV_KV_BF16>(a, maps, chunks, st);
+  return cudaErrorInvalidValue;
+}
+
+template <int DT>
+static int mqtc_max_rows_t() {
   int dev = 0, optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return 0;
-  const long long fixed = TcSmem::kAlign + TcSmem::kRows + 4;  // 2 rows + 1 ints of plan
+  const long long fixed = TcSmem<DT>::kAlign + TcSmem<DT>::kRows + 4;  // 2 rows + 1 ints of plan
   return optin > fixed ? static_cast<int>((optin - fixed) / 8) : 0;
 }
 
-cudaError_t paged_decode_mqtc_blocks_per_sm(int rows, int* blocks) {
-  const size_t smem = TcSmem::bytes(rows);
-  cudaError_t e = mqtc_prepare(smem);
+int paged_decode_mqtc_max_rows(int dtype) {
+  if (dtype == PKV_KV_F16) return mqtc_max_rows_t<PKV_KV_F16>();
+  if (dtype == PKV_KV_BF16) return mqtc_max_rows_t<PKV_KV_BF16>();
+  return 0;
+}
+
+template <int DT>
+static cudaError_t mqtc_occupancy_t(int rows, int* blocks) {
+  const size_t smem = TcSmem<DT>::bytes(rows);
+  cudaError_t e = mqtc_prepare<DT>(smem);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, paged_decode_mqtc_kernel<PKV_KV_F16>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, paged_decode_mqtc_kernel<DT>,
                                                        kTcThreads, smem);
+}
+
+cudaError_t paged_decode_mqtc_blocks_per_sm(int dtype, int rows, int* blocks) {
+  if (dtype == PKV_KV_F16) return mqtc_occupancy_t<PKV_KV_F16>(rows, blocks);
+  if (dtype == PKV_KV_BF16) return mqtc_occupancy_t<PKV_KV_BF16>(rows, blocks);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pkv

@@ -145,15 +145,16 @@ cudaError_t paged_decode_blocks_per_sm(int dtype, int group, int rows, int* bloc
 // The several-query kernels: one pass of up to mq_pass_queries(dtype, group,
 // q_len) queries (a.q0, a.nq) over the same plan; the kernel is chosen by
 // q_len * group (the same for every pass of a call).
-int mq_pass_queries(int dtype, int group, int q_len);
+int mq_pass_queries(int dtype, int group, int q_len, int rows);
 cudaError_t launch_paged_decode_mq(int dtype, int group, const DecodeArgs& a, const TileMaps& maps,
                                    int chunks, cudaStream_t stream);
 cudaError_t paged_decode_mq_blocks_per_sm(int dtype, int group, int q_len, int rows, int* blocks);
-// The tensor-core several-query kernel (f16 KV, passes of up to 32 columns).
-cudaError_t launch_paged_decode_mqtc(const DecodeArgs& a, const TileMaps& maps, int chunks,
-                                     cudaStream_t stream);
-cudaError_t paged_decode_mqtc_blocks_per_sm(int rows, int* blocks);
-int paged_decode_mqtc_max_rows();  // rows per call the tensor-core kernel takes
+// The tensor-core several-query kernel (f16 and bf16 KV, passes of up to 32
+// columns).
+cudaError_t launch_paged_decode_mqtc(int dtype, const DecodeArgs& a, const TileMaps& maps,
+                                     int chunks, cudaStream_t stream);
+cudaError_t paged_decode_mqtc_blocks_per_sm(int dtype, int rows, int* blocks);
+int paged_decode_mqtc_max_rows(int dtype);  // rows per call the tensor-core kernel takes
 constexpr int kMqCols = 32;  // partial-state columns of a several-query workspace slot
 constexpr int kMqCounters = 4;  // arrival counters per (row, KV head): one per warp's columns
 inline size_t mq_flag_bytes(long long segments) {

@@ -124,16 +124,16 @@ def test_mq_split_invariance(dtype, q_len):
         assert float(np.max(np.abs(o - outs[0]))) <= 1e-6
 
 
-@pytest.mark.parametrize("rows", [1300, 2048])
-def test_mq_many_rows(rows):
-    """f16 at 32 columns with many short rows of mixed lengths (many pieces
-    per CTA, whole and split): the tensor-core kernel keeps its plan tables in
-    shared memory beside its rings and takes every row count the API allows
-    (2048); a GPU with less shared memory would route the larger calls to the
-    team kernels."""
+@pytest.mark.parametrize("dtype,rows", [(W.F16, 1300), (W.F16, 2048), (W.BF16, 1000), (W.BF16, 1100)])
+def test_mq_many_rows(dtype, rows):
+    """32 columns with many short rows of mixed lengths (many pieces per CTA,
+    whole and split).  The tensor-core kernel keeps its plan tables in shared
+    memory beside its rings: f16 takes every row count the API allows (2048),
+    bf16 (larger Q^T and P buffers) up to 1029 rows; calls of more rows take
+    the team kernels.  Both sides of the bf16 limit."""
     lengths = [8 + (7 * i) % 29 for i in range(rows)]
     cfg = W.Config(**{**W.CONFIGS["tiny"].__dict__, "rows": rows, "n_q_heads": 32,
-                      "pool": ("spare", 0.10)})
+                      "dtype": dtype, "pool": ("spare", 0.10)})
     wl = W.draw(cfg, seed=3, lengths=lengths)
     q, _, _ = W.mq_inputs(wl, 8, seed=3)
     host = encode_pool(wl)
