@@ -55,7 +55,7 @@ __host__ __device__ constexpr int mq_tiles() {
 //         shared memory with its rings: 2055 rows with 227 KiB), else four
 //         warps of 4 columns per page up to 16 columns, of 8 beyond (passes
 //         of 32).  On the 8B f16 layer at 16 and 32 columns the tensor-core
-//         kernel measured 38.1 and 38.9 us, the team kernels 54.2 and 68.2.
+//         kernel measured 38.1 and 38.4 us, the team kernels 54.2 and 68.2.
 //   bf16: C <= 4 paged_decode_mq_kernel; C <= 8 two warps of 4 columns (four
 //         would leave two idle); beyond, the tensor-core kernel (passes of
 //         32, three bf16 parts of q and P) up to paged_decode_mqtc_max_rows()

@@ -92,9 +92,9 @@ constexpr float kNoMax = -1e30f;                     // a column's m before its 
 // The work split's price of a piece, in units (pages): a chunk that a
 // segment starts in pays it.  One more piece (its end, partial state and
 // merge, and the next piece's start) costs about as long as 50 pages of
-// blocks; on the 8B layer at 32 columns 40, 52 and 64 measured 40.6, 39.3
-// and 39.3 us, at 16 columns 39.4, 38.6 and 39.2 us.
-constexpr int kPiecePenalty = 52;
+// blocks; on the 8B f16 layer at 32 columns 48, 52 and 56 measured 38.7,
+// 38.9 and 38.4 us (40 and 64, earlier: 40.6 and 39.3 us).
+constexpr int kPiecePenalty = 56;
 
 // The KV formats: f16 parts of q and P keep 11 significant bits each, so
 // two of them hold the ~22 bits the other kernels keep; bf16 parts keep 8,
