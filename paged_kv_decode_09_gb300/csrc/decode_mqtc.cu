@@ -1238,14 +1238,24 @@ cudaError_t launch_paged_decode_mqtc(int dtype, const DecodeArgs& a, const TileM
   return cudaErrorInvalidValue;
 }
 
+// Rows whose plan tables fit beside the rings in the device's opt-in shared
+// memory (queried once per device).
 template <int DT>
 static int mqtc_max_rows_t() {
-  int dev = 0, optin = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+  static std::atomic<int> cached[64];  // 0: not queried yet; else rows + 1
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c - 1;
+  }
+  int optin = 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
     return 0;
   const long long fixed = TcSmem<DT>::kAlign + TcSmem<DT>::kRows + 4;  // 2 rows + 1 ints of plan
-  return optin > fixed ? static_cast<int>((optin - fixed) / 8) : 0;
+  const int rows = optin > fixed ? static_cast<int>((optin - fixed) / 8) : 0;
+  if (dev >= 0 && dev < 64) cached[dev].store(rows + 1, std::memory_order_relaxed);
+  return rows;
 }
 
 int paged_decode_mqtc_max_rows(int dtype) {
