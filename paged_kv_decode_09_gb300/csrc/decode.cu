@@ -99,6 +99,23 @@ struct Smem {
                 "vector accesses need 16-byte aligned regions");
 };
 
+// The same parts where `lo` differs between the lanes of a warp (the column
+// a lane holds), without a branch: every lane rounds x - m f, with m = 1 for
+// the remainder and m = 0 for the high part (0 f + x is x, f being finite:
+// the callers keep |x| inside the f16 range, or the tf32 one).  The values
+// of split_f16x2 and tf32_part, but for the sign of a zero high part.
+__device__ __forceinline__ uint32_t split_f16x2_lane(float x0, float x1, bool lo) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  const float2 f = __half22float2(h);
+  const float m = lo ? -1.0f : 0.0f;
+  const float2 r = __ffma2_rn(make_float2(m, m), f, make_float2(x0, x1));
+  const __half2 p = __floats2half2_rn(r.x, r.y);
+  return *reinterpret_cast<const uint32_t*>(&p);
+}
+__device__ __forceinline__ uint32_t tf32_part_lane(float x, bool lo) {
+  return to_tf32(fmaf(lo ? -1.0f : 0.0f, __uint_as_float(to_tf32(x)), x));
+}
+
 // Per-warp online softmax state for one piece.
 template <int DT>
 struct WarpState {
@@ -163,8 +180,8 @@ __device__ __forceinline__ void load_query(const float* qrow, float qscale, int 
     for (int ks = 0; ks < 16; ++ks) {
       float2 x = make_float2(0.f, 0.f);
       if (g2 < G) x = __ldg(reinterpret_cast<const float2*>(qrow + g2 * kD + 8 * ks + 2 * tig));
-      S.qb[ks][0] = tf32_part(x.x * qscale, lo);
-      S.qb[ks][1] = tf32_part(x.y * qscale, lo);
+      S.qb[ks][0] = tf32_part_lane(x.x * qscale, lo);
+      S.qb[ks][1] = tf32_part_lane(x.y * qscale, lo);
     }
     S.qexp = 1.0f;
   } else {
@@ -208,8 +225,8 @@ __device__ __forceinline__ void load_query(const float* qrow, float qscale, int 
     }
   #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      S.qb[ks][0] = split_f16x2(ldexpf(v[4 * ks], -e2), ldexpf(v[4 * ks + 1], -e2), lo);
-      S.qb[ks][1] = split_f16x2(ldexpf(v[4 * ks + 2], -e2), ldexpf(v[4 * ks + 3], -e2), lo);
+      S.qb[ks][0] = split_f16x2_lane(ldexpf(v[4 * ks], -e2), ldexpf(v[4 * ks + 1], -e2), lo);
+      S.qb[ks][1] = split_f16x2_lane(ldexpf(v[4 * ks + 2], -e2), ldexpf(v[4 * ks + 3], -e2), lo);
     }
     // lane 8 tig holds head tig (gid = 2 tig)
     S.qexp = ldexpf(1.0f, __shfl_sync(kFull, e2, 8 * tig));
@@ -379,8 +396,8 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
     }
     if constexpr (DT == PKV_KV_F16) {
       constexpr float kUp = static_cast<float>(1 << kPShift);
-      const uint32_t b0 = split_f16x2(pa * kUp, pb * kUp, lo);
-      const uint32_t b1 = split_f16x2(pc * kUp, pd * kUp, lo);
+      const uint32_t b0 = split_f16x2_lane(pa * kUp, pb * kUp, lo);
+      const uint32_t b1 = split_f16x2_lane(pc * kUp, pd * kUp, lo);
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         uint32_t w0, w1, w2, w3;  // (tokens 0-7 | 8-15) x (chunk 2mt | 2mt+1), transposed
@@ -389,8 +406,8 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
       }
     } else {
       // tf32 k-steps of 8 tokens: k = tig <- token 2tig, k = tig + 4 <- token 2tig + 1
-      const uint32_t b_t0 = tf32_part(pa, lo), b_t1 = tf32_part(pb, lo);
-      const uint32_t b_t8 = tf32_part(pc, lo), b_t9 = tf32_part(pd, lo);
+      const uint32_t b_t0 = tf32_part_lane(pa, lo), b_t1 = tf32_part_lane(pb, lo);
+      const uint32_t b_t8 = tf32_part_lane(pc, lo), b_t9 = tf32_part_lane(pd, lo);
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         uint32_t w0, w1, w2, w3;  // dims (16mt + gid | + 8) x tokens (2tig, 2tig+1 | + 8)
@@ -439,7 +456,7 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
       const float2 x01 = __fmul2_rn(pab, __half22float2(*reinterpret_cast<const __half2*>(&sa)));
       const float2 x23 = __fmul2_rn(pcd, __half22float2(*reinterpret_cast<const __half2*>(&sb)));
       const float x0 = x01.x, x1 = x01.y, x2 = x23.x, x3 = x23.y;
-      const uint32_t b0 = split_f16x2(x0, x1, lo), b1 = split_f16x2(x2, x3, lo);
+      const uint32_t b0 = split_f16x2_lane(x0, x1, lo), b1 = split_f16x2_lane(x2, x3, lo);
       uint32_t w0, w1, w2, w3;  // (tokens 0-7 | 8-15) x (chunk 2b | 2b+1), 16-bit transposed
       ldsm_x4_trans(vt + tile_offset<DT>(ld_tok, 2 * b + ld_chunk), w0, w1, w2, w3);
       w0 ^= 0x80808080u;
