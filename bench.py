@@ -726,8 +726,9 @@ def cpu_baseline(wl, pool, budget_s, window=0, q_len=1, q=None):
         kd = pool.k_data[0].cpu().view(torch.int16).numpy().view(np.uint16)
         vd = pool.v_data[0].cpu().view(torch.int16).numpy().view(np.uint16)
         ks = vs = None
-    else:
-        kd, vd = pool.k_data[0].cpu().numpy(), pool.v_data[0].cpu().numpy()
+    else:  # q8_0 codes: the pool stores them offset-binary (code + 128)
+        kd = (pool.k_data[0].cpu().numpy().view(np.uint8) ^ np.uint8(0x80)).view(np.int8)
+        vd = (pool.v_data[0].cpu().numpy().view(np.uint8) ^ np.uint8(0x80)).view(np.int8)
         ks = pool.k_scales[0].cpu().view(torch.int16).numpy().view(np.uint16)
         vs = pool.v_scales[0].cpu().view(torch.int16).numpy().view(np.uint16)
     per_elem = bytes_per_value(cfg.dtype)

@@ -32,12 +32,14 @@
  *       f16 : data   [num_pages][n_kv_heads][16][head_dim]  binary16
  *       bf16: data   [num_pages][n_kv_heads][16][head_dim]  bfloat16
  *       f32 : data   [num_pages][n_kv_heads][16][head_dim]  binary32
- *       q8_0: data   [num_pages][n_kv_heads][16][head_dim]  int8 codes
+ *       q8_0: data   [num_pages][n_kv_heads][16][head_dim]  code + 128 (uint8)
  *             scales [num_pages][n_kv_heads][16][head_dim/32] binary16
  *     q8_0 value = scale of the element's 32-wide block (along head_dim)
  *     times its code.  Encoding: d = amax / 127 (fp32, IEEE division), stored
  *     scale = binary16(d) rounded to nearest even, code = round(x / d) with
  *     ties away from zero (using the fp32 d); amax = 0 gives d = 0, codes 0.
+ *     The data byte is code + 128 (offset-binary: the int8 code's top bit
+ *     flipped).
  *   - q, out: fp32 [num_rows][n_q_heads][head_dim].  k_new, v_new: fp32
  *     [num_rows][n_kv_heads][head_dim].
  *   - head_dim must be 128; n_q_heads / n_kv_heads must be 1, 2 or 4.
@@ -92,11 +94,14 @@ typedef enum pkv_status {
  * barrier (a tile copy, a peer warp) before the kernel gives up. */
 #define PKV_DEFAULT_WAIT_NS (1ull << 30)
 
-/* Stored KV formats: binary16; q8_0 (int8 codes + one binary16 scale per 32
- * values along head_dim); bfloat16, rounded to nearest even, and binary32,
- * stored as given (tinyllm, "The repository currently provides": BF16/F32 KV
- * caching).  Data arrays hold 2 bytes per value (f16, bf16), 4 (f32) or 1
- * (q8_0 codes). */
+/* Stored KV formats: binary16; q8_0 (codes in [-127, 127] + one binary16
+ * scale per 32 values along head_dim, value = scale * code); bfloat16,
+ * rounded to nearest even, and binary32, stored as given (tinyllm, "The
+ * repository currently provides": BF16/F32 KV caching).  Data arrays hold 2
+ * bytes per value (f16, bf16), 4 (f32) or 1 (q8_0: the code stored
+ * offset-binary, as the unsigned byte code + 128, i.e. the int8 code with its
+ * top bit flipped, which the attention kernels widen to f16 without a
+ * per-byte sign fix). */
 typedef enum pkv_kv_dtype {
     PKV_KV_F16 = 0,
     PKV_KV_Q8_0 = 1,

@@ -15,7 +15,7 @@ import threading
 import torch
 
 F16, Q8_0, BF16, F32 = 0, 1, 2, 3
-_TORCH_DTYPE = {F16: torch.float16, Q8_0: torch.int8, BF16: torch.bfloat16, F32: torch.float32}
+_TORCH_DTYPE = {F16: torch.float16, Q8_0: torch.uint8, BF16: torch.bfloat16, F32: torch.float32}
 PAGE = 16
 HEAD_DIM = 128
 Q8_BLOCK = 32
@@ -143,8 +143,8 @@ def _need(t, dtype, name, shape=None, device=None):
 class KVPool:
     """A caller-owned paged KV pool (torch tensors) and its library descriptor.
 
-    k_data / v_data: [layers][pages][n_kv][16][128] float16 (f16), int8 (q8_0),
-    bfloat16 (bf16) or float32 (f32);
+    k_data / v_data: [layers][pages][n_kv][16][128] float16 (f16), uint8 (q8_0
+    codes stored offset-binary: code + 128), bfloat16 (bf16) or float32 (f32);
     k_scales / v_scales (q8_0): [layers][pages][n_kv][16][4] float16;
     status: int32 [1] device status word."""
 

@@ -53,7 +53,8 @@ __global__ void __launch_bounds__(kD) append_kernel(const AppendArgs a) {
       const float dq = amax / 127.0f;  // IEEE division (no fast-math in this build)
       float c = 0.0f;
       if (dq != 0.0f) c = fminf(fmaxf(roundf(x / dq), -127.0f), 127.0f);
-      reinterpret_cast<int8_t*>(data)[slot_row * kD + d] = static_cast<int8_t>(c);
+      // stored offset-binary: code + 128 (the int8 code with its top bit flipped)
+      data[slot_row * kD + d] = static_cast<uint8_t>(static_cast<int>(c) + 128);
       if ((d & 31) == 0) {
         uint8_t* sc = which == 0 ? a.k_scales : a.v_scales;
         reinterpret_cast<__half*>(sc)[slot_row * (kD / kQBlock) + d / kQBlock] =

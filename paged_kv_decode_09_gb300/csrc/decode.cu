@@ -305,10 +305,6 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
     for (int b = 0; b < 4; ++b) {
       uint32_t w0, w1, w2, w3;  // tokens gid, gid+8 of chunk 2b; the same of chunk 2b+1
       ldsm_x4(kt + tile_offset<DT>(ld_tok, 2 * b + ld_chunk), w0, w1, w2, w3);
-      w0 ^= 0x80808080u;
-      w1 ^= 0x80808080u;
-      w2 ^= 0x80808080u;
-      w3 ^= 0x80808080u;
       float c[4] = {0.f, 0.f, 0.f, 0.f};
       mma_16816(c, codes_to_f16x2<kSelB01>(w0), codes_to_f16x2<kSelB01>(w1),
                 codes_to_f16x2<kSelB23>(w0), codes_to_f16x2<kSelB23>(w1), S.qb[2 * b][0],
@@ -427,11 +423,10 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
       if (t0 + 8 < tlo || t0 + 8 >= nvalid) vb.x = vb.y = 0u;
       if (t0 + 9 < tlo || t0 + 9 >= nvalid) vb.z = vb.w = 0u;
     }
-    // the page's largest |scale|: non-negative f16 bit patterns order as integers
-    uint32_t mb = __vmaxu2(__vmaxu2(va.x & 0x7fff7fffu, va.y & 0x7fff7fffu),
-                           __vmaxu2(va.z & 0x7fff7fffu, va.w & 0x7fff7fffu));
-    mb = __vmaxu2(mb, __vmaxu2(__vmaxu2(vb.x & 0x7fff7fffu, vb.y & 0x7fff7fffu),
-                               __vmaxu2(vb.z & 0x7fff7fffu, vb.w & 0x7fff7fffu)));
+    // the page's largest |scale| (non-negative f16 bit patterns order as integers)
+    uint32_t mb = abs_max_f16x2(abs_max_f16x2(va.x, va.y), abs_max_f16x2(va.z, va.w));
+    mb = abs_max_f16x2(mb, abs_max_f16x2(abs_max_f16x2(vb.x, vb.y), abs_max_f16x2(vb.z, vb.w)));
+    mb &= 0x7fff7fffu;
     uint32_t m16 = max(mb & 0xffffu, mb >> 16);
     m16 = max(m16, __shfl_xor_sync(kFull, m16, 1));  // the page's 16 tokens: over tig
     m16 = max(m16, __shfl_xor_sync(kFull, m16, 2));
@@ -459,10 +454,6 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
       const uint32_t b0 = split_f16x2_lane(x0, x1, lo), b1 = split_f16x2_lane(x2, x3, lo);
       uint32_t w0, w1, w2, w3;  // (tokens 0-7 | 8-15) x (chunk 2b | 2b+1), 16-bit transposed
       ldsm_x4_trans(vt + tile_offset<DT>(ld_tok, 2 * b + ld_chunk), w0, w1, w2, w3);
-      w0 ^= 0x80808080u;
-      w1 ^= 0x80808080u;
-      w2 ^= 0x80808080u;
-      w3 ^= 0x80808080u;
       // row gid <- dim 2gid of the chunk (bytes 0, 2), row gid + 8 <- dim 2gid+1 (bytes 1, 3)
       mma_16816(S.o[2 * b], codes_to_f16x2<kSelB02>(w0), codes_to_f16x2<kSelB13>(w0),
                 codes_to_f16x2<kSelB02>(w1), codes_to_f16x2<kSelB13>(w1), b0, b1);

@@ -107,8 +107,8 @@ __device__ __forceinline__ uint32_t tile_offset(int t, int c) {
     return t * 128 + ((c ^ (t & 7)) << 4);
 }
 
-// Two signed 8-bit codes of `u` (the word xor 0x80808080, i.e. code + 128 in
-// each byte) as an exact f16 pair: the bytes chosen by `sel` go into the low
+// Two 8-bit codes of a stored word `u` (offset-binary: code + 128 in each
+// byte) as an exact f16 pair: the bytes chosen by `sel` go into the low
 // mantissa byte of 1024 (0x64xx = 1024 + code + 128), then 1152 is
 // subtracted in f16.
 template <uint32_t kSel>
@@ -119,6 +119,15 @@ __device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t u) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 constexpr uint32_t kSelB01 = 0x4140, kSelB23 = 0x4342, kSelB02 = 0x4240, kSelB13 = 0x4341;
+
+// Per half, the larger magnitude of two f16 pairs; the sign bit of the result
+// is the xor of the inputs' signs (clear it with 0x7fff7fff at the end of a
+// chain).  A NaN half yields the other operand's half.
+__device__ __forceinline__ uint32_t abs_max_f16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 
 // The tf32 part of x (`lo` false: its rounding; true: the rounding of the
 // remainder), as an fp32 bit pattern.
@@ -528,7 +537,9 @@ __device__ __forceinline__ void append_token(const DecodeArgs& a, long long src_
         const float c = dq != 0.0f ? fminf(fmaxf(roundf(v[e] / dq), -127.0f), 127.0f) : 0.0f;
         packed |= (static_cast<uint32_t>(static_cast<int>(c)) & 0xffu) << (8 * e);
       }
-      *reinterpret_cast<uint32_t*>(data + tile * TL::kData + slot * kD + lane * 4) = packed;
+      // stored offset-binary: code + 128 in each byte
+      *reinterpret_cast<uint32_t*>(data + tile * TL::kData + slot * kD + lane * 4) =
+          packed ^ 0x80808080u;
       if ((lane & 7) == 0) {
         uint8_t* sc = which ? a.v_scales : a.k_scales;
         reinterpret_cast<__half*>(sc + tile * TL::kScale)[slot * (kD / kQBlock) + (lane >> 3)] =

@@ -292,10 +292,6 @@ __device__ __forceinline__ void mq_process_unit(const uint8_t* st, const uint8_t
     for (int b = 0; b < 4; ++b) {
       uint32_t w0, w1, w2, w3;
       ldsm_x4(kt + tile_offset<DT>(ld_tok, 2 * b + ld_chunk), w0, w1, w2, w3);
-      w0 ^= 0x80808080u;
-      w1 ^= 0x80808080u;
-      w2 ^= 0x80808080u;
-      w3 ^= 0x80808080u;
       const uint32_t a0 = codes_to_f16x2<kSelB01>(w0), a1 = codes_to_f16x2<kSelB01>(w1);
       const uint32_t a2 = codes_to_f16x2<kSelB23>(w0), a3 = codes_to_f16x2<kSelB23>(w1);
       const uint32_t b0 = codes_to_f16x2<kSelB01>(w2), b1 = codes_to_f16x2<kSelB01>(w3);
@@ -496,10 +492,9 @@ __device__ __forceinline__ void mq_process_unit(const uint8_t* st, const uint8_t
       if (t0 + 8 < slot_lo || t0 + 8 >= slot_hi) vb.x = vb.y = 0u;
       if (t0 + 9 < slot_lo || t0 + 9 >= slot_hi) vb.z = vb.w = 0u;
     }
-    uint32_t mb = __vmaxu2(__vmaxu2(va.x & 0x7fff7fffu, va.y & 0x7fff7fffu),
-                           __vmaxu2(va.z & 0x7fff7fffu, va.w & 0x7fff7fffu));
-    mb = __vmaxu2(mb, __vmaxu2(__vmaxu2(vb.x & 0x7fff7fffu, vb.y & 0x7fff7fffu),
-                               __vmaxu2(vb.z & 0x7fff7fffu, vb.w & 0x7fff7fffu)));
+    uint32_t mb = abs_max_f16x2(abs_max_f16x2(va.x, va.y), abs_max_f16x2(va.z, va.w));
+    mb = abs_max_f16x2(mb, abs_max_f16x2(abs_max_f16x2(vb.x, vb.y), abs_max_f16x2(vb.z, vb.w)));
+    mb &= 0x7fff7fffu;
     uint32_t m16 = max(mb & 0xffffu, mb >> 16);
     m16 = max(m16, __shfl_xor_sync(kFull, m16, 1));
     m16 = max(m16, __shfl_xor_sync(kFull, m16, 2));
@@ -525,10 +520,6 @@ __device__ __forceinline__ void mq_process_unit(const uint8_t* st, const uint8_t
       const uint32_t l0 = split_f16x2(x01.x, x01.y, true), l1 = split_f16x2(x23.x, x23.y, true);
       uint32_t w0, w1, w2, w3;
       ldsm_x4_trans(vt + tile_offset<DT>(ld_tok, 2 * b + ld_chunk), w0, w1, w2, w3);
-      w0 ^= 0x80808080u;
-      w1 ^= 0x80808080u;
-      w2 ^= 0x80808080u;
-      w3 ^= 0x80808080u;
       const uint32_t e0 = codes_to_f16x2<kSelB02>(w0), e1 = codes_to_f16x2<kSelB13>(w0);
       const uint32_t e2 = codes_to_f16x2<kSelB02>(w1), e3 = codes_to_f16x2<kSelB13>(w1);
       mma_16816(S.o[2 * b], e0, e1, e2, e3, h0, h1);

@@ -2,8 +2,10 @@
 encoder, poison unused slots, and small utilities shared by the tests.
 
 Pool arrays per layer (the library's documented layout): data
-[num_pages][n_kv][16][D] (uint16 f16 / bf16 bits, float32, or int8 q8_0 codes), q8_0 scales
-[num_pages][n_kv][16][D/32] (uint16 f16 bits)."""
+[num_pages][n_kv][16][D] (uint16 f16 / bf16 bits, float32, or q8_0 codes), q8_0 scales
+[num_pages][n_kv][16][D/32] (uint16 f16 bits).  The oracle holds q8_0 codes as int8; the
+library stores them offset-binary (code + 128, the int8 byte with its top bit flipped):
+device_pool and host_arrays convert."""
 from __future__ import annotations
 
 import numpy as np
@@ -75,6 +77,16 @@ def max_abs_err(a, b):
 
 
 # ------------------------------------------------------------- device side ----
+def stored_codes(codes):
+    """int8 q8_0 codes as the pool's offset-binary bytes."""
+    return np.ascontiguousarray(codes).view(np.uint8) ^ np.uint8(0x80)
+
+
+def int8_codes(stored):
+    """The pool's offset-binary q8_0 bytes as int8 codes."""
+    return (np.ascontiguousarray(stored).view(np.uint8) ^ np.uint8(0x80)).view(np.int8)
+
+
 def device_pool(wl: W.Workload, host_pool, num_layers: int = 1, layer: int = 0):
     """A library KVPool on cuda:0 holding the host pool arrays in `layer`
     (other layers are filled with f16 NaN / NaN scales)."""
@@ -99,8 +111,8 @@ def device_pool(wl: W.Workload, host_pool, num_layers: int = 1, layer: int = 0):
             t.view(torch.int16).fill_(0x7E00)
         pool.k_data.fill_(127)
         pool.v_data.fill_(127)
-        pool.k_data[layer].copy_(torch.from_numpy(kd))
-        pool.v_data[layer].copy_(torch.from_numpy(vd))
+        pool.k_data[layer].copy_(torch.from_numpy(stored_codes(kd)))
+        pool.v_data[layer].copy_(torch.from_numpy(stored_codes(vd)))
         pool.k_scales[layer].copy_(torch.from_numpy(ks.view(np.float16)))
         pool.v_scales[layer].copy_(torch.from_numpy(vs.view(np.float16)))
     return pool
@@ -120,7 +132,7 @@ def host_arrays(pool, layer: int = 0):
                 pool.v_data[layer].cpu().view(torch.int16).numpy().view(np.uint16), None, None)
     if pool.dtype == W.F32:
         return pool.k_data[layer].cpu().numpy(), pool.v_data[layer].cpu().numpy(), None, None
-    return (pool.k_data[layer].cpu().numpy(), pool.v_data[layer].cpu().numpy(),
+    return (int8_codes(pool.k_data[layer].cpu().numpy()), int8_codes(pool.v_data[layer].cpu().numpy()),
             pool.k_scales[layer].cpu().view(torch.int16).numpy().view(np.uint16),
             pool.v_scales[layer].cpu().view(torch.int16).numpy().view(np.uint16))
 

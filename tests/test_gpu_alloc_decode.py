@@ -43,6 +43,9 @@ def test_allocator_drives_decode_with_a_fork(dtype):
     pool = api.KVPool(1, PAGES, N_KV, dtype)
     for t in (pool.k_data, pool.v_data) + ((pool.k_scales, pool.v_scales) if dtype else ()):
         t.zero_()
+    if dtype == W.Q8_0:  # code 0 (the host mirror's zeros) is the stored byte 128
+        pool.k_data.fill_(128)
+        pool.v_data.fill_(128)
     host = _empty_host(dtype)
     alloc = api.PageAllocator(PAGES, 8, STRIDE)
     prompts = [37, 16, 70, 5]
