@@ -116,6 +116,15 @@ __device__ __forceinline__ uint32_t tf32_part_lane(float x, bool lo) {
   return to_tf32(fmaf(lo ? -1.0f : 0.0f, __uint_as_float(to_tf32(x)), x));
 }
 
+// 2^x on the special-function unit.  Subnormal results flush to 0: a
+// probability below 2^-126 of the running maximum is lost in the fp32 sums
+// anyway.
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Per-warp online softmax state for one piece.
 template <int DT>
 struct WarpState {
@@ -331,7 +340,7 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
   const bool grow = mx > S.m + 8.0f;  // true on the first page (m = -inf)
   if (__any_sync(kFull, grow)) {
     const float m_new = grow ? mx : S.m;
-    const float al = exp2f(S.m - m_new);  // 1 if unchanged, 0 from -inf
+    const float al = ex2_ftz(S.m - m_new);  // 1 if unchanged, 0 from -inf
     S.l *= al;
 #pragma unroll
     for (int r = 0; r < 8; ++r)
@@ -339,7 +348,7 @@ __device__ __forceinline__ void process_unit(uint8_t* st, const uint8_t* sc, int
       for (int e = 0; e < 4; ++e) S.o[r][e] *= al;
     S.m = m_new;
   }
-  const float p0 = exp2f(s0 - S.m), p1 = exp2f(s1 - S.m);
+  const float p0 = ex2_ftz(s0 - S.m), p1 = ex2_ftz(s1 - S.m);
   S.l += p0 + p1;
 
   if constexpr (DT == PKV_KV_F32) {
@@ -627,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncwarp();
     if (lane == 0) {
-      const int s = u % R;
+      const int s = static_cast<int>(static_cast<unsigned>(u) % R);
       const uint32_t bar = bar0 + 8 * s;
       const uint32_t dst = smem_addr(ring + s * TL::kCodes);
       const int z = pg * a.n_kv + hh;  // tile index (the host checks num_pages * n_kv < 2^31)
@@ -681,10 +690,14 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
     S.vx = kNoScale;
 
     const int r = static_cast<int>((x - c_begin) % kWarps);
-    for (long long pos = x + ((warp - r + kWarps) % kWarps); pos < b; pos += kWarps) {
-      const int u = static_cast<int>((pos - first) / kWarps);
-      const int s = u % R;
-      bool ok = !aborted && mbar_wait_bounded(bar0 + 8 * s, (u / R) & 1, ctl);
+    // this warp's units of the piece: offsets rel in the segment (ints: a
+    // segment has fewer than 2^31 units), u its index among the warp's units
+    const long long pos0 = x + ((warp - r + kWarps) % kWarps);
+    const int rel_end = static_cast<int>(b - seg_start);
+    int u = static_cast<int>((pos0 - first) / kWarps);
+    for (int rel = static_cast<int>(pos0 - seg_start); rel < rel_end; rel += kWarps, ++u) {
+      const int s = static_cast<int>(static_cast<unsigned>(u) % R);
+      bool ok = !aborted && mbar_wait_bounded(bar0 + 8 * s, (static_cast<unsigned>(u) / R) & 1, ctl);
       ok = __all_sync(kFull, ok);
       if (!ok) {
         if (!aborted && lane == 0 && !ctl[0]) {
@@ -695,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, DT == PKV_KV_Q8_0   ? PKV_Q8_CTAS_PE
         continue;
       }
       consumed = u + 1;
-      const int t_page = (p0 + static_cast<int>(pos - seg_start)) * kPage;  // page's first token
+      const int t_page = (p0 + rel) * kPage;  // page's first token
       const int nvalid = min(kPage, L - t_page);
       const int tlo = max(0, ws - t_page);
       process_unit<DT, G>(ring + s * TL::kCodes, ring_sc + s * TL::kScales, tlo, nvalid, lane, S);
