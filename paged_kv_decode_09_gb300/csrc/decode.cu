@@ -116,15 +116,6 @@ __device__ __forceinline__ uint32_t tf32_part_lane(float x, bool lo) {
   return to_tf32(fmaf(lo ? -1.0f : 0.0f, __uint_as_float(to_tf32(x)), x));
 }
 
-// 2^x on the special-function unit.  Subnormal results flush to 0: a
-// probability below 2^-126 of the running maximum is lost in the fp32 sums
-// anyway.
-__device__ __forceinline__ float ex2_ftz(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // Per-warp online softmax state for one piece.
 template <int DT>
 struct WarpState {

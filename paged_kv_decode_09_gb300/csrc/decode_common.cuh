@@ -147,6 +147,15 @@ __device__ __forceinline__ uint32_t split_f16x2(float x0, float x1, bool lo) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// 2^x on the special-function unit, for the page softmax.  Subnormal results
+// flush to 0: a probability below 2^-126 of the running maximum is lost in
+// the fp32 sums anyway.
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // P-operand scaling shared by the kernels (see the single-query kernel's notes).
 // The P operand is scaled by a power of two so that its f16 parts stay
 // normal: f16 KV by 2^7 (p <= 2^8, so P <= 2^15); q8_0, where P carries the V

@@ -330,7 +330,7 @@ __device__ __forceinline__ void mq_process_unit(const uint8_t* st, const uint8_t
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 8));
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 16));
     const bool grow = mx > S.m[t] + 8.0f;  // never for a column with no token here
-    alpha[t] = grow ? exp2f(S.m[t] - mx) : 1.0f;
+    alpha[t] = grow ? ex2_ftz(S.m[t] - mx) : 1.0f;
     if (grow) S.m[t] = mx;
     grow_any |= grow;
   }
@@ -361,8 +361,8 @@ __device__ __forceinline__ void mq_process_unit(const uint8_t* st, const uint8_t
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
     const float mu = S.m[t] == -INFINITY ? 0.f : S.m[t];  // all -inf here: p = 0
-    p[t][0] = exp2f(s[t][0] - mu);
-    p[t][1] = exp2f(s[t][1] - mu);
+    p[t][0] = ex2_ftz(s[t][0] - mu);
+    p[t][1] = ex2_ftz(s[t][1] - mu);
     S.l[t] += p[t][0] + p[t][1];
   }
 
