@@ -148,3 +148,22 @@ def test_missing_library_raises(monkeypatch):
     monkeypatch.setattr(api, "_lib", None)
     with pytest.raises(api.PkvError, match="missing"):
         api.lib()
+
+
+def test_q8_0_code_bytes():
+    """q8_0 codes sit in the pool offset-binary (code + 128, the int8 byte with its top bit
+    flipped): the tests' conversions between the oracle's int8 codes and the stored bytes
+    invert each other, keep the codes' order, and the binding's q8_0 data tensors are bytes."""
+    import numpy as np
+    import torch
+
+    from helpers import int8_codes, stored_codes
+    from paged_kv_decode_09_gb300 import api
+    codes = np.arange(-128, 128, dtype=np.int8)
+    stored = stored_codes(codes)
+    assert stored.dtype == np.uint8
+    np.testing.assert_array_equal(stored.astype(np.int64), codes.astype(np.int64) + 128)
+    assert np.all(np.diff(stored.astype(np.int64)) == 1)  # order kept
+    np.testing.assert_array_equal(int8_codes(stored), codes)
+    assert stored[codes == 0][0] == 128 and stored[codes == -127][0] == 1 and stored[codes == 127][0] == 255
+    assert api._TORCH_DTYPE[api.Q8_0] == torch.uint8
